@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Benchmark of the KV4-RL decode hot path on GB300.
+
+One step = the whole hot path over one batch: quantize-on-append of one new
+K/V token per sequence (kv4_quant_append) followed by mixed INT4/INT8 split-KV
+decode attention with the eq. A1 merge (kv4_decode_attn).  The default
+workload is the Qwen3-8B-shaped decode layer: 64 sequences with lengths
+uniform in [1024, 8192], h_q=32, h_kv=8, d_h=128, S=4, R=128, group 32,
+shuffled 16-token pages, seeded synthetic bf16 K/V/q (4 outlier key channels
+per kv head scaled by 8).  The cache (~385 MB) is larger than L2, so every
+step streams it from HBM.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int8_kv_cache_kv4_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attn resident KV tokens/s per layer and achieved HBM GB/s vs 8 TB/s"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(lens, w: W.Workload):
+    """Decode bytes that must cross HBM once per step: INT4 token-heads
+    (codes + metadata), INT8 token-heads (codes + scale), block-table entries,
+    the query and the bf16 output.  Append bytes: bf16 K/V read plus the INT4
+    and (for protected positions) INT8 entries written."""
+    d = w.d_h
+    int4_th = 2 * (d // 2 + 4 * (d // w.group))   # K and V: codes + (Delta, m) per group
+    int8_th = 2 * (d + 2)                         # K and V: codes + fp16 scale
+    dec = 0
+    n4_tok = 0
+    n8_tok = 0
+    for L in lens:
+        L = int(L)
+        n_p = min(L, w.sink + w.recent)
+        n_4 = L - n_p
+        n4_tok += n_4
+        n8_tok += n_p
+        dec += w.h_kv * (n_p * int8_th + n_4 * int4_th) + ((L + 15) // 16) * 4
+    dec += len(lens) * w.h_q * d * 2 * 2            # q read + out write (bf16)
+    app = len(lens) * w.h_kv * (2 * d * 2 + int4_th + int8_th) + len(lens) * 4 * 3
+    return dec, app, n4_tok, n8_tok
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workload
+
+def build_workload(w: W.Workload, dev, with_bf16=False, lens=None):
+    import torch
+    from int8_kv_cache_kv4_gb300.cache import MixedKVCache
+    lens = W.seq_lengths(w) if lens is None else lens
+    B = len(lens)
+    mpps = (int(lens.max()) + 15) // 16
+    num_pages = W.pool_pages(lens, w.extra_pages)
+    cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
+                         recent=w.recent, max_seqs=B, num_pages=num_pages,
+                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16)
+    cache.set_block_table(W.block_table(w.seed, lens, mpps, num_pages))
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    # populate positions [0, L-1) of every sequence (prefill-style bulk append)
+    for b, L in enumerate(lens):
+        n = int(L) - 1
+        if n <= 0:
+            continue
+        gen = W.torch_generator(w.seed * 1000003 + b, dev)
+        k, v = W.kv_torch(gen, w.h_kv, n, w.d_h, outl, dev)
+        seq = torch.full((n,), b, dtype=torch.int32, device=dev)
+        pos = torch.arange(n, dtype=torch.int32, device=dev)
+        lens_now = torch.as_tensor(np.maximum(lens - 1, 0).astype(np.int32), device=dev)
+        cache.append(k, v, seq, pos, lens_now)
+    # the step's new token (position L-1) and query
+    gen = W.torch_generator(w.seed * 1000003 + 999983, dev)
+    k_new, v_new = W.kv_torch(gen, w.h_kv, B, w.d_h, outl, dev)
+    q = torch.randn((B, w.h_q, w.d_h), generator=gen, device=dev).to(torch.bfloat16)
+    step = {
+        "k": k_new, "v": v_new, "q": q,
+        "seq": torch.arange(B, dtype=torch.int32, device=dev),
+        "pos": torch.as_tensor((lens - 1).astype(np.int32), device=dev),
+        "lens": torch.as_tensor(lens.astype(np.int32), device=dev),
+        "out": torch.empty((B, w.h_q, w.d_h), dtype=torch.bfloat16, device=dev),
+        "lse": torch.empty((B, w.h_q), dtype=torch.float32, device=dev),
+    }
+    torch.cuda.synchronize()
+    return cache, step, lens
+
+
+def run_step(cache, s, max_splits=0, ev=None):
+    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+    if ev is not None:
+        ev.record()
+    cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=max_splits)
+
+
+# ---------------------------------------------------------------- arms
+
+def run_kv4(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from int8_kv_cache_kv4_gb300 import kv4
+    kv4.load(build_if_missing=True)
+
+    w = W.WORKLOADS[args.workload]
+    cache, s, lens = build_workload(w, dev, with_bf16=not args.no_bf16)
+    dec_bytes, app_bytes, n4_tok, n8_tok = algorithmic_bytes(lens, w)
+    tokens = int(lens.sum())
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        run_step(cache, s, args.max_splits)
+    torch.cuda.synchronize()
+    cache.clear_status()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        run_step(cache, s, args.max_splits, ev=mids[i])
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    app_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    status = cache.read_status()
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t.item()) / args.steps
+    value = world * tokens / (ms_per_step / 1e3)
+    dec_avg = statistics.mean(dec_ms)
+    hbm_peak, peak_kind = peaks()
+    achieved = dec_bytes / (dec_avg / 1e3) / 1e9
+
+    # BF16-KV comparator on the same pages / inputs (reported beside, not in the step)
+    comparator = None
+    if not args.no_bf16:
+        out16 = torch.empty_like(s["out"])
+        for _ in range(3):
+            cache.decode_bf16(s["q"], s["lens"], out16, None, max_splits=args.max_splits)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            cache.decode_bf16(s["q"], s["lens"], out16, None, max_splits=args.max_splits)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        bf_ms = e0.elapsed_time(e1) / args.steps
+        bf_bytes = sum(w.h_kv * int(L) * 2 * w.d_h * 2 for L in lens) + len(lens) * w.h_q * w.d_h * 4
+        drift = (s["out"].float() - out16.float()).abs()
+        comparator = {"kernel": "bf16-KV paged decode (same pages, same split plan)",
+                      "ms": bf_ms, "tokens_per_s": tokens / (bf_ms / 1e3),
+                      "algorithmic_GBps": bf_bytes / (bf_ms / 1e3) / 1e9,
+                      "kv4_decode_speedup": bf_ms / dec_avg,
+                      "output_drift_vs_bf16": {"max_abs": float(drift.max()),
+                                               "mean_abs": float(drift.mean())}}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(cache, s, args, stream)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u4/i8 codes, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q, outlier key channels x8)",
+        "config": {"workload": w.name, "batch": int(len(lens)), "mean_len": float(lens.mean()),
+                   "total_tokens": tokens, "h_q": w.h_q, "h_kv": w.h_kv, "d_h": w.d_h,
+                   "sink": w.sink, "recent": w.recent, "group": w.group, "page": 16,
+                   "splits": kv4.num_splits(cache.layout, int(len(lens)), args.max_splits),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "cache working set > L2 (no flush needed)"},
+        "decode_ms": dec_avg, "append_ms": statistics.mean(app_ms),
+        "decode_tokens_per_s": tokens / (dec_avg / 1e3),
+        "decode_algorithmic_GBps": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "kv4_decode_attn (split kernel + combine)",
+                     "bytes_per_launch": dec_bytes, "peak_source": peak_kind},
+        "append_algorithmic_bytes": app_bytes,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "device_status": status,
+        "e2e": e2e,
+        "bf16_comparator": comparator,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, lens, budget_s=args.cpu_budget)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(cache, s, args, stream):
+    """Same step through the binding with pinned host inputs: H2D of the new
+    K/V token and the query, append + decode, D2H of the output."""
+    import torch
+    hk = s["k"].cpu().pin_memory()
+    hv = s["v"].cpu().pin_memory()
+    hq = s["q"].cpu().pin_memory()
+    hout = torch.empty(s["out"].shape, dtype=torch.bfloat16).pin_memory()
+    dk, dv, dq = torch.empty_like(s["k"]), torch.empty_like(s["v"]), torch.empty_like(s["q"])
+    s2 = dict(s, k=dk, v=dv, q=dq)
+
+    def one():
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        run_step(cache, s2, args.max_splits)
+        hout.copy_(s2["out"], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t) / args.steps
+    tokens = int(s["lens"].sum().item())
+    h2d = (hk.numel() + hv.numel() + hq.numel()) * 2
+    return {"value": tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": hout.numel() * 2, "ms_per_step": dt * 1e3}
+
+
+def cpu_baseline(w: W.Workload, lens, budget_s=20.0, kind="oracle"):
+    """The CPU oracle, as it stands, on a bounded sample of the workload: the
+    full quantize + fp64 decode of the first few sequences (all heads)."""
+    import oracle
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    q = W.q_numpy(w.seed, 1, w.h_q, w.d_h)[0]
+    done_tokens = 0
+    spent = 0.0
+    nseq = 0
+    for b, L in enumerate(lens):
+        k, v = W.kv_numpy_block(w.seed, b, w.h_kv, int(L), w.d_h, outl)
+        t = time.perf_counter()
+        oracle.decode_seq(q, k, v, g=w.group, S=w.sink, R=w.recent, sm_scale=1 / math.sqrt(w.d_h))
+        spent += time.perf_counter() - t
+        done_tokens += int(L)
+        nseq += 1
+        if spent >= budget_s:
+            break
+    return {"value": done_tokens / spent, "unit": UNIT, "cores": 1, "kind": kind,
+            "sample": f"{nseq} of {len(lens)} sequences ({done_tokens} tokens, all heads): "
+                      f"quantize + fp64 decode in {spent:.1f} s on 1 host thread"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    lens = W.seq_lengths(w)
+    per_step_budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, lens[:1], budget_s=0.0)
+    vals = []
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        cb = cpu_baseline(w, lens[i % len(lens):], budget_s=per_step_budget)
+        vals.append(cb["value"])
+    elapsed = time.perf_counter() - t_all
+    value = statistics.mean(vals)
+    tokens = int(lens.sum())
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tokens / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": int(len(lens)), "mean_len": float(lens.mean())},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: consecutive sequences for ~{per_step_budget:.1f} s "
+                                       f"(quantize + fp64 decode, 1 host thread); {elapsed:.1f} s total"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kv4", choices=["kv4", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_b64", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kv4(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * kv4.h -- C ABI of the KV4-RL mixed INT4/INT8 paged KV cache for GB300 (sm_103a).
+ *
+ * The method ("KV4-RL: Unlocking Faster Asynchronous Rollouts for RLVR with INT4
+ * KV Cache Quantization"):
+ *   - every cached K/V position is stored as head-wise affine INT4 codes with an
+ *     FP16 scale Delta and FP16 offset m per group of channels, x^ = Delta*c + m
+ *     (Sec. 3 eq. 3.3; Sec. 5.1; App. A.3 "Encoding and allocation");
+ *   - the first S positions (attention sinks) and the most recent R positions
+ *     additionally live in an INT8 side cache with one symmetric scale per
+ *     token and head, computed from the source vector (Sec. 5.2; App. A.3);
+ *   - decode attention reads protected positions from the side cache and all
+ *     others from the INT4 pages (disjoint regions, Sec. 5.3) and merges the
+ *     regional results with the log-sum-exp identity of App. A.3 eq. A1, which
+ *     also merges context splits.
+ *
+ * Conventions for every entry point
+ *   - Memory: the caller owns all memory.  Device pointers are plain CUDA
+ *     device addresses (e.g. from cudaMalloc or a PyTorch tensor); host
+ *     pointers are noted as such.  The library never allocates, frees or
+ *     synchronises; all device work is enqueued on `stream`, a cudaStream_t
+ *     passed as void* (NULL = the legacy default stream).
+ *   - Return value: KV4_OK, or a KV4_ERR_* code for problems found on the host
+ *     (NULL pointers, bad sizes, unsupported shapes, launch failures).  Nothing
+ *     is enqueued when an error is returned.
+ *   - dev_status: a device int32 that kernels OR KV4_STATUS_* bits into for
+ *     data-dependent problems (a block-table entry outside the pool, a position
+ *     outside the sequence, a non-finite input).  Kernels never trap: the
+ *     offending token / page is skipped.  The caller zeroes it and reads it
+ *     back when convenient.  May be NULL (problems are then silently skipped).
+ *   - bf16 tensors are passed as const uint16_t* (IEEE bfloat16 bit patterns).
+ *
+ * Packed layout (bit-exact; the CPU oracle restates it independently)
+ *   paged cache  = [num_pages][num_kv_heads][chunk]
+ *     chunk      = K codes [16 slots][head_dim/2 bytes]
+ *                  V codes [16 slots][head_dim/2 bytes]
+ *                  K meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
+ *                  V meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
+ *     Byte i of a slot's code row holds channel 2i in its low nibble and
+ *     channel 2i+1 in its high nibble.  Position p of request slot s lives in
+ *     page block_table[s][p / 16], slot p % 16.
+ *     chunk bytes = 16*head_dim + 128*head_dim/g  (2560 at d=128, g=32).
+ *   side cache   = [max_seqs][num_kv_heads][block], NS = sink + recent
+ *     block      = K8 codes [NS][head_dim] int8, V8 codes [NS][head_dim] int8,
+ *                  K8 scale [NS] fp16, V8 scale [NS] fp16, zero pad to 16 bytes.
+ *     Sink position p < S uses slot p; position p >= S uses ring slot
+ *     S + (p mod R).  All multi-byte fields are little-endian.
+ *   bf16 comparator cache = [num_pages][num_kv_heads][2 (K,V)][16][head_dim] bf16.
+ *
+ * Quantization rules (the pages leave rounding open; these readings are fixed):
+ *   INT4 group of g channels: m = fp16 rounded down from min(x);
+ *     Delta = fp16 rounded up from ((max(x) -up m) /up 15) (fp32, upward);
+ *     c = clamp(rne((x -rn m) /rn Delta), 0, 15), and c = 0 when Delta = 0.
+ *   INT8 token-head vector: s = fp16 rounded up from (max|x| /up 127);
+ *     c = clamp(rne(x /rn s), -127, 127), and c = 0 when s = 0.
+ *   A group or vector with a non-finite element (or whose metadata overflows
+ *   fp16) is stored as all zeros and sets KV4_STATUS_NONFINITE.
+ */
+#ifndef KV4_H_
+#define KV4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV4_ABI_VERSION 1
+
+/* host return codes */
+#define KV4_OK 0
+#define KV4_ERR_INVALID_ARG 1 /* NULL pointer, negative size, inconsistent layout */
+#define KV4_ERR_UNSUPPORTED 2 /* head_dim not in {64,128}, g not in {32,64,128}, ... */
+#define KV4_ERR_LAUNCH 3      /* a CUDA launch failed (cudaGetLastError) */
+#define KV4_ERR_WORKSPACE 4   /* workspace smaller than kv4_workspace_bytes() */
+
+/* device status bits (ORed into *dev_status) */
+#define KV4_STATUS_BAD_PAGE 1  /* block-table entry outside [0, num_pages) */
+#define KV4_STATUS_BAD_POS 2   /* position < 0, >= seq_len, or beyond the block table */
+#define KV4_STATUS_BAD_SEQ 4   /* request slot outside [0, max_seqs) */
+#define KV4_STATUS_NONFINITE 8 /* non-finite input, or metadata overflowing fp16 */
+#define KV4_STATUS_BAD_LEN 16  /* decode: seq_len < 0 or beyond the block-table capacity */
+
+/* Shape of one attention layer's cache.  All fields are host values. */
+typedef struct kv4_layout {
+  int32_t num_q_heads;       /* h_q (a multiple of num_kv_heads, h_q/h_kv <= 8) */
+  int32_t num_kv_heads;      /* h_kv */
+  int32_t head_dim;          /* d_h: 64 or 128 */
+  int32_t page_size;         /* tokens per page: must be 16 (App. A.2) */
+  int32_t int4_group;        /* g: 32, 64 or 128 and g <= head_dim */
+  int32_t int8_group;        /* INT8 group: must equal head_dim (per token-head) */
+  int32_t sink;              /* S >= 0: protected prefix length */
+  int32_t recent;            /* R >= 0: protected recent window */
+  int32_t max_seqs;          /* request slots: rows of the block table and side cache */
+  int32_t num_pages;         /* pages in the pool */
+  int32_t max_pages_per_seq; /* row stride of block_table */
+} kv4_layout;
+
+/* ABI version and a static, human-readable name for a return code or status bit. */
+int kv4_abi_version(void);
+const char* kv4_status_string(int code);
+
+/* Validate a layout; KV4_OK or a KV4_ERR_* code. */
+int kv4_check_layout(const kv4_layout* layout);
+
+/* Sizes in bytes of the caller-allocated buffers (0 when the layout is invalid). */
+size_t kv4_paged_cache_bytes(const kv4_layout* layout); /* INT4 pages: codes + metadata */
+size_t kv4_side_cache_bytes(const kv4_layout* layout);  /* INT8 sink + ring, per slot */
+size_t kv4_bf16_cache_bytes(const kv4_layout* layout);  /* comparator pages */
+
+/* Number of context splits per (sequence, kv head) that kv4_decode_attn uses
+ * for `num_seqs` sequences when given `max_splits` (0 = automatic), and the
+ * workspace (device scratch: partial outputs and log-normalisers) it needs. */
+int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
+size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
+
+/*
+ * kv4_quant_append -- quantize-on-append (KV4-RL Sec. 5.3: "both
+ * representations are produced directly from the source K/V vectors when each
+ * token is generated"; App. A.3 "Encoding and allocation").
+ *
+ * For each of the T new tokens t (request slot tok_seq[t], position
+ * tok_pos[t]): writes the INT4 codes and per-group (Delta, m) of K and V into
+ * page block_table[slot][pos/16], slot pos%16, for every kv head; and, when
+ * the position is protected for the sequence's length after this append --
+ * pos < S, or R > 0 and pos >= seq_lens[slot] - R -- writes the INT8 codes and
+ * scale into the side cache (sink slot pos, or ring slot S + pos mod R).
+ * Multi-token appends (prefill / re-prefill population, App. A.3) may list
+ * tokens in any order; tokens must not repeat a (slot, position) pair.
+ *
+ *   paged, side     device, written in place (layout above)
+ *   k_new, v_new    device bf16 [T][num_kv_heads][head_dim]
+ *   tok_seq,tok_pos device int32 [T]
+ *   seq_lens        device int32 [max_seqs]: lengths after this append
+ *   block_table     device int32 [max_seqs][max_pages_per_seq]
+ *   T == 0 is a no-op.
+ */
+int kv4_quant_append(const kv4_layout* layout, void* paged, void* side, const uint16_t* k_new,
+                     const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                     int32_t T, const int32_t* seq_lens, const int32_t* block_table,
+                     int32_t* dev_status, void* stream);
+
+/*
+ * kv4_decode_attn -- split-KV GQA decode attention over the mixed cache
+ * (KV4-RL Sec. 5.3 and App. A.3: disjoint INT4 and protected regions, each
+ * split producing a locally normalised output and log-normaliser, merged by
+ * eq. A1).  Query head j reads kv head j / (h_q/h_kv).  For sequence b of
+ * length L = seq_lens[b], positions [0, min(S,L)) and [max(S, L-R), L) are read
+ * from the side cache, the rest from the INT4 pages.  Scores are
+ * sm_scale * q.k^ with the bf16 query used as is; softmax and accumulation in
+ * fp32.
+ *
+ *   q           device bf16 [num_seqs][num_q_heads][head_dim]
+ *   seq_lens    device int32 [num_seqs]; row b of block_table / side cache is slot b
+ *   max_splits  0 = automatic; else an upper bound on splits per (seq, kv head)
+ *   workspace   device, >= kv4_workspace_bytes(layout, num_seqs, max_splits) bytes
+ *   out         device bf16 [num_seqs][num_q_heads][head_dim] (round to nearest even)
+ *   out_lse     device fp32 [num_seqs][num_q_heads] natural-log normaliser, or NULL
+ *   A sequence with L == 0 yields out = 0 and out_lse = -inf.
+ */
+int kv4_decode_attn(const kv4_layout* layout, const void* paged, const void* side,
+                    const uint16_t* q, const int32_t* seq_lens, int32_t num_seqs,
+                    const int32_t* block_table, float sm_scale, int32_t max_splits,
+                    void* workspace, size_t workspace_bytes, uint16_t* out, float* out_lse,
+                    int32_t* dev_status, void* stream);
+
+/*
+ * kv4_split_combine -- the regional / split merge of KV4-RL App. A.3 eq. A1
+ * on its own: for each of `rows` independent rows,
+ *   z = log sum_r exp(z_r),   o = sum_r exp(z_r - z) * o_r,
+ * with zero weight for parts whose z_r = -inf (empty splits or regions).
+ *
+ *   part_o    device fp32 [rows][n_parts][head_dim] (locally normalised outputs)
+ *   part_lse  device fp32 [rows][n_parts]
+ *   out       device bf16 [rows][head_dim]; out_lse device fp32 [rows] or NULL
+ *   A row whose parts are all empty yields out = 0, out_lse = -inf.
+ */
+int kv4_split_combine(const float* part_o, const float* part_lse, int32_t rows, int32_t n_parts,
+                      int32_t head_dim, uint16_t* out, float* out_lse, void* stream);
+
+/*
+ * Comparator: the same paged GQA decode over an unquantized bf16 cache
+ * (layout above), with the same pages, block table and split plan.  Not part
+ * of the method; used to report the speed-up of the mixed cache and the
+ * drift of its outputs.
+ *   kv4_bf16_append writes k_new/v_new [T][h_kv][d_h] into the bf16 pages.
+ */
+int kv4_bf16_append(const kv4_layout* layout, void* cache, const uint16_t* k_new,
+                    const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                    int32_t T, const int32_t* seq_lens, const int32_t* block_table,
+                    int32_t* dev_status, void* stream);
+int kv4_bf16_decode_attn(const kv4_layout* layout, const void* cache, const uint16_t* q,
+                         const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
+                         float sm_scale, int32_t max_splits, void* workspace,
+                         size_t workspace_bytes, uint16_t* out, float* out_lse,
+                         int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV4_H_ */

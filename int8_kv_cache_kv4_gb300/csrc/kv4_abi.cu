@@ -1,0 +1,244 @@
+// kv4_abi.cu -- the extern "C" boundary declared in include/kv4.h: argument
+// validation, buffer sizing, the split plan, and kernel launches.  No entry
+// point allocates, frees or synchronises.
+#include <stdint.h>
+
+#include "kv4_common.cuh"
+
+namespace kv4 {
+cudaError_t launch_quant_append(const Layout&, void*, void*, const uint16_t*, const uint16_t*,
+                                const int32_t*, const int32_t*, int, const int32_t*,
+                                const int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_bf16_append(const Layout&, void*, const uint16_t*, const uint16_t*,
+                               const int32_t*, const int32_t*, int, const int32_t*, const int32_t*,
+                               int32_t*, cudaStream_t);
+cudaError_t launch_decode(const Layout&, const void*, const void*, const uint16_t*, const int32_t*,
+                          int, const int32_t*, float, int, int, int, int, float*, float*, int32_t*,
+                          cudaStream_t);
+cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, const int32_t*, int,
+                               const int32_t*, float, int, int, float*, float*, int32_t*,
+                               cudaStream_t);
+cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
+                           cudaStream_t);
+
+// Split planning.  The host does not know the per-sequence lengths (they live
+// on the device), so the plan is sized from the block-table capacity: about
+// kTargetCtas CTAs in total (16 per SM of a 152-SM GB300), at least
+// kMinPagesPerSplit pages per INT4 split, and one protected split per
+// kProtChunk side-cache slots.
+constexpr int kTargetCtas = 16 * 152;
+constexpr int kMinPagesPerSplit = 4;
+constexpr int kProtChunk = 256;
+
+struct Plan {
+  int n4, pages_per_split, n8, prot_per_split;
+  int total() const { return n4 + n8; }
+};
+
+static Plan make_plan(const kv4_layout* lay, int num_seqs, int max_splits, bool with_prot) {
+  Plan p;
+  const int maxp = lay->max_pages_per_seq;
+  const long long units = (long long)(num_seqs > 0 ? num_seqs : 1) * lay->num_kv_heads;
+  long long n4 = (kTargetCtas + units - 1) / units;
+  if (n4 < 1) n4 = 1;
+  if (max_splits > 0 && n4 > max_splits) n4 = max_splits;
+  int pps = (int)((maxp + n4 - 1) / n4);
+  if (pps < kMinPagesPerSplit) pps = kMinPagesPerSplit;
+  if (max_splits > 0 && (maxp + pps - 1) / pps > max_splits) pps = (maxp + max_splits - 1) / max_splits;
+  p.pages_per_split = pps;
+  p.n4 = (maxp + pps - 1) / pps;
+  const int NS = lay->sink + lay->recent;
+  p.prot_per_split = kProtChunk;
+  p.n8 = (with_prot && NS > 0) ? (NS + kProtChunk - 1) / kProtChunk : 0;
+  return p;
+}
+
+static Layout to_layout(const kv4_layout* l) {
+  Layout L;
+  L.h_q = l->num_q_heads;
+  L.h_kv = l->num_kv_heads;
+  L.d_h = l->head_dim;
+  L.g = l->int4_group;
+  L.S = l->sink;
+  L.R = l->recent;
+  L.max_seqs = l->max_seqs;
+  L.num_pages = l->num_pages;
+  L.max_pages = l->max_pages_per_seq;
+  return L;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p) {
+  const size_t rows = (size_t)num_seqs * l->num_q_heads;
+  size_t o = rows * p.total() * l->head_dim * sizeof(float);
+  o = (o + 255) / 256 * 256;
+  size_t z = rows * p.total() * sizeof(float);
+  return o + (z + 255) / 256 * 256;
+}
+
+}  // namespace kv4
+
+using namespace kv4;
+
+extern "C" {
+
+int kv4_abi_version(void) { return KV4_ABI_VERSION; }
+
+const char* kv4_status_string(int code) {
+  switch (code) {
+    case KV4_OK: return "ok";
+    case KV4_ERR_INVALID_ARG: return "invalid argument";
+    case KV4_ERR_UNSUPPORTED: return "unsupported shape";
+    case KV4_ERR_LAUNCH: return "CUDA launch failed";
+    case KV4_ERR_WORKSPACE: return "workspace too small";
+    default: break;
+  }
+  return "unknown code";
+}
+
+int kv4_check_layout(const kv4_layout* l) {
+  if (!l) return KV4_ERR_INVALID_ARG;
+  if (l->num_q_heads <= 0 || l->num_kv_heads <= 0 || l->num_q_heads % l->num_kv_heads != 0)
+    return KV4_ERR_INVALID_ARG;
+  const int G = l->num_q_heads / l->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV4_ERR_UNSUPPORTED;
+  if (l->head_dim != 64 && l->head_dim != 128) return KV4_ERR_UNSUPPORTED;
+  if (l->page_size != 16) return KV4_ERR_UNSUPPORTED;
+  const int g = l->int4_group;
+  if (g != 32 && g != 64 && g != 128) return KV4_ERR_UNSUPPORTED;
+  if (g > l->head_dim) return KV4_ERR_UNSUPPORTED;
+  if (l->int8_group != l->head_dim) return KV4_ERR_UNSUPPORTED;
+  if (l->sink < 0 || l->recent < 0) return KV4_ERR_INVALID_ARG;
+  if ((long long)l->sink + l->recent > (1LL << 30)) return KV4_ERR_INVALID_ARG;
+  if (l->max_seqs <= 0 || l->num_pages <= 0 || l->max_pages_per_seq <= 0)
+    return KV4_ERR_INVALID_ARG;
+  if ((long long)l->max_pages_per_seq * 16 > (1LL << 30)) return KV4_ERR_INVALID_ARG;
+  return KV4_OK;
+}
+
+size_t kv4_paged_cache_bytes(const kv4_layout* l) {
+  if (kv4_check_layout(l) != KV4_OK) return 0;
+  return (size_t)l->num_pages * l->num_kv_heads * chunk_bytes(l->head_dim, l->int4_group);
+}
+
+size_t kv4_side_cache_bytes(const kv4_layout* l) {
+  if (kv4_check_layout(l) != KV4_OK) return 0;
+  return (size_t)l->max_seqs * l->num_kv_heads *
+         (size_t)side_block_bytes(l->head_dim, l->sink, l->recent);
+}
+
+size_t kv4_bf16_cache_bytes(const kv4_layout* l) {
+  if (kv4_check_layout(l) != KV4_OK) return 0;
+  return (size_t)l->num_pages * l->num_kv_heads * 2 * 16 * l->head_dim * 2;
+}
+
+int32_t kv4_num_splits(const kv4_layout* l, int32_t num_seqs, int32_t max_splits) {
+  if (kv4_check_layout(l) != KV4_OK || num_seqs < 0) return 0;
+  return make_plan(l, num_seqs, max_splits, true).total();
+}
+
+size_t kv4_workspace_bytes(const kv4_layout* l, int32_t num_seqs, int32_t max_splits) {
+  if (kv4_check_layout(l) != KV4_OK || num_seqs < 0) return 0;
+  return ws_bytes(l, num_seqs, make_plan(l, num_seqs, max_splits, true));
+}
+
+int kv4_quant_append(const kv4_layout* l, void* paged, void* side, const uint16_t* k_new,
+                     const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                     int32_t T, const int32_t* seq_lens, const int32_t* block_table,
+                     int32_t* dev_status, void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (T < 0) return KV4_ERR_INVALID_ARG;
+  if (T == 0) return KV4_OK;
+  if (!paged || !k_new || !v_new || !tok_seq || !tok_pos || !seq_lens || !block_table)
+    return KV4_ERR_INVALID_ARG;
+  if (!side && l->sink + l->recent > 0) return KV4_ERR_INVALID_ARG;
+  if (!aligned16(paged) || !aligned16(side) || !aligned16(k_new) || !aligned16(v_new))
+    return KV4_ERR_INVALID_ARG;
+  cudaError_t e = launch_quant_append(to_layout(l), paged, side, k_new, v_new, tok_seq, tok_pos,
+                                      T, seq_lens, block_table, dev_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, const uint16_t* q,
+                    const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
+                    float sm_scale, int32_t max_splits, void* workspace, size_t workspace_bytes,
+                    uint16_t* out, float* out_lse, int32_t* dev_status, void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (num_seqs < 0 || num_seqs > l->max_seqs || max_splits < 0) return KV4_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KV4_OK;
+  if (!paged || !q || !seq_lens || !block_table || !workspace || !out) return KV4_ERR_INVALID_ARG;
+  if (!side && l->sink + l->recent > 0) return KV4_ERR_INVALID_ARG;
+  if (!aligned16(paged) || !aligned16(side) || !aligned16(q) || !aligned16(workspace))
+    return KV4_ERR_INVALID_ARG;
+  const Plan p = make_plan(l, num_seqs, max_splits, true);
+  if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
+  const size_t rows = (size_t)num_seqs * l->num_q_heads;
+  float* part_o = (float*)workspace;
+  size_t o_bytes = (rows * p.total() * l->head_dim * sizeof(float) + 255) / 256 * 256;
+  float* part_lse = (float*)((char*)workspace + o_bytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  const Layout L = to_layout(l);
+  cudaError_t e = launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                                p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse,
+                                dev_status, st);
+  if (e != cudaSuccess) return KV4_ERR_LAUNCH;
+  e = launch_combine(part_o, part_lse, (int)rows, p.total(), l->head_dim, out, out_lse, st);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_split_combine(const float* part_o, const float* part_lse, int32_t rows, int32_t n_parts,
+                      int32_t head_dim, uint16_t* out, float* out_lse, void* stream) {
+  if (rows < 0 || n_parts < 0 || (head_dim != 64 && head_dim != 128)) return KV4_ERR_INVALID_ARG;
+  if (rows == 0) return KV4_OK;
+  if (!out || (n_parts > 0 && (!part_o || !part_lse))) return KV4_ERR_INVALID_ARG;
+  cudaError_t e =
+      launch_combine(part_o, part_lse, rows, n_parts, head_dim, out, out_lse, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_bf16_append(const kv4_layout* l, void* cache, const uint16_t* k_new, const uint16_t* v_new,
+                    const int32_t* tok_seq, const int32_t* tok_pos, int32_t T,
+                    const int32_t* seq_lens, const int32_t* block_table, int32_t* dev_status,
+                    void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (T < 0) return KV4_ERR_INVALID_ARG;
+  if (T == 0) return KV4_OK;
+  if (!cache || !k_new || !v_new || !tok_seq || !tok_pos || !seq_lens || !block_table)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(k_new) || !aligned16(v_new)) return KV4_ERR_INVALID_ARG;
+  cudaError_t e = launch_bf16_append(to_layout(l), cache, k_new, v_new, tok_seq, tok_pos, T,
+                                     seq_lens, block_table, dev_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_bf16_decode_attn(const kv4_layout* l, const void* cache, const uint16_t* q,
+                         const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
+                         float sm_scale, int32_t max_splits, void* workspace,
+                         size_t workspace_bytes, uint16_t* out, float* out_lse,
+                         int32_t* dev_status, void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (num_seqs < 0 || num_seqs > l->max_seqs || max_splits < 0) return KV4_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KV4_OK;
+  if (!cache || !q || !seq_lens || !block_table || !workspace || !out) return KV4_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(q) || !aligned16(workspace)) return KV4_ERR_INVALID_ARG;
+  const Plan p = make_plan(l, num_seqs, max_splits, false);
+  if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
+  const size_t rows = (size_t)num_seqs * l->num_q_heads;
+  float* part_o = (float*)workspace;
+  size_t o_bytes = (rows * p.total() * l->head_dim * sizeof(float) + 255) / 256 * 256;
+  float* part_lse = (float*)((char*)workspace + o_bytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_bf16_decode(to_layout(l), cache, q, seq_lens, num_seqs, block_table,
+                                     sm_scale, p.n4, p.pages_per_split, part_o, part_lse,
+                                     dev_status, st);
+  if (e != cudaSuccess) return KV4_ERR_LAUNCH;
+  e = launch_combine(part_o, part_lse, (int)rows, p.total(), l->head_dim, out, out_lse, st);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,246 @@
+// kv4_append.cu -- quantize-on-append: each new K/V token-head vector is
+// written as head-wise affine INT4 (per group of g channels: FP16 scale Delta
+// and offset m, 4-bit codes c with x^ = Delta*c + m; KV4-RL Sec. 3 eq. 3.3,
+// Sec. 5.1, App. A.3) into its 16-token page, and -- when the position is a
+// sink or inside the final recent window (Sec. 5.2) -- also as a symmetric
+// INT8 side entry computed from the same source vector (App. A.3).
+//
+// One warp per (token, kv head); lane l owns channels [4l, 4l+4) of K and V
+// (head_dim 128; head_dim 64 uses lanes 0..15).  Group min/max and the INT8
+// absolute maximum are warp-shuffle reductions; codes are packed two per byte
+// (low nibble = even channel) and stored as one 16-bit word per lane, so a
+// slot row of 64 bytes is one coalesced store.  Rounding follows the layout
+// header's rules exactly (directed fp32 ops and fp16 conversions), which makes
+// the written bytes bit-identical to the CPU oracle.
+#include "kv4_common.cuh"
+
+namespace kv4 {
+
+// Reduce over the `span` lanes of a group (span a power of two <= 32).
+__device__ inline float group_min(float v, int span) {
+  for (int o = 1; o < span; o <<= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ inline float group_max(float v, int span) {
+  for (int o = 1; o < span; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ inline int group_or(int v, int span) {
+  for (int o = 1; o < span; o <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// INT4-encode this lane's 4 channels of a group whose lanes span `span`
+// lanes.  Returns the packed 16-bit code word and, via meta, (Delta, m) bits.
+__device__ inline uint32_t encode_int4(const float x[4], int span, uint32_t* meta, int* bad) {
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  int nf = !(isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3]));
+  mn = group_min(mn, span);
+  mx = group_max(mx, span);
+  nf = group_or(nf, span);
+  uint32_t codes = 0;
+  uint16_t d16 = 0, m16 = 0;
+  if (!nf) {
+    __half mh = __float2half_rd(mn);
+    float mf = __half2float(mh);
+    float span_f = __fsub_ru(mx, mf);
+    float step = __fdiv_ru(span_f, 15.0f);
+    __half dh = __float2half_ru(step);
+    float df = __half2float(dh);
+    if (!isfinite(mf) || !isfinite(df)) {
+      nf = 1;
+    } else {
+      m16 = __half_as_ushort(mh);
+      d16 = __half_as_ushort(dh);
+      if (df != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int c = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], mf), df));
+          c = min(max(c, 0), 15);
+          codes |= (uint32_t)c << (4 * i);
+        }
+      }
+    }
+  }
+  if (nf) {
+    codes = 0;
+    d16 = 0;
+    m16 = 0;
+  }
+  *bad |= nf;
+  *meta = (uint32_t)d16 | ((uint32_t)m16 << 16);
+  return codes;
+}
+
+// INT8-encode this lane's 4 channels of a token-head vector spread over
+// `lanes` lanes.  Returns 4 packed int8 codes and, via scale, the fp16 bits.
+__device__ inline uint32_t encode_int8(const float x[4], int lanes, uint16_t* scale, int* bad) {
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  int nf = !(isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3]));
+  a = group_max(a, lanes);
+  nf = group_or(nf, lanes);
+  uint32_t out = 0;
+  uint16_t s16 = 0;
+  if (!nf) {
+    __half sh = __float2half_ru(__fdiv_ru(a, 127.0f));
+    float sf = __half2float(sh);
+    if (!isfinite(sf)) {
+      nf = 1;
+    } else {
+      s16 = __half_as_ushort(sh);
+      if (sf != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int c = __float2int_rn(__fdiv_rn(x[i], sf));
+          c = min(max(c, -127), 127);
+          out |= ((uint32_t)c & 0xFFu) << (8 * i);
+        }
+      }
+    }
+  }
+  if (nf) {
+    out = 0;
+    s16 = 0;
+  }
+  *bad |= nf;
+  *scale = s16;
+  return out;
+}
+
+// Validate a token; returns the physical page or -1 (status already set).
+__device__ inline int token_page(const Layout& L, int s, int p, const int32_t* seq_lens,
+                                 const int32_t* block_table, int32_t* status, bool report,
+                                 int* seq_len_out) {
+  if (s < 0 || s >= L.max_seqs) {
+    if (report) set_status(status, KV4_STATUS_BAD_SEQ);
+    return -1;
+  }
+  int len = seq_lens[s];
+  if (p < 0 || p >= len || p >= L.max_pages * kPage) {
+    if (report) set_status(status, KV4_STATUS_BAD_POS);
+    return -1;
+  }
+  int page = block_table[(long long)s * L.max_pages + p / kPage];
+  if (page < 0 || page >= L.num_pages) {
+    if (report) set_status(status, KV4_STATUS_BAD_PAGE);
+    return -1;
+  }
+  *seq_len_out = len;
+  return page;
+}
+
+__global__ void __launch_bounds__(256) quant_append_kernel(
+    Layout L, uint8_t* __restrict__ paged, uint8_t* __restrict__ side,
+    const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+    const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos, int T,
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
+    int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)T * L.h_kv) return;
+  const int t = (int)(w / L.h_kv);
+  const int h = (int)(w % L.h_kv);
+  const int s = tok_seq[t], p = tok_pos[t];
+  int len = 0;
+  const int page = token_page(L, s, p, seq_lens, block_table, status, lane == 0 && h == 0, &len);
+  if (page < 0) return;
+
+  const int d_h = L.d_h, g = L.g, ng = d_h / g;
+  const int lanes = d_h / 4;  // active lanes (32 at d_h = 128, 16 at 64)
+  const int span = g / 4;     // lanes per INT4 group
+  const int slot = p % kPage;
+  const bool active = lane < lanes;
+  const int c0 = (active ? lane : 0) * 4;
+  const bool prot = (p < L.S) || (L.R > 0 && p >= len - L.R);
+
+  uint8_t* chunk = paged + ((long long)page * L.h_kv + h) * chunk_bytes(d_h, g);
+  int bad = 0;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint16_t* src = (kv == 0 ? k_new : v_new) + ((long long)t * L.h_kv + h) * d_h + c0;
+    uint2 raw = *reinterpret_cast<const uint2*>(src);  // 4 bf16, 8-byte aligned
+    float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+    if (!active) x[0] = x[1] = x[2] = x[3] = 0.f;
+    uint32_t meta;
+    uint32_t codes = encode_int4(x, span, &meta, &bad);
+    if (active) {
+      uint8_t* row = chunk + (kv == 0 ? 0 : codes_off_v(d_h)) + slot * (d_h / 2);
+      uint32_t packed = (codes & 0xFu) | ((codes >> 4) & 0xFu) << 4 | ((codes >> 8) & 0xFu) << 8 |
+                        ((codes >> 12) & 0xFu) << 12;
+      *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)packed;
+      if ((lane % span) == 0) {
+        uint8_t* m = chunk + (kv == 0 ? meta_off_k(d_h) : meta_off_v(d_h, g)) + slot * ng * 4;
+        *reinterpret_cast<uint32_t*>(m + 4 * (lane / span)) = meta;
+      }
+    }
+    if (prot) {
+      uint16_t s16;
+      uint32_t c8 = encode_int8(x, lanes < 32 ? lanes : 32, &s16, &bad);
+      const int NS = L.S + L.R;
+      const int ss = side_slot(p, L.S, L.R);
+      uint8_t* blk = side + ((long long)s * L.h_kv + h) * side_block_bytes(d_h, L.S, L.R);
+      if (active)
+        *reinterpret_cast<uint32_t*>(blk + (long long)kv * NS * d_h + (long long)ss * d_h + c0) =
+            c8;
+      if (lane == 0)
+        *reinterpret_cast<uint16_t*>(blk + 2LL * NS * d_h + (long long)kv * NS * 2 + ss * 2) = s16;
+    }
+  }
+  if (bad && lane == 0) set_status(status, KV4_STATUS_NONFINITE);
+}
+
+// Comparator cache: [page][h_kv][K|V][16][d_h] bf16, plain copy.
+__global__ void __launch_bounds__(256) bf16_append_kernel(
+    Layout L, uint16_t* __restrict__ cache, const uint16_t* __restrict__ k_new,
+    const uint16_t* __restrict__ v_new, const int32_t* __restrict__ tok_seq,
+    const int32_t* __restrict__ tok_pos, int T, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ block_table, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)T * L.h_kv) return;
+  const int t = (int)(w / L.h_kv);
+  const int h = (int)(w % L.h_kv);
+  int len = 0;
+  const int page =
+      token_page(L, tok_seq[t], tok_pos[t], seq_lens, block_table, status, lane == 0 && h == 0,
+                 &len);
+  if (page < 0) return;
+  const int d_h = L.d_h;
+  const int slot = tok_pos[t] % kPage;
+  uint16_t* base = cache + ((long long)page * L.h_kv + h) * 2 * kPage * d_h;
+  for (int c = lane * 4; c < d_h; c += 128) {
+    const long long src = ((long long)t * L.h_kv + h) * d_h + c;
+    *reinterpret_cast<uint2*>(base + slot * d_h + c) = *reinterpret_cast<const uint2*>(k_new + src);
+    *reinterpret_cast<uint2*>(base + (kPage + slot) * d_h + c) =
+        *reinterpret_cast<const uint2*>(v_new + src);
+  }
+}
+
+cudaError_t launch_quant_append(const Layout& L, void* paged, void* side, const uint16_t* k_new,
+                                const uint16_t* v_new, const int32_t* tok_seq,
+                                const int32_t* tok_pos, int T, const int32_t* seq_lens,
+                                const int32_t* block_table, int32_t* status, cudaStream_t st) {
+  const long long warps = (long long)T * L.h_kv;
+  const int wpb = 8;
+  const long long blocks = (warps + wpb - 1) / wpb;
+  quant_append_kernel<<<(unsigned)blocks, wpb * 32, 0, st>>>(
+      L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
+      block_table, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_append(const Layout& L, void* cache, const uint16_t* k_new,
+                               const uint16_t* v_new, const int32_t* tok_seq,
+                               const int32_t* tok_pos, int T, const int32_t* seq_lens,
+                               const int32_t* block_table, int32_t* status, cudaStream_t st) {
+  const long long warps = (long long)T * L.h_kv;
+  const int wpb = 8;
+  const long long blocks = (warps + wpb - 1) / wpb;
+  bf16_append_kernel<<<(unsigned)blocks, wpb * 32, 0, st>>>(
+      L, (uint16_t*)cache, k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table, status);
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

@@ -1,0 +1,135 @@
+// kv4_common.cuh -- internal helpers shared by the kv4 CUDA translation units:
+// packed-layout offsets, status reporting, and thin inline-PTX wrappers for
+// the sm_100-family asynchronous copy engine (mbarrier + cp.async.bulk).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kv4.h"
+
+namespace kv4 {
+
+constexpr int kPage = 16;
+
+// ---------------------------------------------------------------- layout
+// Bytes of one (page, kv head) chunk: K codes, V codes, K meta, V meta.
+__host__ __device__ inline int chunk_bytes(int d_h, int g) { return 16 * d_h + 128 * (d_h / g); }
+__host__ __device__ inline int codes_off_v(int d_h) { return 8 * d_h; }  // 16 rows * d_h/2
+__host__ __device__ inline int meta_off_k(int d_h) { return 16 * d_h; }
+__host__ __device__ inline int meta_off_v(int d_h, int g) { return 16 * d_h + 64 * (d_h / g); }
+
+// Side-cache block of one (slot, kv head).
+__host__ __device__ inline long long side_block_bytes(int d_h, int S, int R) {
+  long long b = (long long)(S + R) * (2LL * d_h + 4);
+  return (b + 15) / 16 * 16;
+}
+
+struct Layout {
+  int h_q, h_kv, d_h, g, S, R;
+  int max_seqs, num_pages, max_pages;
+};
+
+// Region split of one sequence (KV4-RL Sec. 5.2-5.3): protected positions are
+// [0, sink_end) and [rec_start, L); the INT4 region is [sink_end, rec_start).
+struct Regions {
+  int sink_end, rec_start, n_prot;
+};
+__host__ __device__ inline Regions regions(int L, int S, int R) {
+  Regions r;
+  r.sink_end = L < S ? L : S;
+  int rs = L - R;
+  r.rec_start = rs > r.sink_end ? rs : r.sink_end;
+  r.n_prot = r.sink_end + (L - r.rec_start);
+  return r;
+}
+// i-th protected position (0 <= i < n_prot) and its side slot.
+__host__ __device__ inline int prot_pos(const Regions& r, int i) {
+  return i < r.sink_end ? i : r.rec_start + (i - r.sink_end);
+}
+__host__ __device__ inline int side_slot(int p, int S, int R) { return p < S ? p : S + (p % R); }
+
+__device__ inline void set_status(int32_t* st, int bits) {
+  if (st && bits) atomicOr(st, bits);
+}
+
+// ------------------------------------------------------------ conversions
+__device__ inline float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ inline float f16_bits_to_f32(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)h));
+}
+// float -> bf16 bits, round to nearest even (NaN kept quiet)
+__device__ inline uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------- mbarrier + 1-D bulk async copy
+__device__ inline uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ inline void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the phase did not
+// complete within the iteration limit (the caller then reports an error and
+// skips the data instead of hanging).
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters = 4000000u) {
+  uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < max_iters; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned) completing on `bar` via complete_tx.
+__device__ inline void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------ reductions
+__device__ inline float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ inline float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace kv4

@@ -1,0 +1,624 @@
+// kv4_decode.cu -- split-KV GQA decode attention over the mixed INT4/INT8
+// paged cache (KV4-RL Sec. 5.3; App. A.3), the eq. A1 split/region merge, and
+// the bf16-cache comparator.
+//
+// Work decomposition.  One CTA per (split, kv head, sequence).  The INT4
+// region of a sequence, [min(S,L), max(S,L-R)), is cut into splits of
+// `pages_per_split` pages; the protected positions (sinks and the recent
+// window, read from the INT8 side cache) form up to `n8` further splits.
+// Every split emits a locally normalised output and log-normaliser per query
+// head; kv4_split_combine merges them (eq. A1), with zero weight for empty
+// splits.
+//
+// Inside a CTA, 4 warps each stream their own pages: lane 0 of a warp issues a
+// 1-D bulk asynchronous copy (cp.async.bulk, TMA engine) of the whole
+// (page, kv head) chunk -- codes and metadata, 2.5 KB at d=128, g=32 -- into a
+// 4-stage shared-memory ring guarded by mbarriers, so each warp keeps up to
+// four chunks in flight while it computes.  The warps merge their online-
+// softmax states through shared memory at the end.
+//
+// Scores use the affine factorisation of eq. 5.1 per group:
+//   q . k^ = Delta * (q . c) + m * sum(q)
+// so the INT4 codes enter the dot product exactly and scale/offset are applied
+// once per group; softmax runs in the log2 domain with sm_scale*log2(e) folded
+// into the scores.  All accumulation is fp32.
+#include <math.h>
+
+#include "kv4_common.cuh"
+
+namespace kv4 {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// exact small-integer -> float (c < 2^23) without the conversion pipe
+__device__ inline float u2f(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
+
+template <int D, int G>
+struct Smem {
+  float q[G][2][D / 2 + 4];      // query, split in two halves (padded: no bank conflicts)
+  float qsum[D / 32][G];         // per 32-channel block sum of q (combined per group)
+  float p[kWarps][16][G];        // probabilities of the current tile, per warp
+  float mrg_m[kWarps][G];
+  float mrg_l[kWarps][G];
+  float mrg_o[kWarps][G][D];
+  uint64_t bar[kWarps][kStages];
+};
+
+// Online softmax state of one warp: lanes own D/32 output channels.
+template <int D, int G>
+struct WarpState {
+  static constexpr int PD = D / 32;
+  float m[G];       // running max (log2 domain), uniform across the warp
+  float l[G];       // partial sum of p over this lane's tokens
+  float acc[G][PD];  // unnormalised output channels [lane*PD, lane*PD+PD)
+  __device__ void init() {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < PD; ++i) acc[j][i] = 0.f;
+    }
+  }
+};
+
+// Given this lane's score s[j] for token t = lane>>1 (both lanes of a token
+// hold the same value; -inf = masked), update the running max, rescale, and
+// publish p[t][j] to shared memory.
+template <int D, int G>
+__device__ inline void softmax_tile(WarpState<D, G>& ws, const float s[G], float (*p)[G],
+                                    int lane) {
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    float tmax = warp_max(s[j]);
+    float mnew = fmaxf(ws.m[j], tmax);
+    float alpha, pj;
+    if (mnew == -INFINITY) {
+      alpha = 1.f;
+      pj = 0.f;
+    } else {
+      alpha = exp2f(ws.m[j] - mnew);
+      pj = exp2f(s[j] - mnew);
+    }
+    ws.m[j] = mnew;
+    ws.l[j] = ws.l[j] * alpha + ((lane & 1) ? 0.f : pj);
+#pragma unroll
+    for (int i = 0; i < WarpState<D, G>::PD; ++i) ws.acc[j][i] *= alpha;
+    if ((lane & 1) == 0) p[lane >> 1][j] = pj;
+  }
+}
+
+// ---------------------------------------------------------------- INT4 tile
+// QK for one 16-token page chunk in shared memory.  Lane (t, half) covers
+// channels [half*D/2, half*D/2 + D/2) of token t.
+template <int D, int G>
+__device__ inline void qk_int4(const Smem<D, G>& sm, const uint8_t* chunk, int g, int t, int half,
+                               float s[G]) {
+  const int ng = D / g;
+  const uint32_t* krow = reinterpret_cast<const uint32_t*>(chunk + t * (D / 2) + half * (D / 4));
+  const uint32_t* kmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_k(D) + t * ng * 4);
+#pragma unroll
+  for (int j = 0; j < G; ++j) s[j] = 0.f;
+  float part[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) part[j] = 0.f;
+  constexpr int WORDS = D / 16;  // 8 nibbles per word, D/2 channels per lane
+#pragma unroll
+  for (int w = 0; w < WORDS; ++w) {
+    const uint32_t word = krow[w];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const float c = u2f((word >> (4 * n)) & 0xFu);
+      const int k = w * 8 + n;
+#pragma unroll
+      for (int j = 0; j < G; ++j) part[j] = fmaf(sm.q[j][half][k], c, part[j]);
+    }
+    const int ch_end = half * (D / 2) + w * 8 + 8;  // channel after this word
+    if (ch_end % g == 0 || w == WORDS - 1) {
+      const int grp = (ch_end - 1) / g;
+      const uint32_t mt = kmeta[grp];
+      const float delta = f16_bits_to_f32(mt & 0xFFFFu);
+      const float off = f16_bits_to_f32(mt >> 16);
+      // sum of q over this lane's part of the group
+      const int lo = max(grp * g, half * (D / 2)) / 32, hi = min((grp + 1) * g, half * (D / 2) + D / 2) / 32;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float qs = 0.f;
+        for (int bq = lo; bq < hi; ++bq) qs += sm.qsum[bq][j];
+        s[j] = fmaf(delta, part[j], fmaf(off, qs, s[j]));
+        part[j] = 0.f;
+      }
+    }
+  }
+}
+
+// PV for one 16-token page: lane owns channels [lane*PD, lane*PD + PD).
+template <int D, int G>
+__device__ inline void pv_int4(WarpState<D, G>& ws, const uint8_t* chunk, int g, const float (*p)[G],
+                               int lane, uint32_t tok_mask) {
+  constexpr int PD = D / 32;
+  const int ng = D / g;
+  const int c0 = lane * PD;
+  const int grp = c0 / g;
+  const uint8_t* vcodes = chunk + codes_off_v(D);
+  const uint32_t* vmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_v(D, g));
+  for (int t = 0; t < kPage; ++t) {
+    if (!((tok_mask >> (2 * t)) & 1u)) continue;  // masked slot: may hold stale bytes
+    uint32_t bits;
+    if (PD == 4)
+      bits = *reinterpret_cast<const uint16_t*>(vcodes + t * (D / 2) + c0 / 2);
+    else
+      bits = vcodes[t * (D / 2) + c0 / 2];
+    const uint32_t mt = vmeta[t * ng + grp];
+    const float delta = f16_bits_to_f32(mt & 0xFFFFu);
+    const float off = f16_bits_to_f32(mt >> 16);
+    float v[PD];
+#pragma unroll
+    for (int i = 0; i < PD; ++i) v[i] = fmaf(delta, u2f((bits >> (4 * i)) & 0xFu), off);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float pj = p[t][j];
+#pragma unroll
+      for (int i = 0; i < PD; ++i) ws.acc[j][i] = fmaf(pj, v[i], ws.acc[j][i]);
+    }
+  }
+}
+
+// ------------------------------------------------------------ merge + store
+template <int D, int G>
+__device__ inline void merge_and_store(Smem<D, G>& sm, WarpState<D, G>& ws, int warp, int lane,
+                                       float* part_o, float* part_lse, long long row0, int n_split,
+                                       int split) {
+  constexpr int PD = D / 32;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const float lsum = warp_sum(ws.l[j]);
+    if (lane == 0) {
+      sm.mrg_m[warp][j] = ws.m[j];
+      sm.mrg_l[warp][j] = lsum;
+    }
+#pragma unroll
+    for (int i = 0; i < PD; ++i) sm.mrg_o[warp][j][lane * PD + i] = ws.acc[j][i];
+  }
+  __syncthreads();
+  // thread -> (head j, channel block)
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int j = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.mrg_m[w][j]);
+    float Lt = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = sm.mrg_m[w][j];
+        if (mw == -INFINITY) continue;
+        const float sc = exp2f(mw - M);
+        Lt += sm.mrg_l[w][j] * sc;
+        o += sm.mrg_o[w][j][d] * sc;
+      }
+    }
+    const long long row = row0 + j;  // (seq * h_q + head)
+    const bool empty = !(Lt > 0.f);
+    part_o[(row * n_split + split) * D + d] = empty ? 0.f : o / Lt;
+    if (d == 0) part_lse[row * n_split + split] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+  }
+}
+
+template <int D, int G>
+__device__ inline void load_query(Smem<D, G>& sm, const uint16_t* q, long long row0) {
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int j = idx / D, d = idx % D;
+    sm.q[j][d / (D / 2)][d % (D / 2)] = bf16_bits_to_f32(q[(row0 + j) * D + d]);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * (D / 32); idx += kThreads) {
+    const int j = idx % G, bq = idx / G;
+    float s = 0.f;
+    for (int d = bq * 32; d < bq * 32 + 32; ++d) s += sm.q[j][d / (D / 2)][d % (D / 2)];
+    sm.qsum[bq][j] = s;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------ main kernel
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(
+    Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
+    const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ block_table, float scale_log2, int n4, int pages_per_split,
+    int prot_per_split, float* __restrict__ part_o, float* __restrict__ part_lse,
+    int32_t* status) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
+  const int cb = chunk_bytes(D, L.g);
+  uint8_t* stage_base = smem_raw + ((sizeof(Smem<D, G>) + 127) / 128) * 128;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int n_split = gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row0 = (long long)b * L.h_q + (long long)h * G;
+
+  int len = seq_lens[b];
+  if (len < 0 || len > L.max_pages * kPage) {
+    if (threadIdx.x == 0 && split == 0 && h == 0) set_status(status, KV4_STATUS_BAD_LEN);
+    len = 0;
+  }
+  const Regions rg = regions(len, L.S, L.R);
+
+  WarpState<D, G> ws;
+  ws.init();
+  load_query(sm, q, row0);
+
+  const int t = lane >> 1, half = lane & 1;
+  if (split < n4) {
+    // ---------------------------------------------------- INT4 region split
+    const int first_page = rg.sink_end / kPage;
+    const int end_page = (rg.rec_start + kPage - 1) / kPage;
+    const int p_lo = first_page + split * pages_per_split;
+    const int p_hi = min(end_page, p_lo + pages_per_split);
+    const int n_my = rg.rec_start > rg.sink_end && p_hi > p_lo + warp
+                         ? (p_hi - p_lo - warp + kWarps - 1) / kWarps
+                         : 0;
+    uint8_t* my_stages = stage_base + (size_t)warp * kStages * cb;
+    const int32_t* bt_row = block_table + (long long)b * L.max_pages;
+    if (lane == 0) {
+      for (int st = 0; st < kStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    auto issue = [&](int i) {
+      const int pg = p_lo + warp + i * kWarps;
+      const int phys = bt_row[pg];
+      uint64_t* bar = &sm.bar[warp][i % kStages];
+      if (phys >= 0 && phys < L.num_pages) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, (uint32_t)cb);
+        bulk_g2s(my_stages + (size_t)(i % kStages) * cb,
+                 paged + ((long long)phys * L.h_kv + h) * cb, (uint32_t)cb, bar);
+      } else {
+        set_status(status, KV4_STATUS_BAD_PAGE);
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+      }
+    };
+    if (lane == 0)
+      for (int i = 0; i < min(kStages, n_my); ++i) issue(i);
+    for (int i = 0; i < n_my; ++i) {
+      const int pg = p_lo + warp + i * kWarps;
+      const int phys = bt_row[pg];
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStages], (i / kStages) & 1));
+      const bool valid = ok && phys >= 0 && phys < L.num_pages;
+      if (!ok && lane == 0) set_status(status, KV4_STATUS_BAD_PAGE);
+      const uint8_t* chunk = my_stages + (size_t)(i % kStages) * cb;
+      const int pos = pg * kPage + t;
+      const bool tok_ok = valid && pos >= rg.sink_end && pos < rg.rec_start;
+      const uint32_t tok_mask = __ballot_sync(0xffffffffu, tok_ok);
+      float s[G];
+      if (valid) {
+        qk_int4<D, G>(sm, chunk, L.g, t, half, s);
+#pragma unroll
+        for (int j = 0; j < G; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], 1);
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) s[j] = tok_ok ? s[j] * scale_log2 : -INFINITY;
+      softmax_tile<D, G>(ws, s, sm.p[warp], lane);
+      __syncwarp();
+      if (valid) pv_int4<D, G>(ws, chunk, L.g, sm.p[warp], lane, tok_mask);
+      __syncwarp();
+      if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+    }
+  } else {
+    // ---------------------------------------- protected (INT8 side) split
+    const int k = split - n4;
+    const int i_lo = k * prot_per_split;
+    const int i_hi = min(rg.n_prot, i_lo + prot_per_split);
+    const int NS = L.S + L.R;
+    const uint8_t* blk = side + ((long long)b * L.h_kv + h) * side_block_bytes(D, L.S, L.R);
+    const int8_t* k8 = reinterpret_cast<const int8_t*>(blk);
+    const int8_t* v8 = reinterpret_cast<const int8_t*>(blk + (long long)NS * D);
+    const uint16_t* ks = reinterpret_cast<const uint16_t*>(blk + 2LL * NS * D);
+    const uint16_t* vs = ks + NS;
+    for (int base = i_lo + warp * 16; base < i_hi; base += kWarps * 16) {
+      const int i = base + t;
+      const bool tok_ok = i < i_hi;
+      const int slot = tok_ok ? side_slot(prot_pos(rg, i), L.S, L.R) : 0;
+      float s[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) s[j] = 0.f;
+      if (tok_ok) {
+        const int8_t* row = k8 + (long long)slot * D + half * (D / 2);
+#pragma unroll
+        for (int w = 0; w < D / 8; ++w) {
+          const uint32_t word = *reinterpret_cast<const uint32_t*>(row + 4 * w);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            const float c = (float)(int8_t)((word >> (8 * n)) & 0xFFu);
+#pragma unroll
+            for (int j = 0; j < G; ++j) s[j] = fmaf(sm.q[j][half][4 * w + n], c, s[j]);
+          }
+        }
+        const float sc = f16_bits_to_f32(ks[slot]);
+#pragma unroll
+        for (int j = 0; j < G; ++j) s[j] *= sc;
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        s[j] += __shfl_xor_sync(0xffffffffu, s[j], 1);
+        s[j] = tok_ok ? s[j] * scale_log2 : -INFINITY;
+      }
+      softmax_tile<D, G>(ws, s, sm.p[warp], lane);
+      __syncwarp();
+      constexpr int PD = D / 32;
+      const int ntok = min(16, i_hi - base);
+      for (int tt = 0; tt < ntok; ++tt) {
+        const int slot2 = side_slot(prot_pos(rg, base + tt), L.S, L.R);
+        const float sc = f16_bits_to_f32(vs[slot2]);
+        uint32_t word;
+        if (PD == 4)
+          word = *reinterpret_cast<const uint32_t*>(v8 + (long long)slot2 * D + lane * PD);
+        else
+          word = *reinterpret_cast<const uint16_t*>(v8 + (long long)slot2 * D + lane * PD);
+        float v[PD];
+#pragma unroll
+        for (int ii = 0; ii < PD; ++ii) v[ii] = sc * (float)(int8_t)((word >> (8 * ii)) & 0xFFu);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pj = sm.p[warp][tt][j];
+#pragma unroll
+          for (int ii = 0; ii < PD; ++ii) ws.acc[j][ii] = fmaf(pj, v[ii], ws.acc[j][ii]);
+        }
+      }
+      __syncwarp();
+    }
+  }
+  merge_and_store<D, G>(sm, ws, warp, lane, part_o, part_lse, row0, n_split, split);
+}
+
+// ------------------------------------------------- bf16 comparator kernel
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads) bf16_decode_split_kernel(
+    Layout L, const uint16_t* __restrict__ cache, const uint16_t* __restrict__ q,
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
+    float scale_log2, int pages_per_split, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* status) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
+  constexpr int cb = 2 * kPage * D * 2;
+  uint8_t* stage_base = smem_raw + ((sizeof(Smem<D, G>) + 127) / 128) * 128;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int n_split = gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row0 = (long long)b * L.h_q + (long long)h * G;
+  int len = seq_lens[b];
+  if (len < 0 || len > L.max_pages * kPage) {
+    if (threadIdx.x == 0 && split == 0 && h == 0) set_status(status, KV4_STATUS_BAD_LEN);
+    len = 0;
+  }
+  WarpState<D, G> ws;
+  ws.init();
+  load_query(sm, q, row0);
+  const int t = lane >> 1, half = lane & 1;
+  const int end_page = (len + kPage - 1) / kPage;
+  const int p_lo = split * pages_per_split;
+  const int p_hi = min(end_page, p_lo + pages_per_split);
+  const int n_my = p_hi > p_lo + warp ? (p_hi - p_lo - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* my_stages = stage_base + (size_t)warp * kStages * cb;
+  const int32_t* bt_row = block_table + (long long)b * L.max_pages;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int i) {
+    const int pg = p_lo + warp + i * kWarps;
+    const int phys = bt_row[pg];
+    uint64_t* bar = &sm.bar[warp][i % kStages];
+    if (phys >= 0 && phys < L.num_pages) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, (uint32_t)cb);
+      bulk_g2s(my_stages + (size_t)(i % kStages) * cb,
+               reinterpret_cast<const uint8_t*>(cache) + ((long long)phys * L.h_kv + h) * cb,
+               (uint32_t)cb, bar);
+    } else {
+      set_status(status, KV4_STATUS_BAD_PAGE);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    }
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(kStages, n_my); ++i) issue(i);
+  constexpr int PD = D / 32;
+  for (int i = 0; i < n_my; ++i) {
+    const int pg = p_lo + warp + i * kWarps;
+    const int phys = bt_row[pg];
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStages], (i / kStages) & 1));
+    const bool valid = ok && phys >= 0 && phys < L.num_pages;
+    if (!ok && lane == 0) set_status(status, KV4_STATUS_BAD_PAGE);
+    const uint16_t* kc = reinterpret_cast<const uint16_t*>(my_stages + (size_t)(i % kStages) * cb);
+    const uint16_t* vc = kc + kPage * D;
+    const int pos = pg * kPage + t;
+    float s[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) s[j] = 0.f;
+    if (valid) {
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(kc + t * D + half * (D / 2));
+#pragma unroll 8
+      for (int w = 0; w < D / 4; ++w) {
+        const uint32_t word = row[w];
+        const float x0 = bf16_bits_to_f32(word & 0xFFFFu), x1 = bf16_bits_to_f32(word >> 16);
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+          s[j] = fmaf(sm.q[j][half][2 * w], x0, fmaf(sm.q[j][half][2 * w + 1], x1, s[j]));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      s[j] += __shfl_xor_sync(0xffffffffu, s[j], 1);
+      s[j] = (valid && pos < len) ? s[j] * scale_log2 : -INFINITY;
+    }
+    const uint32_t tok_mask = __ballot_sync(0xffffffffu, valid && pos < len);
+    softmax_tile<D, G>(ws, s, sm.p[warp], lane);
+    __syncwarp();
+    if (valid) {
+      for (int tt = 0; tt < kPage; ++tt) {
+        if (!((tok_mask >> (2 * tt)) & 1u)) continue;
+        float v[PD];
+        if (PD == 4) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(vc + tt * D + lane * PD);
+          v[0] = bf16_bits_to_f32(raw.x & 0xFFFFu);
+          v[1] = bf16_bits_to_f32(raw.x >> 16);
+          v[2] = bf16_bits_to_f32(raw.y & 0xFFFFu);
+          v[3] = bf16_bits_to_f32(raw.y >> 16);
+        } else {
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>(vc + tt * D + lane * PD);
+          v[0] = bf16_bits_to_f32(raw & 0xFFFFu);
+          v[PD - 1] = bf16_bits_to_f32(raw >> 16);
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pj = sm.p[warp][tt][j];
+#pragma unroll
+          for (int ii = 0; ii < PD; ++ii) ws.acc[j][ii] = fmaf(pj, v[ii], ws.acc[j][ii]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+  }
+  merge_and_store<D, G>(sm, ws, warp, lane, part_o, part_lse, row0, n_split, split);
+}
+
+// ------------------------------------------------------------ combine kernel
+// Eq. A1 over n parts per row; one warp per row, lane owns D/32 channels.
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse, int rows,
+                                                      int n, uint16_t* __restrict__ out,
+                                                      float* __restrict__ out_lse) {
+  constexpr int PD = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float* lse = part_lse + row * n;
+  float M = -INFINITY;
+  for (int r = lane; r < n; r += 32) M = fmaxf(M, lse[r]);
+  M = warp_max(M);
+  float acc[PD];
+#pragma unroll
+  for (int i = 0; i < PD; ++i) acc[i] = 0.f;
+  float Z = 0.f;
+  if (M != -INFINITY) {
+    for (int r = 0; r < n; ++r) {
+      const float z = lse[r];
+      if (z == -INFINITY) continue;
+      const float w = __expf(z - M);
+      Z += w;
+      const float* o = part_o + (row * n + r) * D + lane * PD;
+#pragma unroll
+      for (int i = 0; i < PD; ++i) acc[i] = fmaf(w, o[i], acc[i]);
+    }
+  }
+  const bool empty = !(Z > 0.f);
+#pragma unroll
+  for (int i = 0; i < PD; ++i)
+    out[row * D + lane * PD + i] = f32_to_bf16_bits(empty ? 0.f : acc[i] / Z);
+  if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
+}
+
+// ------------------------------------------------------------ launchers
+template <int D, int G>
+size_t decode_smem_bytes(int cb) {
+  return ((sizeof(Smem<D, G>) + 127) / 128) * 128 + (size_t)kWarps * kStages * cb;
+}
+
+template <int D, int G>
+cudaError_t launch_decode_t(const Layout& L, const void* paged, const void* side,
+                            const uint16_t* q, const int32_t* seq_lens, int num_seqs,
+                            const int32_t* block_table, float sm_scale, int n4,
+                            int pages_per_split, int n8, int prot_per_split, float* part_o,
+                            float* part_lse, int32_t* status, cudaStream_t st) {
+  const size_t smem = decode_smem_bytes<D, G>(chunk_bytes(D, L.g));
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n4 + n8, L.h_kv, num_seqs);
+  decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(
+      L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, block_table,
+      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, status);
+  return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_bf16_decode_t(const Layout& L, const void* cache, const uint16_t* q,
+                                 const int32_t* seq_lens, int num_seqs,
+                                 const int32_t* block_table, float sm_scale, int n_split,
+                                 int pages_per_split, float* part_o, float* part_lse,
+                                 int32_t* status, cudaStream_t st) {
+  const size_t smem = decode_smem_bytes<D, G>(2 * kPage * D * 2);
+  cudaError_t e = cudaFuncSetAttribute(bf16_decode_split_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_split, L.h_kv, num_seqs);
+  bf16_decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(
+      L, (const uint16_t*)cache, q, seq_lens, block_table, sm_scale * kLog2e, pages_per_split,
+      part_o, part_lse, status);
+  return cudaGetLastError();
+}
+
+#define KV4_DISPATCH_DG(D_, G_, CALL)                                                   \
+  do {                                                                                  \
+    if ((D_) == 128) {                                                                  \
+      switch (G_) {                                                                     \
+        case 1: { constexpr int D = 128, G = 1; return CALL; }                          \
+        case 2: { constexpr int D = 128, G = 2; return CALL; }                          \
+        case 4: { constexpr int D = 128, G = 4; return CALL; }                          \
+        case 8: { constexpr int D = 128, G = 8; return CALL; }                          \
+      }                                                                                 \
+    } else if ((D_) == 64) {                                                            \
+      switch (G_) {                                                                     \
+        case 1: { constexpr int D = 64, G = 1; return CALL; }                           \
+        case 2: { constexpr int D = 64, G = 2; return CALL; }                           \
+        case 4: { constexpr int D = 64, G = 4; return CALL; }                           \
+        case 8: { constexpr int D = 64, G = 8; return CALL; }                           \
+      }                                                                                 \
+    }                                                                                   \
+    return cudaErrorInvalidValue;                                                       \
+  } while (0)
+
+cudaError_t launch_decode(const Layout& L, const void* paged, const void* side, const uint16_t* q,
+                          const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
+                          float sm_scale, int n4, int pages_per_split, int n8, int prot_per_split,
+                          float* part_o, float* part_lse, int32_t* status, cudaStream_t st) {
+  KV4_DISPATCH_DG(L.d_h, L.h_q / L.h_kv,
+                  (launch_decode_t<D, G>(L, paged, side, q, seq_lens, num_seqs, block_table,
+                                         sm_scale, n4, pages_per_split, n8, prot_per_split,
+                                         part_o, part_lse, status, st)));
+}
+
+cudaError_t launch_bf16_decode(const Layout& L, const void* cache, const uint16_t* q,
+                               const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
+                               float sm_scale, int n_split, int pages_per_split, float* part_o,
+                               float* part_lse, int32_t* status, cudaStream_t st) {
+  KV4_DISPATCH_DG(L.d_h, L.h_q / L.h_kv,
+                  (launch_bf16_decode_t<D, G>(L, cache, q, seq_lens, num_seqs, block_table,
+                                              sm_scale, n_split, pages_per_split, part_o,
+                                              part_lse, status, st)));
+}
+
+cudaError_t launch_combine(const float* part_o, const float* part_lse, int rows, int n, int d_h,
+                           uint16_t* out, float* out_lse, cudaStream_t st) {
+  const int blocks = (rows + 3) / 4;
+  if (blocks == 0) return cudaSuccess;
+  if (d_h == 128)
+    combine_kernel<128><<<blocks, 128, 0, st>>>(part_o, part_lse, rows, n, out, out_lse);
+  else if (d_h == 64)
+    combine_kernel<64><<<blocks, 128, 0, st>>>(part_o, part_lse, rows, n, out, out_lse);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

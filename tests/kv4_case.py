@@ -1,0 +1,142 @@
+"""Shared helpers for the GPU parity tests: build one seeded case, run the
+CUDA path through the C ABI and the CPU oracle on the same inputs."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+from int8_kv_cache_kv4_gb300 import workloads as W
+
+# spec tolerance for bf16 attention outputs against the fp64 oracle
+MAX_ABS = 2e-3
+MEAN_ABS = 2e-4
+LSE_ABS = 1e-3   # fp32 scores and normaliser vs fp64
+
+
+class Case:
+    """A batch of sequences with seeded K/V/q, a seeded page permutation and
+    token lists for a populate append followed by a one-token append."""
+
+    def __init__(self, lens, *, h_q=32, h_kv=8, d_h=128, g=32, S=4, R=64, seed=1, extra_pages=3):
+        self.lens = np.asarray(lens, dtype=np.int32)
+        self.B = len(self.lens)
+        self.h_q, self.h_kv, self.d_h, self.g, self.S, self.R = h_q, h_kv, d_h, g, S, R
+        self.seed = seed
+        self.mpps = max(1, (int(self.lens.max(initial=0)) + 15) // 16)
+        self.num_pages = W.pool_pages(self.lens, extra_pages)
+        self.bt = W.block_table(seed, self.lens, self.mpps, self.num_pages)
+        outl = W.outlier_channels(seed, h_kv, d_h)
+        self.k = []
+        self.v = []
+        for b, L in enumerate(self.lens):
+            kb, vb = W.kv_numpy_block(seed, b, h_kv, int(L), d_h, outl)
+            self.k.append(kb)
+            self.v.append(vb)
+        self.q = W.q_numpy(seed, self.B, h_q, d_h)
+        self.sm_scale = 1.0 / math.sqrt(d_h)
+
+    def layout_kw(self):
+        return dict(h_kv=self.h_kv, d_h=self.d_h, g=self.g, S=self.S, R=self.R, max_seqs=self.B,
+                    num_pages=self.num_pages, max_pages_per_seq=self.mpps)
+
+    def tokens(self, stage):
+        """stage 0: positions [0, L-1) of every sequence; stage 1: position L-1.
+        Returns (k [T][h_kv][d_h], v, tok_seq, tok_pos, seq_lens_after)."""
+        ks, vs, seqs, poss = [], [], [], []
+        for b, L in enumerate(self.lens):
+            L = int(L)
+            rng = range(0, max(L - 1, 0)) if stage == 0 else (range(L - 1, L) if L > 0 else range(0))
+            for p in rng:
+                ks.append(self.k[b][:, p, :])
+                vs.append(self.v[b][:, p, :])
+                seqs.append(b)
+                poss.append(p)
+        lens_after = np.maximum(self.lens - (1 if stage == 0 else 0), 0).astype(np.int32)
+        if not ks:
+            z = np.zeros((0, self.h_kv, self.d_h), dtype=np.uint16)
+            return z, z, np.zeros(0, np.int32), np.zeros(0, np.int32), lens_after
+        return (np.ascontiguousarray(np.stack(ks)), np.ascontiguousarray(np.stack(vs)),
+                np.array(seqs, np.int32), np.array(poss, np.int32), lens_after)
+
+    # ------------------------------------------------------------- oracle
+    def oracle_cache(self):
+        paged = np.zeros(self.num_pages * self.h_kv * oracle.chunk_bytes(self.d_h, self.g), np.uint8)
+        side = np.zeros(max(16, self.B * self.h_kv * oracle.side_block_bytes(self.d_h, self.S, self.R)),
+                        np.uint8)
+        st = 0
+        for stage in (0, 1):
+            k, v, s, p, la = self.tokens(stage)
+            st |= oracle.quant_append(**self.layout_kw(), paged=paged, side=side, k_new=k, v_new=v,
+                                      tok_seq=s, tok_pos=p, seq_lens=la, block_table=self.bt)
+        return paged, side, st
+
+    def oracle_decode(self, seqs=None):
+        seqs = range(self.B) if seqs is None else seqs
+        outs, lses = {}, {}
+        for b in seqs:
+            o, l, _ = oracle.decode_seq(self.q[b], self.k[b], self.v[b], g=self.g, S=self.S,
+                                        R=self.R, sm_scale=self.sm_scale)
+            outs[b], lses[b] = o, l
+        return outs, lses
+
+    def oracle_bf16(self, seqs=None):
+        seqs = range(self.B) if seqs is None else seqs
+        outs, lses = {}, {}
+        for b in seqs:
+            kh = W.bf16_bits_to_f32(self.k[b]).astype(np.float64)
+            vh = W.bf16_bits_to_f32(self.v[b]).astype(np.float64)
+            outs[b], lses[b] = oracle.attend(self.q[b], kh, vh, self.sm_scale)
+        return outs, lses
+
+    # ---------------------------------------------------------------- GPU
+    def gpu(self, *, with_bf16=False):
+        import torch
+        from int8_kv_cache_kv4_gb300.cache import MixedKVCache
+        dev = torch.device("cuda")
+        c = MixedKVCache(h_q=self.h_q, h_kv=self.h_kv, d_h=self.d_h, group=self.g, sink=self.S,
+                         recent=self.R, max_seqs=self.B, num_pages=self.num_pages,
+                         max_pages_per_seq=self.mpps, device=dev, with_bf16=with_bf16)
+        c.set_block_table(self.bt)
+        for stage in (0, 1):
+            k, v, s, p, la = self.tokens(stage)
+            if len(s) == 0:
+                continue
+            to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)
+            c.append(to(k, torch.int16).view(torch.bfloat16), to(v, torch.int16).view(torch.bfloat16),
+                     to(s, torch.int32), to(p, torch.int32), to(la, torch.int32))
+        return c
+
+    def gpu_decode(self, c, max_splits=0, bf16=False):
+        import torch
+        dev = c.device
+        q = torch.from_numpy(self.q.view(np.int16)).to(dev).view(torch.bfloat16)
+        lens = torch.from_numpy(self.lens).to(dev)
+        out = torch.empty((self.B, self.h_q, self.d_h), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((self.B, self.h_q), dtype=torch.float32, device=dev)
+        if bf16:
+            c.decode_bf16(q, lens, out, lse, max_splits=max_splits)
+        else:
+            c.decode(q, lens, out, lse, max_splits=max_splits)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def compare_outputs(out, lse, ref_out, ref_lse, seqs, lens, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    errs = []
+    for b in seqs:
+        if int(lens[b]) == 0:
+            assert np.all(out[b] == 0), f"seq {b}: empty sequence must give zeros"
+            assert np.all(np.isneginf(lse[b]))
+            continue
+        e = np.abs(out[b] - ref_out[b])
+        errs.append(e)
+        np.testing.assert_allclose(lse[b], ref_lse[b], atol=LSE_ABS, rtol=0,
+                                   err_msg=f"lse of seq {b}")
+    if errs:
+        allerr = np.concatenate([e.ravel() for e in errs])
+        assert allerr.max() <= max_abs, f"max abs err {allerr.max():.3e} > {max_abs}"
+        assert allerr.mean() <= mean_abs, f"mean abs err {allerr.mean():.3e} > {mean_abs}"
+        return float(allerr.max()), float(allerr.mean())
+    return 0.0, 0.0

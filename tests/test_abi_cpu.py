@@ -1,0 +1,74 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every entry point include/kv4.h declares, and its host-only functions
+(validation, sizing, split plan) behave -- no GPU calls."""
+import ctypes
+import subprocess
+
+import pytest
+
+from int8_kv_cache_kv4_gb300 import build, kv4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kv4.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = kv4.declared_symbols()
+    assert "kv4_quant_append" in names and "kv4_decode_attn" in names
+    assert "kv4_split_combine" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", kv4.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+
+
+def test_layout_validation(lib):
+    ok = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+    assert lib.kv4_check_layout(ctypes.byref(ok)) == kv4.KV4_OK
+    for field, val, code in [("head_dim", 96, kv4.KV4_ERR_UNSUPPORTED),
+                             ("page_size", 32, kv4.KV4_ERR_UNSUPPORTED),
+                             ("int4_group", 16, kv4.KV4_ERR_UNSUPPORTED),
+                             ("int8_group", 64, kv4.KV4_ERR_UNSUPPORTED),
+                             ("num_q_heads", 12, kv4.KV4_ERR_INVALID_ARG),
+                             ("sink", -1, kv4.KV4_ERR_INVALID_ARG),
+                             ("num_pages", 0, kv4.KV4_ERR_INVALID_ARG)]:
+        bad = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+        setattr(bad, field, val)
+        assert lib.kv4_check_layout(ctypes.byref(bad)) == code, field
+        assert kv4.paged_cache_bytes(bad) == 0
+
+
+def test_sizes_match_layout_description(lib):
+    for g, chunk in [(32, 2560), (64, 2304), (128, 2176)]:
+        lay = kv4.make_layout(group=g, max_seqs=3, num_pages=7, max_pages_per_seq=5)
+        assert kv4.paged_cache_bytes(lay) == 7 * 8 * chunk
+    lay = kv4.make_layout(sink=4, recent=128, max_seqs=3, num_pages=7, max_pages_per_seq=5)
+    assert kv4.side_cache_bytes(lay) == 3 * 8 * (132 * 260)
+    assert kv4.bf16_cache_bytes(lay) == 7 * 8 * 2 * 16 * 128 * 2
+
+
+def test_split_plan_and_workspace(lib):
+    lay = kv4.make_layout(recent=256, max_seqs=1, num_pages=8192, max_pages_per_seq=8192)
+    n = kv4.num_splits(lay, 1)
+    assert n * 8 >= 2 * 152      # a single long request still fills the GPU
+    assert kv4.workspace_bytes(lay, 1) >= 32 * n * (128 + 1) * 4
+    lay = kv4.make_layout(max_seqs=64, num_pages=40000, max_pages_per_seq=512)
+    assert kv4.num_splits(lay, 64, max_splits=1) == 2   # one INT4 split + one protected split
+    assert kv4.workspace_bytes(lay, 0) == 0 or kv4.workspace_bytes(lay, 0) >= 0
+
+
+def test_null_arguments_rejected_on_host(lib):
+    lay = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+    rc = lib.kv4_quant_append(ctypes.byref(lay), None, None, None, None, None, None, 3, None,
+                              None, None, None)
+    assert rc == kv4.KV4_ERR_INVALID_ARG
+    rc = lib.kv4_decode_attn(ctypes.byref(lay), None, None, None, None, 2, None, 0.1, 0, None, 0,
+                             None, None, None, None)
+    assert rc == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_quant_append(ctypes.byref(lay), None, None, None, None, None, None, 0, None,
+                                None, None, None) == kv4.KV4_OK   # T == 0: no-op
+    assert lib.kv4_status_string(kv4.KV4_ERR_WORKSPACE) == b"workspace too small"
