@@ -123,14 +123,26 @@ class Case:
         return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+def half_ulp_bf16(x):
+    """Half a bf16 ulp at |x|: the rounding error any bf16 output must carry."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
 def compare_outputs(out, lse, ref_out, ref_lse, seqs, lens, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    """Errors are measured beyond the bf16 rounding of the output itself:
+    e = max(0, |out - ref| - half_ulp_bf16(ref)).  For the diffuse attention
+    of the long workloads |o| < 0.5 and this equals the raw error within
+    1e-3; for very short sequences |o| can reach several units, where bf16
+    rounding alone exceeds 2e-3."""
     errs = []
     for b in seqs:
         if int(lens[b]) == 0:
             assert np.all(out[b] == 0), f"seq {b}: empty sequence must give zeros"
             assert np.all(np.isneginf(lse[b]))
             continue
-        e = np.abs(out[b] - ref_out[b])
+        e = np.maximum(np.abs(out[b] - ref_out[b]) - half_ulp_bf16(ref_out[b]), 0.0)
         errs.append(e)
         np.testing.assert_allclose(lse[b], ref_lse[b], atol=LSE_ABS, rtol=0,
                                    err_msg=f"lse of seq {b}")

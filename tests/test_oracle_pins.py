@@ -21,7 +21,8 @@ ALL_F16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
 
 
 def _finite_f16_table():
-    v = ALL_F16.view(np.float16).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        v = ALL_F16.view(np.float16).astype(np.float64)
     ok = np.isfinite(v)
     bits = ALL_F16[ok]
     vals = v[ok]
