@@ -36,9 +36,13 @@
  *                  V codes [16 slots][head_dim/2 bytes]
  *                  K meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
  *                  V meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
- *     Byte i of a slot's code row holds channel 2i in its low nibble and
- *     channel 2i+1 in its high nibble.  Position p of request slot s lives in
- *     page block_table[s][p / 16], slot p % 16.
+ *     Byte i of a K code row holds channel 2i in its low nibble and channel
+ *     2i+1 in its high nibble.  A V code row is the same sequence of bytes
+ *     cut into 16-byte pieces (32 channels each), with piece P of slot t
+ *     stored at piece position P ^ ((t >> 1) & (head_dim/32 - 1)) so that the
+ *     decode kernel's transposing shared-memory reads hit distinct banks.
+ *     Position p of request slot s lives in page block_table[s][p / 16],
+ *     slot p % 16.
  *     chunk bytes = 16*head_dim + 128*head_dim/g  (2560 at d=128, g=32).
  *   side cache   = [max_seqs][num_kv_heads][block], NS = sink + recent
  *     block      = K8 codes [NS][head_dim] int8, V8 codes [NS][head_dim] int8,
@@ -116,9 +120,9 @@ int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_s
 size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 
 /*
- * kv4_quant_append -- quantize-on-append (KV4-RL Sec. 5.3: "both
- * representations are produced directly from the source K/V vectors when each
- * token is generated"; App. A.3 "Encoding and allocation").
+ * kv4_quant_append -- quantize-on-append (KV4-RL Sec. 5.3 and App. A.3
+ * "Encoding and allocation": the INT4 entry and, for protected positions, the
+ * INT8 entry are both computed from the new token's source K/V).
  *
  * For each of the T new tokens t (request slot tok_seq[t], position
  * tok_pos[t]): writes the INT4 codes and per-group (Delta, m) of K and V into

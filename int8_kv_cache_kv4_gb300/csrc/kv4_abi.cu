@@ -20,6 +20,10 @@ cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, cons
                                cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
                            cudaStream_t);
+bool mma_supported(const Layout&);
+cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uint16_t*,
+                              const int32_t*, int, const int32_t*, float, int, int, int, int,
+                              float*, float*, int32_t*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -181,9 +185,16 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   float* part_lse = (float*)((char*)workspace + o_bytes);
   cudaStream_t st = (cudaStream_t)stream;
   const Layout L = to_layout(l);
-  cudaError_t e = launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
-                                p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse,
-                                dev_status, st);
+  // head_dim 128 with 4 query heads per kv head runs the tensor-core kernel;
+  // other shapes the CUDA-core kernel.
+  cudaError_t e =
+      mma_supported(L)
+          ? launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                              p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse,
+                              dev_status, st)
+          : launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                          p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse, dev_status,
+                          st);
   if (e != cudaSuccess) return KV4_ERR_LAUNCH;
   e = launch_combine(part_o, part_lse, (int)rows, p.total(), l->head_dim, out, out_lse, st);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;

@@ -1,0 +1,291 @@
+// kv4_decode_common.cuh -- pieces shared by the decode kernels: shared-memory
+// plan, online-softmax state, query staging, the protected (INT8 side cache)
+// split, and the cross-warp merge that emits one split's partial result
+// (KV4-RL App. A.3 eq. A1 is applied to these partials by the combine).
+#pragma once
+#include <math.h>
+
+#include "kv4_common.cuh"
+
+namespace kv4 {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// exact small-integer -> float (c < 2^23) without the conversion pipe
+__device__ inline float u2f(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
+
+template <int D, int G>
+struct Smem {
+  float q[G][2][D / 2 + 4];      // query, split in two halves (padded: no bank conflicts)
+  float qsum[D / 32][G];         // per 32-channel block sum of q (combined per group)
+  float p[kWarps][16][G];        // probabilities of the current tile, per warp
+  float mrg_m[kWarps][G];
+  float mrg_l[kWarps][G];
+  float mrg_o[kWarps][G][D];
+  float mrg_mt[kWarps][G][D / 32];  // additive term per 32-channel block (tensor-core path)
+  uint64_t bar[kWarps][kStages];
+};
+
+// Online softmax state of one warp: lanes own D/32 output channels.
+template <int D, int G>
+struct WarpState {
+  static constexpr int PD = D / 32;
+  float m[G];       // running max (log2 domain), uniform across the warp
+  float l[G];       // partial sum of p over this lane's tokens
+  float acc[G][PD];  // unnormalised output channels [lane*PD, lane*PD+PD)
+  __device__ void init() {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < PD; ++i) acc[j][i] = 0.f;
+    }
+  }
+};
+
+// Given this lane's score s[j] for token t = lane>>1 (both lanes of a token
+// hold the same value; -inf = masked), update the running max, rescale, and
+// publish p[t][j] to shared memory.
+template <int D, int G>
+__device__ inline void softmax_tile(WarpState<D, G>& ws, const float s[G], float (*p)[G],
+                                    int lane) {
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    float tmax = warp_max(s[j]);
+    float mnew = fmaxf(ws.m[j], tmax);
+    float alpha, pj;
+    if (mnew == -INFINITY) {
+      alpha = 1.f;
+      pj = 0.f;
+    } else {
+      alpha = exp2f(ws.m[j] - mnew);
+      pj = exp2f(s[j] - mnew);
+    }
+    ws.m[j] = mnew;
+    ws.l[j] = ws.l[j] * alpha + ((lane & 1) ? 0.f : pj);
+#pragma unroll
+    for (int i = 0; i < WarpState<D, G>::PD; ++i) ws.acc[j][i] *= alpha;
+    if ((lane & 1) == 0) p[lane >> 1][j] = pj;
+  }
+}
+
+// ---------------------------------------------------------------- INT4 tile
+// QK for one 16-token page chunk in shared memory.  Lane (t, half) covers
+// channels [half*D/2, half*D/2 + D/2) of token t.
+template <int D, int G>
+__device__ inline void qk_int4(const Smem<D, G>& sm, const uint8_t* chunk, int g, int t, int half,
+                               float s[G]) {
+  const int ng = D / g;
+  const uint32_t* krow = reinterpret_cast<const uint32_t*>(chunk + t * (D / 2) + half * (D / 4));
+  const uint32_t* kmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_k(D) + t * ng * 4);
+#pragma unroll
+  for (int j = 0; j < G; ++j) s[j] = 0.f;
+  float part[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) part[j] = 0.f;
+  constexpr int WORDS = D / 16;  // 8 nibbles per word, D/2 channels per lane
+#pragma unroll
+  for (int w = 0; w < WORDS; ++w) {
+    const uint32_t word = krow[w];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const float c = u2f((word >> (4 * n)) & 0xFu);
+      const int k = w * 8 + n;
+#pragma unroll
+      for (int j = 0; j < G; ++j) part[j] = fmaf(sm.q[j][half][k], c, part[j]);
+    }
+    const int ch_end = half * (D / 2) + w * 8 + 8;  // channel after this word
+    if (ch_end % g == 0 || w == WORDS - 1) {
+      const int grp = (ch_end - 1) / g;
+      const uint32_t mt = kmeta[grp];
+      const float delta = f16_bits_to_f32(mt & 0xFFFFu);
+      const float off = f16_bits_to_f32(mt >> 16);
+      // sum of q over this lane's part of the group
+      const int lo = max(grp * g, half * (D / 2)) / 32, hi = min((grp + 1) * g, half * (D / 2) + D / 2) / 32;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float qs = 0.f;
+        for (int bq = lo; bq < hi; ++bq) qs += sm.qsum[bq][j];
+        s[j] = fmaf(delta, part[j], fmaf(off, qs, s[j]));
+        part[j] = 0.f;
+      }
+    }
+  }
+}
+
+// PV for one 16-token page: lane owns channels [lane*PD, lane*PD + PD).
+template <int D, int G>
+__device__ inline void pv_int4(WarpState<D, G>& ws, const uint8_t* chunk, int g, const float (*p)[G],
+                               int lane, uint32_t tok_mask) {
+  constexpr int PD = D / 32;
+  const int ng = D / g;
+  const int c0 = lane * PD;
+  const int grp = c0 / g;
+  const uint8_t* vcodes = chunk + codes_off_v(D);
+  const uint32_t* vmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_v(D, g));
+  for (int t = 0; t < kPage; ++t) {
+    if (!((tok_mask >> (2 * t)) & 1u)) continue;  // masked slot: may hold stale bytes
+    uint32_t bits;
+    if (PD == 4)
+      bits = *reinterpret_cast<const uint16_t*>(vcodes + t * (D / 2) + vrow_byte(c0 / 2, t, D));
+    else
+      bits = vcodes[t * (D / 2) + vrow_byte(c0 / 2, t, D)];
+    const uint32_t mt = vmeta[t * ng + grp];
+    const float delta = f16_bits_to_f32(mt & 0xFFFFu);
+    const float off = f16_bits_to_f32(mt >> 16);
+    float v[PD];
+#pragma unroll
+    for (int i = 0; i < PD; ++i) v[i] = fmaf(delta, u2f((bits >> (4 * i)) & 0xFu), off);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float pj = p[t][j];
+#pragma unroll
+      for (int i = 0; i < PD; ++i) ws.acc[j][i] = fmaf(pj, v[i], ws.acc[j][i]);
+    }
+  }
+}
+
+// ------------------------------------------------------------ merge + store
+// Publish one warp's CUDA-core online-softmax state to shared memory.
+template <int D, int G>
+__device__ inline void write_state(Smem<D, G>& sm, WarpState<D, G>& ws, int warp, int lane) {
+  constexpr int PD = D / 32;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const float lsum = warp_sum(ws.l[j]);
+    if (lane == 0) {
+      sm.mrg_m[warp][j] = ws.m[j];
+      sm.mrg_l[warp][j] = lsum;
+    }
+#pragma unroll
+    for (int i = 0; i < PD; ++i) sm.mrg_o[warp][j][lane * PD + i] = ws.acc[j][i];
+    if (lane < D / 32) sm.mrg_mt[warp][j][lane] = 0.f;
+  }
+}
+
+// Merge the warps' states (each: running max m, sum l, unnormalised output o
+// plus a per-32-channel-block additive term mt) and store the split's locally
+// normalised output and natural-log normaliser.
+template <int D, int G>
+__device__ inline void merge_store(Smem<D, G>& sm, float* part_o, float* part_lse, long long row0,
+                                   int n_split, int split) {
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int j = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.mrg_m[w][j]);
+    float Lt = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = sm.mrg_m[w][j];
+        if (mw == -INFINITY) continue;
+        const float sc = exp2f(mw - M);
+        Lt += sm.mrg_l[w][j] * sc;
+        o += (sm.mrg_o[w][j][d] + sm.mrg_mt[w][j][d / 32]) * sc;
+      }
+    }
+    const long long row = row0 + j;  // (seq * h_q + head)
+    const bool empty = !(Lt > 0.f);
+    part_o[(row * n_split + split) * D + d] = empty ? 0.f : o / Lt;
+    if (d == 0) part_lse[row * n_split + split] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+  }
+}
+
+template <int D, int G>
+__device__ inline void load_query(Smem<D, G>& sm, const uint16_t* q, long long row0) {
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int j = idx / D, d = idx % D;
+    sm.q[j][d / (D / 2)][d % (D / 2)] = bf16_bits_to_f32(q[(row0 + j) * D + d]);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * (D / 32); idx += kThreads) {
+    const int j = idx % G, bq = idx / G;
+    float s = 0.f;
+    for (int d = bq * 32; d < bq * 32 + 32; ++d) s += sm.q[j][d / (D / 2)][d % (D / 2)];
+    sm.qsum[bq][j] = s;
+  }
+  __syncthreads();
+}
+
+// ----------------------------------------- protected (INT8 side) split
+// Positions of the sink and recent windows (KV4-RL Sec. 5.2), read from the
+// INT8 side cache (App. A.3 "Protected path"): the k-th protected split covers
+// protected positions [k*prot_per_split, (k+1)*prot_per_split).  CUDA-core
+// fp32 math; lanes (t, half) as in the INT4 path for QK, lane-owned channels
+// for PV.
+template <int D, int G>
+__device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Layout& L,
+                                  const uint8_t* __restrict__ side, int b, int h,
+                                  const Regions& rg, int k, int prot_per_split, float scale_log2,
+                                  int warp, int lane) {
+  const int t = lane >> 1, half = lane & 1;
+  const int i_lo = k * prot_per_split;
+  const int i_hi = min(rg.n_prot, i_lo + prot_per_split);
+  const int NS = L.S + L.R;
+  const uint8_t* blk = side + ((long long)b * L.h_kv + h) * side_block_bytes(D, L.S, L.R);
+  const int8_t* k8 = reinterpret_cast<const int8_t*>(blk);
+  const int8_t* v8 = reinterpret_cast<const int8_t*>(blk + (long long)NS * D);
+  const uint16_t* ks = reinterpret_cast<const uint16_t*>(blk + 2LL * NS * D);
+  const uint16_t* vs = ks + NS;
+  for (int base = i_lo + warp * 16; base < i_hi; base += kWarps * 16) {
+    const int i = base + t;
+    const bool tok_ok = i < i_hi;
+    const int slot = tok_ok ? side_slot(prot_pos(rg, i), L.S, L.R) : 0;
+    float s[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) s[j] = 0.f;
+    if (tok_ok) {
+      const int8_t* row = k8 + (long long)slot * D + half * (D / 2);
+#pragma unroll
+      for (int w = 0; w < D / 8; ++w) {
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(row + 4 * w);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          const float c = (float)(int8_t)((word >> (8 * n)) & 0xFFu);
+#pragma unroll
+          for (int j = 0; j < G; ++j) s[j] = fmaf(sm.q[j][half][4 * w + n], c, s[j]);
+        }
+      }
+      const float sc = f16_bits_to_f32(ks[slot]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) s[j] *= sc;
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      s[j] += __shfl_xor_sync(0xffffffffu, s[j], 1);
+      s[j] = tok_ok ? s[j] * scale_log2 : -INFINITY;
+    }
+    softmax_tile<D, G>(ws, s, sm.p[warp], lane);
+    __syncwarp();
+    constexpr int PD = D / 32;
+    const int ntok = min(16, i_hi - base);
+    for (int tt = 0; tt < ntok; ++tt) {
+      const int slot2 = side_slot(prot_pos(rg, base + tt), L.S, L.R);
+      const float sc = f16_bits_to_f32(vs[slot2]);
+      uint32_t word;
+      if (PD == 4)
+        word = *reinterpret_cast<const uint32_t*>(v8 + (long long)slot2 * D + lane * PD);
+      else
+        word = *reinterpret_cast<const uint16_t*>(v8 + (long long)slot2 * D + lane * PD);
+      float v[PD];
+#pragma unroll
+      for (int ii = 0; ii < PD; ++ii) v[ii] = sc * (float)(int8_t)((word >> (8 * ii)) & 0xFFu);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float pj = sm.p[warp][tt][j];
+#pragma unroll
+        for (int ii = 0; ii < PD; ++ii) ws.acc[j][ii] = fmaf(pj, v[ii], ws.acc[j][ii]);
+      }
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace kv4

@@ -1,0 +1,435 @@
+// kv4_decode_mma.cu -- tensor-core variant of the INT4-region split of the
+// mixed-cache decode (KV4-RL Sec. 5.3, eq. 5.1; App. A.3) for head_dim 128
+// and 4 query heads per kv head (the Qwen3/Llama-3 layers the paper runs).
+//
+// The TMA staging, split plan, protected (INT8) split and merge are those of
+// the CUDA-core kernel.  What changes is the per-page math, which moves from
+// fp32 FMAs onto warp-level tensor-core MMAs (m16n8k16):
+//
+// QK^T, bf16 in, fp32 accumulate.  Rows of the 16-row A operand are the
+//   (group, head) pairs -- 4 groups x 4 heads at g = 32 -- and A holds each
+//   head's query restricted to that group's channels (block diagonal), so one
+//   accumulator row is the group-partial dot product  sum_{d in g} q_d (128+c_d).
+//   B is the page's 4-bit codes widened in registers to bf16 (128 + c is exact
+//   in bf16).  The score then follows eq. 5.1 per group:
+//     s = sum_g Delta_g * (D_g - 128*sum_g q) + m_g * sum_g q,
+//   so the codes enter the product exactly.  16 MMAs per 16-token page.
+//
+// PV, fp16 in, fp32 accumulate.  A is the page's V codes transposed
+//   (channels x tokens), fetched with ldmatrix.trans and widened to the exact
+//   centred values c - 8 in fp16; B is P' = p * Delta_v per group (rounded to
+//   fp16 once).  The offset term sum_t p_t (m_t + 8 Delta_t) is accumulated on
+//   the CUDA cores per group.  8 MMAs per page.
+//
+// The QK accumulator layout equals the PV operand layout for the tokens each
+// lane holds, so probabilities never leave registers.
+#include "kv4_decode_common.cuh"
+
+namespace kv4 {
+
+__device__ inline void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ inline void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ inline void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ inline uint32_t hfma2(uint32_t x, uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(a), "r"(b));
+  return d;
+}
+
+__device__ inline uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ inline uint32_t u4word(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// fp16 pairs: 1.0, -1032 (= -(1024 + 8)), 1/16, -72 (= -(64 + 8))
+constexpr uint32_t kOne2 = 0x3C003C00u, kM1032 = 0xE408E408u;
+constexpr uint32_t kSixteenth2 = 0x2C002C00u, kM72 = 0xD480D480u;
+
+// Widen 8 V codes (two tokens x four channels, nibbles 0-3 and 4-7 of w) to
+// fp16 pairs (token a, token b) of the centred value c - 8, channel +0..+3.
+__device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
+  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
+  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+  const uint32_t w8 = w >> 8;
+  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
+  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+}
+
+template <int NG>
+struct MetaRow;  // one slot's NG (Delta, m) words
+template <>
+struct MetaRow<4> {
+  uint4 v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ uint32_t get(int g) const { return u4word(v, g); }
+};
+template <>
+struct MetaRow<2> {
+  uint2 v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ uint32_t get(int g) const { return g == 0 ? v.x : v.y; }
+};
+template <>
+struct MetaRow<1> {
+  uint32_t v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ uint32_t get(int) const { return v; }
+};
+
+__device__ inline float lo_f(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
+__device__ inline float hi_f(uint32_t w) { return f16_bits_to_f32(w >> 16); }
+
+constexpr int D128 = 128, G4 = 4;
+
+template <int NG>
+__global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
+    Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
+    const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ block_table, float scale_log2, int n4, int pages_per_split,
+    int prot_per_split, float* __restrict__ part_o, float* __restrict__ part_lse,
+    int32_t* status) {
+  constexpr int D = D128, G = G4;
+  constexpr int GS = D / NG;  // channels per INT4 group
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
+  constexpr int cb = 16 * D + 128 * NG;
+  uint8_t* stage_base = smem_raw + ((sizeof(Smem<D, G>) + 127) / 128) * 128;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int n_split = gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row0 = (long long)b * L.h_q + (long long)h * G;
+
+  int len = seq_lens[b];
+  if (len < 0 || len > L.max_pages * kPage) {
+    if (threadIdx.x == 0 && split == 0 && h == 0) set_status(status, KV4_STATUS_BAD_LEN);
+    len = 0;
+  }
+  const Regions rg = regions(len, L.S, L.R);
+  load_query(sm, q, row0);
+
+  if (split >= n4) {
+    WarpState<D, G> ws;
+    ws.init();
+    prot_split<D, G>(sm, ws, L, side, b, h, rg, split - n4, prot_per_split, scale_log2, warp,
+                     lane);
+    write_state<D, G>(sm, ws, warp, lane);
+    merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+    return;
+  }
+
+  // ------------------------------------------------ per-lane constant setup
+  const int r = lane >> 2, qd = lane & 3;
+  const int j = r & 3;                        // this lane's softmax head
+  const int g0 = r >> 2, g1 = g0 + 2;         // groups of QK rows r and r+8
+  const bool v0 = g0 < NG, v1 = g1 < NG;
+  // Q operand: block-diagonal (group, head) rows, bf16.
+  uint32_t qa[8][4];
+  auto qbits = [&](int jj, int d) -> uint32_t {
+    return (uint32_t)f32_to_bf16_bits(sm.q[jj][d / (D / 2)][d % (D / 2)]);
+  };
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int base = 32 * qd + 8 * (s >> 1) + 2 * (s & 1);
+    uint32_t e[4][2];
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int dlo = base + 4 * e2;      // k = 2qd + e2
+      const int dhi = base + 1 + 4 * e2;  // k = 2qd + 8 + e2
+      e[0][e2] = (v0 && dlo / GS == g0) ? qbits(j, dlo) : 0u;
+      e[1][e2] = (v1 && dlo / GS == g1) ? qbits(j, dlo) : 0u;
+      e[2][e2] = (v0 && dhi / GS == g0) ? qbits(j, dhi) : 0u;
+      e[3][e2] = (v1 && dhi / GS == g1) ? qbits(j, dhi) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qa[s][k] = e[k][0] | (e[k][1] << 16);
+  }
+  float qs0 = 0.f, qs1 = 0.f;
+  for (int bq = 0; bq < D / 32; ++bq) {
+    if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][j];
+    if (v1 && (bq * 32) / GS == g1) qs1 += sm.qsum[bq][j];
+  }
+  const float qs0_128 = 128.f * qs0, qs1_128 = 128.f * qs1;
+
+  // ------------------------------------------------------ running state
+  float m_run = -INFINITY, l_run = 0.f;
+  constexpr int NGH = NG > 1 ? NG / 2 : 1;  // m-term groups per lane half
+  const int mt_g0 = (r >= 4) ? NG / 2 : 0;
+  const bool mt_on = (r < 4) || NG > 1;
+  float mt[NGH];
+#pragma unroll
+  for (int i = 0; i < NGH; ++i) mt[i] = 0.f;
+  float acc[4][2][4];
+#pragma unroll
+  for (int G_ = 0; G_ < 4; ++G_)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
+
+  // ------------------------------------------------------ page pipeline
+  const int first_page = rg.sink_end / kPage;
+  const int end_page = (rg.rec_start + kPage - 1) / kPage;
+  const int p_lo = first_page + split * pages_per_split;
+  const int p_hi = min(end_page, p_lo + pages_per_split);
+  const int n_my = rg.rec_start > rg.sink_end && p_hi > p_lo + warp
+                       ? (p_hi - p_lo - warp + kWarps - 1) / kWarps
+                       : 0;
+  uint8_t* my_stages = stage_base + (size_t)warp * kStages * cb;
+  const int32_t* bt_row = block_table + (long long)b * L.max_pages;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int i) {
+    const int pg = p_lo + warp + i * kWarps;
+    const int phys = bt_row[pg];
+    uint64_t* bar = &sm.bar[warp][i % kStages];
+    if (phys >= 0 && phys < L.num_pages) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, (uint32_t)cb);
+      bulk_g2s(my_stages + (size_t)(i % kStages) * cb,
+               paged + ((long long)phys * L.h_kv + h) * cb, (uint32_t)cb, bar);
+    } else {
+      set_status(status, KV4_STATUS_BAD_PAGE);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    }
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(kStages, n_my); ++i) issue(i);
+
+  // ldmatrix row addresses (relative to the V code block): matrix mi = lane/8
+  // holds tokens (mi&1)*8 + 0..7 of channel piece P = mi>>1 (+2 on the second
+  // load); pieces are XOR-swizzled by token pair.
+  const int lm_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int lm_p = lane >> 4;
+  const uint32_t lm_off0 = lm_tok * 64 + 16 * ((lm_p) ^ ((lm_tok >> 1) & 3));
+  const uint32_t lm_off1 = lm_tok * 64 + 16 * ((lm_p + 2) ^ ((lm_tok >> 1) & 3));
+  const int tk[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};  // this lane's tokens
+
+  for (int i = 0; i < n_my; ++i) {
+    const int pg = p_lo + warp + i * kWarps;
+    const int phys = bt_row[pg];
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStages], (i / kStages) & 1));
+    const bool valid = ok && phys >= 0 && phys < L.num_pages;
+    if (!ok && lane == 0) set_status(status, KV4_STATUS_BAD_PAGE);
+    const uint8_t* chunk = my_stages + (size_t)(i % kStages) * cb;
+    if (valid) {
+      // ---------------- QK^T on tensor cores
+      const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + 16 * qd);
+      const uint4 k1 = *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + 16 * qd);
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t w0 = u4word(k0, s >> 1), w1 = u4word(k1, s >> 1);
+        const int sh = 8 * (s & 1);
+        const uint32_t b00 = ((w0 >> sh) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t b01 = ((w0 >> (sh + 4)) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t b10 = ((w1 >> sh) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t b11 = ((w1 >> (sh + 4)) & 0x000F000Fu) | 0x43004300u;
+        mma_bf16(d0, qa[s], b00, b01);
+        mma_bf16(d1, qa[s], b10, b11);
+      }
+      // ---------------- scores (eq. 5.1 per group) for this lane's 4 tokens
+      const float draw0[4] = {d0[0], d0[1], d1[0], d1[1]};  // row r   (group g0)
+      const float draw1[4] = {d0[2], d0[3], d1[2], d1[3]};  // row r+8 (group g1)
+      float sc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        MetaRow<NG> km;
+        km.load(chunk + meta_off_k(D) + tk[e] * NG * 4);
+        float part = 0.f;
+        if (v0) {
+          const uint32_t mw = km.get(g0 < NG ? g0 : 0);
+          part = fmaf(lo_f(mw), draw0[e] - qs0_128, hi_f(mw) * qs0);
+        }
+        if (v1) {
+          const uint32_t mw = km.get(g1 < NG ? g1 : 0);
+          part += fmaf(lo_f(mw), draw1[e] - qs1_128, hi_f(mw) * qs1);
+        }
+        sc[e] = part;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 16);
+        const int pos = pg * kPage + tk[e];
+        sc[e] = (pos >= rg.sink_end && pos < rg.rec_start) ? sc[e] * scale_log2 : -INFINITY;
+      }
+      // ---------------- online softmax for head j over this page
+      float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float mnew = fmaxf(m_run, tmax);
+      float p[4], alpha;
+      if (mnew == -INFINITY) {
+        alpha = 1.f;
+        p[0] = p[1] = p[2] = p[3] = 0.f;
+      } else {
+        alpha = exp2f(m_run - mnew);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = exp2f(sc[e] - mnew);
+      }
+      if (__any_sync(0xffffffffu, mnew > m_run)) {
+        const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
+        const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
+#pragma unroll
+        for (int G_ = 0; G_ < 4; ++G_)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            acc[G_][hh][0] *= aA;
+            acc[G_][hh][1] *= aB;
+            acc[G_][hh][2] *= aA;
+            acc[G_][hh][3] *= aB;
+          }
+#pragma unroll
+        for (int gi = 0; gi < NGH; ++gi) mt[gi] *= alpha;
+        l_run *= alpha;
+      }
+      m_run = mnew;
+      l_run += (p[0] + p[1]) + (p[2] + p[3]);
+
+      // ---------------- PV on tensor cores
+      uint32_t va[4], vb[4];
+      const uint32_t vbase = smem_u32(chunk + codes_off_v(D));
+      ldsm_x4_trans(va, vbase + lm_off0);  // pieces 0,1: (tok lo, P0) (tok hi, P0) (lo, P1) (hi, P1)
+      ldsm_x4_trans(vb, vbase + lm_off1);  // pieces 2,3
+      MetaRow<NG> vm[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
+      // offset term: sum_t p_t (m_t + 8 Delta_t) per group
+      if (mt_on) {
+#pragma unroll
+        for (int gi = 0; gi < NGH; ++gi)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t w = vm[e].get(mt_g0 + gi < NG ? mt_g0 + gi : 0);
+            // masked slots (p = 0) may hold stale metadata: select, don't multiply
+            mt[gi] += p[e] > 0.f ? p[e] * fmaf(8.f, lo_f(w), hi_f(w)) : 0.f;
+          }
+      }
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int grp = (P * 32) / GS;
+        uint32_t b0 = 0u, b1 = 0u;
+        if (r < 4) {
+          float pp[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pp[e] = p[e] > 0.f ? p[e] * lo_f(vm[e].get(grp)) : 0.f;
+          b0 = pack_f16(pp[0], pp[1]);
+          b1 = pack_f16(pp[2], pp[3]);
+        }
+        const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
+        const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
+        uint32_t xl[4], xh[4];
+        widen_v(wlo, xl);
+        widen_v(whi, xh);
+        mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
+        mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+  }
+
+  // ------------------------------------------------ publish warp state
+  float lsum = (r < 4) ? l_run : 0.f;
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+#pragma unroll
+  for (int gi = 0; gi < NGH; ++gi) {
+    mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 1);
+    mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 2);
+  }
+  if (qd == 0 && r < 4) {
+    sm.mrg_m[warp][j] = m_run;
+    sm.mrg_l[warp][j] = lsum;
+  }
+  if (qd == 0 && mt_on) {
+#pragma unroll
+    for (int gi = 0; gi < NGH; ++gi) {
+      const int grp = mt_g0 + gi;
+      for (int blk = grp * (GS / 32); blk < (grp + 1) * (GS / 32); ++blk)
+        sm.mrg_mt[warp][j][blk] = mt[gi];
+    }
+  }
+  if (qd < 2) {
+    const int hA = 2 * qd, hB = 2 * qd + 1;
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int d = 32 * P + 4 * r + 2 * hh;
+        sm.mrg_o[warp][hA][d] = acc[P][hh][0];
+        sm.mrg_o[warp][hB][d] = acc[P][hh][1];
+        sm.mrg_o[warp][hA][d + 1] = acc[P][hh][2];
+        sm.mrg_o[warp][hB][d + 1] = acc[P][hh][3];
+      }
+  }
+  merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+}
+
+template <int NG>
+cudaError_t launch_mma_t(const Layout& L, const void* paged, const void* side, const uint16_t* q,
+                         const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
+                         float sm_scale, int n4, int pages_per_split, int n8, int prot_per_split,
+                         float* part_o, float* part_lse, int32_t* status, cudaStream_t st) {
+  constexpr int cb = 16 * D128 + 128 * NG;
+  const size_t smem = ((sizeof(Smem<D128, G4>) + 127) / 128) * 128 + (size_t)kWarps * kStages * cb;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<NG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n4 + n8, L.h_kv, num_seqs);
+  decode_mma_kernel<NG><<<grid, kThreads, smem, st>>>(
+      L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, block_table,
+      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, status);
+  return cudaGetLastError();
+}
+
+bool mma_supported(const Layout& L) { return L.d_h == 128 && L.h_q == 4 * L.h_kv; }
+
+cudaError_t launch_decode_mma(const Layout& L, const void* paged, const void* side,
+                              const uint16_t* q, const int32_t* seq_lens, int num_seqs,
+                              const int32_t* block_table, float sm_scale, int n4,
+                              int pages_per_split, int n8, int prot_per_split, float* part_o,
+                              float* part_lse, int32_t* status, cudaStream_t st) {
+  switch (L.d_h / L.g) {
+    case 4:
+      return launch_mma_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+    case 2:
+      return launch_mma_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+    case 1:
+      return launch_mma_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kv4
