@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from int8_kv_cache_kv4_gb300 import workloads as W  # noqa: E402
+from int8_kv_cache_kv4_gb300.cache import build_workload  # noqa: E402
 
 METRIC = "decode-attn resident KV tokens/s per layer and achieved HBM GB/s vs 8 TB/s"
 UNIT = "tokens/s"
@@ -117,45 +118,6 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workload
 
-def build_workload(w: W.Workload, dev, with_bf16=False, lens=None):
-    import torch
-    from int8_kv_cache_kv4_gb300.cache import MixedKVCache
-    lens = W.seq_lengths(w) if lens is None else lens
-    B = len(lens)
-    mpps = (int(lens.max()) + 15) // 16
-    num_pages = W.pool_pages(lens, w.extra_pages)
-    cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
-                         recent=w.recent, max_seqs=B, num_pages=num_pages,
-                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16)
-    cache.set_block_table(W.block_table(w.seed, lens, mpps, num_pages))
-    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
-    # populate positions [0, L-1) of every sequence (prefill-style bulk append)
-    for b, L in enumerate(lens):
-        n = int(L) - 1
-        if n <= 0:
-            continue
-        gen = W.torch_generator(w.seed * 1000003 + b, dev)
-        k, v = W.kv_torch(gen, w.h_kv, n, w.d_h, outl, dev)
-        seq = torch.full((n,), b, dtype=torch.int32, device=dev)
-        pos = torch.arange(n, dtype=torch.int32, device=dev)
-        lens_now = torch.as_tensor(np.maximum(lens - 1, 0).astype(np.int32), device=dev)
-        cache.append(k, v, seq, pos, lens_now)
-    # the step's new token (position L-1) and query
-    gen = W.torch_generator(w.seed * 1000003 + 999983, dev)
-    k_new, v_new = W.kv_torch(gen, w.h_kv, B, w.d_h, outl, dev)
-    q = torch.randn((B, w.h_q, w.d_h), generator=gen, device=dev).to(torch.bfloat16)
-    step = {
-        "k": k_new, "v": v_new, "q": q,
-        "seq": torch.arange(B, dtype=torch.int32, device=dev),
-        "pos": torch.as_tensor((lens - 1).astype(np.int32), device=dev),
-        "lens": torch.as_tensor(lens.astype(np.int32), device=dev),
-        "out": torch.empty((B, w.h_q, w.d_h), dtype=torch.bfloat16, device=dev),
-        "lse": torch.empty((B, w.h_q), dtype=torch.float32, device=dev),
-    }
-    torch.cuda.synchronize()
-    return cache, step, lens
-
-
 def run_step(cache, s, max_splits=0, ev=None):
     cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
     if ev is not None:
@@ -180,7 +142,7 @@ def run_kv4(args):
     kv4.load(build_if_missing=True)
 
     w = W.WORKLOADS[args.workload]
-    cache, s, lens = build_workload(w, dev, with_bf16=not args.no_bf16)
+    cache, s, lens, w = build_workload(w, dev, with_bf16=not args.no_bf16)
     dec_bytes, app_bytes, n4_tok, n8_tok = algorithmic_bytes(lens, w)
     tokens = int(lens.sum())
     stream = torch.cuda.current_stream()

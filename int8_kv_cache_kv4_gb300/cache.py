@@ -12,6 +12,7 @@ from typing import Optional
 import numpy as np
 
 from . import kv4
+from . import workloads as W
 
 
 class MixedKVCache:
@@ -75,3 +76,88 @@ class MixedKVCache:
 
     def clear_status(self):
         self.status.zero_()
+
+
+def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, seed=None,
+                   extra_tokens=0):
+    """Populate a cache with a seeded synthetic workload (see workloads.py):
+    positions [0, L-1) of every sequence by bulk appends, then return the
+    decode step's inputs (the new token at position L-1 and the query).
+    Sequence b's source K/V come from the generator seeded seed*1000003+b, the
+    step token and query from seed*1000003+999983, so any sequence can be
+    regenerated for a parity check.  `extra_tokens` reserves block-table room
+    for that many later appends per sequence."""
+    import torch
+    import dataclasses
+    if group is not None or recent is not None or seed is not None:
+        w = dataclasses.replace(w, group=w.group if group is None else group,
+                                recent=w.recent if recent is None else recent,
+                                seed=w.seed if seed is None else seed)
+    lens = W.seq_lengths(w) if lens is None else lens
+    B = len(lens)
+    cap = lens + int(extra_tokens)
+    mpps = (int(cap.max()) + 15) // 16
+    num_pages = W.pool_pages(cap, w.extra_pages)
+    cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
+                         recent=w.recent, max_seqs=B, num_pages=num_pages,
+                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16)
+    cache.set_block_table(W.block_table(w.seed, cap, mpps, num_pages))
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    # populate positions [0, L-1) of every sequence (prefill-style bulk append)
+    for b, L in enumerate(lens):
+        n = int(L) - 1
+        if n <= 0:
+            continue
+        gen = W.torch_generator(w.seed * 1000003 + b, dev)
+        k, v = W.kv_torch(gen, w.h_kv, n, w.d_h, outl, dev)
+        seq = torch.full((n,), b, dtype=torch.int32, device=dev)
+        pos = torch.arange(n, dtype=torch.int32, device=dev)
+        lens_now = torch.as_tensor(np.maximum(lens - 1, 0).astype(np.int32), device=dev)
+        cache.append(k, v, seq, pos, lens_now)
+    # the step's new token (position L-1) and query
+    k_new, v_new, q = step_inputs(w, B, 0, dev)
+    step = {
+        "k": k_new, "v": v_new, "q": q,
+        "seq": torch.arange(B, dtype=torch.int32, device=dev),
+        "pos": torch.as_tensor((lens - 1).astype(np.int32), device=dev),
+        "lens": torch.as_tensor(lens.astype(np.int32), device=dev),
+        "out": torch.empty((B, w.h_q, w.d_h), dtype=torch.bfloat16, device=dev),
+        "lse": torch.empty((B, w.h_q), dtype=torch.float32, device=dev),
+    }
+    torch.cuda.synchronize()
+    return cache, step, lens, w
+
+
+def step_inputs(w, B, step, dev):
+    """New K/V token of every sequence and the query for rollout step `step`
+    (step 0 is the token build_workload returns)."""
+    import torch
+    gen = W.torch_generator(w.seed * 1000003 + 999983 + 7919 * step, dev)
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    k_new, v_new = W.kv_torch(gen, w.h_kv, B, w.d_h, outl, dev)
+    q = torch.randn((B, w.h_q, w.d_h), generator=gen, device=dev).to(torch.bfloat16)
+    return k_new, v_new, q
+
+
+def source_kv(w, b, L0, dev, steps=1):
+    """Regenerate the source K/V of sequence b (bf16 bits, numpy
+    [h_kv][L0 - 1 + steps][d_h]): the populated prefix [0, L0 - 1) and one
+    token per rollout step."""
+    import torch
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    parts_k, parts_v = [], []
+    n = int(L0) - 1
+    if n > 0:
+        gen = W.torch_generator(w.seed * 1000003 + b, dev)
+        k, v = W.kv_torch(gen, w.h_kv, n, w.d_h, outl, dev)
+        parts_k.append(k)
+        parts_v.append(v)
+    B = None
+    for s in range(steps):
+        kk, vv, _ = step_inputs(w, w.batch, s, dev)
+        parts_k.append(kk[b:b + 1])
+        parts_v.append(vv[b:b + 1])
+    k = torch.cat(parts_k).transpose(0, 1).contiguous()
+    v = torch.cat(parts_v).transpose(0, 1).contiguous()
+    return (k.view(torch.int16).cpu().numpy().view(np.uint16),
+            v.view(torch.int16).cpu().numpy().view(np.uint16))

@@ -14,16 +14,17 @@ cudaError_t launch_bf16_append(const Layout&, void*, const uint16_t*, const uint
                                int32_t*, cudaStream_t);
 cudaError_t launch_decode(const Layout&, const void*, const void*, const uint16_t*, const int32_t*,
                           int, const int32_t*, float, int, int, int, int, float*, float*, int32_t*,
-                          cudaStream_t);
+                          uint16_t*, float*, int32_t*, cudaStream_t);
 cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, const int32_t*, int,
                                const int32_t*, float, int, int, float*, float*, int32_t*,
-                               cudaStream_t);
+                               uint16_t*, float*, int32_t*, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
                            cudaStream_t);
 bool mma_supported(const Layout&);
 cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uint16_t*,
                               const int32_t*, int, const int32_t*, float, int, int, int, int,
-                              float*, float*, int32_t*, cudaStream_t);
+                              float*, float*, int32_t*, uint16_t*, float*, int32_t*,
+                              cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -73,12 +74,30 @@ static Layout to_layout(const kv4_layout* l) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p) {
+// Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
+// [rows][n_split], and one int32 completion ticket per (sequence, kv head).
+struct Workspace {
+  float* part_o;
+  float* part_lse;
+  int32_t* tickets;
+  size_t ticket_bytes;
+  size_t bytes;
+};
+static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, void* base) {
   const size_t rows = (size_t)num_seqs * l->num_q_heads;
-  size_t o = rows * p.total() * l->head_dim * sizeof(float);
-  o = (o + 255) / 256 * 256;
-  size_t z = rows * p.total() * sizeof(float);
-  return o + (z + 255) / 256 * 256;
+  const size_t o = round256(rows * p.total() * l->head_dim * sizeof(float));
+  const size_t z = round256(rows * p.total() * sizeof(float));
+  Workspace w;
+  w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
+  w.bytes = o + z + round256(w.ticket_bytes);
+  w.part_o = (float*)base;
+  w.part_lse = (float*)((char*)base + o);
+  w.tickets = (int32_t*)((char*)base + o + z);
+  return w;
+}
+static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p) {
+  return ws_layout(l, num_seqs, p, nullptr).bytes;
 }
 
 }  // namespace kv4
@@ -179,24 +198,22 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
     return KV4_ERR_INVALID_ARG;
   const Plan p = make_plan(l, num_seqs, max_splits, true);
   if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
-  const size_t rows = (size_t)num_seqs * l->num_q_heads;
-  float* part_o = (float*)workspace;
-  size_t o_bytes = (rows * p.total() * l->head_dim * sizeof(float) + 255) / 256 * 256;
-  float* part_lse = (float*)((char*)workspace + o_bytes);
+  const Workspace w = ws_layout(l, num_seqs, p, workspace);
   cudaStream_t st = (cudaStream_t)stream;
   const Layout L = to_layout(l);
+  // Completion tickets for the fused eq. A1 merge start at zero on every call.
+  if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
   // head_dim 128 with 4 query heads per kv head runs the tensor-core kernel;
-  // other shapes the CUDA-core kernel.
+  // other shapes the CUDA-core kernel.  Both merge their splits in the
+  // last-finishing CTA of each (sequence, kv head).
   cudaError_t e =
       mma_supported(L)
           ? launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
-                              p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse,
-                              dev_status, st)
+                              p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
+                              w.tickets, out, out_lse, dev_status, st)
           : launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
-                          p.pages_per_split, p.n8, p.prot_per_split, part_o, part_lse, dev_status,
-                          st);
-  if (e != cudaSuccess) return KV4_ERR_LAUNCH;
-  e = launch_combine(part_o, part_lse, (int)rows, p.total(), l->head_dim, out, out_lse, st);
+                          p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
+                          w.tickets, out, out_lse, dev_status, st);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 
@@ -239,16 +256,12 @@ int kv4_bf16_decode_attn(const kv4_layout* l, const void* cache, const uint16_t*
   if (!aligned16(cache) || !aligned16(q) || !aligned16(workspace)) return KV4_ERR_INVALID_ARG;
   const Plan p = make_plan(l, num_seqs, max_splits, false);
   if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
-  const size_t rows = (size_t)num_seqs * l->num_q_heads;
-  float* part_o = (float*)workspace;
-  size_t o_bytes = (rows * p.total() * l->head_dim * sizeof(float) + 255) / 256 * 256;
-  float* part_lse = (float*)((char*)workspace + o_bytes);
+  const Workspace w = ws_layout(l, num_seqs, p, workspace);
   cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
   cudaError_t e = launch_bf16_decode(to_layout(l), cache, q, seq_lens, num_seqs, block_table,
-                                     sm_scale, p.n4, p.pages_per_split, part_o, part_lse,
-                                     dev_status, st);
-  if (e != cudaSuccess) return KV4_ERR_LAUNCH;
-  e = launch_combine(part_o, part_lse, (int)rows, p.total(), l->head_dim, out, out_lse, st);
+                                     sm_scale, p.n4, p.pages_per_split, w.part_o, w.part_lse,
+                                     w.tickets, out, out_lse, dev_status, st);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 

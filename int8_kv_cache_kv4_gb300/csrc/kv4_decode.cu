@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ block_table, float scale_log2, int n4, int pages_per_split,
     int prot_per_split, float* __restrict__ part_o, float* __restrict__ part_lse,
+    int32_t* __restrict__ tickets, uint16_t* __restrict__ out, float* __restrict__ out_lse,
     int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
@@ -117,6 +118,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
   }
   write_state<D, G>(sm, ws, warp, lane);
   merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+  combine_if_last<D, G>(sm, tickets, b * L.h_kv + h, part_o, part_lse, row0, n_split, out,
+                        out_lse);
 }
 
 // ------------------------------------------------- bf16 comparator kernel
@@ -125,7 +128,8 @@ __global__ void __launch_bounds__(kThreads) bf16_decode_split_kernel(
     Layout L, const uint16_t* __restrict__ cache, const uint16_t* __restrict__ q,
     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
     float scale_log2, int pages_per_split, float* __restrict__ part_o,
-    float* __restrict__ part_lse, int32_t* status) {
+    float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
+    float* __restrict__ out_lse, int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
   constexpr int cb = 2 * kPage * D * 2;
@@ -231,6 +235,8 @@ __global__ void __launch_bounds__(kThreads) bf16_decode_split_kernel(
   }
   write_state<D, G>(sm, ws, warp, lane);
   merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+  combine_if_last<D, G>(sm, tickets, b * L.h_kv + h, part_o, part_lse, row0, n_split, out,
+                        out_lse);
 }
 
 // ------------------------------------------------------------ combine kernel
@@ -281,7 +287,8 @@ cudaError_t launch_decode_t(const Layout& L, const void* paged, const void* side
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                             const int32_t* block_table, float sm_scale, int n4,
                             int pages_per_split, int n8, int prot_per_split, float* part_o,
-                            float* part_lse, int32_t* status, cudaStream_t st) {
+                            float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
+                            int32_t* status, cudaStream_t st) {
   const size_t smem = decode_smem_bytes<D, G>(chunk_bytes(D, L.g));
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -289,7 +296,8 @@ cudaError_t launch_decode_t(const Layout& L, const void* paged, const void* side
   dim3 grid(n4 + n8, L.h_kv, num_seqs);
   decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, block_table,
-      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, status);
+      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, tickets, out,
+      out_lse, status);
   return cudaGetLastError();
 }
 
@@ -298,6 +306,7 @@ cudaError_t launch_bf16_decode_t(const Layout& L, const void* cache, const uint1
                                  const int32_t* seq_lens, int num_seqs,
                                  const int32_t* block_table, float sm_scale, int n_split,
                                  int pages_per_split, float* part_o, float* part_lse,
+                                 int32_t* tickets, uint16_t* out, float* out_lse,
                                  int32_t* status, cudaStream_t st) {
   const size_t smem = decode_smem_bytes<D, G>(2 * kPage * D * 2);
   cudaError_t e = cudaFuncSetAttribute(bf16_decode_split_kernel<D, G>,
@@ -306,7 +315,7 @@ cudaError_t launch_bf16_decode_t(const Layout& L, const void* cache, const uint1
   dim3 grid(n_split, L.h_kv, num_seqs);
   bf16_decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(
       L, (const uint16_t*)cache, q, seq_lens, block_table, sm_scale * kLog2e, pages_per_split,
-      part_o, part_lse, status);
+      part_o, part_lse, tickets, out, out_lse, status);
   return cudaGetLastError();
 }
 
@@ -333,21 +342,23 @@ cudaError_t launch_bf16_decode_t(const Layout& L, const void* cache, const uint1
 cudaError_t launch_decode(const Layout& L, const void* paged, const void* side, const uint16_t* q,
                           const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
                           float sm_scale, int n4, int pages_per_split, int n8, int prot_per_split,
-                          float* part_o, float* part_lse, int32_t* status, cudaStream_t st) {
+                          float* part_o, float* part_lse, int32_t* tickets, uint16_t* out,
+                          float* out_lse, int32_t* status, cudaStream_t st) {
   KV4_DISPATCH_DG(L.d_h, L.h_q / L.h_kv,
                   (launch_decode_t<D, G>(L, paged, side, q, seq_lens, num_seqs, block_table,
                                          sm_scale, n4, pages_per_split, n8, prot_per_split,
-                                         part_o, part_lse, status, st)));
+                                         part_o, part_lse, tickets, out, out_lse, status, st)));
 }
 
 cudaError_t launch_bf16_decode(const Layout& L, const void* cache, const uint16_t* q,
                                const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
                                float sm_scale, int n_split, int pages_per_split, float* part_o,
-                               float* part_lse, int32_t* status, cudaStream_t st) {
+                               float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
+                               int32_t* status, cudaStream_t st) {
   KV4_DISPATCH_DG(L.d_h, L.h_q / L.h_kv,
                   (launch_bf16_decode_t<D, G>(L, cache, q, seq_lens, num_seqs, block_table,
                                               sm_scale, n_split, pages_per_split, part_o,
-                                              part_lse, status, st)));
+                                              part_lse, tickets, out, out_lse, status, st)));
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, int rows, int n, int d_h,

@@ -25,8 +25,14 @@ struct Smem {
   float p[kWarps][16][G];        // probabilities of the current tile, per warp
   float mrg_m[kWarps][G];
   float mrg_l[kWarps][G];
-  float mrg_o[kWarps][G][D];
+  union {
+    float mrg_o[kWarps][G][D];      // per-warp unnormalised outputs (end of a split)
+    uint32_t qfrag[8][32][4];       // tensor-core query fragments (start of a split)
+  };
   float mrg_mt[kWarps][G][D / 32];  // additive term per 32-channel block (tensor-core path)
+  uint16_t qh[G][D];                // query as fp16 bits
+  int32_t phys[kWarps][kStages];    // physical page of each in-flight stage
+  int32_t ticket;
   uint64_t bar[kWarps][kStages];
 };
 
@@ -198,11 +204,58 @@ __device__ inline void merge_store(Smem<D, G>& sm, float* part_o, float* part_ls
   }
 }
 
+// Eq. A1 over the n_split partials of `G` consecutive rows, done by the last
+// CTA of a (sequence, kv head) to finish (an atomic ticket per pair; the
+// partials of the other CTAs are made visible by their __threadfence()).
+template <int D, int G>
+__device__ inline void combine_if_last(Smem<D, G>& sm, int32_t* tickets, int pair,
+                                       const float* part_o, const float* part_lse,
+                                       long long row0, int n_split, uint16_t* out,
+                                       float* out_lse) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sm.ticket = atomicAdd(&tickets[pair], 1);
+  __syncthreads();
+  if (sm.ticket != n_split - 1) return;
+  __threadfence();
+  constexpr int PD = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = warp; j < G; j += kWarps) {
+    const long long row = row0 + j;
+    const float* lse = part_lse + row * n_split;
+    float M = -INFINITY;
+    for (int r = lane; r < n_split; r += 32) M = fmaxf(M, __ldcg(lse + r));
+    M = warp_max(M);
+    float acc[PD];
+#pragma unroll
+    for (int i = 0; i < PD; ++i) acc[i] = 0.f;
+    float Z = 0.f;
+    if (M != -INFINITY) {
+      for (int r = 0; r < n_split; ++r) {
+        const float z = __ldcg(lse + r);
+        if (z == -INFINITY) continue;
+        const float w = exp2f((z - M) * kLog2e);
+        Z += w;
+        const float* o = part_o + (row * n_split + r) * D + lane * PD;
+#pragma unroll
+        for (int i = 0; i < PD; ++i) acc[i] = fmaf(w, __ldcg(o + i), acc[i]);
+      }
+    }
+    const bool empty = !(Z > 0.f);
+#pragma unroll
+    for (int i = 0; i < PD; ++i)
+      out[row * D + lane * PD + i] = f32_to_bf16_bits(empty ? 0.f : acc[i] / Z);
+    if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
+  }
+}
+
 template <int D, int G>
 __device__ inline void load_query(Smem<D, G>& sm, const uint16_t* q, long long row0) {
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
     const int j = idx / D, d = idx % D;
-    sm.q[j][d / (D / 2)][d % (D / 2)] = bf16_bits_to_f32(q[(row0 + j) * D + d]);
+    const float x = bf16_bits_to_f32(q[(row0 + j) * D + d]);
+    sm.qh[j][d] = __half_as_ushort(__float2half_rn(x));
+    sm.q[j][d / (D / 2)][d % (D / 2)] = x;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * (D / 32); idx += kThreads) {

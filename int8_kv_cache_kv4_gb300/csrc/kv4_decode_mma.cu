@@ -6,14 +6,15 @@
 // the CUDA-core kernel.  What changes is the per-page math, which moves from
 // fp32 FMAs onto warp-level tensor-core MMAs (m16n8k16):
 //
-// QK^T, bf16 in, fp32 accumulate.  Rows of the 16-row A operand are the
+// QK^T, fp16 in, fp32 accumulate.  Rows of the 16-row A operand are the
 //   (group, head) pairs -- 4 groups x 4 heads at g = 32 -- and A holds each
 //   head's query restricted to that group's channels (block diagonal), so one
-//   accumulator row is the group-partial dot product  sum_{d in g} q_d (128+c_d).
-//   B is the page's 4-bit codes widened in registers to bf16 (128 + c is exact
-//   in bf16).  The score then follows eq. 5.1 per group:
-//     s = sum_g Delta_g * (D_g - 128*sum_g q) + m_g * sum_g q,
-//   so the codes enter the product exactly.  16 MMAs per 16-token page.
+//   accumulator row is the group-partial dot product  D_g = sum_{d in g} q_d c_d.
+//   B is the page's 4-bit codes widened in registers to exact fp16 integers
+//   (magic-number OR, then one fp16 fma per pair).  The score then follows
+//   eq. 5.1 per group:  s = sum_g Delta_g * D_g + m_g * sum_{d in g} q_d,
+//   so the codes enter the product exactly.  16 MMAs per 16-token page.  The
+//   bf16 query converts to fp16 without loss (|q| within fp16's normal range).
 //
 // PV, fp16 in, fp32 accumulate.  A is the page's V codes transposed
 //   (channels x tokens), fetched with ldmatrix.trans and widened to the exact
@@ -26,14 +27,6 @@
 #include "kv4_decode_common.cuh"
 
 namespace kv4 {
-
-__device__ inline void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __device__ inline void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                uint32_t b0, uint32_t b1) {
@@ -54,6 +47,25 @@ __device__ inline uint32_t hfma2(uint32_t x, uint32_t a, uint32_t b) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(a), "r"(b));
   return d;
+}
+
+__device__ inline float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ inline uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// (low half of a, low half of b)
+__device__ inline uint32_t lo_lo(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
+
+__device__ inline float2 h2f2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 __device__ inline uint32_t pack_f16(float lo, float hi) {
@@ -79,6 +91,19 @@ __device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
   x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
 }
 
+// fp16 pairs -1024 and -64
+constexpr uint32_t kM1024 = 0xE400E400u, kM64 = 0xD400D400u;
+
+// Widen one K code word (8 channels of one token) to 4 fp16 pairs of exact
+// codes: pair i = (channel i, channel i + 4).
+__device__ inline void widen_k(uint32_t w, uint32_t x[4]) {
+  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
+  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+  const uint32_t w8 = w >> 8;
+  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
+  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+}
+
 template <int NG>
 struct MetaRow;  // one slot's NG (Delta, m) words
 template <>
@@ -86,18 +111,21 @@ struct MetaRow<4> {
   uint4 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint4*>(p); }
   __device__ uint32_t get(int g) const { return u4word(v, g); }
+  __device__ void zero() { v = make_uint4(0u, 0u, 0u, 0u); }
 };
 template <>
 struct MetaRow<2> {
   uint2 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint2*>(p); }
   __device__ uint32_t get(int g) const { return g == 0 ? v.x : v.y; }
+  __device__ void zero() { v = make_uint2(0u, 0u); }
 };
 template <>
 struct MetaRow<1> {
   uint32_t v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
   __device__ uint32_t get(int) const { return v; }
+  __device__ void zero() { v = 0u; }
 };
 
 __device__ inline float lo_f(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
@@ -111,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ block_table, float scale_log2, int n4, int pages_per_split,
     int prot_per_split, float* __restrict__ part_o, float* __restrict__ part_lse,
+    int32_t* __restrict__ tickets, uint16_t* __restrict__ out, float* __restrict__ out_lse,
     int32_t* status) {
   constexpr int D = D128, G = G4;
   constexpr int GS = D / NG;  // channels per INT4 group
@@ -139,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
                      lane);
     write_state<D, G>(sm, ws, warp, lane);
     merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+    combine_if_last<D, G>(sm, tickets, b * L.h_kv + h, part_o, part_lse, row0, n_split, out,
+                          out_lse);
     return;
   }
 
@@ -147,42 +178,49 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   const int j = r & 3;                        // this lane's softmax head
   const int g0 = r >> 2, g1 = g0 + 2;         // groups of QK rows r and r+8
   const bool v0 = g0 < NG, v1 = g1 < NG;
-  // Q operand: block-diagonal (group, head) rows, bf16.
+  // Q operand fragments: block-diagonal (group, head) rows, fp16.  Identical
+  // for the CTA's four warps, so built once into shared memory.
+  for (int idx = threadIdx.x; idx < 8 * 32 * 4; idx += kThreads) {
+    const int s = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
+    const int rr = ln >> 2, qq = ln & 3;
+    const int row = rr + 8 * (k & 1);              // A rows r (k = 0, 2) and r + 8 (k = 1, 3)
+    const int grp = row >> 2, jj = row & 3;
+    const int base = 32 * qq + 8 * (s >> 1) + 2 * (s & 1) + ((k & 2) ? 1 : 0);
+    uint32_t w = 0u;
+    if (grp < NG) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int d = base + 4 * e2;               // k-index 2qd+e2 (k<2) or 2qd+8+e2 (k>=2)
+        if (d / GS == grp) w |= (uint32_t)sm.qh[jj][d] << (16 * e2);
+      }
+    }
+    sm.qfrag[s][ln][k] = w;
+  }
+  __syncthreads();
   uint32_t qa[8][4];
-  auto qbits = [&](int jj, int d) -> uint32_t {
-    return (uint32_t)f32_to_bf16_bits(sm.q[jj][d / (D / 2)][d % (D / 2)]);
-  };
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const int base = 32 * qd + 8 * (s >> 1) + 2 * (s & 1);
-    uint32_t e[4][2];
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      const int dlo = base + 4 * e2;      // k = 2qd + e2
-      const int dhi = base + 1 + 4 * e2;  // k = 2qd + 8 + e2
-      e[0][e2] = (v0 && dlo / GS == g0) ? qbits(j, dlo) : 0u;
-      e[1][e2] = (v1 && dlo / GS == g1) ? qbits(j, dlo) : 0u;
-      e[2][e2] = (v0 && dhi / GS == g0) ? qbits(j, dhi) : 0u;
-      e[3][e2] = (v1 && dhi / GS == g1) ? qbits(j, dhi) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) qa[s][k] = e[k][0] | (e[k][1] << 16);
+    const uint4 v = *reinterpret_cast<const uint4*>(&sm.qfrag[s][lane][0]);
+    qa[s][0] = v.x;
+    qa[s][1] = v.y;
+    qa[s][2] = v.z;
+    qa[s][3] = v.w;
   }
+  __syncthreads();  // qfrag aliases the merge buffers
   float qs0 = 0.f, qs1 = 0.f;
   for (int bq = 0; bq < D / 32; ++bq) {
     if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][j];
     if (v1 && (bq * 32) / GS == g1) qs1 += sm.qsum[bq][j];
   }
-  const float qs0_128 = 128.f * qs0, qs1_128 = 128.f * qs1;
 
   // ------------------------------------------------------ running state
   float m_run = -INFINITY, l_run = 0.f;
   constexpr int NGH = NG > 1 ? NG / 2 : 1;  // m-term groups per lane half
   const int mt_g0 = (r >= 4) ? NG / 2 : 0;
   const bool mt_on = (r < 4) || NG > 1;
-  float mt[NGH];
+  float mt_m[NGH], mt_d[NGH];  // sum_t p_t m_t and sum_t p_t Delta_t per handled group
 #pragma unroll
-  for (int i = 0; i < NGH; ++i) mt[i] = 0.f;
+  for (int i = 0; i < NGH; ++i) mt_m[i] = mt_d[i] = 0.f;
   float acc[4][2][4];
 #pragma unroll
   for (int G_ = 0; G_ < 4; ++G_)
@@ -206,11 +244,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
     fence_mbar_init();
   }
   __syncwarp();
-  auto issue = [&](int i) {
-    const int pg = p_lo + warp + i * kWarps;
-    const int phys = bt_row[pg];
+  // Lane 0 issues the bulk copies; the block-table entry of each page is
+  // read one iteration before its copy is issued, so the issue never waits
+  // on global-memory latency.
+  auto issue = [&](int i, int phys) {
     uint64_t* bar = &sm.bar[warp][i % kStages];
-    if (phys >= 0 && phys < L.num_pages) {
+    const bool good = phys >= 0 && phys < L.num_pages;
+    sm.phys[warp][i % kStages] = good ? phys : -1;  // published by the arrive below
+    if (good) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, (uint32_t)cb);
       bulk_g2s(my_stages + (size_t)(i % kStages) * cb,
@@ -220,8 +261,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
     }
   };
-  if (lane == 0)
-    for (int i = 0; i < min(kStages, n_my); ++i) issue(i);
+  int next_phys = -1;  // lane 0: block-table entry of page i + kStages
+  if (lane == 0) {
+    for (int i = 0; i < min(kStages, n_my); ++i) issue(i, bt_row[p_lo + warp + i * kWarps]);
+    if (kStages < n_my) next_phys = bt_row[p_lo + warp + kStages * kWarps];
+  }
 
   // ldmatrix row addresses (relative to the V code block): matrix mi = lane/8
   // holds tokens (mi&1)*8 + 0..7 of channel piece P = mi>>1 (+2 on the second
@@ -232,70 +276,77 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   const uint32_t lm_off1 = lm_tok * 64 + 16 * ((lm_p + 2) ^ ((lm_tok >> 1) & 3));
   const int tk[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};  // this lane's tokens
 
+  const uint32_t p_keep = (r < 4) ? 0xFFFFFFFFu : 0u;  // lanes r >= 4 feed zero PV columns
   for (int i = 0; i < n_my; ++i) {
     const int pg = p_lo + warp + i * kWarps;
-    const int phys = bt_row[pg];
     const bool ok =
         __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStages], (i / kStages) & 1));
-    const bool valid = ok && phys >= 0 && phys < L.num_pages;
+    const bool valid = ok && sm.phys[warp][i % kStages] >= 0;
     if (!ok && lane == 0) set_status(status, KV4_STATUS_BAD_PAGE);
     const uint8_t* chunk = my_stages + (size_t)(i % kStages) * cb;
     if (valid) {
+      // slots at or beyond the sequence length were never written: their
+      // metadata may be any bit pattern, so it is zeroed before use
+      const bool tail = (pg + 1) * kPage > len;
       // ---------------- QK^T on tensor cores
       const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + 16 * qd);
       const uint4 k1 = *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + 16 * qd);
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t w0 = u4word(k0, s >> 1), w1 = u4word(k1, s >> 1);
-        const int sh = 8 * (s & 1);
-        const uint32_t b00 = ((w0 >> sh) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t b01 = ((w0 >> (sh + 4)) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t b10 = ((w1 >> sh) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t b11 = ((w1 >> (sh + 4)) & 0x000F000Fu) | 0x43004300u;
-        mma_bf16(d0, qa[s], b00, b01);
-        mma_bf16(d1, qa[s], b10, b11);
+      for (int u = 0; u < 4; ++u) {
+        uint32_t x0[4], x1[4];
+        widen_k(u4word(k0, u), x0);
+        widen_k(u4word(k1, u), x1);
+        // k-steps 2u and 2u+1 use pairs (0,1) and (2,3) of word u
+        mma_f16(d0, qa[2 * u][0], qa[2 * u][1], qa[2 * u][2], qa[2 * u][3], x0[0], x0[1]);
+        mma_f16(d1, qa[2 * u][0], qa[2 * u][1], qa[2 * u][2], qa[2 * u][3], x1[0], x1[1]);
+        mma_f16(d0, qa[2 * u + 1][0], qa[2 * u + 1][1], qa[2 * u + 1][2], qa[2 * u + 1][3], x0[2],
+                x0[3]);
+        mma_f16(d1, qa[2 * u + 1][0], qa[2 * u + 1][1], qa[2 * u + 1][2], qa[2 * u + 1][3], x1[2],
+                x1[3]);
       }
       // ---------------- scores (eq. 5.1 per group) for this lane's 4 tokens
       const float draw0[4] = {d0[0], d0[1], d1[0], d1[1]};  // row r   (group g0)
       const float draw1[4] = {d0[2], d0[3], d1[2], d1[3]};  // row r+8 (group g1)
+      const uint8_t* kmeta = chunk + meta_off_k(D);
       float sc[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        MetaRow<NG> km;
-        km.load(chunk + meta_off_k(D) + tk[e] * NG * 4);
         float part = 0.f;
         if (v0) {
-          const uint32_t mw = km.get(g0 < NG ? g0 : 0);
-          part = fmaf(lo_f(mw), draw0[e] - qs0_128, hi_f(mw) * qs0);
+          const float2 dm = h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g0) * 4));
+          part = fmaf(dm.x, draw0[e], dm.y * qs0);
         }
         if (v1) {
-          const uint32_t mw = km.get(g1 < NG ? g1 : 0);
-          part += fmaf(lo_f(mw), draw1[e] - qs1_128, hi_f(mw) * qs1);
+          const float2 dm = h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g1) * 4));
+          part += fmaf(dm.x, draw1[e], dm.y * qs1);
         }
         sc[e] = part;
       }
+      const bool interior = pg * kPage >= rg.sink_end && (pg + 1) * kPage <= rg.rec_start;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 16);
-        const int pos = pg * kPage + tk[e];
-        sc[e] = (pos >= rg.sink_end && pos < rg.rec_start) ? sc[e] * scale_log2 : -INFINITY;
+        sc[e] *= scale_log2;
+      }
+      if (!interior) {  // first / last page of the region: mask positions outside it
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pos = pg * kPage + tk[e];
+          if (!(pos >= rg.sink_end && pos < rg.rec_start)) sc[e] = -INFINITY;
+        }
       }
       // ---------------- online softmax for head j over this page
       float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
       const float mnew = fmaxf(m_run, tmax);
-      float p[4], alpha;
-      if (mnew == -INFINITY) {
-        alpha = 1.f;
-        p[0] = p[1] = p[2] = p[3] = 0.f;
-      } else {
-        alpha = exp2f(m_run - mnew);
+      const float mref = mnew == -INFINITY ? 0.f : mnew;
+      float p[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p[e] = exp2f(sc[e] - mnew);
-      }
+      for (int e = 0; e < 4; ++e) p[e] = ex2(sc[e] - mref);  // masked: ex2(-inf) = 0
       if (__any_sync(0xffffffffu, mnew > m_run)) {
+        const float alpha = ex2(m_run - mref);
         const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
         const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
 #pragma unroll
@@ -308,10 +359,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
             acc[G_][hh][3] *= aB;
           }
 #pragma unroll
-        for (int gi = 0; gi < NGH; ++gi) mt[gi] *= alpha;
+        for (int gi = 0; gi < NGH; ++gi) {
+          mt_m[gi] *= alpha;
+          mt_d[gi] *= alpha;
+        }
         l_run *= alpha;
+        m_run = mnew;
       }
-      m_run = mnew;
       l_run += (p[0] + p[1]) + (p[2] + p[3]);
 
       // ---------------- PV on tensor cores
@@ -322,28 +376,41 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       MetaRow<NG> vm[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
-      // offset term: sum_t p_t (m_t + 8 Delta_t) per group
+      if (tail) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (pg * kPage + tk[e] >= len) vm[e].zero();
+      }
+      // offset term: sum_t p_t (m_t + 8 Delta_t) per group, fp32; this lane
+      // handles groups [mt_g0, mt_g0 + NGH)
       if (mt_on) {
 #pragma unroll
-        for (int gi = 0; gi < NGH; ++gi)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t w = vm[e].get(mt_g0 + gi < NG ? mt_g0 + gi : 0);
-            // masked slots (p = 0) may hold stale metadata: select, don't multiply
-            mt[gi] += p[e] > 0.f ? p[e] * fmaf(8.f, lo_f(w), hi_f(w)) : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
+          uint32_t w[NGH];
+          if (NGH == 2) {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(row);
+            w[0] = v2.x;
+            w[NGH - 1] = v2.y;
+          } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(row);
           }
+#pragma unroll
+          for (int gi = 0; gi < NGH; ++gi) {
+            const float2 dm = h2f2(tail && pg * kPage + tk[e] >= len ? 0u : w[gi]);
+            mt_d[gi] = fmaf(p[e], dm.x, mt_d[gi]);
+            mt_m[gi] = fmaf(p[e], dm.y, mt_m[gi]);
+          }
+        }
       }
+      // P' = p * Delta_v per group, formed in fp16x2 (token pairs)
+      const uint32_t p01 = pack_f16(p[0], p[1]) & p_keep;
+      const uint32_t p23 = pack_f16(p[2], p[3]) & p_keep;
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
         const int grp = (P * 32) / GS;
-        uint32_t b0 = 0u, b1 = 0u;
-        if (r < 4) {
-          float pp[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pp[e] = p[e] > 0.f ? p[e] * lo_f(vm[e].get(grp)) : 0.f;
-          b0 = pack_f16(pp[0], pp[1]);
-          b1 = pack_f16(pp[2], pp[3]);
-        }
+        const uint32_t b0 = hmul2(p01, lo_lo(vm[0].get(grp), vm[1].get(grp)));
+        const uint32_t b1 = hmul2(p23, lo_lo(vm[2].get(grp), vm[3].get(grp)));
         const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
         const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
         uint32_t xl[4], xh[4];
@@ -354,15 +421,20 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       }
     }
     __syncwarp();
-    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+    if (lane == 0 && i + kStages < n_my) {
+      issue(i + kStages, next_phys);
+      if (i + kStages + 1 < n_my) next_phys = bt_row[p_lo + warp + (i + kStages + 1) * kWarps];
+    }
   }
 
   // ------------------------------------------------ publish warp state
   float lsum = (r < 4) ? l_run : 0.f;
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+  float mt[NGH];
 #pragma unroll
   for (int gi = 0; gi < NGH; ++gi) {
+    mt[gi] = fmaf(8.f, mt_d[gi], mt_m[gi]);
     mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 1);
     mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 2);
   }
@@ -392,13 +464,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       }
   }
   merge_store<D, G>(sm, part_o, part_lse, row0, n_split, split);
+  combine_if_last<D, G>(sm, tickets, b * L.h_kv + h, part_o, part_lse, row0, n_split, out,
+                        out_lse);
 }
 
 template <int NG>
 cudaError_t launch_mma_t(const Layout& L, const void* paged, const void* side, const uint16_t* q,
                          const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
                          float sm_scale, int n4, int pages_per_split, int n8, int prot_per_split,
-                         float* part_o, float* part_lse, int32_t* status, cudaStream_t st) {
+                         float* part_o, float* part_lse, int32_t* tickets, uint16_t* out,
+                         float* out_lse, int32_t* status, cudaStream_t st) {
   constexpr int cb = 16 * D128 + 128 * NG;
   const size_t smem = ((sizeof(Smem<D128, G4>) + 127) / 128) * 128 + (size_t)kWarps * kStages * cb;
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<NG>,
@@ -407,7 +482,8 @@ cudaError_t launch_mma_t(const Layout& L, const void* paged, const void* side, c
   dim3 grid(n4 + n8, L.h_kv, num_seqs);
   decode_mma_kernel<NG><<<grid, kThreads, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, block_table,
-      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, status);
+      sm_scale * kLog2e, n4, pages_per_split, prot_per_split, part_o, part_lse, tickets, out,
+      out_lse, status);
   return cudaGetLastError();
 }
 
@@ -417,17 +493,21 @@ cudaError_t launch_decode_mma(const Layout& L, const void* paged, const void* si
                               const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                               const int32_t* block_table, float sm_scale, int n4,
                               int pages_per_split, int n8, int prot_per_split, float* part_o,
-                              float* part_lse, int32_t* status, cudaStream_t st) {
+                              float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
+                              int32_t* status, cudaStream_t st) {
   switch (L.d_h / L.g) {
     case 4:
       return launch_mma_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
-                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, tickets, out,
+                             out_lse, status, st);
     case 2:
       return launch_mma_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
-                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, tickets, out,
+                             out_lse, status, st);
     case 1:
       return launch_mma_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, n4,
-                             pages_per_split, n8, prot_per_split, part_o, part_lse, status, st);
+                             pages_per_split, n8, prot_per_split, part_o, part_lse, tickets, out,
+                             out_lse, status, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -1,0 +1,141 @@
+"""Full-size parity: the workloads at their stated sizes, run through the C ABI
+in the launch configuration the benchmark times, checked against the CPU
+oracle on a seeded sample of sequences (all heads): the cache bytes of every
+position of a sampled sequence bit for bit, and the decode outputs within the
+tolerance.  Sequence sources are regenerated from their seeds."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+import oracle  # noqa: E402
+from kv4_case import compare_outputs, half_ulp_bf16  # noqa: E402
+from int8_kv_cache_kv4_gb300 import kv4, workloads as W  # noqa: E402
+from int8_kv_cache_kv4_gb300.cache import build_workload, source_kv, step_inputs  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kv4.load(build_if_missing=True)
+
+
+def _check_seq_bytes(cache, w, b, k_src, v_src, L):
+    """Oracle-append sequence b's L positions into a private pool (page p at
+    pool page p) and compare every page chunk and the side block with the
+    device cache."""
+    npages = (L + 15) // 16
+    cb = oracle.chunk_bytes(w.d_h, w.group)
+    sb = oracle.side_block_bytes(w.d_h, w.sink, w.recent)
+    paged = np.zeros(npages * w.h_kv * cb, np.uint8)
+    side = np.zeros(max(16, w.h_kv * sb), np.uint8)
+    bt = np.arange(npages, dtype=np.int32)[None, :]
+    st = oracle.quant_append(h_kv=w.h_kv, d_h=w.d_h, g=w.group, S=w.sink, R=w.recent, max_seqs=1,
+                             num_pages=npages, max_pages_per_seq=npages, paged=paged, side=side,
+                             k_new=np.ascontiguousarray(k_src.transpose(1, 0, 2)),
+                             v_new=np.ascontiguousarray(v_src.transpose(1, 0, 2)),
+                             tok_seq=np.zeros(L, np.int32), tok_pos=np.arange(L, dtype=np.int32),
+                             seq_lens=np.array([L], np.int32), block_table=bt)
+    assert st == 0
+    dev_bt = cache.block_table[b, :npages].cpu().numpy()
+    allp = cache.paged.view(-1, w.h_kv * cb)
+    got = allp[torch.as_tensor(dev_bt.astype(np.int64), device=allp.device)].cpu().numpy().ravel()
+    assert np.array_equal(got, paged), f"seq {b}: INT4 page bytes differ from the oracle"
+    if w.sink + w.recent > 0:
+        gs = cache.side[b * w.h_kv * sb:(b + 1) * w.h_kv * sb].cpu().numpy()
+        assert np.array_equal(gs, side[: w.h_kv * sb]), f"seq {b}: side cache differs"
+
+
+def _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=None):
+    ref_o, ref_l = {}, {}
+    for b in seqs:
+        k, v = srcs[b]
+        ref_o[b], ref_l[b], _ = oracle.decode_seq(qs[b], k, v, g=w.group, S=w.sink, R=w.recent,
+                                                  sm_scale=1 / math.sqrt(w.d_h))
+    mx, mean = compare_outputs(out, lse, ref_o, ref_l, seqs, lens)
+    raw = max(float(np.abs(out[b] - ref_o[b]).max()) for b in seqs)
+    print(f"{w.name} g={w.group} R={w.recent}: max {mx:.2e} mean {mean:.2e} raw max {raw:.2e}")
+    if raw_max is not None:
+        assert raw <= raw_max, f"raw max abs error {raw:.3e}"
+
+
+def _run_step(cache, s):
+    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+    cache.decode(s["q"], s["lens"], s["out"], s["lse"])
+    torch.cuda.synchronize()
+    assert cache.read_status() == 0
+    return (s["out"].float().cpu().numpy().astype(np.float64),
+            s["lse"].cpu().numpy().astype(np.float64))
+
+
+def _sample(w, lens, n=8):
+    return W.sample_rows(w.seed, len(lens), n, extra=[int(np.argmin(lens)), int(np.argmax(lens))])
+
+
+def test_qwen3_8b_batch64_full_size():
+    w = W.WORKLOADS["qwen3_8b_b64"]
+    dev = torch.device("cuda")
+    cache, s, lens, w = build_workload(w, dev)
+    out, lse = _run_step(cache, s)
+    seqs = _sample(w, lens, 6)
+    qs = s["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+    srcs = {b: source_kv(w, b, int(lens[b]), dev) for b in seqs}
+    for b in seqs[:3]:
+        _check_seq_bytes(cache, w, b, *srcs[b], int(lens[b]))
+    # diffuse attention at these lengths: the raw error also meets 2e-3
+    _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=2e-3)
+
+
+@pytest.mark.parametrize("recent", [256, 131072])
+def test_long_context_128k(recent):
+    # mixed INT4/INT8 (R = 256) and INT8-everywhere (R >= L, same code path)
+    w = W.WORKLOADS["long_128k"]
+    dev = torch.device("cuda")
+    cache, s, lens, w = build_workload(w, dev, recent=recent)
+    assert kv4.num_splits(cache.layout, 1) * w.h_kv >= 148
+    out, lse = _run_step(cache, s)
+    qs = s["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+    srcs = {0: source_kv(w, 0, int(lens[0]), dev)}
+    _check_decode(out, lse, w, [0], srcs, qs, lens, raw_max=2e-3)
+
+
+def test_rollout_batch256_100_steps():
+    w = W.WORKLOADS["rollout_b256"]
+    dev = torch.device("cuda")
+    steps = w.steps
+    cache, s, lens0, w = build_workload(w, dev, extra_tokens=steps)
+    B = len(lens0)
+    _run_step(cache, s)
+    for st in range(1, steps):
+        k, v, q = step_inputs(w, B, st, dev)
+        lens = lens0 + st
+        s2 = dict(s, k=k, v=v, q=q, pos=torch.as_tensor((lens - 1).astype(np.int32), device=dev),
+                  lens=torch.as_tensor(lens.astype(np.int32), device=dev))
+        out, lse = _run_step(cache, s2)
+    lens = lens0 + steps - 1
+    seqs = _sample(w, lens, 8)
+    qs = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    srcs = {b: source_kv(w, b, int(lens0[b]), dev, steps=steps) for b in seqs}
+    for b in seqs:
+        _check_seq_bytes(cache, w, b, *srcs[b], int(lens[b]))
+    _check_decode(out, lse, w, seqs, srcs, qs, lens)
+
+
+@pytest.mark.parametrize("recent,group", [(0, 32), (128, 64), (512, 128), (64, 32)])
+def test_36_layer_workload_one_layer(recent, group):
+    # one layer (seed 500) of the 128 x 8192 step at points of the R x group sweep
+    w = W.WORKLOADS["qwen3_8b_36l"]
+    dev = torch.device("cuda")
+    cache, s, lens, w = build_workload(w, dev, recent=recent, group=group)
+    out, lse = _run_step(cache, s)
+    seqs = _sample(w, lens, 4)
+    qs = s["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+    srcs = {b: source_kv(w, b, int(lens[b]), dev) for b in seqs}
+    _check_seq_bytes(cache, w, seqs[0], *srcs[seqs[0]], int(lens[seqs[0]]))
+    _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=2e-3)
+    del cache
+    torch.cuda.empty_cache()
