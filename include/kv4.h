@@ -36,11 +36,12 @@
  *                  V codes [16 slots][head_dim/2 bytes]
  *                  K meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
  *                  V meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
- *     Byte i of a K code row holds channel 2i in its low nibble and channel
- *     2i+1 in its high nibble.  A V code row is the same sequence of bytes
- *     cut into 16-byte pieces (32 channels each), with piece P of slot t
- *     stored at piece position P ^ ((t >> 1) & (head_dim/32 - 1)) so that the
- *     decode kernel's transposing shared-memory reads hit distinct banks.
+ *     A code row is the sequence of bytes whose byte i holds channel 2i in
+ *     its low nibble and channel 2i+1 in its high nibble, cut into 16-byte
+ *     pieces (32 channels each); piece P of slot t is stored at piece position
+ *     P ^ ((t >> 1) & (head_dim/32 - 1)), for K and V alike, so that the
+ *     decode kernels' row-wise and transposing shared-memory reads across
+ *     consecutive slots hit distinct banks.
  *     Position p of request slot s lives in page block_table[s][p / 16],
  *     slot p % 16.
  *     chunk bytes = 16*head_dim + 128*head_dim/g  (2560 at d=128, g=32).
@@ -85,6 +86,7 @@ extern "C" {
 #define KV4_STATUS_BAD_SEQ 4   /* request slot outside [0, max_seqs) */
 #define KV4_STATUS_NONFINITE 8 /* non-finite input, or metadata overflowing fp16 */
 #define KV4_STATUS_BAD_LEN 16  /* decode: seq_len < 0 or beyond the block-table capacity */
+#define KV4_STATUS_TIMEOUT 32  /* a bounded wait inside a kernel expired; its outputs are invalid */
 
 /* Shape of one attention layer's cache.  All fields are host values. */
 typedef struct kv4_layout {

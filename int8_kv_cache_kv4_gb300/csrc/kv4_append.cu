@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     if (active) {
       uint8_t* row = chunk + (kv == 0 ? 0 : codes_off_v(d_h)) + slot * (d_h / 2);
       // 4 codes of channels c0..c0+3 -> two bytes (low nibble = even channel)
-      const int b = kv == 0 ? 2 * lane : vrow_byte(2 * lane, slot, d_h);
+      const int b = row_byte(2 * lane, slot, d_h);
       *reinterpret_cast<uint16_t*>(row + b) = (uint16_t)codes;
       if ((lane % span) == 0) {
         uint8_t* m = chunk + (kv == 0 ? meta_off_k(d_h) : meta_off_v(d_h, g)) + slot * ng * 4;

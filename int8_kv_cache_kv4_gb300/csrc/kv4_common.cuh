@@ -20,10 +20,10 @@ __host__ __device__ inline int chunk_bytes(int d_h, int g) { return 16 * d_h + 1
 __host__ __device__ inline int codes_off_v(int d_h) { return 8 * d_h; }  // 16 rows * d_h/2
 __host__ __device__ inline int meta_off_k(int d_h) { return 16 * d_h; }
 __host__ __device__ inline int meta_off_v(int d_h, int g) { return 16 * d_h + 64 * (d_h / g); }
-// Byte offset inside a V code row of logical byte `b` for slot `t`: the row's
-// 16-byte pieces are XOR-permuted by (t >> 1) so that transposing 8x16-byte
-// shared-memory reads across 8 consecutive slots touch distinct banks.
-__host__ __device__ inline int vrow_byte(int b, int t, int d_h) {
+// Byte offset inside a K or V code row of logical byte `b` for slot `t`: the
+// row's 16-byte pieces are XOR-permuted by (t >> 1) so that 16-byte reads of
+// one piece index across 8 consecutive slots touch distinct banks.
+__host__ __device__ inline int row_byte(int b, int t, int d_h) {
   const int np = d_h / 32;
   return 16 * ((b >> 4) ^ ((t >> 1) & (np - 1))) + (b & 15);
 }

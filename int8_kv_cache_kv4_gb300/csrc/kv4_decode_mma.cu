@@ -289,8 +289,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       // metadata may be any bit pattern, so it is zeroed before use
       const bool tail = (pg + 1) * kPage > len;
       // ---------------- QK^T on tensor cores
-      const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + 16 * qd);
-      const uint4 k1 = *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + 16 * qd);
+      const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + row_byte(16 * qd, r, D));
+      const uint4 k1 =
+          *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + row_byte(16 * qd, r + 8, D));
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {

@@ -265,13 +265,13 @@ int kv4o_side_slot(int p, int S, int R) { return p < S ? p : S + (p % R); }
  *
  *   paged cache = [num_pages][h_kv][chunk], chunk bytes = 16*d_h + 128*(d_h/g)
  *   (page size 16), and inside one chunk:
- *     K codes  [16 slots][d_h/2 bytes]   byte i of a slot row holds channel 2i in
- *                                        its low nibble and channel 2i+1 in its
- *                                        high nibble
- *     V codes  [16 slots][d_h/2 bytes]   same bytes, but the row is cut into
- *                                        16-byte pieces of 32 channels and piece
- *                                        P of slot t is stored at piece position
- *                                        P xor ((t / 2) mod (d_h / 32))
+ *     K codes  [16 slots][d_h/2 bytes]   logical byte i of a slot row holds
+ *                                        channel 2i in its low nibble and channel
+ *                                        2i+1 in its high nibble; the row is cut
+ *                                        into 16-byte pieces of 32 channels and
+ *                                        piece P of slot t is stored at piece
+ *                                        position P xor ((t / 2) mod (d_h / 32))
+ *     V codes  [16 slots][d_h/2 bytes]   same as K
  *     K meta   [16 slots][d_h/g][2 x u16] (Delta16, m16) per group
  *     V meta   [16 slots][d_h/g][2 x u16]
  *
@@ -342,11 +342,8 @@ int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int 
         }
         int npieces = d_h / 32;
         for (int i = 0; i < d_h / 2; ++i) {
-          int dst = i;
-          if (kv == 1) {
-            int piece = i / 16, within = i % 16;
-            dst = 16 * (piece ^ ((slot / 2) % npieces)) + within;
-          }
+          int piece = i / 16, within = i % 16;
+          int dst = 16 * (piece ^ ((slot / 2) % npieces)) + within;
           rows[dst] = (uint8_t)(c4[2 * i] | (c4[2 * i + 1] << 4));
         }
         if (prot) {

@@ -28,14 +28,17 @@ def _unpack_chunk(chunk, d_h, g):
         out[:, 1::2] = rows >> 4
         return out
 
-    # V rows: 16-byte piece P of slot t sits at piece position P ^ ((t >> 1) % npieces)
+    # rows: 16-byte piece P of slot t sits at piece position P ^ ((t >> 1) % npieces)
     npieces = d_h // 32
-    vlog = np.empty_like(vc)
-    for t in range(16):
-        for P in range(npieces):
-            phys = P ^ ((t >> 1) % npieces)
-            vlog[t, 16 * P:16 * P + 16] = vc[t, 16 * phys:16 * phys + 16]
-    return nib(kc), nib(vlog), meta[0], meta[1]
+
+    def unswizzle(rows):
+        out = np.empty_like(rows)
+        for t in range(16):
+            for P in range(npieces):
+                phys = P ^ ((t >> 1) % npieces)
+                out[t, 16 * P:16 * P + 16] = rows[t, 16 * phys:16 * phys + 16]
+        return out
+    return nib(unswizzle(kc)), nib(unswizzle(vc)), meta[0], meta[1]
 
 
 def _side_block(side, s, h, h_kv, d_h, S, R):
