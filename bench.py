@@ -140,6 +140,9 @@ def run_kv4(args):
     dev = torch.device("cuda", local)
     from int8_kv_cache_kv4_gb300 import kv4
     kv4.load(build_if_missing=True)
+    kv4.kv4_set_decode_kernel({"auto": kv4.KV4_KERNEL_AUTO, "tcgen05": kv4.KV4_KERNEL_TCGEN05,
+                               "mma": kv4.KV4_KERNEL_MMA_SYNC,
+                               "cuda": kv4.KV4_KERNEL_CUDA_CORE}[args.kernel])
 
     w = W.WORKLOADS[args.workload]
     cache, s, lens, w = build_workload(w, dev, with_bf16=not args.no_bf16)
@@ -222,7 +225,7 @@ def run_kv4(args):
                    "total_tokens": tokens, "h_q": w.h_q, "h_kv": w.h_kv, "d_h": w.d_h,
                    "sink": w.sink, "recent": w.recent, "group": w.group, "page": 16,
                    "splits": kv4.num_splits(cache.layout, int(len(lens)), args.max_splits),
-                   "parallelism": f"replicas x{world}",
+                   "parallelism": f"replicas x{world}", "decode_kernel": args.kernel,
                    "l2": "cache working set > L2 (no flush needed)"},
         "decode_ms": dec_avg, "append_ms": statistics.mean(app_ms),
         "decode_tokens_per_s": tokens / (dec_avg / 1e3),
@@ -338,6 +341,8 @@ def main():
     ap.add_argument("--impl", default="kv4", choices=["kv4", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b64", choices=sorted(W.WORKLOADS))
     ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tcgen05", "mma", "cuda"],
+                    help="decode kernel (auto = tcgen05 for this shape)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")

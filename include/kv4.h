@@ -107,6 +107,19 @@ typedef struct kv4_layout {
 int kv4_abi_version(void);
 const char* kv4_status_string(int code);
 
+/* Decode kernel selection (process-wide; default KV4_KERNEL_AUTO).  AUTO picks
+ * the fastest kernel measured on GB300 for the layout: the warp-level
+ * tensor-core (mma.sync) kernel for head_dim 128 with 4 query heads per kv
+ * head, the CUDA-core kernel otherwise.  TCGEN05 selects the tensor-memory
+ * (tcgen05.mma) kernel, MMA_SYNC the warp-level one, CUDA_CORE the fp32 one
+ * (all compute the same result within the stated tolerance).  A kernel that does not support the
+ * layout falls back to the CUDA-core kernel.  Returns the previous value. */
+#define KV4_KERNEL_AUTO 0
+#define KV4_KERNEL_CUDA_CORE 1
+#define KV4_KERNEL_MMA_SYNC 2
+#define KV4_KERNEL_TCGEN05 3
+int kv4_set_decode_kernel(int which);
+
 /* Validate a layout; KV4_OK or a KV4_ERR_* code. */
 int kv4_check_layout(const kv4_layout* layout);
 

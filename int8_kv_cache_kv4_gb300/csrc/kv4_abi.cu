@@ -21,6 +21,11 @@ cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, cons
 cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
                            cudaStream_t);
 bool mma_supported(const Layout&);
+cudaError_t launch_decode_tc(const Layout&, const void*, const void*, const uint16_t*,
+                             const int32_t*, int, const int32_t*, float, int, int, int, int,
+                             float*, float*, int32_t*, uint16_t*, float*, int32_t*,
+                             cudaStream_t);
+static int g_decode_kernel = KV4_KERNEL_AUTO;
 cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uint16_t*,
                               const int32_t*, int, const int32_t*, float, int, int, int, int,
                               float*, float*, int32_t*, uint16_t*, float*, int32_t*,
@@ -29,11 +34,12 @@ cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uin
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
 // kTargetCtas CTAs in total (16 per SM of a 152-SM GB300), at least
-// kMinPagesPerSplit pages per INT4 split, and one protected split per
-// kProtChunk side-cache slots.
+// kMinPagesPerSplit pages per INT4 split, a whole number of 8-page tiles per
+// split, and one protected split per kProtChunk side-cache slots.
 constexpr int kTargetCtas = 16 * 152;
 constexpr int kMinPagesPerSplit = 4;
 constexpr int kProtChunk = 256;
+constexpr int kTilePagesPlan = 8;
 
 struct Plan {
   int n4, pages_per_split, n8, prot_per_split;
@@ -50,6 +56,8 @@ static Plan make_plan(const kv4_layout* lay, int num_seqs, int max_splits, bool 
   int pps = (int)((maxp + n4 - 1) / n4);
   if (pps < kMinPagesPerSplit) pps = kMinPagesPerSplit;
   if (max_splits > 0 && (maxp + pps - 1) / pps > max_splits) pps = (maxp + max_splits - 1) / max_splits;
+  // whole 8-page tiles (the tensor-memory kernel's unit of work)
+  pps = (pps + kTilePagesPlan - 1) / kTilePagesPlan * kTilePagesPlan;
   p.pages_per_split = pps;
   p.n4 = (maxp + pps - 1) / pps;
   const int NS = lay->sink + lay->recent;
@@ -107,6 +115,12 @@ using namespace kv4;
 extern "C" {
 
 int kv4_abi_version(void) { return KV4_ABI_VERSION; }
+
+int kv4_set_decode_kernel(int which) {
+  const int prev = g_decode_kernel;
+  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_TCGEN05) g_decode_kernel = which;
+  return prev;
+}
 
 const char* kv4_status_string(int code) {
   switch (code) {
@@ -203,17 +217,25 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   const Layout L = to_layout(l);
   // Completion tickets for the fused eq. A1 merge start at zero on every call.
   if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
-  // head_dim 128 with 4 query heads per kv head runs the tensor-core kernel;
-  // other shapes the CUDA-core kernel.  Both merge their splits in the
-  // last-finishing CTA of each (sequence, kv head).
-  cudaError_t e =
-      mma_supported(L)
-          ? launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
-                              p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
-                              w.tickets, out, out_lse, dev_status, st)
-          : launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+  // head_dim 128 with 4 query heads per kv head runs a tensor-core kernel
+  // (the warp-level mma kernel by default); other shapes the CUDA-core kernel.  All merge their
+  // splits in the last-finishing CTA of each (sequence, kv head).
+  int which = g_decode_kernel;
+  if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_MMA_SYNC;  // fastest measured on GB300
+  if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
+  cudaError_t e;
+  if (which == KV4_KERNEL_TCGEN05)
+    e = launch_decode_tc(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                         p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
+                         w.tickets, out, out_lse, dev_status, st);
+  else if (which == KV4_KERNEL_MMA_SYNC)
+    e = launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                           p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
                           w.tickets, out, out_lse, dev_status, st);
+  else
+    e = launch_decode(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                      p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
+                      w.tickets, out, out_lse, dev_status, st);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 

@@ -25,10 +25,20 @@ struct Smem {
   float p[kWarps][16][G];        // probabilities of the current tile, per warp
   float mrg_m[kWarps][G];
   float mrg_l[kWarps][G];
-  union {
+  union __align__(128) {
     float mrg_o[kWarps][G][D];      // per-warp unnormalised outputs (end of a split)
-    uint32_t qfrag[8][32][4];       // tensor-core query fragments (start of a split)
+    uint32_t qfrag[8][32][4];       // mma.sync query fragments (start of a split)
+    struct {
+      uint16_t bq[16 * D];          // tcgen05: block-diagonal query operand (K-major)
+      uint16_t bp[16 * D];          // tcgen05: probability operand P' (MN-major)
+    } tc;
   };
+  float tc_wmax[kWarps][G];         // tcgen05: per-warp tile maxima
+  float tc_red[kWarps][G][5];       // tcgen05: per-warp l and offset-term partials
+  int32_t tc_phys[2][8];            // tcgen05: physical pages of a staged tile
+  uint64_t tc_bar[4];               // tcgen05: tile full x2, QK done, PV done
+  uint32_t tc_tmem;                 // tcgen05: tensor-memory base address
+  int32_t tc_abort;
   float mrg_mt[kWarps][G][D / 32];  // additive term per 32-channel block (tensor-core path)
   uint16_t qh[G][D];                // query as fp16 bits
   int32_t phys[kWarps][kStages];    // physical page of each in-flight stage
@@ -87,7 +97,7 @@ template <int D, int G>
 __device__ inline void qk_int4(const Smem<D, G>& sm, const uint8_t* chunk, int g, int t, int half,
                                float s[G]) {
   const int ng = D / g;
-  const uint32_t* krow = reinterpret_cast<const uint32_t*>(chunk + t * (D / 2) + half * (D / 4));
+  const uint8_t* krow = chunk + t * (D / 2);
   const uint32_t* kmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_k(D) + t * ng * 4);
 #pragma unroll
   for (int j = 0; j < G; ++j) s[j] = 0.f;
@@ -97,7 +107,8 @@ __device__ inline void qk_int4(const Smem<D, G>& sm, const uint8_t* chunk, int g
   constexpr int WORDS = D / 16;  // 8 nibbles per word, D/2 channels per lane
 #pragma unroll
   for (int w = 0; w < WORDS; ++w) {
-    const uint32_t word = krow[w];
+    const uint32_t word =
+        *reinterpret_cast<const uint32_t*>(krow + row_byte(half * (D / 4) + 4 * w, t, D));
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
       const float c = u2f((word >> (4 * n)) & 0xFu);
@@ -138,9 +149,9 @@ __device__ inline void pv_int4(WarpState<D, G>& ws, const uint8_t* chunk, int g,
     if (!((tok_mask >> (2 * t)) & 1u)) continue;  // masked slot: may hold stale bytes
     uint32_t bits;
     if (PD == 4)
-      bits = *reinterpret_cast<const uint16_t*>(vcodes + t * (D / 2) + vrow_byte(c0 / 2, t, D));
+      bits = *reinterpret_cast<const uint16_t*>(vcodes + t * (D / 2) + row_byte(c0 / 2, t, D));
     else
-      bits = vcodes[t * (D / 2) + vrow_byte(c0 / 2, t, D)];
+      bits = vcodes[t * (D / 2) + row_byte(c0 / 2, t, D)];
     const uint32_t mt = vmeta[t * ng + grp];
     const float delta = f16_bits_to_f32(mt & 0xFFFFu);
     const float off = f16_bits_to_f32(mt >> 16);

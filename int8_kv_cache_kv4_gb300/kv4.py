@@ -28,6 +28,12 @@ KV4_STATUS_BAD_POS = 2
 KV4_STATUS_BAD_SEQ = 4
 KV4_STATUS_NONFINITE = 8
 KV4_STATUS_BAD_LEN = 16
+KV4_STATUS_TIMEOUT = 32
+
+KV4_KERNEL_AUTO = 0
+KV4_KERNEL_CUDA_CORE = 1
+KV4_KERNEL_MMA_SYNC = 2
+KV4_KERNEL_TCGEN05 = 3
 
 
 class kv4_layout(ctypes.Structure):
@@ -81,6 +87,7 @@ def load(build_if_missing: bool = False):
     LP = ctypes.POINTER(kv4_layout)
     sig = {
         "kv4_abi_version": (ctypes.c_int, []),
+        "kv4_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
         "kv4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv4_check_layout": (ctypes.c_int, [LP]),
         "kv4_paged_cache_bytes": (Sz, [LP]),
@@ -135,6 +142,11 @@ def _dev(t, dtype, name):
         raise KV4Error(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise KV4Error(f"{name} must be contiguous")
+
+
+def kv4_set_decode_kernel(which: int) -> int:
+    """Select the decode kernel (KV4_KERNEL_*); returns the previous choice."""
+    return int(load().kv4_set_decode_kernel(int(which)))
 
 
 def paged_cache_bytes(layout: kv4_layout) -> int:

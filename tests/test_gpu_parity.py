@@ -20,6 +20,16 @@ def _lib():
     kv4.load(build_if_missing=True)
 
 
+# every decode kernel (tcgen05, warp-level mma, CUDA cores) must meet the bar;
+# shapes a kernel does not support run the CUDA-core kernel
+@pytest.fixture(autouse=True, params=[kv4.KV4_KERNEL_TCGEN05, kv4.KV4_KERNEL_MMA_SYNC,
+                                      kv4.KV4_KERNEL_CUDA_CORE], ids=["tcgen05", "mma", "cuda"])
+def kernel(request):
+    prev = kv4.kv4_set_decode_kernel(request.param)
+    yield request.param
+    kv4.kv4_set_decode_kernel(prev)
+
+
 def _bytes_equal(gpu_t, ref, what):
     got = gpu_t.cpu().numpy()[: ref.size]
     if not np.array_equal(got, ref):
