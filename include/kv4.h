@@ -215,6 +215,41 @@ int kv4_bf16_decode_attn(const kv4_layout* layout, const void* cache, const uint
                          size_t workspace_bytes, uint16_t* out, float* out_lse,
                          int32_t* dev_status, void* stream);
 
+/*
+ * kv4_decode_attn_noalloc -- kv4_decode_attn for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this is a convenience of this
+ * library.
+ *
+ * Who needs it: kv4_decode_attn takes a caller-allocated workspace.  Some
+ * callers cannot provide one -- a plug-in whose host framework has reserved
+ * all free device memory for its own pool, a decode loop that must not call
+ * cudaMalloc (it synchronises the device and can fail under memory pressure),
+ * or a runtime with no device allocator.  This entry point computes exactly
+ * what kv4_decode_attn computes, taking its workspace from one fixed scratch
+ * array compiled into the library instead.
+ *
+ * Limits and behaviour:
+ *   - The scratch holds kv4_noalloc_scratch_bytes() bytes (16 MiB) on every
+ *     GPU that loads the library, for the life of the process.  A call whose
+ *     kv4_workspace_bytes(layout, num_seqs, max_splits) exceeds it returns
+ *     KV4_ERR_WORKSPACE and enqueues nothing.
+ *   - Nothing is allocated or freed: the first call on a device looks up the
+ *     scratch's device address (cudaGetSymbolAddress, with that device
+ *     current) and caches it, so make that first call before any stream
+ *     capture.
+ *   - All calls share the one scratch array, which keeps the last call's
+ *     contents; the completion counters that must start at zero are cleared on
+ *     the stream at the start of every call.  Calls whose work overlaps on the
+ *     GPU (different streams, or different host threads) race on the scratch
+ *     and must be serialised by the caller.
+ *   Arguments are those of kv4_decode_attn without workspace/workspace_bytes.
+ */
+size_t kv4_noalloc_scratch_bytes(void);
+int kv4_decode_attn_noalloc(const kv4_layout* layout, const void* paged, const void* side,
+                            const uint16_t* q, const int32_t* seq_lens, int32_t num_seqs,
+                            const int32_t* block_table, float sm_scale, int32_t max_splits,
+                            uint16_t* out, float* out_lse, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,6 +102,9 @@ def load(build_if_missing: bool = False):
         "kv4_bf16_append": (ctypes.c_int, [LP, P, P, P, P, P, I, P, P, P, P]),
         "kv4_bf16_decode_attn": (ctypes.c_int, [LP, P, P, P, I, P, ctypes.c_float, I, P, Sz, P,
                                                 P, P, P]),
+        "kv4_noalloc_scratch_bytes": (Sz, []),
+        "kv4_decode_attn_noalloc": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, P,
+                                                   P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -250,3 +253,27 @@ def kv4_bf16_decode_attn(layout, cache, q, seq_lens, block_table, workspace, out
                                      _ptr(workspace), workspace.numel(), _ptr(out), _ptr(out_lse),
                                      _ptr(status), _stream(stream))
     _check(rc, "kv4_bf16_decode_attn")
+
+
+def kv4_decode_attn_noalloc(layout, paged, side, q, seq_lens, block_table, out, out_lse=None,
+                            sm_scale=None, max_splits=0, status=None, stream=None):
+    """kv4_decode_attn without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed scratch array is used instead
+    (see include/kv4.h for its size, first-call set-up and sharing rules)."""
+    import torch
+    _dev(paged, torch.uint8, "paged")
+    _dev(side, torch.uint8, "side")
+    _dev(q, torch.bfloat16, "q")
+    _dev(out, torch.bfloat16, "out")
+    _dev(out_lse, torch.float32, "out_lse")
+    _dev(seq_lens, torch.int32, "seq_lens")
+    _dev(block_table, torch.int32, "block_table")
+    _dev(status, torch.int32, "status")
+    B = int(q.shape[0])
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(layout.head_dim)
+    rc = load().kv4_decode_attn_noalloc(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(q),
+                                        _ptr(seq_lens), B, _ptr(block_table), float(sm_scale),
+                                        int(max_splits), _ptr(out), _ptr(out_lse), _ptr(status),
+                                        _stream(stream))
+    _check(rc, "kv4_decode_attn_noalloc")
