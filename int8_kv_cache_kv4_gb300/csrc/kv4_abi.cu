@@ -52,7 +52,7 @@ static Plan make_plan(const kv4_layout* lay, int num_seqs, int max_splits, bool 
   const long long units = (long long)(num_seqs > 0 ? num_seqs : 1) * lay->num_kv_heads;
   long long n4 = (kTargetCtas + units - 1) / units;
   if (n4 < 1) n4 = 1;
-  if (max_splits > 0 && n4 > max_splits) n4 = max_splits;
+  if (max_splits > 0) n4 = max_splits;  // caller's choice (still an upper bound below)
   int pps = (int)((maxp + n4 - 1) / n4);
   if (pps < kMinPagesPerSplit) pps = kMinPagesPerSplit;
   if (max_splits > 0 && (maxp + pps - 1) / pps > max_splits) pps = (maxp + max_splits - 1) / max_splits;

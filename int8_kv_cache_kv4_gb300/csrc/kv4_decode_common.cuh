@@ -216,19 +216,23 @@ __device__ inline void merge_store(Smem<D, G>& sm, float* part_o, float* part_ls
 }
 
 // Eq. A1 over the n_split partials of `G` consecutive rows, done by the last
-// CTA of a (sequence, kv head) to finish (an atomic ticket per pair; the
-// partials of the other CTAs are made visible by their __threadfence()).
+// CTA of a (sequence, kv head) to finish.  An atomic ticket per pair counts
+// finished CTAs: the CTA barrier makes every thread's partial writes visible
+// to thread 0, whose device-scope fence then orders them (cumulatively)
+// before its ticket increment; the last CTA fences again before reading.
 template <int D, int G>
 __device__ inline void combine_if_last(Smem<D, G>& sm, int32_t* tickets, int pair,
                                        const float* part_o, const float* part_lse,
                                        long long row0, int n_split, uint16_t* out,
                                        float* out_lse) {
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) sm.ticket = atomicAdd(&tickets[pair], 1);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sm.ticket = atomicAdd(&tickets[pair], 1);
+    if (sm.ticket == n_split - 1) __threadfence();
+  }
   __syncthreads();
   if (sm.ticket != n_split - 1) return;
-  __threadfence();
   constexpr int PD = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = warp; j < G; j += kWarps) {
@@ -240,18 +244,34 @@ __device__ inline void combine_if_last(Smem<D, G>& sm, int32_t* tickets, int pai
     float acc[PD];
 #pragma unroll
     for (int i = 0; i < PD; ++i) acc[i] = 0.f;
-    float Z = 0.f;
+    float Zl = 0.f;
     if (M != -INFINITY) {
-      for (int r = 0; r < n_split; ++r) {
-        const float z = __ldcg(lse + r);
-        if (z == -INFINITY) continue;
-        const float w = exp2f((z - M) * kLog2e);
-        Z += w;
-        const float* o = part_o + (row * n_split + r) * D + lane * PD;
+      for (int r0 = 0; r0 < n_split; r0 += 32) {
+        const int r = r0 + lane;
+        const float z = r < n_split ? __ldcg(lse + r) : -INFINITY;
+        const float wl = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
+        Zl += wl;
+        const int nr = min(32, n_split - r0);
+        // four parts' outputs in flight at a time
+        for (int rr = 0; rr < nr; rr += 4) {
+          float wv[4], o[4][PD];
 #pragma unroll
-        for (int i = 0; i < PD; ++i) acc[i] = fmaf(w, __ldcg(o + i), acc[i]);
+          for (int u = 0; u < 4; ++u) {
+            wv[u] = __shfl_sync(0xffffffffu, wl, (rr + u) & 31);
+            const bool use = rr + u < nr && wv[u] != 0.f;
+            const float* op = part_o + (row * n_split + r0 + rr + u) * D + lane * PD;
+#pragma unroll
+            for (int i = 0; i < PD; ++i) o[u][i] = use ? __ldcg(op + i) : 0.f;
+            if (!use) wv[u] = 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < PD; ++i) acc[i] = fmaf(wv[u], o[u][i], acc[i]);
+        }
       }
     }
+    const float Z = warp_sum(Zl);
     const bool empty = !(Z > 0.f);
 #pragma unroll
     for (int i = 0; i < PD; ++i)
@@ -262,18 +282,28 @@ __device__ inline void combine_if_last(Smem<D, G>& sm, int32_t* tickets, int pai
 
 template <int D, int G>
 __device__ inline void load_query(Smem<D, G>& sm, const uint16_t* q, long long row0) {
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-    const int j = idx / D, d = idx % D;
-    const float x = bf16_bits_to_f32(q[(row0 + j) * D + d]);
-    sm.qh[j][d] = __half_as_ushort(__float2half_rn(x));
-    sm.q[j][d / (D / 2)][d % (D / 2)] = x;
+  // A warp's 32 lanes hold 32 consecutive channels of one head, so the
+  // per-32-channel query sums are warp reductions.
+  const int lane = threadIdx.x & 31;
+  constexpr int kIters = (G * D + kThreads - 1) / kThreads;
+  uint16_t raw[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {  // all loads in flight first
+    const int idx = it * kThreads + threadIdx.x;
+    raw[it] = idx < G * D ? q[(row0 + idx / D) * D + idx % D] : (uint16_t)0;
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * (D / 32); idx += kThreads) {
-    const int j = idx % G, bq = idx / G;
-    float s = 0.f;
-    for (int d = bq * 32; d < bq * 32 + 32; ++d) s += sm.q[j][d / (D / 2)][d % (D / 2)];
-    sm.qsum[bq][j] = s;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int idx = it * kThreads + threadIdx.x;
+    const bool ok = idx < G * D;
+    const int j = idx / D, d = idx % D;
+    const float x = bf16_bits_to_f32(raw[it]);
+    if (ok) {
+      sm.qh[j][d] = __half_as_ushort(__float2half_rn(x));
+      sm.q[j][d / (D / 2)][d % (D / 2)] = x;
+    }
+    const float s = warp_sum(x);
+    if (ok && lane == 0) sm.qsum[d / 32][j] = s;
   }
   __syncthreads();
 }
@@ -298,54 +328,76 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
   const int8_t* v8 = reinterpret_cast<const int8_t*>(blk + (long long)NS * D);
   const uint16_t* ks = reinterpret_cast<const uint16_t*>(blk + 2LL * NS * D);
   const uint16_t* vs = ks + NS;
+  constexpr int PD = D / 32;
   for (int base = i_lo + warp * 16; base < i_hi; base += kWarps * 16) {
     const int i = base + t;
     const bool tok_ok = i < i_hi;
     const int slot = tok_ok ? side_slot(prot_pos(rg, i), L.S, L.R) : 0;
+    const int ntok = min(16, i_hi - base);
+    // every global load of this 16-position block is issued before any use;
+    // V scales stay packed as fp16 pairs to keep the register count down
+    const uint4* krow = reinterpret_cast<const uint4*>(k8 + (long long)slot * D + half * (D / 2));
+    uint4 kraw0 = tok_ok ? krow[0] : make_uint4(0u, 0u, 0u, 0u);
+    uint4 kraw1 = tok_ok ? krow[1] : make_uint4(0u, 0u, 0u, 0u);
+    const float ksc = tok_ok ? f16_bits_to_f32(ks[slot]) : 0.f;
+    uint32_t vword[16];
+    uint32_t vsc2[8];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      const bool ok = tt < ntok;
+      const int slot2 = ok ? side_slot(prot_pos(rg, base + tt), L.S, L.R) : 0;
+      const uint32_t sbits = ok ? (uint32_t)vs[slot2] : 0u;
+      if (tt & 1)
+        vsc2[tt >> 1] |= sbits << 16;
+      else
+        vsc2[tt >> 1] = sbits;
+      if (PD == 4)
+        vword[tt] = ok ? *reinterpret_cast<const uint32_t*>(v8 + (long long)slot2 * D + lane * PD) : 0u;
+      else
+        vword[tt] = ok ? *reinterpret_cast<const uint16_t*>(v8 + (long long)slot2 * D + lane * PD) : 0u;
+    }
     float s[G];
 #pragma unroll
     for (int j = 0; j < G; ++j) s[j] = 0.f;
-    if (tok_ok) {
-      const int8_t* row = k8 + (long long)slot * D + half * (D / 2);
 #pragma unroll
-      for (int w = 0; w < D / 8; ++w) {
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(row + 4 * w);
+    for (int w = 0; w < D / 32; ++w) {
+      if (w == 2) {  // second half of this lane's 64 channels
+        kraw0 = tok_ok ? krow[2] : make_uint4(0u, 0u, 0u, 0u);
+        kraw1 = tok_ok ? krow[3] : make_uint4(0u, 0u, 0u, 0u);
+      }
+      const uint4 kr = (w & 1) ? kraw1 : kraw0;
+      const uint32_t words[4] = {kr.x, kr.y, kr.z, kr.w};
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi)
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          const float c = (float)(int8_t)((word >> (8 * n)) & 0xFFu);
+          const float c = (float)(int8_t)((words[wi] >> (8 * n)) & 0xFFu);
 #pragma unroll
-          for (int j = 0; j < G; ++j) s[j] = fmaf(sm.q[j][half][4 * w + n], c, s[j]);
+          for (int j = 0; j < G; ++j) s[j] = fmaf(sm.q[j][half][16 * w + 4 * wi + n], c, s[j]);
         }
-      }
-      const float sc = f16_bits_to_f32(ks[slot]);
-#pragma unroll
-      for (int j = 0; j < G; ++j) s[j] *= sc;
     }
 #pragma unroll
     for (int j = 0; j < G; ++j) {
+      s[j] *= ksc;
       s[j] += __shfl_xor_sync(0xffffffffu, s[j], 1);
       s[j] = tok_ok ? s[j] * scale_log2 : -INFINITY;
     }
     softmax_tile<D, G>(ws, s, sm.p[warp], lane);
     __syncwarp();
-    constexpr int PD = D / 32;
-    const int ntok = min(16, i_hi - base);
-    for (int tt = 0; tt < ntok; ++tt) {
-      const int slot2 = side_slot(prot_pos(rg, base + tt), L.S, L.R);
-      const float sc = f16_bits_to_f32(vs[slot2]);
-      uint32_t word;
-      if (PD == 4)
-        word = *reinterpret_cast<const uint32_t*>(v8 + (long long)slot2 * D + lane * PD);
-      else
-        word = *reinterpret_cast<const uint16_t*>(v8 + (long long)slot2 * D + lane * PD);
-      float v[PD];
 #pragma unroll
-      for (int ii = 0; ii < PD; ++ii) v[ii] = sc * (float)(int8_t)((word >> (8 * ii)) & 0xFFu);
+    for (int tt = 0; tt < 16; ++tt) {
+      if (tt < ntok) {
+        float v[PD];
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float pj = sm.p[warp][tt][j];
+        const float vsc = f16_bits_to_f32((vsc2[tt >> 1] >> (16 * (tt & 1))) & 0xFFFFu);
 #pragma unroll
-        for (int ii = 0; ii < PD; ++ii) ws.acc[j][ii] = fmaf(pj, v[ii], ws.acc[j][ii]);
+        for (int ii = 0; ii < PD; ++ii) v[ii] = vsc * (float)(int8_t)((vword[tt] >> (8 * ii)) & 0xFFu);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pj = sm.p[warp][tt][j];
+#pragma unroll
+          for (int ii = 0; ii < PD; ++ii) ws.acc[j][ii] = fmaf(pj, v[ii], ws.acc[j][ii]);
+        }
       }
     }
     __syncwarp();

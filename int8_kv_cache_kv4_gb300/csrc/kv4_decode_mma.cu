@@ -132,9 +132,13 @@ __device__ inline float lo_f(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); 
 __device__ inline float hi_f(uint32_t w) { return f16_bits_to_f32(w >> 16); }
 
 constexpr int D128 = 128, G4 = 4;
+// Two page stages per warp and the query fragments in shared memory keep the
+// kernel at <= 102 registers and ~38 KB of shared memory, so five CTAs (20
+// warps) share an SM.
+constexpr int kStagesMma = 2;
 
 template <int NG>
-__global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
+__global__ void __launch_bounds__(kThreads, 5) decode_mma_kernel(
     Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ block_table, float scale_log2, int n4, int pages_per_split,
@@ -147,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
   constexpr int cb = 16 * D + 128 * NG;
   uint8_t* stage_base = smem_raw + ((sizeof(Smem<D, G>) + 127) / 128) * 128;
+  uint32_t* qfrag = reinterpret_cast<uint32_t*>(stage_base + (size_t)kWarps * kStagesMma * cb);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int n_split = gridDim.x;
@@ -159,6 +164,20 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
     len = 0;
   }
   const Regions rg = regions(len, L.S, L.R);
+  const int first_page = rg.sink_end / kPage;
+  const int end_page = (rg.rec_start + kPage - 1) / kPage;
+  const int p_lo = first_page + split * pages_per_split;
+  const int p_hi = min(end_page, p_lo + pages_per_split);
+  const bool empty_int4 =
+      split < n4 && !(rg.rec_start > rg.sink_end && p_hi > p_lo);
+  const bool empty_prot = split >= n4 && (split - n4) * prot_per_split >= rg.n_prot;
+  if (empty_int4 || empty_prot) {
+    // nothing to attend: an empty part (weight 0 in the merge)
+    if (threadIdx.x < G) part_lse[(row0 + threadIdx.x) * n_split + split] = -INFINITY;
+    combine_if_last<D, G>(sm, tickets, b * L.h_kv + h, part_o, part_lse, row0, n_split, out,
+                          out_lse);
+    return;
+  }
   load_query(sm, q, row0);
 
   if (split >= n4) {
@@ -179,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   const int g0 = r >> 2, g1 = g0 + 2;         // groups of QK rows r and r+8
   const bool v0 = g0 < NG, v1 = g1 < NG;
   // Q operand fragments: block-diagonal (group, head) rows, fp16.  Identical
-  // for the CTA's four warps, so built once into shared memory.
+  // for the CTA's four warps: built once into shared memory ([s][lane][4]
+  // words) and read back per k-step.
   for (int idx = threadIdx.x; idx < 8 * 32 * 4; idx += kThreads) {
     const int s = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
     const int rr = ln >> 2, qq = ln & 3;
@@ -194,19 +214,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
         if (d / GS == grp) w |= (uint32_t)sm.qh[jj][d] << (16 * e2);
       }
     }
-    sm.qfrag[s][ln][k] = w;
+    qfrag[idx] = w;
   }
   __syncthreads();
-  uint32_t qa[8][4];
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint4 v = *reinterpret_cast<const uint4*>(&sm.qfrag[s][lane][0]);
-    qa[s][0] = v.x;
-    qa[s][1] = v.y;
-    qa[s][2] = v.z;
-    qa[s][3] = v.w;
-  }
-  __syncthreads();  // qfrag aliases the merge buffers
+  const uint4* qa_s = reinterpret_cast<const uint4*>(qfrag) + lane;  // + 32 * s
   float qs0 = 0.f, qs1 = 0.f;
   for (int bq = 0; bq < D / 32; ++bq) {
     if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][j];
@@ -230,17 +241,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
 
   // ------------------------------------------------------ page pipeline
-  const int first_page = rg.sink_end / kPage;
-  const int end_page = (rg.rec_start + kPage - 1) / kPage;
-  const int p_lo = first_page + split * pages_per_split;
-  const int p_hi = min(end_page, p_lo + pages_per_split);
   const int n_my = rg.rec_start > rg.sink_end && p_hi > p_lo + warp
                        ? (p_hi - p_lo - warp + kWarps - 1) / kWarps
                        : 0;
-  uint8_t* my_stages = stage_base + (size_t)warp * kStages * cb;
+  uint8_t* my_stages = stage_base + (size_t)warp * kStagesMma * cb;
   const int32_t* bt_row = block_table + (long long)b * L.max_pages;
   if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+    for (int st = 0; st < kStagesMma; ++st) mbar_init(&sm.bar[warp][st], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -248,23 +255,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   // read one iteration before its copy is issued, so the issue never waits
   // on global-memory latency.
   auto issue = [&](int i, int phys) {
-    uint64_t* bar = &sm.bar[warp][i % kStages];
+    uint64_t* bar = &sm.bar[warp][i % kStagesMma];
     const bool good = phys >= 0 && phys < L.num_pages;
-    sm.phys[warp][i % kStages] = good ? phys : -1;  // published by the arrive below
+    sm.phys[warp][i % kStagesMma] = good ? phys : -1;  // published by the arrive below
     if (good) {
-      fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, (uint32_t)cb);
-      bulk_g2s(my_stages + (size_t)(i % kStages) * cb,
+      bulk_g2s(my_stages + (size_t)(i % kStagesMma) * cb,
                paged + ((long long)phys * L.h_kv + h) * cb, (uint32_t)cb, bar);
     } else {
       set_status(status, KV4_STATUS_BAD_PAGE);
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
     }
   };
-  int next_phys = -1;  // lane 0: block-table entry of page i + kStages
+  int next_phys = -1;  // lane 0: block-table entry of page i + kStagesMma
   if (lane == 0) {
-    for (int i = 0; i < min(kStages, n_my); ++i) issue(i, bt_row[p_lo + warp + i * kWarps]);
-    if (kStages < n_my) next_phys = bt_row[p_lo + warp + kStages * kWarps];
+    for (int i = 0; i < min(kStagesMma, n_my); ++i) issue(i, bt_row[p_lo + warp + i * kWarps]);
+    if (kStagesMma < n_my) next_phys = bt_row[p_lo + warp + kStagesMma * kWarps];
   }
 
   // ldmatrix row addresses (relative to the V code block): matrix mi = lane/8
@@ -280,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
   for (int i = 0; i < n_my; ++i) {
     const int pg = p_lo + warp + i * kWarps;
     const bool ok =
-        __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStages], (i / kStages) & 1));
-    const bool valid = ok && sm.phys[warp][i % kStages] >= 0;
+        __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][i % kStagesMma], (i / kStagesMma) & 1));
+    const bool valid = ok && sm.phys[warp][i % kStagesMma] >= 0;
     if (!ok && lane == 0) set_status(status, KV4_STATUS_BAD_PAGE);
-    const uint8_t* chunk = my_stages + (size_t)(i % kStages) * cb;
+    const uint8_t* chunk = my_stages + (size_t)(i % kStagesMma) * cb;
     if (valid) {
       // slots at or beyond the sequence length were never written: their
       // metadata may be any bit pattern, so it is zeroed before use
@@ -292,19 +298,26 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + row_byte(16 * qd, r, D));
       const uint4 k1 =
           *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + row_byte(16 * qd, r + 8, D));
+      // four independent accumulator chains (tokens 0-7 / 8-15 x even / odd
+      // k-steps), summed afterwards
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         uint32_t x0[4], x1[4];
         widen_k(u4word(k0, u), x0);
         widen_k(u4word(k1, u), x1);
+        const uint4 qa0 = qa_s[32 * (2 * u)], qa1 = qa_s[32 * (2 * u + 1)];
         // k-steps 2u and 2u+1 use pairs (0,1) and (2,3) of word u
-        mma_f16(d0, qa[2 * u][0], qa[2 * u][1], qa[2 * u][2], qa[2 * u][3], x0[0], x0[1]);
-        mma_f16(d1, qa[2 * u][0], qa[2 * u][1], qa[2 * u][2], qa[2 * u][3], x1[0], x1[1]);
-        mma_f16(d0, qa[2 * u + 1][0], qa[2 * u + 1][1], qa[2 * u + 1][2], qa[2 * u + 1][3], x0[2],
-                x0[3]);
-        mma_f16(d1, qa[2 * u + 1][0], qa[2 * u + 1][1], qa[2 * u + 1][2], qa[2 * u + 1][3], x1[2],
-                x1[3]);
+        mma_f16(d0, qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
+        mma_f16(d1, qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
+        mma_f16(e0, qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
+        mma_f16(e1, qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        d0[k] += e0[k];
+        d1[k] += e1[k];
       }
       // ---------------- scores (eq. 5.1 per group) for this lane's 4 tokens
       const float draw0[4] = {d0[0], d0[1], d1[0], d1[1]};  // row r   (group g0)
@@ -335,6 +348,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
         for (int e = 0; e < 4; ++e) {
           const int pos = pg * kPage + tk[e];
           if (!(pos >= rg.sink_end && pos < rg.rec_start)) sc[e] = -INFINITY;
+        }
+      }
+      // metadata for PV, loaded early so its latency overlaps the softmax
+      MetaRow<NG> vm[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
+      uint32_t mtw[4][NGH];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
+        if (NGH == 2) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(row);
+          mtw[e][0] = v2.x;
+          mtw[e][NGH - 1] = v2.y;
+        } else {
+          mtw[e][0] = *reinterpret_cast<const uint32_t*>(row);
         }
       }
       // ---------------- online softmax for head j over this page
@@ -374,9 +403,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       const uint32_t vbase = smem_u32(chunk + codes_off_v(D));
       ldsm_x4_trans(va, vbase + lm_off0);  // pieces 0,1: (tok lo, P0) (tok hi, P0) (lo, P1) (hi, P1)
       ldsm_x4_trans(vb, vbase + lm_off1);  // pieces 2,3
-      MetaRow<NG> vm[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
       if (tail) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -386,23 +412,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       // handles groups [mt_g0, mt_g0 + NGH)
       if (mt_on) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
-          uint32_t w[NGH];
-          if (NGH == 2) {
-            const uint2 v2 = *reinterpret_cast<const uint2*>(row);
-            w[0] = v2.x;
-            w[NGH - 1] = v2.y;
-          } else {
-            w[0] = *reinterpret_cast<const uint32_t*>(row);
-          }
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
           for (int gi = 0; gi < NGH; ++gi) {
-            const float2 dm = h2f2(tail && pg * kPage + tk[e] >= len ? 0u : w[gi]);
+            const float2 dm = h2f2(tail && pg * kPage + tk[e] >= len ? 0u : mtw[e][gi]);
             mt_d[gi] = fmaf(p[e], dm.x, mt_d[gi]);
             mt_m[gi] = fmaf(p[e], dm.y, mt_m[gi]);
           }
-        }
       }
       // P' = p * Delta_v per group, formed in fp16x2 (token pairs)
       const uint32_t p01 = pack_f16(p[0], p[1]) & p_keep;
@@ -422,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
       }
     }
     __syncwarp();
-    if (lane == 0 && i + kStages < n_my) {
-      issue(i + kStages, next_phys);
-      if (i + kStages + 1 < n_my) next_phys = bt_row[p_lo + warp + (i + kStages + 1) * kWarps];
+    if (lane == 0 && i + kStagesMma < n_my) {
+      issue(i + kStagesMma, next_phys);
+      if (i + kStagesMma + 1 < n_my) next_phys = bt_row[p_lo + warp + (i + kStagesMma + 1) * kWarps];
     }
   }
 
@@ -476,7 +492,8 @@ cudaError_t launch_mma_t(const Layout& L, const void* paged, const void* side, c
                          float* part_o, float* part_lse, int32_t* tickets, uint16_t* out,
                          float* out_lse, int32_t* status, cudaStream_t st) {
   constexpr int cb = 16 * D128 + 128 * NG;
-  const size_t smem = ((sizeof(Smem<D128, G4>) + 127) / 128) * 128 + (size_t)kWarps * kStages * cb;
+  const size_t smem = ((sizeof(Smem<D128, G4>) + 127) / 128) * 128 +
+                      (size_t)kWarps * kStagesMma * cb + 8 * 32 * 4 * sizeof(uint32_t);
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<NG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
