@@ -45,9 +45,15 @@
  *     Position p of request slot s lives in page block_table[s][p / 16],
  *     slot p % 16.
  *     chunk bytes = 16*head_dim + 128*head_dim/g  (2560 at d=128, g=32).
- *   side cache   = [max_seqs][num_kv_heads][block], NS = sink + recent
+ *   side cache   = [max_seqs][num_kv_heads][block], NS = sink + recent,
+ *                  NSP = NS rounded up to a multiple of 8
  *     block      = K8 codes [NS][head_dim] int8, V8 codes [NS][head_dim] int8,
- *                  K8 scale [NS] fp16, V8 scale [NS] fp16, zero pad to 16 bytes.
+ *                  K8 scale [NSP] fp16, V8 scale [NSP] fp16 (entries NS..NSP-1
+ *                  are padding, never written), 2*NS*head_dim + 4*NSP bytes;
+ *                  every 8-slot run of codes or scales starts 16-byte aligned.
+ *     An INT8 code row (one slot) is cut into 16-byte pieces of 16 channels;
+ *     piece P of slot t is stored at piece position P ^ (t % (head_dim/16)),
+ *     so that reads of one piece across 8 consecutive slots hit distinct banks.
  *     Sink position p < S uses slot p; position p >= S uses ring slot
  *     S + (p mod R).  All multi-byte fields are little-endian.
  *   bf16 comparator cache = [num_pages][num_kv_heads][2 (K,V)][16][head_dim] bf16.
@@ -71,7 +77,7 @@
 extern "C" {
 #endif
 
-#define KV4_ABI_VERSION 1
+#define KV4_ABI_VERSION 2
 
 /* host return codes */
 #define KV4_OK 0
@@ -108,16 +114,21 @@ int kv4_abi_version(void);
 const char* kv4_status_string(int code);
 
 /* Decode kernel selection (process-wide; default KV4_KERNEL_AUTO).  AUTO picks
- * the fastest kernel measured on GB300 for the layout: the warp-level
- * tensor-core (mma.sync) kernel for head_dim 128 with 4 query heads per kv
- * head, the CUDA-core kernel otherwise.  TCGEN05 selects the tensor-memory
- * (tcgen05.mma) kernel, MMA_SYNC the warp-level one, CUDA_CORE the fp32 one
- * (all compute the same result within the stated tolerance).  A kernel that does not support the
- * layout falls back to the CUDA-core kernel.  Returns the previous value. */
+ * the fastest kernel measured on GB300 for the layout: for head_dim 128 with 4
+ * query heads per kv head the warp-level split kernel (MMA_SYNC), the
+ * CUDA-core kernel otherwise.
+ * STREAM cuts every (sequence, kv head) into 16-token INT4 pages and 8-slot
+ * protected units and gives each CTA of a grid that fills the GPU an equal
+ * share; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.
+ * TCGEN05 selects the tensor-memory (tcgen05.mma) split kernel, MMA_SYNC the
+ * warp-level one, CUDA_CORE the fp32 one.  All compute the same result within
+ * the stated tolerance.  A kernel that does not support the layout falls back
+ * to the CUDA-core kernel.  Returns the previous value. */
 #define KV4_KERNEL_AUTO 0
 #define KV4_KERNEL_CUDA_CORE 1
 #define KV4_KERNEL_MMA_SYNC 2
 #define KV4_KERNEL_TCGEN05 3
+#define KV4_KERNEL_STREAM 4
 int kv4_set_decode_kernel(int which);
 
 /* Validate a layout; KV4_OK or a KV4_ERR_* code. */
@@ -128,9 +139,10 @@ size_t kv4_paged_cache_bytes(const kv4_layout* layout); /* INT4 pages: codes + m
 size_t kv4_side_cache_bytes(const kv4_layout* layout);  /* INT8 sink + ring, per slot */
 size_t kv4_bf16_cache_bytes(const kv4_layout* layout);  /* comparator pages */
 
-/* Number of context splits per (sequence, kv head) that kv4_decode_attn uses
+/* Number of context splits per (sequence, kv head) that the split kernels use
  * for `num_seqs` sequences when given `max_splits` (0 = automatic), and the
- * workspace (device scratch: partial outputs and log-normalisers) it needs. */
+ * workspace (device scratch: partial outputs, log-normalisers and completion
+ * counters) kv4_decode_attn needs with that max_splits, for any kernel choice. */
 int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 

@@ -30,6 +30,11 @@ cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uin
                               const int32_t*, int, const int32_t*, float, int, int, int, int,
                               float*, float*, int32_t*, uint16_t*, float*, int32_t*,
                               cudaStream_t);
+bool stream_supported(const Layout&);
+long long stream_partials(const Layout&, int);
+cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
+                                 const int32_t*, int, const int32_t*, float, float*, float*,
+                                 int32_t*, uint16_t*, float*, int32_t*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -92,10 +97,25 @@ struct Workspace {
   size_t bytes;
 };
 static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, void* base) {
+// Partial results per query row: the split plan's, or (max_splits = 0, a
+// layout the work-balanced kernel serves) the larger of that and the
+// work-balanced kernel's partial count spread over the rows.
+static size_t parts_per_row(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
+  size_t n = (size_t)p.total();
+  const Layout L = to_layout(l);
+  if (max_splits == 0 && stream_supported(L) && num_seqs > 0) {
+    const size_t groups = (size_t)num_seqs * l->num_kv_heads;  // rows = groups * G
+    const size_t s = ((size_t)stream_partials(L, num_seqs) + groups - 1) / groups;
+    if (s > n) n = s;
+  }
+  return n;
+}
+static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits,
+                           void* base) {
   const size_t rows = (size_t)num_seqs * l->num_q_heads;
-  const size_t o = round256(rows * p.total() * l->head_dim * sizeof(float));
-  const size_t z = round256(rows * p.total() * sizeof(float));
+  const size_t np = parts_per_row(l, num_seqs, p, max_splits);
+  const size_t o = round256(rows * np * l->head_dim * sizeof(float));
+  const size_t z = round256(rows * np * sizeof(float));
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
   w.bytes = o + z + round256(w.ticket_bytes);
@@ -104,8 +124,8 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, voi
   w.tickets = (int32_t*)((char*)base + o + z);
   return w;
 }
-static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p) {
-  return ws_layout(l, num_seqs, p, nullptr).bytes;
+static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
+  return ws_layout(l, num_seqs, p, max_splits, nullptr).bytes;
 }
 
 }  // namespace kv4
@@ -118,7 +138,7 @@ int kv4_abi_version(void) { return KV4_ABI_VERSION; }
 
 int kv4_set_decode_kernel(int which) {
   const int prev = g_decode_kernel;
-  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_TCGEN05) g_decode_kernel = which;
+  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_STREAM) g_decode_kernel = which;
   return prev;
 }
 
@@ -177,7 +197,7 @@ int32_t kv4_num_splits(const kv4_layout* l, int32_t num_seqs, int32_t max_splits
 
 size_t kv4_workspace_bytes(const kv4_layout* l, int32_t num_seqs, int32_t max_splits) {
   if (kv4_check_layout(l) != KV4_OK || num_seqs < 0) return 0;
-  return ws_bytes(l, num_seqs, make_plan(l, num_seqs, max_splits, true));
+  return ws_bytes(l, num_seqs, make_plan(l, num_seqs, max_splits, true), max_splits);
 }
 
 int kv4_quant_append(const kv4_layout* l, void* paged, void* side, const uint16_t* k_new,
@@ -211,8 +231,8 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   if (!aligned16(paged) || !aligned16(side) || !aligned16(q) || !aligned16(workspace))
     return KV4_ERR_INVALID_ARG;
   const Plan p = make_plan(l, num_seqs, max_splits, true);
-  if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
-  const Workspace w = ws_layout(l, num_seqs, p, workspace);
+  if (workspace_bytes < ws_bytes(l, num_seqs, p, max_splits)) return KV4_ERR_WORKSPACE;
+  const Workspace w = ws_layout(l, num_seqs, p, max_splits, workspace);
   cudaStream_t st = (cudaStream_t)stream;
   const Layout L = to_layout(l);
   // Completion tickets for the fused eq. A1 merge start at zero on every call.
@@ -222,9 +242,14 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   // splits in the last-finishing CTA of each (sequence, kv head).
   int which = g_decode_kernel;
   if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_MMA_SYNC;  // fastest measured on GB300
+  if (which == KV4_KERNEL_STREAM && (max_splits > 0 || !stream_supported(L)))
+    which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
   cudaError_t e;
-  if (which == KV4_KERNEL_TCGEN05)
+  if (which == KV4_KERNEL_STREAM)
+    e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
+                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, st);
+  else if (which == KV4_KERNEL_TCGEN05)
     e = launch_decode_tc(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                          p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
                          w.tickets, out, out_lse, dev_status, st);
@@ -277,8 +302,9 @@ int kv4_bf16_decode_attn(const kv4_layout* l, const void* cache, const uint16_t*
   if (!cache || !q || !seq_lens || !block_table || !workspace || !out) return KV4_ERR_INVALID_ARG;
   if (!aligned16(cache) || !aligned16(q) || !aligned16(workspace)) return KV4_ERR_INVALID_ARG;
   const Plan p = make_plan(l, num_seqs, max_splits, false);
-  if (workspace_bytes < ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
-  const Workspace w = ws_layout(l, num_seqs, p, workspace);
+  // the comparator runs split kernels only: size as for a fixed split count
+  if (workspace_bytes < ws_bytes(l, num_seqs, p, -1)) return KV4_ERR_WORKSPACE;
+  const Workspace w = ws_layout(l, num_seqs, p, -1, workspace);
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
   cudaError_t e = launch_bf16_decode(to_layout(l), cache, q, seq_lens, num_seqs, block_table,

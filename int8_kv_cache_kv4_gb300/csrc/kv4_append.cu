@@ -182,10 +182,11 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
       const int ss = side_slot(p, L.S, L.R);
       uint8_t* blk = side + ((long long)s * L.h_kv + h) * side_block_bytes(d_h, L.S, L.R);
       if (active)
-        *reinterpret_cast<uint32_t*>(blk + (long long)kv * NS * d_h + (long long)ss * d_h + c0) =
-            c8;
+        *reinterpret_cast<uint32_t*>(blk + (long long)kv * NS * d_h + (long long)ss * d_h +
+                                     side_byte(c0, ss, d_h)) = c8;
       if (lane == 0)
-        *reinterpret_cast<uint16_t*>(blk + 2LL * NS * d_h + (long long)kv * NS * 2 + ss * 2) = s16;
+        *reinterpret_cast<uint16_t*>(blk + 2LL * NS * d_h +
+                                     (long long)kv * side_scale_entries(L.S, L.R) * 2 + ss * 2) = s16;
     }
   }
   if (bad && lane == 0) set_status(status, KV4_STATUS_NONFINITE);

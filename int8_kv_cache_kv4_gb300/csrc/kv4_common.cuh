@@ -28,11 +28,23 @@ __host__ __device__ inline int row_byte(int b, int t, int d_h) {
   return 16 * ((b >> 4) ^ ((t >> 1) & (np - 1))) + (b & 15);
 }
 
-// Side-cache block of one (slot, kv head).
-__host__ __device__ inline long long side_block_bytes(int d_h, int S, int R) {
-  long long b = (long long)(S + R) * (2LL * d_h + 4);
-  return (b + 15) / 16 * 16;
+// Byte offset of channel c inside an INT8 side-cache code row of slot t: the
+// row's 16-byte pieces (16 channels each) are XOR-swizzled by the slot.
+__host__ __device__ inline int side_byte(int c, int t, int d_h) {
+  return 16 * ((c >> 4) ^ (t & (d_h / 16 - 1))) + (c & 15);
 }
+
+// Side-cache block of one (slot, kv head): K8 codes [NS][d_h], V8 codes
+// [NS][d_h], K8 scales [NSP], V8 scales [NSP] with NSP = NS rounded up to 8,
+// so that every 8-slot run of codes or scales starts on a 16-byte boundary.
+__host__ __device__ inline int side_scale_entries(int S, int R) { return (S + R + 7) / 8 * 8; }
+__host__ __device__ inline long long side_block_bytes(int d_h, int S, int R) {
+  return 2LL * (S + R) * d_h + 4LL * side_scale_entries(S, R);
+}
+
+// Upper bound on the grid of the work-balanced decode kernel (it sizes the
+// grid to the resident-CTA capacity of the GPU, 760 on a 152-SM GB300).
+constexpr int kMaxStreamCtas = 1024;
 
 struct Layout {
   int h_q, h_kv, d_h, g, S, R;

@@ -327,7 +327,7 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
   const int8_t* k8 = reinterpret_cast<const int8_t*>(blk);
   const int8_t* v8 = reinterpret_cast<const int8_t*>(blk + (long long)NS * D);
   const uint16_t* ks = reinterpret_cast<const uint16_t*>(blk + 2LL * NS * D);
-  const uint16_t* vs = ks + NS;
+  const uint16_t* vs = ks + side_scale_entries(L.S, L.R);
   constexpr int PD = D / 32;
   for (int base = i_lo + warp * 16; base < i_hi; base += kWarps * 16) {
     const int i = base + t;
@@ -336,9 +336,14 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
     const int ntok = min(16, i_hi - base);
     // every global load of this 16-position block is issued before any use;
     // V scales stay packed as fp16 pairs to keep the register count down
-    const uint4* krow = reinterpret_cast<const uint4*>(k8 + (long long)slot * D + half * (D / 2));
-    uint4 kraw0 = tok_ok ? krow[0] : make_uint4(0u, 0u, 0u, 0u);
-    uint4 kraw1 = tok_ok ? krow[1] : make_uint4(0u, 0u, 0u, 0u);
+    // this lane's half of the K row: pieces half*D/32 + i, stored swizzled
+    const int8_t* krow = k8 + (long long)slot * D;
+    auto kpiece = [&](int i) {
+      return tok_ok ? *reinterpret_cast<const uint4*>(krow + side_byte(16 * (half * (D / 32) + i), slot, D))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint4 kraw0 = kpiece(0);
+    uint4 kraw1 = kpiece(1);
     const float ksc = tok_ok ? f16_bits_to_f32(ks[slot]) : 0.f;
     uint32_t vword[16];
     uint32_t vsc2[8];
@@ -351,10 +356,11 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
         vsc2[tt >> 1] |= sbits << 16;
       else
         vsc2[tt >> 1] = sbits;
+      const int8_t* vp = v8 + (long long)slot2 * D + side_byte(lane * PD, slot2, D);
       if (PD == 4)
-        vword[tt] = ok ? *reinterpret_cast<const uint32_t*>(v8 + (long long)slot2 * D + lane * PD) : 0u;
+        vword[tt] = ok ? *reinterpret_cast<const uint32_t*>(vp) : 0u;
       else
-        vword[tt] = ok ? *reinterpret_cast<const uint16_t*>(v8 + (long long)slot2 * D + lane * PD) : 0u;
+        vword[tt] = ok ? *reinterpret_cast<const uint16_t*>(vp) : 0u;
     }
     float s[G];
 #pragma unroll
@@ -362,8 +368,8 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
 #pragma unroll
     for (int w = 0; w < D / 32; ++w) {
       if (w == 2) {  // second half of this lane's 64 channels
-        kraw0 = tok_ok ? krow[2] : make_uint4(0u, 0u, 0u, 0u);
-        kraw1 = tok_ok ? krow[3] : make_uint4(0u, 0u, 0u, 0u);
+        kraw0 = kpiece(2);
+        kraw1 = kpiece(3);
       }
       const uint4 kr = (w & 1) ? kraw1 : kraw0;
       const uint32_t words[4] = {kr.x, kr.y, kr.z, kr.w};
@@ -388,7 +394,6 @@ __device__ inline void prot_split(Smem<D, G>& sm, WarpState<D, G>& ws, const Lay
     for (int tt = 0; tt < 16; ++tt) {
       if (tt < ntok) {
         float v[PD];
-#pragma unroll
         const float vsc = f16_bits_to_f32((vsc2[tt >> 1] >> (16 * (tt & 1))) & 0xFFFFu);
 #pragma unroll
         for (int ii = 0; ii < PD; ++ii) v[ii] = vsc * (float)(int8_t)((vword[tt] >> (8 * ii)) & 0xFFu);

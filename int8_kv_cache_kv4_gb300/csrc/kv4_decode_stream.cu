@@ -1,0 +1,974 @@
+// kv4_decode_stream.cu -- work-balanced persistent decode over the mixed
+// INT4 / INT8 cache (KV4-RL Sec. 5.3 and eq. 5.1; App. A.3 "Protected path"
+// and eq. A1), head_dim 128 with 4 query heads per kv head.
+//
+// Work is one stream of units over all (sequence, kv head) pairs.  For each
+// pair, in order: its protected units (8 consecutive INT8 side-cache slots
+// each, the sink slots and the recent-window ring), then one unit per
+// 16-token INT4 page of the region between the sinks and the recent window.
+// A pair's protected units form one segment of the stream, its INT4 units a
+// second.  The grid is sized to fill the GPU once, and CTA c takes the units
+// [c*U/C, (c+1)*U/C) of the U units in the stream (C = min(grid, U)), so all
+// CTAs carry the same work.
+//
+// Inside a CTA the four warps take the units of the current segment
+// round-robin; each warp streams its units through its own two-stage ring of
+// bulk copies, issued ahead across segment boundaries.  When a segment ends
+// the warps' online-softmax states are merged into one partial result (a
+// locally normalised output and its log-normaliser) for the pair's four query
+// heads.  The CTA that stores the last partial of a pair merges them (eq. A1)
+// into the output.  The CTA holding units of segment s (s = 2 * pair + region)
+// writes partial s + c: CTA ranges are contiguous, ordered and non-empty, so
+// these indices are distinct and below 2 * pairs + C.
+//
+// Per-unit math on the tensor cores (m16n8k16, fp16 operands, fp32
+// accumulation):
+//  INT4 page: as in the split kernel -- block-diagonal query rows against the
+//    widened 4-bit K codes, scores by eq. 5.1 per group, then the transposed
+//    centred V codes against P' = p * Delta_v plus the offset term.
+//  INT8 unit: the query (rows = heads) against the 8 slots' K codes widened
+//    exactly to fp16, scores scaled by each slot's K scale; then the
+//    transposed V codes against P' = p * s_v.  Slots outside the protected
+//    set (not yet written, or outside the final recent window) are masked.
+#include <algorithm>
+
+#include "kv4_decode_common.cuh"
+#include "kv4_mma.cuh"
+
+namespace kv4 {
+namespace {
+
+constexpr int SD = 128, SG = 4;     // head_dim, query heads per kv head
+constexpr int kSStages = 2;         // bulk-copy stages per warp
+constexpr int kProtUnit = 8;        // side-cache slots per protected unit
+constexpr int kStreamMinBlocks = 5; // CTAs per SM the register budget targets
+
+// One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
+struct Seg {
+  long long start;  // stream index of its first unit
+  int b, h, type, len, n;
+};
+
+// Producer cursor of one warp: the next unit (segment, index) to copy in.
+struct Prod {
+  Seg s;
+  int j;     // unit index inside segment s
+  int more;  // a next unit exists
+};
+
+// A pair whose partial results are to be merged, with where they are.
+struct Pend {
+  long long row0;      // first output row (sequence * h_q + kv head * G)
+  long long s0;        // partial index base of the protected segment (= 2 * pair)
+  int pair, type, c0, n0, c1, n1, valid;
+};
+
+struct __align__(16) StreamSmem {
+  uint32_t qfrag4[8][32][4];        // INT4 path: block-diagonal query fragments
+  uint2 qfrag8[8][32];              // INT8 path: query fragments (a0, a2), rows = heads
+  float mrg_o[kWarps][SG][SD];      // per-warp unnormalised outputs at a segment end
+  uint16_t qh[SG][SD];              // query of the current pair as fp16 bits
+  uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
+  float qsum[SD / 32][SG];          // per 32-channel block sums of the query
+  float mrg_m[kWarps][SG];
+  float mrg_l[kWarps][SG];
+  float mrg_mt[kWarps][SG][SD / 32];
+  long long scan[kThreads];         // per-thread unit counts, then their exclusive prefix
+  long long total;
+  long long start_pre;              // stream index of the first unit of sequence start_b
+  long long u_begin, u_end;         // this CTA's share of the stream
+  Seg cs;                           // first segment of this CTA
+  Prod prod[kWarps];
+  Seg nx;                           // segment after cs (thread 0, at segment start)
+  Pend pcur;                        // partial bookkeeping of segment cs (thread 0)
+  Pend pend;                        // partial whose ticket is in flight (thread 0)
+  Pend comb;                        // pair to merge at this boundary
+  int go;                           // comb is valid
+  int start_b;
+  int32_t phys[kWarps][kSStages];   // INT4 stage: physical page, -1 = not loaded
+  uint64_t bar[kWarps][kSStages];
+  uint64_t qbar;                    // completion of the qraw copy
+};
+
+__device__ inline int clamp_len(int len, const Layout& L) {
+  return (len < 0 || len > L.max_pages * kPage) ? 0 : len;
+}
+// protected units of a sequence of length len: the sink slots alone while
+// len <= S, else every side slot (the ring is masked to the window)
+__device__ inline int prot_units(int len, const Layout& L) {
+  if (len <= 0) return 0;
+  const int ns = len <= L.S ? len : L.S + L.R;
+  return (ns + kProtUnit - 1) / kProtUnit;
+}
+__device__ inline int int4_units(int len, const Layout& L) {
+  const Regions rg = regions(len, L.S, L.R);
+  return rg.rec_start > rg.sink_end ? (rg.rec_start + kPage - 1) / kPage - rg.sink_end / kPage
+                                    : 0;
+}
+
+// Next non-empty segment (b == B when the stream is exhausted).
+__device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B) {
+  do {
+    s.start += s.n;
+    if (s.type == 0) {
+      s.type = 1;
+      s.n = int4_units(s.len, L);
+    } else {
+      s.type = 0;
+      if (++s.h == L.h_kv) {
+        s.h = 0;
+        ++s.b;
+        s.len = s.b < B ? clamp_len(__ldg(seq_lens + s.b), L) : 0;
+      }
+      s.n = prot_units(s.len, L);
+    }
+  } while (s.n == 0 && s.b < B);
+}
+
+// Atomic add with release semantics at GPU scope; returns the old value.
+__device__ inline int atom_add_release_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// CTA holding stream unit u when U >= C units are split over C CTAs as
+// [c*U/C, (c+1)*U/C) (every CTA then holds at least one unit).
+__device__ inline int cta_of(long long u, long long U, int C) {
+  return (int)(((u + 1) * C - 1) / U);
+}
+
+// Is side slot sl part of the protected set of a sequence of length len?
+// Sinks: sl < min(S, len).  Ring slot S + r: holds a position p of the final
+// window [ws, len) with p = r (mod R).
+__device__ inline bool slot_valid(int sl, int len, const Layout& L, int ws_mod, int n_rec) {
+  if (sl < L.S) return sl < len;
+  if (sl >= L.S + L.R) return false;
+  int d = sl - L.S - ws_mod;
+  if (d < 0) d += L.R;
+  return d < n_rec;
+}
+
+// Query of pair `row0` (G consecutive bf16 rows of D) -> fp16 copy, per-block
+// sums and both fragment sets.  Every warp must be past its last use of the
+// previous query (the caller's barrier).
+// Thread 0: start the bulk copy of pair `row0`'s query (G rows of D bf16,
+// 1 KB, 16-byte aligned) into sm.qraw; it completes on sm.qbar.
+__device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __restrict__ q,
+                                          long long row0) {
+  mbar_arrive_expect_tx(&sm.qbar, SG * SD * 2);
+  bulk_g2s(sm.qraw, q + row0 * SD, SG * SD * 2, &sm.qbar);
+}
+
+// sm.qraw (after its copy completed) -> fp16 copy and per-32-channel-block
+// sums.  No warp may still read qh or qsum (they are read only when a
+// segment starts).
+__device__ inline void stream_query_store(StreamSmem& sm) {
+  const int t = threadIdx.x;
+  const int j = t >> 5, d0 = 4 * (t & 31);
+  const uint2 raw = reinterpret_cast<const uint2*>(sm.qraw)[t];
+  const float x0 = bf16_bits_to_f32(raw.x & 0xFFFFu), x1 = bf16_bits_to_f32(raw.x >> 16);
+  const float x2 = bf16_bits_to_f32(raw.y & 0xFFFFu), x3 = bf16_bits_to_f32(raw.y >> 16);
+  *reinterpret_cast<uint2*>(&sm.qh[j][d0]) = make_uint2(pack_f16(x0, x1), pack_f16(x2, x3));
+  float s = (x0 + x1) + (x2 + x3);
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  if ((t & 7) == 0) sm.qsum[(t & 31) >> 3][j] = s;
+}
+
+// Both fragment sets from qh (after a barrier that follows stream_query_store;
+// no warp may still read the fragments).
+template <int NG>
+__device__ inline void stream_build_frags(StreamSmem& sm) {
+  constexpr int GS = SD / NG;
+  const int t = threadIdx.x;
+  // INT4 fragments: A rows (group, head), block diagonal; k-index order as the
+  // widened K words produce it (see the split kernel)
+  for (int idx = t; idx < 8 * 32 * 4; idx += kThreads) {
+    const int s_ = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
+    const int rr = ln >> 2, qq = ln & 3;
+    const int row = rr + 8 * (k & 1);
+    const int grp = row >> 2, jj = row & 3;
+    const int base = 32 * qq + 8 * (s_ >> 1) + 2 * (s_ & 1) + ((k & 2) ? 1 : 0);
+    uint32_t w = 0u;
+    if (grp < NG) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int d = base + 4 * e2;
+        if (d / GS == grp) w |= (uint32_t)sm.qh[jj][d] << (16 * e2);
+      }
+    }
+    sm.qfrag4[s_][ln][k] = w;
+  }
+  // INT8 fragments: A rows = heads 0..3; k-step s, lane quad qd covers
+  // channels 32*qd + 4*s + {0,1} (a0) and + {2,3} (a2)
+  for (int idx = t; idx < 8 * 32; idx += kThreads) {
+    const int s_ = idx >> 5, ln = idx & 31;
+    const int rr = ln >> 2, qq = ln & 3;
+    uint2 w = make_uint2(0u, 0u);
+    if (rr < SG) w = *reinterpret_cast<const uint2*>(&sm.qh[rr][32 * qq + 4 * s_]);
+    sm.qfrag8[s_][ln] = w;
+  }
+}
+
+// Merge the warps' states of one segment and store its partial result P
+// (after a barrier that follows every warp's publish).  Warp j merges query
+// head j: the four warps' weights 2^(m_w - M) / L are formed once, then each
+// lane combines four channels.
+__device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ part_o,
+                                          float* __restrict__ part_lse, long long P) {
+  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float mw = lane < kWarps ? sm.mrg_m[lane][j] : -INFINITY;
+  const float lw = lane < kWarps ? sm.mrg_l[lane][j] : 0.f;
+  float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+  M = __shfl_sync(0xffffffffu, M, 0);
+  const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+  float Lt = e * lw;
+  Lt += __shfl_xor_sync(0xffffffffu, Lt, 1);
+  Lt += __shfl_xor_sync(0xffffffffu, Lt, 2);
+  Lt = __shfl_sync(0xffffffffu, Lt, 0);
+  const bool empty = !(Lt > 0.f);
+  const float f = empty ? 0.f : e / Lt;  // lanes 0..3: weight of warp `lane`
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float fw = __shfl_sync(0xffffffffu, f, w);
+    const float4 a = reinterpret_cast<const float4*>(&sm.mrg_o[w][j][0])[lane];
+    const float mt = sm.mrg_mt[w][j][lane >> 3];  // channels 4*lane.. lie in block lane/8
+    o.x = fmaf(fw, a.x + mt, o.x);
+    o.y = fmaf(fw, a.y + mt, o.y);
+    o.z = fmaf(fw, a.z + mt, o.z);
+    o.w = fmaf(fw, a.w + mt, o.w);
+  }
+  reinterpret_cast<float4*>(part_o + (P * SG + j) * SD)[lane] = o;
+  if (lane == 0) part_lse[P * SG + j] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+}
+
+// Eq. A1 over the n0 + n1 partials of one pair (partials s0 + c0 + k, then
+// s1 + c1 + k); warp j merges query head j.
+__device__ inline void stream_combine(const float* __restrict__ part_o,
+                                      const float* __restrict__ part_lse, long long s0, int c0,
+                                      int n0, long long s1, int c1, int n1, long long row0,
+                                      uint16_t* __restrict__ out, float* __restrict__ out_lse) {
+  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = n0 + n1;
+  auto pidx = [&](int k) { return k < n0 ? s0 + c0 + k : s1 + c1 + (k - n0); };
+  float M = -INFINITY;
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(part_lse + pidx(k) * SG + j));
+  M = warp_max(M);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Zl = 0.f;
+  if (M != -INFINITY) {
+    for (int k0 = 0; k0 < n; k0 += 32) {
+      const int k = k0 + lane;
+      const float z = k < n ? __ldcg(part_lse + pidx(k) * SG + j) : -INFINITY;
+      const float wl = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
+      Zl += wl;
+      const int nr = min(32, n - k0);
+      for (int rr = 0; rr < nr; rr += 4) {  // four partials' loads in flight
+        float wv[4];
+        float4 o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wv[u] = __shfl_sync(0xffffffffu, wl, (rr + u) & 31);
+          const bool use = rr + u < nr && wv[u] != 0.f;
+          o[u] = use ? __ldcg(reinterpret_cast<const float4*>(part_o + (pidx(k0 + rr + u) * SG + j) * SD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!use) wv[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc.x = fmaf(wv[u], o[u].x, acc.x);
+          acc.y = fmaf(wv[u], o[u].y, acc.y);
+          acc.z = fmaf(wv[u], o[u].z, acc.z);
+          acc.w = fmaf(wv[u], o[u].w, acc.w);
+        }
+      }
+    }
+  }
+  const float Z = warp_sum(Zl);
+  const bool empty = !(Z > 0.f);
+  const float inv = empty ? 0.f : 1.f / Z;
+  const long long row = row0 + j;
+  uint16_t* o = out + row * SD + 4 * lane;  // the output need only be 2-byte aligned
+  o[0] = f32_to_bf16_bits(acc.x * inv);
+  o[1] = f32_to_bf16_bits(acc.y * inv);
+  o[2] = f32_to_bf16_bits(acc.z * inv);
+  o[3] = f32_to_bf16_bits(acc.w * inv);
+  if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kernel(
+    Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
+    const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
+    const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
+    float* __restrict__ out_lse, int32_t* status) {
+  constexpr int D = SD;
+  constexpr int GS = D / NG;  // channels per INT4 group
+  constexpr int cb = 16 * D + 128 * NG;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  StreamSmem& sm = *reinterpret_cast<StreamSmem*>(smem_raw);
+  uint8_t* stage_base = smem_raw + ((sizeof(StreamSmem) + 127) / 128) * 128;
+  const int C = gridDim.x, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ------------------------------------------ stream size and this CTA's start
+  const int per = (B + kThreads - 1) / kThreads;
+  const int b_lo = min(B, (int)threadIdx.x * per), b_hi = min(B, b_lo + per);
+  long long mine = 0;
+  bool bad_len = false;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int raw = __ldg(seq_lens + b);
+    const int len = clamp_len(raw, L);
+    bad_len |= len != raw;
+    mine += (long long)L.h_kv * (prot_units(len, L) + int4_units(len, L));
+  }
+  if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
+  sm.scan[threadIdx.x] = mine;
+  if (threadIdx.x == 0) sm.start_b = B;
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix over the 128 per-thread counts
+    long long v[4], run = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = run;
+      run += sm.scan[4 * lane + k];
+    }
+    long long incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long excl = incl - run;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sm.scan[4 * lane + k] = excl + v[k];
+    if (lane == 31) sm.total = incl;
+  }
+  __syncthreads();
+  // The stream is cut over Cw = min(C, U) CTAs, so that every working CTA
+  // holds at least one unit (the partial counts below rely on it).
+  const long long U = sm.total;
+  const int Cw = (int)min((long long)C, U);
+  const long long u_begin = c < Cw ? U * c / Cw : U, u_end = c < Cw ? U * (c + 1) / Cw : U;
+  if (u_begin < u_end) {
+    const long long ex = sm.scan[threadIdx.x];
+    if (u_begin >= ex && u_begin < ex + mine) {
+      long long pre = ex;
+      for (int b = b_lo; b < b_hi; ++b) {
+        const int len = clamp_len(__ldg(seq_lens + b), L);
+        const long long ub = (long long)L.h_kv * (prot_units(len, L) + int4_units(len, L));
+        if (u_begin < pre + ub) {
+          sm.start_b = b;
+          sm.start_pre = pre;
+          break;
+        }
+        pre += ub;
+      }
+    }
+  }
+  // sequences with nothing to attend: zero output, log-normaliser -inf
+  for (int b = c; b < B; b += C) {
+    if (clamp_len(__ldg(seq_lens + b), L) != 0) continue;
+    for (int idx = threadIdx.x; idx < L.h_q * D; idx += kThreads)
+      out[(long long)b * L.h_q * D + idx] = 0;
+    if (out_lse)
+      for (int idx = threadIdx.x; idx < L.h_q; idx += kThreads)
+        out_lse[(long long)b * L.h_q + idx] = -INFINITY;
+  }
+  if (lane == 0) {
+    for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+    if (warp == 0) mbar_init(&sm.qbar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (sm.start_b >= B) return;  // no units for this CTA
+  if (threadIdx.x == 0) {
+    Seg cs;
+    cs.b = sm.start_b;
+    cs.h = 0;
+    cs.type = 0;
+    cs.len = clamp_len(__ldg(seq_lens + cs.b), L);
+    cs.start = sm.start_pre;
+    cs.n = prot_units(cs.len, L);
+    while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
+    sm.cs = cs;
+    sm.u_begin = u_begin;
+    sm.u_end = u_end;
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------ producer (lane 0)
+  const int NS = L.S + L.R;
+  const int NSP = side_scale_entries(L.S, L.R);
+  const long long side_blk = side_block_bytes(D, L.S, L.R);
+  uint8_t* my_stages = stage_base + (size_t)warp * kSStages * cb;
+  // Producer (lane 0 of each warp; cursor in shared memory): advance to this
+  // warp's next unit, moving over segments, and start reading its
+  // block-table entry into a register, consumed only at the next issue so
+  // the load's latency is not waited for here.
+  int pphys = -1;
+  auto prod_next = [&](Prod& pr) {
+    const long long ub = sm.u_begin, ue = sm.u_end;
+    while (true) {
+      if (pr.s.b >= B || pr.s.start >= ue) {
+        pr.more = 0;
+        return;
+      }
+      if (pr.j < (int)(min(ue, pr.s.start + pr.s.n) - pr.s.start)) break;
+      seg_next(pr.s, L, seq_lens, B);
+      pr.j = (int)(max(ub, pr.s.start) - pr.s.start) + warp;
+    }
+    pr.more = 1;
+    if (pr.s.type == 1) {
+      const int pg = min(pr.s.len, L.S) / kPage + pr.j;
+      pphys = __ldg(block_table + (long long)pr.s.b * L.max_pages + pg);
+    }
+  };
+  auto issue = [&](int st) {
+    Prod& pr = sm.prod[warp];
+    const Seg& ps = pr.s;
+    const int pj = pr.j;
+    uint64_t* bar = &sm.bar[warp][st];
+    uint8_t* dst = my_stages + (size_t)st * cb;
+    if (ps.type == 1) {
+      const bool good = pphys >= 0 && pphys < L.num_pages;
+      sm.phys[warp][st] = good ? pphys : -1;  // published by the arrive below
+      if (good) {
+        mbar_arrive_expect_tx(bar, (uint32_t)cb);
+        bulk_g2s(dst, paged + ((long long)pphys * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
+      } else {
+        set_status(status, KV4_STATUS_BAD_PAGE);
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+      }
+    } else {
+      const uint8_t* blk = side + ((long long)ps.b * L.h_kv + ps.h) * side_blk;
+      const int slot0 = pj * kProtUnit;
+      const int ns = ps.len <= L.S ? ps.len : NS;
+      const uint32_t rows = (uint32_t)min(kProtUnit, ns - slot0);
+      sm.phys[warp][st] = 0;
+      mbar_arrive_expect_tx(bar, 2u * rows * D + 32u);
+      bulk_g2s(dst, blk + (long long)slot0 * D, rows * D, bar);
+      bulk_g2s(dst + kProtUnit * D, blk + (long long)(NS + slot0) * D, rows * D, bar);
+      bulk_g2s(dst + 2 * kProtUnit * D, blk + 2LL * NS * D + 2 * slot0, 16u, bar);
+      bulk_g2s(dst + 2 * kProtUnit * D + 16, blk + 2LL * NS * D + 2LL * NSP + 2 * slot0, 16u,
+               bar);
+    }
+  };
+  if (lane == 0) {
+    Prod& pr = sm.prod[warp];
+    pr.s = sm.cs;
+    pr.j = (int)(max(u_begin, pr.s.start) - pr.s.start) + warp;
+    prod_next(pr);
+    for (int st = 0; st < kSStages && pr.more; ++st) {
+      issue(st);
+      pr.j += kWarps;
+      prod_next(pr);
+    }
+  }
+  auto refill = [&](int st) {  // after the warp released stage st
+    __syncwarp();
+    if (lane == 0 && sm.prod[warp].more) {
+      issue(st);
+      Prod& pr = sm.prod[warp];
+      pr.j += kWarps;
+      prod_next(pr);
+    }
+  };
+
+  // ------------------------------------------------------ per-lane constants
+  const int r = lane >> 2, qd = lane & 3;
+  const int jh = r & 3;                 // INT4 path: this lane's softmax head
+  const int g0 = r >> 2, g1 = g0 + 2;   // INT4 path: groups of QK rows r and r+8
+  const bool v0 = g0 < NG, v1 = g1 < NG;
+  constexpr int NGH = NG > 1 ? NG / 2 : 1;
+  const int mt_g0 = (r >= 4) ? NG / 2 : 0;
+  const bool mt_on = (r < 4) || NG > 1;
+  const int tk[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
+  const uint32_t p_keep = (r < 4) ? 0xFFFFFFFFu : 0u;
+  // INT4 V ldmatrix rows: matrix lane/8 = tokens (mi&1)*8.., piece mi>>1 (+2)
+  const int lm_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int lm_p = lane >> 4;
+  const uint32_t lm_off0 = lm_tok * 64 + 16 * ((lm_p) ^ ((lm_tok >> 1) & 3));
+  const uint32_t lm_off1 = lm_tok * 64 + 16 * ((lm_p + 2) ^ ((lm_tok >> 1) & 3));
+  // INT8 V ldmatrix rows: matrix lane/8 = piece, row lane&7 = slot (swizzled)
+  const int l8_t = lane & 7, l8_m = lane >> 3;
+  const uint32_t l8_off0 = l8_t * D + 16 * ((l8_m) ^ l8_t);
+  const uint32_t l8_off1 = l8_t * D + 16 * ((l8_m + 4) ^ l8_t);
+
+  int it = 0;  // this warp's consumed units (stage it % 2, phase (it / 2) & 1)
+  int pend_t = 0;  // thread 0: ticket value returned for the pending partial
+  uint32_t qphase = 0;  // completed copies into sm.qraw
+  if (threadIdx.x == 0) {
+    sm.pend.valid = 0;
+    const Seg c0s = sm.cs;
+    stream_query_fetch(sm, q, (long long)c0s.b * L.h_q + (long long)c0s.h * SG);
+  }
+  if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
+  ++qphase;
+  stream_query_store(sm);
+  __syncthreads();
+  stream_build_frags<NG>(sm);
+  __syncthreads();
+  // The current segment lives in sm.cs (advanced by thread 0 between the
+  // boundary barriers); the loop below keeps only what the units need.
+  while (true) {
+    const Seg cs = sm.cs;
+    if (cs.b >= B || cs.start >= sm.u_end) break;
+    // the next segment's pair: read its query ahead when it changes
+    bool new_q;
+    {
+      Seg nx = cs;
+      seg_next(nx, L, seq_lens, B);
+      new_q = nx.b < B && nx.start < sm.u_end && (nx.b != cs.b || nx.h != cs.h);
+      if (threadIdx.x == 0) {
+        // the previous query copy was consumed before the last barrier
+        if (new_q) stream_query_fetch(sm, q, (long long)nx.b * L.h_q + (long long)nx.h * SG);
+        // bookkeeping for the boundary, done here so that no barrier waits on it
+        sm.nx = nx;
+        const int pair = cs.b * L.h_kv + cs.h;
+        const int np = prot_units(cs.len, L), n4 = int4_units(cs.len, L);
+        const long long gs = cs.type == 0 ? cs.start : cs.start - np;  // pair's first unit
+        const long long U = sm.total;
+        const int Cw = (int)min((long long)C, U);
+        Pend pd;
+        pd.row0 = (long long)cs.b * L.h_q + (long long)cs.h * SG;
+        pd.s0 = 2LL * pair;
+        pd.pair = pair;
+        pd.type = cs.type;
+        pd.c0 = np ? cta_of(gs, U, Cw) : 0;
+        pd.n0 = np ? cta_of(gs + np - 1, U, Cw) - pd.c0 + 1 : 0;
+        pd.c1 = n4 ? cta_of(gs + np, U, Cw) : 0;
+        pd.n1 = n4 ? cta_of(gs + np + n4 - 1, U, Cw) - pd.c1 + 1 : 0;
+        pd.valid = 1;
+        sm.pcur = pd;
+      }
+    }
+    const int lo = (int)(max(sm.u_begin, cs.start) - cs.start);
+    const int hi = (int)(min(sm.u_end, cs.start + cs.n) - cs.start);
+    const Regions rg = regions(cs.len, L.S, L.R);
+
+    if (cs.type == 1) {
+      // ============================================= INT4 pages (eq. 5.1)
+      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qfrag4[0][0][0]) + lane;
+      float qs0 = 0.f, qs1 = 0.f;
+#pragma unroll
+      for (int bq = 0; bq < D / 32; ++bq) {
+        if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][jh];
+        if (v1 && (bq * 32) / GS == g1) qs1 += sm.qsum[bq][jh];
+      }
+      const int first_page = rg.sink_end / kPage;
+      float m_run = -INFINITY, l_run = 0.f;
+      float mt_m[NGH], mt_d[NGH];
+#pragma unroll
+      for (int i = 0; i < NGH; ++i) mt_m[i] = mt_d[i] = 0.f;
+      float acc[4][2][4];
+#pragma unroll
+      for (int G_ = 0; G_ < 4; ++G_)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
+
+      for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
+        const int st = it % kSStages;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], (it / kSStages) & 1));
+        if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
+        const bool valid = ok && sm.phys[warp][st] >= 0;
+        const uint8_t* chunk = my_stages + (size_t)st * cb;
+        const int pg = first_page + jj;
+        if (valid) {
+          const bool tail = (pg + 1) * kPage > cs.len;
+          const uint4 k0 =
+              *reinterpret_cast<const uint4*>(chunk + r * 64 + row_byte(16 * qd, r, D));
+          const uint4 k1 =
+              *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + row_byte(16 * qd, r + 8, D));
+          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+          float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t x0[4], x1[4];
+            widen_k(u4word(k0, u), x0);
+            widen_k(u4word(k1, u), x1);
+            const uint4 qa0 = qa_s[32 * (2 * u)], qa1 = qa_s[32 * (2 * u + 1)];
+            mma_f16(d0, qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
+            mma_f16(d1, qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
+            mma_f16(e0, qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
+            mma_f16(e1, qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            d0[k] += e0[k];
+            d1[k] += e1[k];
+          }
+          const float draw0[4] = {d0[0], d0[1], d1[0], d1[1]};
+          const float draw1[4] = {d0[2], d0[3], d1[2], d1[3]};
+          const uint8_t* kmeta = chunk + meta_off_k(D);
+          float sc[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float part = 0.f;
+            if (v0) {
+              const float2 dm =
+                  h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g0) * 4));
+              part = fmaf(dm.x, draw0[e], dm.y * qs0);
+            }
+            if (v1) {
+              const float2 dm =
+                  h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g1) * 4));
+              part += fmaf(dm.x, draw1[e], dm.y * qs1);
+            }
+            sc[e] = part;
+          }
+          const bool interior = pg * kPage >= rg.sink_end && (pg + 1) * kPage <= rg.rec_start;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 16);
+            sc[e] *= scale_log2;
+          }
+          if (!interior) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int pos = pg * kPage + tk[e];
+              if (!(pos >= rg.sink_end && pos < rg.rec_start)) sc[e] = -INFINITY;
+            }
+          }
+          MetaRow<NG> vm[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
+          uint32_t mtw[4][NGH];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
+            if (NGH == 2) {
+              const uint2 v2 = *reinterpret_cast<const uint2*>(row);
+              mtw[e][0] = v2.x;
+              mtw[e][NGH - 1] = v2.y;
+            } else {
+              mtw[e][0] = *reinterpret_cast<const uint32_t*>(row);
+            }
+          }
+          float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+          const float mnew = fmaxf(m_run, tmax);
+          const float mref = mnew == -INFINITY ? 0.f : mnew;
+          float p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[e] = ex2(sc[e] - mref);
+          if (__any_sync(0xffffffffu, mnew > m_run)) {
+            const float alpha = ex2(m_run - mref);
+            const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
+            const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
+#pragma unroll
+            for (int G_ = 0; G_ < 4; ++G_)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                acc[G_][hh][0] *= aA;
+                acc[G_][hh][1] *= aB;
+                acc[G_][hh][2] *= aA;
+                acc[G_][hh][3] *= aB;
+              }
+#pragma unroll
+            for (int gi = 0; gi < NGH; ++gi) {
+              mt_m[gi] *= alpha;
+              mt_d[gi] *= alpha;
+            }
+            l_run *= alpha;
+            m_run = mnew;
+          }
+          l_run += (p[0] + p[1]) + (p[2] + p[3]);
+          uint32_t va[4], vb[4];
+          const uint32_t vbase = smem_u32(chunk + codes_off_v(D));
+          ldsm_x4_trans(va, vbase + lm_off0);
+          ldsm_x4_trans(vb, vbase + lm_off1);
+          if (tail) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (pg * kPage + tk[e] >= cs.len) vm[e].zero();
+          }
+          if (mt_on) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+              for (int gi = 0; gi < NGH; ++gi) {
+                const float2 dm = h2f2(tail && pg * kPage + tk[e] >= cs.len ? 0u : mtw[e][gi]);
+                mt_d[gi] = fmaf(p[e], dm.x, mt_d[gi]);
+                mt_m[gi] = fmaf(p[e], dm.y, mt_m[gi]);
+              }
+          }
+          const uint32_t p01 = pack_f16(p[0], p[1]) & p_keep;
+          const uint32_t p23 = pack_f16(p[2], p[3]) & p_keep;
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const int grp = (P * 32) / GS;
+            const uint32_t b0 = hmul2(p01, lo_lo(vm[0].get(grp), vm[1].get(grp)));
+            const uint32_t b1 = hmul2(p23, lo_lo(vm[2].get(grp), vm[3].get(grp)));
+            const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
+            const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
+            uint32_t xl[4], xh[4];
+            widen_v(wlo, xl);
+            widen_v(whi, xh);
+            mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
+            mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
+          }
+        }
+        refill(st);
+      }
+      // publish this warp's state
+      float lsum = (r < 4) ? l_run : 0.f;
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+      float mt[NGH];
+#pragma unroll
+      for (int gi = 0; gi < NGH; ++gi) {
+        mt[gi] = fmaf(8.f, mt_d[gi], mt_m[gi]);
+        mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 1);
+        mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 2);
+      }
+      if (qd == 0 && r < 4) {
+        sm.mrg_m[warp][jh] = m_run;
+        sm.mrg_l[warp][jh] = lsum;
+      }
+      if (qd == 0 && mt_on) {
+#pragma unroll
+        for (int gi = 0; gi < NGH; ++gi) {
+          const int grp = mt_g0 + gi;
+          for (int blk = grp * (GS / 32); blk < (grp + 1) * (GS / 32); ++blk)
+            sm.mrg_mt[warp][jh][blk] = mt[gi];
+        }
+      }
+      if (qd < 2) {
+        const int hA = 2 * qd, hB = 2 * qd + 1;
+#pragma unroll
+        for (int P = 0; P < 4; ++P)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int d = 32 * P + 4 * r + 2 * hh;
+            sm.mrg_o[warp][hA][d] = acc[P][hh][0];
+            sm.mrg_o[warp][hB][d] = acc[P][hh][1];
+            sm.mrg_o[warp][hA][d + 1] = acc[P][hh][2];
+            sm.mrg_o[warp][hB][d + 1] = acc[P][hh][3];
+          }
+      }
+    } else {
+      // ================================= INT8 protected units (App. A.3)
+      const int n_rec = cs.len > L.S ? cs.len - rg.rec_start : 0;
+      const int ws_mod = L.R > 0 ? rg.rec_start % L.R : 0;
+      float m8 = -INFINITY, l8 = 0.f;
+      float acc8[8][4];
+#pragma unroll
+      for (int P = 0; P < 8; ++P)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
+      for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
+        const int st = it % kSStages;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], (it / kSStages) & 1));
+        if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
+        const uint8_t* stg = my_stages + (size_t)st * cb;
+        if (ok) {
+          const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0, sl0 + 1
+          const bool ok0 = slot_valid(sl0, cs.len, L, ws_mod, n_rec);
+          const bool ok1 = slot_valid(sl0 + 1, cs.len, L, ws_mod, n_rec);
+          // ---- QK: B = K codes of slot r, channels 32*qd + [0, 32)
+          const uint8_t* krow = stg + r * D;
+          const uint4 kA = *reinterpret_cast<const uint4*>(krow + 16 * ((2 * qd) ^ r));
+          const uint4 kB = *reinterpret_cast<const uint4*>(krow + 16 * ((2 * qd + 1) ^ r));
+          float dq0[4] = {0.f, 0.f, 0.f, 0.f}, dq1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s_ = 0; s_ < 8; ++s_) {
+            const uint32_t xb = (s_ < 4 ? u4word(kA, s_) : u4word(kB, s_ - 4)) ^ 0x80808080u;
+            const uint2 qa = sm.qfrag8[s_][lane];
+            mma_f16((s_ & 1) ? dq1 : dq0, qa.x, 0u, qa.y, 0u, i8pair(xb, 0x4140u),
+                    i8pair(xb, 0x4342u));
+          }
+          // scores of head r (lanes r < 4) for slots sl0, sl0 + 1
+          const float2 ks = h2f2(*reinterpret_cast<const uint32_t*>(stg + 2 * kProtUnit * D + 4 * qd));
+          float s0 = (dq0[0] + dq1[0]) * ks.x * scale_log2;
+          float s1 = (dq0[1] + dq1[1]) * ks.y * scale_log2;
+          if (!ok0) s0 = -INFINITY;
+          if (!ok1) s1 = -INFINITY;
+          float tmax = fmaxf(s0, s1);
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+          const float mnew = fmaxf(m8, tmax);
+          const float mref = mnew == -INFINITY ? 0.f : mnew;
+          const float p0 = ex2(s0 - mref), p1 = ex2(s1 - mref);
+          if (__any_sync(0xffffffffu, mnew > m8)) {
+            const float alpha = ex2(m8 - mref);
+            const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
+            const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
+#pragma unroll
+            for (int P = 0; P < 8; ++P) {
+              acc8[P][0] *= aA;
+              acc8[P][1] *= aB;
+              acc8[P][2] *= aA;
+              acc8[P][3] *= aB;
+            }
+            l8 *= alpha;
+            m8 = mnew;
+          }
+          l8 += p0 + p1;
+          // ---- PV: A = V codes transposed (rows = channels), B = p * s_v
+          uint32_t vs2 = *reinterpret_cast<const uint32_t*>(stg + 2 * kProtUnit * D + 16 + 4 * qd);
+          vs2 &= (ok0 ? 0x0000FFFFu : 0u) | (ok1 ? 0xFFFF0000u : 0u);
+          const uint32_t pb = hmul2(pack_f16(p0, p1) & p_keep, vs2);
+          uint32_t va[4], vb[4];
+          const uint32_t vbase = smem_u32(stg + kProtUnit * D);
+          ldsm_x4_trans(va, vbase + l8_off0);  // pieces 0..3
+          ldsm_x4_trans(vb, vbase + l8_off1);  // pieces 4..7
+#pragma unroll
+          for (int P = 0; P < 8; ++P) {
+            const uint32_t xb = (P < 4 ? va[P] : vb[P - 4]) ^ 0x80808080u;
+            // rows r / r+8 = channels 16P + 2r / 16P + 2r + 1; k = slots 2qd, 2qd+1
+            mma_f16(acc8[P], i8pair(xb, 0x4240u), i8pair(xb, 0x4341u), 0u, 0u, pb, 0u);
+          }
+        }
+        refill(st);
+      }
+      // publish this warp's state
+      float lsum = (r < 4) ? l8 : 0.f;
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+      if (qd == 0 && r < 4) {
+        sm.mrg_m[warp][r] = m8;
+        sm.mrg_l[warp][r] = lsum;
+      }
+      if (lane < SG * (D / 32)) sm.mrg_mt[warp][lane / (D / 32)][lane % (D / 32)] = 0.f;
+      if (qd < 2) {
+        const int hA = 2 * qd, hB = 2 * qd + 1;
+#pragma unroll
+        for (int P = 0; P < 8; ++P) {
+          const int d = 16 * P + 2 * r;
+          sm.mrg_o[warp][hA][d] = acc8[P][0];
+          sm.mrg_o[warp][hB][d] = acc8[P][1];
+          sm.mrg_o[warp][hA][d + 1] = acc8[P][2];
+          sm.mrg_o[warp][hB][d + 1] = acc8[P][3];
+        }
+      }
+    }
+
+    // ----------------------------------------- segment end: partial + merge
+    // B1: every warp has published; merge into partial 2 * pair + region + c
+    __syncthreads();
+    // (sm.pcur is fixed until the next segment starts; thread 0 rewrites
+    // sm.cs before the next barrier)
+    stream_merge_store(sm, part_o, part_lse, sm.pcur.s0 + sm.pcur.type + c);
+    if (threadIdx.x == 0) {
+      // the previous partial's ticket (taken one segment ago) decides whether
+      // this CTA merges that pair now
+      int go = 0;
+      if (sm.pend.valid) {
+        go = pend_t == sm.pend.n0 + sm.pend.n1 - 1;
+        if (go) {
+          __threadfence();  // acquire: the other CTAs' partials are visible
+          sm.comb = sm.pend;
+        }
+      }
+      sm.go = go;
+      sm.cs = sm.nx;  // read by all after the next barrier
+    }
+    if (new_q) {
+      if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0)
+        set_status(status, KV4_STATUS_TIMEOUT);
+      ++qphase;
+      stream_query_store(sm);
+    }
+    __syncthreads();  // B2: partial stored; qh, qsum, comb and cs written
+    if (new_q) {
+      stream_build_frags<NG>(sm);
+      __syncthreads();  // B3: next pair's fragments ready
+    }
+    if (threadIdx.x == 0) {
+      // take this partial's ticket with release semantics (the barrier above
+      // makes the CTA's partial stores part of what is released); the
+      // result is read at the next boundary
+      pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], 1);
+      sm.pend = sm.pcur;
+    }
+    if (sm.go) {
+      const Pend& cm = sm.comb;
+      stream_combine(part_o, part_lse, cm.s0, cm.c0, cm.n0, cm.s0 + 1, cm.c1, cm.n1, cm.row0, out,
+                     out_lse);
+    }
+  }
+  // the last partial's ticket
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int go = 0;
+    if (sm.pend.valid) {
+      go = pend_t == sm.pend.n0 + sm.pend.n1 - 1;
+      if (go) {
+        __threadfence();
+        sm.comb = sm.pend;
+      }
+    }
+    sm.go = go;
+  }
+  __syncthreads();
+  if (sm.go) {
+    const Pend& cm = sm.comb;
+    stream_combine(part_o, part_lse, cm.s0, cm.c0, cm.n0, cm.s0 + 1, cm.c1, cm.n1, cm.row0, out,
+                   out_lse);
+  }
+}
+
+}  // namespace
+
+bool stream_supported(const Layout& L) { return L.d_h == SD && L.h_q == SG * L.h_kv; }
+
+// Partial results the stream kernel may write for num_seqs sequences.
+long long stream_partials(const Layout& L, int num_seqs) {
+  return 2LL * num_seqs * L.h_kv + kMaxStreamCtas;
+}
+
+template <int NG>
+cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side,
+                            const uint16_t* q, const int32_t* seq_lens, int num_seqs,
+                            const int32_t* block_table, float sm_scale, float* part_o,
+                            float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
+                            int32_t* status, cudaStream_t st) {
+  constexpr int cb = 16 * SD + 128 * NG;
+  const size_t smem = ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kWarps * kSStages * cb;
+  cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<NG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NG>,
+                                                         kThreads, smem)) != cudaSuccess)
+    return e;
+  const int grid = std::max(1, std::min(kMaxStreamCtas, sms * std::max(1, per_sm)));
+  decode_stream_kernel<NG><<<grid, kThreads, smem, st>>>(
+      L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
+      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_stream(const Layout& L, const void* paged, const void* side,
+                                 const uint16_t* q, const int32_t* seq_lens, int num_seqs,
+                                 const int32_t* block_table, float sm_scale, float* part_o,
+                                 float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
+                                 int32_t* status, cudaStream_t st) {
+  switch (L.d_h / L.g) {
+    case 4:
+      return launch_stream_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
+                                part_o, part_lse, tickets, out, out_lse, status, st);
+    case 2:
+      return launch_stream_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
+                                part_o, part_lse, tickets, out, out_lse, status, st);
+    case 1:
+      return launch_stream_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
+                                part_o, part_lse, tickets, out, out_lse, status, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kv4

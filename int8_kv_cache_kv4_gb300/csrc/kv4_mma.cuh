@@ -1,0 +1,127 @@
+// kv4_mma.cuh -- warp-level tensor-core helpers shared by the decode kernels:
+// the m16n8k16 fp16 MMA, transposing shared-memory matrix loads, and the
+// conversions that widen packed 4-bit / 8-bit codes to exact fp16 values.
+#pragma once
+#include "kv4_common.cuh"
+
+namespace kv4 {
+
+__device__ inline void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ inline void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ inline uint32_t hfma2(uint32_t x, uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(a), "r"(b));
+  return d;
+}
+
+__device__ inline float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ inline uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// (low half of a, low half of b)
+__device__ inline uint32_t lo_lo(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
+
+__device__ inline float2 h2f2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+__device__ inline uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ inline uint32_t u4word(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// fp16 pairs: 1.0, -1032 (= -(1024 + 8)), 1/16, -72 (= -(64 + 8))
+constexpr uint32_t kOne2 = 0x3C003C00u, kM1032 = 0xE408E408u;
+constexpr uint32_t kSixteenth2 = 0x2C002C00u, kM72 = 0xD480D480u;
+
+// Widen 8 V codes (two tokens x four channels, nibbles 0-3 and 4-7 of w) to
+// fp16 pairs (token a, token b) of the centred value c - 8, channel +0..+3.
+__device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
+  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
+  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+  const uint32_t w8 = w >> 8;
+  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
+  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+}
+
+// fp16 pairs -1024 and -64
+constexpr uint32_t kM1024 = 0xE400E400u, kM64 = 0xD400D400u;
+
+// Widen one K code word (8 channels of one token) to 4 fp16 pairs of exact
+// codes: pair i = (channel i, channel i + 4).
+__device__ inline void widen_k(uint32_t w, uint32_t x[4]) {
+  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
+  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+  const uint32_t w8 = w >> 8;
+  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
+  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+}
+
+template <int NG>
+struct MetaRow;  // one slot's NG (Delta, m) words
+template <>
+struct MetaRow<4> {
+  uint4 v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ uint32_t get(int g) const { return u4word(v, g); }
+  __device__ void zero() { v = make_uint4(0u, 0u, 0u, 0u); }
+};
+template <>
+struct MetaRow<2> {
+  uint2 v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ uint32_t get(int g) const { return g == 0 ? v.x : v.y; }
+  __device__ void zero() { v = make_uint2(0u, 0u); }
+};
+template <>
+struct MetaRow<1> {
+  uint32_t v;
+  __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ uint32_t get(int) const { return v; }
+  __device__ void zero() { v = 0u; }
+};
+
+__device__ inline float lo_f(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
+__device__ inline float hi_f(uint32_t w) { return f16_bits_to_f32(w >> 16); }
+
+// 8-bit codes: x ^ 0x80 turns a signed code c into the byte c + 128; with the
+// byte placed under an fp16 exponent of 2^10 the half is 1024 + 128 + c, and
+// subtracting 1152 leaves c exactly.
+constexpr uint32_t kMagic64 = 0x64646464u, kF1152x2 = 0x64806480u;
+__device__ inline uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// fp16 pair (code of byte i, code of byte j) of the biased word xb = w ^ 0x80808080;
+// sel = 0x4j4i selects the two bytes under the 0x64 exponent byte
+__device__ inline uint32_t i8pair(uint32_t xb, uint32_t sel) {
+  return hsub2(__byte_perm(xb, kMagic64, sel), kF1152x2);
+}
+
+}  // namespace kv4

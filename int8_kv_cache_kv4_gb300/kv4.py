@@ -34,6 +34,7 @@ KV4_KERNEL_AUTO = 0
 KV4_KERNEL_CUDA_CORE = 1
 KV4_KERNEL_MMA_SYNC = 2
 KV4_KERNEL_TCGEN05 = 3
+KV4_KERNEL_STREAM = 4
 
 
 class kv4_layout(ctypes.Structure):

@@ -165,9 +165,13 @@ def chunk_bytes(d_h: int, g: int) -> int:
     return 16 * d_h + 128 * (d_h // g)
 
 
+def side_scale_entries(S: int, R: int) -> int:
+    """Entries of each side-cache scale array: S + R rounded up to 8."""
+    return (S + R + 7) // 8 * 8
+
+
 def side_block_bytes(d_h: int, S: int, R: int) -> int:
-    b = (S + R) * (2 * d_h + 4)
-    return (b + 15) // 16 * 16
+    return 2 * (S + R) * d_h + 4 * side_scale_entries(S, R)
 
 
 def quant_append(*, h_kv, d_h, g, S, R, max_seqs, num_pages, max_pages_per_seq,

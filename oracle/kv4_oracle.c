@@ -275,17 +275,20 @@ int kv4o_side_slot(int p, int S, int R) { return p < S ? p : S + (p % R); }
  *     K meta   [16 slots][d_h/g][2 x u16] (Delta16, m16) per group
  *     V meta   [16 slots][d_h/g][2 x u16]
  *
- *   side cache = [max_seqs][h_kv][block], NS = S + R, block bytes =
- *   round_up(NS*(2*d_h + 4), 16), and inside one block:
+ *   side cache = [max_seqs][h_kv][block], NS = S + R, NSP = NS rounded up to
+ *   a multiple of 8, block bytes = 2*NS*d_h + 4*NSP, and inside one block:
  *     K8 codes [NS][d_h] int8, V8 codes [NS][d_h] int8,
- *     K8 scale [NS] u16 (fp16), V8 scale [NS] u16 (fp16), zero padding.
+ *     K8 scale [NSP] u16 (fp16), V8 scale [NSP] u16 (fp16); scale entries
+ *     NS..NSP-1 are padding that is never written.  A code row (one slot) is
+ *     cut into 16-byte pieces of 16 channels; piece P of slot t is stored at
+ *     piece position P xor (t mod (d_h / 16)).
  *
  * All multi-byte fields are little-endian.
  */
 static long chunk_bytes(int d_h, int g) { return 16L * d_h + 128L * (d_h / g); }
+static long side_scale_entries(int S, int R) { return ((long)S + R + 7) / 8 * 8; }
 static long side_block_bytes(int d_h, int S, int R) {
-  long b = (long)(S + R) * (2L * d_h + 4);
-  return (b + 15) / 16 * 16;
+  return 2L * (S + R) * d_h + 4L * side_scale_entries(S, R);
 }
 
 static void put_u16(uint8_t* p, uint16_t v) {
@@ -350,10 +353,13 @@ int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int 
           int ss = kv4o_side_slot(p, S, R);
           uint8_t* blk = side + ((long)s * h_kv + h) * sb;
           uint8_t* codes = blk + (long)kv * NS * d_h + (long)ss * d_h;
-          uint8_t* scl = blk + 2L * NS * d_h + (long)kv * NS * 2 + (long)ss * 2;
+          uint8_t* scl = blk + 2L * NS * d_h + (long)kv * side_scale_entries(S, R) * 2 + (long)ss * 2;
           uint16_t s16;
           status |= kv4o_int8_encode_vec(x, d_h, c8, &s16);
-          memcpy(codes, c8, (size_t)d_h);
+          for (int i = 0; i < d_h; ++i) {
+            int dst = 16 * ((i / 16) ^ (ss % (d_h / 16))) + i % 16;
+            codes[dst] = c8[i];
+          }
           put_u16(scl, s16);
         }
       }

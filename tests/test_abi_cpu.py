@@ -47,7 +47,10 @@ def test_sizes_match_layout_description(lib):
         lay = kv4.make_layout(group=g, max_seqs=3, num_pages=7, max_pages_per_seq=5)
         assert kv4.paged_cache_bytes(lay) == 7 * 8 * chunk
     lay = kv4.make_layout(sink=4, recent=128, max_seqs=3, num_pages=7, max_pages_per_seq=5)
-    assert kv4.side_cache_bytes(lay) == 3 * 8 * (132 * 260)
+    # per block: K8 and V8 codes 132 x 128 each, two scale arrays padded to 136
+    assert kv4.side_cache_bytes(lay) == 3 * 8 * (2 * 132 * 128 + 4 * 136)
+    lay = kv4.make_layout(sink=4, recent=124, max_seqs=3, num_pages=7, max_pages_per_seq=5)
+    assert kv4.side_cache_bytes(lay) == 3 * 8 * (128 * 260)  # NS = 128: no padding
     assert kv4.bf16_cache_bytes(lay) == 7 * 8 * 2 * 16 * 128 * 2
 
 

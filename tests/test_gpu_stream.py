@@ -1,0 +1,63 @@
+"""GPU parity of the work-balanced decode kernel's scheduling: the stream of
+8-slot protected units and 16-token INT4 pages cut into equal CTA shares.
+Cases aim at the bookkeeping -- pairs spread over many CTAs, CTAs without
+work, empty and very short sequences, partly filled recent-window rings,
+more sequences than threads in the start search -- and compare with the
+CPU oracle like the other parity tests."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from kv4_case import Case, compare_outputs  # noqa: E402
+from int8_kv_cache_kv4_gb300 import kv4  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kv4.load(build_if_missing=True)
+    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_STREAM)
+    yield
+    kv4.kv4_set_decode_kernel(prev)
+
+
+def _run(c):
+    gc = c.gpu()
+    gc.clear_status()
+    out, lse = c.gpu_decode(gc)
+    assert gc.read_status() == 0
+    ref, rlse = c.oracle_decode()
+    return compare_outputs(out, lse, ref, rlse, range(c.B), c.lens)
+
+
+def test_one_long_sequence_spread_over_many_ctas():
+    # 8 pairs of ~1250 pages each: every pair's INT4 region spans ~90 CTAs
+    _run(Case([20000], S=4, R=128, g=32, seed=21))
+
+
+def test_single_token_leaves_most_ctas_without_work():
+    _run(Case([1], S=4, R=64, g=32, seed=22))
+
+
+def test_all_sequences_empty():
+    _run(Case([0, 0, 0], S=4, R=64, g=32, seed=23, h_q=8, h_kv=2))
+
+
+@pytest.mark.parametrize("g_", [32, 64, 128])
+def test_many_short_sequences_and_partial_rings(g_):
+    # 300 sequences (more than the 128 threads of the start search): empty,
+    # shorter than the sinks, inside the ring (S < L <= S + R), page-aligned
+    # and longer, in seeded order
+    rng = np.random.default_rng(24)
+    kinds = [0, 1, 3, 4, 5, 17, 36, 68, 69, 70, 80, 96, 128, 200, 333, 511, 512]
+    lens = list(rng.choice(kinds, size=300))
+    _run(Case(lens, S=4, R=64, g=g_, seed=25, h_q=8, h_kv=2))
+
+
+@pytest.mark.parametrize("S,R", [(0, 0), (4, 0), (0, 16), (3, 13), (16, 128)])
+def test_window_shapes(S, R):
+    # sink / window sizes that are not multiples of the 8-slot unit
+    _run(Case([1, 2, 3, 15, 16, 17, 29, 150, 777], S=S, R=R, g=32, seed=26, h_q=16, h_kv=4))

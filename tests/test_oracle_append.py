@@ -41,14 +41,27 @@ def _unpack_chunk(chunk, d_h, g):
     return nib(unswizzle(kc)), nib(unswizzle(vc)), meta[0], meta[1]
 
 
+def _unswizzle8(rows):
+    """Undo the side cache's piece order: 16-byte piece P of slot t sits at
+    piece position P ^ (t % (d_h / 16))."""
+    n, d_h = rows.shape
+    out = np.empty_like(rows)
+    for t in range(n):
+        for P in range(d_h // 16):
+            src = P ^ (t % (d_h // 16))
+            out[t, 16 * P:16 * P + 16] = rows[t, 16 * src:16 * src + 16]
+    return out
+
+
 def _side_block(side, s, h, h_kv, d_h, S, R):
     sb = oracle.side_block_bytes(d_h, S, R)
     NS = S + R
     blk = side[(s * h_kv + h) * sb:(s * h_kv + h + 1) * sb]
-    k8 = blk[: NS * d_h].view(np.int8).reshape(NS, d_h)
-    v8 = blk[NS * d_h: 2 * NS * d_h].view(np.int8).reshape(NS, d_h)
+    k8 = _unswizzle8(blk[: NS * d_h].view(np.int8).reshape(NS, d_h))
+    v8 = _unswizzle8(blk[NS * d_h: 2 * NS * d_h].view(np.int8).reshape(NS, d_h))
+    NSP = (NS + 7) // 8 * 8  # scale arrays padded to a multiple of 8 entries
     ks = blk[2 * NS * d_h: 2 * NS * d_h + 2 * NS].view(np.uint16)
-    vs = blk[2 * NS * d_h + 2 * NS: 2 * NS * d_h + 4 * NS].view(np.uint16)
+    vs = blk[2 * NS * d_h + 2 * NSP: 2 * NS * d_h + 2 * NSP + 2 * NS].view(np.uint16)
     return k8, v8, ks, vs
 
 
