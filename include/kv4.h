@@ -115,8 +115,9 @@ const char* kv4_status_string(int code);
 
 /* Decode kernel selection (process-wide; default KV4_KERNEL_AUTO).  AUTO picks
  * the fastest kernel measured on GB300 for the layout: for head_dim 128 with 4
- * query heads per kv head the warp-level split kernel (MMA_SYNC), the
- * CUDA-core kernel otherwise.
+ * query heads per kv head, the work-balanced persistent tensor-core kernel
+ * (STREAM) when max_splits is 0 and the warp-level split kernel (MMA_SYNC)
+ * when the caller fixes the split count; the CUDA-core kernel otherwise.
  * STREAM cuts every (sequence, kv head) into 16-token INT4 pages and 8-slot
  * protected units and gives each CTA of a grid that fills the GPU an equal
  * share; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.

@@ -241,7 +241,7 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   // (the warp-level mma kernel by default); other shapes the CUDA-core kernel.  All merge their
   // splits in the last-finishing CTA of each (sequence, kv head).
   int which = g_decode_kernel;
-  if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_MMA_SYNC;  // fastest measured on GB300
+  if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_STREAM;  // fastest measured on GB300
   if (which == KV4_KERNEL_STREAM && (max_splits > 0 || !stream_supported(L)))
     which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;

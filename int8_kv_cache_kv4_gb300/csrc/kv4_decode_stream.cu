@@ -31,6 +31,7 @@
 //    transposed V codes against P' = p * s_v.  Slots outside the protected
 //    set (not yet written, or outside the final recent window) are masked.
 #include <algorithm>
+#include <type_traits>
 
 #include "kv4_decode_common.cuh"
 #include "kv4_mma.cuh"
@@ -42,6 +43,10 @@ constexpr int SD = 128, SG = 4;     // head_dim, query heads per kv head
 constexpr int kSStages = 2;         // bulk-copy stages per warp
 constexpr int kProtUnit = 8;        // side-cache slots per protected unit
 constexpr int kStreamMinBlocks = 5; // CTAs per SM the register budget targets
+// The thread that keeps the segment bookkeeping and takes the completion
+// tickets: lane 0 of the last warp, which the round-robin unit assignment
+// never gives more units than the others.
+constexpr int kTicketThread = (kWarps - 1) * 32;
 
 // One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
 struct Seg {
@@ -52,8 +57,10 @@ struct Seg {
 // Producer cursor of one warp: the next unit (segment, index) to copy in.
 struct Prod {
   Seg s;
-  int j;     // unit index inside segment s
-  int more;  // a next unit exists
+  const int32_t* bt;  // INT4 segment: block-table entries from its first page on
+  int j;              // unit index inside segment s
+  int hi;             // end of this CTA's units inside segment s
+  int more;           // a next unit exists
 };
 
 // A pair whose partial results are to be merged, with where they are.
@@ -67,9 +74,9 @@ struct __align__(16) StreamSmem {
   uint32_t qfrag4[8][32][4];        // INT4 path: block-diagonal query fragments
   uint2 qfrag8[8][32];              // INT8 path: query fragments (a0, a2), rows = heads
   float mrg_o[kWarps][SG][SD];      // per-warp unnormalised outputs at a segment end
-  uint16_t qh[SG][SD];              // query of the current pair as fp16 bits
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
   float qsum[SD / 32][SG];          // per 32-channel block sums of the query
+  float kc[4][SG];                  // per (group, head): 1024 * sum of the group's A values
   float mrg_m[kWarps][SG];
   float mrg_l[kWarps][SG];
   float mrg_mt[kWarps][SG][SD / 32];
@@ -84,6 +91,7 @@ struct __align__(16) StreamSmem {
   Pend pend;                        // partial whose ticket is in flight (thread 0)
   Pend comb;                        // pair to merge at this boundary
   int go;                           // comb is valid
+  int new_q;                        // the next segment starts a new pair
   int start_b;
   int32_t phys[kWarps][kSStages];   // INT4 stage: physical page, -1 = not loaded
   uint64_t bar[kWarps][kSStages];
@@ -160,31 +168,46 @@ __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __rest
   bulk_g2s(sm.qraw, q + row0 * SD, SG * SD * 2, &sm.qbar);
 }
 
-// sm.qraw (after its copy completed) -> fp16 copy and per-32-channel-block
-// sums.  No warp may still read qh or qsum (they are read only when a
-// segment starts).
-__device__ inline void stream_query_store(StreamSmem& sm) {
-  const int t = threadIdx.x;
-  const int j = t >> 5, d0 = 4 * (t & 31);
-  const uint2 raw = reinterpret_cast<const uint2*>(sm.qraw)[t];
-  const float x0 = bf16_bits_to_f32(raw.x & 0xFFFFu), x1 = bf16_bits_to_f32(raw.x >> 16);
-  const float x2 = bf16_bits_to_f32(raw.y & 0xFFFFu), x3 = bf16_bits_to_f32(raw.y >> 16);
-  *reinterpret_cast<uint2*>(&sm.qh[j][d0]) = make_uint2(pack_f16(x0, x1), pack_f16(x2, x3));
-  float s = (x0 + x1) + (x2 + x3);
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  s += __shfl_xor_sync(0xffffffffu, s, 4);
-  if ((t & 7) == 0) sm.qsum[(t & 31) >> 3][j] = s;
+// A query element (bf16 bits) as fp16 bits, optionally divided by 16 (the
+// same two roundings wherever the value is used).
+__device__ inline uint32_t q16(uint32_t bf, bool sixteenth) {
+  __half h = __float2half_rn(bf16_bits_to_f32(bf));
+  if (sixteenth) h = __float2half_rn(__half2float(h) * 0.0625f);
+  return __half_as_ushort(h);
 }
 
-// Both fragment sets from qh (after a barrier that follows stream_query_store;
-// no warp may still read the fragments).
+// Everything the units need from the query of the next pair, built from
+// sm.qraw once its copy has completed: per-32-channel-block sums, both
+// fragment sets, and per (group, head) the constant 1024-part of the INT4
+// QK sums.  No warp may still read the old values.
 template <int NG>
-__device__ inline void stream_build_frags(StreamSmem& sm) {
+__device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
   constexpr int GS = SD / NG;
   const int t = threadIdx.x;
+  const uint16_t* qr = sm.qraw;
+  {
+    // warp j: head j, lane: channels 4 * lane .. + 3
+    const int jj = t >> 5, ln = t & 31;
+    const uint2 raw = reinterpret_cast<const uint2*>(qr)[t];
+    const uint32_t b[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+    float sq = 0.f, sa = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sq += bf16_bits_to_f32(b[i]);
+      sa += __half2float(__ushort_as_half((unsigned short)q16(b[i], i & 1)));
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+#pragma unroll
+    for (int o = 1; o < GS / 4; o <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    if ((ln & 7) == 0) sm.qsum[ln >> 3][jj] = sq;
+    if ((ln % (GS / 4)) == 0) sm.kc[ln / (GS / 4)][jj] = 1024.f * sa;
+  }
   // INT4 fragments: A rows (group, head), block diagonal; k-index order as the
-  // widened K words produce it (see the split kernel)
+  // widened K words produce it.  The B values are 1024 + c for even channels
+  // (low nibbles) and 1024 + 16 c for odd ones (high nibbles, k-indices 8..15
+  // of each step, A registers 2 and 3), so the odd channels' query values are
+  // stored divided by 16 (exact in fp16 for |q| >= 2^-10).
   for (int idx = t; idx < 8 * 32 * 4; idx += kThreads) {
     const int s_ = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
     const int rr = ln >> 2, qq = ln & 3;
@@ -196,7 +219,7 @@ __device__ inline void stream_build_frags(StreamSmem& sm) {
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int d = base + 4 * e2;
-        if (d / GS == grp) w |= (uint32_t)sm.qh[jj][d] << (16 * e2);
+        if (d / GS == grp) w |= q16(qr[jj * SD + d], k & 2) << (16 * e2);
       }
     }
     sm.qfrag4[s_][ln][k] = w;
@@ -207,7 +230,11 @@ __device__ inline void stream_build_frags(StreamSmem& sm) {
     const int s_ = idx >> 5, ln = idx & 31;
     const int rr = ln >> 2, qq = ln & 3;
     uint2 w = make_uint2(0u, 0u);
-    if (rr < SG) w = *reinterpret_cast<const uint2*>(&sm.qh[rr][32 * qq + 4 * s_]);
+    if (rr < SG) {
+      const uint16_t* src = qr + rr * SD + 32 * qq + 4 * s_;
+      w.x = q16(src[0], false) | (q16(src[1], false) << 16);
+      w.y = q16(src[2], false) | (q16(src[3], false) << 16);
+    }
     sm.qfrag8[s_][ln] = w;
   }
 }
@@ -413,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   // block-table entry into a register, consumed only at the next issue so
   // the load's latency is not waited for here.
   int pphys = -1;
+  // slow path: (pr.s, pr.j) may lie past its segment's end; move over
+  // segments until it names a unit of this warp
   auto prod_next = [&](Prod& pr) {
     const long long ub = sm.u_begin, ue = sm.u_end;
     while (true) {
@@ -420,15 +449,14 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         pr.more = 0;
         return;
       }
-      if (pr.j < (int)(min(ue, pr.s.start + pr.s.n) - pr.s.start)) break;
+      pr.hi = (int)(min(ue, pr.s.start + pr.s.n) - pr.s.start);
+      if (pr.j < pr.hi) break;
       seg_next(pr.s, L, seq_lens, B);
       pr.j = (int)(max(ub, pr.s.start) - pr.s.start) + warp;
     }
     pr.more = 1;
-    if (pr.s.type == 1) {
-      const int pg = min(pr.s.len, L.S) / kPage + pr.j;
-      pphys = __ldg(block_table + (long long)pr.s.b * L.max_pages + pg);
-    }
+    pr.bt = block_table + (long long)pr.s.b * L.max_pages + min(pr.s.len, L.S) / kPage;
+    if (pr.s.type == 1) pphys = __ldg(pr.bt + pr.j);
   };
   auto issue = [&](int st) {
     Prod& pr = sm.prod[warp];
@@ -477,7 +505,11 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       issue(st);
       Prod& pr = sm.prod[warp];
       pr.j += kWarps;
-      prod_next(pr);
+      if (pr.j < pr.hi) {  // fast path: next unit of the same segment
+        if (pr.s.type == 1) pphys = __ldg(pr.bt + pr.j);
+      } else {
+        prod_next(pr);
+      }
     }
   };
 
@@ -485,11 +517,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   const int r = lane >> 2, qd = lane & 3;
   const int jh = r & 3;                 // INT4 path: this lane's softmax head
   const int g0 = r >> 2, g1 = g0 + 2;   // INT4 path: groups of QK rows r and r+8
-  const bool v0 = g0 < NG, v1 = g1 < NG;
-  constexpr int NGH = NG > 1 ? NG / 2 : 1;
-  const int mt_g0 = (r >= 4) ? NG / 2 : 0;
-  const bool mt_on = (r < 4) || NG > 1;
-  const int tk[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
+  const bool v0 = NG == 4 || g0 < NG, v1 = NG == 4 || g1 < NG;
   const uint32_t p_keep = (r < 4) ? 0xFFFFFFFFu : 0u;
   // INT4 V ldmatrix rows: matrix lane/8 = tokens (mi&1)*8.., piece mi>>1 (+2)
   const int lm_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -504,30 +532,29 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   int it = 0;  // this warp's consumed units (stage it % 2, phase (it / 2) & 1)
   int pend_t = 0;  // thread 0: ticket value returned for the pending partial
   uint32_t qphase = 0;  // completed copies into sm.qraw
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kTicketThread) {
     sm.pend.valid = 0;
     const Seg c0s = sm.cs;
     stream_query_fetch(sm, q, (long long)c0s.b * L.h_q + (long long)c0s.h * SG);
   }
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
   ++qphase;
-  stream_query_store(sm);
+  stream_query_setup<NG>(sm);
   __syncthreads();
-  stream_build_frags<NG>(sm);
-  __syncthreads();
-  // The current segment lives in sm.cs (advanced by thread 0 between the
-  // boundary barriers); the loop below keeps only what the units need.
+  // The current segment lives in sm.cs (advanced by the ticket thread between
+  // the boundary barriers); the loop below keeps only what the units need.
   while (true) {
     const Seg cs = sm.cs;
     if (cs.b >= B || cs.start >= sm.u_end) break;
-    // the next segment's pair: read its query ahead when it changes
-    bool new_q;
-    {
-      Seg nx = cs;
-      seg_next(nx, L, seq_lens, B);
-      new_q = nx.b < B && nx.start < sm.u_end && (nx.b != cs.b || nx.h != cs.h);
-      if (threadIdx.x == 0) {
-        // the previous query copy was consumed before the last barrier
+    if (threadIdx.x == kTicketThread) {
+      // the next segment (its pair's query is read ahead when it changes:
+      // the previous copy was consumed before the last barrier), and this
+      // segment's partial bookkeeping -- none of it is waited for by a barrier
+      {
+        Seg nx = cs;
+        seg_next(nx, L, seq_lens, B);
+        const bool new_q = nx.b < B && nx.start < sm.u_end && (nx.b != cs.b || nx.h != cs.h);
+        sm.new_q = new_q;
         if (new_q) stream_query_fetch(sm, q, (long long)nx.b * L.h_q + (long long)nx.h * SG);
         // bookkeeping for the boundary, done here so that no barrier waits on it
         sm.nx = nx;
@@ -555,18 +582,26 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 
     if (cs.type == 1) {
       // ============================================= INT4 pages (eq. 5.1)
-      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qfrag4[0][0][0]) + lane;
+      // QK^T: block-diagonal query rows against K codes widened with their
+      // exponent offset (1024 + c, 1024 + 16 c); the fragments carry the 1/16
+      // and the accumulators start at minus the constant 1024-part, so each
+      // row sums q_d c_d over its group.  Scores by eq. 5.1 per group; online
+      // softmax; PV against the centred V codes with P' = p * Delta_v; the
+      // offset term sum_t p_t (Delta_t, m_t) of every group as one more MMA
+      // whose A rows are the page's V metadata (group, Delta | m).
+      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qfrag4[0][0][0]) + lane;  // + 32 * s
       float qs0 = 0.f, qs1 = 0.f;
 #pragma unroll
       for (int bq = 0; bq < D / 32; ++bq) {
         if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][jh];
         if (v1 && (bq * 32) / GS == g1) qs1 += sm.qsum[bq][jh];
       }
+      const float kc0 = v0 ? sm.kc[g0][jh] : 0.f;
+      const float kc1 = v1 ? sm.kc[g1][jh] : 0.f;
       const int first_page = rg.sink_end / kPage;
+      const int len = cs.len;
       float m_run = -INFINITY, l_run = 0.f;
-      float mt_m[NGH], mt_d[NGH];
-#pragma unroll
-      for (int i = 0; i < NGH; ++i) mt_m[i] = mt_d[i] = 0.f;
+      float mtacc[4] = {0.f, 0.f, 0.f, 0.f};  // rows (group, Delta | m), columns heads
       float acc[4][2][4];
 #pragma unroll
       for (int G_ = 0; G_ < 4; ++G_)
@@ -574,85 +609,82 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
+      // per-lane byte offsets inside a stage
+      const uint8_t* k_lane = my_stages + r * 64 + row_byte(16 * qd, r, D);  // token r (+512: r + 8)
+      const uint8_t* km_lane = my_stages + meta_off_k(D) + (2 * qd * NG + g0) * 4;
+      const uint8_t* vm_lane = my_stages + meta_off_v(D, GS) + 2 * qd * NG * 4;
+      const int mt_g = r >> 1;                  // offset-term MMA: this lane's A row group
+      const bool mt_row = mt_g < NG;
+      const uint32_t mt_sel = (r & 1) ? 0x7632u : 0x5410u;  // Delta (low) or m (high) halves
+      const uint32_t v_lane = smem_u32(my_stages) + codes_off_v(D);
+      constexpr int TK[4] = {0, 1, 8, 9};      // this lane's tokens: 2 * qd + TK[e]
 
-      for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
-        const int st = it % kSStages;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], (it / kSStages) & 1));
+      // (one copy of the page body: unrolling it per stage overflows the
+      // instruction cache)
+      for (int jj = lo + warp; jj < hi; jj += kWarps) {
+        const int ST = it & 1;
+        const int SO = ST * cb;  // stage offset
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][ST], (it >> 1) & 1));
         if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
-        const bool valid = ok && sm.phys[warp][st] >= 0;
-        const uint8_t* chunk = my_stages + (size_t)st * cb;
-        const int pg = first_page + jj;
-        if (valid) {
-          const bool tail = (pg + 1) * kPage > cs.len;
-          const uint4 k0 =
-              *reinterpret_cast<const uint4*>(chunk + r * 64 + row_byte(16 * qd, r, D));
-          const uint4 k1 =
-              *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + row_byte(16 * qd, r + 8, D));
-          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok && sm.phys[warp][ST] >= 0) {
+          const int pg = first_page + jj;
+          const bool tail = (pg + 1) * kPage > len;
+          // ---------------- QK^T
+          const uint4 k0 = *reinterpret_cast<const uint4*>(k_lane + SO);
+          const uint4 k1 = *reinterpret_cast<const uint4*>(k_lane + SO + 512);
+          float d0[4] = {-kc0, -kc0, -kc1, -kc1}, d1[4] = {-kc0, -kc0, -kc1, -kc1};
           float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint32_t x0[4], x1[4];
-            widen_k(u4word(k0, u), x0);
-            widen_k(u4word(k1, u), x1);
+            widen_k_biased(u4word(k0, u), x0);
+            widen_k_biased(u4word(k1, u), x1);
             const uint4 qa0 = qa_s[32 * (2 * u)], qa1 = qa_s[32 * (2 * u + 1)];
             mma_f16(d0, qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
             mma_f16(d1, qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
             mma_f16(e0, qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
             mma_f16(e1, qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
           }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            d0[k] += e0[k];
-            d1[k] += e1[k];
-          }
-          const float draw0[4] = {d0[0], d0[1], d1[0], d1[1]};
-          const float draw1[4] = {d0[2], d0[3], d1[2], d1[3]};
-          const uint8_t* kmeta = chunk + meta_off_k(D);
+          // ---------------- scores (eq. 5.1 per group) of this lane's 4 tokens
+          const float draw0[4] = {d0[0] + e0[0], d0[1] + e0[1], d1[0] + e1[0], d1[1] + e1[1]};
+          const float draw1[4] = {d0[2] + e0[2], d0[3] + e0[3], d1[2] + e1[2], d1[3] + e1[3]};
           float sc[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float part = 0.f;
             if (v0) {
-              const float2 dm =
-                  h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g0) * 4));
+              const float2 dm = h2f2(*reinterpret_cast<const uint32_t*>(km_lane + SO + TK[e] * NG * 4));
               part = fmaf(dm.x, draw0[e], dm.y * qs0);
             }
             if (v1) {
               const float2 dm =
-                  h2f2(*reinterpret_cast<const uint32_t*>(kmeta + (tk[e] * NG + g1) * 4));
+                  h2f2(*reinterpret_cast<const uint32_t*>(km_lane + SO + TK[e] * NG * 4 + 8));
               part += fmaf(dm.x, draw1[e], dm.y * qs1);
             }
             sc[e] = part;
           }
-          const bool interior = pg * kPage >= rg.sink_end && (pg + 1) * kPage <= rg.rec_start;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 16);
             sc[e] *= scale_log2;
           }
-          if (!interior) {
+          if (!(pg * kPage >= rg.sink_end && (pg + 1) * kPage <= rg.rec_start)) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int pos = pg * kPage + tk[e];
+            for (int e = 0; e < 4; ++e) {  // first / last page: mask outside the region
+              const int pos = pg * kPage + 2 * qd + TK[e];
               if (!(pos >= rg.sink_end && pos < rg.rec_start)) sc[e] = -INFINITY;
             }
           }
+          // V metadata: Delta_v of every group for P', and this lane's offset-term row
           MetaRow<NG> vm[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
-          uint32_t mtw[4][NGH];
+          uint32_t mw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
-            if (NGH == 2) {
-              const uint2 v2 = *reinterpret_cast<const uint2*>(row);
-              mtw[e][0] = v2.x;
-              mtw[e][NGH - 1] = v2.y;
-            } else {
-              mtw[e][0] = *reinterpret_cast<const uint32_t*>(row);
-            }
+            vm[e].load(vm_lane + SO + TK[e] * NG * 4);
+            mw[e] = mt_row ? *reinterpret_cast<const uint32_t*>(vm_lane + SO + TK[e] * NG * 4 + mt_g * 4)
+                           : 0u;
           }
+          // ---------------- online softmax for head jh
           float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
@@ -674,36 +706,29 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
                 acc[G_][hh][2] *= aA;
                 acc[G_][hh][3] *= aB;
               }
-#pragma unroll
-            for (int gi = 0; gi < NGH; ++gi) {
-              mt_m[gi] *= alpha;
-              mt_d[gi] *= alpha;
-            }
+            mtacc[0] *= aA;
+            mtacc[1] *= aB;
             l_run *= alpha;
             m_run = mnew;
           }
           l_run += (p[0] + p[1]) + (p[2] + p[3]);
+          // ---------------- PV
           uint32_t va[4], vb[4];
-          const uint32_t vbase = smem_u32(chunk + codes_off_v(D));
-          ldsm_x4_trans(va, vbase + lm_off0);
-          ldsm_x4_trans(vb, vbase + lm_off1);
-          if (tail) {
+          ldsm_x4_trans(va, v_lane + SO + lm_off0);
+          ldsm_x4_trans(vb, v_lane + SO + lm_off1);
+          if (tail) {  // slots at or past the length were never written
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (pg * kPage + tk[e] >= cs.len) vm[e].zero();
-          }
-          if (mt_on) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-#pragma unroll
-              for (int gi = 0; gi < NGH; ++gi) {
-                const float2 dm = h2f2(tail && pg * kPage + tk[e] >= cs.len ? 0u : mtw[e][gi]);
-                mt_d[gi] = fmaf(p[e], dm.x, mt_d[gi]);
-                mt_m[gi] = fmaf(p[e], dm.y, mt_m[gi]);
+              if (pg * kPage + 2 * qd + TK[e] >= len) {
+                vm[e].zero();
+                mw[e] = 0u;
               }
           }
           const uint32_t p01 = pack_f16(p[0], p[1]) & p_keep;
           const uint32_t p23 = pack_f16(p[2], p[3]) & p_keep;
+          // offset term: rows (group, Delta | m) x tokens, against p
+          mma_f16(mtacc, __byte_perm(mw[0], mw[1], mt_sel), 0u, __byte_perm(mw[2], mw[3], mt_sel), 0u,
+                  p01, p23);
 #pragma unroll
           for (int P = 0; P < 4; ++P) {
             const int grp = (P * 32) / GS;
@@ -718,29 +743,29 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
             mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
           }
         }
-        refill(st);
+        refill(ST);
+        ++it;
       }
+
       // publish this warp's state
       float lsum = (r < 4) ? l_run : 0.f;
       lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
       lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-      float mt[NGH];
-#pragma unroll
-      for (int gi = 0; gi < NGH; ++gi) {
-        mt[gi] = fmaf(8.f, mt_d[gi], mt_m[gi]);
-        mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 1);
-        mt[gi] += __shfl_xor_sync(0xffffffffu, mt[gi], 2);
-      }
       if (qd == 0 && r < 4) {
         sm.mrg_m[warp][jh] = m_run;
         sm.mrg_l[warp][jh] = lsum;
       }
-      if (qd == 0 && mt_on) {
-#pragma unroll
-        for (int gi = 0; gi < NGH; ++gi) {
-          const int grp = mt_g0 + gi;
-          for (int blk = grp * (GS / 32); blk < (grp + 1) * (GS / 32); ++blk)
-            sm.mrg_mt[warp][jh][blk] = mt[gi];
+      // offset term of group g, heads 2qd, 2qd+1: sum p m + 8 sum p Delta (rows
+      // 2g and 2g + 1 live in lanes 8g + qd and 8g + 4 + qd)
+      {
+        const float om0 = __shfl_xor_sync(0xffffffffu, mtacc[0], 4);
+        const float om1 = __shfl_xor_sync(0xffffffffu, mtacc[1], 4);
+        if ((r & 1) == 0 && mt_row && qd < 2) {
+          const float tA = fmaf(8.f, mtacc[0], om0), tB = fmaf(8.f, mtacc[1], om1);
+          for (int blk = mt_g * (GS / 32); blk < (mt_g + 1) * (GS / 32); ++blk) {
+            sm.mrg_mt[warp][2 * qd][blk] = tA;
+            sm.mrg_mt[warp][2 * qd + 1][blk] = tB;
+          }
         }
       }
       if (qd < 2) {
@@ -855,11 +880,11 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 
     // ----------------------------------------- segment end: partial + merge
     // B1: every warp has published; merge into partial 2 * pair + region + c
+    // (sm.pcur, sm.new_q: written at this segment's start; the ticket thread
+    // rewrites sm.cs before the next barrier)
     __syncthreads();
-    // (sm.pcur is fixed until the next segment starts; thread 0 rewrites
-    // sm.cs before the next barrier)
     stream_merge_store(sm, part_o, part_lse, sm.pcur.s0 + sm.pcur.type + c);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == kTicketThread) {
       // the previous partial's ticket (taken one segment ago) decides whether
       // this CTA merges that pair now
       int go = 0;
@@ -873,18 +898,14 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       sm.go = go;
       sm.cs = sm.nx;  // read by all after the next barrier
     }
-    if (new_q) {
+    if (sm.new_q) {  // fragments are not read again before the next barrier
       if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0)
         set_status(status, KV4_STATUS_TIMEOUT);
       ++qphase;
-      stream_query_store(sm);
+      stream_query_setup<NG>(sm);
     }
-    __syncthreads();  // B2: partial stored; qh, qsum, comb and cs written
-    if (new_q) {
-      stream_build_frags<NG>(sm);
-      __syncthreads();  // B3: next pair's fragments ready
-    }
-    if (threadIdx.x == 0) {
+    __syncthreads();  // B2: partial stored; next pair's query set up; comb, cs written
+    if (threadIdx.x == kTicketThread) {
       // take this partial's ticket with release semantics (the barrier above
       // makes the CTA's partial stores part of what is released); the
       // result is read at the next boundary
@@ -899,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   }
   // the last partial's ticket
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kTicketThread) {
     int go = 0;
     if (sm.pend.valid) {
       go = pend_t == sm.pend.n0 + sm.pend.n1 - 1;

@@ -6,9 +6,11 @@
 
 namespace kv4 {
 
+// (no side effects besides its register results: not volatile, so the
+// compiler may schedule shared-memory reads across it)
 __device__ inline void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -67,6 +69,18 @@ __device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
   const uint32_t w8 = w >> 8;
   x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
   x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+}
+
+// Widen one K code word (8 channels of one token) to 4 fp16 pairs without
+// removing the exponent offset: pairs 0 and 2 hold 1024 + c (channels i and
+// i + 4 of the low nibbles), pairs 1 and 3 hold 1024 + 16 c (high nibbles).
+// The consumer folds the 1024 and the 16 into its other operand.
+__device__ inline void widen_k_biased(uint32_t w, uint32_t x[4]) {
+  x[0] = (w & 0x000F000Fu) | 0x64006400u;
+  x[1] = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  x[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+  x[3] = (w8 & 0x00F000F0u) | 0x64006400u;
 }
 
 // fp16 pairs -1024 and -64
