@@ -36,6 +36,14 @@ from int8_kv_cache_kv4_gb300.cache import build_workload  # noqa: E402
 METRIC = "decode-attn resident KV tokens/s per layer and achieved HBM GB/s vs 8 TB/s"
 UNIT = "tokens/s"
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the default decode kernel on the default workload, from the ncu capture
+# summarised in profiles/decode_stream_kernel_qwen3_8b_b64.md.  Keyed by a
+# hash of the sources that kernel is compiled from: once they change, the
+# figure no longer describes the kernel and the bench reports null.
+KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_mma.cuh", "kv4_decode_common.cuh", "kv4_common.cuh"]
+TRAFFIC = {("e015b76441dfb51d", "qwen3_8b_b64"): 388330496 + 5408256}
+
 
 # ------------------------------------------------------------------ helpers
 
@@ -45,6 +53,15 @@ def peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "int8_kv_cache_kv4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def algorithmic_bytes(lens, w: W.Workload):
@@ -190,6 +207,8 @@ def run_kv4(args):
     dec_avg = statistics.mean(dec_ms)
     hbm_peak, peak_kind = peaks()
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
+    ksrc = kernel_source_hash()
+    traffic = TRAFFIC.get((ksrc, w.name)) if args.kernel in ("auto", "stream") and args.max_splits == 0 else None
 
     # BF16-KV comparator on the same pages / inputs (reported beside, not in the step)
     comparator = None
@@ -232,11 +251,15 @@ def run_kv4(args):
         "decode_tokens_per_s": tokens / (dec_avg / 1e3),
         "decode_algorithmic_GBps": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
-                     "kernel": "kv4_decode_attn (split kernel + combine)",
-                     "bytes_per_launch": dec_bytes, "peak_source": peak_kind},
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "kernel": decode_kernel_name(args, w),
+                     "timed": "kv4_decode_attn call on the launching stream: ticket memset + decode kernel",
+                     "bytes_per_launch": dec_bytes, "peak_source": peak_kind,
+                     "kernel_source_hash": ksrc},
         "append_algorithmic_bytes": app_bytes,
-        "gpu_launches": 3 * args.steps,
+        # per step: quant_append_kernel and the decode kernel (plus one CUDA
+        # runtime memset of the completion counters, not ours)
+        "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "device_status": status,
         "e2e": e2e,
@@ -248,6 +271,16 @@ def run_kv4(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def decode_kernel_name(args, w):
+    if args.kernel == "cuda" or w.d_h != 128 or w.h_q != 4 * w.h_kv:
+        return "decode_split_kernel (CUDA cores, fused eq. A1 merge)"
+    if args.kernel == "tcgen05":
+        return "decode_tc_kernel (tcgen05, fused eq. A1 merge)"
+    if args.kernel == "mma" or args.max_splits > 0:
+        return "decode_mma_kernel (mma.sync split kernel, fused eq. A1 merge)"
+    return "decode_stream_kernel (work-balanced, mma.sync, fused eq. A1 merge)"
 
 
 def run_e2e(cache, s, args, stream):
