@@ -42,7 +42,7 @@ UNIT = "tokens/s"
 # hash of the sources that kernel is compiled from: once they change, the
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_mma.cuh", "kv4_decode_common.cuh", "kv4_common.cuh"]
-TRAFFIC = {("e015b76441dfb51d", "qwen3_8b_b64"): 388330496 + 5408256}
+TRAFFIC = {("07d998d06c4da89f", "qwen3_8b_b64"): 388357376 + 4740864}
 
 
 # ------------------------------------------------------------------ helpers
@@ -133,6 +133,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------- replicas (N > 1)
+
+def reduce_max_ms(total_ms: float, world: int, device) -> float:
+    """The slowest rank's timed-region length: every rank contributes its own
+    CUDA-event time and all receive the maximum (NCCL on the GPU machine, gloo in
+    the CPU tests).  A barrier precedes and follows the timed region."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(world: int, tokens_per_replica: int, ms_per_step: float) -> float:
+    """Whole-job throughput of N independent replicas (weak scaling): every
+    rank decodes its own copy of the workload in each step."""
+    return world * tokens_per_replica / (ms_per_step / 1e3)
+
+
 # --------------------------------------------------------------- workload
 
 def run_step(cache, s, max_splits=0, ev=None):
@@ -172,6 +192,20 @@ def run_kv4(args):
         run_step(cache, s, args.max_splits)
     torch.cuda.synchronize()
     cache.clear_status()
+    # The timed steps replay CUDA graphs captured from the same C-ABI calls
+    # (one for the append, one for the decode), so that host-side argument
+    # marshalling does not starve the GPU; --no-graph times eager calls.
+    g_app = g_dec = None
+    if not args.no_graph:
+        g_app, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_app):
+            cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+        with torch.cuda.graph(g_dec):
+            cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)
+        for _ in range(args.warmup):
+            g_app.replay()
+            g_dec.replay()
+        torch.cuda.synchronize()
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -187,7 +221,12 @@ def run_kv4(args):
     t0.record(stream)
     for i in range(args.steps):
         starts[i].record(stream)
-        run_step(cache, s, args.max_splits, ev=mids[i])
+        if g_app is not None:
+            g_app.replay()
+            mids[i].record(stream)
+            g_dec.replay()
+        else:
+            run_step(cache, s, args.max_splits, ev=mids[i])
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -199,11 +238,8 @@ def run_kv4(args):
     app_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
     status = cache.read_status()
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t.item()) / args.steps
-    value = world * tokens / (ms_per_step / 1e3)
+    ms_per_step = reduce_max_ms(total_ms, world, dev) / args.steps
+    value = replica_value(world, tokens, ms_per_step)
     dec_avg = statistics.mean(dec_ms)
     hbm_peak, peak_kind = peaks()
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
@@ -246,6 +282,7 @@ def run_kv4(args):
                    "sink": w.sink, "recent": w.recent, "group": w.group, "page": 16,
                    "splits": kv4.num_splits(cache.layout, int(len(lens)), args.max_splits),
                    "parallelism": f"replicas x{world}", "decode_kernel": args.kernel,
+                   "launch": "eager" if args.no_graph else "CUDA graph replay of the C-ABI calls",
                    "l2": "cache working set > L2 (no flush needed)"},
         "decode_ms": dec_avg, "append_ms": statistics.mean(app_ms),
         "decode_tokens_per_s": tokens / (dec_avg / 1e3),
@@ -367,6 +404,181 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- report mode
+
+def _timed(fn, warm=10, samples=90, flush=None):
+    """CUDA-event times (ms) of fn on the current stream: `warm` untimed calls,
+    then `samples` timed ones, each after an optional L2 flush."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(samples):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return {"median_ms": statistics.median(ts), "mean_ms": statistics.mean(ts)}
+
+
+def _graph(fn):
+    """fn (one or more C-ABI calls) captured as a CUDA graph after one eager
+    call (which also performs the library's one-time per-device setup)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _oracle_all_cores(w, lens, nseq):
+    """The CPU oracle on the first nseq sequences, one process per host core
+    (spawned), as a throughput baseline."""
+    import multiprocessing as mpr
+    cores = os.cpu_count() or 1
+    nseq = min(nseq, len(lens))
+    t = time.perf_counter()
+    with mpr.get_context("spawn").Pool(min(cores, nseq)) as pool:
+        pool.map(_oracle_one, [(w, int(lens[b]), b) for b in range(nseq)])
+    dt = time.perf_counter() - t
+    return {"value": float(sum(int(x) for x in lens[:nseq]) / dt), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"first {nseq} sequences, all heads, quantize + fp64 decode, "
+                                        f"{min(cores, nseq)} processes, {dt:.1f} s incl. start-up"}
+
+
+def _oracle_one(a):
+    import oracle
+    w, L, b = a
+    outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
+    q = W.q_numpy(w.seed, 1, w.h_q, w.d_h)[0]
+    k, v = W.kv_numpy_block(w.seed, b, w.h_kv, L, w.d_h, outl)
+    oracle.decode_seq(q, k, v, g=w.group, S=w.sink, R=w.recent, sm_scale=1 / math.sqrt(w.d_h))
+    return L
+
+
+def run_report(args):
+    """One JSON object per config of the pages' workloads (see workloads.py):
+    decode time (median and mean of 90 CUDA-event samples after 10 warm-ups),
+    resident KV tokens/s, algorithmic GB/s and its fraction of the measured HBM
+    copy bandwidth, append time, the bf16-KV comparator, and the config's own
+    variants.  Not the bench line; for the design doc and the profiles."""
+    import dataclasses
+    import torch
+    from int8_kv_cache_kv4_gb300 import kv4
+    kv4.load(build_if_missing=True)
+    dev = torch.device("cuda")
+    hbm, peak_kind = peaks()
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def decode_line(name, w, cache, s, lens, flush=False, extra=None):
+        dec_b, app_b, _, _ = algorithmic_bytes(lens, w)
+        f = (lambda: l2_flush.zero_()) if flush else None
+        gd, ga = _graph(lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"])), \
+            _graph(lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"]))
+        td = _timed(gd.replay, flush=f)
+        ta = _timed(ga.replay, flush=f)
+        tok = int(lens.sum())
+        line = {"report": name, "workload": w.name, "batch": int(len(lens)), "tokens": tok,
+                "sink": w.sink, "recent": w.recent, "group": w.group,
+                "decode": td, "append": ta, "decode_bytes": dec_b,
+                "tokens_per_s": tok / (td["median_ms"] / 1e3),
+                "GBps": dec_b / (td["median_ms"] / 1e3) / 1e9,
+                "frac_of_hbm": dec_b / (td["median_ms"] / 1e3) / 1e9 / hbm, "peak": peak_kind,
+                "l2_flushed": flush, "status": cache.read_status()}
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+        return line
+
+    def bf16_line(name, w, cache, s, lens):
+        out16 = torch.empty_like(s["out"])
+        t = _timed(_graph(lambda: cache.decode_bf16(s["q"], s["lens"], out16, None)).replay)
+        cache.decode(s["q"], s["lens"], s["out"], s["lse"])
+        drift = (s["out"].float() - out16.float()).abs()
+        b = sum(w.h_kv * int(L) * 2 * w.d_h * 2 for L in lens) + len(lens) * w.h_q * w.d_h * 4
+        print(json.dumps({"report": name, "workload": w.name, "kernel": "bf16-KV decode", "decode": t,
+                          "GBps": b / (t["median_ms"] / 1e3) / 1e9, "bytes": b,
+                          "drift_vs_kv4": {"max_abs": float(drift.max()),
+                                           "mean_abs": float(drift.mean())}}), flush=True)
+
+    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5"}
+    if "1" in sel:  # tiny: L2-resident, flushed
+        w = W.WORKLOADS["tiny_b4_l512"]
+        cache, s, lens, w = build_workload(w, dev)
+        decode_line("config 1", w, cache, s, lens, flush=True)
+        del cache
+    if "2" in sel:
+        w = W.WORKLOADS["qwen3_8b_b64"]
+        cache, s, lens, w = build_workload(w, dev, with_bf16=True)
+        decode_line("config 2", w, cache, s, lens,
+                    extra={"cpu_oracle_all_cores": _oracle_all_cores(w, lens, 32)})
+        bf16_line("config 2", w, cache, s, lens)
+        del cache
+    if "3" in sel:  # 100 rollout steps: fresh token per sequence, append then decode
+        w = W.WORKLOADS["rollout_b256"]
+        cache, s, lens, w = build_workload(w, dev, extra_tokens=w.steps)
+        from int8_kv_cache_kv4_gb300.cache import step_inputs
+        steps = [step_inputs(w, len(lens), i, dev) for i in range(w.steps)]
+        seq = s["seq"]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(w.steps)]
+        torch.cuda.synchronize()
+        for i, (k, v, q) in enumerate(steps):
+            pos = torch.as_tensor((lens - 1 + i).astype(np.int32), device=dev)
+            ln = torch.as_tensor((lens + i).astype(np.int32), device=dev)
+            ev[i][0].record()
+            cache.append(k, v, seq, pos, ln)
+            ev[i][1].record()
+            cache.decode(q, ln, s["out"], s["lse"])
+            ev[i][2].record()
+        torch.cuda.synchronize()
+        app = [e[0].elapsed_time(e[1]) for e in ev]
+        dec = [e[1].elapsed_time(e[2]) for e in ev]
+        dec_b, _, _, _ = algorithmic_bytes(lens + w.steps // 2, w)
+        print(json.dumps({"report": "config 3", "workload": w.name, "steps": w.steps,
+                          "append_ms": {"median": statistics.median(app), "mean": statistics.mean(app)},
+                          "decode_ms": {"median": statistics.median(dec), "mean": statistics.mean(dec)},
+                          "step_ms_mean": statistics.mean(a + d for a, d in zip(app, dec)),
+                          "decode_GBps_mid": dec_b / (statistics.median(dec) / 1e3) / 1e9,
+                          "frac_of_hbm_mid": dec_b / (statistics.median(dec) / 1e3) / 1e9 / hbm,
+                          "resident_tokens_mid": int((lens + w.steps // 2).sum()),
+                          "status": cache.read_status()}), flush=True)
+        del cache, steps
+    if "4" in sel:  # long context: mixed, INT8 everywhere (R >= L), bf16
+        w = W.WORKLOADS["long_128k"]
+        cache, s, lens, w = build_workload(w, dev, with_bf16=True)
+        decode_line("config 4 mixed", w, cache, s, lens)
+        bf16_line("config 4", w, cache, s, lens)
+        del cache
+        w8 = dataclasses.replace(w, recent=int(lens.max()))
+        cache, s, lens, w8 = build_workload(w8, dev)
+        decode_line("config 4 int8 everywhere", w8, cache, s, lens)
+        del cache
+    if "5" in sel:  # one layer of the 36-layer step per sweep point (x36 for the step)
+        w = W.WORKLOADS["qwen3_8b_36l"]
+        base = {}
+        for g in (32, 64, 128):
+            for R in (0, 64, 128, 512):
+                cache, s, lens, wr = build_workload(w, dev, group=g, recent=R)
+                ln = decode_line(f"config 5 layer (g={g}, R={R})", wr, cache, s, lens)
+                if R == 0:
+                    base[g] = ln["decode"]["median_ms"]
+                print(json.dumps({"report": "config 5 point", "group": g, "recent": R,
+                                  "layer_decode_ms": ln["decode"]["median_ms"],
+                                  "layer_append_ms": ln["append"]["median_ms"],
+                                  "step_36_layers_ms (x36, one layer timed)":
+                                      36 * (ln["decode"]["median_ms"] + ln["append"]["median_ms"]),
+                                  "cost_vs_R0": ln["decode"]["median_ms"] / base[g]}), flush=True)
+                del cache
+                torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,11 +590,16 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=["auto", "stream", "tcgen05", "mma", "cuda"],
                     help="decode kernel (auto = the fastest measured for the layout)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
+    ap.add_argument("--report", default=None,
+                    help="instead of the bench line: per-config report for configs 'all' or e.g. '2,4'")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    if args.impl == "reference":
+    if args.report:
+        run_report(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_kv4(args)

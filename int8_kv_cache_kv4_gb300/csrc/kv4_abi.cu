@@ -34,7 +34,7 @@ bool stream_supported(const Layout&);
 long long stream_partials(const Layout&, int);
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
-                                 int32_t*, uint16_t*, float*, int32_t*, cudaStream_t);
+                                 int32_t*, uint16_t*, float*, int32_t*, long long*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -88,11 +88,13 @@ static Layout to_layout(const kv4_layout* l) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
-// [rows][n_split], and one int32 completion ticket per (sequence, kv head).
+// [rows][n_split], one int32 completion ticket per (sequence, kv head), and
+// the stream length the work-balanced kernel records for its separate merge.
 struct Workspace {
   float* part_o;
   float* part_lse;
   int32_t* tickets;
+  long long* u_total;
   size_t ticket_bytes;
   size_t bytes;
 };
@@ -118,10 +120,11 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   const size_t z = round256(rows * np * sizeof(float));
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
-  w.bytes = o + z + round256(w.ticket_bytes);
+  w.bytes = o + z + round256(w.ticket_bytes) + 256;
   w.part_o = (float*)base;
   w.part_lse = (float*)((char*)base + o);
   w.tickets = (int32_t*)((char*)base + o + z);
+  w.u_total = (long long*)((char*)base + o + z + round256(w.ticket_bytes));
   return w;
 }
 static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
@@ -248,7 +251,8 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   cudaError_t e;
   if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, st);
+                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total,
+                             st);
   else if (which == KV4_KERNEL_TCGEN05)
     e = launch_decode_tc(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                          p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,

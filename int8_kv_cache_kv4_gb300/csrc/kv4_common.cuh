@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "kv4.h"
 
 namespace kv4 {
@@ -40,6 +43,35 @@ __host__ __device__ inline int side_byte(int c, int t, int d_h) {
 __host__ __device__ inline int side_scale_entries(int S, int R) { return (S + R + 7) / 8 * 8; }
 __host__ __device__ inline long long side_block_bytes(int d_h, int S, int R) {
   return 2LL * (S + R) * d_h + 4LL * side_scale_entries(S, R);
+}
+
+// ------------------------------------------------ one-time launch setup
+// Per-device, per-kernel host setup (the dynamic shared-memory attribute and,
+// for the persistent kernel, its resident-CTA count) costs microseconds of
+// host time; it runs once per device and its result is cached.
+constexpr int kMaxDevices = 64;
+struct OnceSetup {
+  std::atomic<int> state[kMaxDevices];  // 1 = done (static storage: zero at start)
+  int value[kMaxDevices];
+  std::mutex mu;
+};
+template <class Init>
+inline cudaError_t once_per_device(OnceSetup& s, Init init, int* value) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!s.state[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.state[dev].load(std::memory_order_relaxed)) {
+      int v = 0;
+      if ((e = init(dev, &v)) != cudaSuccess) return e;
+      s.value[dev] = v;
+      s.state[dev].store(1, std::memory_order_release);
+    }
+  }
+  *value = s.value[dev];
+  return cudaSuccess;
 }
 
 // Upper bound on the grid of the work-balanced decode kernel (it sizes the

@@ -290,8 +290,17 @@ cudaError_t launch_decode_t(const Layout& L, const void* paged, const void* side
                             float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
                             int32_t* status, cudaStream_t st) {
   const size_t smem = decode_smem_bytes<D, G>(chunk_bytes(D, L.g));
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the attribute, once per device, for the largest chunk (group 32)
+  const size_t smem_max = decode_smem_bytes<D, G>(chunk_bytes(D, 32));
+  static OnceSetup setup;
+  int unused = 0;
+  cudaError_t e = once_per_device(
+      setup,
+      [&](int, int*) {
+        return cudaFuncSetAttribute(decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_max);
+      },
+      &unused);
   if (e != cudaSuccess) return e;
   dim3 grid(n4 + n8, L.h_kv, num_seqs);
   decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(
@@ -309,8 +318,15 @@ cudaError_t launch_bf16_decode_t(const Layout& L, const void* cache, const uint1
                                  int32_t* tickets, uint16_t* out, float* out_lse,
                                  int32_t* status, cudaStream_t st) {
   const size_t smem = decode_smem_bytes<D, G>(2 * kPage * D * 2);
-  cudaError_t e = cudaFuncSetAttribute(bf16_decode_split_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static OnceSetup setup;  // the shared-memory attribute, once per device
+  int unused = 0;
+  cudaError_t e = once_per_device(
+      setup,
+      [&](int, int*) {
+        return cudaFuncSetAttribute(bf16_decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+      },
+      &unused);
   if (e != cudaSuccess) return e;
   dim3 grid(n_split, L.h_kv, num_seqs);
   bf16_decode_split_kernel<D, G><<<grid, kThreads, smem, st>>>(

@@ -392,8 +392,15 @@ cudaError_t launch_mma_t(const Layout& L, const void* paged, const void* side, c
   constexpr int cb = 16 * D128 + 128 * NG;
   const size_t smem = ((sizeof(Smem<D128, G4>) + 127) / 128) * 128 +
                       (size_t)kWarps * kStagesMma * cb + 8 * 32 * 4 * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<NG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static OnceSetup setup;  // the shared-memory attribute, once per device
+  int unused = 0;
+  cudaError_t e = once_per_device(
+      setup,
+      [&](int, int*) {
+        return cudaFuncSetAttribute(decode_mma_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+      },
+      &unused);
   if (e != cudaSuccess) return e;
   dim3 grid(n4 + n8, L.h_kv, num_seqs);
   decode_mma_kernel<NG><<<grid, kThreads, smem, st>>>(

@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
-    float* __restrict__ out_lse, int32_t* status) {
+    float* __restrict__ out_lse, int32_t* status, int defer, long long* __restrict__ u_total) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   // holds at least one unit (the partial counts below rely on it).
   const long long U = sm.total;
   const int Cw = (int)min((long long)C, U);
+  if (defer && c == 0 && threadIdx.x == 0) *u_total = U;  // for stream_merge_kernel
   const long long u_begin = c < Cw ? U * c / Cw : U, u_end = c < Cw ? U * (c + 1) / Cw : U;
   if (u_begin < u_end) {
     const long long ex = sm.scan[threadIdx.x];
@@ -622,9 +623,10 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       // (one copy of the page body: unrolling it per stage overflows the
       // instruction cache)
       for (int jj = lo + warp; jj < hi; jj += kWarps) {
-        const int ST = it & 1;
+        const int ST = (int)((unsigned)it % kSStages);
         const int SO = ST * cb;  // stage offset
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][ST], (it >> 1) & 1));
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][ST], ((unsigned)it / kSStages) & 1));
         if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
         if (ok && sm.phys[warp][ST] >= 0) {
           const int pg = first_page + jj;
@@ -792,8 +794,9 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
       for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
-        const int st = it % kSStages;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], (it / kSStages) & 1));
+        const int st = (int)((unsigned)it % kSStages);
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], ((unsigned)it / kSStages) & 1));
         if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
         const uint8_t* stg = my_stages + (size_t)st * cb;
         if (ok) {
@@ -905,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       stream_query_setup<NG>(sm);
     }
     __syncthreads();  // B2: partial stored; next pair's query set up; comb, cs written
-    if (threadIdx.x == kTicketThread) {
+    if (threadIdx.x == kTicketThread && !defer) {
       // take this partial's ticket with release semantics (the barrier above
       // makes the CTA's partial stores part of what is released); the
       // result is read at the next boundary
@@ -939,6 +942,110 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   }
 }
 
+// Eq. A1 for pairs whose partials are spread over many CTAs (few, long
+// sequences): run after decode_stream_kernel, one CTA per (pair, query head),
+// eight warps splitting the pair's partials.  The partial positions follow
+// from the stream's share arithmetic (U recorded by the decode kernel).
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
+    Layout L, const int32_t* __restrict__ seq_lens, int B, const float* __restrict__ part_o,
+    const float* __restrict__ part_lse, const long long* __restrict__ u_total, int C,
+    uint16_t* __restrict__ out, float* __restrict__ out_lse) {
+  __shared__ long long red64[kMergeThreads / 32];
+  __shared__ float redf[kMergeThreads / 32];
+  __shared__ float4 acc_s[kMergeThreads / 32][32];
+  const int pair = blockIdx.x / SG, j = blockIdx.x % SG;
+  const int b = pair / L.h_kv, h = pair % L.h_kv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int len = clamp_len(__ldg(seq_lens + b), L);
+  if (len == 0) return;  // the decode kernel wrote its zero output
+  // stream index of the pair's first unit: units of all earlier sequences
+  long long mine = 0;
+  for (int bb = threadIdx.x; bb < b; bb += kMergeThreads) {
+    const int lb = clamp_len(__ldg(seq_lens + bb), L);
+    mine += (long long)L.h_kv * (prot_units(lb, L) + int4_units(lb, L));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) red64[warp] = mine;
+  __syncthreads();
+  long long pre = 0;
+  for (int w = 0; w < kMergeThreads / 32; ++w) pre += red64[w];
+  const int np = prot_units(len, L), n4 = int4_units(len, L);
+  const long long gs = pre + (long long)h * (np + n4);
+  const long long U = *u_total;
+  const int Cw = (int)min((long long)C, U);
+  const int c0 = np ? cta_of(gs, U, Cw) : 0;
+  const int n0 = np ? cta_of(gs + np - 1, U, Cw) - c0 + 1 : 0;
+  const int c1 = n4 ? cta_of(gs + np, U, Cw) : 0;
+  const int n1 = n4 ? cta_of(gs + np + n4 - 1, U, Cw) - c1 + 1 : 0;
+  const int n = n0 + n1;
+  auto pidx = [&](int k) { return k < n0 ? 2LL * pair + c0 + k : 2LL * pair + 1 + c1 + (k - n0); };
+  // log-normaliser of the whole pair: M = max z_k, Z = sum 2^(z_k - M)
+  float M = -INFINITY;
+  for (int k = threadIdx.x; k < n; k += kMergeThreads) M = fmaxf(M, __ldg(part_lse + pidx(k) * SG + j));
+  M = warp_max(M);
+  if (lane == 0) redf[warp] = M;
+  __syncthreads();
+  M = -INFINITY;
+  for (int w = 0; w < kMergeThreads / 32; ++w) M = fmaxf(M, redf[w]);
+  __syncthreads();
+  float Zl = 0.f;
+  if (M != -INFINITY)
+    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
+      const float z = __ldg(part_lse + pidx(k) * SG + j);
+      Zl += z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
+    }
+  Zl = warp_sum(Zl);
+  if (lane == 0) redf[warp] = Zl;
+  __syncthreads();
+  float Z = 0.f;
+  for (int w = 0; w < kMergeThreads / 32; ++w) Z += redf[w];
+  // sum_k w_k o_k: warp w takes partials k = w, w + 8, ...; lane: channels 4 lane ..
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int k0 = warp; k0 < n; k0 += 4 * (kMergeThreads / 32)) {
+      float wv[4];
+      float4 o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // four partials' loads in flight
+        const int k = k0 + u * (kMergeThreads / 32);
+        const float z = k < n ? __ldg(part_lse + pidx(k) * SG + j) : -INFINITY;
+        wv[u] = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
+        o[u] = wv[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(part_o + (pidx(k) * SG + j) * SD) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a.x = fmaf(wv[u], o[u].x, a.x);
+        a.y = fmaf(wv[u], o[u].y, a.y);
+        a.z = fmaf(wv[u], o[u].z, a.z);
+        a.w = fmaf(wv[u], o[u].w, a.w);
+      }
+    }
+  }
+  acc_s[warp][lane] = a;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < kMergeThreads / 32; ++w) {
+      t.x += acc_s[w][lane].x;
+      t.y += acc_s[w][lane].y;
+      t.z += acc_s[w][lane].z;
+      t.w += acc_s[w][lane].w;
+    }
+    const bool empty = !(Z > 0.f);
+    const float inv = empty ? 0.f : 1.f / Z;
+    const long long row = (long long)b * L.h_q + (long long)h * SG + j;
+    uint16_t* o = out + row * SD + 4 * lane;
+    o[0] = f32_to_bf16_bits(t.x * inv);
+    o[1] = f32_to_bf16_bits(t.y * inv);
+    o[2] = f32_to_bf16_bits(t.z * inv);
+    o[3] = f32_to_bf16_bits(t.w * inv);
+    if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
+  }
+}
+
 }  // namespace
 
 bool stream_supported(const Layout& L) { return L.d_h == SD && L.h_q == SG * L.h_kv; }
@@ -953,41 +1060,57 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                             const int32_t* block_table, float sm_scale, float* part_o,
                             float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                            int32_t* status, cudaStream_t st) {
+                            int32_t* status, long long* u_total, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   const size_t smem = ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kWarps * kSStages * cb;
-  cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<NG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // once per device: the shared-memory attribute and the resident-CTA capacity
+  static OnceSetup setup;
+  int grid = 0;
+  cudaError_t e = once_per_device(
+      setup,
+      [&](int dev, int* g) {
+        cudaError_t r = cudaFuncSetAttribute(decode_stream_kernel<NG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        int sms = 0, per_sm = 0;
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess)
+          r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NG>,
+                                                            kThreads, smem);
+        *g = std::max(1, std::min(kMaxStreamCtas, sms * std::max(1, per_sm)));
+        return r;
+      },
+      &grid);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NG>,
-                                                         kThreads, smem)) != cudaSuccess)
-    return e;
-  const int grid = std::max(1, std::min(kMaxStreamCtas, sms * std::max(1, per_sm)));
+  // With few pairs each one spreads over many CTAs; its merge then runs as a
+  // separate, wider kernel instead of in the last CTA.
+  const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
   decode_stream_kernel<NG><<<grid, kThreads, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
-      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status);
-  return cudaGetLastError();
+      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer, u_total);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (defer) {
+    stream_merge_kernel<<<num_seqs * L.h_kv * SG, kMergeThreads, 0, st>>>(
+        L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out, out_lse);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 cudaError_t launch_decode_stream(const Layout& L, const void* paged, const void* side,
                                  const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                                  const int32_t* block_table, float sm_scale, float* part_o,
                                  float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                                 int32_t* status, cudaStream_t st) {
+                                 int32_t* status, long long* u_total, cudaStream_t st) {
   switch (L.d_h / L.g) {
     case 4:
       return launch_stream_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
     case 2:
       return launch_stream_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
     case 1:
       return launch_stream_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -559,8 +559,15 @@ cudaError_t launch_tc_t(const Layout& L, const void* paged, const void* side, co
   constexpr int cb = 16 * tc::D + 128 * NG;
   const size_t smem = ((sizeof(Smem<tc::D, tc::G>) + 1023) / 1024) * 1024 +
                       (size_t)tc::kStagesTc * tc::kTilePages * cb;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static OnceSetup setup;  // the shared-memory attribute, once per device
+  int unused = 0;
+  cudaError_t e = once_per_device(
+      setup,
+      [&](int, int*) {
+        return cudaFuncSetAttribute(decode_tc_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+      },
+      &unused);
   if (e != cudaSuccess) return e;
   dim3 grid(n4 + n8, L.h_kv, num_seqs);
   decode_tc_kernel<NG><<<grid, kThreads, smem, st>>>(
