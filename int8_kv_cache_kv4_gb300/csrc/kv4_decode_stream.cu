@@ -41,8 +41,22 @@ namespace {
 
 constexpr int SD = 128, SG = 4;     // head_dim, query heads per kv head
 constexpr int kSStages = 2;         // bulk-copy stages per warp
-constexpr int kProtUnit = 8;        // side-cache slots per protected unit
-constexpr int kStreamMinBlocks = 5; // CTAs per SM the register budget targets
+constexpr int kSPages = 2;          // 16-token INT4 pages per unit (and per stage)
+constexpr int kProtUnit = 16;       // side-cache slots per protected unit
+// Online softmax with a lazily moved reference: the running reference m
+// (log2 domain) is raised only when a score exceeds it by more than this, so
+// probabilities 2^(s - m) stay below 2^kLazyLog2 = 256 (fp16-safe in P')
+// and the accumulators are rescaled on a few pages only.  The split's
+// log-normaliser m + log2(l) is exact for any reference.
+constexpr float kLazyLog2 = 8.f;
+// INT4 QK^T with the codes' exponent offset folded into the query side
+// (1024 + c against q, 1024 + 16 c against q / 16, accumulators started at
+// minus the constant part): exact-enough only while a group's constant part
+// (1024 x the sum of its query values) stays small, i.e. for 32-channel
+// groups; larger groups widen the codes to their exact values instead.
+template <int NG>
+__host__ __device__ constexpr bool fold_k_offset() { return NG >= 4; }
+constexpr int kStreamMinBlocks = 4; // CTAs per SM (shared memory: 4 x 56 KB)
 // The thread that keeps the segment bookkeeping and takes the completion
 // tickets: lane 0 of the last warp, which the round-robin unit assignment
 // never gives more units than the others.
@@ -60,6 +74,7 @@ struct Prod {
   const int32_t* bt;  // INT4 segment: block-table entries from its first page on
   int j;              // unit index inside segment s
   int hi;             // end of this CTA's units inside segment s
+  int np4;            // INT4 pages of segment s's sequence
   int more;           // a next unit exists
 };
 
@@ -72,15 +87,17 @@ struct Pend {
 
 struct __align__(16) StreamSmem {
   uint32_t qfrag4[8][32][4];        // INT4 path: block-diagonal query fragments
-  uint2 qfrag8[8][32];              // INT8 path: query fragments (a0, a2), rows = heads
-  float mrg_o[kWarps][SG][SD];      // per-warp unnormalised outputs at a segment end
+  uint2 qfrag8[8][16];              // INT8 path: query fragments (a0, a2) of lanes 0..15
+  union {
+    float mrg_o[kWarps][SG][SD];    // per-warp unnormalised outputs at a segment end
+    long long scan[kThreads];       // start-up: per-thread unit counts, then their prefix
+  };
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
   float qsum[SD / 32][SG];          // per 32-channel block sums of the query
   float kc[4][SG];                  // per (group, head): 1024 * sum of the group's A values
   float mrg_m[kWarps][SG];
   float mrg_l[kWarps][SG];
   float mrg_mt[kWarps][SG][SD / 32];
-  long long scan[kThreads];         // per-thread unit counts, then their exclusive prefix
   long long total;
   long long start_pre;              // stream index of the first unit of sequence start_b
   long long u_begin, u_end;         // this CTA's share of the stream
@@ -93,7 +110,7 @@ struct __align__(16) StreamSmem {
   int go;                           // comb is valid
   int new_q;                        // the next segment starts a new pair
   int start_b;
-  int32_t phys[kWarps][kSStages];   // INT4 stage: physical page, -1 = not loaded
+  int32_t phys[kWarps][kSStages][kSPages];  // INT4 stage: physical pages, < 0 = not loaded
   uint64_t bar[kWarps][kSStages];
   uint64_t qbar;                    // completion of the qraw copy
 };
@@ -108,10 +125,14 @@ __device__ inline int prot_units(int len, const Layout& L) {
   const int ns = len <= L.S ? len : L.S + L.R;
   return (ns + kProtUnit - 1) / kProtUnit;
 }
-__device__ inline int int4_units(int len, const Layout& L) {
+// INT4 pages of a sequence of length len (between the sinks and the window)
+__device__ inline int int4_pages(int len, const Layout& L) {
   const Regions rg = regions(len, L.S, L.R);
   return rg.rec_start > rg.sink_end ? (rg.rec_start + kPage - 1) / kPage - rg.sink_end / kPage
                                     : 0;
+}
+__device__ inline int int4_units(int len, const Layout& L) {
+  return (int4_pages(len, L) + kSPages - 1) / kSPages;
 }
 
 // Next non-empty segment (b == B when the stream is exhausted).
@@ -201,7 +222,7 @@ __device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
 #pragma unroll
     for (int o = 1; o < GS / 4; o <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, o);
     if ((ln & 7) == 0) sm.qsum[ln >> 3][jj] = sq;
-    if ((ln % (GS / 4)) == 0) sm.kc[ln / (GS / 4)][jj] = 1024.f * sa;
+    if ((ln % (GS / 4)) == 0) sm.kc[ln / (GS / 4)][jj] = fold_k_offset<NG>() ? 1024.f * sa : 0.f;
   }
   // INT4 fragments: A rows (group, head), block diagonal; k-index order as the
   // widened K words produce it.  The B values are 1024 + c for even channels
@@ -219,22 +240,22 @@ __device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int d = base + 4 * e2;
-        if (d / GS == grp) w |= q16(qr[jj * SD + d], k & 2) << (16 * e2);
+        if (d / GS == grp) w |= q16(qr[jj * SD + d], fold_k_offset<NG>() && (k & 2)) << (16 * e2);
       }
     }
     sm.qfrag4[s_][ln][k] = w;
   }
   // INT8 fragments: A rows = heads 0..3; k-step s, lane quad qd covers
   // channels 32*qd + 4*s + {0,1} (a0) and + {2,3} (a2)
-  for (int idx = t; idx < 8 * 32; idx += kThreads) {
-    const int s_ = idx >> 5, ln = idx & 31;
+  // (lanes 16..31, rows 4..7, read lane - 16's words: they duplicate heads
+  // 0..3, whose results those lanes never publish)
+  for (int idx = t; idx < 8 * 16; idx += kThreads) {
+    const int s_ = idx >> 4, ln = idx & 15;
     const int rr = ln >> 2, qq = ln & 3;
-    uint2 w = make_uint2(0u, 0u);
-    if (rr < SG) {
-      const uint16_t* src = qr + rr * SD + 32 * qq + 4 * s_;
-      w.x = q16(src[0], false) | (q16(src[1], false) << 16);
-      w.y = q16(src[2], false) | (q16(src[3], false) << 16);
-    }
+    const uint16_t* src = qr + rr * SD + 32 * qq + 4 * s_;
+    uint2 w;
+    w.x = q16(src[0], false) | (q16(src[1], false) << 16);
+    w.y = q16(src[2], false) | (q16(src[3], false) << 16);
     sm.qfrag8[s_][ln] = w;
   }
 }
@@ -435,12 +456,14 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   const int NS = L.S + L.R;
   const int NSP = side_scale_entries(L.S, L.R);
   const long long side_blk = side_block_bytes(D, L.S, L.R);
-  uint8_t* my_stages = stage_base + (size_t)warp * kSStages * cb;
+  constexpr int SB = kSPages * cb;  // stage bytes: two INT4 chunks or one 16-slot INT8 unit
+  static_assert(2 * kProtUnit * SD + 4 * kProtUnit <= SB, "an INT8 unit fits a stage");
+  uint8_t* my_stages = stage_base + (size_t)warp * kSStages * SB;
   // Producer (lane 0 of each warp; cursor in shared memory): advance to this
   // warp's next unit, moving over segments, and start reading its
   // block-table entry into a register, consumed only at the next issue so
   // the load's latency is not waited for here.
-  int pphys = -1;
+  int pphys = -1, pphys1 = -1;  // the unit's two pages (-2: no second page)
   // slow path: (pr.s, pr.j) may lie past its segment's end; move over
   // segments until it names a unit of this warp
   auto prod_next = [&](Prod& pr) {
@@ -457,22 +480,32 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     }
     pr.more = 1;
     pr.bt = block_table + (long long)pr.s.b * L.max_pages + min(pr.s.len, L.S) / kPage;
-    if (pr.s.type == 1) pphys = __ldg(pr.bt + pr.j);
+    pr.np4 = int4_pages(pr.s.len, L);
+    if (pr.s.type == 1) {
+      pphys = __ldg(pr.bt + kSPages * pr.j);
+      pphys1 = kSPages * pr.j + 1 < pr.np4 ? __ldg(pr.bt + kSPages * pr.j + 1) : -2;
+    }
   };
   auto issue = [&](int st) {
     Prod& pr = sm.prod[warp];
     const Seg& ps = pr.s;
     const int pj = pr.j;
     uint64_t* bar = &sm.bar[warp][st];
-    uint8_t* dst = my_stages + (size_t)st * cb;
+    uint8_t* dst = my_stages + (size_t)st * SB;
     if (ps.type == 1) {
-      const bool good = pphys >= 0 && pphys < L.num_pages;
-      sm.phys[warp][st] = good ? pphys : -1;  // published by the arrive below
-      if (good) {
-        mbar_arrive_expect_tx(bar, (uint32_t)cb);
-        bulk_g2s(dst, paged + ((long long)pphys * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
+      // pages 2j and 2j + 1 of the segment (the second may not exist: -2)
+      const bool good0 = pphys >= 0 && pphys < L.num_pages;
+      const bool good1 = pphys1 >= 0 && pphys1 < L.num_pages;
+      if (!good0 || (pphys1 != -2 && !good1)) set_status(status, KV4_STATUS_BAD_PAGE);
+      sm.phys[warp][st][0] = good0 ? pphys : -1;  // published by the arrive below
+      sm.phys[warp][st][1] = good1 ? pphys1 : -1;
+      const uint32_t bytes = (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u);
+      if (bytes) {
+        mbar_arrive_expect_tx(bar, bytes);
+        if (good0) bulk_g2s(dst, paged + ((long long)pphys * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
+        if (good1)
+          bulk_g2s(dst + cb, paged + ((long long)pphys1 * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
       } else {
-        set_status(status, KV4_STATUS_BAD_PAGE);
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
       }
     } else {
@@ -480,13 +513,14 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       const int slot0 = pj * kProtUnit;
       const int ns = ps.len <= L.S ? ps.len : NS;
       const uint32_t rows = (uint32_t)min(kProtUnit, ns - slot0);
-      sm.phys[warp][st] = 0;
-      mbar_arrive_expect_tx(bar, 2u * rows * D + 32u);
+      // scales of the 8-slot runs that hold copied rows (within the NSP padding)
+      const uint32_t sbytes = 16u * ((rows + 7) / 8);
+      mbar_arrive_expect_tx(bar, 2u * rows * D + 2u * sbytes);
       bulk_g2s(dst, blk + (long long)slot0 * D, rows * D, bar);
       bulk_g2s(dst + kProtUnit * D, blk + (long long)(NS + slot0) * D, rows * D, bar);
-      bulk_g2s(dst + 2 * kProtUnit * D, blk + 2LL * NS * D + 2 * slot0, 16u, bar);
-      bulk_g2s(dst + 2 * kProtUnit * D + 16, blk + 2LL * NS * D + 2LL * NSP + 2 * slot0, 16u,
-               bar);
+      bulk_g2s(dst + 2 * kProtUnit * D, blk + 2LL * NS * D + 2 * slot0, sbytes, bar);
+      bulk_g2s(dst + 2 * kProtUnit * D + 2 * kProtUnit, blk + 2LL * NS * D + 2LL * NSP + 2 * slot0,
+               sbytes, bar);
     }
   };
   if (lane == 0) {
@@ -507,7 +541,10 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       Prod& pr = sm.prod[warp];
       pr.j += kWarps;
       if (pr.j < pr.hi) {  // fast path: next unit of the same segment
-        if (pr.s.type == 1) pphys = __ldg(pr.bt + pr.j);
+        if (pr.s.type == 1) {
+          pphys = __ldg(pr.bt + kSPages * pr.j);
+          pphys1 = kSPages * pr.j + 1 < pr.np4 ? __ldg(pr.bt + kSPages * pr.j + 1) : -2;
+        }
       } else {
         prod_next(pr);
       }
@@ -525,10 +562,10 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   const int lm_p = lane >> 4;
   const uint32_t lm_off0 = lm_tok * 64 + 16 * ((lm_p) ^ ((lm_tok >> 1) & 3));
   const uint32_t lm_off1 = lm_tok * 64 + 16 * ((lm_p + 2) ^ ((lm_tok >> 1) & 3));
-  // INT8 V ldmatrix rows: matrix lane/8 = piece, row lane&7 = slot (swizzled)
-  const int l8_t = lane & 7, l8_m = lane >> 3;
-  const uint32_t l8_off0 = l8_t * D + 16 * ((l8_m) ^ l8_t);
-  const uint32_t l8_off1 = l8_t * D + 16 * ((l8_m + 4) ^ l8_t);
+  // INT8 V ldmatrix rows: matrix lane/8 = (slots 0-7 | 8-15) x (piece, piece + 1),
+  // row lane & 7; pieces are swizzled by slot
+  const int l8_t = lane & 7, l8_row = ((lane >> 3) & 1) * 8 + l8_t, l8_pp = lane >> 4;
+  constexpr int TK8[4] = {0, 1, 8, 9};  // INT8 unit: this lane's slots 2 * qd + TK8[e]
 
   int it = 0;  // this warp's consumed units (stage it % 2, phase (it / 2) & 1)
   int pend_t = 0;  // thread 0: ticket value returned for the pending partial
@@ -583,11 +620,12 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 
     if (cs.type == 1) {
       // ============================================= INT4 pages (eq. 5.1)
-      // QK^T: block-diagonal query rows against K codes widened with their
-      // exponent offset (1024 + c, 1024 + 16 c); the fragments carry the 1/16
-      // and the accumulators start at minus the constant 1024-part, so each
-      // row sums q_d c_d over its group.  Scores by eq. 5.1 per group; online
-      // softmax; PV against the centred V codes with P' = p * Delta_v; the
+      // Per unit of two pages.  QK^T: block-diagonal query rows against K
+      // codes widened with their exponent offset (1024 + c, 1024 + 16 c); the
+      // fragments carry the 1/16 and the accumulators start at minus the
+      // constant 1024-part, so each row sums q_d c_d over its group.  Scores
+      // by eq. 5.1 per group; one online-softmax step for both pages; then per
+      // page PV against the centred V codes with P' = p * Delta_v, and the
       // offset term sum_t p_t (Delta_t, m_t) of every group as one more MMA
       // whose A rows are the page's V metadata (group, Delta | m).
       const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qfrag4[0][0][0]) + lane;  // + 32 * s
@@ -601,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       const float kc1 = v1 ? sm.kc[g1][jh] : 0.f;
       const int first_page = rg.sink_end / kPage;
       const int len = cs.len;
+      const int last_j = cs.n - 1;
       float m_run = -INFINITY, l_run = 0.f;
       float mtacc[4] = {0.f, 0.f, 0.f, 0.f};  // rows (group, Delta | m), columns heads
       float acc[4][2][4];
@@ -610,93 +649,100 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
-      // per-lane byte offsets inside a stage
-      const uint8_t* k_lane = my_stages + r * 64 + row_byte(16 * qd, r, D);  // token r (+512: r + 8)
-      const uint8_t* km_lane = my_stages + meta_off_k(D) + (2 * qd * NG + g0) * 4;
-      const uint8_t* vm_lane = my_stages + meta_off_v(D, GS) + 2 * qd * NG * 4;
+      // per-lane shared addresses inside a stage (page p of a unit at + p * cb)
+      const uint32_t k_lane = smem_u32(my_stages) + r * 64 + row_byte(16 * qd, r, D);  // (+512: r + 8)
+      const uint32_t km_lane = smem_u32(my_stages) + meta_off_k(D) + (2 * qd * NG + g0) * 4;
+      const uint32_t vm_lane = smem_u32(my_stages) + meta_off_v(D, GS) + 2 * qd * NG * 4;
       const int mt_g = r >> 1;                  // offset-term MMA: this lane's A row group
       const bool mt_row = mt_g < NG;
       const uint32_t mt_sel = (r & 1) ? 0x7632u : 0x5410u;  // Delta (low) or m (high) halves
       const uint32_t v_lane = smem_u32(my_stages) + codes_off_v(D);
       constexpr int TK[4] = {0, 1, 8, 9};      // this lane's tokens: 2 * qd + TK[e]
 
-      // (one copy of the page body: unrolling it per stage overflows the
-      // instruction cache)
       for (int jj = lo + warp; jj < hi; jj += kWarps) {
         const int ST = (int)((unsigned)it % kSStages);
-        const int SO = ST * cb;  // stage offset
+        const int SO = ST * SB;  // stage offset
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][ST], ((unsigned)it / kSStages) & 1));
         if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
-        if (ok && sm.phys[warp][ST] >= 0) {
-          const int pg = first_page + jj;
-          const bool tail = (pg + 1) * kPage > len;
-          // ---------------- QK^T
-          const uint4 k0 = *reinterpret_cast<const uint4*>(k_lane + SO);
-          const uint4 k1 = *reinterpret_cast<const uint4*>(k_lane + SO + 512);
-          float d0[4] = {-kc0, -kc0, -kc1, -kc1}, d1[4] = {-kc0, -kc0, -kc1, -kc1};
-          float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int ph0 = sm.phys[warp][ST][0], ph1 = sm.phys[warp][ST][1];
+        if (ok) {
+          const int pg0 = first_page + kSPages * jj;
+          // ---------------- QK^T of both pages (k-step fragments shared)
+          uint4 kw[2][2];
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            kw[pp][0] = lds128(k_lane + SO + pp * cb);
+            kw[pp][1] = lds128(k_lane + SO + pp * cb + 512);
+          }
+          float d[2][2][4];  // [page][tokens 0-7 | 8-15][accumulator]
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int t2 = 0; t2 < 2; ++t2) {
+              d[pp][t2][0] = d[pp][t2][1] = -kc0;
+              d[pp][t2][2] = d[pp][t2][3] = -kc1;
+            }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            uint32_t x0[4], x1[4];
-            widen_k_biased(u4word(k0, u), x0);
-            widen_k_biased(u4word(k1, u), x1);
             const uint4 qa0 = qa_s[32 * (2 * u)], qa1 = qa_s[32 * (2 * u + 1)];
-            mma_f16(d0, qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
-            mma_f16(d1, qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
-            mma_f16(e0, qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
-            mma_f16(e1, qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
-          }
-          // ---------------- scores (eq. 5.1 per group) of this lane's 4 tokens
-          const float draw0[4] = {d0[0] + e0[0], d0[1] + e0[1], d1[0] + e1[0], d1[1] + e1[1]};
-          const float draw1[4] = {d0[2] + e0[2], d0[3] + e0[3], d1[2] + e1[2], d1[3] + e1[3]};
-          float sc[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float part = 0.f;
-            if (v0) {
-              const float2 dm = h2f2(*reinterpret_cast<const uint32_t*>(km_lane + SO + TK[e] * NG * 4));
-              part = fmaf(dm.x, draw0[e], dm.y * qs0);
-            }
-            if (v1) {
-              const float2 dm =
-                  h2f2(*reinterpret_cast<const uint32_t*>(km_lane + SO + TK[e] * NG * 4 + 8));
-              part += fmaf(dm.x, draw1[e], dm.y * qs1);
-            }
-            sc[e] = part;
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], 16);
-            sc[e] *= scale_log2;
-          }
-          if (!(pg * kPage >= rg.sink_end && (pg + 1) * kPage <= rg.rec_start)) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {  // first / last page: mask outside the region
-              const int pos = pg * kPage + 2 * qd + TK[e];
-              if (!(pos >= rg.sink_end && pos < rg.rec_start)) sc[e] = -INFINITY;
+            for (int pp = 0; pp < 2; ++pp) {
+              uint32_t x0[4], x1[4];
+              if (fold_k_offset<NG>()) {
+                widen_k_biased(u4word(kw[pp][0], u), x0);
+                widen_k_biased(u4word(kw[pp][1], u), x1);
+              } else {
+                widen_k(u4word(kw[pp][0], u), x0);
+                widen_k(u4word(kw[pp][1], u), x1);
+              }
+              mma_f16(d[pp][0], qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
+              mma_f16(d[pp][1], qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
+              mma_f16(d[pp][0], qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
+              mma_f16(d[pp][1], qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
             }
           }
-          // V metadata: Delta_v of every group for P', and this lane's offset-term row
-          MetaRow<NG> vm[4];
-          uint32_t mw[4];
+          // ---------------- scores (eq. 5.1 per group) of this lane's 8 tokens
+          float sc[2][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            vm[e].load(vm_lane + SO + TK[e] * NG * 4);
-            mw[e] = mt_row ? *reinterpret_cast<const uint32_t*>(vm_lane + SO + TK[e] * NG * 4 + mt_g * 4)
-                           : 0u;
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float raw0 = e < 2 ? d[pp][0][e] : d[pp][1][e - 2];      // row r   (group g0)
+              const float raw1 = e < 2 ? d[pp][0][e + 2] : d[pp][1][e];      // row r+8 (group g1)
+              float part = 0.f;
+              if (v0) {
+                const float2 dm = h2f2(lds32(km_lane + SO + pp * cb + TK[e] * NG * 4));
+                part = fmaf(dm.x, raw0, dm.y * qs0);
+              }
+              if (v1) {
+                const float2 dm = h2f2(lds32(km_lane + SO + pp * cb + TK[e] * NG * 4 + 8));
+                part += fmaf(dm.x, raw1, dm.y * qs1);
+              }
+              part += __shfl_xor_sync(0xffffffffu, part, 16);
+              sc[pp][e] = part * scale_log2;
+            }
+          // first / last unit of the segment, or a page not loaded: mask
+          if (jj == 0 || jj == last_j || ph0 < 0 || ph1 < 0) {
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int pos = (pg0 + pp) * kPage + 2 * qd + TK[e];
+                const bool in = (pp == 0 ? ph0 : ph1) >= 0 && pos >= rg.sink_end && pos < rg.rec_start;
+                if (!in) sc[pp][e] = -INFINITY;
+              }
           }
-          // ---------------- online softmax for head jh
-          float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+          // ---------------- online softmax for head jh over both pages
+          float tmax = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
+                             fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-          const float mnew = fmaxf(m_run, tmax);
-          const float mref = mnew == -INFINITY ? 0.f : mnew;
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) p[e] = ex2(sc[e] - mref);
-          if (__any_sync(0xffffffffu, mnew > m_run)) {
-            const float alpha = ex2(m_run - mref);
+          // lazy rescaling: the reference m_run moves only when a score
+          // exceeds it by more than kLazyLog2 (p then stays below 2^kLazyLog2)
+          if (__any_sync(0xffffffffu, tmax > m_run + kLazyLog2)) {
+            const float mnew = fmaxf(m_run, tmax);
+            const float alpha = mnew == -INFINITY ? 1.f : ex2(m_run - mnew);
             const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
             const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
 #pragma unroll
@@ -713,36 +759,54 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
             l_run *= alpha;
             m_run = mnew;
           }
-          l_run += (p[0] + p[1]) + (p[2] + p[3]);
-          // ---------------- PV
-          uint32_t va[4], vb[4];
-          ldsm_x4_trans(va, v_lane + SO + lm_off0);
-          ldsm_x4_trans(vb, v_lane + SO + lm_off1);
-          if (tail) {  // slots at or past the length were never written
+          const float mref = m_run == -INFINITY ? 0.f : m_run;
+          float pr_[2][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (pg * kPage + 2 * qd + TK[e] >= len) {
-                vm[e].zero();
-                mw[e] = 0u;
-              }
-          }
-          const uint32_t p01 = pack_f16(p[0], p[1]) & p_keep;
-          const uint32_t p23 = pack_f16(p[2], p[3]) & p_keep;
-          // offset term: rows (group, Delta | m) x tokens, against p
-          mma_f16(mtacc, __byte_perm(mw[0], mw[1], mt_sel), 0u, __byte_perm(mw[2], mw[3], mt_sel), 0u,
-                  p01, p23);
+          for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-          for (int P = 0; P < 4; ++P) {
-            const int grp = (P * 32) / GS;
-            const uint32_t b0 = hmul2(p01, lo_lo(vm[0].get(grp), vm[1].get(grp)));
-            const uint32_t b1 = hmul2(p23, lo_lo(vm[2].get(grp), vm[3].get(grp)));
-            const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
-            const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
-            uint32_t xl[4], xh[4];
-            widen_v(wlo, xl);
-            widen_v(whi, xh);
-            mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
-            mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
+            for (int e = 0; e < 4; ++e) pr_[pp][e] = ex2(sc[pp][e] - mref);  // masked: 0
+          l_run += ((pr_[0][0] + pr_[0][1]) + (pr_[0][2] + pr_[0][3])) +
+                   ((pr_[1][0] + pr_[1][1]) + (pr_[1][2] + pr_[1][3]));
+          // ---------------- PV, one page at a time
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            if ((pp == 0 ? ph0 : ph1) < 0) continue;  // not loaded: all its p are 0
+            MetaRow<NG> vm[4];
+            uint32_t mw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              vm[e].load_s(vm_lane + SO + pp * cb + TK[e] * NG * 4);
+              mw[e] = mt_row ? lds32(vm_lane + SO + pp * cb + TK[e] * NG * 4 + mt_g * 4) : 0u;
+            }
+            uint32_t va[4], vb[4];
+            ldsm_x4_trans(va, v_lane + SO + pp * cb + lm_off0);
+            ldsm_x4_trans(vb, v_lane + SO + pp * cb + lm_off1);
+            if ((pg0 + pp + 1) * kPage > len) {  // slots at or past the length were never written
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if ((pg0 + pp) * kPage + 2 * qd + TK[e] >= len) {
+                  vm[e].zero();
+                  mw[e] = 0u;
+                }
+            }
+            const uint32_t p01 = pack_f16(pr_[pp][0], pr_[pp][1]) & p_keep;
+            const uint32_t p23 = pack_f16(pr_[pp][2], pr_[pp][3]) & p_keep;
+            // offset term: rows (group, Delta | m) x tokens, against p
+            mma_f16(mtacc, __byte_perm(mw[0], mw[1], mt_sel), 0u, __byte_perm(mw[2], mw[3], mt_sel),
+                    0u, p01, p23);
+#pragma unroll
+            for (int P = 0; P < 4; ++P) {
+              const int grp = (P * 32) / GS;
+              const uint32_t b0 = hmul2(p01, lo_lo(vm[0].get(grp), vm[1].get(grp)));
+              const uint32_t b1 = hmul2(p23, lo_lo(vm[2].get(grp), vm[3].get(grp)));
+              const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
+              const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
+              uint32_t xl[4], xh[4];
+              widen_v(wlo, xl);
+              widen_v(whi, xh);
+              mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
+              mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
+            }
           }
         }
         refill(ST);
@@ -776,15 +840,19 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         for (int P = 0; P < 4; ++P)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const int d = 32 * P + 4 * r + 2 * hh;
-            sm.mrg_o[warp][hA][d] = acc[P][hh][0];
-            sm.mrg_o[warp][hB][d] = acc[P][hh][1];
-            sm.mrg_o[warp][hA][d + 1] = acc[P][hh][2];
-            sm.mrg_o[warp][hB][d + 1] = acc[P][hh][3];
+            const int dd = 32 * P + 4 * r + 2 * hh;
+            sm.mrg_o[warp][hA][dd] = acc[P][hh][0];
+            sm.mrg_o[warp][hB][dd] = acc[P][hh][1];
+            sm.mrg_o[warp][hA][dd + 1] = acc[P][hh][2];
+            sm.mrg_o[warp][hB][dd + 1] = acc[P][hh][3];
           }
       }
     } else {
       // ================================= INT8 protected units (App. A.3)
+      // Per unit of 16 side slots: QK^T with the query rows (heads) against
+      // the slots' codes widened exactly to fp16 (two 8-slot tiles), scores
+      // scaled by each slot's K scale; then PV with the transposed codes
+      // against P' = p * s_v.  Slots outside the protected set are masked.
       const int n_rec = cs.len > L.S ? cs.len - rg.rec_start : 0;
       const int ws_mod = L.R > 0 ? rg.rec_start % L.R : 0;
       float m8 = -INFINITY, l8 = 0.f;
@@ -793,42 +861,45 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       for (int P = 0; P < 8; ++P)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
+      const uint2* q8 = &sm.qfrag8[0][lane & 15];  // + 16 * s
       for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
         const int st = (int)((unsigned)it % kSStages);
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], ((unsigned)it / kSStages) & 1));
         if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
-        const uint8_t* stg = my_stages + (size_t)st * cb;
+        const uint32_t stg = smem_u32(my_stages) + st * SB;
         if (ok) {
-          const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0, sl0 + 1
-          const bool ok0 = slot_valid(sl0, cs.len, L, ws_mod, n_rec);
-          const bool ok1 = slot_valid(sl0 + 1, cs.len, L, ws_mod, n_rec);
-          // ---- QK: B = K codes of slot r, channels 32*qd + [0, 32)
-          const uint8_t* krow = stg + r * D;
-          const uint4 kA = *reinterpret_cast<const uint4*>(krow + 16 * ((2 * qd) ^ r));
-          const uint4 kB = *reinterpret_cast<const uint4*>(krow + 16 * ((2 * qd + 1) ^ r));
+          const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
+          bool okv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) okv[e] = slot_valid(sl0 + TK8[e], cs.len, L, ws_mod, n_rec);
+          // ---- QK: B = K codes of slot r (tile 0) and slot r + 8 (tile 1),
+          // channels 32*qd + [0, 32); pieces are swizzled by slot (r + 8 & 7 = r)
+          const uint4 kA0 = lds128(stg + r * D + 16 * ((2 * qd) ^ r));
+          const uint4 kB0 = lds128(stg + r * D + 16 * ((2 * qd + 1) ^ r));
+          const uint4 kA1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd) ^ r));
+          const uint4 kB1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd + 1) ^ r));
           float dq0[4] = {0.f, 0.f, 0.f, 0.f}, dq1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int s_ = 0; s_ < 8; ++s_) {
-            const uint32_t xb = (s_ < 4 ? u4word(kA, s_) : u4word(kB, s_ - 4)) ^ 0x80808080u;
-            const uint2 qa = sm.qfrag8[s_][lane];
-            mma_f16((s_ & 1) ? dq1 : dq0, qa.x, 0u, qa.y, 0u, i8pair(xb, 0x4140u),
-                    i8pair(xb, 0x4342u));
+            const uint32_t x0 = (s_ < 4 ? u4word(kA0, s_) : u4word(kB0, s_ - 4)) ^ 0x80808080u;
+            const uint32_t x1 = (s_ < 4 ? u4word(kA1, s_) : u4word(kB1, s_ - 4)) ^ 0x80808080u;
+            const uint2 qa = q8[16 * s_];
+            mma_f16(dq0, qa.x, 0u, qa.y, 0u, i8pair(x0, 0x4140u), i8pair(x0, 0x4342u));
+            mma_f16(dq1, qa.x, 0u, qa.y, 0u, i8pair(x1, 0x4140u), i8pair(x1, 0x4342u));
           }
-          // scores of head r (lanes r < 4) for slots sl0, sl0 + 1
-          const float2 ks = h2f2(*reinterpret_cast<const uint32_t*>(stg + 2 * kProtUnit * D + 4 * qd));
-          float s0 = (dq0[0] + dq1[0]) * ks.x * scale_log2;
-          float s1 = (dq0[1] + dq1[1]) * ks.y * scale_log2;
-          if (!ok0) s0 = -INFINITY;
-          if (!ok1) s1 = -INFINITY;
-          float tmax = fmaxf(s0, s1);
+          // scores of head r & 3 for the four slots
+          const float2 ksA = h2f2(lds32(stg + 2 * kProtUnit * D + 4 * qd));
+          const float2 ksB = h2f2(lds32(stg + 2 * kProtUnit * D + 16 + 4 * qd));
+          float sv[4] = {dq0[0] * ksA.x, dq0[1] * ksA.y, dq1[0] * ksB.x, dq1[1] * ksB.y};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sv[e] = okv[e] ? sv[e] * scale_log2 : -INFINITY;
+          float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-          const float mnew = fmaxf(m8, tmax);
-          const float mref = mnew == -INFINITY ? 0.f : mnew;
-          const float p0 = ex2(s0 - mref), p1 = ex2(s1 - mref);
-          if (__any_sync(0xffffffffu, mnew > m8)) {
-            const float alpha = ex2(m8 - mref);
+          if (__any_sync(0xffffffffu, tmax > m8 + kLazyLog2)) {  // lazy rescaling, as above
+            const float mnew = fmaxf(m8, tmax);
+            const float alpha = mnew == -INFINITY ? 1.f : ex2(m8 - mnew);
             const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
             const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
 #pragma unroll
@@ -841,20 +912,31 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
             l8 *= alpha;
             m8 = mnew;
           }
-          l8 += p0 + p1;
-          // ---- PV: A = V codes transposed (rows = channels), B = p * s_v
-          uint32_t vs2 = *reinterpret_cast<const uint32_t*>(stg + 2 * kProtUnit * D + 16 + 4 * qd);
-          vs2 &= (ok0 ? 0x0000FFFFu : 0u) | (ok1 ? 0xFFFF0000u : 0u);
-          const uint32_t pb = hmul2(pack_f16(p0, p1) & p_keep, vs2);
-          uint32_t va[4], vb[4];
-          const uint32_t vbase = smem_u32(stg + kProtUnit * D);
-          ldsm_x4_trans(va, vbase + l8_off0);  // pieces 0..3
-          ldsm_x4_trans(vb, vbase + l8_off1);  // pieces 4..7
+          const float mref = m8 == -INFINITY ? 0.f : m8;
+          float pv[4];
 #pragma unroll
-          for (int P = 0; P < 8; ++P) {
-            const uint32_t xb = (P < 4 ? va[P] : vb[P - 4]) ^ 0x80808080u;
-            // rows r / r+8 = channels 16P + 2r / 16P + 2r + 1; k = slots 2qd, 2qd+1
-            mma_f16(acc8[P], i8pair(xb, 0x4240u), i8pair(xb, 0x4341u), 0u, 0u, pb, 0u);
+          for (int e = 0; e < 4; ++e) pv[e] = ex2(sv[e] - mref);
+          l8 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          // ---- PV: A = V codes transposed (rows = channels, k = 16 slots), B = p * s_v
+          uint32_t vsA = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 4 * qd);
+          uint32_t vsB = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 16 + 4 * qd);
+          vsA &= (okv[0] ? 0x0000FFFFu : 0u) | (okv[1] ? 0xFFFF0000u : 0u);
+          vsB &= (okv[2] ? 0x0000FFFFu : 0u) | (okv[3] ? 0xFFFF0000u : 0u);
+          const uint32_t pb0 = hmul2(pack_f16(pv[0], pv[1]) & p_keep, vsA);
+          const uint32_t pb1 = hmul2(pack_f16(pv[2], pv[3]) & p_keep, vsB);
+          const uint32_t vbase = stg + kProtUnit * D;
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {  // pieces 2 c2 and 2 c2 + 1
+            uint32_t vr[4];  // (slots 0-7, piece), (slots 8-15, piece), same for piece + 1
+            ldsm_x4_trans(vr, vbase + l8_row * D + 16 * ((2 * c2 + l8_pp) ^ l8_t));
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t xlo = vr[2 * h2] ^ 0x80808080u, xhi = vr[2 * h2 + 1] ^ 0x80808080u;
+              // rows r / r+8 = channels 16P + 2r / 16P + 2r + 1; k = slots 2qd,
+              // 2qd+1 (a0, a1) and 2qd+8, 2qd+9 (a2, a3)
+              mma_f16(acc8[2 * c2 + h2], i8pair(xlo, 0x4240u), i8pair(xlo, 0x4341u),
+                      i8pair(xhi, 0x4240u), i8pair(xhi, 0x4341u), pb0, pb1);
+            }
           }
         }
         refill(st);
@@ -872,11 +954,11 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         const int hA = 2 * qd, hB = 2 * qd + 1;
 #pragma unroll
         for (int P = 0; P < 8; ++P) {
-          const int d = 16 * P + 2 * r;
-          sm.mrg_o[warp][hA][d] = acc8[P][0];
-          sm.mrg_o[warp][hB][d] = acc8[P][1];
-          sm.mrg_o[warp][hA][d + 1] = acc8[P][2];
-          sm.mrg_o[warp][hB][d + 1] = acc8[P][3];
+          const int dd = 16 * P + 2 * r;
+          sm.mrg_o[warp][hA][dd] = acc8[P][0];
+          sm.mrg_o[warp][hB][dd] = acc8[P][1];
+          sm.mrg_o[warp][hA][dd + 1] = acc8[P][2];
+          sm.mrg_o[warp][hB][dd + 1] = acc8[P][3];
         }
       }
     }
@@ -1062,7 +1144,10 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
                             float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
                             int32_t* status, long long* u_total, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
-  const size_t smem = ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kWarps * kSStages * cb;
+  constexpr size_t smem =
+      ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kWarps * kSStages * kSPages * cb;
+  // four CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
+  static_assert(smem <= 228 * 1024 / kStreamMinBlocks - 1024, "shared memory for 4 CTAs per SM");
   // once per device: the shared-memory attribute and the resident-CTA capacity
   static OnceSetup setup;
   int grid = 0;

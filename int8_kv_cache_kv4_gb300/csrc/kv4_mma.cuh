@@ -57,6 +57,36 @@ __device__ inline uint32_t u4word(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// Shared-memory loads at 32-bit shared addresses (base register + immediate
+// offsets).  Volatile: kept after the mbarrier wait and before the refill
+// that reuses the stage, which are volatile too.
+__device__ inline uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ inline uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ inline uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// (a & m) | c as one three-input logic op.  Written as C++ the same
+// expression compiled to two logic ops per value on sm_103a (measured with
+// the executed-instruction counters); the widening routines below are the
+// decode kernels' busiest code.
+__device__ inline uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+  return d;
+}
+
 // fp16 pairs: 1.0, -1032 (= -(1024 + 8)), 1/16, -72 (= -(64 + 8))
 constexpr uint32_t kOne2 = 0x3C003C00u, kM1032 = 0xE408E408u;
 constexpr uint32_t kSixteenth2 = 0x2C002C00u, kM72 = 0xD480D480u;
@@ -64,11 +94,11 @@ constexpr uint32_t kSixteenth2 = 0x2C002C00u, kM72 = 0xD480D480u;
 // Widen 8 V codes (two tokens x four channels, nibbles 0-3 and 4-7 of w) to
 // fp16 pairs (token a, token b) of the centred value c - 8, channel +0..+3.
 __device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
-  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
-  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+  x[0] = hfma2(and_or(w, 0x000F000Fu, 0x64006400u), kOne2, kM1032);
+  x[1] = hfma2(and_or(w, 0x00F000F0u, 0x64006400u), kSixteenth2, kM72);
   const uint32_t w8 = w >> 8;
-  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1032);
-  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM72);
+  x[2] = hfma2(and_or(w8, 0x000F000Fu, 0x64006400u), kOne2, kM1032);
+  x[3] = hfma2(and_or(w8, 0x00F000F0u, 0x64006400u), kSixteenth2, kM72);
 }
 
 // Widen one K code word (8 channels of one token) to 4 fp16 pairs without
@@ -76,11 +106,11 @@ __device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
 // i + 4 of the low nibbles), pairs 1 and 3 hold 1024 + 16 c (high nibbles).
 // The consumer folds the 1024 and the 16 into its other operand.
 __device__ inline void widen_k_biased(uint32_t w, uint32_t x[4]) {
-  x[0] = (w & 0x000F000Fu) | 0x64006400u;
-  x[1] = (w & 0x00F000F0u) | 0x64006400u;
+  x[0] = and_or(w, 0x000F000Fu, 0x64006400u);
+  x[1] = and_or(w, 0x00F000F0u, 0x64006400u);
   const uint32_t w8 = w >> 8;
-  x[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  x[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+  x[2] = and_or(w8, 0x000F000Fu, 0x64006400u);
+  x[3] = and_or(w8, 0x00F000F0u, 0x64006400u);
 }
 
 // fp16 pairs -1024 and -64
@@ -89,11 +119,11 @@ constexpr uint32_t kM1024 = 0xE400E400u, kM64 = 0xD400D400u;
 // Widen one K code word (8 channels of one token) to 4 fp16 pairs of exact
 // codes: pair i = (channel i, channel i + 4).
 __device__ inline void widen_k(uint32_t w, uint32_t x[4]) {
-  x[0] = hfma2((w & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
-  x[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+  x[0] = hfma2(and_or(w, 0x000F000Fu, 0x64006400u), kOne2, kM1024);
+  x[1] = hfma2(and_or(w, 0x00F000F0u, 0x64006400u), kSixteenth2, kM64);
   const uint32_t w8 = w >> 8;
-  x[2] = hfma2((w8 & 0x000F000Fu) | 0x64006400u, kOne2, kM1024);
-  x[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, kSixteenth2, kM64);
+  x[2] = hfma2(and_or(w8, 0x000F000Fu, 0x64006400u), kOne2, kM1024);
+  x[3] = hfma2(and_or(w8, 0x00F000F0u, 0x64006400u), kSixteenth2, kM64);
 }
 
 template <int NG>
@@ -102,6 +132,7 @@ template <>
 struct MetaRow<4> {
   uint4 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ void load_s(uint32_t a) { v = lds128(a); }
   __device__ uint32_t get(int g) const { return u4word(v, g); }
   __device__ void zero() { v = make_uint4(0u, 0u, 0u, 0u); }
 };
@@ -109,6 +140,7 @@ template <>
 struct MetaRow<2> {
   uint2 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ void load_s(uint32_t a) { v = lds64(a); }
   __device__ uint32_t get(int g) const { return g == 0 ? v.x : v.y; }
   __device__ void zero() { v = make_uint2(0u, 0u); }
 };
@@ -116,6 +148,7 @@ template <>
 struct MetaRow<1> {
   uint32_t v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ void load_s(uint32_t a) { v = lds32(a); }
   __device__ uint32_t get(int) const { return v; }
   __device__ void zero() { v = 0u; }
 };
