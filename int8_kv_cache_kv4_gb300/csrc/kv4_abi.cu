@@ -99,25 +99,24 @@ struct Workspace {
   size_t bytes;
 };
 static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-// Partial results per query row: the split plan's, or (max_splits = 0, a
-// layout the work-balanced kernel serves) the larger of that and the
-// work-balanced kernel's partial count spread over the rows.
-static size_t parts_per_row(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
-  size_t n = (size_t)p.total();
+// Rows of d partial-output values: [query row][split] for the split plan's
+// kernels, or (max_splits = 0, a layout the work-balanced kernel serves) at
+// least that kernel's partial results x G query heads.
+static size_t partial_rows(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
+  size_t n = (size_t)num_seqs * l->num_q_heads * (size_t)p.total();
   const Layout L = to_layout(l);
   if (max_splits == 0 && stream_supported(L) && num_seqs > 0) {
-    const size_t groups = (size_t)num_seqs * l->num_kv_heads;  // rows = groups * G
-    const size_t s = ((size_t)stream_partials(L, num_seqs) + groups - 1) / groups;
+    const size_t s =
+        (size_t)stream_partials(L, num_seqs) * (size_t)(l->num_q_heads / l->num_kv_heads);
     if (s > n) n = s;
   }
   return n;
 }
 static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits,
                            void* base) {
-  const size_t rows = (size_t)num_seqs * l->num_q_heads;
-  const size_t np = parts_per_row(l, num_seqs, p, max_splits);
-  const size_t o = round256(rows * np * l->head_dim * sizeof(float));
-  const size_t z = round256(rows * np * sizeof(float));
+  const size_t prow = partial_rows(l, num_seqs, p, max_splits);
+  const size_t o = round256(prow * l->head_dim * sizeof(float));
+  const size_t z = round256(prow * sizeof(float));
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
   w.bytes = o + z + round256(w.ticket_bytes) + 256;
