@@ -178,7 +178,7 @@ def run_kv4(args):
     from int8_kv_cache_kv4_gb300 import kv4
     kv4.load(build_if_missing=True)
     kv4.kv4_set_decode_kernel({"auto": kv4.KV4_KERNEL_AUTO, "tcgen05": kv4.KV4_KERNEL_TCGEN05,
-                               "stream": kv4.KV4_KERNEL_STREAM,
+                               "stream": kv4.KV4_KERNEL_STREAM, "sm": kv4.KV4_KERNEL_SM,
                                "mma": kv4.KV4_KERNEL_MMA_SYNC,
                                "cuda": kv4.KV4_KERNEL_CUDA_CORE}[args.kernel])
 
@@ -587,7 +587,7 @@ def main():
     ap.add_argument("--impl", default="kv4", choices=["kv4", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b64", choices=sorted(W.WORKLOADS))
     ap.add_argument("--max-splits", type=int, default=0)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "stream", "tcgen05", "mma", "cuda"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "sm", "stream", "tcgen05", "mma", "cuda"],
                     help="decode kernel (auto = the fastest measured for the layout)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")

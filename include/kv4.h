@@ -93,6 +93,7 @@ extern "C" {
 #define KV4_STATUS_NONFINITE 8 /* non-finite input, or metadata overflowing fp16 */
 #define KV4_STATUS_BAD_LEN 16  /* decode: seq_len < 0 or beyond the block-table capacity */
 #define KV4_STATUS_TIMEOUT 32  /* a bounded wait inside a kernel expired; its outputs are invalid */
+#define KV4_STATUS_INTERNAL 64 /* a kernel's internal consistency check failed; outputs invalid */
 
 /* Shape of one attention layer's cache.  All fields are host values. */
 typedef struct kv4_layout {
@@ -121,6 +122,10 @@ const char* kv4_status_string(int code);
  * STREAM cuts every (sequence, kv head) into 16-token INT4 pages and 8-slot
  * protected units and gives each CTA of a grid that fills the GPU an equal
  * share; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.
+ * SM runs the same stream with one CTA of sixteen warps per SM, the warps
+ * claiming units one at a time and merging their states without CTA-wide
+ * barriers (after a small kernel that prepares each pair's query fragments
+ * in the workspace); like STREAM it needs max_splits = 0.
  * TCGEN05 selects the tensor-memory (tcgen05.mma) split kernel, MMA_SYNC the
  * warp-level one, CUDA_CORE the fp32 one.  All compute the same result within
  * the stated tolerance.  A kernel that does not support the layout falls back
@@ -130,6 +135,7 @@ const char* kv4_status_string(int code);
 #define KV4_KERNEL_MMA_SYNC 2
 #define KV4_KERNEL_TCGEN05 3
 #define KV4_KERNEL_STREAM 4
+#define KV4_KERNEL_SM 5
 int kv4_set_decode_kernel(int which);
 
 /* Validate a layout; KV4_OK or a KV4_ERR_* code. */

@@ -35,6 +35,11 @@ long long stream_partials(const Layout&, int);
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
                                  int32_t*, uint16_t*, float*, int32_t*, long long*, cudaStream_t);
+bool sm_supported(const Layout&);
+size_t sm_qprep_bytes(const Layout&, int);
+cudaError_t launch_decode_sm(const Layout&, const void*, const void*, const uint16_t*,
+                             const int32_t*, int, const int32_t*, float, void*, float*, float*,
+                             int32_t*, uint16_t*, float*, int32_t*, long long*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -88,13 +93,15 @@ static Layout to_layout(const kv4_layout* l) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
-// [rows][n_split], one int32 completion ticket per (sequence, kv head), and
-// the stream length the work-balanced kernel records for its separate merge.
+// [rows][n_split], one int32 completion ticket per (sequence, kv head), the
+// stream length the work-balanced kernels record for their separate merge,
+// and (max_splits = 0) the per-pair query fragments of the SM kernel.
 struct Workspace {
   float* part_o;
   float* part_lse;
   int32_t* tickets;
   long long* u_total;
+  void* qprep;
   size_t ticket_bytes;
   size_t bytes;
 };
@@ -119,7 +126,10 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   const size_t z = round256(prow * sizeof(float));
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
-  w.bytes = o + z + round256(w.ticket_bytes) + 256;
+  const Layout L = to_layout(l);
+  const size_t qb = (max_splits == 0 && sm_supported(L)) ? sm_qprep_bytes(L, num_seqs) : 0;
+  w.bytes = o + z + round256(w.ticket_bytes) + 256 + round256(qb);
+  w.qprep = qb ? (void*)((char*)base + o + z + round256(w.ticket_bytes) + 256) : nullptr;
   w.part_o = (float*)base;
   w.part_lse = (float*)((char*)base + o);
   w.tickets = (int32_t*)((char*)base + o + z);
@@ -140,7 +150,7 @@ int kv4_abi_version(void) { return KV4_ABI_VERSION; }
 
 int kv4_set_decode_kernel(int which) {
   const int prev = g_decode_kernel;
-  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_STREAM) g_decode_kernel = which;
+  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_SM) g_decode_kernel = which;
   return prev;
 }
 
@@ -237,8 +247,6 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   const Workspace w = ws_layout(l, num_seqs, p, max_splits, workspace);
   cudaStream_t st = (cudaStream_t)stream;
   const Layout L = to_layout(l);
-  // Completion tickets for the fused eq. A1 merge start at zero on every call.
-  if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
   // head_dim 128 with 4 query heads per kv head runs a tensor-core kernel
   // (the warp-level mma kernel by default); other shapes the CUDA-core kernel.  All merge their
   // splits in the last-finishing CTA of each (sequence, kv head).
@@ -246,9 +254,18 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_STREAM;  // fastest measured on GB300
   if (which == KV4_KERNEL_STREAM && (max_splits > 0 || !stream_supported(L)))
     which = KV4_KERNEL_MMA_SYNC;
+  if (which == KV4_KERNEL_SM && (max_splits > 0 || !sm_supported(L))) which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
+  // Completion tickets for the fused eq. A1 merge start at zero on every call
+  // (the SM kernel's query-preparation kernel clears them itself).
+  if (which != KV4_KERNEL_SM &&
+      cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
+    return KV4_ERR_LAUNCH;
   cudaError_t e;
-  if (which == KV4_KERNEL_STREAM)
+  if (which == KV4_KERNEL_SM)
+    e = launch_decode_sm(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, w.qprep,
+                         w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total, st);
+  else if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
                              w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total,
                              st);

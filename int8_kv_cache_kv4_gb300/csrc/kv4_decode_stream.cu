@@ -35,38 +35,17 @@
 
 #include "kv4_decode_common.cuh"
 #include "kv4_mma.cuh"
+#include "kv4_stream_common.cuh"
 
 namespace kv4 {
 namespace {
 
-constexpr int SD = 128, SG = 4;     // head_dim, query heads per kv head
 constexpr int kSStages = 2;         // bulk-copy stages per warp
-constexpr int kSPages = 2;          // 16-token INT4 pages per unit (and per stage)
-constexpr int kProtUnit = 16;       // side-cache slots per protected unit
-// Online softmax with a lazily moved reference: the running reference m
-// (log2 domain) is raised only when a score exceeds it by more than this, so
-// probabilities 2^(s - m) stay below 2^kLazyLog2 = 256 (fp16-safe in P')
-// and the accumulators are rescaled on a few pages only.  The split's
-// log-normaliser m + log2(l) is exact for any reference.
-constexpr float kLazyLog2 = 8.f;
-// INT4 QK^T with the codes' exponent offset folded into the query side
-// (1024 + c against q, 1024 + 16 c against q / 16, accumulators started at
-// minus the constant part): exact-enough only while a group's constant part
-// (1024 x the sum of its query values) stays small, i.e. for 32-channel
-// groups; larger groups widen the codes to their exact values instead.
-template <int NG>
-__host__ __device__ constexpr bool fold_k_offset() { return NG >= 4; }
 constexpr int kStreamMinBlocks = 4; // CTAs per SM (shared memory: 4 x 56 KB)
 // The thread that keeps the segment bookkeeping and takes the completion
 // tickets: lane 0 of the last warp, which the round-robin unit assignment
 // never gives more units than the others.
 constexpr int kTicketThread = (kWarps - 1) * 32;
-
-// One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
-struct Seg {
-  long long start;  // stream index of its first unit
-  int b, h, type, len, n;
-};
 
 // Producer cursor of one warp: the next unit (segment, index) to copy in.
 struct Prod {
@@ -86,15 +65,12 @@ struct Pend {
 };
 
 struct __align__(16) StreamSmem {
-  uint32_t qfrag4[8][32][4];        // INT4 path: block-diagonal query fragments
-  uint2 qfrag8[8][16];              // INT8 path: query fragments (a0, a2) of lanes 0..15
+  QPrep qp;                         // the current pair's query fragments and sums
   union {
     float mrg_o[kWarps][SG][SD];    // per-warp unnormalised outputs at a segment end
     long long scan[kThreads];       // start-up: per-thread unit counts, then their prefix
   };
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
-  float qsum[SD / 32][SG];          // per 32-channel block sums of the query
-  float kc[4][SG];                  // per (group, head): 1024 * sum of the group's A values
   float mrg_m[kWarps][SG];
   float mrg_l[kWarps][SG];
   float mrg_mt[kWarps][SG][SD / 32];
@@ -115,69 +91,6 @@ struct __align__(16) StreamSmem {
   uint64_t qbar;                    // completion of the qraw copy
 };
 
-__device__ inline int clamp_len(int len, const Layout& L) {
-  return (len < 0 || len > L.max_pages * kPage) ? 0 : len;
-}
-// protected units of a sequence of length len: the sink slots alone while
-// len <= S, else every side slot (the ring is masked to the window)
-__device__ inline int prot_units(int len, const Layout& L) {
-  if (len <= 0) return 0;
-  const int ns = len <= L.S ? len : L.S + L.R;
-  return (ns + kProtUnit - 1) / kProtUnit;
-}
-// INT4 pages of a sequence of length len (between the sinks and the window)
-__device__ inline int int4_pages(int len, const Layout& L) {
-  const Regions rg = regions(len, L.S, L.R);
-  return rg.rec_start > rg.sink_end ? (rg.rec_start + kPage - 1) / kPage - rg.sink_end / kPage
-                                    : 0;
-}
-__device__ inline int int4_units(int len, const Layout& L) {
-  return (int4_pages(len, L) + kSPages - 1) / kSPages;
-}
-
-// Next non-empty segment (b == B when the stream is exhausted).
-__device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B) {
-  do {
-    s.start += s.n;
-    if (s.type == 0) {
-      s.type = 1;
-      s.n = int4_units(s.len, L);
-    } else {
-      s.type = 0;
-      if (++s.h == L.h_kv) {
-        s.h = 0;
-        ++s.b;
-        s.len = s.b < B ? clamp_len(__ldg(seq_lens + s.b), L) : 0;
-      }
-      s.n = prot_units(s.len, L);
-    }
-  } while (s.n == 0 && s.b < B);
-}
-
-// Atomic add with release semantics at GPU scope; returns the old value.
-__device__ inline int atom_add_release_gpu(int32_t* p, int v) {
-  int old;
-  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// CTA holding stream unit u when U >= C units are split over C CTAs as
-// [c*U/C, (c+1)*U/C) (every CTA then holds at least one unit).
-__device__ inline int cta_of(long long u, long long U, int C) {
-  return (int)(((u + 1) * C - 1) / U);
-}
-
-// Is side slot sl part of the protected set of a sequence of length len?
-// Sinks: sl < min(S, len).  Ring slot S + r: holds a position p of the final
-// window [ws, len) with p = r (mod R).
-__device__ inline bool slot_valid(int sl, int len, const Layout& L, int ws_mod, int n_rec) {
-  if (sl < L.S) return sl < len;
-  if (sl >= L.S + L.R) return false;
-  int d = sl - L.S - ws_mod;
-  if (d < 0) d += L.R;
-  return d < n_rec;
-}
-
 // Query of pair `row0` (G consecutive bf16 rows of D) -> fp16 copy, per-block
 // sums and both fragment sets.  Every warp must be past its last use of the
 // previous query (the caller's barrier).
@@ -189,75 +102,11 @@ __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __rest
   bulk_g2s(sm.qraw, q + row0 * SD, SG * SD * 2, &sm.qbar);
 }
 
-// A query element (bf16 bits) as fp16 bits, optionally divided by 16 (the
-// same two roundings wherever the value is used).
-__device__ inline uint32_t q16(uint32_t bf, bool sixteenth) {
-  __half h = __float2half_rn(bf16_bits_to_f32(bf));
-  if (sixteenth) h = __float2half_rn(__half2float(h) * 0.0625f);
-  return __half_as_ushort(h);
-}
-
 // Everything the units need from the query of the next pair, built from
-// sm.qraw once its copy has completed: per-32-channel-block sums, both
-// fragment sets, and per (group, head) the constant 1024-part of the INT4
-// QK sums.  No warp may still read the old values.
+// sm.qraw once its copy has completed.  No warp may still read the old values.
 template <int NG>
 __device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
-  constexpr int GS = SD / NG;
-  const int t = threadIdx.x;
-  const uint16_t* qr = sm.qraw;
-  {
-    // warp j: head j, lane: channels 4 * lane .. + 3
-    const int jj = t >> 5, ln = t & 31;
-    const uint2 raw = reinterpret_cast<const uint2*>(qr)[t];
-    const uint32_t b[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-    float sq = 0.f, sa = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      sq += bf16_bits_to_f32(b[i]);
-      sa += __half2float(__ushort_as_half((unsigned short)q16(b[i], i & 1)));
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-#pragma unroll
-    for (int o = 1; o < GS / 4; o <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, o);
-    if ((ln & 7) == 0) sm.qsum[ln >> 3][jj] = sq;
-    if ((ln % (GS / 4)) == 0) sm.kc[ln / (GS / 4)][jj] = fold_k_offset<NG>() ? 1024.f * sa : 0.f;
-  }
-  // INT4 fragments: A rows (group, head), block diagonal; k-index order as the
-  // widened K words produce it.  The B values are 1024 + c for even channels
-  // (low nibbles) and 1024 + 16 c for odd ones (high nibbles, k-indices 8..15
-  // of each step, A registers 2 and 3), so the odd channels' query values are
-  // stored divided by 16 (exact in fp16 for |q| >= 2^-10).
-  for (int idx = t; idx < 8 * 32 * 4; idx += kThreads) {
-    const int s_ = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
-    const int rr = ln >> 2, qq = ln & 3;
-    const int row = rr + 8 * (k & 1);
-    const int grp = row >> 2, jj = row & 3;
-    const int base = 32 * qq + 8 * (s_ >> 1) + 2 * (s_ & 1) + ((k & 2) ? 1 : 0);
-    uint32_t w = 0u;
-    if (grp < NG) {
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int d = base + 4 * e2;
-        if (d / GS == grp) w |= q16(qr[jj * SD + d], fold_k_offset<NG>() && (k & 2)) << (16 * e2);
-      }
-    }
-    sm.qfrag4[s_][ln][k] = w;
-  }
-  // INT8 fragments: A rows = heads 0..3; k-step s, lane quad qd covers
-  // channels 32*qd + 4*s + {0,1} (a0) and + {2,3} (a2)
-  // (lanes 16..31, rows 4..7, read lane - 16's words: they duplicate heads
-  // 0..3, whose results those lanes never publish)
-  for (int idx = t; idx < 8 * 16; idx += kThreads) {
-    const int s_ = idx >> 4, ln = idx & 15;
-    const int rr = ln >> 2, qq = ln & 3;
-    const uint16_t* src = qr + rr * SD + 32 * qq + 4 * s_;
-    uint2 w;
-    w.x = q16(src[0], false) | (q16(src[1], false) << 16);
-    w.y = q16(src[2], false) | (q16(src[3], false) << 16);
-    sm.qfrag8[s_][ln] = w;
-  }
+  build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x);
 }
 
 // Merge the warps' states of one segment and store its partial result P
@@ -628,15 +477,15 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       // page PV against the centred V codes with P' = p * Delta_v, and the
       // offset term sum_t p_t (Delta_t, m_t) of every group as one more MMA
       // whose A rows are the page's V metadata (group, Delta | m).
-      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qfrag4[0][0][0]) + lane;  // + 32 * s
+      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qp.qfrag4[0][0][0]) + lane;  // + 32 * s
       float qs0 = 0.f, qs1 = 0.f;
 #pragma unroll
       for (int bq = 0; bq < D / 32; ++bq) {
-        if (v0 && (bq * 32) / GS == g0) qs0 += sm.qsum[bq][jh];
-        if (v1 && (bq * 32) / GS == g1) qs1 += sm.qsum[bq][jh];
+        if (v0 && (bq * 32) / GS == g0) qs0 += sm.qp.qsum[bq][jh];
+        if (v1 && (bq * 32) / GS == g1) qs1 += sm.qp.qsum[bq][jh];
       }
-      const float kc0 = v0 ? sm.kc[g0][jh] : 0.f;
-      const float kc1 = v1 ? sm.kc[g1][jh] : 0.f;
+      const float kc0 = v0 ? sm.qp.kc[g0][jh] : 0.f;
+      const float kc1 = v1 ? sm.qp.kc[g1][jh] : 0.f;
       const int first_page = rg.sink_end / kPage;
       const int len = cs.len;
       const int last_j = cs.n - 1;
@@ -861,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       for (int P = 0; P < 8; ++P)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
-      const uint2* q8 = &sm.qfrag8[0][lane & 15];  // + 16 * s
+      const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
       for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
         const int st = (int)((unsigned)it % kSStages);
         const bool ok =
@@ -1137,6 +986,17 @@ long long stream_partials(const Layout& L, int num_seqs) {
   return 2LL * num_seqs * L.h_kv + kMaxStreamCtas;
 }
 
+// Eq. A1 for every pair from the partials a work-balanced decode kernel left
+// on a grid of C CTAs (U: the stream length it recorded).
+cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
+                                const float* part_o, const float* part_lse,
+                                const long long* u_total, int C, uint16_t* out, float* out_lse,
+                                cudaStream_t st) {
+  stream_merge_kernel<<<num_seqs * L.h_kv * SG, kMergeThreads, 0, st>>>(
+      L, seq_lens, num_seqs, part_o, part_lse, u_total, C, out, out_lse);
+  return cudaGetLastError();
+}
+
 template <int NG>
 cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side,
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
@@ -1173,11 +1033,8 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
       sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer, u_total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (defer) {
-    stream_merge_kernel<<<num_seqs * L.h_kv * SG, kMergeThreads, 0, st>>>(
-        L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out, out_lse);
-    e = cudaGetLastError();
-  }
+  if (defer) e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out,
+                                     out_lse, st);
   return e;
 }
 

@@ -29,12 +29,14 @@ KV4_STATUS_BAD_SEQ = 4
 KV4_STATUS_NONFINITE = 8
 KV4_STATUS_BAD_LEN = 16
 KV4_STATUS_TIMEOUT = 32
+KV4_STATUS_INTERNAL = 64
 
 KV4_KERNEL_AUTO = 0
 KV4_KERNEL_CUDA_CORE = 1
 KV4_KERNEL_MMA_SYNC = 2
 KV4_KERNEL_TCGEN05 = 3
 KV4_KERNEL_STREAM = 4
+KV4_KERNEL_SM = 5
 
 
 class kv4_layout(ctypes.Structure):

@@ -1,5 +1,7 @@
-"""GPU parity of the work-balanced decode kernel's scheduling: the stream of
-8-slot protected units and 16-token INT4 pages cut into equal CTA shares.
+"""GPU parity of the work-balanced decode kernels' scheduling: the stream of
+16-slot protected units and two-page INT4 units cut into equal CTA shares,
+walked by warps in lock step (STREAM) or claimed one unit at a time by the
+warps of one CTA per SM (SM).
 Cases aim at the bookkeeping -- pairs spread over many CTAs, CTAs without
 work, empty and very short sequences, partly filled recent-window rings,
 more sequences than threads in the start search -- and compare with the
@@ -14,12 +16,13 @@ from kv4_case import Case, compare_outputs  # noqa: E402
 from int8_kv_cache_kv4_gb300 import kv4  # noqa: E402
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _lib():
+@pytest.fixture(scope="module", autouse=True, params=[kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_SM],
+                ids=["stream", "sm"])
+def _lib(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     kv4.load(build_if_missing=True)
-    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_STREAM)
+    prev = kv4.kv4_set_decode_kernel(request.param)
     yield
     kv4.kv4_set_decode_kernel(prev)
 
