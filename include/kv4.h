@@ -124,8 +124,10 @@ const char* kv4_status_string(int code);
  * share; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.
  * SM runs the same stream with one CTA of sixteen warps per SM, the warps
  * claiming units one at a time and merging their states without CTA-wide
- * barriers (after a small kernel that prepares each pair's query fragments
- * in the workspace); like STREAM it needs max_splits = 0.
+ * barriers, between a small kernel that prepares each pair's query
+ * fragments in the workspace and a kernel that merges each pair's partials
+ * (eq. A1); like STREAM it needs max_splits = 0.  It balances work best and
+ * is slower than STREAM on GB300 (measured), so AUTO does not pick it.
  * TCGEN05 selects the tensor-memory (tcgen05.mma) split kernel, MMA_SYNC the
  * warp-level one, CUDA_CORE the fp32 one.  All compute the same result within
  * the stated tolerance.  A kernel that does not support the layout falls back

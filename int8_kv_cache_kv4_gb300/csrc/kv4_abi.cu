@@ -39,7 +39,7 @@ bool sm_supported(const Layout&);
 size_t sm_qprep_bytes(const Layout&, int);
 cudaError_t launch_decode_sm(const Layout&, const void*, const void*, const uint16_t*,
                              const int32_t*, int, const int32_t*, float, void*, float*, float*,
-                             int32_t*, uint16_t*, float*, int32_t*, long long*, cudaStream_t);
+                             uint16_t*, float*, int32_t*, long long*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -257,14 +257,14 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   if (which == KV4_KERNEL_SM && (max_splits > 0 || !sm_supported(L))) which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
   // Completion tickets for the fused eq. A1 merge start at zero on every call
-  // (the SM kernel's query-preparation kernel clears them itself).
+  // (the SM kernel takes none: its pairs are merged by a separate kernel).
   if (which != KV4_KERNEL_SM &&
       cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
     return KV4_ERR_LAUNCH;
   cudaError_t e;
   if (which == KV4_KERNEL_SM)
     e = launch_decode_sm(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, w.qprep,
-                         w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total, st);
+                         w.part_o, w.part_lse, out, out_lse, dev_status, w.u_total, st);
   else if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
                              w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total,

@@ -9,14 +9,15 @@
 // no barrier: each warp claims the CTA's units one at a time from a shared
 // counter, streams them through its own two-stage ring of bulk copies, and
 // keeps one online-softmax state for the segment (a pair's protected or INT4
-// units) it is in.  A warp that moves on to another segment merges its state
-// into that segment's slot in shared memory, under the slot's lock; the warp
-// that brings the slot's unit count up to the segment's units in this CTA
-// writes the partial result (2 * pair + region + c, as in the work-balanced
-// kernel), takes the pair's completion ticket and, if it was the last, merges
-// the pair's partials into the output (eq. A1).  A warp that runs ahead never
-// waits for the others except on a slot or query buffer whose earlier user
-// has not finished, so the SM stays busy until its units are done.
+// units) it is in.  A warp that moves on to another segment hands its state
+// over without a lock: it takes the segment's published state (if any),
+// merges it into its own registers and publishes the result; the warp whose
+// state comes to cover all of the segment's units in this CTA writes the
+// partial result (2 * pair + region + c, as in the work-balanced kernel).
+// The separate merge kernel then applies eq. A1 to every pair's partials.  A
+// warp that runs ahead never waits for the others except on its own deposit
+// area or a query buffer whose earlier pair has not finished, so the SM stays
+// busy until its units are done.
 //
 // The per-pair query fragments are built once per call by
 // decode_sm_qprep_kernel and bulk-copied into one of four buffers when a
@@ -111,66 +112,11 @@ __device__ inline int pair_units_in(const Seg& s, const Layout& L, long long ub,
   return (int)(min(ue, gs + np + n4) - max(ub, gs));
 }
 
-// Eq. A1 over the n0 + n1 partials of one pair for query head j, by one warp
-// (partials s0 + c0 + k, then s0 + 1 + c1 + k).
-__device__ inline void combine_head(const float* __restrict__ part_o,
-                                    const float* __restrict__ part_lse, long long s0, int c0,
-                                    int n0, int c1, int n1, long long row, int j,
-                                    uint16_t* __restrict__ out, float* __restrict__ out_lse) {
-  const int lane = threadIdx.x & 31;
-  const int n = n0 + n1;
-  auto pidx = [&](int k) { return k < n0 ? s0 + c0 + k : s0 + 1 + c1 + (k - n0); };
-  float M = -INFINITY;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(part_lse + pidx(k) * SG + j));
-  M = warp_max(M);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Zl = 0.f;
-  if (M != -INFINITY) {
-    for (int k0 = 0; k0 < n; k0 += 32) {
-      const int k = k0 + lane;
-      const float z = k < n ? __ldcg(part_lse + pidx(k) * SG + j) : -INFINITY;
-      const float wl = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
-      Zl += wl;
-      const int nr = min(32, n - k0);
-      for (int rr = 0; rr < nr; rr += 4) {  // four partials' loads in flight
-        float wv[4];
-        float4 o[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wv[u] = __shfl_sync(0xffffffffu, wl, (rr + u) & 31);
-          const bool use = rr + u < nr && wv[u] != 0.f;
-          o[u] = use ? __ldcg(reinterpret_cast<const float4*>(part_o + (pidx(k0 + rr + u) * SG + j) * SD) + lane)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!use) wv[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          acc.x = fmaf(wv[u], o[u].x, acc.x);
-          acc.y = fmaf(wv[u], o[u].y, acc.y);
-          acc.z = fmaf(wv[u], o[u].z, acc.z);
-          acc.w = fmaf(wv[u], o[u].w, acc.w);
-        }
-      }
-    }
-  }
-  const float Z = warp_sum(Zl);
-  const bool empty = !(Z > 0.f);
-  const float inv = empty ? 0.f : 1.f / Z;
-  uint16_t* o = out + row * SD + 4 * lane;  // the output need only be 2-byte aligned
-  o[0] = f32_to_bf16_bits(acc.x * inv);
-  o[1] = f32_to_bf16_bits(acc.y * inv);
-  o[2] = f32_to_bf16_bits(acc.z * inv);
-  o[3] = f32_to_bf16_bits(acc.w * inv);
-  if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
-}
-
-// One CTA per pair: the pair's query fragments and sums (QPrep), and its
-// completion ticket cleared.
+// One CTA per pair: the pair's query fragments and sums (QPrep).
 template <int NG>
 __global__ void __launch_bounds__(128) decode_sm_qprep_kernel(Layout L,
                                                               const uint16_t* __restrict__ q,
-                                                              QPrep* __restrict__ qprep,
-                                                              int32_t* __restrict__ tickets) {
+                                                              QPrep* __restrict__ qprep) {
   __shared__ __align__(16) uint16_t qraw[SG * SD];
   __shared__ QPrep qp;
   const int pair = blockIdx.x;
@@ -178,7 +124,6 @@ __global__ void __launch_bounds__(128) decode_sm_qprep_kernel(Layout L,
   const uint4* src = reinterpret_cast<const uint4*>(q + row0 * SD);
   if (threadIdx.x < SG * SD / 8)  // G rows of D bf16: 64 x 16 B
     reinterpret_cast<uint4*>(qraw)[threadIdx.x] = __ldg(src + threadIdx.x);
-  if (threadIdx.x == 0) tickets[pair] = 0;
   __syncthreads();
   build_qprep<NG>(qraw, qp, threadIdx.x);
   __syncthreads();
@@ -192,8 +137,8 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
     Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
     const QPrep* __restrict__ qprep, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
-    float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
-    float* __restrict__ out_lse, int32_t* status, int defer, long long* __restrict__ u_total) {
+    float* __restrict__ part_lse, uint16_t* __restrict__ out, float* __restrict__ out_lse,
+    int32_t* status, long long* __restrict__ u_total) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -242,7 +187,7 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
   __syncthreads();
   const long long U = sm.total;
   const int Cw = (int)min((long long)C, U);
-  if (defer && c == 0 && threadIdx.x == 0) *u_total = U;  // for stream_merge_kernel
+  if (c == 0 && threadIdx.x == 0) *u_total = U;  // for stream_merge_kernel
   const long long u_begin = c < Cw ? U * c / Cw : U, u_end = c < Cw ? U * (c + 1) / Cw : U;
   if (threadIdx.x == 0) {
     sm.u_begin = u_begin;
@@ -478,7 +423,7 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
   // merges it into its own registers, and publishes the result in its own
   // deposit area; if another state was published meanwhile it takes that one
   // too.  The warp whose state comes to cover all of the segment's units in
-  // this CTA writes the partial result and takes the pair's ticket.  A warp
+  // this CTA writes the partial result.  A warp
   // waits only for its own deposit area (its previous deposit not yet taken)
   // or a segment entry still serving an older segment.
   auto retire = [&]() {
@@ -637,27 +582,6 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
     }
     if (lane < SG) part_lse[P * SG + lane] = Lh > 0.f ? (Mh + log2f(Lh)) * kLn2 : -INFINITY;
     __syncwarp();
-    if (!defer) {
-      // this partial's ticket (release: the warp's partial stores come first)
-      int last = 0;
-      const int np = prot_units(cur_len, L), n4 = int4_units(cur_len, L);
-      const long long gs = cur_type == 0 ? cur_start : cur_start - np;
-      const int c0 = np ? cta_of(gs, U, Cw) : 0;
-      const int n0 = np ? cta_of(gs + np - 1, U, Cw) - c0 + 1 : 0;
-      const int c1 = n4 ? cta_of(gs + np, U, Cw) : 0;
-      const int n1 = n4 ? cta_of(gs + np + n4 - 1, U, Cw) - c1 + 1 : 0;
-      if (lane == 0) {
-        __threadfence();
-        last = atom_add_release_gpu(&tickets[pair], 1) == n0 + n1 - 1;
-        if (last) __threadfence();  // acquire: the other CTAs' partials are visible
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        const long long row0 = (long long)cur_b * L.h_q + (long long)cur_h * SG;
-        for (int j = 0; j < SG; ++j)
-          combine_head(part_o, part_lse, 2LL * pair, c0, n0, c1, n1, row0 + j, j, out, out_lse);
-      }
-    }
   };
 
   int it = 0;  // this warp's consumed units (stage it % 2, phase (it / 2) & 1)
@@ -952,7 +876,7 @@ template <int NG>
 cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, const uint16_t* q,
                         const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
                         float sm_scale, void* qprep, float* part_o, float* part_lse,
-                        int32_t* tickets, uint16_t* out, float* out_lse, int32_t* status,
+                        uint16_t* out, float* out_lse, int32_t* status,
                         long long* u_total, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
@@ -974,15 +898,17 @@ cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, co
       &grid);
   if (e != cudaSuccess) return e;
   const int pairs = num_seqs * L.h_kv;
-  decode_sm_qprep_kernel<NG><<<pairs, 128, 0, st>>>(L, q, (QPrep*)qprep, tickets);
+  decode_sm_qprep_kernel<NG><<<pairs, 128, 0, st>>>(L, q, (QPrep*)qprep);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int defer = 8LL * pairs < grid ? 1 : 0;
   decode_sm_kernel<NG><<<grid, kMThreads, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, (const QPrep*)qprep, seq_lens, num_seqs,
-      block_table, sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer,
+      block_table, sm_scale * kLog2e, part_o, part_lse, out, out_lse, status,
       u_total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (defer) e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out,
+  // every pair's partials are merged by the separate merge kernel: a warp of
+  // this kernel that merged them itself would hold up its claimed units for
+  // the whole of the pair's eq. A1 (measured: slower than one more launch)
+  e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out,
                                      out_lse, st);
   return e;
 }
@@ -990,18 +916,18 @@ cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, co
 cudaError_t launch_decode_sm(const Layout& L, const void* paged, const void* side,
                              const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                              const int32_t* block_table, float sm_scale, void* qprep,
-                             float* part_o, float* part_lse, int32_t* tickets, uint16_t* out,
+                             float* part_o, float* part_lse, uint16_t* out,
                              float* out_lse, int32_t* status, long long* u_total, cudaStream_t st) {
   switch (L.d_h / L.g) {
     case 4:
       return launch_sm_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, u_total, st);
     case 2:
       return launch_sm_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, u_total, st);
     case 1:
       return launch_sm_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, u_total, st);
   }
   return cudaErrorInvalidValue;
 }
