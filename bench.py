@@ -41,8 +41,9 @@ UNIT = "tokens/s"
 # summarised in profiles/decode_stream_kernel_qwen3_8b_b64.md.  Keyed by a
 # hash of the sources that kernel is compiled from: once they change, the
 # figure no longer describes the kernel and the bench reports null.
-KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_mma.cuh", "kv4_decode_common.cuh", "kv4_common.cuh"]
-TRAFFIC = {("07d998d06c4da89f", "qwen3_8b_b64"): 388357376 + 4740864}
+KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
+                  "kv4_common.cuh"]
+TRAFFIC = {("3562fa66b809959f", "qwen3_8b_b64"): 388392448 + 4488192}
 
 
 # ------------------------------------------------------------------ helpers
