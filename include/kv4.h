@@ -151,7 +151,10 @@ size_t kv4_bf16_cache_bytes(const kv4_layout* layout);  /* comparator pages */
 /* Number of context splits per (sequence, kv head) that the split kernels use
  * for `num_seqs` sequences when given `max_splits` (0 = automatic), and the
  * workspace (device scratch: partial outputs, log-normalisers and completion
- * counters) kv4_decode_attn needs with that max_splits, for any kernel choice. */
+ * counters) kv4_decode_attn needs with that max_splits.  The size covers every
+ * kernel choice except that the SM kernel's per-pair query fragments (5,248 B
+ * per sequence and kv head) are counted only while KV4_KERNEL_SM is selected:
+ * select it before sizing, or kv4_decode_attn returns KV4_ERR_WORKSPACE. */
 int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 

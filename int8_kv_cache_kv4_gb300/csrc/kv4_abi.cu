@@ -95,7 +95,8 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
 // [rows][n_split], one int32 completion ticket per (sequence, kv head), the
 // stream length the work-balanced kernels record for their separate merge,
-// and (max_splits = 0) the per-pair query fragments of the SM kernel.
+// and (max_splits = 0, while the SM kernel is selected) its per-pair query
+// fragments.
 struct Workspace {
   float* part_o;
   float* part_lse;
@@ -127,7 +128,10 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
   const Layout L = to_layout(l);
-  const size_t qb = (max_splits == 0 && sm_supported(L)) ? sm_qprep_bytes(L, num_seqs) : 0;
+  // (the SM kernel's query fragments: only while it is the selected kernel)
+  const size_t qb = (max_splits == 0 && sm_supported(L) && g_decode_kernel == KV4_KERNEL_SM)
+                        ? sm_qprep_bytes(L, num_seqs)
+                        : 0;
   w.bytes = o + z + round256(w.ticket_bytes) + 256 + round256(qb);
   w.qprep = qb ? (void*)((char*)base + o + z + round256(w.ticket_bytes) + 256) : nullptr;
   w.part_o = (float*)base;

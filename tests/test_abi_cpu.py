@@ -64,6 +64,23 @@ def test_split_plan_and_workspace(lib):
     assert kv4.workspace_bytes(lay, 0) == 0 or kv4.workspace_bytes(lay, 0) >= 0
 
 
+def test_workspace_holds_sm_query_fragments_only_while_selected(lib):
+    # the SM kernel's per-pair query fragments (5248 B per sequence and kv
+    # head) are part of the workspace only while that kernel is selected
+    lay = kv4.make_layout(max_seqs=64, num_pages=40000, max_pages_per_seq=512)
+    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_AUTO)
+    try:
+        auto = kv4.workspace_bytes(lay, 64)
+        kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_SM)
+        sm = kv4.workspace_bytes(lay, 64)
+        fixed = kv4.workspace_bytes(lay, 64, max_splits=2)   # the SM kernel needs max_splits = 0
+        kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_AUTO)
+        assert fixed == kv4.workspace_bytes(lay, 64, max_splits=2)
+    finally:
+        kv4.kv4_set_decode_kernel(prev)
+    assert sm - auto == (64 * 8 * 5248 + 255) // 256 * 256
+
+
 def test_null_arguments_rejected_on_host(lib):
     lay = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
     rc = lib.kv4_quant_append(ctypes.byref(lay), None, None, None, None, None, None, 3, None,
