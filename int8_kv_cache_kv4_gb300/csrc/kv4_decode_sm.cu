@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
         const long long ub = (long long)L.h_kv * pu;
         if (u_begin < pre + ub) {
           Seg sg;
+          sg.cs = 0;
           sg.b = b;
           sg.len = len;
           const long long off = u_begin - pre;
@@ -597,6 +598,7 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
       if (cur_sig >= 0) retire();
       const int pord = rc.pord;
       Seg sg;
+      sg.cs = 0;
       sg.start = rc.start;
       sg.b = rc.b;
       sg.h = rc.h;
@@ -863,8 +865,8 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
 
 cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
                                 const float* part_o, const float* part_lse,
-                                const long long* u_total, int C, uint16_t* out, float* out_lse,
-                                cudaStream_t st);
+                                const long long* u_total, int C, int by_cost, uint16_t* out,
+                                float* out_lse, cudaStream_t st);
 
 bool sm_supported(const Layout& L) { return L.d_h == SD && L.h_q == SG * L.h_kv; }
 
@@ -908,8 +910,8 @@ cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, co
   // every pair's partials are merged by the separate merge kernel: a warp of
   // this kernel that merged them itself would hold up its claimed units for
   // the whole of the pair's eq. A1 (measured: slower than one more launch)
-  e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out,
-                                     out_lse, st);
+  e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, 0, out, out_lse,
+                          st);
   return e;
 }
 

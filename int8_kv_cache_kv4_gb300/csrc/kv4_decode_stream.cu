@@ -7,9 +7,11 @@
 // each, the sink slots and the recent-window ring), then one unit per
 // 16-token INT4 page of the region between the sinks and the recent window.
 // A pair's protected units form one segment of the stream, its INT4 units a
-// second.  The grid is sized to fill the GPU once, and CTA c takes the units
-// [c*U/C, (c+1)*U/C) of the U units in the stream (C = min(grid, U)), so all
-// CTAs carry the same work.
+// second.  The grid is sized to fill the GPU once, and the stream is cut into
+// contiguous CTA shares of equal cost: an INT4 unit counts 4, a protected
+// unit 7 and a segment start 24 (seg_cost), the measured ratios of their
+// times, so that CTAs whose share crosses many short segments take fewer
+// units and all CTAs finish together.
 //
 // Inside a CTA the four warps take the units of the current segment
 // round-robin; each warp streams its units through its own two-stage ring of
@@ -47,6 +49,76 @@ constexpr int kStreamMinBlocks = 4; // CTAs per SM (shared memory: 4 x 56 KB)
 // never gives more units than the others.
 constexpr int kTicketThread = (kWarps - 1) * 32;
 
+// CTAs the stream of total cost Wc is cut over: at most C, and few enough that
+// every share is at least one unit's cost wide (no CTA is left without units).
+__device__ inline int stream_ctas(long long Wc, int C) {
+  return Wc > 0 ? (int)max(1LL, min((long long)C, Wc / (kCostSeg + kCost8))) : 0;
+}
+
+// First unit whose stream cost (the cost of all units before it, a segment's
+// start counted with its first unit) is at least T, for T inside the cost of
+// sequences [b_lo, b_hi); pre_u / pre_c: units and cost before b_lo.
+__device__ inline long long unit_at_cost(long long T, int b_lo, int b_hi, long long pre_u,
+                                         long long pre_c, const Layout& L,
+                                         const int32_t* __restrict__ seq_lens) {
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int len = clamp_len(__ldg(seq_lens + b), L);
+    const int np = prot_units(len, L), n4 = int4_units(len, L);
+    const long long pc = seg_cost(np, 0) + seg_cost(n4, 1);  // one pair
+    if (T < pre_c + (long long)L.h_kv * pc) {
+      const long long h = (T - pre_c) / pc;
+      long long within = T - pre_c - h * pc, u = pre_u + h * (np + n4);
+      int n = np, w = kCost8;
+      if (within >= seg_cost(np, 0)) {  // in the pair's INT4 segment
+        within -= seg_cost(np, 0);
+        u += np;
+        n = n4;
+        w = kCost4;
+      }
+      // unit j > 0 of a segment starts at cost kCostSeg + j w into it
+      const long long j = within <= 0 ? 0 : max(1LL, (within - kCostSeg + w - 1) / w);
+      return u + min(j, (long long)n);  // j = n: the next segment's first unit
+    }
+    pre_c += (long long)L.h_kv * pc;
+    pre_u += (long long)L.h_kv * (np + n4);
+  }
+  return pre_u;  // (not reached: T lies in these sequences)
+}
+
+// CTAs holding a pair's protected units (c0 .. c0 + n0 - 1) and its INT4
+// units (c1 .. c1 + n1 - 1).  gs / pcs: the pair's first unit and the stream
+// cost before it.  by_cost: the stream was cut by cost (Wc over Cw CTAs),
+// else into equal unit counts (U over Cw CTAs).
+struct PairParts {
+  int c0, n0, c1, n1;
+};
+__device__ inline PairParts pair_parts(long long gs, long long pcs, int np, int n4, bool by_cost,
+                                       long long U, long long Wc, int Cw) {
+  PairParts r{0, 0, 0, 0};
+  if (by_cost) {
+    auto at = [&](long long P) { return (int)((P * Cw) / Wc); };
+    const long long p4 = pcs + seg_cost(np, 0);
+    if (np) {
+      r.c0 = at(pcs);
+      r.n0 = at(pcs + (np > 1 ? kCostSeg + (long long)(np - 1) * kCost8 : 0)) - r.c0 + 1;
+    }
+    if (n4) {
+      r.c1 = at(p4);
+      r.n1 = at(p4 + (n4 > 1 ? kCostSeg + (long long)(n4 - 1) * kCost4 : 0)) - r.c1 + 1;
+    }
+  } else {
+    if (np) {
+      r.c0 = cta_of(gs, U, Cw);
+      r.n0 = cta_of(gs + np - 1, U, Cw) - r.c0 + 1;
+    }
+    if (n4) {
+      r.c1 = cta_of(gs + np, U, Cw);
+      r.n1 = cta_of(gs + np + n4 - 1, U, Cw) - r.c1 + 1;
+    }
+  }
+  return r;
+}
+
 // Producer cursor of one warp: the next unit (segment, index) to copy in.
 struct Prod {
   Seg s;
@@ -68,14 +140,16 @@ struct __align__(16) StreamSmem {
   QPrep qp;                         // the current pair's query fragments and sums
   union {
     float mrg_o[kWarps][SG][SD];    // per-warp unnormalised outputs at a segment end
-    long long scan[kThreads];       // start-up: per-thread unit counts, then their prefix
+    long long scan[2 * kThreads];   // start-up: per-thread unit counts and costs, then prefixes
   };
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
   float mrg_m[kWarps][SG];
   float mrg_l[kWarps][SG];
   float mrg_mt[kWarps][SG][SD / 32];
-  long long total;
+  long long total, totalc;          // units and cost of the stream
   long long start_pre;              // stream index of the first unit of sequence start_b
+  long long start_pre_c;            // stream cost before sequence start_b
+  int cw;                           // CTAs the stream is cut over
   long long u_begin, u_end;         // this CTA's share of the stream
   Seg cs;                           // first segment of this CTA
   Prod prod[kWarps];
@@ -216,24 +290,32 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   // ------------------------------------------ stream size and this CTA's start
   const int per = (B + kThreads - 1) / kThreads;
   const int b_lo = min(B, (int)threadIdx.x * per), b_hi = min(B, b_lo + per);
-  long long mine = 0;
+  long long mine = 0, mine_c = 0;  // units and cost of this thread's sequences
   bool bad_len = false;
   for (int b = b_lo; b < b_hi; ++b) {
     const int raw = __ldg(seq_lens + b);
     const int len = clamp_len(raw, L);
     bad_len |= len != raw;
-    mine += (long long)L.h_kv * (prot_units(len, L) + int4_units(len, L));
+    const int np = prot_units(len, L), n4 = int4_units(len, L);
+    mine += (long long)L.h_kv * (np + n4);
+    mine_c += (long long)L.h_kv * (seg_cost(np, 0) + seg_cost(n4, 1));
   }
   if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
   sm.scan[threadIdx.x] = mine;
-  if (threadIdx.x == 0) sm.start_b = B;
+  sm.scan[kThreads + threadIdx.x] = mine_c;
+  if (threadIdx.x == 0) {
+    sm.start_b = B;
+    sm.u_begin = -1;  // (set below by the thread that finds this CTA's first / end unit)
+    sm.u_end = -1;
+  }
   __syncthreads();
-  if (warp == 0) {  // exclusive prefix over the 128 per-thread counts
+  if (warp < 2) {  // exclusive prefixes over the 128 per-thread counts (warp 0) and costs (warp 1)
+    long long* sc = sm.scan + warp * kThreads;
     long long v[4], run = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       v[k] = run;
-      run += sm.scan[4 * lane + k];
+      run += sc[4 * lane + k];
     }
     long long incl = run;
 #pragma unroll
@@ -244,29 +326,50 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     const long long excl = incl - run;
     __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sm.scan[4 * lane + k] = excl + v[k];
-    if (lane == 31) sm.total = incl;
+    for (int k = 0; k < 4; ++k) sc[4 * lane + k] = excl + v[k];
+    if (lane == 31) {
+      if (warp == 0) sm.total = incl;
+      else sm.totalc = incl;
+    }
   }
   __syncthreads();
-  // The stream is cut over Cw = min(C, U) CTAs, so that every working CTA
-  // holds at least one unit (the partial counts below rely on it).
-  const long long U = sm.total;
-  const int Cw = (int)min((long long)C, U);
-  if (defer && c == 0 && threadIdx.x == 0) *u_total = U;  // for stream_merge_kernel
-  const long long u_begin = c < Cw ? U * c / Cw : U, u_end = c < Cw ? U * (c + 1) / Cw : U;
+  // The stream is cut by cost over Cw CTAs: CTA c takes the units from the
+  // first whose stream cost reaches c Wc / Cw up to the first whose cost
+  // reaches (c + 1) Wc / Cw.  Cw keeps every share at least one unit's cost
+  // wide, so every working CTA holds a unit (the partial counts rely on it).
+  const long long U = sm.total, Wc = sm.totalc;
+  const int Cw = stream_ctas(Wc, C);
+  if (defer && c == 0 && threadIdx.x == 0) {  // for stream_merge_kernel
+    u_total[0] = U;
+    u_total[1] = Wc;
+  }
+  if (c < Cw) {
+    const long long Tb = (c * Wc + Cw - 1) / Cw, Te = ((c + 1) * Wc + Cw - 1) / Cw;
+    const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kThreads + threadIdx.x];
+    if (Tb >= exc && Tb < exc + mine_c)
+      sm.u_begin = unit_at_cost(Tb, b_lo, b_hi, exu, exc, L, seq_lens);
+    if (Te < Wc && Te >= exc && Te < exc + mine_c)
+      sm.u_end = unit_at_cost(Te, b_lo, b_hi, exu, exc, L, seq_lens);
+  }
+  __syncthreads();
+  const long long u_begin = c < Cw ? sm.u_begin : U;
+  const long long u_end = c < Cw && sm.u_end >= 0 ? sm.u_end : U;
   if (u_begin < u_end) {
     const long long ex = sm.scan[threadIdx.x];
     if (u_begin >= ex && u_begin < ex + mine) {
-      long long pre = ex;
+      long long pre = ex, pre_c = sm.scan[kThreads + threadIdx.x];
       for (int b = b_lo; b < b_hi; ++b) {
         const int len = clamp_len(__ldg(seq_lens + b), L);
-        const long long ub = (long long)L.h_kv * (prot_units(len, L) + int4_units(len, L));
+        const int np = prot_units(len, L), n4 = int4_units(len, L);
+        const long long ub = (long long)L.h_kv * (np + n4);
         if (u_begin < pre + ub) {
           sm.start_b = b;
           sm.start_pre = pre;
+          sm.start_pre_c = pre_c;
           break;
         }
         pre += ub;
+        pre_c += (long long)L.h_kv * (seg_cost(np, 0) + seg_cost(n4, 1));
       }
     }
   }
@@ -293,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     cs.type = 0;
     cs.len = clamp_len(__ldg(seq_lens + cs.b), L);
     cs.start = sm.start_pre;
+    cs.cs = sm.start_pre_c;
+    sm.cw = Cw;
     cs.n = prot_units(cs.len, L);
     while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
     sm.cs = cs;
@@ -448,17 +553,17 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
         const int pair = cs.b * L.h_kv + cs.h;
         const int np = prot_units(cs.len, L), n4 = int4_units(cs.len, L);
         const long long gs = cs.type == 0 ? cs.start : cs.start - np;  // pair's first unit
-        const long long U = sm.total;
-        const int Cw = (int)min((long long)C, U);
+        const long long pcs = cs.type == 0 ? cs.cs : cs.cs - seg_cost(np, 0);  // cost before it
+        const PairParts pp = pair_parts(gs, pcs, np, n4, true, sm.total, sm.totalc, sm.cw);
         Pend pd;
         pd.row0 = (long long)cs.b * L.h_q + (long long)cs.h * SG;
         pd.s0 = 2LL * pair;
         pd.pair = pair;
         pd.type = cs.type;
-        pd.c0 = np ? cta_of(gs, U, Cw) : 0;
-        pd.n0 = np ? cta_of(gs + np - 1, U, Cw) - pd.c0 + 1 : 0;
-        pd.c1 = n4 ? cta_of(gs + np, U, Cw) : 0;
-        pd.n1 = n4 ? cta_of(gs + np + n4 - 1, U, Cw) - pd.c1 + 1 : 0;
+        pd.c0 = pp.c0;
+        pd.n0 = pp.n0;
+        pd.c1 = pp.c1;
+        pd.n1 = pp.n1;
         pd.valid = 1;
         sm.pcur = pd;
       }
@@ -880,9 +985,10 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 constexpr int kMergeThreads = 256;
 __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
     Layout L, const int32_t* __restrict__ seq_lens, int B, const float* __restrict__ part_o,
-    const float* __restrict__ part_lse, const long long* __restrict__ u_total, int C,
+    const float* __restrict__ part_lse, const long long* __restrict__ u_total, int C, int by_cost,
     uint16_t* __restrict__ out, float* __restrict__ out_lse) {
   __shared__ long long red64[kMergeThreads / 32];
+  __shared__ long long redc[kMergeThreads / 32];
   __shared__ float redf[kMergeThreads / 32];
   __shared__ float4 acc_s[kMergeThreads / 32][32];
   const int pair = blockIdx.x / SG, j = blockIdx.x % SG;
@@ -890,26 +996,37 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int len = clamp_len(__ldg(seq_lens + b), L);
   if (len == 0) return;  // the decode kernel wrote its zero output
-  // stream index of the pair's first unit: units of all earlier sequences
-  long long mine = 0;
+  // stream index and stream cost of the pair's first unit: the units and cost
+  // of all earlier sequences, then of the sequence's earlier kv heads
+  long long mine = 0, mine_c = 0;
   for (int bb = threadIdx.x; bb < b; bb += kMergeThreads) {
     const int lb = clamp_len(__ldg(seq_lens + bb), L);
-    mine += (long long)L.h_kv * (prot_units(lb, L) + int4_units(lb, L));
+    const int np_ = prot_units(lb, L), n4_ = int4_units(lb, L);
+    mine += (long long)L.h_kv * (np_ + n4_);
+    mine_c += (long long)L.h_kv * (seg_cost(np_, 0) + seg_cost(n4_, 1));
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if (lane == 0) red64[warp] = mine;
+  for (int o = 16; o > 0; o >>= 1) {
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    mine_c += __shfl_xor_sync(0xffffffffu, mine_c, o);
+  }
+  if (lane == 0) {
+    red64[warp] = mine;
+    redc[warp] = mine_c;
+  }
   __syncthreads();
-  long long pre = 0;
-  for (int w = 0; w < kMergeThreads / 32; ++w) pre += red64[w];
+  long long pre = 0, pre_c = 0;
+  for (int w = 0; w < kMergeThreads / 32; ++w) {
+    pre += red64[w];
+    pre_c += redc[w];
+  }
   const int np = prot_units(len, L), n4 = int4_units(len, L);
   const long long gs = pre + (long long)h * (np + n4);
-  const long long U = *u_total;
-  const int Cw = (int)min((long long)C, U);
-  const int c0 = np ? cta_of(gs, U, Cw) : 0;
-  const int n0 = np ? cta_of(gs + np - 1, U, Cw) - c0 + 1 : 0;
-  const int c1 = n4 ? cta_of(gs + np, U, Cw) : 0;
-  const int n1 = n4 ? cta_of(gs + np + n4 - 1, U, Cw) - c1 + 1 : 0;
+  const long long pcs = pre_c + (long long)h * (seg_cost(np, 0) + seg_cost(n4, 1));
+  const long long U = u_total[0], Wc = by_cost ? u_total[1] : 0;
+  const int Cw = by_cost ? stream_ctas(Wc, C) : (int)min((long long)C, U);
+  const PairParts pp = pair_parts(gs, pcs, np, n4, by_cost != 0, U, Wc, Cw);
+  const int c0 = pp.c0, n0 = pp.n0, c1 = pp.c1, n1 = pp.n1;
   const int n = n0 + n1;
   auto pidx = [&](int k) { return k < n0 ? 2LL * pair + c0 + k : 2LL * pair + 1 + c1 + (k - n0); };
   // log-normaliser of the whole pair: M = max z_k, Z = sum 2^(z_k - M)
@@ -987,13 +1104,14 @@ long long stream_partials(const Layout& L, int num_seqs) {
 }
 
 // Eq. A1 for every pair from the partials a work-balanced decode kernel left
-// on a grid of C CTAs (U: the stream length it recorded).
+// on a grid of C CTAs (u_total: the stream length and, when the kernel cut the
+// stream by cost (by_cost), its cost).
 cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
                                 const float* part_o, const float* part_lse,
-                                const long long* u_total, int C, uint16_t* out, float* out_lse,
-                                cudaStream_t st) {
+                                const long long* u_total, int C, int by_cost, uint16_t* out,
+                                float* out_lse, cudaStream_t st) {
   stream_merge_kernel<<<num_seqs * L.h_kv * SG, kMergeThreads, 0, st>>>(
-      L, seq_lens, num_seqs, part_o, part_lse, u_total, C, out, out_lse);
+      L, seq_lens, num_seqs, part_o, part_lse, u_total, C, by_cost, out, out_lse);
   return cudaGetLastError();
 }
 
@@ -1033,8 +1151,9 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
       sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer, u_total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (defer) e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, out,
-                                     out_lse, st);
+  if (defer)
+    e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, 1, out,
+                            out_lse, st);
   return e;
 }
 

@@ -27,8 +27,18 @@ __host__ __device__ constexpr bool fold_k_offset() { return NG >= 4; }
 // One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
 struct Seg {
   long long start;  // stream index of its first unit
+  long long cs;     // cost of the stream before it (see seg_cost)
   int b, h, type, len, n;
 };
+
+// Cost model of the stream for splitting it over CTAs: an INT4 unit counts 4,
+// a protected unit 7, and the start of a segment 24 more (its share of the
+// barriers, merge and query setup at a segment boundary).  Ratios measured on
+// GB300 (per-CTA timelines of the work-balanced kernel).
+constexpr int kCost4 = 4, kCost8 = 7, kCostSeg = 24;
+__host__ __device__ inline long long seg_cost(int n, int type) {
+  return n ? kCostSeg + (long long)n * (type == 0 ? kCost8 : kCost4) : 0;
+}
 
 __device__ inline int clamp_len(int len, const Layout& L) {
   return (len < 0 || len > L.max_pages * kPage) ? 0 : len;
@@ -54,6 +64,7 @@ __device__ inline int int4_units(int len, const Layout& L) {
 __device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B) {
   do {
     s.start += s.n;
+    s.cs += seg_cost(s.n, s.type);
     if (s.type == 0) {
       s.type = 1;
       s.n = int4_units(s.len, L);
@@ -77,7 +88,8 @@ __device__ inline int atom_add_release_gpu(int32_t* p, int v) {
 }
 
 // CTA holding stream unit u when U >= C units are split over C CTAs as
-// [c*U/C, (c+1)*U/C) (every CTA then holds at least one unit).
+// [c*U/C, (c+1)*U/C) (every CTA then holds at least one unit); the
+// stream kernel (decode_stream_kernel) cuts by cost instead.
 __device__ inline int cta_of(long long u, long long U, int C) {
   return (int)(((u + 1) * C - 1) / U);
 }
