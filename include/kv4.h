@@ -98,7 +98,7 @@ extern "C" {
 /* Shape of one attention layer's cache.  All fields are host values. */
 typedef struct kv4_layout {
   int32_t num_q_heads;       /* h_q (a multiple of num_kv_heads, h_q/h_kv <= 8) */
-  int32_t num_kv_heads;      /* h_kv */
+  int32_t num_kv_heads;      /* h_kv (1 .. 65536) */
   int32_t head_dim;          /* d_h: 64 or 128 */
   int32_t page_size;         /* tokens per page: must be 16 (App. A.2) */
   int32_t int4_group;        /* g: 32, 64 or 128 and g <= head_dim */

@@ -174,6 +174,7 @@ int kv4_check_layout(const kv4_layout* l) {
   if (!l) return KV4_ERR_INVALID_ARG;
   if (l->num_q_heads <= 0 || l->num_kv_heads <= 0 || l->num_q_heads % l->num_kv_heads != 0)
     return KV4_ERR_INVALID_ARG;
+  if (l->num_kv_heads > (1 << 16)) return KV4_ERR_INVALID_ARG;  // kernels index heads x chunk in 32 bits
   const int G = l->num_q_heads / l->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return KV4_ERR_UNSUPPORTED;
   if (l->head_dim != 64 && l->head_dim != 128) return KV4_ERR_UNSUPPORTED;

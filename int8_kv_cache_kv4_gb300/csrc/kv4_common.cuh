@@ -171,6 +171,24 @@ __device__ inline void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t b
       : "memory");
 }
 
+// The same with shared-memory addresses already in the shared window (saves
+// the generic-to-shared conversions on a producer's per-copy path).
+__device__ inline void mbar_arrive_expect_tx_s(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ inline void mbar_arrive_s(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ inline void bulk_g2s_s(uint32_t smem_dst, const void* gmem_src, uint32_t bytes,
+                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_dst),
+      "l"(gmem_src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------ reductions
 __device__ inline float warp_max(float v) {
 #pragma unroll

@@ -119,16 +119,6 @@ __device__ inline PairParts pair_parts(long long gs, long long pcs, int np, int 
   return r;
 }
 
-// Producer cursor of one warp: the next unit (segment, index) to copy in.
-struct Prod {
-  Seg s;
-  const int32_t* bt;  // INT4 segment: block-table entries from its first page on
-  int j;              // unit index inside segment s
-  int hi;             // end of this CTA's units inside segment s
-  int np4;            // INT4 pages of segment s's sequence
-  int more;           // a next unit exists
-};
-
 // A pair whose partial results are to be merged, with where they are.
 struct Pend {
   long long row0;      // first output row (sequence * h_q + kv head * G)
@@ -152,7 +142,7 @@ struct __align__(16) StreamSmem {
   int cw;                           // CTAs the stream is cut over
   long long u_begin, u_end;         // this CTA's share of the stream
   Seg cs;                           // first segment of this CTA
-  Prod prod[kWarps];
+  Seg prod[kWarps];                 // producer cursors (segment of each warp's next unit)
   Seg nx;                           // segment after cs (thread 0, at segment start)
   Pend pcur;                        // partial bookkeeping of segment cs (thread 0)
   Pend pend;                        // partial whose ticket is in flight (thread 0)
@@ -413,94 +403,98 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   constexpr int SB = kSPages * cb;  // stage bytes: two INT4 chunks or one 16-slot INT8 unit
   static_assert(2 * kProtUnit * SD + 4 * kProtUnit <= SB, "an INT8 unit fits a stage");
   uint8_t* my_stages = stage_base + (size_t)warp * kSStages * SB;
-  // Producer (lane 0 of each warp; cursor in shared memory): advance to this
-  // warp's next unit, moving over segments, and start reading its
-  // block-table entry into a register, consumed only at the next issue so
-  // the load's latency is not waited for here.
+  // Producer (lane 0 of each warp).  Its segment cursor lives in shared
+  // memory and moves only when a segment is used up; what each unit needs is
+  // kept in registers: the unit index in the segment and its end, the
+  // segment's type, INT4 page count, block-table row, copy source (INT4: this
+  // head's column of the pool; INT8: the pair's side block) and the next
+  // unit's pages, read one unit ahead so that the load's latency is not
+  // waited for at the issue.
+  int p_more = 0, p_j = 0, p_hi = 0, p_type = 0, p_np4 = 0, p_ns = 0;
+  const int32_t* p_bt = block_table;
+  const uint8_t* p_src = paged;
   int pphys = -1, pphys1 = -1;  // the unit's two pages (-2: no second page)
-  // slow path: (pr.s, pr.j) may lie past its segment's end; move over
+  const uint32_t stages_s = smem_u32(my_stages), bars_s = smem_u32(&sm.bar[warp][0]);
+  // slow path: (cursor, p_j) may lie past its segment's end; move over
   // segments until it names a unit of this warp
-  auto prod_next = [&](Prod& pr) {
+  auto prod_next = [&]() {
+    Seg& s_ = sm.prod[warp];
     const long long ub = sm.u_begin, ue = sm.u_end;
     while (true) {
-      if (pr.s.b >= B || pr.s.start >= ue) {
-        pr.more = 0;
+      if (s_.b >= B || s_.start >= ue) {
+        p_more = 0;
         return;
       }
-      pr.hi = (int)(min(ue, pr.s.start + pr.s.n) - pr.s.start);
-      if (pr.j < pr.hi) break;
-      seg_next(pr.s, L, seq_lens, B);
-      pr.j = (int)(max(ub, pr.s.start) - pr.s.start) + warp;
+      p_hi = (int)(min(ue, s_.start + s_.n) - s_.start);
+      if (p_j < p_hi) break;
+      seg_next(s_, L, seq_lens, B);
+      p_j = (int)(max(ub, s_.start) - s_.start) + warp;
     }
-    pr.more = 1;
-    pr.bt = block_table + (long long)pr.s.b * L.max_pages + min(pr.s.len, L.S) / kPage;
-    pr.np4 = int4_pages(pr.s.len, L);
-    if (pr.s.type == 1) {
-      pphys = __ldg(pr.bt + kSPages * pr.j);
-      pphys1 = kSPages * pr.j + 1 < pr.np4 ? __ldg(pr.bt + kSPages * pr.j + 1) : -2;
+    p_more = 1;
+    p_type = s_.type;
+    p_bt = block_table + (long long)s_.b * L.max_pages + min(s_.len, L.S) / kPage;
+    p_np4 = int4_pages(s_.len, L);
+    p_ns = s_.len <= L.S ? s_.len : NS;
+    p_src = s_.type == 1 ? paged + (long long)s_.h * cb
+                         : side + ((long long)s_.b * L.h_kv + s_.h) * side_blk;
+    if (s_.type == 1) {
+      pphys = __ldg(p_bt + kSPages * p_j);
+      pphys1 = kSPages * p_j + 1 < p_np4 ? __ldg(p_bt + kSPages * p_j + 1) : -2;
     }
   };
   auto issue = [&](int st) {
-    Prod& pr = sm.prod[warp];
-    const Seg& ps = pr.s;
-    const int pj = pr.j;
-    uint64_t* bar = &sm.bar[warp][st];
-    uint8_t* dst = my_stages + (size_t)st * SB;
-    if (ps.type == 1) {
+    const uint32_t bar = bars_s + 8u * st;
+    const uint32_t dst = stages_s + (uint32_t)(st * SB);
+    if (p_type == 1) {
       // pages 2j and 2j + 1 of the segment (the second may not exist: -2)
-      const bool good0 = pphys >= 0 && pphys < L.num_pages;
-      const bool good1 = pphys1 >= 0 && pphys1 < L.num_pages;
+      const bool good0 = (unsigned)pphys < (unsigned)L.num_pages;
+      const bool good1 = (unsigned)pphys1 < (unsigned)L.num_pages;
       if (!good0 || (pphys1 != -2 && !good1)) set_status(status, KV4_STATUS_BAD_PAGE);
       sm.phys[warp][st][0] = good0 ? pphys : -1;  // published by the arrive below
       sm.phys[warp][st][1] = good1 ? pphys1 : -1;
-      const uint32_t bytes = (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u);
-      if (bytes) {
-        mbar_arrive_expect_tx(bar, bytes);
-        if (good0) bulk_g2s(dst, paged + ((long long)pphys * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
-        if (good1)
-          bulk_g2s(dst + cb, paged + ((long long)pphys1 * L.h_kv + ps.h) * cb, (uint32_t)cb, bar);
+      const int page_stride = L.h_kv * cb;  // bytes between pages of one head (< 2^31)
+      if (good0 || good1) {
+        mbar_arrive_expect_tx_s(bar, (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u));
+        if (good0) bulk_g2s_s(dst, p_src + (long long)pphys * page_stride, (uint32_t)cb, bar);
+        if (good1) bulk_g2s_s(dst + cb, p_src + (long long)pphys1 * page_stride, (uint32_t)cb, bar);
       } else {
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+        mbar_arrive_s(bar);
       }
     } else {
-      const uint8_t* blk = side + ((long long)ps.b * L.h_kv + ps.h) * side_blk;
-      const int slot0 = pj * kProtUnit;
-      const int ns = ps.len <= L.S ? ps.len : NS;
-      const uint32_t rows = (uint32_t)min(kProtUnit, ns - slot0);
+      const int slot0 = p_j * kProtUnit;
+      const uint32_t rows = (uint32_t)min(kProtUnit, p_ns - slot0);
       // scales of the 8-slot runs that hold copied rows (within the NSP padding)
       const uint32_t sbytes = 16u * ((rows + 7) / 8);
-      mbar_arrive_expect_tx(bar, 2u * rows * D + 2u * sbytes);
-      bulk_g2s(dst, blk + (long long)slot0 * D, rows * D, bar);
-      bulk_g2s(dst + kProtUnit * D, blk + (long long)(NS + slot0) * D, rows * D, bar);
-      bulk_g2s(dst + 2 * kProtUnit * D, blk + 2LL * NS * D + 2 * slot0, sbytes, bar);
-      bulk_g2s(dst + 2 * kProtUnit * D + 2 * kProtUnit, blk + 2LL * NS * D + 2LL * NSP + 2 * slot0,
-               sbytes, bar);
+      mbar_arrive_expect_tx_s(bar, 2u * rows * D + 2u * sbytes);
+      bulk_g2s_s(dst, p_src + (long long)slot0 * D, rows * D, bar);
+      bulk_g2s_s(dst + kProtUnit * D, p_src + (long long)(NS + slot0) * D, rows * D, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D, p_src + 2LL * NS * D + 2 * slot0, sbytes, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D + 2 * kProtUnit, p_src + 2LL * NS * D + 2LL * NSP + 2 * slot0,
+                 sbytes, bar);
     }
   };
   if (lane == 0) {
-    Prod& pr = sm.prod[warp];
-    pr.s = sm.cs;
-    pr.j = (int)(max(u_begin, pr.s.start) - pr.s.start) + warp;
-    prod_next(pr);
-    for (int st = 0; st < kSStages && pr.more; ++st) {
+    sm.prod[warp] = sm.cs;
+    p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
+    prod_next();
+    for (int st = 0; st < kSStages && p_more; ++st) {
       issue(st);
-      pr.j += kWarps;
-      prod_next(pr);
+      p_j += kWarps;
+      prod_next();
     }
   }
   auto refill = [&](int st) {  // after the warp released stage st
     __syncwarp();
-    if (lane == 0 && sm.prod[warp].more) {
+    if (lane == 0 && p_more) {
       issue(st);
-      Prod& pr = sm.prod[warp];
-      pr.j += kWarps;
-      if (pr.j < pr.hi) {  // fast path: next unit of the same segment
-        if (pr.s.type == 1) {
-          pphys = __ldg(pr.bt + kSPages * pr.j);
-          pphys1 = kSPages * pr.j + 1 < pr.np4 ? __ldg(pr.bt + kSPages * pr.j + 1) : -2;
+      p_j += kWarps;
+      if (p_j < p_hi) {  // fast path: next unit of the same segment
+        if (p_type == 1) {
+          pphys = __ldg(p_bt + kSPages * p_j);
+          pphys1 = kSPages * p_j + 1 < p_np4 ? __ldg(p_bt + kSPages * p_j + 1) : -2;
         }
       } else {
-        prod_next(pr);
+        prod_next();
       }
     }
   };
