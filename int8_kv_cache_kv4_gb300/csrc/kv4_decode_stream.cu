@@ -42,12 +42,15 @@
 namespace kv4 {
 namespace {
 
+// warps per CTA of this kernel, and its threads
+constexpr int kSW = 4;
+constexpr int kST = kSW * 32;
 constexpr int kSStages = 2;         // bulk-copy stages per warp
 constexpr int kStreamMinBlocks = 4; // CTAs per SM (shared memory: 4 x 56 KB)
 // The thread that keeps the segment bookkeeping and takes the completion
 // tickets: lane 0 of the last warp, which the round-robin unit assignment
 // never gives more units than the others.
-constexpr int kTicketThread = (kWarps - 1) * 32;
+constexpr int kTicketThread = (kSW - 1) * 32;
 
 // CTAs the stream of total cost Wc is cut over: at most C, and few enough that
 // every share is at least one unit's cost wide (no CTA is left without units).
@@ -129,20 +132,20 @@ struct Pend {
 struct __align__(16) StreamSmem {
   QPrep qp;                         // the current pair's query fragments and sums
   union {
-    float mrg_o[kWarps][SG][SD];    // per-warp unnormalised outputs at a segment end
-    long long scan[2 * kThreads];   // start-up: per-thread unit counts and costs, then prefixes
+    float mrg_o[kSW][SG][SD];    // per-warp unnormalised outputs at a segment end
+    long long scan[2 * kST];   // start-up: per-thread unit counts and costs, then prefixes
   };
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
-  float mrg_m[kWarps][SG];
-  float mrg_l[kWarps][SG];
-  float mrg_mt[kWarps][SG][SD / 32];
+  float mrg_m[kSW][SG];
+  float mrg_l[kSW][SG];
+  float mrg_mt[kSW][SG][SD / 32];
   long long total, totalc;          // units and cost of the stream
   long long start_pre;              // stream index of the first unit of sequence start_b
   long long start_pre_c;            // stream cost before sequence start_b
   int cw;                           // CTAs the stream is cut over
   long long u_begin, u_end;         // this CTA's share of the stream
   Seg cs;                           // first segment of this CTA
-  Seg prod[kWarps];                 // producer cursors (segment of each warp's next unit)
+  Seg prod[kSW];                 // producer cursors (segment of each warp's next unit)
   Seg nx;                           // segment after cs (thread 0, at segment start)
   Pend pcur;                        // partial bookkeeping of segment cs (thread 0)
   Pend pend;                        // partial whose ticket is in flight (thread 0)
@@ -150,8 +153,8 @@ struct __align__(16) StreamSmem {
   int go;                           // comb is valid
   int new_q;                        // the next segment starts a new pair
   int start_b;
-  int32_t phys[kWarps][kSStages][kSPages];  // INT4 stage: physical pages, < 0 = not loaded
-  uint64_t bar[kWarps][kSStages];
+  int32_t phys[kSW][kSStages][kSPages];  // INT4 stage: physical pages, < 0 = not loaded
+  uint64_t bar[kSW][kSStages];
   uint64_t qbar;                    // completion of the qraw copy
 };
 
@@ -170,31 +173,33 @@ __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __rest
 // sm.qraw once its copy has completed.  No warp may still read the old values.
 template <int NG>
 __device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
-  build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x);
+  if (threadIdx.x < 128) build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x);  // (built by 128 threads)
 }
 
 // Merge the warps' states of one segment and store its partial result P
-// (after a barrier that follows every warp's publish).  Warp j merges query
-// head j: the four warps' weights 2^(m_w - M) / L are formed once, then each
+// (after a barrier that follows every warp's publish).  Warp j < G merges
+// query head j: the warps' weights 2^(m_w - M) / L are formed once, then each
 // lane combines four channels.
 __device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ part_o,
                                           float* __restrict__ part_lse, long long P) {
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float mw = lane < kWarps ? sm.mrg_m[lane][j] : -INFINITY;
-  const float lw = lane < kWarps ? sm.mrg_l[lane][j] : 0.f;
-  float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+  if (j >= SG) return;
+  const float mw = lane < kSW ? sm.mrg_m[lane][j] : -INFINITY;
+  const float lw = lane < kSW ? sm.mrg_l[lane][j] : 0.f;
+  float M = mw;
+#pragma unroll
+  for (int o = 1; o < kSW; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   M = __shfl_sync(0xffffffffu, M, 0);
   const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
   float Lt = e * lw;
-  Lt += __shfl_xor_sync(0xffffffffu, Lt, 1);
-  Lt += __shfl_xor_sync(0xffffffffu, Lt, 2);
+#pragma unroll
+  for (int o = 1; o < kSW; o <<= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
   Lt = __shfl_sync(0xffffffffu, Lt, 0);
   const bool empty = !(Lt > 0.f);
-  const float f = empty ? 0.f : e / Lt;  // lanes 0..3: weight of warp `lane`
+  const float f = empty ? 0.f : e / Lt;  // lanes 0 .. kSW-1: weight of warp `lane`
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kSW; ++w) {
     const float fw = __shfl_sync(0xffffffffu, f, w);
     const float4 a = reinterpret_cast<const float4*>(&sm.mrg_o[w][j][0])[lane];
     const float mt = sm.mrg_mt[w][j][lane >> 3];  // channels 4*lane.. lie in block lane/8
@@ -213,7 +218,8 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
                                       const float* __restrict__ part_lse, long long s0, int c0,
                                       int n0, long long s1, int c1, int n1, long long row0,
                                       uint16_t* __restrict__ out, float* __restrict__ out_lse) {
-  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;  // warp j < G: query head j
+  if (j >= SG) return;
   const int n = n0 + n1;
   auto pidx = [&](int k) { return k < n0 ? s0 + c0 + k : s1 + c1 + (k - n0); };
   float M = -INFINITY;
@@ -262,7 +268,7 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
 }
 
 template <int NG>
-__global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kernel(
+__global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ------------------------------------------ stream size and this CTA's start
-  const int per = (B + kThreads - 1) / kThreads;
+  const int per = (B + kST - 1) / kST;
   const int b_lo = min(B, (int)threadIdx.x * per), b_hi = min(B, b_lo + per);
   long long mine = 0, mine_c = 0;  // units and cost of this thread's sequences
   bool bad_len = false;
@@ -292,20 +298,21 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   }
   if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
   sm.scan[threadIdx.x] = mine;
-  sm.scan[kThreads + threadIdx.x] = mine_c;
+  sm.scan[kST + threadIdx.x] = mine_c;
   if (threadIdx.x == 0) {
     sm.start_b = B;
     sm.u_begin = -1;  // (set below by the thread that finds this CTA's first / end unit)
     sm.u_end = -1;
   }
   __syncthreads();
-  if (warp < 2) {  // exclusive prefixes over the 128 per-thread counts (warp 0) and costs (warp 1)
-    long long* sc = sm.scan + warp * kThreads;
-    long long v[4], run = 0;
+  if (warp < 2) {  // exclusive prefixes over the per-thread counts (warp 0) and costs (warp 1)
+    constexpr int E = kST / 32;
+    long long* sc = sm.scan + warp * kST;
+    long long v[E], run = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < E; ++k) {
       v[k] = run;
-      run += sc[4 * lane + k];
+      run += sc[E * lane + k];
     }
     long long incl = run;
 #pragma unroll
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     const long long excl = incl - run;
     __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sc[4 * lane + k] = excl + v[k];
+    for (int k = 0; k < E; ++k) sc[E * lane + k] = excl + v[k];
     if (lane == 31) {
       if (warp == 0) sm.total = incl;
       else sm.totalc = incl;
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   }
   if (c < Cw) {
     const long long Tb = (c * Wc + Cw - 1) / Cw, Te = ((c + 1) * Wc + Cw - 1) / Cw;
-    const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kThreads + threadIdx.x];
+    const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kST + threadIdx.x];
     if (Tb >= exc && Tb < exc + mine_c)
       sm.u_begin = unit_at_cost(Tb, b_lo, b_hi, exu, exc, L, seq_lens);
     if (Te < Wc && Te >= exc && Te < exc + mine_c)
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   if (u_begin < u_end) {
     const long long ex = sm.scan[threadIdx.x];
     if (u_begin >= ex && u_begin < ex + mine) {
-      long long pre = ex, pre_c = sm.scan[kThreads + threadIdx.x];
+      long long pre = ex, pre_c = sm.scan[kST + threadIdx.x];
       for (int b = b_lo; b < b_hi; ++b) {
         const int len = clamp_len(__ldg(seq_lens + b), L);
         const int np = prot_units(len, L), n4 = int4_units(len, L);
@@ -366,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
   // sequences with nothing to attend: zero output, log-normaliser -inf
   for (int b = c; b < B; b += C) {
     if (clamp_len(__ldg(seq_lens + b), L) != 0) continue;
-    for (int idx = threadIdx.x; idx < L.h_q * D; idx += kThreads)
+    for (int idx = threadIdx.x; idx < L.h_q * D; idx += kST)
       out[(long long)b * L.h_q * D + idx] = 0;
     if (out_lse)
-      for (int idx = threadIdx.x; idx < L.h_q; idx += kThreads)
+      for (int idx = threadIdx.x; idx < L.h_q; idx += kST)
         out_lse[(long long)b * L.h_q + idx] = -INFINITY;
   }
   if (lane == 0) {
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     prod_next();
     for (int st = 0; st < kSStages && p_more; ++st) {
       issue(st);
-      p_j += kWarps;
+      p_j += kSW;
       prod_next();
     }
   }
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
     __syncwarp();
     if (lane == 0 && p_more) {
       issue(st);
-      p_j += kWarps;
+      p_j += kSW;
       if (p_j < p_hi) {  // fast path: next unit of the same segment
         if (p_type == 1) {
           pphys = __ldg(p_bt + kSPages * p_j);
@@ -607,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
       const uint32_t v_lane = smem_u32(my_stages) + codes_off_v(D);
       constexpr int TK[4] = {0, 1, 8, 9};      // this lane's tokens: 2 * qd + TK[e]
 
-      for (int jj = lo + warp; jj < hi; jj += kWarps) {
+      for (int jj = lo + warp; jj < hi; jj += kSW) {
         const int ST = (int)((unsigned)it % kSStages);
         const int SO = ST * SB;  // stage offset
         const bool ok =
@@ -810,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, kStreamMinBlocks) decode_stream_kern
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
       const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
-      for (int jj = lo + warp; jj < hi; jj += kWarps, ++it) {
+      for (int jj = lo + warp; jj < hi; jj += kSW, ++it) {
         const int st = (int)((unsigned)it % kSStages);
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], ((unsigned)it / kSStages) & 1));
@@ -1117,7 +1124,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
                             int32_t* status, long long* u_total, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
-      ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kWarps * kSStages * kSPages * cb;
+      ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kSW * kSStages * kSPages * cb;
   // four CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
   static_assert(smem <= 228 * 1024 / kStreamMinBlocks - 1024, "shared memory for 4 CTAs per SM");
   // once per device: the shared-memory attribute and the resident-CTA capacity
@@ -1132,7 +1139,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
         if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
           r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NG>,
-                                                            kThreads, smem);
+                                                            kST, smem);
         *g = std::max(1, std::min(kMaxStreamCtas, sms * std::max(1, per_sm)));
         return r;
       },
@@ -1141,7 +1148,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   // With few pairs each one spreads over many CTAs; its merge then runs as a
   // separate, wider kernel instead of in the last CTA.
   const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
-  decode_stream_kernel<NG><<<grid, kThreads, smem, st>>>(
+  decode_stream_kernel<NG><<<grid, kST, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
       sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer, u_total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
