@@ -825,9 +825,14 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         const uint32_t stg = smem_u32(my_stages) + st * SB;
         if (ok) {
           const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
-          bool okv[4];
+          // a sequence of at least S + R tokens fills every sink and ring slot:
+          // only a unit reaching into the padding past NS needs the test
+          const bool all_in = cs.len >= NS && (jj + 1) * kProtUnit <= NS;
+          bool okv[4] = {true, true, true, true};
+          if (!all_in) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) okv[e] = slot_valid(sl0 + TK8[e], cs.len, L, ws_mod, n_rec);
+            for (int e = 0; e < 4; ++e) okv[e] = slot_valid(sl0 + TK8[e], cs.len, L, ws_mod, n_rec);
+          }
           // ---- QK: B = K codes of slot r (tile 0) and slot r + 8 (tile 1),
           // channels 32*qd + [0, 32); pieces are swizzled by slot (r + 8 & 7 = r)
           const uint4 kA0 = lds128(stg + r * D + 16 * ((2 * qd) ^ r));

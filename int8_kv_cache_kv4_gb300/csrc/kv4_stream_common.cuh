@@ -153,21 +153,25 @@ __device__ inline void build_qprep(const uint16_t* qr, QPrep& qp, int t) {
   // (low nibbles) and 1024 + 16 c for odd ones (high nibbles, k-indices 8..15
   // of each step, A registers 2 and 3), so the odd channels' query values are
   // stored divided by 16 (exact in fp16 for |q| >= 2^-10).
-  for (int idx = t; idx < 8 * 32 * 4; idx += 128) {
-    const int s_ = idx >> 7, ln = (idx >> 2) & 31, k = idx & 3;
+  {
+    // thread t (< 128) fills word k of lane ln at every k-step: row (group,
+    // head) and the channel block are the same at every step
+    const int ln = (t >> 2) & 31, k = t & 3;
     const int rr = ln >> 2, qq = ln & 3;
     const int row = rr + 8 * (k & 1);
     const int grp = row >> 2, jj = row & 3;
-    const int base = 32 * qq + 8 * (s_ >> 1) + 2 * (s_ & 1) + ((k & 2) ? 1 : 0);
-    uint32_t w = 0u;
-    if (grp < NG) {
+    // the step's channels 32 qq + [0, 32) lie in group (32 qq) / GS
+    const bool in_group = grp < NG && (32 * qq) / GS == grp;
+    const bool sixteenth = fold_k_offset<NG>() && (k & 2);
+    const uint16_t* qrow = qr + jj * SD + 32 * qq + ((k & 2) ? 1 : 0);
 #pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int d = base + 4 * e2;
-        if (d / GS == grp) w |= q16(qr[jj * SD + d], fold_k_offset<NG>() && (k & 2)) << (16 * e2);
-      }
+    for (int s_ = 0; s_ < 8; ++s_) {
+      const int off = 8 * (s_ >> 1) + 2 * (s_ & 1);  // channels off and off + 4 of the block
+      uint32_t w = 0u;
+      if (in_group)
+        w = q16(qrow[off], sixteenth) | (q16(qrow[off + 4], sixteenth) << 16);
+      qp.qfrag4[s_][ln][k] = w;
     }
-    qp.qfrag4[s_][ln][k] = w;
   }
   // INT8 fragments: A rows = heads 0..3; k-step s, lane quad qd covers
   // channels 32*qd + 4*s + {0,1} (a0) and + {2,3} (a2)
