@@ -43,7 +43,7 @@ UNIT = "tokens/s"
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("60b606b6bc386e61", "qwen3_8b_b64"): 388413696 + 4461568}
+TRAFFIC = {("77ef04e0d9a7af6a", "qwen3_8b_b64"): 388411648 + 4569088}
 
 
 # ------------------------------------------------------------------ helpers
