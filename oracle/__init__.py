@@ -68,9 +68,11 @@ def _get():
             lib.kv4o_is_protected.restype = I
             lib.kv4o_side_slot.argtypes = [I, I, I]
             lib.kv4o_side_slot.restype = I
-            lib.kv4o_quant_append.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, I, P, P]
+            lib.kv4o_quant_append.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
             lib.kv4o_quant_append.restype = I
-            lib.kv4o_dequant_seq.argtypes = [I, I, I, I, I, I, P, P, P, P]
+            lib.kv4o_dequant_seq.argtypes = [I, I, I, I, I, I, P, P, P, P, I]
+            lib.kv4o_hadamard_f32_n.argtypes = [P, Lg, I]
+            lib.kv4o_hadamard_f32_n.restype = None
             lib.kv4o_dequant_seq.restype = I
             lib.kv4o_attend.argtypes = [I, I, I, I, P, P, P, D, P, P, P]
             lib.kv4o_attend.restype = None
@@ -177,9 +179,10 @@ def side_block_bytes(d_h: int, S: int, R: int) -> int:
 def quant_append(*, h_kv, d_h, g, S, R, max_seqs, num_pages, max_pages_per_seq,
                  paged: np.ndarray, side: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
                  tok_seq: np.ndarray, tok_pos: np.ndarray, seq_lens: np.ndarray,
-                 block_table: np.ndarray) -> int:
+                 block_table: np.ndarray, rotate_k: bool = False) -> int:
     """Write T new tokens into the packed cache bytes ``paged`` / ``side`` in place.
-    k_new/v_new: bf16 bits uint16 [T][h_kv][d_h].  Returns status bits."""
+    k_new/v_new: bf16 bits uint16 [T][h_kv][d_h].  rotate_k: K is rotated by
+    hadamard_f32 before it is quantized (V never is).  Returns status bits."""
     k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
     v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
     tok_seq = np.ascontiguousarray(tok_seq, dtype=np.int32)
@@ -193,20 +196,23 @@ def quant_append(*, h_kv, d_h, g, S, R, max_seqs, num_pages, max_pages_per_seq,
     return int(_get().kv4o_quant_append(h_kv, d_h, g, S, R, max_seqs, num_pages,
                                         max_pages_per_seq, _p(paged), _p(side), _p(k_new),
                                         _p(v_new), _p(tok_seq), _p(tok_pos), T, _p(seq_lens),
-                                        _p(block_table)))
+                                        _p(block_table), 1 if rotate_k else 0))
 
 
 # ----------------------------------------------------------------- decoding
 
-def dequant_seq(k_src: np.ndarray, v_src: np.ndarray, *, g: int, S: int, R: int):
+def dequant_seq(k_src: np.ndarray, v_src: np.ndarray, *, g: int, S: int, R: int,
+                rotate_k: bool = False):
     """Dequantized cache of one sequence (fp64).  k_src/v_src: bf16 bits
-    [h_kv][L][d_h].  Protected positions decode INT8, the rest INT4."""
+    [h_kv][L][d_h].  Protected positions decode INT8, the rest INT4.
+    rotate_k: K is rotated (hadamard_f32) before it is quantized."""
     k_src = np.ascontiguousarray(k_src, dtype=np.uint16)
     v_src = np.ascontiguousarray(v_src, dtype=np.uint16)
     h_kv, L, d_h = k_src.shape
     kh = np.empty((h_kv, L, d_h), dtype=np.float64)
     vh = np.empty_like(kh)
-    st = _get().kv4o_dequant_seq(h_kv, d_h, g, S, R, L, _p(k_src), _p(v_src), _p(kh), _p(vh))
+    st = _get().kv4o_dequant_seq(h_kv, d_h, g, S, R, L, _p(k_src), _p(v_src), _p(kh), _p(vh),
+                                 1 if rotate_k else 0)
     return kh, vh, st
 
 
@@ -227,10 +233,11 @@ def attend(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, sm_scale: float)
 
 
 def decode_seq(q: np.ndarray, k_src: np.ndarray, v_src: np.ndarray, *, g: int, S: int, R: int,
-               sm_scale: float):
+               sm_scale: float, rotate_k: bool = False):
     """Quantize one sequence's source K/V with the protection rule, then attend.
-    Returns (out fp64 [h_q][d_h], lse fp64 [h_q], status)."""
-    kh, vh, st = dequant_seq(k_src, v_src, g=g, S=S, R=R)
+    rotate_k: K is rotated before quantization (q must then be the rotated
+    query).  Returns (out fp64 [h_q][d_h], lse fp64 [h_q], status)."""
+    kh, vh, st = dequant_seq(k_src, v_src, g=g, S=S, R=R, rotate_k=rotate_k)
     out, lse = attend(q, kh, vh, sm_scale)
     return out, lse, st
 
@@ -244,6 +251,28 @@ def combine(o_parts: np.ndarray, z_parts: np.ndarray):
     z = np.empty((1,), dtype=np.float64)
     _get().kv4o_combine(n, d, _p(o_parts), _p(z_parts), _p(out), _p(z))
     return out, float(z[0])
+
+
+def hadamard_f32(x: np.ndarray) -> np.ndarray:
+    """Normalized Sylvester-Hadamard rotation of every row of x (float32, last
+    axis a power of two) in fp32, in the fixed order kv4o_hadamard_f32 states."""
+    x = np.array(x, dtype=np.float32, order="C", copy=True)
+    n = x.shape[-1]
+    assert n > 0 and n & (n - 1) == 0
+    _get().kv4o_hadamard_f32_n(_p(x), x.size // n, n)
+    return x
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bits, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def hadamard_bf16(bits: np.ndarray) -> np.ndarray:
+    """Rotated query rows: bf16 bits in, hadamard_f32 of their values, rounded
+    to bf16 (nearest even) bits out."""
+    return f32_to_bf16_bits(hadamard_f32(bf16_to_f32(np.asarray(bits, dtype=np.uint16))))
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

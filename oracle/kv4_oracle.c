@@ -32,11 +32,20 @@
  *      [-127,127]; s == 0 gives c = 0.
  *   R5 protected set of a sequence of length L: [0, min(S,L)) U [max(S,L-R), L).
  *      Sink slot of position p < S is p; ring slot of p >= S is S + (p mod R).
- *   R6 attention is fp64 softmax over the dequantized cache, bf16 query used as
+ *   R6 in a multi-token append a position is written to the ring only if it lies
+ *      in the window of its sequence's length after the append (seq_lens).
+ *   R7 attention is fp64 softmax over the dequantized cache, bf16 query used as
  *      is, softmax scale passed in (1/sqrt(d_h) by convention), query head j
  *      reads kv head j / (h_q / h_kv).
- *   R7 a non-finite input element, or metadata that overflows FP16, marks the
+ *   R8 a non-finite input element, or metadata that overflows FP16, marks the
  *      status word and stores an all-zero group (codes 0, Delta 0, m 0).
+ *   R9 Hadamard K-rotation (Sec. 3 eq. 3.4; App. A.3 "Encoding and
+ *      allocation"; App. D.4 keeps K-only): the fixed normalized Sylvester
+ *      matrix of order d_h (no random signs), applied to the bf16 K vector of
+ *      every token-head before both encoders (INT4 and INT8), V unrotated; the
+ *      query is rotated by the same matrix and rounded to bf16.  The pages fix
+ *      no precision: fp32, in the order kv4o_hadamard_f32 states, so that the
+ *      quantization decisions are reproducible bit for bit.
  *
  * Every function pins against closed forms / invariants / brute force in
  * tests/test_oracle_*.py.
@@ -168,7 +177,7 @@ static double rne_int(float v) {
 
 /* ------------------------------------------------------------ encoders */
 
-/* INT4 affine encode of one group of g values (readings R2, R3, R7).
+/* INT4 affine encode of one group of g values (readings R2, R3, R8).
  * Returns 0, or KV4O_ST_NONFINITE (and an all-zero group). */
 int kv4o_int4_encode_group(const float* x, int g, uint8_t* codes, uint16_t* delta16,
                            uint16_t* off16) {
@@ -212,7 +221,7 @@ int kv4o_int4_encode_group(const float* x, int g, uint8_t* codes, uint16_t* delt
   return 0;
 }
 
-/* INT8 symmetric encode of one token-head vector of n values (reading R4, R7). */
+/* INT8 symmetric encode of one token-head vector of n values (reading R4, R8). */
 int kv4o_int8_encode_vec(const float* x, int n, int8_t* codes, uint16_t* scale16) {
   float a = 0.f;
   int bad = 0;
@@ -259,6 +268,32 @@ int kv4o_is_protected(int p, int L, int S, int R) {
 /* side-cache slot of a protected position */
 int kv4o_side_slot(int p, int S, int R) { return p < S ? p : S + (p % R); }
 
+/* Normalized Hadamard rotation of n values (n a power of two), in place:
+ * y = H_n x / sqrt(n), with the Sylvester matrix H_1 = [1],
+ * H_2m = [[H_m, H_m], [H_m, -H_m]] (Sec. 3 eq. 3.4: an orthogonal rotation
+ * leaves q.k unchanged; App. D.4 rotates K only).  Evaluated in fp32 with
+ * round-to-nearest in this order: butterfly stages h = 1, 2, 4, ..., n/2, in
+ * which each pair (i, i + h) with bit h of i clear becomes (a + b, a - b);
+ * then every value is multiplied by the fp32 value nearest to 1/sqrt(n). */
+void kv4o_hadamard_f32(float* x, int n) {
+  int old = fegetround();
+  fesetround(FE_TONEAREST);
+  for (int h = 1; h < n; h <<= 1)
+    for (int i = 0; i < n; ++i)
+      if (!(i & h)) {
+        float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+  float c = (float)(1.0 / sqrt((double)n));
+  for (int i = 0; i < n; ++i) x[i] = x[i] * c;
+  fesetround(old);
+}
+
+void kv4o_hadamard_f32_n(float* x, long rows, int n) {
+  for (long r = 0; r < rows; ++r) kv4o_hadamard_f32(x + r * n, n);
+}
+
 /* ------------------------------------------------- packed append (bytes) */
 /*
  * Packed layout, restated from the library's layout description:
@@ -298,12 +333,13 @@ static void put_u16(uint8_t* p, uint16_t v) {
 
 /* Append T tokens: INT4 for every position, INT8 side entry for protected
  * positions of the final length seq_lens[seq] (ring entries only for positions
- * inside the final recent window).  Returns the OR of status bits. */
+ * inside the final recent window, reading R6).  rotate_k: K is first rotated
+ * by kv4o_hadamard_f32 (reading R9; V never is).  Returns the OR of status bits. */
 int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int num_pages,
                       int max_pages_per_seq, uint8_t* paged, uint8_t* side,
                       const uint16_t* k_new, const uint16_t* v_new, const int32_t* tok_seq,
                       const int32_t* tok_pos, int T, const int32_t* seq_lens,
-                      const int32_t* block_table) {
+                      const int32_t* block_table, int rotate_k) {
   int status = 0;
   int ng = d_h / g;
   long cb = chunk_bytes(d_h, g);
@@ -335,6 +371,7 @@ int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int 
       for (int kv = 0; kv < 2; ++kv) {
         const uint16_t* src = (kv == 0 ? k_new : v_new) + ((long)t * h_kv + h) * d_h;
         for (int d = 0; d < d_h; ++d) x[d] = kv4o_bf16_to_f32(src[d]);
+        if (rotate_k && kv == 0) kv4o_hadamard_f32(x, d_h);
         uint8_t* rows = chunk + (long)kv * 16 * (d_h / 2) + (long)slot * (d_h / 2);
         uint8_t* meta = chunk + 16L * d_h + (long)kv * 16 * ng * 4 + (long)slot * ng * 4;
         for (int j = 0; j < ng; ++j) {
@@ -373,9 +410,10 @@ int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int 
 /* Dequantized cache of one sequence, fp64, for all L positions (reading R5):
  * protected positions decode the INT8 entry s*c, the rest the INT4 entry
  * Delta*c + m (Sec. 3 eq. 3.3).  k_src/v_src: [h_kv][L][d_h] bf16 bits.
- * k_hat/v_hat: [h_kv][L][d_h].  Returns status bits. */
+ * k_hat/v_hat: [h_kv][L][d_h].  rotate_k: K is rotated (kv4o_hadamard_f32)
+ * before it is quantized.  Returns status bits. */
 int kv4o_dequant_seq(int h_kv, int d_h, int g, int S, int R, int L, const uint16_t* k_src,
-                     const uint16_t* v_src, double* k_hat, double* v_hat) {
+                     const uint16_t* v_src, double* k_hat, double* v_hat, int rotate_k) {
   int status = 0;
   int ng = d_h / g;
   float x[1024];
@@ -387,6 +425,7 @@ int kv4o_dequant_seq(int h_kv, int d_h, int g, int S, int R, int L, const uint16
         const uint16_t* src = (kv == 0 ? k_src : v_src) + ((long)h * L + p) * d_h;
         double* dst = (kv == 0 ? k_hat : v_hat) + ((long)h * L + p) * d_h;
         for (int d = 0; d < d_h; ++d) x[d] = kv4o_bf16_to_f32(src[d]);
+        if (rotate_k && kv == 0) kv4o_hadamard_f32(x, d_h);
         if (kv4o_is_protected(p, L, S, R)) {
           uint16_t s16;
           status |= kv4o_int8_encode_vec(x, d_h, c8, &s16);
@@ -406,7 +445,7 @@ int kv4o_dequant_seq(int h_kv, int d_h, int g, int S, int R, int L, const uint16
   return status;
 }
 
-/* Plain softmax attention in fp64 over a dequantized sequence (reading R6).
+/* Plain softmax attention in fp64 over a dequantized sequence (reading R7).
  * q: [h_q][d_h] bf16 bits; k_hat/v_hat: [h_kv][L][d_h]; out: [h_q][d_h];
  * lse: [h_q] (natural log of the softmax normaliser of the scaled scores).
  * scratch: L doubles.  L == 0 gives out = 0 and lse = -inf. */
