@@ -185,6 +185,42 @@ int kv4_quant_append(const kv4_layout* layout, void* paged, void* side, const ui
                      int32_t* dev_status, void* stream);
 
 /*
+ * Hadamard K-rotation (KV4-RL Sec. 3 eq. 3.4: for a normalized Hadamard H with
+ * H H^T = I, (qH)(kH)^T = q k^T, so keys may be stored rotated when queries
+ * are rotated too; App. A.3 "Encoding and allocation": K and Q rotated after
+ * RoPE, V in its original basis; App. D.4 keeps the rotation K-only).
+ *
+ * H is the normalized Sylvester matrix of order head_dim (H_1 = [1],
+ * H_2m = [[H_m, H_m], [H_m, -H_m]], divided by sqrt(head_dim)); no random
+ * signs.  It is evaluated in fp32 in one fixed order: butterfly stages
+ * h = 1, 2, 4, ..., head_dim/2, each turning the channel pair (i, i+h) with
+ * bit h of i clear into (a + b, a - b), then a multiply by the fp32 value
+ * nearest 1/sqrt(head_dim); every operation rounds to nearest even.
+ *
+ * kv4_quant_append_hadamard -- kv4_quant_append with every K vector replaced
+ *   by H k (fp32, before both the INT4 and the INT8 encoding); V is encoded
+ *   as given.  Same arguments, layout, validation and status bits.  A cache
+ *   must be written by one of the two entry points only, and read with
+ *   rotated queries when written by this one.
+ *
+ * kv4_hadamard_bf16 -- the query side: each of `rows` rows of `dim` bf16
+ *   values x becomes H x rounded to bf16 (nearest even).  Use it on q before
+ *   kv4_decode_attn over a cache written by kv4_quant_append_hadamard; the
+ *   scores are then sm_scale * (Hq).(k^ of Hk).
+ *     x, y   device bf16 [rows][dim], 8-byte aligned; y == x (in place) is
+ *            allowed, any other overlap is KV4_ERR_INVALID_ARG
+ *     dim    64 or 128 (the supported head dimensions), else KV4_ERR_INVALID_ARG
+ *     rows   >= 0; rows == 0 is a no-op
+ *   Non-finite inputs give non-finite outputs (no status word).
+ */
+int kv4_quant_append_hadamard(const kv4_layout* layout, void* paged, void* side,
+                              const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* tok_seq, const int32_t* tok_pos, int32_t T,
+                              const int32_t* seq_lens, const int32_t* block_table,
+                              int32_t* dev_status, void* stream);
+int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim, void* stream);
+
+/*
  * kv4_decode_attn -- split-KV GQA decode attention over the mixed cache
  * (KV4-RL Sec. 5.3 and App. A.3: disjoint INT4 and protected regions, each
  * split producing a locally normalised output and log-normaliser, merged by

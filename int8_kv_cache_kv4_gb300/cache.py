@@ -16,8 +16,12 @@ from . import workloads as W
 
 
 class MixedKVCache:
+    """hadamard_k=True stores K rotated by the normalized Hadamard matrix
+    (kv4_quant_append_hadamard) and rotates each query the same way
+    (kv4_hadamard_bf16) before decode; callers pass unrotated K and q."""
+
     def __init__(self, *, h_q=32, h_kv=8, d_h=128, group=32, sink=4, recent=128, max_seqs,
-                 num_pages, max_pages_per_seq, device="cuda", with_bf16=False):
+                 num_pages, max_pages_per_seq, device="cuda", with_bf16=False, hadamard_k=False):
         import torch
         self.layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=group, sink=sink,
                                       recent=recent, max_seqs=max_seqs, num_pages=num_pages,
@@ -36,6 +40,8 @@ class MixedKVCache:
                                       device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self._ws = {}
+        self.hadamard_k = bool(hadamard_k)
+        self._qrot = {}
 
     @property
     def sm_scale(self) -> float:
@@ -55,14 +61,25 @@ class MixedKVCache:
         return self._ws[key]
 
     def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
-        kv4.kv4_quant_append(self.layout, self.paged, self.side, k_new, v_new, tok_seq, tok_pos,
-                             seq_lens, self.block_table, self.status, stream)
+        fn = kv4.kv4_quant_append_hadamard if self.hadamard_k else kv4.kv4_quant_append
+        fn(self.layout, self.paged, self.side, k_new, v_new, tok_seq, tok_pos, seq_lens,
+           self.block_table, self.status, stream)
         if self.bf16 is not None:
             kv4.kv4_bf16_append(self.layout, self.bf16, k_new, v_new, tok_seq, tok_pos, seq_lens,
                                 self.block_table, self.status, stream)
 
+    def rotated_query(self, q, stream=None):
+        """q rotated like the stored keys (a scratch tensor reused per shape)."""
+        import torch
+        key = tuple(q.shape)
+        if key not in self._qrot:
+            self._qrot[key] = torch.empty_like(q)
+        return kv4.kv4_hadamard_bf16(q, self._qrot[key], stream)
+
     def decode(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
         ws = self.workspace(int(q.shape[0]), max_splits)
+        if self.hadamard_k:
+            q = self.rotated_query(q, stream)
         kv4.kv4_decode_attn(self.layout, self.paged, self.side, q, seq_lens, self.block_table, ws,
                             out, out_lse, self.sm_scale, max_splits, self.status, stream)
 

@@ -8,7 +8,8 @@
 namespace kv4 {
 cudaError_t launch_quant_append(const Layout&, void*, void*, const uint16_t*, const uint16_t*,
                                 const int32_t*, const int32_t*, int, const int32_t*,
-                                const int32_t*, int32_t*, cudaStream_t);
+                                const int32_t*, int32_t*, bool, cudaStream_t);
+cudaError_t launch_hadamard_bf16(const uint16_t*, uint16_t*, long long, int, cudaStream_t);
 cudaError_t launch_bf16_append(const Layout&, void*, const uint16_t*, const uint16_t*,
                                const int32_t*, const int32_t*, int, const int32_t*, const int32_t*,
                                int32_t*, cudaStream_t);
@@ -217,10 +218,10 @@ size_t kv4_workspace_bytes(const kv4_layout* l, int32_t num_seqs, int32_t max_sp
   return ws_bytes(l, num_seqs, make_plan(l, num_seqs, max_splits, true), max_splits);
 }
 
-int kv4_quant_append(const kv4_layout* l, void* paged, void* side, const uint16_t* k_new,
-                     const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
-                     int32_t T, const int32_t* seq_lens, const int32_t* block_table,
-                     int32_t* dev_status, void* stream) {
+static int quant_append(const kv4_layout* l, void* paged, void* side, const uint16_t* k_new,
+                        const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                        int32_t T, const int32_t* seq_lens, const int32_t* block_table,
+                        int32_t* dev_status, bool rotate_k, void* stream) {
   int rc = kv4_check_layout(l);
   if (rc != KV4_OK) return rc;
   if (T < 0) return KV4_ERR_INVALID_ARG;
@@ -231,7 +232,36 @@ int kv4_quant_append(const kv4_layout* l, void* paged, void* side, const uint16_
   if (!aligned16(paged) || !aligned16(side) || !aligned16(k_new) || !aligned16(v_new))
     return KV4_ERR_INVALID_ARG;
   cudaError_t e = launch_quant_append(to_layout(l), paged, side, k_new, v_new, tok_seq, tok_pos,
-                                      T, seq_lens, block_table, dev_status, (cudaStream_t)stream);
+                                      T, seq_lens, block_table, dev_status, rotate_k,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_quant_append(const kv4_layout* l, void* paged, void* side, const uint16_t* k_new,
+                     const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                     int32_t T, const int32_t* seq_lens, const int32_t* block_table,
+                     int32_t* dev_status, void* stream) {
+  return quant_append(l, paged, side, k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table,
+                      dev_status, false, stream);
+}
+
+int kv4_quant_append_hadamard(const kv4_layout* l, void* paged, void* side,
+                              const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* tok_seq, const int32_t* tok_pos, int32_t T,
+                              const int32_t* seq_lens, const int32_t* block_table,
+                              int32_t* dev_status, void* stream) {
+  return quant_append(l, paged, side, k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table,
+                      dev_status, true, stream);
+}
+
+int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim, void* stream) {
+  if (rows < 0 || (dim != 64 && dim != 128)) return KV4_ERR_INVALID_ARG;
+  if (rows == 0) return KV4_OK;
+  if (!x || !y || ((uintptr_t)x & 7u) || ((uintptr_t)y & 7u)) return KV4_ERR_INVALID_ARG;
+  const uintptr_t bytes = (uintptr_t)rows * (uintptr_t)dim * 2u;
+  if (x != y && (uintptr_t)x < (uintptr_t)y + bytes && (uintptr_t)y < (uintptr_t)x + bytes)
+    return KV4_ERR_INVALID_ARG;  // partial overlap
+  cudaError_t e = launch_hadamard_bf16(x, y, rows, dim, (cudaStream_t)stream);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 

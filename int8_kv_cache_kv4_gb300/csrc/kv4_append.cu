@@ -12,6 +12,15 @@
 // slot row of 64 bytes is one coalesced store.  Rounding follows the layout
 // header's rules exactly (directed fp32 ops and fp16 conversions), which makes
 // the written bytes bit-identical to the CPU oracle.
+//
+// The rotating variant first turns each K vector into H k with H the
+// normalized Sylvester-Hadamard matrix of order head_dim (KV4-RL Sec. 3
+// eq. 3.4: an orthogonal H applied to both q and k leaves q.k unchanged;
+// App. A.3 "Encoding and allocation": K rotated after RoPE, V in its own
+// basis; App. D.4 keeps the rotation K-only).  The query side of the same
+// rotation is hadamard_bf16_kernel below.
+#include <cmath>
+
 #include "kv4_common.cuh"
 
 namespace kv4 {
@@ -108,6 +117,39 @@ __device__ inline uint32_t encode_int8(const float x[4], int lanes, uint16_t* sc
   return out;
 }
 
+// In-place normalized Hadamard rotation of a head_dim-vector spread over the
+// warp: lane l holds channels 4l..4l+3 in x[0..3]; lanes at or past d/4 hold
+// zeros and only ever pair among themselves.  The butterfly runs stages
+// h = 1, 2, 4, ..., d/2 in that order; at each, the pair of channels (i, i+h)
+// with bit h of i clear becomes (a + b, a - b) for a = x_i, b = x_(i+h).
+// Stages 1 and 2 stay inside a lane; stage h = 4m pairs lane l with lane
+// l ^ m.  A final multiply by c (the fp32 value nearest 1/sqrt(d)) normalizes.
+// Every step is an explicitly rounded fp32 operation in this fixed order, so
+// the result is reproducible bit for bit by any implementation of the same
+// order.  All 32 lanes must call it (full-mask shuffles).
+__device__ inline void hadamard_warp(float x[4], int d, float c) {
+  const float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
+  const float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
+  x[0] = __fadd_rn(a0, a2);
+  x[2] = __fsub_rn(a0, a2);
+  x[1] = __fadd_rn(a1, a3);
+  x[3] = __fsub_rn(a1, a3);
+  const int lane = threadIdx.x & 31;
+  for (int m = 1; 4 * m < d; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], c);
+}
+
+// fp32 value nearest 1/sqrt(d), computed on the host in double precision.
+static float hadamard_scale(int d) { return (float)(1.0 / std::sqrt((double)d)); }
+
 // Validate a token; returns the physical page or -1 (status already set).
 __device__ inline int token_page(const Layout& L, int s, int p, const int32_t* seq_lens,
                                  const int32_t* block_table, int32_t* status, bool report,
@@ -130,12 +172,13 @@ __device__ inline int token_page(const Layout& L, int s, int p, const int32_t* s
   return page;
 }
 
+template <bool kRotateK>
 __global__ void __launch_bounds__(256) quant_append_kernel(
     Layout L, uint8_t* __restrict__ paged, uint8_t* __restrict__ side,
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
     const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos, int T,
     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
-    int32_t* status) {
+    int32_t* status, float hc) {
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= (long long)T * L.h_kv) return;
@@ -163,6 +206,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
                   bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
     if (!active) x[0] = x[1] = x[2] = x[3] = 0.f;
+    if (kRotateK && kv == 0) hadamard_warp(x, d_h, hc);  // before both encoders
     uint32_t meta;
     uint32_t codes = encode_int4(x, span, &meta, &bad);
     if (active) {
@@ -222,13 +266,56 @@ __global__ void __launch_bounds__(256) bf16_append_kernel(
 cudaError_t launch_quant_append(const Layout& L, void* paged, void* side, const uint16_t* k_new,
                                 const uint16_t* v_new, const int32_t* tok_seq,
                                 const int32_t* tok_pos, int T, const int32_t* seq_lens,
-                                const int32_t* block_table, int32_t* status, cudaStream_t st) {
+                                const int32_t* block_table, int32_t* status, bool rotate_k,
+                                cudaStream_t st) {
   const long long warps = (long long)T * L.h_kv;
   const int wpb = 8;
   const long long blocks = (warps + wpb - 1) / wpb;
-  quant_append_kernel<<<(unsigned)blocks, wpb * 32, 0, st>>>(
-      L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
-      block_table, status);
+  if (rotate_k)
+    quant_append_kernel<true><<<(unsigned)blocks, wpb * 32, 0, st>>>(
+        L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
+        block_table, status, hadamard_scale(L.d_h));
+  else
+    quant_append_kernel<false><<<(unsigned)blocks, wpb * 32, 0, st>>>(
+        L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
+        block_table, status, 1.0f);
+  return cudaGetLastError();
+}
+
+// Query side of the K rotation: each row of d bf16 values becomes H x rounded
+// to bf16 (nearest even).  One warp per row; lane l reads and writes channels
+// 4l..4l+3 as one 8-byte word.  x and y may be the same array: a warp reads its
+// whole row into registers before any lane writes.
+__global__ void __launch_bounds__(256) hadamard_bf16_kernel(const uint16_t* x, uint16_t* y,
+                                                            long long rows, int d, float hc) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const bool active = 4 * lane < d;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (active) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + r * d + 4 * lane);
+    v[0] = bf16_bits_to_f32(raw.x & 0xFFFFu);
+    v[1] = bf16_bits_to_f32(raw.x >> 16);
+    v[2] = bf16_bits_to_f32(raw.y & 0xFFFFu);
+    v[3] = bf16_bits_to_f32(raw.y >> 16);
+  }
+  hadamard_warp(v, d, hc);
+  if (active) {
+    uint2 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[0])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[3])) << 16);
+    *reinterpret_cast<uint2*>(y + r * d + 4 * lane) = o;
+  }
+}
+
+cudaError_t launch_hadamard_bf16(const uint16_t* x, uint16_t* y, long long rows, int d,
+                                 cudaStream_t st) {
+  const int wpb = 8;
+  const long long blocks = (rows + wpb - 1) / wpb;
+  hadamard_bf16_kernel<<<(unsigned)blocks, wpb * 32, 0, st>>>(x, y, rows, d, hadamard_scale(d));
   return cudaGetLastError();
 }
 

@@ -99,6 +99,8 @@ def load(build_if_missing: bool = False):
         "kv4_num_splits": (I, [LP, I, I]),
         "kv4_workspace_bytes": (Sz, [LP, I, I]),
         "kv4_quant_append": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
+        "kv4_quant_append_hadamard": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
+        "kv4_hadamard_bf16": (ctypes.c_int, [P, P, I, I, P]),
         "kv4_decode_attn": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, Sz, P, P,
                                            P, P]),
         "kv4_split_combine": (ctypes.c_int, [P, P, I, I, I, P, P, P]),
@@ -178,6 +180,36 @@ def workspace_bytes(layout: kv4_layout, num_seqs: int, max_splits: int = 0) -> i
 def kv4_quant_append(layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens, block_table,
                      status=None, stream=None):
     """Quantize-on-append of T tokens (k_new/v_new bf16 [T][h_kv][d_h])."""
+    _quant_append("kv4_quant_append", layout, paged, side, k_new, v_new, tok_seq, tok_pos,
+                  seq_lens, block_table, status, stream)
+
+
+def kv4_quant_append_hadamard(layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens,
+                              block_table, status=None, stream=None):
+    """kv4_quant_append with K rotated by the normalized Hadamard matrix first."""
+    _quant_append("kv4_quant_append_hadamard", layout, paged, side, k_new, v_new, tok_seq,
+                  tok_pos, seq_lens, block_table, status, stream)
+
+
+def kv4_hadamard_bf16(x, y=None, stream=None):
+    """Rotate every row of x (bf16 [..., d], d = 64 or 128) by the normalized
+    Hadamard matrix into y (default: in place).  Returns y."""
+    import torch
+    _dev(x, torch.bfloat16, "x")
+    if y is None:
+        y = x
+    _dev(y, torch.bfloat16, "y")
+    if y.shape != x.shape:
+        raise KV4Error("kv4_hadamard_bf16: x and y differ in shape")
+    d = int(x.shape[-1]) if x.dim() else 0
+    rows = x.numel() // d if d else 0
+    rc = load().kv4_hadamard_bf16(_ptr(x), _ptr(y), rows, d, _stream(stream))
+    _check(rc, "kv4_hadamard_bf16")
+    return y
+
+
+def _quant_append(name, layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens,
+                  block_table, status, stream):
     import torch
     _dev(paged, torch.uint8, "paged")
     _dev(side, torch.uint8, "side")
@@ -188,11 +220,11 @@ def kv4_quant_append(layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_le
         _dev(t, torch.int32, n)
     T = int(tok_seq.numel())
     if tok_pos.numel() != T or k_new.numel() != T * layout.num_kv_heads * layout.head_dim:
-        raise KV4Error("kv4_quant_append: token arrays disagree in length")
-    rc = load().kv4_quant_append(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(k_new),
-                                 _ptr(v_new), _ptr(tok_seq), _ptr(tok_pos), T, _ptr(seq_lens),
-                                 _ptr(block_table), _ptr(status), _stream(stream))
-    _check(rc, "kv4_quant_append")
+        raise KV4Error(f"{name}: token arrays disagree in length")
+    rc = getattr(load(), name)(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(k_new),
+                               _ptr(v_new), _ptr(tok_seq), _ptr(tok_pos), T, _ptr(seq_lens),
+                               _ptr(block_table), _ptr(status), _stream(stream))
+    _check(rc, name)
 
 
 def kv4_decode_attn(layout, paged, side, q, seq_lens, block_table, workspace, out, out_lse=None,

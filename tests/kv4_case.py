@@ -19,7 +19,9 @@ class Case:
     """A batch of sequences with seeded K/V/q, a seeded page permutation and
     token lists for a populate append followed by a one-token append."""
 
-    def __init__(self, lens, *, h_q=32, h_kv=8, d_h=128, g=32, S=4, R=64, seed=1, extra_pages=3):
+    def __init__(self, lens, *, h_q=32, h_kv=8, d_h=128, g=32, S=4, R=64, seed=1, extra_pages=3,
+                 rotate_k=False):
+        self.rotate_k = bool(rotate_k)
         self.lens = np.asarray(lens, dtype=np.int32)
         self.B = len(self.lens)
         self.h_q, self.h_kv, self.d_h, self.g, self.S, self.R = h_q, h_kv, d_h, g, S, R
@@ -69,15 +71,17 @@ class Case:
         for stage in (0, 1):
             k, v, s, p, la = self.tokens(stage)
             st |= oracle.quant_append(**self.layout_kw(), paged=paged, side=side, k_new=k, v_new=v,
-                                      tok_seq=s, tok_pos=p, seq_lens=la, block_table=self.bt)
+                                      tok_seq=s, tok_pos=p, seq_lens=la, block_table=self.bt,
+                                      rotate_k=self.rotate_k)
         return paged, side, st
 
     def oracle_decode(self, seqs=None):
         seqs = range(self.B) if seqs is None else seqs
         outs, lses = {}, {}
         for b in seqs:
-            o, l, _ = oracle.decode_seq(self.q[b], self.k[b], self.v[b], g=self.g, S=self.S,
-                                        R=self.R, sm_scale=self.sm_scale)
+            q = oracle.hadamard_bf16(self.q[b]) if self.rotate_k else self.q[b]
+            o, l, _ = oracle.decode_seq(q, self.k[b], self.v[b], g=self.g, S=self.S,
+                                        R=self.R, sm_scale=self.sm_scale, rotate_k=self.rotate_k)
             outs[b], lses[b] = o, l
         return outs, lses
 
@@ -97,7 +101,8 @@ class Case:
         dev = torch.device("cuda")
         c = MixedKVCache(h_q=self.h_q, h_kv=self.h_kv, d_h=self.d_h, group=self.g, sink=self.S,
                          recent=self.R, max_seqs=self.B, num_pages=self.num_pages,
-                         max_pages_per_seq=self.mpps, device=dev, with_bf16=with_bf16)
+                         max_pages_per_seq=self.mpps, device=dev, with_bf16=with_bf16,
+                         hadamard_k=self.rotate_k)
         c.set_block_table(self.bt)
         for stage in (0, 1):
             k, v, s, p, la = self.tokens(stage)

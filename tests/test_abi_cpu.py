@@ -92,3 +92,22 @@ def test_null_arguments_rejected_on_host(lib):
     assert lib.kv4_quant_append(ctypes.byref(lay), None, None, None, None, None, None, 0, None,
                                 None, None, None) == kv4.KV4_OK   # T == 0: no-op
     assert lib.kv4_status_string(kv4.KV4_ERR_WORKSPACE) == b"workspace too small"
+
+
+def test_hadamard_entry_points_validate_on_host(lib):
+    # every rejection happens before any launch; rows == 0 / T == 0 are no-ops
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.kv4_hadamard_bf16(base, base, 0, 128, None) == kv4.KV4_OK
+    assert lib.kv4_hadamard_bf16(base, base, 4, 96, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_hadamard_bf16(base, base, -1, 128, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_hadamard_bf16(None, base, 4, 128, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_hadamard_bf16(base + 2, base + 2, 4, 64, None) == kv4.KV4_ERR_INVALID_ARG
+    # y overlapping x without being x
+    assert lib.kv4_hadamard_bf16(base, base + 8, 4, 128, None) == kv4.KV4_ERR_INVALID_ARG
+    lay = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+    rc = lib.kv4_quant_append_hadamard(ctypes.byref(lay), None, None, None, None, None, None, 3,
+                                       None, None, None, None)
+    assert rc == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_quant_append_hadamard(ctypes.byref(lay), None, None, None, None, None, None,
+                                         0, None, None, None, None) == kv4.KV4_OK
