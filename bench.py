@@ -509,7 +509,7 @@ def run_report(args):
                           "drift_vs_kv4": {"max_abs": float(drift.max()),
                                            "mean_abs": float(drift.mean())}}), flush=True)
 
-    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5"}
+    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h"}
     if "1" in sel:  # tiny: L2-resident, flushed
         w = W.WORKLOADS["tiny_b4_l512"]
         cache, s, lens, w = build_workload(w, dev)
@@ -560,6 +560,17 @@ def run_report(args):
         w8 = dataclasses.replace(w, recent=int(lens.max()))
         cache, s, lens, w8 = build_workload(w8, dev)
         decode_line("config 4 int8 everywhere", w8, cache, s, lens)
+        del cache
+    if "h" in sel:  # Hadamard K-rotation on the batch-64 layer: rotated append, query rotation
+        w = W.WORKLOADS["qwen3_8b_b64"]
+        cache, s, lens, w = build_workload(w, dev, hadamard_k=True)
+        q_rot = torch.empty_like(s["q"])
+        tq = _timed(_graph(lambda: kv4.kv4_hadamard_bf16(s["q"], q_rot)).replay)
+        qb = 2 * s["q"].numel() * 2
+        # decode here includes the query rotation (MixedKVCache.decode rotates q)
+        decode_line("config 2 hadamard-k", w, cache, s, lens,
+                    extra={"query_rotation": tq,
+                           "query_rotation_GBps": qb / (tq["median_ms"] / 1e3) / 1e9})
         del cache
     if "5" in sel:  # one layer of the 36-layer step per sweep point (x36 for the step)
         w = W.WORKLOADS["qwen3_8b_36l"]

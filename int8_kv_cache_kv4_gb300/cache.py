@@ -96,14 +96,15 @@ class MixedKVCache:
 
 
 def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, seed=None,
-                   extra_tokens=0):
+                   extra_tokens=0, hadamard_k=False):
     """Populate a cache with a seeded synthetic workload (see workloads.py):
     positions [0, L-1) of every sequence by bulk appends, then return the
     decode step's inputs (the new token at position L-1 and the query).
     Sequence b's source K/V come from the generator seeded seed*1000003+b, the
     step token and query from seed*1000003+999983, so any sequence can be
     regenerated for a parity check.  `extra_tokens` reserves block-table room
-    for that many later appends per sequence."""
+    for that many later appends per sequence.  hadamard_k: the cache stores
+    rotated K (MixedKVCache(hadamard_k=True))."""
     import torch
     import dataclasses
     if group is not None or recent is not None or seed is not None:
@@ -117,7 +118,8 @@ def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, 
     num_pages = W.pool_pages(cap, w.extra_pages)
     cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
                          recent=w.recent, max_seqs=B, num_pages=num_pages,
-                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16)
+                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16,
+                         hadamard_k=hadamard_k)
     cache.set_block_table(W.block_table(w.seed, cap, mpps, num_pages))
     outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
     # populate positions [0, L-1) of every sequence (prefill-style bulk append)

@@ -24,7 +24,7 @@ def _lib():
     kv4.load(build_if_missing=True)
 
 
-def _check_seq_bytes(cache, w, b, k_src, v_src, L):
+def _check_seq_bytes(cache, w, b, k_src, v_src, L, rotate_k=False):
     """Oracle-append sequence b's L positions into a private pool (page p at
     pool page p) and compare every page chunk and the side block with the
     device cache."""
@@ -39,7 +39,7 @@ def _check_seq_bytes(cache, w, b, k_src, v_src, L):
                              k_new=np.ascontiguousarray(k_src.transpose(1, 0, 2)),
                              v_new=np.ascontiguousarray(v_src.transpose(1, 0, 2)),
                              tok_seq=np.zeros(L, np.int32), tok_pos=np.arange(L, dtype=np.int32),
-                             seq_lens=np.array([L], np.int32), block_table=bt)
+                             seq_lens=np.array([L], np.int32), block_table=bt, rotate_k=rotate_k)
     assert st == 0
     dev_bt = cache.block_table[b, :npages].cpu().numpy()
     allp = cache.paged.view(-1, w.h_kv * cb)
@@ -50,15 +50,18 @@ def _check_seq_bytes(cache, w, b, k_src, v_src, L):
         assert np.array_equal(gs, side[: w.h_kv * sb]), f"seq {b}: side cache differs"
 
 
-def _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=None):
+def _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=None, rotate_k=False):
     ref_o, ref_l = {}, {}
     for b in seqs:
         k, v = srcs[b]
-        ref_o[b], ref_l[b], _ = oracle.decode_seq(qs[b], k, v, g=w.group, S=w.sink, R=w.recent,
-                                                  sm_scale=1 / math.sqrt(w.d_h))
+        q = oracle.hadamard_bf16(qs[b]) if rotate_k else qs[b]
+        ref_o[b], ref_l[b], _ = oracle.decode_seq(q, k, v, g=w.group, S=w.sink, R=w.recent,
+                                                  sm_scale=1 / math.sqrt(w.d_h), rotate_k=rotate_k)
     mx, mean = compare_outputs(out, lse, ref_o, ref_l, seqs, lens)
     raw = max(float(np.abs(out[b] - ref_o[b]).max()) for b in seqs)
-    print(f"{w.name} g={w.group} R={w.recent}: max {mx:.2e} mean {mean:.2e} raw max {raw:.2e}")
+    big = max(float(np.abs(ref_o[b]).max()) for b in seqs)
+    print(f"{w.name} g={w.group} R={w.recent}: max {mx:.2e} mean {mean:.2e} raw max {raw:.2e} "
+          f"max |o| {big:.3f}")
     if raw_max is not None:
         assert raw <= raw_max, f"raw max abs error {raw:.3e}"
 
@@ -88,6 +91,26 @@ def test_qwen3_8b_batch64_full_size():
         _check_seq_bytes(cache, w, b, *srcs[b], int(lens[b]))
     # diffuse attention at these lengths: the raw error also meets 2e-3
     _check_decode(out, lse, w, seqs, srcs, qs, lens, raw_max=2e-3)
+
+
+def test_qwen3_8b_batch64_full_size_hadamard_k():
+    # the same layer with the K rotation on append and the query rotation
+    w = W.WORKLOADS["qwen3_8b_b64"]
+    dev = torch.device("cuda")
+    cache, s, lens, w = build_workload(w, dev, hadamard_k=True)
+    out, lse = _run_step(cache, s)
+    seqs = _sample(w, lens, 4)
+    qs = s["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+    srcs = {b: source_kv(w, b, int(lens[b]), dev) for b in seqs}
+    for b in seqs[:2]:
+        _check_seq_bytes(cache, w, b, *srcs[b], int(lens[b]), rotate_k=True)
+    # raw error not bounded here: a sampled row attends sharply enough that
+    # |o| >= 1, where half a bf16 ulp of the output alone is 3.9e-3
+    _check_decode(out, lse, w, seqs, srcs, qs, lens, rotate_k=True)
+    plain = max(float(np.abs(oracle.decode_seq(qs[b], *srcs[b], g=w.group, S=w.sink, R=w.recent,
+                                               sm_scale=1 / math.sqrt(w.d_h))[0]).max())
+                for b in seqs)
+    print(f"unrotated cache, same sample: max |o| {plain:.3f}")
 
 
 @pytest.mark.parametrize("recent", [256, 131072])
