@@ -77,6 +77,24 @@ def seq_lengths(w: Workload) -> np.ndarray:
     raise ValueError(w.lengths)
 
 
+def lognormal_length_pmf(median: float, sigma: float, lo: int, hi: int):
+    """The exact distribution of the lognormal lengths seq_lengths draws:
+    round(exp(N(log median, sigma^2))) clipped to [lo, hi].  Returns (support,
+    pmf) over lo..hi; the clipped tails sit on lo and hi."""
+    l = np.arange(lo, hi + 1, dtype=np.float64)
+    mu = math.log(median)
+    cdf = lambda x: 0.5 * (1.0 + np.vectorize(math.erf)((np.log(x) - mu) / (sigma * math.sqrt(2.0))))
+    upper = np.append(cdf(l[:-1] + 0.5), 1.0)
+    lower = np.concatenate([[0.0], cdf(l[1:] - 0.5)])
+    pmf = np.maximum(upper - lower, 0.0)
+    return l.astype(np.int64), pmf / pmf.sum()
+
+
+def sample_lengths(support, pmf, rng, n: int) -> np.ndarray:
+    """n i.i.d. lengths from an explicit pmf."""
+    return np.asarray(support)[rng.choice(len(support), size=n, p=pmf)].astype(np.int64)
+
+
 def outlier_channels(seed: int, h_kv: int, d_h: int) -> np.ndarray:
     """Four fixed key channels per kv head, drawn once per seed: int32 [h_kv][4]."""
     rng = np.random.default_rng([seed, 2])
