@@ -509,7 +509,7 @@ def run_report(args):
                           "drift_vs_kv4": {"max_abs": float(drift.max()),
                                            "mean_abs": float(drift.mean())}}), flush=True)
 
-    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h"}
+    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h", "c"}
     if "1" in sel:  # tiny: L2-resident, flushed
         w = W.WORKLOADS["tiny_b4_l512"]
         cache, s, lens, w = build_workload(w, dev)
@@ -561,6 +561,29 @@ def run_report(args):
         cache, s, lens, w8 = build_workload(w8, dev)
         decode_line("config 4 int8 everywhere", w8, cache, s, lens)
         del cache
+    if "c" in sel:  # KV concentration: continuous refill vs synchronous waves, driven on the GPU
+        from int8_kv_cache_kv4_gb300 import rollout as RO
+        w = W.WORKLOADS["rollout_b256"]
+        sup, pmf = W.lognormal_length_pmf(w.length, w.sigma, w.length_lo, w.length_hi)
+        shape = dict(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
+                     recent=w.recent)
+        waves = RO.wave_schedule(w.batch, args.prompt, sup, pmf, 1, np.random.default_rng([w.seed, 30]))
+        refill = RO.refill_schedule(w.batch, args.prompt, sup, pmf, waves.steps,
+                                    np.random.default_rng([w.seed, 31]))
+        lines = {}
+        for sched in (refill, waves):
+            res = RO.drive(sched, seed=w.seed, **shape)
+            lines[sched.kind] = RO.report(sched, res, **shape)
+            del res
+            torch.cuda.empty_cache()
+            print(json.dumps(dict({"report": "config 3 concentration", "workload": w.name,
+                                   "lengths": "lognormal(median 3000, sigma 0.8) clipped to [256, 16384]",
+                                   "peak_GBps": hbm}, **lines[sched.kind])), flush=True)
+        r, wv = lines["refill"], lines["waves"]
+        print(json.dumps({"report": "config 3 concentration ratio",
+                          "volume_ratio_measured": r["volume_tokens"] / wv["volume_tokens"],
+                          "decode_ms_ratio": r["decode_ms_mean"] / wv["decode_ms_mean"],
+                          "occupancy_waves": wv["active"], "steps_each": waves.steps}), flush=True)
     if "h" in sel:  # Hadamard K-rotation on the batch-64 layer: rotated append, query rotation
         w = W.WORKLOADS["qwen3_8b_b64"]
         cache, s, lens, w = build_workload(w, dev, hadamard_k=True)
@@ -605,6 +628,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
+    ap.add_argument("--prompt", type=int, default=256,
+                    help="prompt length P of the driven rollout schedules (--report c)")
     ap.add_argument("--report", default=None,
                     help="instead of the bench line: per-config report for configs 'all' or e.g. '2,4'")
     args = ap.parse_args()

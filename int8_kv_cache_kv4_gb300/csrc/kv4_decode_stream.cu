@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       }
       p_hi = (int)(min(ue, s_.start + s_.n) - s_.start);
       if (p_j < p_hi) break;
-      seg_next(s_, L, seq_lens, B);
+      seg_next(s_, L, seq_lens, B, ue);
       p_j = (int)(max(ub, s_.start) - s_.start) + warp;
     }
     p_more = 1;
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // segment's partial bookkeeping -- none of it is waited for by a barrier
       {
         Seg nx = cs;
-        seg_next(nx, L, seq_lens, B);
+        seg_next(nx, L, seq_lens, B, sm.u_end);
         const bool new_q = nx.b < B && nx.start < sm.u_end && (nx.b != cs.b || nx.h != cs.h);
         sm.new_q = new_q;
         if (new_q) stream_query_fetch(sm, q, (long long)nx.b * L.h_q + (long long)nx.h * SG);

@@ -60,11 +60,20 @@ __device__ inline int int4_units(int len, const Layout& L) {
   return (int4_pages(len, L) + kSPages - 1) / kSPages;
 }
 
-// Next non-empty segment (b == B when the stream is exhausted).
-__device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B) {
-  do {
-    s.start += s.n;
-    s.cs += seg_cost(s.n, s.type);
+// Next non-empty segment (b == B when the stream is exhausted).  Sequences of
+// length 0 are skipped whole, one length load each.  A caller that needs no
+// segment starting at or after stream position `stop` passes it: the walk then
+// ends (b = B) as soon as the position reaches it, instead of crossing the
+// empty sequences that may follow (idle slots of a batch).
+__device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B,
+                                long long stop = 0x7fffffffffffffffLL) {
+  s.start += s.n;
+  s.cs += seg_cost(s.n, s.type);
+  if (s.start >= stop) {
+    s.b = B;
+    return;
+  }
+  do {  // empty segments add nothing to start or cs
     if (s.type == 0) {
       s.type = 1;
       s.n = int4_units(s.len, L);
@@ -72,8 +81,10 @@ __device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens
       s.type = 0;
       if (++s.h == L.h_kv) {
         s.h = 0;
-        ++s.b;
-        s.len = s.b < B ? clamp_len(__ldg(seq_lens + s.b), L) : 0;
+        do {
+          ++s.b;
+          s.len = s.b < B ? clamp_len(__ldg(seq_lens + s.b), L) : 0;
+        } while (s.len == 0 && s.b < B);
       }
       s.n = prot_units(s.len, L);
     }

@@ -161,6 +161,42 @@ def q_numpy(seed: int, B: int, h_q: int, d_h: int, step: int = 0) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal((B, h_q, d_h), dtype=np.float32))
 
 
+# ------------------------------------------------- rollout token content
+
+# Rollout drivers draw every token's K/V and every step's query from fixed
+# seeded pools, indexed by (response id, position), so that any slot's cache
+# contents can be regenerated on the host for a parity check.
+POOL_TOKENS = 4099
+POOL_QUERIES = 1031
+
+
+def token_pool(seed: int, h_kv: int, d_h: int, n: int = POOL_TOKENS):
+    """K and V rows of the pool: bf16 bits [n][h_kv][d_h], keys with the
+    outlier channels of this seed."""
+    rng = np.random.default_rng([seed, 20])
+    K = rng.standard_normal((n, h_kv, d_h), dtype=np.float32)
+    V = rng.standard_normal((n, h_kv, d_h), dtype=np.float32)
+    outl = outlier_channels(seed, h_kv, d_h)
+    for h in range(h_kv):
+        K[:, h, outl[h]] *= OUTLIER_GAIN
+    return f32_to_bf16_bits(K), f32_to_bf16_bits(V)
+
+
+def query_pool(seed: int, h_q: int, d_h: int, n: int = POOL_QUERIES) -> np.ndarray:
+    rng = np.random.default_rng([seed, 21])
+    return f32_to_bf16_bits(rng.standard_normal((n, h_q, d_h), dtype=np.float32))
+
+
+def token_row(resp, pos, n: int = POOL_TOKENS):
+    """Pool row of the token at position ``pos`` of response ``resp``."""
+    return (np.asarray(resp, dtype=np.int64) * 7919 + np.asarray(pos, dtype=np.int64)) % n
+
+
+def query_row(resp, age, n: int = POOL_QUERIES):
+    """Pool row of the query of response ``resp`` at decode step ``age``."""
+    return (np.asarray(resp, dtype=np.int64) * 131 + np.asarray(age, dtype=np.int64)) % n
+
+
 # ----------------------------------------------------------- device variants
 
 def torch_generator(seed: int, device):

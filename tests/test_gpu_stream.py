@@ -64,3 +64,14 @@ def test_many_short_sequences_and_partial_rings(g_):
 def test_window_shapes(S, R):
     # sink / window sizes that are not multiples of the 8-slot unit
     _run(Case([1, 2, 3, 15, 16, 17, 29, 150, 777], S=S, R=R, g=32, seed=26, h_q=16, h_kv=4))
+
+
+@pytest.mark.parametrize("where", ["spread", "front"])
+def test_few_long_sequences_among_idle_slots(where):
+    # a batch of 240 slots with four long sequences (a synchronous wave's
+    # tail): interleaved with idle slots, or all in front of a tail of idle ones
+    lens = np.zeros(240, dtype=np.int64)
+    pos = [3, 77, 150, 239] if where == "spread" else [0, 1, 2, 3]
+    lens[pos] = [2500, 3100, 1800, 2900]
+    c = Case(lens, S=4, R=64, g=32, seed=24, h_q=8, h_kv=2)
+    _run(c)
