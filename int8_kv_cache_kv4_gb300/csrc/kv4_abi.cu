@@ -35,12 +35,12 @@ bool stream_supported(const Layout&);
 long long stream_partials(const Layout&, int);
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
-                                 int32_t*, uint16_t*, float*, int32_t*, long long*, cudaStream_t);
+                                 int32_t*, uint16_t*, float*, int32_t*, cudaStream_t);
 bool sm_supported(const Layout&);
 size_t sm_qprep_bytes(const Layout&, int);
 cudaError_t launch_decode_sm(const Layout&, const void*, const void*, const uint16_t*,
                              const int32_t*, int, const int32_t*, float, void*, float*, float*,
-                             uint16_t*, float*, int32_t*, long long*, cudaStream_t);
+                             uint16_t*, float*, int32_t*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -94,15 +94,13 @@ static Layout to_layout(const kv4_layout* l) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
-// [rows][n_split], one int32 completion ticket per (sequence, kv head), the
-// stream length the work-balanced kernels record for their separate merge,
-// and (max_splits = 0, while the SM kernel is selected) its per-pair query
+// [rows][n_split], one int32 completion ticket per (sequence, kv head), and
+// (max_splits = 0, while the SM kernel is selected) its per-pair query
 // fragments.
 struct Workspace {
   float* part_o;
   float* part_lse;
   int32_t* tickets;
-  long long* u_total;
   void* qprep;
   size_t ticket_bytes;
   size_t bytes;
@@ -133,12 +131,11 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   const size_t qb = (max_splits == 0 && sm_supported(L) && g_decode_kernel == KV4_KERNEL_SM)
                         ? sm_qprep_bytes(L, num_seqs)
                         : 0;
-  w.bytes = o + z + round256(w.ticket_bytes) + 256 + round256(qb);
-  w.qprep = qb ? (void*)((char*)base + o + z + round256(w.ticket_bytes) + 256) : nullptr;
+  w.bytes = o + z + round256(w.ticket_bytes) + round256(qb);
+  w.qprep = qb ? (void*)((char*)base + o + z + round256(w.ticket_bytes)) : nullptr;
   w.part_o = (float*)base;
   w.part_lse = (float*)((char*)base + o);
   w.tickets = (int32_t*)((char*)base + o + z);
-  w.u_total = (long long*)((char*)base + o + z + round256(w.ticket_bytes));
   return w;
 }
 static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
@@ -292,18 +289,18 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   if (which == KV4_KERNEL_SM && (max_splits > 0 || !sm_supported(L))) which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
   // Completion tickets for the fused eq. A1 merge start at zero on every call
-  // (the SM kernel takes none: its pairs are merged by a separate kernel).
-  if (which != KV4_KERNEL_SM &&
+  // (the SM kernel takes none: its pairs are merged by a separate kernel; the
+  // stream kernel clears them itself when it merges in-kernel).
+  if (which != KV4_KERNEL_SM && which != KV4_KERNEL_STREAM &&
       cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
     return KV4_ERR_LAUNCH;
   cudaError_t e;
   if (which == KV4_KERNEL_SM)
     e = launch_decode_sm(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, w.qprep,
-                         w.part_o, w.part_lse, out, out_lse, dev_status, w.u_total, st);
+                         w.part_o, w.part_lse, out, out_lse, dev_status, st);
   else if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, w.u_total,
-                             st);
+                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, st);
   else if (which == KV4_KERNEL_TCGEN05)
     e = launch_decode_tc(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                          p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
     const QPrep* __restrict__ qprep, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
     float* __restrict__ part_lse, uint16_t* __restrict__ out, float* __restrict__ out_lse,
-    int32_t* status, long long* __restrict__ u_total) {
+    int32_t* status) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -187,7 +187,6 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
   __syncthreads();
   const long long U = sm.total;
   const int Cw = (int)min((long long)C, U);
-  if (c == 0 && threadIdx.x == 0) *u_total = U;  // for stream_merge_kernel
   const long long u_begin = c < Cw ? U * c / Cw : U, u_end = c < Cw ? U * (c + 1) / Cw : U;
   if (threadIdx.x == 0) {
     sm.u_begin = u_begin;
@@ -864,9 +863,8 @@ __global__ void __launch_bounds__(kMThreads, 1) decode_sm_kernel(
 }  // namespace
 
 cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
-                                const float* part_o, const float* part_lse,
-                                const long long* u_total, int C, int by_cost, uint16_t* out,
-                                float* out_lse, cudaStream_t st);
+                                const float* part_o, const float* part_lse, int C, int by_cost,
+                                bool overlap, uint16_t* out, float* out_lse, cudaStream_t st);
 
 bool sm_supported(const Layout& L) { return L.d_h == SD && L.h_q == SG * L.h_kv; }
 
@@ -878,8 +876,7 @@ template <int NG>
 cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, const uint16_t* q,
                         const int32_t* seq_lens, int num_seqs, const int32_t* block_table,
                         float sm_scale, void* qprep, float* part_o, float* part_lse,
-                        uint16_t* out, float* out_lse, int32_t* status,
-                        long long* u_total, cudaStream_t st) {
+                        uint16_t* out, float* out_lse, int32_t* status, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
       ((sizeof(SmSmem) + 127) / 128) * 128 + (size_t)kMW * kMStages * kSPages * cb;
@@ -904,13 +901,12 @@ cudaError_t launch_sm_t(const Layout& L, const void* paged, const void* side, co
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   decode_sm_kernel<NG><<<grid, kMThreads, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, (const QPrep*)qprep, seq_lens, num_seqs,
-      block_table, sm_scale * kLog2e, part_o, part_lse, out, out_lse, status,
-      u_total);
+      block_table, sm_scale * kLog2e, part_o, part_lse, out, out_lse, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // every pair's partials are merged by the separate merge kernel: a warp of
   // this kernel that merged them itself would hold up its claimed units for
   // the whole of the pair's eq. A1 (measured: slower than one more launch)
-  e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, 0, out, out_lse,
+  e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, grid, 0, false, out, out_lse,
                           st);
   return e;
 }
@@ -919,17 +915,17 @@ cudaError_t launch_decode_sm(const Layout& L, const void* paged, const void* sid
                              const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                              const int32_t* block_table, float sm_scale, void* qprep,
                              float* part_o, float* part_lse, uint16_t* out,
-                             float* out_lse, int32_t* status, long long* u_total, cudaStream_t st) {
+                             float* out_lse, int32_t* status, cudaStream_t st) {
   switch (L.d_h / L.g) {
     case 4:
       return launch_sm_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, st);
     case 2:
       return launch_sm_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, st);
     case 1:
       return launch_sm_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, qprep,
-                            part_o, part_lse, out, out_lse, status, u_total, st);
+                            part_o, part_lse, out, out_lse, status, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
-    float* __restrict__ out_lse, int32_t* status, int defer, long long* __restrict__ u_total) {
+    float* __restrict__ out_lse, int32_t* status, int defer) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -282,6 +282,10 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   uint8_t* stage_base = smem_raw + ((sizeof(StreamSmem) + 127) / 128) * 128;
   const int C = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a deferred merge (stream_merge_kernel, launched as this grid's programmatic
+  // dependent) may take the SMs this grid's CTAs free; it waits for the whole
+  // grid before reading any result
+  if (defer) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ------------------------------------------ stream size and this CTA's start
   const int per = (B + kST - 1) / kST;
@@ -336,10 +340,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   // wide, so every working CTA holds a unit (the partial counts rely on it).
   const long long U = sm.total, Wc = sm.totalc;
   const int Cw = stream_ctas(Wc, C);
-  if (defer && c == 0 && threadIdx.x == 0) {  // for stream_merge_kernel
-    u_total[0] = U;
-    u_total[1] = Wc;
-  }
   if (c < Cw) {
     const long long Tb = (c * Wc + Cw - 1) / Cw, Te = ((c + 1) * Wc + Cw - 1) / Cw;
     const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kST + threadIdx.x];
@@ -989,12 +989,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
 // eight warps splitting the pair's partials.  The partial positions follow
 // from the stream's share arithmetic (U recorded by the decode kernel).
 constexpr int kMergeThreads = 256;
+// partials of one pair: each of its two regions spans at most every CTA of the grid
+constexpr int kMergeMaxParts = 2 * kMaxStreamCtas + 2;
 __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
     Layout L, const int32_t* __restrict__ seq_lens, int B, const float* __restrict__ part_o,
-    const float* __restrict__ part_lse, const long long* __restrict__ u_total, int C, int by_cost,
+    const float* __restrict__ part_lse, int C, int by_cost,
     uint16_t* __restrict__ out, float* __restrict__ out_lse) {
-  __shared__ long long red64[kMergeThreads / 32];
-  __shared__ long long redc[kMergeThreads / 32];
+  __shared__ long long red64[4][kMergeThreads / 32];
   __shared__ float redf[kMergeThreads / 32];
   __shared__ float4 acc_s[kMergeThreads / 32][32];
   const int pair = blockIdx.x / SG, j = blockIdx.x % SG;
@@ -1002,42 +1003,59 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int len = clamp_len(__ldg(seq_lens + b), L);
   if (len == 0) return;  // the decode kernel wrote its zero output
-  // stream index and stream cost of the pair's first unit: the units and cost
-  // of all earlier sequences, then of the sequence's earlier kv heads
-  long long mine = 0, mine_c = 0;
-  for (int bb = threadIdx.x; bb < b; bb += kMergeThreads) {
+  // stream index and stream cost of the pair's first unit (the units and cost
+  // of all earlier sequences, then of the sequence's earlier kv heads), and the
+  // stream's length U and cost Wc, by the decode kernel's own count
+  long long v[4] = {0, 0, 0, 0};  // units and cost before sequence b; units and cost of all
+  for (int bb = threadIdx.x; bb < B; bb += kMergeThreads) {
     const int lb = clamp_len(__ldg(seq_lens + bb), L);
     const int np_ = prot_units(lb, L), n4_ = int4_units(lb, L);
-    mine += (long long)L.h_kv * (np_ + n4_);
-    mine_c += (long long)L.h_kv * (seg_cost(np_, 0) + seg_cost(n4_, 1));
+    const long long u_ = (long long)L.h_kv * (np_ + n4_);
+    const long long c_ = (long long)L.h_kv * (seg_cost(np_, 0) + seg_cost(n4_, 1));
+    if (bb < b) {
+      v[0] += u_;
+      v[1] += c_;
+    }
+    v[2] += u_;
+    v[3] += c_;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mine += __shfl_xor_sync(0xffffffffu, mine, o);
-    mine_c += __shfl_xor_sync(0xffffffffu, mine_c, o);
-  }
-  if (lane == 0) {
-    red64[warp] = mine;
-    redc[warp] = mine_c;
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    if (lane == 0) red64[i][warp] = v[i];
   }
   __syncthreads();
-  long long pre = 0, pre_c = 0;
+  long long pre = 0, pre_c = 0, U = 0, Wc = 0;
   for (int w = 0; w < kMergeThreads / 32; ++w) {
-    pre += red64[w];
-    pre_c += redc[w];
+    pre += red64[0][w];
+    pre_c += red64[1][w];
+    U += red64[2][w];
+    Wc += red64[3][w];
   }
+  if (!by_cost) Wc = 0;
   const int np = prot_units(len, L), n4 = int4_units(len, L);
   const long long gs = pre + (long long)h * (np + n4);
   const long long pcs = pre_c + (long long)h * (seg_cost(np, 0) + seg_cost(n4, 1));
-  const long long U = u_total[0], Wc = by_cost ? u_total[1] : 0;
   const int Cw = by_cost ? stream_ctas(Wc, C) : (int)min((long long)C, U);
   const PairParts pp = pair_parts(gs, pcs, np, n4, by_cost != 0, U, Wc, Cw);
   const int c0 = pp.c0, n0 = pp.n0, c1 = pp.c1, n1 = pp.n1;
   const int n = n0 + n1;
   auto pidx = [&](int k) { return k < n0 ? 2LL * pair + c0 + k : 2LL * pair + 1 + c1 + (k - n0); };
-  // log-normaliser of the whole pair: M = max z_k, Z = sum 2^(z_k - M)
+  // Everything above reads only the inputs; what follows reads what the decode
+  // kernel wrote (launched as its programmatic dependent, this is where the
+  // merge waits for it to complete; otherwise the wait returns at once).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // log-normaliser of the whole pair: M = max z_k, Z = sum 2^(z_k - M).  Each
+  // z_k is read once and its weight kept in shared memory, so that the
+  // partials' outputs are then all requested at once.
+  __shared__ float wsm[kMergeMaxParts];
   float M = -INFINITY;
-  for (int k = threadIdx.x; k < n; k += kMergeThreads) M = fmaxf(M, __ldg(part_lse + pidx(k) * SG + j));
+  for (int k = threadIdx.x; k < n; k += kMergeThreads) {
+    const float z = __ldg(part_lse + pidx(k) * SG + j);
+    wsm[k] = z;
+    M = fmaxf(M, z);
+  }
   M = warp_max(M);
   if (lane == 0) redf[warp] = M;
   __syncthreads();
@@ -1045,11 +1063,12 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   for (int w = 0; w < kMergeThreads / 32; ++w) M = fmaxf(M, redf[w]);
   __syncthreads();
   float Zl = 0.f;
-  if (M != -INFINITY)
-    for (int k = threadIdx.x; k < n; k += kMergeThreads) {
-      const float z = __ldg(part_lse + pidx(k) * SG + j);
-      Zl += z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
-    }
+  for (int k = threadIdx.x; k < n; k += kMergeThreads) {  // the thread's own entries
+    const float z = wsm[k];
+    const float wv = (M == -INFINITY || z == -INFINITY) ? 0.f : exp2f((z - M) * kLog2e);
+    wsm[k] = wv;
+    Zl += wv;
+  }
   Zl = warp_sum(Zl);
   if (lane == 0) redf[warp] = Zl;
   __syncthreads();
@@ -1058,19 +1077,18 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   // sum_k w_k o_k: warp w takes partials k = w, w + 8, ...; lane: channels 4 lane ..
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int k0 = warp; k0 < n; k0 += 4 * (kMergeThreads / 32)) {
-      float wv[4];
-      float4 o[4];
+    for (int k0 = warp; k0 < n; k0 += 8 * (kMergeThreads / 32)) {
+      float wv[8];
+      float4 o[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // four partials' loads in flight
+      for (int u = 0; u < 8; ++u) {  // eight partials' loads in flight
         const int k = k0 + u * (kMergeThreads / 32);
-        const float z = k < n ? __ldg(part_lse + pidx(k) * SG + j) : -INFINITY;
-        wv[u] = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
+        wv[u] = k < n ? wsm[k] : 0.f;
         o[u] = wv[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(part_o + (pidx(k) * SG + j) * SD) + lane)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         a.x = fmaf(wv[u], o[u].x, a.x);
         a.y = fmaf(wv[u], o[u].y, a.y);
         a.z = fmaf(wv[u], o[u].z, a.z);
@@ -1110,15 +1128,26 @@ long long stream_partials(const Layout& L, int num_seqs) {
 }
 
 // Eq. A1 for every pair from the partials a work-balanced decode kernel left
-// on a grid of C CTAs (u_total: the stream length and, when the kernel cut the
-// stream by cost (by_cost), its cost).
+// on a grid of C CTAs, its stream cut into equal unit counts or (by_cost)
+// equal costs; the merge recounts the stream from the lengths.
 cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
-                                const float* part_o, const float* part_lse,
-                                const long long* u_total, int C, int by_cost, uint16_t* out,
-                                float* out_lse, cudaStream_t st) {
-  stream_merge_kernel<<<num_seqs * L.h_kv * SG, kMergeThreads, 0, st>>>(
-      L, seq_lens, num_seqs, part_o, part_lse, u_total, C, by_cost, out, out_lse);
-  return cudaGetLastError();
+                                const float* part_o, const float* part_lse, int C, int by_cost,
+                                bool overlap, uint16_t* out, float* out_lse, cudaStream_t st) {
+  // overlap: the previous kernel on the stream lets its dependents start early
+  // (griddepcontrol.launch_dependents); this kernel then starts on the SMs its
+  // CTAs free and waits for its completion only before reading its results
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_seqs * L.h_kv * SG));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, stream_merge_kernel, L, seq_lens, num_seqs, part_o, part_lse, C,
+                            by_cost, out, out_lse);
 }
 
 template <int NG>
@@ -1126,7 +1155,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                             const int32_t* block_table, float sm_scale, float* part_o,
                             float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                            int32_t* status, long long* u_total, cudaStream_t st) {
+                            int32_t* status, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
       ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kSW * kSStages * kSPages * cb;
@@ -1153,13 +1182,17 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   // With few pairs each one spreads over many CTAs; its merge then runs as a
   // separate, wider kernel instead of in the last CTA.
   const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
+  // the in-kernel merge counts finished CTAs per pair on tickets that start at 0
+  if (!defer && (e = cudaMemsetAsync(tickets, 0, sizeof(int32_t) * (size_t)num_seqs * L.h_kv, st)) !=
+                    cudaSuccess)
+    return e;
   decode_stream_kernel<NG><<<grid, kST, smem, st>>>(
       L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
-      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer, u_total);
+      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (defer)
-    e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, u_total, grid, 1, out,
-                            out_lse, st);
+    e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, grid, 1, true, out, out_lse,
+                            st);
   return e;
 }
 
@@ -1167,17 +1200,17 @@ cudaError_t launch_decode_stream(const Layout& L, const void* paged, const void*
                                  const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                                  const int32_t* block_table, float sm_scale, float* part_o,
                                  float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                                 int32_t* status, long long* u_total, cudaStream_t st) {
+                                 int32_t* status, cudaStream_t st) {
   switch (L.d_h / L.g) {
     case 4:
       return launch_stream_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                                part_o, part_lse, tickets, out, out_lse, status, st);
     case 2:
       return launch_stream_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                                part_o, part_lse, tickets, out, out_lse, status, st);
     case 1:
       return launch_stream_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, u_total, st);
+                                part_o, part_lse, tickets, out, out_lse, status, st);
   }
   return cudaErrorInvalidValue;
 }
