@@ -509,7 +509,7 @@ def run_report(args):
                           "drift_vs_kv4": {"max_abs": float(drift.max()),
                                            "mean_abs": float(drift.mean())}}), flush=True)
 
-    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h", "c"}
+    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h", "c", "i8"}
     if "1" in sel:  # tiny: L2-resident, flushed
         w = W.WORKLOADS["tiny_b4_l512"]
         cache, s, lens, w = build_workload(w, dev)
@@ -561,6 +561,16 @@ def run_report(args):
         cache, s, lens, w8 = build_workload(w8, dev)
         decode_line("config 4 int8 everywhere", w8, cache, s, lens)
         del cache
+    if "i8" in sel:  # tensor-pipe rates behind the integer decode variant: int8 vs fp16 mma.sync
+        sink = torch.zeros(1, dtype=torch.int32, device=dev)
+        blocks = torch.cuda.get_device_properties(dev).multi_processor_count * 8
+        iters = 4096
+        for kind, name, ops in ((0, "fp16 m16n8k16 (fp32 accumulate)", 4096),
+                                (1, "int8 m16n8k32 (int32 accumulate)", 8192)):
+            t = _timed(lambda: kv4.kv4_diag_mma_rate(kind, blocks, iters, sink), warm=3, samples=10)
+            total = blocks * 8 * 4 * iters * ops
+            print(json.dumps({"report": "mma rate", "kind": name, "ms": t["median_ms"],
+                              "TOPS": total / (t["median_ms"] / 1e3) / 1e12}), flush=True)
     if "c" in sel:  # KV concentration: continuous refill vs synchronous waves, driven on the GPU
         from int8_kv_cache_kv4_gb300 import rollout as RO
         w = W.WORKLOADS["rollout_b256"]

@@ -221,6 +221,20 @@ int kv4_quant_append_hadamard(const kv4_layout* layout, void* paged, void* side,
 int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim, void* stream);
 
 /*
+ * kv4_diag_mma_rate -- diagnostic, not part of the method.  KV4-RL's deployed
+ * decode multiplies INT8 operands on the tensor cores (Sec. 5.3 and App. A.3
+ * "Integer decode path"); this library's decode multiplies fp16 ones.  The
+ * probe launches `blocks` CTAs of 8 warps, each warp issuing 4 x `iters`
+ * warp-level MMAs on register operands: kind 0 = m16n8k16 fp16 with fp32
+ * accumulation (4,096 flops each), kind 1 = m16n8k32 int8 with int32
+ * accumulation (8,192 ops each).  Time it with events on `stream` to get the
+ * rate.  `sink`: device, 4 bytes, written only to keep the results live.
+ * Returns KV4_ERR_INVALID_ARG for another kind, non-positive sizes or a NULL
+ * sink.
+ */
+int kv4_diag_mma_rate(int32_t kind, int32_t blocks, int32_t iters, uint32_t* sink, void* stream);
+
+/*
  * kv4_decode_attn -- split-KV GQA decode attention over the mixed cache
  * (KV4-RL Sec. 5.3 and App. A.3: disjoint INT4 and protected regions, each
  * split producing a locally normalised output and log-normaliser, merged by

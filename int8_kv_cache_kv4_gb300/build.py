@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libkv4.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["kv4_abi.cu", "kv4_append.cu", "kv4_decode.cu", "kv4_decode_mma.cu", "kv4_decode_tc.cu", "kv4_decode_stream.cu",
-           "kv4_decode_sm.cu", "kv4_noalloc.cu"]
+           "kv4_decode_sm.cu", "kv4_noalloc.cu", "kv4_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

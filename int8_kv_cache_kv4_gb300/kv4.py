@@ -101,6 +101,7 @@ def load(build_if_missing: bool = False):
         "kv4_quant_append": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_quant_append_hadamard": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_hadamard_bf16": (ctypes.c_int, [P, P, I, I, P]),
+        "kv4_diag_mma_rate": (ctypes.c_int, [I, I, I, P, P]),
         "kv4_decode_attn": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, Sz, P, P,
                                            P, P]),
         "kv4_split_combine": (ctypes.c_int, [P, P, I, I, I, P, P, P]),
@@ -206,6 +207,12 @@ def kv4_hadamard_bf16(x, y=None, stream=None):
     rc = load().kv4_hadamard_bf16(_ptr(x), _ptr(y), rows, d, _stream(stream))
     _check(rc, "kv4_hadamard_bf16")
     return y
+
+
+def kv4_diag_mma_rate(kind, blocks, iters, sink, stream=None):
+    """Launch the tensor-pipe rate probe (kind 0: fp16 MMA, 1: int8 MMA)."""
+    _check(load().kv4_diag_mma_rate(int(kind), int(blocks), int(iters), _ptr(sink), _stream(stream)),
+           "kv4_diag_mma_rate")
 
 
 def _quant_append(name, layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens,
