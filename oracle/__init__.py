@@ -21,6 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kv4_oracle.c")
+_SRC_FP4 = os.path.join(_HERE, "kv4_fp4_oracle.c")
 _LIB = os.path.join(_HERE, "libkv4_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -34,10 +35,11 @@ PAGE = 16
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no fast-math, no FMA contraction, dynamic
     rounding modes honoured).  Returns the library path."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_FP4))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".{os.getpid()}.tmp"
         cmd = ["gcc", "-std=c11", "-O1", "-frounding-math", "-fno-fast-math",
-               "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+               "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, _SRC_FP4, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -73,6 +75,22 @@ def _get():
             lib.kv4o_dequant_seq.argtypes = [I, I, I, I, I, I, P, P, P, P, I]
             lib.kv4o_hadamard_f32_n.argtypes = [P, Lg, I]
             lib.kv4o_hadamard_f32_n.restype = None
+            lib.fp4o_e2m1_round_n.argtypes = [P, Lg, P]
+            lib.fp4o_e2m1_round_n.restype = None
+            lib.fp4o_e4m3_round_n.argtypes = [P, Lg, P]
+            lib.fp4o_e4m3_round_n.restype = None
+            lib.fp4o_e2m1_value.argtypes = [I]
+            lib.fp4o_e2m1_value.restype = ctypes.c_float
+            lib.fp4o_e4m3_value.argtypes = [I]
+            lib.fp4o_e4m3_value.restype = ctypes.c_float
+            lib.fp4o_encode_n.argtypes = [I, P, Lg, I, P, P, P]
+            lib.fp4o_encode_n.restype = I
+            lib.fp4o_decode_n.argtypes = [I, P, P, P, Lg, I, P]
+            lib.fp4o_decode_n.restype = None
+            lib.fp4o_append.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, I, P, P]
+            lib.fp4o_append.restype = I
+            lib.fp4o_dequant_seq.argtypes = [I, I, I, I, I, P, P, P, P]
+            lib.fp4o_dequant_seq.restype = I
             lib.kv4o_dequant_seq.restype = I
             lib.kv4o_attend.argtypes = [I, I, I, I, P, P, P, D, P, P, P]
             lib.kv4o_attend.restype = None
@@ -281,3 +299,97 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32) << 16
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------------ FP4 probe formats
+# (kv4_fp4_oracle.c: NVFP4 and MXFP4 as KV4-RL App. D.4 compares them)
+
+NVFP4, MXFP4 = 1, 2
+
+
+def e2m1_round(y: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code (uint8, sign in bit 3) of every fp32 value."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    _get().fp4o_e2m1_round_n(_p(y), y.size, _p(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    return float(_get().fp4o_e2m1_value(int(code)))
+
+
+def e4m3_round(t: np.ndarray) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float32)
+    out = np.empty(t.shape, dtype=np.uint8)
+    _get().fp4o_e4m3_round_n(_p(t), t.size, _p(out))
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    return float(_get().fp4o_e4m3_value(int(code)))
+
+
+def fp4_encode(x: np.ndarray, fmt: int):
+    """Encode every row (last axis n) of x (fp32): codes uint8 [.., n] (one
+    E2M1 code per element), block scales uint8 [.., n/16 | n/32], global
+    scales fp32 [..] (NVFP4; zero for MXFP4), status."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n = x.shape[-1]
+    nv = x.size // n
+    nb = n // 16 if fmt == NVFP4 else n // 32
+    codes = np.empty(x.shape, dtype=np.uint8)
+    bs = np.empty(x.shape[:-1] + (nb,), dtype=np.uint8)
+    g = np.zeros(x.shape[:-1], dtype=np.float32)
+    st = _get().fp4o_encode_n(fmt, _p(x), nv, n, _p(codes), _p(bs), _p(g))
+    return codes, bs, g, st
+
+
+def fp4_decode(codes: np.ndarray, bs: np.ndarray, g: np.ndarray, fmt: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    bs = np.ascontiguousarray(bs, dtype=np.uint8)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    n = codes.shape[-1]
+    out = np.empty(codes.shape, dtype=np.float32)
+    _get().fp4o_decode_n(fmt, _p(codes), _p(bs), _p(g), codes.size // n, n, _p(out))
+    return out
+
+
+def fp4_row_bytes(d_h: int) -> int:
+    return d_h // 2 + 16
+
+
+def fp4_append(*, h_kv, d_h, fmt, rotate_k=False, max_seqs, num_pages, max_pages_per_seq,
+               cache: np.ndarray, k_new, v_new, tok_seq, tok_pos, seq_lens, block_table) -> int:
+    """Write T tokens into the packed FP4 probe cache bytes in place."""
+    T = int(len(tok_seq))
+    if T == 0:
+        return 0
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    tok_seq = np.ascontiguousarray(tok_seq, dtype=np.int32)
+    tok_pos = np.ascontiguousarray(tok_pos, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    return int(_get().fp4o_append(h_kv, d_h, fmt, 1 if rotate_k else 0, max_seqs, num_pages,
+                                  max_pages_per_seq, _p(cache), _p(k_new), _p(v_new),
+                                  _p(tok_seq), _p(tok_pos), T, _p(seq_lens), _p(block_table)))
+
+
+def fp4_dequant_seq(k_src: np.ndarray, v_src: np.ndarray, *, fmt: int, rotate_k: bool = False):
+    """The probe's bf16 attention operands of one sequence (fp64 [h_kv][L][d_h])."""
+    k_src = np.ascontiguousarray(k_src, dtype=np.uint16)
+    v_src = np.ascontiguousarray(v_src, dtype=np.uint16)
+    h_kv, L, d_h = k_src.shape
+    kh = np.empty((h_kv, L, d_h))
+    vh = np.empty((h_kv, L, d_h))
+    st = _get().fp4o_dequant_seq(h_kv, d_h, fmt, 1 if rotate_k else 0, L, _p(k_src), _p(v_src),
+                                 _p(kh), _p(vh))
+    return kh, vh, int(st)
+
+
+def fp4_decode_seq(q, k_src, v_src, *, fmt: int, sm_scale: float, rotate_k: bool = False):
+    """Probe attention of one sequence: FP4-reconstructed bf16 K/V, fp64 softmax."""
+    kh, vh, st = fp4_dequant_seq(k_src, v_src, fmt=fmt, rotate_k=rotate_k)
+    out, lse = attend(q, kh, vh, sm_scale)
+    return out, lse, st
