@@ -221,6 +221,52 @@ int kv4_quant_append_hadamard(const kv4_layout* layout, void* paged, void* side,
 int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim, void* stream);
 
 /*
+ * FP4 probe formats (KV4-RL App. D.4, Fig. A4(c)): the pages compare affine
+ * INT4 with NVFP4 (E2M1 values, one E4M3 scale per 16 elements and one FP32
+ * global scale per token-head vector, 4.75 bits per element) and MXFP4 (E2M1
+ * values, one E8M0 scale per 32 elements, 4.25 bits per element) as fidelity
+ * probes that reconstruct the stored cache and attend with bf16 operands; no
+ * FP4 attention kernel is part of the method.  These entry points write such a
+ * cache and reconstruct it into the bf16 comparator layout, so that
+ * kv4_bf16_decode_attn computes the probe's attention.
+ *
+ * Scale rules (one fp32 operation each, rounded to nearest even):
+ *   NVFP4  S = max|x| / 2688 over the token-head vector (2688 = 6 * 448);
+ *          per block of 16: s_b = E4M3(max|x_b| / (6 S)), e_b = value(s_b) * S,
+ *          q = E2M1(x / e_b), q = 0 when e_b = 0
+ *   MXFP4  per block of 32: E = floor(log2 max|x_b|) - 2 clamped to
+ *          [-127, 127] (-127 for an all-zero block), q = E2M1(x * 2^-E)
+ *   E2M1 rounds to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with ties to the
+ *   even code, saturates at 6 and keeps the sign; E4M3 rounds to nearest
+ *   even and saturates at 448.  A vector with a non-finite element is stored
+ *   as zeros and sets KV4_STATUS_NONFINITE.
+ *
+ * Probe cache = [num_pages][num_kv_heads][K, V][16 slots][row], row =
+ *   head_dim/2 + 16 bytes: the E2M1 codes (byte i: channel 2i in the low
+ *   nibble, 2i+1 in the high nibble), then the block scales one byte each
+ *   (NVFP4 head_dim/16 E4M3, MXFP4 head_dim/32 E8M0), and for NVFP4 the fp32
+ *   S (little-endian) at byte head_dim/2 + 12; other bytes are never written.
+ *   Size: kv4_fp4_cache_bytes(layout).
+ *
+ * kv4_fp4_append -- kv4_quant_append's arguments and validation, writing one
+ *   probe row per token, kv head and K/V; rotate_k != 0 rotates K first as
+ *   kv4_quant_append_hadamard does (V never).  format: KV4_FP4_NVFP4 or
+ *   KV4_FP4_MXFP4, else KV4_ERR_INVALID_ARG.
+ * kv4_fp4_to_bf16 -- every row of the pool reconstructed (q times its scale,
+ *   rounded to bf16 nearest even) into bf16_cache, a device buffer of
+ *   kv4_bf16_cache_bytes(layout) in the comparator layout.
+ */
+#define KV4_FP4_NVFP4 1
+#define KV4_FP4_MXFP4 2
+size_t kv4_fp4_cache_bytes(const kv4_layout* layout);
+int kv4_fp4_append(const kv4_layout* layout, int32_t format, int32_t rotate_k, void* cache,
+                   const uint16_t* k_new, const uint16_t* v_new, const int32_t* tok_seq,
+                   const int32_t* tok_pos, int32_t T, const int32_t* seq_lens,
+                   const int32_t* block_table, int32_t* dev_status, void* stream);
+int kv4_fp4_to_bf16(const kv4_layout* layout, int32_t format, const void* cache, void* bf16_cache,
+                    void* stream);
+
+/*
  * kv4_diag_mma_rate -- diagnostic, not part of the method.  KV4-RL's deployed
  * decode multiplies INT8 operands on the tensor cores (Sec. 5.3 and App. A.3
  * "Integer decode path"); this library's decode multiplies fp16 ones.  The

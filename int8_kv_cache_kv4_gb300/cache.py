@@ -95,8 +95,57 @@ class MixedKVCache:
         self.status.zero_()
 
 
+class FP4ProbeCache:
+    """FP4 probe cache of one layer (KV4-RL App. D.4: NVFP4 or MXFP4 K/V,
+    reconstructed and attended with bf16 operands).  `append` writes the
+    packed format; `decode` reconstructs the pool into a bf16 comparator cache
+    and runs the bf16 decode over it, rotating the query when K is rotated.
+    Same call shapes as MixedKVCache.  No compute happens here."""
+
+    def __init__(self, *, fmt, h_q=32, h_kv=8, d_h=128, max_seqs, num_pages, max_pages_per_seq,
+                 device="cuda", hadamard_k=False):
+        import torch
+        self.fmt = int(fmt)
+        self.layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=32, sink=0, recent=0,
+                                      max_seqs=max_seqs, num_pages=num_pages,
+                                      max_pages_per_seq=max_pages_per_seq)
+        self.device = torch.device(device)
+        self.cache = torch.zeros(kv4.fp4_cache_bytes(self.layout), dtype=torch.uint8,
+                                 device=self.device)
+        self.bf16 = torch.zeros(kv4.bf16_cache_bytes(self.layout), dtype=torch.uint8,
+                                device=self.device)
+        self.block_table = torch.full((max_seqs, max_pages_per_seq), -1, dtype=torch.int32,
+                                      device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.hadamard_k = bool(hadamard_k)
+        self._ws = {}
+        self._qrot = {}
+
+    sm_scale = MixedKVCache.sm_scale
+    set_block_table = MixedKVCache.set_block_table
+    workspace = MixedKVCache.workspace
+    rotated_query = MixedKVCache.rotated_query
+    read_status = MixedKVCache.read_status
+    clear_status = MixedKVCache.clear_status
+
+    def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
+        kv4.kv4_fp4_append(self.layout, self.fmt, self.cache, k_new, v_new, tok_seq, tok_pos,
+                           seq_lens, self.block_table, self.hadamard_k, self.status, stream)
+
+    def reconstruct(self, stream=None):
+        kv4.kv4_fp4_to_bf16(self.layout, self.fmt, self.cache, self.bf16, stream)
+
+    def decode(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
+        self.reconstruct(stream)
+        if self.hadamard_k:
+            q = self.rotated_query(q, stream)
+        ws = self.workspace(int(q.shape[0]), max_splits)
+        kv4.kv4_bf16_decode_attn(self.layout, self.bf16, q, seq_lens, self.block_table, ws, out,
+                                 out_lse, self.sm_scale, max_splits, self.status, stream)
+
+
 def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, seed=None,
-                   extra_tokens=0, hadamard_k=False):
+                   extra_tokens=0, hadamard_k=False, fp4=None):
     """Populate a cache with a seeded synthetic workload (see workloads.py):
     positions [0, L-1) of every sequence by bulk appends, then return the
     decode step's inputs (the new token at position L-1 and the query).
@@ -104,7 +153,8 @@ def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, 
     step token and query from seed*1000003+999983, so any sequence can be
     regenerated for a parity check.  `extra_tokens` reserves block-table room
     for that many later appends per sequence.  hadamard_k: the cache stores
-    rotated K (MixedKVCache(hadamard_k=True))."""
+    rotated K (MixedKVCache(hadamard_k=True)).  fp4: KV4_FP4_NVFP4 or
+    KV4_FP4_MXFP4 builds an FP4ProbeCache of that format instead."""
     import torch
     import dataclasses
     if group is not None or recent is not None or seed is not None:
@@ -116,10 +166,15 @@ def build_workload(w, dev, with_bf16=False, lens=None, group=None, recent=None, 
     cap = lens + int(extra_tokens)
     mpps = (int(cap.max()) + 15) // 16
     num_pages = W.pool_pages(cap, w.extra_pages)
-    cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
-                         recent=w.recent, max_seqs=B, num_pages=num_pages,
-                         max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16,
-                         hadamard_k=hadamard_k)
+    if fp4:
+        cache = FP4ProbeCache(fmt=fp4, h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, max_seqs=B,
+                              num_pages=num_pages, max_pages_per_seq=mpps, device=dev,
+                              hadamard_k=hadamard_k)
+    else:
+        cache = MixedKVCache(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
+                             recent=w.recent, max_seqs=B, num_pages=num_pages,
+                             max_pages_per_seq=mpps, device=dev, with_bf16=with_bf16,
+                             hadamard_k=hadamard_k)
     cache.set_block_table(W.block_table(w.seed, cap, mpps, num_pages))
     outl = W.outlier_channels(w.seed, w.h_kv, w.d_h)
     # populate positions [0, L-1) of every sequence (prefill-style bulk append)

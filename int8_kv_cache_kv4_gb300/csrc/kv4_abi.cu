@@ -10,6 +10,10 @@ cudaError_t launch_quant_append(const Layout&, void*, void*, const uint16_t*, co
                                 const int32_t*, const int32_t*, int, const int32_t*,
                                 const int32_t*, int32_t*, bool, cudaStream_t);
 cudaError_t launch_hadamard_bf16(const uint16_t*, uint16_t*, long long, int, cudaStream_t);
+cudaError_t launch_fp4_append(const Layout&, int, bool, void*, const uint16_t*, const uint16_t*,
+                              const int32_t*, const int32_t*, int, const int32_t*, const int32_t*,
+                              int32_t*, cudaStream_t);
+cudaError_t launch_fp4_to_bf16(const Layout&, int, const void*, void*, cudaStream_t);
 cudaError_t launch_bf16_append(const Layout&, void*, const uint16_t*, const uint16_t*,
                                const int32_t*, const int32_t*, int, const int32_t*, const int32_t*,
                                int32_t*, cudaStream_t);
@@ -249,6 +253,39 @@ int kv4_quant_append_hadamard(const kv4_layout* l, void* paged, void* side,
                               int32_t* dev_status, void* stream) {
   return quant_append(l, paged, side, k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table,
                       dev_status, true, stream);
+}
+
+size_t kv4_fp4_cache_bytes(const kv4_layout* l) {
+  if (kv4_check_layout(l) != KV4_OK) return 0;
+  return (size_t)l->num_pages * l->num_kv_heads * 2 * 16 * (size_t)(l->head_dim / 2 + 16);
+}
+
+int kv4_fp4_append(const kv4_layout* l, int32_t format, int32_t rotate_k, void* cache,
+                   const uint16_t* k_new, const uint16_t* v_new, const int32_t* tok_seq,
+                   const int32_t* tok_pos, int32_t T, const int32_t* seq_lens,
+                   const int32_t* block_table, int32_t* dev_status, void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (format != KV4_FP4_NVFP4 && format != KV4_FP4_MXFP4) return KV4_ERR_INVALID_ARG;
+  if (T < 0) return KV4_ERR_INVALID_ARG;
+  if (T == 0) return KV4_OK;
+  if (!cache || !k_new || !v_new || !tok_seq || !tok_pos || !seq_lens || !block_table)
+    return KV4_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(k_new) || !aligned16(v_new)) return KV4_ERR_INVALID_ARG;
+  cudaError_t e = launch_fp4_append(to_layout(l), format, rotate_k != 0, cache, k_new, v_new,
+                                    tok_seq, tok_pos, T, seq_lens, block_table, dev_status,
+                                    (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+int kv4_fp4_to_bf16(const kv4_layout* l, int32_t format, const void* cache, void* bf16_cache,
+                    void* stream) {
+  int rc = kv4_check_layout(l);
+  if (rc != KV4_OK) return rc;
+  if (format != KV4_FP4_NVFP4 && format != KV4_FP4_MXFP4) return KV4_ERR_INVALID_ARG;
+  if (!cache || !bf16_cache || !aligned16(cache) || !aligned16(bf16_cache)) return KV4_ERR_INVALID_ARG;
+  cudaError_t e = launch_fp4_to_bf16(to_layout(l), format, cache, bf16_cache, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 
 int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim, void* stream) {

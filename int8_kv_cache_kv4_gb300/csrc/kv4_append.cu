@@ -331,4 +331,189 @@ cudaError_t launch_bf16_append(const Layout& L, void* cache, const uint16_t* k_n
   return cudaGetLastError();
 }
 
+// ------------------------------------------------- FP4 probe formats
+// KV4-RL App. D.4 (Fig. A4(c)) compares affine INT4 with two FP4 formats as
+// fidelity probes that reconstruct the stored cache and attend with bf16
+// operands: NVFP4 (E2M1 values, one E4M3 scale per 16 elements, one fp32
+// global scale per token-head vector) and MXFP4 (E2M1 values, one E8M0 scale
+// per 32 elements).  Scale rules (the pages name the formats only):
+//   NVFP4  S = a / 2688 (a = max|x| of the vector, 2688 = 6 * 448);
+//          s_b = E4M3(amax_b / (6 S)) per block of 16; e_b = E4M3value(s_b) * S;
+//          q = E2M1(x / e_b)                      (q = 0 when e_b = 0)
+//   MXFP4  E = floor(log2 amax_b) - 2 per block of 32, clamped to [-127, 127]
+//          (-127 for an all-zero block); q = E2M1(x * 2^-E)
+// each step one fp32 operation rounded to nearest even; E2M1 rounds to the
+// nearest of 0, .5, 1, 1.5, 2, 3, 4, 6 with ties to the even code, saturating
+// at 6 and keeping the sign; E4M3 rounds to nearest even, saturating at 448.
+// Probe cache: [page][h_kv][K, V][16 slots][row], row = d/2 + 16 bytes: the
+// codes (byte i = channel 2i low nibble, 2i+1 high), then the block scales,
+// and for NVFP4 the fp32 S at byte d/2 + 12.
+
+constexpr int kFp4Nv = 1, kFp4Mx = 2;
+__host__ __device__ inline int fp4_row_bytes(int d_h) { return d_h / 2 + 16; }
+
+// E2M1 code of y: nearest magnitude, ties to the even code (strict '>' at the
+// midpoints that round down, '>=' where they round up), saturating at 6.
+__device__ inline uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return c | (signbit(y) ? 8u : 0u);
+}
+__device__ inline float e2m1_value(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float v = e == 0 ? 0.5f * (float)m : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -v : v;
+}
+// E4M3 code of t >= 0 (nearest even, saturating at 448), and its value
+__device__ inline uint32_t e4m3_code(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+__device__ inline float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  const float v = e == 0 ? (float)m * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (c & 0x80u) ? -v : v;
+}
+// 2^k as an fp32 for k in [-127, 127] (2^-127 is subnormal)
+__device__ inline float pow2f(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+// floor(log2 a) of a finite a > 0
+__device__ inline int ilog2f(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int ex = (int)(u >> 23);
+  return ex ? ex - 127 : (31 - __clz((int)(u & 0x7FFFFFu))) - 149;
+}
+
+template <int kFmt, bool kRotateK>
+__global__ void __launch_bounds__(256) fp4_append_kernel(
+    Layout L, uint8_t* __restrict__ cache, const uint16_t* __restrict__ k_new,
+    const uint16_t* __restrict__ v_new, const int32_t* __restrict__ tok_seq,
+    const int32_t* __restrict__ tok_pos, int T, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ block_table, int32_t* status, float hc) {
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)T * L.h_kv) return;
+  const int t = (int)(w / L.h_kv);
+  const int h = (int)(w % L.h_kv);
+  const int s = tok_seq[t], p = tok_pos[t];
+  int len = 0;
+  const int page = token_page(L, s, p, seq_lens, block_table, status, lane == 0 && h == 0, &len);
+  if (page < 0) return;
+  const int d_h = L.d_h, lanes = d_h / 4, rb = fp4_row_bytes(d_h);
+  const bool active = lane < lanes;
+  const int c0 = (active ? lane : 0) * 4;
+  int bad = 0;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint16_t* src = (kv == 0 ? k_new : v_new) + ((long long)t * L.h_kv + h) * d_h + c0;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+    if (!active) x[0] = x[1] = x[2] = x[3] = 0.f;
+    if (kRotateK && kv == 0) hadamard_warp(x, d_h, hc);
+    const int nf = group_or(!(isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3])), 32);
+    float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    uint32_t codes = 0, bsc = 0;
+    float S = 0.f;
+    if (!nf) {
+      float scale;  // the divisor (NVFP4) or multiplier (MXFP4) of x
+      bool zero;
+      if (kFmt == kFp4Nv) {
+        S = __fdiv_rn(group_max(am, 32), 2688.0f);
+        const float six_s = __fmul_rn(6.0f, S);
+        const float ab = group_max(am, 4);  // block of 16 channels = 4 lanes
+        bsc = six_s > 0.f ? e4m3_code(__fdiv_rn(ab, six_s)) : 0u;
+        scale = __fmul_rn(e4m3_value(bsc), S);
+        zero = scale == 0.f;
+      } else {
+        const float ab = group_max(am, 8);  // block of 32 channels = 8 lanes
+        const int E = ab > 0.f ? max(-127, min(127, ilog2f(ab) - 2)) : -127;
+        bsc = (uint32_t)(E + 127);
+        scale = pow2f(-E);
+        zero = false;
+      }
+      if (!zero) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float y = kFmt == kFp4Nv ? __fdiv_rn(x[i], scale) : __fmul_rn(x[i], scale);
+          codes |= e2m1_code(y) << (4 * i);
+        }
+      }
+    }
+    bad |= nf;
+    if (active) {
+      uint8_t* row = cache + ((((long long)page * L.h_kv + h) * 2 + kv) * 16 + p % 16) * rb;
+      *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)codes;
+      if (kFmt == kFp4Nv) {
+        if ((lane & 3) == 0) row[d_h / 2 + lane / 4] = (uint8_t)bsc;
+        if (lane == 0) *reinterpret_cast<float*>(row + d_h / 2 + 12) = S;
+      } else if ((lane & 7) == 0) {
+        row[d_h / 2 + lane / 8] = (uint8_t)bsc;
+      }
+    }
+  }
+  if (bad && lane == 0) set_status(status, KV4_STATUS_NONFINITE);
+}
+
+// Reconstruction into the bf16 comparator cache ([page][h_kv][K, V][16][d]):
+// one warp per row, lane l producing channels 4l .. 4l + 3.
+template <int kFmt>
+__global__ void __launch_bounds__(256) fp4_to_bf16_kernel(Layout L, const uint8_t* __restrict__ cache,
+                                                          uint16_t* __restrict__ out, long long rows) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int d_h = L.d_h;
+  if (r >= rows || 4 * lane >= d_h) return;
+  const uint8_t* row = cache + r * fp4_row_bytes(d_h);
+  const uint32_t codes = *reinterpret_cast<const uint16_t*>(row + 2 * lane);
+  float scale;
+  if (kFmt == kFp4Nv) {
+    const float S = *reinterpret_cast<const float*>(row + d_h / 2 + 12);
+    scale = __fmul_rn(e4m3_value(row[d_h / 2 + lane / 4]), S);
+  } else {
+    scale = pow2f((int)row[d_h / 2 + lane / 8] - 127);
+  }
+  uint32_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = f32_to_bf16_bits(__fmul_rn(e2m1_value((codes >> (4 * i)) & 15u), scale));
+  *reinterpret_cast<uint2*>(out + r * d_h + 4 * lane) = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+cudaError_t launch_fp4_append(const Layout& L, int fmt, bool rotate_k, void* cache,
+                              const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* tok_seq, const int32_t* tok_pos, int T,
+                              const int32_t* seq_lens, const int32_t* block_table, int32_t* status,
+                              cudaStream_t st) {
+  const long long warps = (long long)T * L.h_kv;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  const float hc = hadamard_scale(L.d_h);
+  uint8_t* c = (uint8_t*)cache;
+#define KV4_FP4_LAUNCH(F, R)                                                                   \
+  fp4_append_kernel<F, R><<<blocks, 256, 0, st>>>(L, c, k_new, v_new, tok_seq, tok_pos, T, seq_lens, \
+                                                  block_table, status, hc)
+  if (fmt == kFp4Nv) {
+    if (rotate_k) KV4_FP4_LAUNCH(kFp4Nv, true);
+    else KV4_FP4_LAUNCH(kFp4Nv, false);
+  } else {
+    if (rotate_k) KV4_FP4_LAUNCH(kFp4Mx, true);
+    else KV4_FP4_LAUNCH(kFp4Mx, false);
+  }
+#undef KV4_FP4_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp4_to_bf16(const Layout& L, int fmt, const void* cache, void* out,
+                               cudaStream_t st) {
+  const long long rows = (long long)L.num_pages * L.h_kv * 2 * 16;
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  if (fmt == kFp4Nv)
+    fp4_to_bf16_kernel<kFp4Nv><<<blocks, 256, 0, st>>>(L, (const uint8_t*)cache, (uint16_t*)out, rows);
+  else
+    fp4_to_bf16_kernel<kFp4Mx><<<blocks, 256, 0, st>>>(L, (const uint8_t*)cache, (uint16_t*)out, rows);
+  return cudaGetLastError();
+}
+
 }  // namespace kv4

@@ -102,6 +102,9 @@ def load(build_if_missing: bool = False):
         "kv4_quant_append_hadamard": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_hadamard_bf16": (ctypes.c_int, [P, P, I, I, P]),
         "kv4_diag_mma_rate": (ctypes.c_int, [I, I, I, P, P]),
+        "kv4_fp4_cache_bytes": (Sz, [LP]),
+        "kv4_fp4_append": (ctypes.c_int, [LP, I, I, P, P, P, P, P, I, P, P, P, P]),
+        "kv4_fp4_to_bf16": (ctypes.c_int, [LP, I, P, P, P]),
         "kv4_decode_attn": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, Sz, P, P,
                                            P, P]),
         "kv4_split_combine": (ctypes.c_int, [P, P, I, I, I, P, P, P]),
@@ -213,6 +216,41 @@ def kv4_diag_mma_rate(kind, blocks, iters, sink, stream=None):
     """Launch the tensor-pipe rate probe (kind 0: fp16 MMA, 1: int8 MMA)."""
     _check(load().kv4_diag_mma_rate(int(kind), int(blocks), int(iters), _ptr(sink), _stream(stream)),
            "kv4_diag_mma_rate")
+
+
+KV4_FP4_NVFP4, KV4_FP4_MXFP4 = 1, 2
+
+
+def fp4_cache_bytes(layout: kv4_layout) -> int:
+    return int(load().kv4_fp4_cache_bytes(ctypes.byref(layout)))
+
+
+def kv4_fp4_append(layout, fmt, cache, k_new, v_new, tok_seq, tok_pos, seq_lens, block_table,
+                   rotate_k=False, status=None, stream=None):
+    """FP4 probe append (NVFP4 or MXFP4) of T tokens, k_new/v_new bf16 [T][h_kv][d_h]."""
+    import torch
+    _dev(cache, torch.uint8, "cache")
+    for n, t in (("k_new", k_new), ("v_new", v_new)):
+        _dev(t, torch.bfloat16, n)
+    for n, t in (("tok_seq", tok_seq), ("tok_pos", tok_pos), ("seq_lens", seq_lens),
+                 ("block_table", block_table), ("status", status)):
+        _dev(t, torch.int32, n)
+    T = int(tok_seq.numel())
+    if tok_pos.numel() != T or k_new.numel() != T * layout.num_kv_heads * layout.head_dim:
+        raise KV4Error("kv4_fp4_append: token arrays disagree in length")
+    _check(load().kv4_fp4_append(ctypes.byref(layout), int(fmt), 1 if rotate_k else 0, _ptr(cache),
+                                 _ptr(k_new), _ptr(v_new), _ptr(tok_seq), _ptr(tok_pos), T,
+                                 _ptr(seq_lens), _ptr(block_table), _ptr(status), _stream(stream)),
+           "kv4_fp4_append")
+
+
+def kv4_fp4_to_bf16(layout, fmt, cache, bf16_cache, stream=None):
+    """Reconstruct the whole FP4 probe pool into the bf16 comparator layout."""
+    import torch
+    _dev(cache, torch.uint8, "cache")
+    _dev(bf16_cache, torch.uint8, "bf16_cache")
+    _check(load().kv4_fp4_to_bf16(ctypes.byref(layout), int(fmt), _ptr(cache), _ptr(bf16_cache),
+                                  _stream(stream)), "kv4_fp4_to_bf16")
 
 
 def _quant_append(name, layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens,
