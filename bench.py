@@ -509,7 +509,7 @@ def run_report(args):
                           "drift_vs_kv4": {"max_abs": float(drift.max()),
                                            "mean_abs": float(drift.mean())}}), flush=True)
 
-    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h", "c", "i8"}
+    sel = set(args.report.split(",")) if args.report != "all" else {"1", "2", "3", "4", "5", "h", "c", "i8", "f4"}
     if "1" in sel:  # tiny: L2-resident, flushed
         w = W.WORKLOADS["tiny_b4_l512"]
         cache, s, lens, w = build_workload(w, dev)
@@ -561,6 +561,33 @@ def run_report(args):
         cache, s, lens, w8 = build_workload(w8, dev)
         decode_line("config 4 int8 everywhere", w8, cache, s, lens)
         del cache
+    if "f4" in sel:  # representation drift against bf16 attention: affine INT4 vs NVFP4 / MXFP4
+        w = W.WORKLOADS["qwen3_8b_b64"]
+        ref_cache, s, lens, w = build_workload(w, dev, with_bf16=True)
+        ref = torch.empty_like(s["out"])
+        ref_cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+        ref_cache.decode_bf16(s["q"], s["lens"], ref, None)
+        torch.cuda.synchronize()
+        del ref_cache
+        variants = [("affine INT4 g32 + INT8 S4 R128 (deployed)", dict()),
+                    ("affine INT4 g128, no protection", dict(group=128, recent=0)),
+                    ("affine INT4 g128, no protection, K rotated", dict(group=128, recent=0, hadamard_k=True)),
+                    ("NVFP4", dict(fp4=kv4.KV4_FP4_NVFP4)),
+                    ("NVFP4, K rotated", dict(fp4=kv4.KV4_FP4_NVFP4, hadamard_k=True)),
+                    ("MXFP4", dict(fp4=kv4.KV4_FP4_MXFP4)),
+                    ("MXFP4, K rotated", dict(fp4=kv4.KV4_FP4_MXFP4, hadamard_k=True))]
+        for name, kw in variants:
+            wv = w if "group" not in kw else dataclasses.replace(w, sink=0 if kw.get("recent") == 0 else w.sink)
+            cache, s2, lens2, _ = build_workload(wv, dev, **kw)
+            cache.append(s2["k"], s2["v"], s2["seq"], s2["pos"], s2["lens"])
+            cache.decode(s2["q"], s2["lens"], s2["out"], s2["lse"])
+            torch.cuda.synchronize()
+            d = (s2["out"].float() - ref.float()).abs()
+            print(json.dumps({"report": "representation drift vs bf16 attention", "workload": w.name,
+                              "representation": name, "max_abs": float(d.max()),
+                              "mean_abs": float(d.mean()), "status": cache.read_status()}), flush=True)
+            del cache
+            torch.cuda.empty_cache()
     if "i8" in sel:  # tensor-pipe rates behind the integer decode variant: int8 vs fp16 mma.sync
         sink = torch.zeros(1, dtype=torch.int32, device=dev)
         blocks = torch.cuda.get_device_properties(dev).multi_processor_count * 8
