@@ -43,7 +43,8 @@ UNIT = "tokens/s"
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("77ef04e0d9a7af6a", "qwen3_8b_b64"): 388411648 + 4569088}
+TRAFFIC = {("85f2d33b8d498662", "qwen3_8b_b64"): 388407040 + 4196096,
+           ("85f2d33b8d498662", "long_128k"): 168132352 + 2948352}
 
 
 # ------------------------------------------------------------------ helpers
