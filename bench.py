@@ -139,7 +139,7 @@ class ClockSampler:
 
 def reduce_max_ms(total_ms: float, world: int, device) -> float:
     """The slowest rank's timed-region length: every rank contributes its own
-    CUDA-event time and all receive the maximum (NCCL on the GPU machine, gloo in
+    CUDA-event time and all receive the maximum (NCCL on GPUs, gloo in
     the CPU tests).  A barrier precedes and follows the timed region."""
     import torch
     import torch.distributed as dist
