@@ -111,3 +111,21 @@ def test_hadamard_entry_points_validate_on_host(lib):
     assert rc == kv4.KV4_ERR_INVALID_ARG
     assert lib.kv4_quant_append_hadamard(ctypes.byref(lay), None, None, None, None, None, None,
                                          0, None, None, None, None) == kv4.KV4_OK
+
+
+def test_fp4_and_diag_entry_points_validate_on_host(lib):
+    lay = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+    # probe cache: 10 pages x 8 kv heads x (K, V) x 16 slots x (64 + 16) bytes
+    assert kv4.fp4_cache_bytes(lay) == 10 * 8 * 2 * 16 * 80
+    bad = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
+    bad.head_dim = 96
+    assert kv4.fp4_cache_bytes(bad) == 0
+    args = (None, None, None, None, None, 3, None, None, None, None)
+    assert lib.kv4_fp4_append(ctypes.byref(lay), 3, 0, *args) == kv4.KV4_ERR_INVALID_ARG  # format
+    assert lib.kv4_fp4_append(ctypes.byref(lay), 1, 0, *args) == kv4.KV4_ERR_INVALID_ARG  # NULLs
+    assert lib.kv4_fp4_append(ctypes.byref(lay), 2, 1, None, None, None, None, None, 0, None,
+                              None, None, None) == kv4.KV4_OK                             # T == 0
+    assert lib.kv4_fp4_to_bf16(ctypes.byref(lay), 0, None, None, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_fp4_to_bf16(ctypes.byref(lay), 1, None, None, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_diag_mma_rate(2, 1, 1, None, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_diag_mma_rate(0, 0, 1, None, None) == kv4.KV4_ERR_INVALID_ARG
