@@ -168,3 +168,38 @@ def test_host_argument_errors_enqueue_nothing():
     with pytest.raises(kv4.KV4Error, match="workspace"):
         kv4.kv4_decode_attn(gc.layout, gc.paged, gc.side, q, torch.ones(1, dtype=torch.int32,
                             device="cuda"), gc.block_table, small_ws, out)
+
+
+def test_sequence_filling_its_block_table_row():
+    # L = max_pages_per_seq * 16: the last page is full and the row has no spare entry
+    c = Case([256, 240, 17], S=4, R=32, g=32, seed=12, h_q=8, h_kv=2)
+    assert c.mpps * 16 == 256
+    gc = c.gpu()
+    out, lse = c.gpu_decode(gc)
+    assert gc.read_status() == 0
+    ref, rlse = c.oracle_decode()
+    compare_outputs(out, lse, ref, rlse, range(c.B), c.lens)
+
+
+def test_lengths_outside_the_block_table_are_reported_and_read_as_empty():
+    # a length past the row's capacity or negative: the kernels' own checks
+    # report KV4_STATUS_BAD_LEN and treat the sequence as empty; the others
+    # are unaffected
+    c = Case([100, 60, 33], S=4, R=16, g=32, seed=13, h_q=8, h_kv=2)
+    gc = c.gpu()
+    gc.clear_status()
+    lens = c.lens.copy()
+    lens[1] = c.mpps * 16 + 1
+    lens[2] = -5
+    dev = torch.device("cuda")
+    q = torch.from_numpy(c.q.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((c.B, c.h_q, c.d_h), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((c.B, c.h_q), dtype=torch.float32, device=dev)
+    gc.decode(q, torch.from_numpy(lens).to(dev), out, lse)
+    torch.cuda.synchronize()
+    assert gc.read_status() & kv4.KV4_STATUS_BAD_LEN
+    o = out.float().cpu().numpy().astype(np.float64)
+    z = lse.cpu().numpy().astype(np.float64)
+    assert np.all(o[1:] == 0) and np.all(np.isneginf(z[1:]))
+    ref, rlse = c.oracle_decode([0])
+    compare_outputs(o, z, ref, rlse, [0], c.lens)
