@@ -220,6 +220,11 @@ def run_kv4(args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # Keep the GPU busy while the host enqueues the timed steps, so that the
+    # events bracket back-to-back device work rather than host submission
+    # latency (on a loaded host a step's launch can arrive after the previous
+    # step has finished).  The sleep precedes t0 and is not timed.
+    torch.cuda._sleep(int(2.1e6 * max(5.0, 0.2 * args.steps)))
     t0.record(stream)
     for i in range(args.steps):
         starts[i].record(stream)
