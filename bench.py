@@ -428,6 +428,7 @@ def _timed(fn, warm=10, samples=90, flush=None):
         if flush is not None:
             flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(210000)  # ~0.1 ms of untimed GPU work while the host enqueues e0, fn, e1
         e0.record()
         fn()
         e1.record()
