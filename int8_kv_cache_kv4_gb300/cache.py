@@ -15,32 +15,23 @@ from . import kv4
 from . import workloads as W
 
 
-class MixedKVCache:
-    """hadamard_k=True stores K rotated by the normalized Hadamard matrix
-    (kv4_quant_append_hadamard) and rotates each query the same way
-    (kv4_hadamard_bf16) before decode; callers pass unrotated K and q."""
+class _LayerCache:
+    """What both cache kinds share: the layout, block table, status word,
+    per-shape workspaces and the rotated-query scratch."""
 
-    def __init__(self, *, h_q=32, h_kv=8, d_h=128, group=32, sink=4, recent=128, max_seqs,
-                 num_pages, max_pages_per_seq, device="cuda", with_bf16=False, hadamard_k=False):
+    def _init_common(self, layout, max_seqs, max_pages_per_seq, device, hadamard_k):
         import torch
-        self.layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=group, sink=sink,
-                                      recent=recent, max_seqs=max_seqs, num_pages=num_pages,
-                                      max_pages_per_seq=max_pages_per_seq)
-        rc = kv4.load().kv4_check_layout(__import__("ctypes").byref(self.layout))
+        import ctypes
+        rc = kv4.load().kv4_check_layout(ctypes.byref(layout))
         if rc != kv4.KV4_OK:
             raise kv4.KV4Error(f"bad layout: {kv4.load().kv4_status_string(rc).decode()}")
+        self.layout = layout
         self.device = torch.device(device)
-        self.paged = torch.zeros(kv4.paged_cache_bytes(self.layout), dtype=torch.uint8,
-                                 device=self.device)
-        self.side = torch.zeros(max(16, kv4.side_cache_bytes(self.layout)), dtype=torch.uint8,
-                                device=self.device)
-        self.bf16 = (torch.zeros(kv4.bf16_cache_bytes(self.layout), dtype=torch.uint8,
-                                 device=self.device) if with_bf16 else None)
         self.block_table = torch.full((max_seqs, max_pages_per_seq), -1, dtype=torch.int32,
                                       device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self._ws = {}
         self.hadamard_k = bool(hadamard_k)
+        self._ws = {}
         self._qrot = {}
 
     @property
@@ -60,14 +51,6 @@ class MixedKVCache:
             self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws[key]
 
-    def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
-        fn = kv4.kv4_quant_append_hadamard if self.hadamard_k else kv4.kv4_quant_append
-        fn(self.layout, self.paged, self.side, k_new, v_new, tok_seq, tok_pos, seq_lens,
-           self.block_table, self.status, stream)
-        if self.bf16 is not None:
-            kv4.kv4_bf16_append(self.layout, self.bf16, k_new, v_new, tok_seq, tok_pos, seq_lens,
-                                self.block_table, self.status, stream)
-
     def rotated_query(self, q, stream=None):
         """q rotated like the stored keys (a scratch tensor reused per shape)."""
         import torch
@@ -75,6 +58,41 @@ class MixedKVCache:
         if key not in self._qrot:
             self._qrot[key] = torch.empty_like(q)
         return kv4.kv4_hadamard_bf16(q, self._qrot[key], stream)
+
+    def read_status(self) -> int:
+        return int(self.status.item())
+
+    def clear_status(self):
+        self.status.zero_()
+
+
+class MixedKVCache(_LayerCache):
+    """The mixed INT4/INT8 cache.  hadamard_k=True stores K rotated by the
+    normalized Hadamard matrix (kv4_quant_append_hadamard) and rotates each
+    query the same way (kv4_hadamard_bf16) before decode; callers pass
+    unrotated K and q.  with_bf16 keeps an unquantized comparator copy."""
+
+    def __init__(self, *, h_q=32, h_kv=8, d_h=128, group=32, sink=4, recent=128, max_seqs,
+                 num_pages, max_pages_per_seq, device="cuda", with_bf16=False, hadamard_k=False):
+        import torch
+        layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=group, sink=sink,
+                                 recent=recent, max_seqs=max_seqs, num_pages=num_pages,
+                                 max_pages_per_seq=max_pages_per_seq)
+        self._init_common(layout, max_seqs, max_pages_per_seq, device, hadamard_k)
+        self.paged = torch.zeros(kv4.paged_cache_bytes(self.layout), dtype=torch.uint8,
+                                 device=self.device)
+        self.side = torch.zeros(max(16, kv4.side_cache_bytes(self.layout)), dtype=torch.uint8,
+                                device=self.device)
+        self.bf16 = (torch.zeros(kv4.bf16_cache_bytes(self.layout), dtype=torch.uint8,
+                                 device=self.device) if with_bf16 else None)
+
+    def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
+        fn = kv4.kv4_quant_append_hadamard if self.hadamard_k else kv4.kv4_quant_append
+        fn(self.layout, self.paged, self.side, k_new, v_new, tok_seq, tok_pos, seq_lens,
+           self.block_table, self.status, stream)
+        if self.bf16 is not None:
+            kv4.kv4_bf16_append(self.layout, self.bf16, k_new, v_new, tok_seq, tok_pos, seq_lens,
+                                self.block_table, self.status, stream)
 
     def decode(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
         ws = self.workspace(int(q.shape[0]), max_splits)
@@ -88,14 +106,8 @@ class MixedKVCache:
         kv4.kv4_bf16_decode_attn(self.layout, self.bf16, q, seq_lens, self.block_table, ws, out,
                                  out_lse, self.sm_scale, max_splits, self.status, stream)
 
-    def read_status(self) -> int:
-        return int(self.status.item())
 
-    def clear_status(self):
-        self.status.zero_()
-
-
-class FP4ProbeCache:
+class FP4ProbeCache(_LayerCache):
     """FP4 probe cache of one layer (KV4-RL App. D.4: NVFP4 or MXFP4 K/V,
     reconstructed and attended with bf16 operands).  `append` writes the
     packed format; `decode` reconstructs the pool into a bf16 comparator cache
@@ -106,27 +118,14 @@ class FP4ProbeCache:
                  device="cuda", hadamard_k=False):
         import torch
         self.fmt = int(fmt)
-        self.layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=32, sink=0, recent=0,
-                                      max_seqs=max_seqs, num_pages=num_pages,
-                                      max_pages_per_seq=max_pages_per_seq)
-        self.device = torch.device(device)
+        layout = kv4.make_layout(h_q=h_q, h_kv=h_kv, d_h=d_h, group=32, sink=0, recent=0,
+                                 max_seqs=max_seqs, num_pages=num_pages,
+                                 max_pages_per_seq=max_pages_per_seq)
+        self._init_common(layout, max_seqs, max_pages_per_seq, device, hadamard_k)
         self.cache = torch.zeros(kv4.fp4_cache_bytes(self.layout), dtype=torch.uint8,
                                  device=self.device)
         self.bf16 = torch.zeros(kv4.bf16_cache_bytes(self.layout), dtype=torch.uint8,
                                 device=self.device)
-        self.block_table = torch.full((max_seqs, max_pages_per_seq), -1, dtype=torch.int32,
-                                      device=self.device)
-        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.hadamard_k = bool(hadamard_k)
-        self._ws = {}
-        self._qrot = {}
-
-    sm_scale = MixedKVCache.sm_scale
-    set_block_table = MixedKVCache.set_block_table
-    workspace = MixedKVCache.workspace
-    rotated_query = MixedKVCache.rotated_query
-    read_status = MixedKVCache.read_status
-    clear_status = MixedKVCache.clear_status
 
     def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
         kv4.kv4_fp4_append(self.layout, self.fmt, self.cache, k_new, v_new, tok_seq, tok_pos,
