@@ -614,7 +614,8 @@ def run_report(args):
         sup, pmf = W.lognormal_length_pmf(w.length, w.sigma, w.length_lo, w.length_hi)
         shape = dict(h_q=w.h_q, h_kv=w.h_kv, d_h=w.d_h, group=w.group, sink=w.sink,
                      recent=w.recent)
-        waves = RO.wave_schedule(w.batch, args.prompt, sup, pmf, 1, np.random.default_rng([w.seed, 30]))
+        waves = RO.wave_schedule(w.batch, args.prompt, sup, pmf, args.waves,
+                                 np.random.default_rng([w.seed, 30]))
         refill = RO.refill_schedule(w.batch, args.prompt, sup, pmf, waves.steps,
                                     np.random.default_rng([w.seed, 31]))
         lines = {}
@@ -675,6 +676,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
+    ap.add_argument("--waves", type=int, default=2,
+                    help="synchronous waves of the driven rollout schedules (--report c)")
     ap.add_argument("--prompt", type=int, default=256,
                     help="prompt length P of the driven rollout schedules (--report c)")
     ap.add_argument("--report", default=None,
