@@ -43,8 +43,8 @@ UNIT = "tokens/s"
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("85f2d33b8d498662", "qwen3_8b_b64"): 388407040 + 4196096,
-           ("85f2d33b8d498662", "long_128k"): 168132352 + 2948352}
+TRAFFIC = {("37b5efaf3b5e8203", "qwen3_8b_b64"): 388365568 + 4518144,
+           ("37b5efaf3b5e8203", "long_128k"): 168151808 + 3310592}
 
 
 # ------------------------------------------------------------------ helpers

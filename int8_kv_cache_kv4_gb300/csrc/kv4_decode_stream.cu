@@ -27,7 +27,8 @@
 // accumulation):
 //  INT4 page: as in the split kernel -- block-diagonal query rows against the
 //    widened 4-bit K codes, scores by eq. 5.1 per group, then the transposed
-//    centred V codes against P' = p * Delta_v plus the offset term.
+//    V codes (entered as fp16 subnormals, bit pattern = code) against
+//    P' = p * Delta_v plus the offset term sum p m.
 //  INT8 unit: the query (rows = heads) against the 8 slots' K codes widened
 //    exactly to fp16, scores scaled by each slot's K scale; then the
 //    transposed V codes against P' = p * s_v.  Slots outside the protected
@@ -580,9 +581,12 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // fragments carry the 1/16 and the accumulators start at minus the
       // constant 1024-part, so each row sums q_d c_d over its group.  Scores
       // by eq. 5.1 per group; one online-softmax step for both pages; then per
-      // page PV against the centred V codes with P' = p * Delta_v, and the
-      // offset term sum_t p_t (Delta_t, m_t) of every group as one more MMA
-      // whose A rows are the page's V metadata (group, Delta | m).
+      // page PV against the V codes with P' = p * Delta_v -- each code enters
+      // the MMA as the fp16 subnormal with its own bit pattern (c 2^-24, or
+      // 16 c 2^-24 for high nibbles: one logic op per pair, products exact),
+      // the accumulators scaled back when published -- and the offset term
+      // sum_t p_t m_t of every group as one more MMA whose A rows are the
+      // page's V metadata (group, Delta | m).
       const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qp.qfrag4[0][0][0]) + lane;  // + 32 * s
       float qs0 = 0.f, qs1 = 0.f;
 #pragma unroll
@@ -757,8 +761,8 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
               const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
               const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
               uint32_t xl[4], xh[4];
-              widen_v(wlo, xl);
-              widen_v(whi, xh);
+              widen_v_sub(wlo, xl);
+              widen_v_sub(whi, xh);
               mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
               mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
             }
@@ -776,13 +780,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         sm.mrg_m[warp][jh] = m_run;
         sm.mrg_l[warp][jh] = lsum;
       }
-      // offset term of group g, heads 2qd, 2qd+1: sum p m + 8 sum p Delta (rows
-      // 2g and 2g + 1 live in lanes 8g + qd and 8g + 4 + qd)
+      // offset term of group g, heads 2qd, 2qd+1: sum p m (row 2g + 1, in lane
+      // 8g + 4 + qd; row 2g, sum p Delta, is not needed with uncentred codes)
       {
         const float om0 = __shfl_xor_sync(0xffffffffu, mtacc[0], 4);
         const float om1 = __shfl_xor_sync(0xffffffffu, mtacc[1], 4);
         if ((r & 1) == 0 && mt_row && qd < 2) {
-          const float tA = fmaf(8.f, mtacc[0], om0), tB = fmaf(8.f, mtacc[1], om1);
+          const float tA = om0, tB = om1;
           for (int blk = mt_g * (GS / 32); blk < (mt_g + 1) * (GS / 32); ++blk) {
             sm.mrg_mt[warp][2 * qd][blk] = tA;
             sm.mrg_mt[warp][2 * qd + 1][blk] = tB;
@@ -795,11 +799,12 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         for (int P = 0; P < 4; ++P)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
+            // codes entered as c 2^-24 (even channels) and 16 c 2^-24 (odd)
             const int dd = 32 * P + 4 * r + 2 * hh;
-            sm.mrg_o[warp][hA][dd] = acc[P][hh][0];
-            sm.mrg_o[warp][hB][dd] = acc[P][hh][1];
-            sm.mrg_o[warp][hA][dd + 1] = acc[P][hh][2];
-            sm.mrg_o[warp][hB][dd + 1] = acc[P][hh][3];
+            sm.mrg_o[warp][hA][dd] = acc[P][hh][0] * 0x1p24f;
+            sm.mrg_o[warp][hB][dd] = acc[P][hh][1] * 0x1p24f;
+            sm.mrg_o[warp][hA][dd + 1] = acc[P][hh][2] * 0x1p20f;
+            sm.mrg_o[warp][hB][dd + 1] = acc[P][hh][3] * 0x1p20f;
           }
       }
     } else {

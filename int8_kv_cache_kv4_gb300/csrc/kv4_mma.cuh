@@ -101,6 +101,18 @@ __device__ inline void widen_v(uint32_t w, uint32_t x[4]) {
   x[3] = hfma2(and_or(w8, 0x00F000F0u, 0x64006400u), kSixteenth2, kM72);
 }
 
+// Widen 8 V codes (two tokens x four channels) to fp16 pairs whose bit
+// patterns are the codes themselves: subnormal values c * 2^-24 (low nibbles,
+// pairs 0 and 2) and 16 c * 2^-24 (high nibbles, pairs 1 and 3).  One logic
+// op per pair; the consumer scales its accumulators by 2^24 and 2^20.
+__device__ inline void widen_v_sub(uint32_t w, uint32_t x[4]) {
+  x[0] = w & 0x000F000Fu;
+  x[1] = w & 0x00F000F0u;
+  const uint32_t w8 = w >> 8;
+  x[2] = w8 & 0x000F000Fu;
+  x[3] = w8 & 0x00F000F0u;
+}
+
 // Widen one K code word (8 channels of one token) to 4 fp16 pairs without
 // removing the exponent offset: pairs 0 and 2 hold 1024 + c (channels i and
 // i + 4 of the low nibbles), pairs 1 and 3 hold 1024 + 16 c (high nibbles).
