@@ -179,8 +179,7 @@ def run_kv4(args):
     dev = torch.device("cuda", local)
     from int8_kv_cache_kv4_gb300 import kv4
     kv4.load(build_if_missing=True)
-    kv4.kv4_set_decode_kernel({"auto": kv4.KV4_KERNEL_AUTO, "tcgen05": kv4.KV4_KERNEL_TCGEN05,
-                               "stream": kv4.KV4_KERNEL_STREAM, "sm": kv4.KV4_KERNEL_SM,
+    kv4.kv4_set_decode_kernel({"auto": kv4.KV4_KERNEL_AUTO, "stream": kv4.KV4_KERNEL_STREAM,
                                "mma": kv4.KV4_KERNEL_MMA_SYNC,
                                "cuda": kv4.KV4_KERNEL_CUDA_CORE}[args.kernel])
 
@@ -320,8 +319,6 @@ def run_kv4(args):
 def decode_kernel_name(args, w):
     if args.kernel == "cuda" or w.d_h != 128 or w.h_q != 4 * w.h_kv:
         return "decode_split_kernel (CUDA cores, fused eq. A1 merge)"
-    if args.kernel == "tcgen05":
-        return "decode_tc_kernel (tcgen05, fused eq. A1 merge)"
     if args.kernel == "mma" or args.max_splits > 0:
         return "decode_mma_kernel (mma.sync split kernel, fused eq. A1 merge)"
     return "decode_stream_kernel (work-balanced, mma.sync, fused eq. A1 merge)"
@@ -598,16 +595,21 @@ def run_report(args):
                               "mean_abs": float(d.mean()), "status": cache.read_status()}), flush=True)
             del cache
             torch.cuda.empty_cache()
-    if "i8" in sel:  # tensor-pipe rates behind the integer decode variant: int8 vs fp16 mma.sync
+    if "i8" in sel:  # tensor-pipe rates behind the integer decode variant (libkv4_diag.so)
+        from int8_kv_cache_kv4_gb300 import diag
         sink = torch.zeros(1, dtype=torch.int32, device=dev)
-        blocks = torch.cuda.get_device_properties(dev).multi_processor_count * 8
-        iters = 4096
-        for kind, name, ops in ((0, "fp16 m16n8k16 (fp32 accumulate)", 4096),
-                                (1, "int8 m16n8k32 (int32 accumulate)", 8192)):
-            t = _timed(lambda: kv4.kv4_diag_mma_rate(kind, blocks, iters, sink), warm=3, samples=10)
-            total = blocks * 8 * 4 * iters * ops
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        for kind, name, blocks, iters in (
+                (diag.KIND_MMA_F16, "mma.sync m16n8k16 fp16 (fp32 accumulate)", sms * 8, 4096),
+                (diag.KIND_MMA_I8, "mma.sync m16n8k32 int8 (int32 accumulate)", sms * 8, 4096),
+                (diag.KIND_TC_F16, "tcgen05.mma kind::f16 128x256x16 (fp32 in tensor memory)",
+                 sms, 4096)):
+            t = _timed(lambda: diag.kv4_diag_mma_rate(kind, blocks, iters, sink), warm=3, samples=10)
             print(json.dumps({"report": "mma rate", "kind": name, "ms": t["median_ms"],
-                              "TOPS": total / (t["median_ms"] / 1e3) / 1e12}), flush=True)
+                              "TOPS": diag.ops(kind, blocks, iters) / (t["median_ms"] / 1e3) / 1e12,
+                              "status": int(sink.item())}), flush=True)
+        print(json.dumps({"report": "mma rate", "kind": "tcgen05.mma kind::i8",
+                          "unavailable": "ptxas rejects it for sm_103a"}), flush=True)
     if "c" in sel:  # KV concentration: continuous refill vs synchronous waves, driven on the GPU
         from int8_kv_cache_kv4_gb300 import rollout as RO
         w = W.WORKLOADS["rollout_b256"]
@@ -670,7 +672,7 @@ def main():
     ap.add_argument("--impl", default="kv4", choices=["kv4", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b64", choices=sorted(W.WORKLOADS))
     ap.add_argument("--max-splits", type=int, default=0)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "sm", "stream", "tcgen05", "mma", "cuda"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "stream", "mma", "cuda"],
                     help="decode kernel (auto = the fastest measured for the layout)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")

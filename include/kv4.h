@@ -119,25 +119,17 @@ const char* kv4_status_string(int code);
  * query heads per kv head, the work-balanced persistent tensor-core kernel
  * (STREAM) when max_splits is 0 and the warp-level split kernel (MMA_SYNC)
  * when the caller fixes the split count; the CUDA-core kernel otherwise.
- * STREAM cuts every (sequence, kv head) into 16-token INT4 pages and 8-slot
- * protected units and gives each CTA of a grid that fills the GPU an equal
- * share; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.
- * SM runs the same stream with one CTA of sixteen warps per SM, the warps
- * claiming units one at a time and merging their states without CTA-wide
- * barriers, between a small kernel that prepares each pair's query
- * fragments in the workspace and a kernel that merges each pair's partials
- * (eq. A1); like STREAM it needs max_splits = 0.  It balances work best and
- * is slower than STREAM on GB300 (measured), so AUTO does not pick it.
- * TCGEN05 selects the tensor-memory (tcgen05.mma) split kernel, MMA_SYNC the
- * warp-level one, CUDA_CORE the fp32 one.  All compute the same result within
+ * STREAM cuts every (sequence, kv head) into two-page INT4 units and 16-slot
+ * protected units and gives each CTA of a grid that fills the GPU a share of
+ * equal cost; it ignores max_splits, so with max_splits > 0 it runs MMA_SYNC.
+ * CUDA_CORE selects the fp32 split kernel.  All compute the same result within
  * the stated tolerance.  A kernel that does not support the layout falls back
- * to the CUDA-core kernel.  Returns the previous value. */
+ * to the CUDA-core kernel.  Any other value leaves the selection unchanged.
+ * Returns the previous value. */
 #define KV4_KERNEL_AUTO 0
 #define KV4_KERNEL_CUDA_CORE 1
 #define KV4_KERNEL_MMA_SYNC 2
-#define KV4_KERNEL_TCGEN05 3
 #define KV4_KERNEL_STREAM 4
-#define KV4_KERNEL_SM 5
 int kv4_set_decode_kernel(int which);
 
 /* Validate a layout; KV4_OK or a KV4_ERR_* code. */
@@ -151,10 +143,8 @@ size_t kv4_bf16_cache_bytes(const kv4_layout* layout);  /* comparator pages */
 /* Number of context splits per (sequence, kv head) that the split kernels use
  * for `num_seqs` sequences when given `max_splits` (0 = automatic), and the
  * workspace (device scratch: partial outputs, log-normalisers and completion
- * counters) kv4_decode_attn needs with that max_splits.  The size covers every
- * kernel choice except that the SM kernel's per-pair query fragments (5,248 B
- * per sequence and kv head) are counted only while KV4_KERNEL_SM is selected:
- * select it before sizing, or kv4_decode_attn returns KV4_ERR_WORKSPACE. */
+ * counters) kv4_decode_attn needs with that max_splits, for every kernel
+ * choice. */
 int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 
@@ -267,20 +257,6 @@ int kv4_fp4_to_bf16(const kv4_layout* layout, int32_t format, const void* cache,
                     void* stream);
 
 /*
- * kv4_diag_mma_rate -- diagnostic, not part of the method.  KV4-RL's deployed
- * decode multiplies INT8 operands on the tensor cores (Sec. 5.3 and App. A.3
- * "Integer decode path"); this library's decode multiplies fp16 ones.  The
- * probe launches `blocks` CTAs of 8 warps, each warp issuing 4 x `iters`
- * warp-level MMAs on register operands: kind 0 = m16n8k16 fp16 with fp32
- * accumulation (4,096 flops each), kind 1 = m16n8k32 int8 with int32
- * accumulation (8,192 ops each).  Time it with events on `stream` to get the
- * rate.  `sink`: device, 4 bytes, written only to keep the results live.
- * Returns KV4_ERR_INVALID_ARG for another kind, non-positive sizes or a NULL
- * sink.
- */
-int kv4_diag_mma_rate(int32_t kind, int32_t blocks, int32_t iters, uint32_t* sink, void* stream);
-
-/*
  * kv4_decode_attn -- split-KV GQA decode attention over the mixed cache
  * (KV4-RL Sec. 5.3 and App. A.3: disjoint INT4 and protected regions, each
  * split producing a locally normalised output and log-normaliser, merged by
@@ -356,7 +332,13 @@ int kv4_bf16_decode_attn(const kv4_layout* layout, const void* cache, const uint
  *   - Nothing is allocated or freed: the first call on a device looks up the
  *     scratch's device address (cudaGetSymbolAddress, with that device
  *     current) and caches it, so make that first call before any stream
- *     capture.
+ *     capture.  The cached address belongs to the device's primary context:
+ *     resetting the device (cudaDeviceReset) while the library is loaded is
+ *     not supported by this entry point.
+ *   - The limit depends on the kernel that runs: test
+ *     kv4_workspace_bytes(layout, num_seqs, max_splits) <=
+ *     kv4_noalloc_scratch_bytes() before the call (at h_q = 32, h_kv = 8,
+ *     head_dim 128 the default kernel fits up to 443 sequences).
  *   - All calls share the one scratch array, which keeps the last call's
  *     contents; the completion counters that must start at zero are cleared on
  *     the stream at the start of every call.  Calls whose work overlaps on the

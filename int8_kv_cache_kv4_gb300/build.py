@@ -1,8 +1,11 @@
-"""Build the kv4 CUDA library (libkv4.so) in-tree for GB300 (sm_103a).
+"""Build the kv4 CUDA libraries in-tree for GB300 (sm_103a).
 
-Each translation unit is compiled in parallel with nvcc, then linked into a
-shared library against the shared CUDA runtime (the same libcudart that
-PyTorch loads).  The result sits next to this file and is git-ignored.
+libkv4.so is the decode library (include/kv4.h); libkv4_diag.so holds the
+tensor-pipe rate probes (include/kv4_diag.h), which only the benchmark's
+report mode loads.  Each translation unit is compiled in parallel with nvcc,
+then linked into a shared library against the shared CUDA runtime (the same
+libcudart that PyTorch loads).  The results sit next to this file and are
+git-ignored.
 """
 from __future__ import annotations
 
@@ -17,9 +20,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libkv4.so")
+DIAG_OUT = os.path.join(HERE, "libkv4_diag.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["kv4_abi.cu", "kv4_append.cu", "kv4_decode.cu", "kv4_decode_mma.cu", "kv4_decode_tc.cu", "kv4_decode_stream.cu",
-           "kv4_decode_sm.cu", "kv4_noalloc.cu", "kv4_diag.cu"]
+SOURCES = ["kv4_abi.cu", "kv4_append.cu", "kv4_decode.cu", "kv4_decode_mma.cu",
+           "kv4_decode_stream.cu", "kv4_noalloc.cu"]
+DIAG_SOURCES = ["diag/kv4_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,16 +36,18 @@ def _nvcc() -> str:
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "kv4.h"))
+    files = []
+    for d, _, names in os.walk(CSRC):
+        files += [os.path.join(d, f) for f in names]
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 
 
 def stale() -> bool:
-    if not os.path.exists(OUT):
+    if not os.path.exists(OUT) or not os.path.exists(DIAG_OUT):
         return True
-    t = os.path.getmtime(OUT)
+    t = min(os.path.getmtime(OUT), os.path.getmtime(DIAG_OUT))
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
@@ -54,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                      f"-I{INCLUDE}", "-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(BUILD_DIR, os.path.basename(os.path.splitext(src)[0]) + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         with open(obj + ".log", "w") as f:
@@ -63,17 +70,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr[-4000:]}")
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = OUT + f".{os.getpid()}.tmp"
-    link = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
-        "-Xlinker", f"-rpath,{os.path.join(cuda_home, 'lib64')}"]
-    r = subprocess.run(link, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, OUT)
-    if verbose:
-        print(f"built {OUT}")
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(DIAG_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES + DIAG_SOURCES))
+    for out, part in ((OUT, objs[:len(SOURCES)]), (DIAG_OUT, objs[len(SOURCES):])):
+        tmp = out + f".{os.getpid()}.tmp"
+        link = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + part + [
+            "-Xlinker", f"-rpath,{os.path.join(cuda_home, 'lib64')}"]
+        r = subprocess.run(link, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
+        os.replace(tmp, out)
+        if verbose:
+            print(f"built {out}")
     return OUT
 
 

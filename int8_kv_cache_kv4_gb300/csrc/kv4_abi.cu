@@ -26,10 +26,6 @@ cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, cons
 cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
                            cudaStream_t);
 bool mma_supported(const Layout&);
-cudaError_t launch_decode_tc(const Layout&, const void*, const void*, const uint16_t*,
-                             const int32_t*, int, const int32_t*, float, int, int, int, int,
-                             float*, float*, int32_t*, uint16_t*, float*, int32_t*,
-                             cudaStream_t);
 static int g_decode_kernel = KV4_KERNEL_AUTO;
 cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uint16_t*,
                               const int32_t*, int, const int32_t*, float, int, int, int, int,
@@ -40,17 +36,13 @@ long long stream_partials(const Layout&, int);
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
                                  int32_t*, uint16_t*, float*, int32_t*, cudaStream_t);
-bool sm_supported(const Layout&);
-size_t sm_qprep_bytes(const Layout&, int);
-cudaError_t launch_decode_sm(const Layout&, const void*, const void*, const uint16_t*,
-                             const int32_t*, int, const int32_t*, float, void*, float*, float*,
-                             uint16_t*, float*, int32_t*, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
 // kTargetCtas CTAs in total (16 per SM of a 152-SM GB300), at least
 // kMinPagesPerSplit pages per INT4 split, a whole number of 8-page tiles per
-// split, and one protected split per kProtChunk side-cache slots.
+// split (the split kernels' page loop), and one protected split per
+// kProtChunk side-cache slots.
 constexpr int kTargetCtas = 16 * 152;
 constexpr int kMinPagesPerSplit = 4;
 constexpr int kProtChunk = 256;
@@ -71,7 +63,7 @@ static Plan make_plan(const kv4_layout* lay, int num_seqs, int max_splits, bool 
   int pps = (int)((maxp + n4 - 1) / n4);
   if (pps < kMinPagesPerSplit) pps = kMinPagesPerSplit;
   if (max_splits > 0 && (maxp + pps - 1) / pps > max_splits) pps = (maxp + max_splits - 1) / max_splits;
-  // whole 8-page tiles (the tensor-memory kernel's unit of work)
+  // whole 8-page tiles
   pps = (pps + kTilePagesPlan - 1) / kTilePagesPlan * kTilePagesPlan;
   p.pages_per_split = pps;
   p.n4 = (maxp + pps - 1) / pps;
@@ -98,14 +90,11 @@ static Layout to_layout(const kv4_layout* l) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
-// [rows][n_split], one int32 completion ticket per (sequence, kv head), and
-// (max_splits = 0, while the SM kernel is selected) its per-pair query
-// fragments.
+// [rows][n_split] and one int32 completion ticket per (sequence, kv head).
 struct Workspace {
   float* part_o;
   float* part_lse;
   int32_t* tickets;
-  void* qprep;
   size_t ticket_bytes;
   size_t bytes;
 };
@@ -130,13 +119,7 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   const size_t z = round256(prow * sizeof(float));
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
-  const Layout L = to_layout(l);
-  // (the SM kernel's query fragments: only while it is the selected kernel)
-  const size_t qb = (max_splits == 0 && sm_supported(L) && g_decode_kernel == KV4_KERNEL_SM)
-                        ? sm_qprep_bytes(L, num_seqs)
-                        : 0;
-  w.bytes = o + z + round256(w.ticket_bytes) + round256(qb);
-  w.qprep = qb ? (void*)((char*)base + o + z + round256(w.ticket_bytes)) : nullptr;
+  w.bytes = o + z + round256(w.ticket_bytes);
   w.part_o = (float*)base;
   w.part_lse = (float*)((char*)base + o);
   w.tickets = (int32_t*)((char*)base + o + z);
@@ -156,7 +139,9 @@ int kv4_abi_version(void) { return KV4_ABI_VERSION; }
 
 int kv4_set_decode_kernel(int which) {
   const int prev = g_decode_kernel;
-  if (which >= KV4_KERNEL_AUTO && which <= KV4_KERNEL_SM) g_decode_kernel = which;
+  if (which == KV4_KERNEL_AUTO || which == KV4_KERNEL_CUDA_CORE || which == KV4_KERNEL_MMA_SYNC ||
+      which == KV4_KERNEL_STREAM)
+    g_decode_kernel = which;
   return prev;
 }
 
@@ -316,32 +301,22 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   const Workspace w = ws_layout(l, num_seqs, p, max_splits, workspace);
   cudaStream_t st = (cudaStream_t)stream;
   const Layout L = to_layout(l);
-  // head_dim 128 with 4 query heads per kv head runs a tensor-core kernel
-  // (the warp-level mma kernel by default); other shapes the CUDA-core kernel.  All merge their
-  // splits in the last-finishing CTA of each (sequence, kv head).
+  // head_dim 128 with 4 query heads per kv head runs a tensor-core kernel:
+  // the work-balanced stream kernel, or with a caller-fixed split count the
+  // warp-level split kernel; other shapes the CUDA-core kernel.
   int which = g_decode_kernel;
   if (which == KV4_KERNEL_AUTO) which = KV4_KERNEL_STREAM;  // fastest measured on GB300
   if (which == KV4_KERNEL_STREAM && (max_splits > 0 || !stream_supported(L)))
     which = KV4_KERNEL_MMA_SYNC;
-  if (which == KV4_KERNEL_SM && (max_splits > 0 || !sm_supported(L))) which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
   // Completion tickets for the fused eq. A1 merge start at zero on every call
-  // (the SM kernel takes none: its pairs are merged by a separate kernel; the
-  // stream kernel clears them itself when it merges in-kernel).
-  if (which != KV4_KERNEL_SM && which != KV4_KERNEL_STREAM &&
-      cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
+  // (the stream kernel's launcher clears them itself when it merges in-kernel).
+  if (which != KV4_KERNEL_STREAM && cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
     return KV4_ERR_LAUNCH;
   cudaError_t e;
-  if (which == KV4_KERNEL_SM)
-    e = launch_decode_sm(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, w.qprep,
-                         w.part_o, w.part_lse, out, out_lse, dev_status, st);
-  else if (which == KV4_KERNEL_STREAM)
+  if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
                              w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, st);
-  else if (which == KV4_KERNEL_TCGEN05)
-    e = launch_decode_tc(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
-                         p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
-                         w.tickets, out, out_lse, dev_status, st);
   else if (which == KV4_KERNEL_MMA_SYNC)
     e = launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                           p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,

@@ -34,9 +34,7 @@ KV4_STATUS_INTERNAL = 64
 KV4_KERNEL_AUTO = 0
 KV4_KERNEL_CUDA_CORE = 1
 KV4_KERNEL_MMA_SYNC = 2
-KV4_KERNEL_TCGEN05 = 3
 KV4_KERNEL_STREAM = 4
-KV4_KERNEL_SM = 5
 
 
 class kv4_layout(ctypes.Structure):
@@ -101,7 +99,6 @@ def load(build_if_missing: bool = False):
         "kv4_quant_append": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_quant_append_hadamard": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_hadamard_bf16": (ctypes.c_int, [P, P, I, I, P]),
-        "kv4_diag_mma_rate": (ctypes.c_int, [I, I, I, P, P]),
         "kv4_fp4_cache_bytes": (Sz, [LP]),
         "kv4_fp4_append": (ctypes.c_int, [LP, I, I, P, P, P, P, P, I, P, P, P, P]),
         "kv4_fp4_to_bf16": (ctypes.c_int, [LP, I, P, P, P]),
@@ -212,12 +209,6 @@ def kv4_hadamard_bf16(x, y=None, stream=None):
     return y
 
 
-def kv4_diag_mma_rate(kind, blocks, iters, sink, stream=None):
-    """Launch the tensor-pipe rate probe (kind 0: fp16 MMA, 1: int8 MMA)."""
-    _check(load().kv4_diag_mma_rate(int(kind), int(blocks), int(iters), _ptr(sink), _stream(stream)),
-           "kv4_diag_mma_rate")
-
-
 KV4_FP4_NVFP4, KV4_FP4_MXFP4 = 1, 2
 
 
@@ -272,9 +263,10 @@ def _quant_append(name, layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq
     _check(rc, name)
 
 
-def kv4_decode_attn(layout, paged, side, q, seq_lens, block_table, workspace, out, out_lse=None,
-                    sm_scale=None, max_splits=0, status=None, stream=None):
-    """Split-KV GQA decode attention; q/out bf16 [B][h_q][d_h]."""
+def _check_decode_args(name, layout, paged, side, q, seq_lens, block_table, out, out_lse, status):
+    """Types, devices and shapes of a decode call's tensors, so that a
+    mis-sized tensor is a KV4Error here instead of an out-of-bounds access on
+    the device.  Returns the number of sequences B = q.shape[0]."""
     import torch
     _dev(paged, torch.uint8, "paged")
     _dev(side, torch.uint8, "side")
@@ -284,8 +276,35 @@ def kv4_decode_attn(layout, paged, side, q, seq_lens, block_table, workspace, ou
     _dev(seq_lens, torch.int32, "seq_lens")
     _dev(block_table, torch.int32, "block_table")
     _dev(status, torch.int32, "status")
-    _dev(workspace, torch.uint8, "workspace")
+    shape = (layout.num_q_heads, layout.head_dim)
+    if q.dim() != 3 or tuple(q.shape[1:]) != shape or not q.is_contiguous():
+        raise KV4Error(f"{name}: q must be a contiguous [B][{shape[0]}][{shape[1]}] tensor")
     B = int(q.shape[0])
+    if tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+        raise KV4Error(f"{name}: out must be contiguous and shaped like q")
+    if out_lse is not None and (tuple(out_lse.shape) != (B, layout.num_q_heads)
+                                or not out_lse.is_contiguous()):
+        raise KV4Error(f"{name}: out_lse must be a contiguous [B][h_q] tensor")
+    if seq_lens.numel() < B or B > layout.max_seqs:
+        raise KV4Error(f"{name}: seq_lens holds fewer than B entries or B > max_seqs")
+    if tuple(block_table.shape) != (layout.max_seqs, layout.max_pages_per_seq) or \
+            not block_table.is_contiguous():
+        raise KV4Error(f"{name}: block_table must be a contiguous [max_seqs][max_pages_per_seq] tensor")
+    if paged.numel() < paged_cache_bytes(layout) or \
+            (layout.sink + layout.recent > 0 and side.numel() < side_cache_bytes(layout)):
+        raise KV4Error(f"{name}: cache buffers smaller than the layout's sizes")
+    if status is not None and status.numel() < 1:
+        raise KV4Error(f"{name}: status must hold one int32")
+    return B
+
+
+def kv4_decode_attn(layout, paged, side, q, seq_lens, block_table, workspace, out, out_lse=None,
+                    sm_scale=None, max_splits=0, status=None, stream=None):
+    """Split-KV GQA decode attention; q/out bf16 [B][h_q][d_h]."""
+    import torch
+    B = _check_decode_args("kv4_decode_attn", layout, paged, side, q, seq_lens, block_table, out,
+                           out_lse, status)
+    _dev(workspace, torch.uint8, "workspace")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(layout.head_dim)
     rc = load().kv4_decode_attn(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(q),
@@ -340,16 +359,8 @@ def kv4_decode_attn_noalloc(layout, paged, side, q, seq_lens, block_table, out, 
     """kv4_decode_attn without a caller workspace, for callers that cannot
     allocate device memory: the library's fixed scratch array is used instead
     (see include/kv4.h for its size, first-call set-up and sharing rules)."""
-    import torch
-    _dev(paged, torch.uint8, "paged")
-    _dev(side, torch.uint8, "side")
-    _dev(q, torch.bfloat16, "q")
-    _dev(out, torch.bfloat16, "out")
-    _dev(out_lse, torch.float32, "out_lse")
-    _dev(seq_lens, torch.int32, "seq_lens")
-    _dev(block_table, torch.int32, "block_table")
-    _dev(status, torch.int32, "status")
-    B = int(q.shape[0])
+    B = _check_decode_args("kv4_decode_attn_noalloc", layout, paged, side, q, seq_lens,
+                           block_table, out, out_lse, status)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(layout.head_dim)
     rc = load().kv4_decode_attn_noalloc(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(q),

@@ -135,25 +135,77 @@ def half_ulp_bf16(x):
     return np.where(a > 0, 2.0 ** (e - 8), 0.0)
 
 
-def compare_outputs(out, lse, ref_out, ref_lse, seqs, lens, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
-    """Errors are measured beyond the bf16 rounding of the output itself:
-    e = max(0, |out - ref| - half_ulp_bf16(ref)).  For the diffuse attention
-    of the long workloads |o| < 0.5 and this equals the raw error within
-    1e-3; for very short sequences |o| can reach several units, where bf16
-    rounding alone exceeds 2e-3."""
-    errs = []
+def ulp_bf16(x):
+    """One bf16 ulp at |x| (8 significant bits)."""
+    return 2.0 * half_ulp_bf16(x)
+
+
+def oracle_decode_many(jobs, threads=None):
+    """oracle.decode_seq over many sequences on the host's cores.  jobs:
+    {key: (q, k_src, v_src, kwargs)}.  The oracle is C behind ctypes, which
+    releases the GIL during each call, so threads run the sequences in
+    parallel without copying their sources."""
+    import concurrent.futures as cf
+    import os
+    threads = threads or min(len(jobs), os.cpu_count() or 1) or 1
+
+    def one(item):
+        key, (q, k, v, kw) = item
+        o, l, st = oracle.decode_seq(q, k, v, **kw)
+        assert st == 0
+        return key, o, l
+
+    outs, lses = {}, {}
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for key, o, l in ex.map(one, list(jobs.items())):
+            outs[key], lses[key] = o, l
+    return outs, lses
+
+
+def compare_outputs(out, lse, ref_out, ref_lse, seqs, lens, max_abs=MAX_ABS, mean_abs=MEAN_ABS,
+                    label=""):
+    """bf16 decode outputs against the fp64 oracle, with the raw error
+    e = |out - ref|.
+
+    - Every element: e <= 2e-3, or, where |ref| >= 0.5 (half a bf16 ulp there
+      is 2^-9 or more, so the output's own rounding alone can reach 2e-3),
+      `out` is one of the two bf16 values bracketing ref (e < 1 ulp: faithful
+      rounding).  Below 0.5 the second clause adds nothing: an ulp there is
+      at most 2^-9 < 2e-3.
+    - Mean: when max |ref| < 0.5 over the compared sequences (every
+      long-context and full-size workload), the raw mean e <= 2e-4 and the raw
+      max e <= 2e-3, the stated figures as they stand.  Otherwise the mean of
+      |out - bf16(ref)|, the deviation from the correctly rounded oracle
+      output, is <= 2e-4 (the raw mean of such a case is dominated by the
+      rounding of the |o| >= 0.5 outputs, which no bf16 output avoids).
+    The log-normaliser (fp32) is within 1e-3 of the oracle's.
+    Returns (raw max, raw mean) and prints both statistics."""
+    raws, rnds, refs = [], [], []
     for b in seqs:
         if int(lens[b]) == 0:
             assert np.all(out[b] == 0), f"seq {b}: empty sequence must give zeros"
             assert np.all(np.isneginf(lse[b]))
             continue
-        e = np.maximum(np.abs(out[b] - ref_out[b]) - half_ulp_bf16(ref_out[b]), 0.0)
-        errs.append(e)
+        ref = np.asarray(ref_out[b], dtype=np.float64)
+        e = np.abs(out[b] - ref)
+        ok = (e <= max_abs) | ((np.abs(ref) >= 0.5) & (e < ulp_bf16(ref)))
+        assert ok.all(), (f"seq {b}: {int((~ok).sum())} outputs beyond 2e-3 and not a bf16 "
+                          f"neighbour of the oracle value (worst {e[~ok].max():.3e})")
+        raws.append(e.ravel())
+        rnds.append(np.abs(out[b] - oracle.bf16_round(ref)).ravel())
+        refs.append(np.abs(ref).ravel())
         np.testing.assert_allclose(lse[b], ref_lse[b], atol=LSE_ABS, rtol=0,
                                    err_msg=f"lse of seq {b}")
-    if errs:
-        allerr = np.concatenate([e.ravel() for e in errs])
-        assert allerr.max() <= max_abs, f"max abs err {allerr.max():.3e} > {max_abs}"
-        assert allerr.mean() <= mean_abs, f"mean abs err {allerr.mean():.3e} > {mean_abs}"
-        return float(allerr.max()), float(allerr.mean())
-    return 0.0, 0.0
+    if not raws:
+        return 0.0, 0.0
+    raw = np.concatenate(raws)
+    rnd = np.concatenate(rnds)
+    big = float(np.concatenate(refs).max())
+    print(f"{label} raw max {raw.max():.3e} raw mean {raw.mean():.3e} | vs bf16(oracle): max "
+          f"{rnd.max():.3e} mean {rnd.mean():.3e} | max |o| {big:.3f}")
+    if big < 0.5:
+        assert raw.max() <= max_abs, f"raw max abs err {raw.max():.3e} > {max_abs}"
+        assert raw.mean() <= mean_abs, f"raw mean abs err {raw.mean():.3e} > {mean_abs}"
+    else:
+        assert rnd.mean() <= mean_abs, f"mean |out - bf16(ref)| {rnd.mean():.3e} > {mean_abs}"
+    return float(raw.max()), float(raw.mean())

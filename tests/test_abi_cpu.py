@@ -2,6 +2,7 @@
 every entry point include/kv4.h declares, and its host-only functions
 (validation, sizing, split plan) behave -- no GPU calls."""
 import ctypes
+import os
 import subprocess
 
 import pytest
@@ -64,21 +65,16 @@ def test_split_plan_and_workspace(lib):
     assert kv4.workspace_bytes(lay, 0) == 0 or kv4.workspace_bytes(lay, 0) >= 0
 
 
-def test_workspace_holds_sm_query_fragments_only_while_selected(lib):
-    # the SM kernel's per-pair query fragments (5248 B per sequence and kv
-    # head) are part of the workspace only while that kernel is selected
-    lay = kv4.make_layout(max_seqs=64, num_pages=40000, max_pages_per_seq=512)
-    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_AUTO)
+def test_retired_kernel_ids_leave_the_selection_unchanged(lib):
+    # only AUTO, CUDA_CORE, MMA_SYNC and STREAM select a kernel; other values
+    # (3 and 5 named kernels that are no longer part of the library) are ignored
+    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_STREAM)
     try:
-        auto = kv4.workspace_bytes(lay, 64)
-        kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_SM)
-        sm = kv4.workspace_bytes(lay, 64)
-        fixed = kv4.workspace_bytes(lay, 64, max_splits=2)   # the SM kernel needs max_splits = 0
-        kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_AUTO)
-        assert fixed == kv4.workspace_bytes(lay, 64, max_splits=2)
+        for bad in (3, 5, -1, 99):
+            assert kv4.kv4_set_decode_kernel(bad) == kv4.KV4_KERNEL_STREAM
+        assert kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_AUTO) == kv4.KV4_KERNEL_STREAM
     finally:
         kv4.kv4_set_decode_kernel(prev)
-    assert sm - auto == (64 * 8 * 5248 + 255) // 256 * 256
 
 
 def test_null_arguments_rejected_on_host(lib):
@@ -113,7 +109,7 @@ def test_hadamard_entry_points_validate_on_host(lib):
                                          0, None, None, None, None) == kv4.KV4_OK
 
 
-def test_fp4_and_diag_entry_points_validate_on_host(lib):
+def test_fp4_entry_points_validate_on_host(lib):
     lay = kv4.make_layout(max_seqs=4, num_pages=10, max_pages_per_seq=4)
     # probe cache: 10 pages x 8 kv heads x (K, V) x 16 slots x (64 + 16) bytes
     assert kv4.fp4_cache_bytes(lay) == 10 * 8 * 2 * 16 * 80
@@ -127,5 +123,24 @@ def test_fp4_and_diag_entry_points_validate_on_host(lib):
                               None, None, None) == kv4.KV4_OK                             # T == 0
     assert lib.kv4_fp4_to_bf16(ctypes.byref(lay), 0, None, None, None) == kv4.KV4_ERR_INVALID_ARG
     assert lib.kv4_fp4_to_bf16(ctypes.byref(lay), 1, None, None, None) == kv4.KV4_ERR_INVALID_ARG
-    assert lib.kv4_diag_mma_rate(2, 1, 1, None, None) == kv4.KV4_ERR_INVALID_ARG
-    assert lib.kv4_diag_mma_rate(0, 0, 1, None, None) == kv4.KV4_ERR_INVALID_ARG
+
+
+def test_diag_library_exports_its_header_and_validates_on_host():
+    # the rate probe lives in its own library, declared in include/kv4_diag.h
+    from int8_kv_cache_kv4_gb300 import build, diag
+    if not os.path.exists(diag.LIB_PATH):
+        build.build()
+    dl = diag.load()
+    names = diag.declared_symbols()
+    assert names == ["kv4_diag_mma_rate"]
+    for n in names:
+        assert hasattr(dl, n)
+    sink = ctypes.c_uint32(0)
+    assert dl.kv4_diag_mma_rate(3, 1, 1, ctypes.addressof(sink), None) == 1  # no tcgen05 int8 kind
+    assert dl.kv4_diag_mma_rate(0, 0, 1, ctypes.addressof(sink), None) == 1
+    assert dl.kv4_diag_mma_rate(0, 1, 1, None, None) == 1
+    assert not hasattr(lib_handle(), "kv4_diag_mma_rate")   # not in the decode library
+
+
+def lib_handle():
+    return kv4.load()

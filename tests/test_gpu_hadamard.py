@@ -92,9 +92,9 @@ def test_rotated_append_head_dim_64():
     compare_outputs(out, lse, ref, rlse, range(c.B), c.lens)
 
 
-@pytest.mark.parametrize("which", [kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_SM, kv4.KV4_KERNEL_TCGEN05,
-                                   kv4.KV4_KERNEL_MMA_SYNC, kv4.KV4_KERNEL_CUDA_CORE],
-                         ids=["stream", "sm", "tcgen05", "mma", "cuda"])
+@pytest.mark.parametrize("which", [kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_MMA_SYNC,
+                                   kv4.KV4_KERNEL_CUDA_CORE],
+                         ids=["stream", "mma", "cuda"])
 def test_rotated_decode_every_kernel(which):
     lens = [0, 1, 3, 4, 17, 64, 84, 85, 700, 1500]
     c = Case(lens, S=4, R=80, g=32, seed=17, h_q=32, h_kv=8, rotate_k=True)

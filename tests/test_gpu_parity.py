@@ -20,12 +20,13 @@ def _lib():
     kv4.load(build_if_missing=True)
 
 
-# every decode kernel (work-balanced stream, tcgen05, warp-level mma, CUDA
-# cores) must meet the bar; shapes a kernel does not support run the CUDA-core
-# kernel, and the stream kernel runs the mma split kernel when max_splits > 0
-@pytest.fixture(autouse=True, params=[kv4.KV4_KERNEL_SM, kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_TCGEN05,
-                                      kv4.KV4_KERNEL_MMA_SYNC, kv4.KV4_KERNEL_CUDA_CORE],
-                ids=["sm", "stream", "tcgen05", "mma", "cuda"])
+# every decode kernel (work-balanced stream, warp-level mma split kernel,
+# CUDA cores) must meet the bar; shapes a kernel does not support run the
+# CUDA-core kernel, and the stream kernel runs the mma split kernel when
+# max_splits > 0
+@pytest.fixture(autouse=True, params=[kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_MMA_SYNC,
+                                      kv4.KV4_KERNEL_CUDA_CORE],
+                ids=["stream", "mma", "cuda"])
 def kernel(request):
     prev = kv4.kv4_set_decode_kernel(request.param)
     yield request.param

@@ -1,7 +1,6 @@
-"""GPU parity of the work-balanced decode kernels' scheduling: the stream of
-16-slot protected units and two-page INT4 units cut into equal CTA shares,
-walked by warps in lock step (STREAM) or claimed one unit at a time by the
-warps of one CTA per SM (SM).
+"""GPU parity of the work-balanced decode kernel's scheduling: the stream of
+16-slot protected units and two-page INT4 units cut into CTA shares of equal
+cost and walked by the warps of each CTA.
 Cases aim at the bookkeeping -- pairs spread over many CTAs, CTAs without
 work, empty and very short sequences, partly filled recent-window rings,
 more sequences than threads in the start search -- and compare with the
@@ -16,8 +15,7 @@ from kv4_case import Case, compare_outputs  # noqa: E402
 from int8_kv_cache_kv4_gb300 import kv4  # noqa: E402
 
 
-@pytest.fixture(scope="module", autouse=True, params=[kv4.KV4_KERNEL_STREAM, kv4.KV4_KERNEL_SM],
-                ids=["stream", "sm"])
+@pytest.fixture(scope="module", autouse=True, params=[kv4.KV4_KERNEL_STREAM], ids=["stream"])
 def _lib(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
