@@ -35,13 +35,21 @@
  *     chunk      = K codes [16 slots][head_dim/2 bytes]
  *                  V codes [16 slots][head_dim/2 bytes]
  *                  K meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
- *                  V meta  [16 slots][head_dim/g][2 x fp16: Delta, m]
- *     A code row is the sequence of bytes whose byte i holds channel 2i in
- *     its low nibble and channel 2i+1 in its high nibble, cut into 16-byte
- *     pieces (32 channels each); piece P of slot t is stored at piece position
- *     P ^ ((t >> 1) & (head_dim/32 - 1)), for K and V alike, so that the
- *     decode kernels' row-wise and transposing shared-memory reads across
- *     consecutive slots hit distinct banks.
+ *                  V Delta [4 quads][head_dim/g][4 x fp16]
+ *                  V m     [4 quads][head_dim/g][4 x fp16]
+ *     A byte of a code row holds two consecutive channels, the even one in
+ *     its low nibble.
+ *     K code row: four quarters q = 0..3 of head_dim/32 four-byte words; word
+ *     b of quarter q holds channels 32b + 8q .. 32b + 8q + 7 (block b), so
+ *     that one 16-byte read gives a lane one word of every block.
+ *     V code row: byte i holds channels 2i and 2i+1, cut into 16-byte pieces
+ *     (32 channels each); piece P of slot t is stored at piece position
+ *     P ^ ((t >> 1) & (head_dim/32 - 1)), so that transposing shared-memory
+ *     reads across consecutive slots hit distinct banks.
+ *     V metadata: quad u lists the slots 2u, 2u+1, 2u+8, 2u+9 in that order;
+ *     entry (u, group, k) of V Delta / V m holds the Delta / m of the k-th
+ *     slot of quad u for that group (the four slots one tensor-core lane
+ *     multiplies, read as one 8-byte run per group).
  *     Position p of request slot s lives in page block_table[s][p / 16],
  *     slot p % 16.
  *     chunk bytes = 16*head_dim + 128*head_dim/g  (2560 at d=128, g=32).
@@ -77,7 +85,7 @@
 extern "C" {
 #endif
 
-#define KV4_ABI_VERSION 2
+#define KV4_ABI_VERSION 3
 
 /* host return codes */
 #define KV4_OK 0

@@ -212,11 +212,17 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     if (active) {
       uint8_t* row = chunk + (kv == 0 ? 0 : codes_off_v(d_h)) + slot * (d_h / 2);
       // 4 codes of channels c0..c0+3 -> two bytes (low nibble = even channel)
-      const int b = row_byte(2 * lane, slot, d_h);
+      const int b = kv == 0 ? k_row_byte(c0, d_h) : row_byte(2 * lane, slot, d_h);
       *reinterpret_cast<uint16_t*>(row + b) = (uint16_t)codes;
       if ((lane % span) == 0) {
-        uint8_t* m = chunk + (kv == 0 ? meta_off_k(d_h) : meta_off_v(d_h, g)) + slot * ng * 4;
-        *reinterpret_cast<uint32_t*>(m + 4 * (lane / span)) = meta;
+        const int grp = lane / span;
+        if (kv == 0) {
+          *reinterpret_cast<uint32_t*>(chunk + meta_off_k(d_h) + slot * ng * 4 + 4 * grp) = meta;
+        } else {
+          *reinterpret_cast<uint16_t*>(chunk + v_delta_byte(slot, grp, d_h, g)) = (uint16_t)meta;
+          *reinterpret_cast<uint16_t*>(chunk + v_offset_byte(slot, grp, d_h, g)) =
+              (uint16_t)(meta >> 16);
+        }
       }
     }
     if (prot) {

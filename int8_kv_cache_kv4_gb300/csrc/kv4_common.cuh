@@ -23,12 +23,33 @@ __host__ __device__ inline int chunk_bytes(int d_h, int g) { return 16 * d_h + 1
 __host__ __device__ inline int codes_off_v(int d_h) { return 8 * d_h; }  // 16 rows * d_h/2
 __host__ __device__ inline int meta_off_k(int d_h) { return 16 * d_h; }
 __host__ __device__ inline int meta_off_v(int d_h, int g) { return 16 * d_h + 64 * (d_h / g); }
-// Byte offset inside a K or V code row of logical byte `b` for slot `t`: the
-// row's 16-byte pieces are XOR-permuted by (t >> 1) so that 16-byte reads of
-// one piece index across 8 consecutive slots touch distinct banks.
+// Byte offset inside a V code row of logical byte `b` (channels 2b, 2b + 1)
+// for slot `t`: the row's 16-byte pieces (32 channels each) are XOR-permuted
+// by (t >> 1) so that transposing 16-byte reads of one piece across 8
+// consecutive slots touch distinct banks.
 __host__ __device__ inline int row_byte(int b, int t, int d_h) {
   const int np = d_h / 32;
   return 16 * ((b >> 4) ^ ((t >> 1) & (np - 1))) + (b & 15);
+}
+// Byte offset inside a K code row of the byte holding channels c and c + 1
+// (c even).  The row is four quarters q = 0..3 of d_h/32 words each; word b
+// of quarter q holds the 8 channels 32 b + 8 q .. 32 b + 8 q + 7 of block b.
+// A lane that needs quarter q of every block reads one contiguous run.
+__host__ __device__ inline int k_row_byte(int c, int d_h) {
+  const int nb = d_h / 32;
+  return 4 * (nb * ((c & 31) >> 3) + (c >> 5)) + ((c & 7) >> 1);
+}
+// V metadata of a chunk: Delta_v for every (slot, group), then m_v, each
+// [4 quads][d_h/g groups][4 slots] fp16, quad u holding slots 2u, 2u + 1,
+// 2u + 8, 2u + 9 (the slots one tensor-core lane multiplies).
+__host__ __device__ inline int v_meta_half(int t, int grp, int ng) {
+  return (((t & 7) >> 1) * ng + grp) * 4 + 2 * (t >> 3) + (t & 1);
+}
+__host__ __device__ inline int v_delta_byte(int t, int grp, int d_h, int g) {
+  return 16 * d_h + 64 * (d_h / g) + 2 * v_meta_half(t, grp, d_h / g);
+}
+__host__ __device__ inline int v_offset_byte(int t, int grp, int d_h, int g) {
+  return 16 * d_h + 96 * (d_h / g) + 2 * v_meta_half(t, grp, d_h / g);
 }
 
 // Byte offset of channel c inside an INT8 side-cache code row of slot t: the
@@ -187,6 +208,20 @@ __device__ inline void bulk_g2s_s(uint32_t smem_dst, const void* gmem_src, uint3
           smem_dst),
       "l"(gmem_src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// ------------------------------------------ cp.async (16-byte, L2 only)
+// Copy 16 bytes global -> shared; src_bytes 0 writes zeros and reads nothing.
+__device__ inline void cp_async16(uint32_t smem_dst, const void* gmem_src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gmem_src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are pending.
+template <int N>
+__device__ inline void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ------------------------------------------------------------ reductions

@@ -107,8 +107,9 @@ __device__ inline void qk_int4(const Smem<D, G>& sm, const uint8_t* chunk, int g
   constexpr int WORDS = D / 16;  // 8 nibbles per word, D/2 channels per lane
 #pragma unroll
   for (int w = 0; w < WORDS; ++w) {
+    // channels half * D/2 + 8 w .. + 7: one word of the K row
     const uint32_t word =
-        *reinterpret_cast<const uint32_t*>(krow + row_byte(half * (D / 4) + 4 * w, t, D));
+        *reinterpret_cast<const uint32_t*>(krow + k_row_byte(half * (D / 2) + 8 * w, D));
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
       const float c = u2f((word >> (4 * n)) & 0xFu);
@@ -140,11 +141,9 @@ template <int D, int G>
 __device__ inline void pv_int4(WarpState<D, G>& ws, const uint8_t* chunk, int g, const float (*p)[G],
                                int lane, uint32_t tok_mask) {
   constexpr int PD = D / 32;
-  const int ng = D / g;
   const int c0 = lane * PD;
   const int grp = c0 / g;
   const uint8_t* vcodes = chunk + codes_off_v(D);
-  const uint32_t* vmeta = reinterpret_cast<const uint32_t*>(chunk + meta_off_v(D, g));
   for (int t = 0; t < kPage; ++t) {
     if (!((tok_mask >> (2 * t)) & 1u)) continue;  // masked slot: may hold stale bytes
     uint32_t bits;
@@ -152,9 +151,10 @@ __device__ inline void pv_int4(WarpState<D, G>& ws, const uint8_t* chunk, int g,
       bits = *reinterpret_cast<const uint16_t*>(vcodes + t * (D / 2) + row_byte(c0 / 2, t, D));
     else
       bits = vcodes[t * (D / 2) + row_byte(c0 / 2, t, D)];
-    const uint32_t mt = vmeta[t * ng + grp];
-    const float delta = f16_bits_to_f32(mt & 0xFFFFu);
-    const float off = f16_bits_to_f32(mt >> 16);
+    const float delta =
+        f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(chunk + v_delta_byte(t, grp, D, g)));
+    const float off =
+        f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(chunk + v_offset_byte(t, grp, D, g)));
     float v[PD];
 #pragma unroll
     for (int i = 0; i < PD; ++i) v[i] = fmaf(delta, u2f((bits >> (4 * i)) & 0xFu), off);

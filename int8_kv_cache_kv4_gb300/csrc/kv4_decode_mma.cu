@@ -193,9 +193,8 @@ __global__ void __launch_bounds__(kThreads, 5) decode_mma_kernel(
       // metadata may be any bit pattern, so it is zeroed before use
       const bool tail = (pg + 1) * kPage > len;
       // ---------------- QK^T on tensor cores
-      const uint4 k0 = *reinterpret_cast<const uint4*>(chunk + r * 64 + row_byte(16 * qd, r, D));
-      const uint4 k1 =
-          *reinterpret_cast<const uint4*>(chunk + (r + 8) * 64 + row_byte(16 * qd, r + 8, D));
+      const uint4 k0 = k_block_words(chunk + r * 64, qd, D);        // block qd of row r
+      const uint4 k1 = k_block_words(chunk + (r + 8) * 64, qd, D);  // ... and of row r + 8
       // four independent accumulator chains (tokens 0-7 / 8-15 x even / odd
       // k-steps), summed afterwards
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -251,19 +250,12 @@ __global__ void __launch_bounds__(kThreads, 5) decode_mma_kernel(
       // metadata for PV, loaded early so its latency overlaps the softmax
       MetaRow<NG> vm[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) vm[e].load(chunk + meta_off_v(D, GS) + tk[e] * NG * 4);
+      for (int e = 0; e < 4; ++e) vm[e].load_v(chunk, tk[e], D);
       uint32_t mtw[4][NGH];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint8_t* row = chunk + meta_off_v(D, GS) + (tk[e] * NG + mt_g0) * 4;
-        if (NGH == 2) {
-          const uint2 v2 = *reinterpret_cast<const uint2*>(row);
-          mtw[e][0] = v2.x;
-          mtw[e][NGH - 1] = v2.y;
-        } else {
-          mtw[e][0] = *reinterpret_cast<const uint32_t*>(row);
-        }
-      }
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int gi = 0; gi < NGH; ++gi) mtw[e][gi] = vmeta_word(chunk, tk[e], mt_g0 + gi, D, GS);
       // ---------------- online softmax for head j over this page
       float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));

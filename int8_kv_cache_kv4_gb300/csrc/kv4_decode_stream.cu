@@ -46,8 +46,16 @@ namespace {
 // warps per CTA of this kernel, and its threads
 constexpr int kSW = 4;
 constexpr int kST = kSW * 32;
-constexpr int kSStages = 2;         // bulk-copy stages per warp
-constexpr int kStreamMinBlocks = 4; // CTAs per SM (shared memory: 4 x 56 KB)
+// Copy stages per warp and CTAs per SM (build-time constants; the defaults
+// are the measured best on GB300).
+#ifndef KV4_STREAM_STAGES
+#define KV4_STREAM_STAGES 2
+#endif
+#ifndef KV4_STREAM_CTAS_PER_SM
+#define KV4_STREAM_CTAS_PER_SM 4
+#endif
+constexpr int kSStages = KV4_STREAM_STAGES;
+constexpr int kStreamMinBlocks = KV4_STREAM_CTAS_PER_SM;
 // The thread that keeps the segment bookkeeping and takes the completion
 // tickets: lane 0 of the last warp, which the round-robin unit assignment
 // never gives more units than the others.
@@ -154,8 +162,6 @@ struct __align__(16) StreamSmem {
   int go;                           // comb is valid
   int new_q;                        // the next segment starts a new pair
   int start_b;
-  int32_t phys[kSW][kSStages][kSPages];  // INT4 stage: physical pages, < 0 = not loaded
-  uint64_t bar[kSW][kSStages];
   uint64_t qbar;                    // completion of the qraw copy
 };
 
@@ -173,8 +179,8 @@ __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __rest
 // Everything the units need from the query of the next pair, built from
 // sm.qraw once its copy has completed.  No warp may still read the old values.
 template <int NG>
-__device__ __noinline__ void stream_query_setup(StreamSmem& sm) {
-  if (threadIdx.x < 128) build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x);  // (built by 128 threads)
+__device__ __noinline__ void stream_query_setup(StreamSmem& sm, float scale_log2) {
+  if (threadIdx.x < 128) build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x, scale_log2);
 }
 
 // Merge the warps' states of one segment and store its partial result P
@@ -381,7 +387,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         out_lse[(long long)b * L.h_q + idx] = -INFINITY;
   }
   if (lane == 0) {
-    for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
     if (warp == 0) mbar_init(&sm.qbar, 1);
     fence_mbar_init();
   }
@@ -404,15 +409,22 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   }
   __syncthreads();
 
-  // ------------------------------------------------------ producer (lane 0)
+  // ------------------------------------------------------ producer (all lanes)
   const int NS = L.S + L.R;
   const int NSP = side_scale_entries(L.S, L.R);
   const long long side_blk = side_block_bytes(D, L.S, L.R);
   constexpr int SB = kSPages * cb;  // stage bytes: two INT4 chunks or one 16-slot INT8 unit
   static_assert(2 * kProtUnit * SD + 4 * kProtUnit <= SB, "an INT8 unit fits a stage");
+  constexpr int kFull = cb / 512, kRem = (cb % 512) / 16;  // 16-byte chunks of a page per lane
   uint8_t* my_stages = stage_base + (size_t)warp * kSStages * SB;
-  // Producer (lane 0 of each warp).  Its segment cursor lives in shared
-  // memory and moves only when a segment is used up; what each unit needs is
+  // Producer: every lane of the warp, in step.  Each unit is one group of
+  // 16-byte cp.async copies (lane l copies chunks l, l + 32, ...: every
+  // instruction moves 512 contiguous bytes), committed in the order the warp
+  // consumes the units.  Group k fills stage k % kSStages; after consuming
+  // group k the warp commits group k + kSStages (an empty group when nothing
+  // is left), so that waiting for "at most kSStages - 1 groups pending"
+  // always waits for exactly the unit at hand.  The segment cursor lives in shared memory (written by
+  // lane 0) and moves only when a segment is used up; what each unit needs is
   // kept in registers: the unit index in the segment and its end, the
   // segment's type, INT4 page count, block-table row, copy source (INT4: this
   // head's column of the pool; INT8: the pair's side block) and the next
@@ -422,23 +434,30 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   const int32_t* p_bt = block_table;
   const uint8_t* p_src = paged;
   int pphys = -1, pphys1 = -1;  // the unit's two pages (-2: no second page)
-  const uint32_t stages_s = smem_u32(my_stages), bars_s = smem_u32(&sm.bar[warp][0]);
+  uint32_t vbits = 0;           // bit 2 st + p: page p of stage st was copied
+  const uint32_t stages_s = smem_u32(my_stages);
   // slow path: (cursor, p_j) may lie past its segment's end; move over
   // segments until it names a unit of this warp
   auto prod_next = [&]() {
-    Seg& s_ = sm.prod[warp];
+    Seg s_ = sm.prod[warp];
     const long long ub = sm.u_begin, ue = sm.u_end;
     while (true) {
       if (s_.b >= B || s_.start >= ue) {
         p_more = 0;
-        return;
+        break;
       }
       p_hi = (int)(min(ue, s_.start + s_.n) - s_.start);
-      if (p_j < p_hi) break;
+      if (p_j < p_hi) {
+        p_more = 1;
+        break;
+      }
       seg_next(s_, L, seq_lens, B, ue);
       p_j = (int)(max(ub, s_.start) - s_.start) + warp;
     }
-    p_more = 1;
+    __syncwarp();
+    if (lane == 0) sm.prod[warp] = s_;
+    __syncwarp();
+    if (!p_more) return;
     p_type = s_.type;
     p_bt = block_table + (long long)s_.b * L.max_pages + min(s_.len, L.S) / kPage;
     p_np4 = int4_pages(s_.len, L);
@@ -451,49 +470,55 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     }
   };
   auto issue = [&](int st) {
-    const uint32_t bar = bars_s + 8u * st;
-    const uint32_t dst = stages_s + (uint32_t)(st * SB);
+    const uint32_t dst = stages_s + (uint32_t)(st * SB) + 16u * lane;
     if (p_type == 1) {
-      // pages 2j and 2j + 1 of the segment (the second may not exist: -2)
+      // pages 2j and 2j + 1 of the segment (the second may not exist: -2);
+      // a page id outside the pool is zero-filled and marked not copied
       const bool good0 = (unsigned)pphys < (unsigned)L.num_pages;
       const bool good1 = (unsigned)pphys1 < (unsigned)L.num_pages;
-      if (!good0 || (pphys1 != -2 && !good1)) set_status(status, KV4_STATUS_BAD_PAGE);
-      sm.phys[warp][st][0] = good0 ? pphys : -1;  // published by the arrive below
-      sm.phys[warp][st][1] = good1 ? pphys1 : -1;
+      if (lane == 0 && (!good0 || (pphys1 != -2 && !good1))) set_status(status, KV4_STATUS_BAD_PAGE);
+      vbits = (vbits & ~(3u << (2 * st))) | ((good0 ? 1u : 0u) << (2 * st)) |
+              ((good1 ? 1u : 0u) << (2 * st + 1));
       const int page_stride = L.h_kv * cb;  // bytes between pages of one head (< 2^31)
-      if (good0 || good1) {
-        mbar_arrive_expect_tx_s(bar, (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u));
-        if (good0) bulk_g2s_s(dst, p_src + (long long)pphys * page_stride, (uint32_t)cb, bar);
-        if (good1) bulk_g2s_s(dst + cb, p_src + (long long)pphys1 * page_stride, (uint32_t)cb, bar);
-      } else {
-        mbar_arrive_s(bar);
+      const uint8_t* s0 = good0 ? p_src + (long long)pphys * page_stride + 16 * lane : paged;
+      const uint32_t n0 = good0 ? 16u : 0u;
+#pragma unroll
+      for (int k = 0; k < kFull; ++k) cp_async16(dst + 512u * k, s0 + 512 * k, n0);
+      if (kRem && lane < kRem) cp_async16(dst + 512u * kFull, s0 + 512 * kFull, n0);
+      if (pphys1 != -2) {
+        const uint8_t* s1 = good1 ? p_src + (long long)pphys1 * page_stride + 16 * lane : paged;
+        const uint32_t n1 = good1 ? 16u : 0u;
+#pragma unroll
+        for (int k = 0; k < kFull; ++k) cp_async16(dst + cb + 512u * k, s1 + 512 * k, n1);
+        if (kRem && lane < kRem) cp_async16(dst + cb + 512u * kFull, s1 + 512 * kFull, n1);
       }
     } else {
+      // INT8 unit: rows slot0 .. slot0 + rows - 1 of the K8 and V8 codes, and
+      // the scales of the 8-slot runs that hold them (within the padding)
       const int slot0 = p_j * kProtUnit;
-      const uint32_t rows = (uint32_t)min(kProtUnit, p_ns - slot0);
-      // scales of the 8-slot runs that hold copied rows (within the NSP padding)
-      const uint32_t sbytes = 16u * ((rows + 7) / 8);
-      mbar_arrive_expect_tx_s(bar, 2u * rows * D + 2u * sbytes);
-      bulk_g2s_s(dst, p_src + (long long)slot0 * D, rows * D, bar);
-      bulk_g2s_s(dst + kProtUnit * D, p_src + (long long)(NS + slot0) * D, rows * D, bar);
-      bulk_g2s_s(dst + 2 * kProtUnit * D, p_src + 2LL * NS * D + 2 * slot0, sbytes, bar);
-      bulk_g2s_s(dst + 2 * kProtUnit * D + 2 * kProtUnit, p_src + 2LL * NS * D + 2LL * NSP + 2 * slot0,
-                 sbytes, bar);
+      const int rows = min(kProtUnit, p_ns - slot0);
+      const uint8_t* kc = p_src + (long long)slot0 * D;
+      const uint8_t* vc = p_src + (long long)(NS + slot0) * D;
+#pragma unroll
+      for (int k = 0; k < kProtUnit * D / 512; ++k) {
+        const int c = lane + 32 * k;
+        if (c < rows * (D / 16)) {
+          cp_async16(dst + 512u * k, kc + 512 * k + 16 * lane, 16u);
+          cp_async16(dst + kProtUnit * D + 512u * k, vc + 512 * k + 16 * lane, 16u);
+        }
+      }
+      const int runs = (rows + 7) / 8;  // 16-byte scale chunks
+      if (lane < 4 && (lane & 1) < runs) {
+        const int which = lane >> 1, c = lane & 1;  // K (0) or V (1) scales, chunk c
+        cp_async16(stages_s + (uint32_t)(st * SB) + 2 * kProtUnit * D + which * 2 * kProtUnit + 16 * c,
+                   p_src + 2LL * NS * D + which * 2LL * NSP + 2 * slot0 + 16 * c, 16u);
+      }
     }
   };
-  if (lane == 0) {
-    sm.prod[warp] = sm.cs;
-    p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
-    prod_next();
-    for (int st = 0; st < kSStages && p_more; ++st) {
-      issue(st);
-      p_j += kSW;
-      prod_next();
-    }
-  }
-  auto refill = [&](int st) {  // after the warp released stage st
-    __syncwarp();
-    if (lane == 0 && p_more) {
+  // After the warp consumed the unit in stage st: the next unit into it.
+  auto refill = [&](int st) {
+    __syncwarp();  // every lane is past its reads of stage st
+    if (p_more) {
       issue(st);
       p_j += kSW;
       if (p_j < p_hi) {  // fast path: next unit of the same segment
@@ -505,14 +530,25 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         prod_next();
       }
     }
+    cp_async_commit();
   };
+  if (lane == 0) sm.prod[warp] = sm.cs;
+  __syncwarp();
+  p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
+  prod_next();
+#pragma unroll 1
+  for (int st = 0; st < kSStages; ++st) {
+    if (p_more) {
+      issue(st);
+      p_j += kSW;
+      prod_next();
+    }
+    cp_async_commit();
+  }
 
   // ------------------------------------------------------ per-lane constants
   const int r = lane >> 2, qd = lane & 3;
-  const int jh = r & 3;                 // INT4 path: this lane's softmax head
-  const int g0 = r >> 2, g1 = g0 + 2;   // INT4 path: groups of QK rows r and r+8
-  const bool v0 = NG == 4 || g0 < NG, v1 = NG == 4 || g1 < NG;
-  const uint32_t p_keep = (r < 4) ? 0xFFFFFFFFu : 0u;
+  const uint32_t p_keep = (r < 4) ? 0xFFFFFFFFu : 0u;  // INT8 path: lanes of heads 0..3
   // INT4 V ldmatrix rows: matrix lane/8 = tokens (mi&1)*8.., piece mi>>1 (+2)
   const int lm_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
   const int lm_p = lane >> 4;
@@ -523,7 +559,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   const int l8_t = lane & 7, l8_row = ((lane >> 3) & 1) * 8 + l8_t, l8_pp = lane >> 4;
   constexpr int TK8[4] = {0, 1, 8, 9};  // INT8 unit: this lane's slots 2 * qd + TK8[e]
 
-  int it = 0;  // this warp's consumed units (stage it % 2, phase (it / 2) & 1)
+  int it = 0;  // stage of this warp's next unit (0 .. kSStages - 1)
   int pend_t = 0;  // thread 0: ticket value returned for the pending partial
   uint32_t qphase = 0;  // completed copies into sm.qraw
   if (threadIdx.x == kTicketThread) {
@@ -533,7 +569,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   }
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
   ++qphase;
-  stream_query_setup<NG>(sm);
+  stream_query_setup<NG>(sm, scale_log2);
   __syncthreads();
   // The current segment lives in sm.cs (advanced by the ticket thread between
   // the boundary barriers); the loop below keeps only what the units need.
@@ -576,31 +612,32 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
 
     if (cs.type == 1) {
       // ============================================= INT4 pages (eq. 5.1)
-      // Per unit of two pages.  QK^T: block-diagonal query rows against K
-      // codes widened with their exponent offset (1024 + c, 1024 + 16 c); the
-      // fragments carry the 1/16 and the accumulators start at minus the
-      // constant 1024-part, so each row sums q_d c_d over its group.  Scores
-      // by eq. 5.1 per group; one online-softmax step for both pages; then per
-      // page PV against the V codes with P' = p * Delta_v -- each code enters
-      // the MMA as the fp16 subnormal with its own bit pattern (c 2^-24, or
-      // 16 c 2^-24 for high nibbles: one logic op per pair, products exact),
-      // the accumulators scaled back when published -- and the offset term
-      // sum_t p_t m_t of every group as one more MMA whose A rows are the
-      // page's V metadata (group, Delta | m).
-      const uint4* qa_s = reinterpret_cast<const uint4*>(&sm.qp.qfrag4[0][0][0]) + lane;  // + 32 * s
-      float qs0 = 0.f, qs1 = 0.f;
+      // Per unit of two pages.  QK^T with the tokens as MMA rows: A = the K
+      // codes of the page's 16 tokens entered as fp16 subnormals (bit
+      // pattern = code: one logic op per pair of values), B = the scaled
+      // query fragments of the pair (in registers for the whole segment),
+      // one 32-channel block per two k-steps; accumulator set A holds blocks
+      // 0 and 1, set B blocks 2 and 3, so each lane ends with the four
+      // per-block sums of tokens r and r + 8 for head q.  Scores by eq. 5.1
+      // per group, one online-softmax step for both pages.  The probabilities
+      // are moved into the PV operand layout by two shuffles per page; per
+      // page PV against the transposed V codes (subnormals as well) with
+      // P' = p * Delta_v, and the offset term sum_t p_t m_t of every group as
+      // one more MMA whose A rows are the page's V offsets.  Units inside the
+      // region with both pages copied (all but a segment's first and last)
+      // skip every mask.
+      uint4 qbf[4];  // this lane's B fragments of the four blocks (lo b0, lo b1, hi b0, hi b1)
 #pragma unroll
-      for (int bq = 0; bq < D / 32; ++bq) {
-        if (v0 && (bq * 32) / GS == g0) qs0 += sm.qp.qsum[bq][jh];
-        if (v1 && (bq * 32) / GS == g1) qs1 += sm.qp.qsum[bq][jh];
-      }
-      const float kc0 = v0 ? sm.qp.kc[g0][jh] : 0.f;
-      const float kc1 = v1 ? sm.qp.kc[g1][jh] : 0.f;
+      for (int bl = 0; bl < 4; ++bl) qbf[bl] = sm.qp.qb[bl][lane];
+      float qsv[4];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) qsv[gg] = gg < NG ? sm.qp.qs[qd][gg] : 0.f;
+      const float ksc = sm.qp.ks[qd];
       const int first_page = rg.sink_end / kPage;
       const int len = cs.len;
       const int last_j = cs.n - 1;
-      float m_run = -INFINITY, l_run = 0.f;
-      float mtacc[4] = {0.f, 0.f, 0.f, 0.f};  // rows (group, Delta | m), columns heads
+      float m_run = -INFINITY, l_run = 0.f, m_thr = -INFINITY;  // m_thr = m_run + kLazyLog2
+      float mtacc[4] = {0.f, 0.f, 0.f, 0.f};  // rows = groups (V offsets), columns = heads
       float acc[4][2][4];
 #pragma unroll
       for (int G_ = 0; G_ < 4; ++G_)
@@ -608,189 +645,198 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
-      // per-lane shared addresses inside a stage (page p of a unit at + p * cb)
-      const uint32_t k_lane = smem_u32(my_stages) + r * 64 + row_byte(16 * qd, r, D);  // (+512: r + 8)
-      const uint32_t km_lane = smem_u32(my_stages) + meta_off_k(D) + (2 * qd * NG + g0) * 4;
-      const uint32_t vm_lane = smem_u32(my_stages) + meta_off_v(D, GS) + 2 * qd * NG * 4;
-      const int mt_g = r >> 1;                  // offset-term MMA: this lane's A row group
-      const bool mt_row = mt_g < NG;
-      const uint32_t mt_sel = (r & 1) ? 0x7632u : 0x5410u;  // Delta (low) or m (high) halves
-      const uint32_t v_lane = smem_u32(my_stages) + codes_off_v(D);
-      constexpr int TK[4] = {0, 1, 8, 9};      // this lane's tokens: 2 * qd + TK[e]
+      const int mrow = r < NG ? r : 0;  // offset-term MMA: this lane's A row group
+      // lane offsets inside a page chunk: K codes (row r, quarter q: one word
+      // per block), K meta of row r, this lane's quad of V Deltas (all
+      // groups) and of V offsets (group mrow)
+      const uint32_t kq_off = r * 64 + 16 * qd;
+      const uint32_t km_off = meta_off_k(D) + r * NG * 4;
+      const uint32_t vd_off = meta_off_v(D, GS) + qd * NG * 8;
+      const uint32_t vm_off = meta_off_v(D, GS) + 32 * NG + (qd * NG + mrow) * 8;
+      const uint32_t vc_off = codes_off_v(D);
+      // probabilities of tokens (r, r + 8) for head q, moved to the PV B
+      // layout (tokens 2 q' + {0, 1} and 2 q' + {8, 9} of head r'): the lanes
+      // holding tokens 2 q' and 2 q' + 1 for head r' (any value for r' > 3)
+      const int src_a = (8 * qd + r) & 31, src_b = (8 * qd + 4 + r) & 31;
 
       for (int jj = lo + warp; jj < hi; jj += kSW) {
-        const int ST = (int)((unsigned)it % kSStages);
-        const int SO = ST * SB;  // stage offset
-        const bool ok =
-            __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][ST], ((unsigned)it / kSStages) & 1));
-        if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
-        const int ph0 = sm.phys[warp][ST][0], ph1 = sm.phys[warp][ST][1];
-        if (ok) {
-          const int pg0 = first_page + kSPages * jj;
-          // ---------------- QK^T of both pages (k-step fragments shared)
-          uint4 kw[2][2];
+        const int ST = it;
+        const uint32_t sb = stages_s + (uint32_t)(ST * SB);
+        cp_async_wait<kSStages - 1>();  // this lane's copies of the unit
+        __syncwarp();        // ... and every other lane's
+        const uint32_t pv = (vbits >> (2 * ST)) & 3u;  // pages copied
+        const bool clean = (unsigned)(jj - 1) < (unsigned)(last_j - 1) && pv == 3u;
+        const int pg0 = first_page + kSPages * jj;
+        // ---------------- S = K codes x Q^T and scores (eq. 5.1 per group),
+        // log2 domain, relative to the running reference
+        const float mref = m_run == -INFINITY ? 0.f : m_run;
+        float sc[2][2];  // [page][token r | r + 8]
 #pragma unroll
-          for (int pp = 0; pp < 2; ++pp) {
-            kw[pp][0] = lds128(k_lane + SO + pp * cb);
-            kw[pp][1] = lds128(k_lane + SO + pp * cb + 512);
+        for (int pp = 0; pp < 2; ++pp) {
+          const uint32_t pb = sb + pp * cb;
+          const uint4 w0 = lds128(pb + kq_off), w1 = lds128(pb + kq_off + 512);
+          float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int bl = 0; bl < 4; ++bl) {
+            uint32_t x0[4], x1[4];
+            widen_v_sub(u4word(w0, bl), x0);
+            widen_v_sub(u4word(w1, bl), x1);
+            float* d = bl < 2 ? sA : sB;
+            mma_f16(d, x0[0], x1[0], x0[2], x1[2], qbf[bl].x, qbf[bl].y);
+            mma_f16(d, x0[1], x1[1], x0[3], x1[3], qbf[bl].z, qbf[bl].w);
           }
-          float d[2][2][4];  // [page][tokens 0-7 | 8-15][accumulator]
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            MetaRow<NG> km;
+            km.load_s(pb + km_off + e * 8 * NG * 4);
+            // block sums of this token: blocks 0, 1 in set A, 2, 3 in set B
+            const float s0 = sA[2 * e], s1 = sA[2 * e + 1];
+            const float s2 = sB[2 * e], s3 = sB[2 * e + 1];
+            float dsum, msum = -mref;
+            if (NG == 4) {
+              const float2 g0 = h2f2(km.get(0)), g1 = h2f2(km.get(1));
+              const float2 g2 = h2f2(km.get(2)), g3 = h2f2(km.get(3));
+              dsum = fmaf(g3.x, s3, fmaf(g2.x, s2, fmaf(g1.x, s1, g0.x * s0)));
+              msum = fmaf(g3.y, qsv[3], fmaf(g2.y, qsv[2], fmaf(g1.y, qsv[1], fmaf(g0.y, qsv[0], msum))));
+            } else if (NG == 2) {
+              const float2 g0 = h2f2(km.get(0)), g1 = h2f2(km.get(1));
+              dsum = fmaf(g1.x, s2 + s3, g0.x * (s0 + s1));
+              msum = fmaf(g1.y, qsv[1], fmaf(g0.y, qsv[0], msum));
+            } else {
+              const float2 g0 = h2f2(km.get(0));
+              dsum = g0.x * ((s0 + s1) + (s2 + s3));
+              msum = fmaf(g0.y, qsv[0], msum);
+            }
+            sc[pp][e] = fmaf(ksc, dsum, msum);
+          }
+        }
+        if (!clean) {  // first / last unit of the segment, or a page not copied: mask
 #pragma unroll
           for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2) {
-              d[pp][t2][0] = d[pp][t2][1] = -kc0;
-              d[pp][t2][2] = d[pp][t2][3] = -kc1;
+            for (int e = 0; e < 2; ++e) {
+              const int pos = (pg0 + pp) * kPage + r + 8 * e;
+              const bool in = ((pv >> pp) & 1u) && pos >= rg.sink_end && pos < rg.rec_start;
+              if (!in) sc[pp][e] = -INFINITY;
             }
+        }
+        // ---------------- online softmax for head q over both pages.  Lazy
+        // rescaling: the reference m_run moves only when a score exceeds it
+        // by more than kLazyLog2 (p then stays below 2^kLazyLog2).
+        const float tmax = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) + mref;
+        if (__any_sync(0xffffffffu, tmax > m_thr)) {
+          float hm = tmax;  // the head's maximum over the warp's 32 tokens
+          hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 4));
+          hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 8));
+          hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
+          const float mnew = fmaxf(m_run, hm);
+          const float alpha = mnew == -INFINITY ? 1.f : ex2(m_run - mnew);
+          // PV accumulators of this lane: heads 2 q and 2 q + 1 (columns)
+          const float aA = __shfl_sync(0xffffffffu, alpha, (2 * qd) & 3);
+          const float aB = __shfl_sync(0xffffffffu, alpha, (2 * qd + 1) & 3);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 qa0 = qa_s[32 * (2 * u)], qa1 = qa_s[32 * (2 * u + 1)];
+          for (int G_ = 0; G_ < 4; ++G_)
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-              uint32_t x0[4], x1[4];
-              if (fold_k_offset<NG>()) {
-                widen_k_biased(u4word(kw[pp][0], u), x0);
-                widen_k_biased(u4word(kw[pp][1], u), x1);
-              } else {
-                widen_k(u4word(kw[pp][0], u), x0);
-                widen_k(u4word(kw[pp][1], u), x1);
-              }
-              mma_f16(d[pp][0], qa0.x, qa0.y, qa0.z, qa0.w, x0[0], x0[1]);
-              mma_f16(d[pp][1], qa0.x, qa0.y, qa0.z, qa0.w, x1[0], x1[1]);
-              mma_f16(d[pp][0], qa1.x, qa1.y, qa1.z, qa1.w, x0[2], x0[3]);
-              mma_f16(d[pp][1], qa1.x, qa1.y, qa1.z, qa1.w, x1[2], x1[3]);
+            for (int hh = 0; hh < 2; ++hh) {
+              acc[G_][hh][0] *= aA;
+              acc[G_][hh][1] *= aB;
+              acc[G_][hh][2] *= aA;
+              acc[G_][hh][3] *= aB;
             }
-          }
-          // ---------------- scores (eq. 5.1 per group) of this lane's 8 tokens
-          float sc[2][4];
+          mtacc[0] *= aA;
+          mtacc[1] *= aB;
+          l_run *= alpha;
+          const float shift = mnew == -INFINITY ? 0.f : mnew - mref;  // new reference vs old
 #pragma unroll
           for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float raw0 = e < 2 ? d[pp][0][e] : d[pp][1][e - 2];      // row r   (group g0)
-              const float raw1 = e < 2 ? d[pp][0][e + 2] : d[pp][1][e];      // row r+8 (group g1)
-              float part = 0.f;
-              if (v0) {
-                const float2 dm = h2f2(lds32(km_lane + SO + pp * cb + TK[e] * NG * 4));
-                part = fmaf(dm.x, raw0, dm.y * qs0);
-              }
-              if (v1) {
-                const float2 dm = h2f2(lds32(km_lane + SO + pp * cb + TK[e] * NG * 4 + 8));
-                part += fmaf(dm.x, raw1, dm.y * qs1);
-              }
-              part += __shfl_xor_sync(0xffffffffu, part, 16);
-              sc[pp][e] = part * scale_log2;
-            }
-          // first / last unit of the segment, or a page not loaded: mask
-          if (jj == 0 || jj == last_j || ph0 < 0 || ph1 < 0) {
+            for (int e = 0; e < 2; ++e) sc[pp][e] -= shift;
+          m_run = mnew;
+          m_thr = mnew + kLazyLog2;
+        }
+        float pr_[2][2];
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp)
+        for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int pos = (pg0 + pp) * kPage + 2 * qd + TK[e];
-                const bool in = (pp == 0 ? ph0 : ph1) >= 0 && pos >= rg.sink_end && pos < rg.rec_start;
-                if (!in) sc[pp][e] = -INFINITY;
-              }
+          for (int e = 0; e < 2; ++e) pr_[pp][e] = ex2(sc[pp][e]);  // masked: 0
+        l_run += (pr_[0][0] + pr_[0][1]) + (pr_[1][0] + pr_[1][1]);
+        // ---------------- PV, one page at a time
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          if (!clean && !((pv >> pp) & 1u)) continue;  // not copied: all its p are 0
+          const uint32_t pb = sb + pp * cb;
+          // p of tokens 2 q + {0, 1} (b0) and 2 q + {8, 9} (b1), head r
+          const uint32_t ph = pack_f16(pr_[pp][0], pr_[pp][1]);
+          const uint32_t hA = __shfl_sync(0xffffffffu, ph, src_a);
+          const uint32_t hB = __shfl_sync(0xffffffffu, ph, src_b);
+          const uint32_t p01 = __byte_perm(hA, hB, 0x5410);
+          const uint32_t p23 = __byte_perm(hA, hB, 0x7632);
+          uint32_t va[4], vb[4];
+          ldsm_x4_trans(va, pb + vc_off + lm_off0);
+          ldsm_x4_trans(vb, pb + vc_off + lm_off1);
+          // V Deltas of the lane's four tokens, words (t0, t1), (t2, t3) per group
+          uint32_t dl[4][2];
+          if (NG == 4) {
+            const uint4 a = lds128(pb + vd_off), b = lds128(pb + vd_off + 16);
+            dl[0][0] = a.x; dl[0][1] = a.y; dl[1][0] = a.z; dl[1][1] = a.w;
+            dl[2][0] = b.x; dl[2][1] = b.y; dl[3][0] = b.z; dl[3][1] = b.w;
+          } else if (NG == 2) {
+            const uint4 a = lds128(pb + vd_off);
+            dl[0][0] = a.x; dl[0][1] = a.y; dl[1][0] = a.z; dl[1][1] = a.w;
+          } else {
+            const uint2 a = lds64(pb + vd_off);
+            dl[0][0] = a.x; dl[0][1] = a.y;
           }
-          // ---------------- online softmax for head jh over both pages
-          float tmax = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
-                             fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-          // lazy rescaling: the reference m_run moves only when a score
-          // exceeds it by more than kLazyLog2 (p then stays below 2^kLazyLog2)
-          if (__any_sync(0xffffffffu, tmax > m_run + kLazyLog2)) {
-            const float mnew = fmaxf(m_run, tmax);
-            const float alpha = mnew == -INFINITY ? 1.f : ex2(m_run - mnew);
-            const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
-            const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
+          uint2 mw = lds64(pb + vm_off);  // V offsets of group mrow, same tokens
+          if (!clean && (pg0 + pp + 1) * kPage > len) {
+            // slots at or past the length were never written: zero their metadata
+            const int p0 = (pg0 + pp) * kPage + 2 * qd;
+            const uint32_t k0 = (p0 < len ? 0x0000FFFFu : 0u) | (p0 + 1 < len ? 0xFFFF0000u : 0u);
+            const uint32_t k1 = (p0 + 8 < len ? 0x0000FFFFu : 0u) | (p0 + 9 < len ? 0xFFFF0000u : 0u);
 #pragma unroll
-            for (int G_ = 0; G_ < 4; ++G_)
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                acc[G_][hh][0] *= aA;
-                acc[G_][hh][1] *= aB;
-                acc[G_][hh][2] *= aA;
-                acc[G_][hh][3] *= aB;
-              }
-            mtacc[0] *= aA;
-            mtacc[1] *= aB;
-            l_run *= alpha;
-            m_run = mnew;
+            for (int gg = 0; gg < NG; ++gg) {
+              dl[gg][0] &= k0;
+              dl[gg][1] &= k1;
+            }
+            mw.x &= k0;
+            mw.y &= k1;
           }
-          const float mref = m_run == -INFINITY ? 0.f : m_run;
-          float pr_[2][4];
+          // offset term: rows = groups (their m), columns = heads, against p
+          mma_f16(mtacc, mw.x, 0u, mw.y, 0u, p01, p23);
 #pragma unroll
-          for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pr_[pp][e] = ex2(sc[pp][e] - mref);  // masked: 0
-          l_run += ((pr_[0][0] + pr_[0][1]) + (pr_[0][2] + pr_[0][3])) +
-                   ((pr_[1][0] + pr_[1][1]) + (pr_[1][2] + pr_[1][3]));
-          // ---------------- PV, one page at a time
-#pragma unroll
-          for (int pp = 0; pp < 2; ++pp) {
-            if ((pp == 0 ? ph0 : ph1) < 0) continue;  // not loaded: all its p are 0
-            MetaRow<NG> vm[4];
-            uint32_t mw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              vm[e].load_s(vm_lane + SO + pp * cb + TK[e] * NG * 4);
-              mw[e] = mt_row ? lds32(vm_lane + SO + pp * cb + TK[e] * NG * 4 + mt_g * 4) : 0u;
-            }
-            uint32_t va[4], vb[4];
-            ldsm_x4_trans(va, v_lane + SO + pp * cb + lm_off0);
-            ldsm_x4_trans(vb, v_lane + SO + pp * cb + lm_off1);
-            if ((pg0 + pp + 1) * kPage > len) {  // slots at or past the length were never written
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if ((pg0 + pp) * kPage + 2 * qd + TK[e] >= len) {
-                  vm[e].zero();
-                  mw[e] = 0u;
-                }
-            }
-            const uint32_t p01 = pack_f16(pr_[pp][0], pr_[pp][1]) & p_keep;
-            const uint32_t p23 = pack_f16(pr_[pp][2], pr_[pp][3]) & p_keep;
-            // offset term: rows (group, Delta | m) x tokens, against p
-            mma_f16(mtacc, __byte_perm(mw[0], mw[1], mt_sel), 0u, __byte_perm(mw[2], mw[3], mt_sel),
-                    0u, p01, p23);
-#pragma unroll
-            for (int P = 0; P < 4; ++P) {
-              const int grp = (P * 32) / GS;
-              const uint32_t b0 = hmul2(p01, lo_lo(vm[0].get(grp), vm[1].get(grp)));
-              const uint32_t b1 = hmul2(p23, lo_lo(vm[2].get(grp), vm[3].get(grp)));
-              const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
-              const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
-              uint32_t xl[4], xh[4];
-              widen_v_sub(wlo, xl);
-              widen_v_sub(whi, xh);
-              mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
-              mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
-            }
+          for (int P = 0; P < 4; ++P) {
+            const int grp = (P * 32) / GS;
+            const uint32_t b0 = hmul2(p01, dl[grp][0]);
+            const uint32_t b1 = hmul2(p23, dl[grp][1]);
+            const uint32_t wlo = (P < 2) ? va[2 * P] : vb[2 * (P - 2)];
+            const uint32_t whi = (P < 2) ? va[2 * P + 1] : vb[2 * (P - 2) + 1];
+            uint32_t xl[4], xh[4];
+            widen_v_sub(wlo, xl);
+            widen_v_sub(whi, xh);
+            mma_f16(acc[P][0], xl[0], xl[1], xh[0], xh[1], b0, b1);
+            mma_f16(acc[P][1], xl[2], xl[3], xh[2], xh[3], b0, b1);
           }
         }
         refill(ST);
-        ++it;
+        it = it + 1 == kSStages ? 0 : it + 1;
       }
 
-      // publish this warp's state
-      float lsum = (r < 4) ? l_run : 0.f;
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-      if (qd == 0 && r < 4) {
-        sm.mrg_m[warp][jh] = m_run;
-        sm.mrg_l[warp][jh] = lsum;
+      // publish this warp's state: head q's running max and sum over the
+      // lanes of rows r = 0..7 (lane q holds the totals)
+      float lsum = l_run;
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+      if (r == 0) {
+        sm.mrg_m[warp][qd] = m_run;
+        sm.mrg_l[warp][qd] = lsum;
       }
-      // offset term of group g, heads 2qd, 2qd+1: sum p m (row 2g + 1, in lane
-      // 8g + 4 + qd; row 2g, sum p Delta, is not needed with uncentred codes)
-      {
-        const float om0 = __shfl_xor_sync(0xffffffffu, mtacc[0], 4);
-        const float om1 = __shfl_xor_sync(0xffffffffu, mtacc[1], 4);
-        if ((r & 1) == 0 && mt_row && qd < 2) {
-          const float tA = om0, tB = om1;
-          for (int blk = mt_g * (GS / 32); blk < (mt_g + 1) * (GS / 32); ++blk) {
-            sm.mrg_mt[warp][2 * qd][blk] = tA;
-            sm.mrg_mt[warp][2 * qd + 1][blk] = tB;
-          }
+      // offset term of group g (row g, in lanes 4 g + q): sum_t p m for heads
+      // 2 q and 2 q + 1
+      if (r < NG && qd < 2) {
+        for (int blk = r * (GS / 32); blk < (r + 1) * (GS / 32); ++blk) {
+          sm.mrg_mt[warp][2 * qd][blk] = mtacc[0];
+          sm.mrg_mt[warp][2 * qd + 1][blk] = mtacc[1];
         }
       }
       if (qd < 2) {
@@ -822,13 +868,12 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
       const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
-      for (int jj = lo + warp; jj < hi; jj += kSW, ++it) {
-        const int st = (int)((unsigned)it % kSStages);
-        const bool ok =
-            __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], ((unsigned)it / kSStages) & 1));
-        if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
+      for (int jj = lo + warp; jj < hi; jj += kSW, it = it + 1 == kSStages ? 0 : it + 1) {
+        const int st = it;
+        cp_async_wait<kSStages - 1>();  // this lane's copies of the unit
+        __syncwarp();        // ... and every other lane's
         const uint32_t stg = smem_u32(my_stages) + st * SB;
-        if (ok) {
+        {
           const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
           // a sequence of at least S + R tokens fills every sink and ring slot:
           // only a unit reaching into the padding past NS needs the test
@@ -952,7 +997,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0)
         set_status(status, KV4_STATUS_TIMEOUT);
       ++qphase;
-      stream_query_setup<NG>(sm);
+      stream_query_setup<NG>(sm, scale_log2);
     }
     __syncthreads();  // B2: partial stored; next pair's query set up; comb, cs written
     if (threadIdx.x == kTicketThread && !defer) {
@@ -968,6 +1013,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
                      out_lse);
     }
   }
+  cp_async_wait<0>();  // (every group left is empty: the warp consumed every unit it copied)
   // the last partial's ticket
   __syncthreads();
   if (threadIdx.x == kTicketThread) {
@@ -1165,7 +1211,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   constexpr size_t smem =
       ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kSW * kSStages * kSPages * cb;
   // four CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
-  static_assert(smem <= 228 * 1024 / kStreamMinBlocks - 1024, "shared memory for 4 CTAs per SM");
+  static_assert(smem <= 228 * 1024 / kStreamMinBlocks - 1024, "shared memory per CTA");
   // once per device: the shared-memory attribute and the resident-CTA capacity
   static OnceSetup setup;
   int grid = 0;

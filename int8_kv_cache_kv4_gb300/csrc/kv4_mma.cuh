@@ -138,12 +138,34 @@ __device__ inline void widen_k(uint32_t w, uint32_t x[4]) {
   x[3] = hfma2(and_or(w8, 0x00F000F0u, 0x64006400u), kSixteenth2, kM64);
 }
 
+// (Delta, m) of V for slot t and group grp of a chunk, as one word (Delta in
+// the low half), gathered from the V metadata's two arrays.
+__device__ inline uint32_t vmeta_word(const uint8_t* chunk, int t, int grp, int d_h, int g) {
+  return (uint32_t)*reinterpret_cast<const uint16_t*>(chunk + v_delta_byte(t, grp, d_h, g)) |
+         ((uint32_t)*reinterpret_cast<const uint16_t*>(chunk + v_offset_byte(t, grp, d_h, g))
+          << 16);
+}
+// The four words of a K code row that hold block blk (channels 32 blk ..
+// 32 blk + 31), in channel order.
+__device__ inline uint4 k_block_words(const uint8_t* row, int blk, int d_h) {
+  uint4 w;
+  w.x = *reinterpret_cast<const uint32_t*>(row + k_row_byte(32 * blk, d_h));
+  w.y = *reinterpret_cast<const uint32_t*>(row + k_row_byte(32 * blk + 8, d_h));
+  w.z = *reinterpret_cast<const uint32_t*>(row + k_row_byte(32 * blk + 16, d_h));
+  w.w = *reinterpret_cast<const uint32_t*>(row + k_row_byte(32 * blk + 24, d_h));
+  return w;
+}
+
 template <int NG>
 struct MetaRow;  // one slot's NG (Delta, m) words
 template <>
 struct MetaRow<4> {
   uint4 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ void load_v(const uint8_t* c, int t, int d_h) {
+    v = make_uint4(vmeta_word(c, t, 0, d_h, d_h / 4), vmeta_word(c, t, 1, d_h, d_h / 4),
+                   vmeta_word(c, t, 2, d_h, d_h / 4), vmeta_word(c, t, 3, d_h, d_h / 4));
+  }
   __device__ void load_s(uint32_t a) { v = lds128(a); }
   __device__ uint32_t get(int g) const { return u4word(v, g); }
   __device__ void zero() { v = make_uint4(0u, 0u, 0u, 0u); }
@@ -152,6 +174,9 @@ template <>
 struct MetaRow<2> {
   uint2 v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ void load_v(const uint8_t* c, int t, int d_h) {
+    v = make_uint2(vmeta_word(c, t, 0, d_h, d_h / 2), vmeta_word(c, t, 1, d_h, d_h / 2));
+  }
   __device__ void load_s(uint32_t a) { v = lds64(a); }
   __device__ uint32_t get(int g) const { return g == 0 ? v.x : v.y; }
   __device__ void zero() { v = make_uint2(0u, 0u); }
@@ -160,6 +185,7 @@ template <>
 struct MetaRow<1> {
   uint32_t v;
   __device__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ void load_v(const uint8_t* c, int t, int d_h) { v = vmeta_word(c, t, 0, d_h, d_h); }
   __device__ void load_s(uint32_t a) { v = lds32(a); }
   __device__ uint32_t get(int) const { return v; }
   __device__ void zero() { v = 0u; }

@@ -17,13 +17,6 @@ constexpr int kProtUnit = 16;       // side-cache slots per protected unit
 // and the accumulators are rescaled on a few pages only.  The split's
 // log-normaliser m + log2(l) is exact for any reference.
 constexpr float kLazyLog2 = 8.f;
-// INT4 QK^T with the codes' exponent offset folded into the query side
-// (1024 + c against q, 1024 + 16 c against q / 16, accumulators started at
-// minus the constant part): exact-enough only while a group's constant part
-// (1024 x the sum of its query values) stays small, i.e. for 32-channel
-// groups; larger groups widen the codes to their exact values instead.
-template <int NG>
-__host__ __device__ constexpr bool fold_k_offset() { return NG >= 4; }
 // One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
 struct Seg {
   long long start;  // stream index of its first unit
@@ -116,86 +109,101 @@ __device__ inline bool slot_valid(int sl, int len, const Layout& L, int ws_mod, 
   return d < n_rec;
 }
 
-// A query element (bf16 bits) as fp16 bits, optionally divided by 16 (the
-// same two roundings wherever the value is used).
-__device__ inline uint32_t q16(uint32_t bf, bool sixteenth) {
-  __half h = __float2half_rn(bf16_bits_to_f32(bf));
-  if (sixteenth) h = __float2half_rn(__half2float(h) * 0.0625f);
-  return __half_as_ushort(h);
+// A query element (bf16 bits) as fp16 bits (the INT8 units' query operand).
+__device__ inline uint32_t q16(uint32_t bf) {
+  return __half_as_ushort(__float2half_rn(bf16_bits_to_f32(bf)));
+}
+// bf16 bits times 2^e (exact in fp32) as fp16 bits, rounded to nearest even.
+__device__ inline uint32_t q16_scaled(uint32_t bf, float two_e) {
+  return __half_as_ushort(__float2half_rn(bf16_bits_to_f32(bf) * two_e));
 }
 
 // One pair's query in the forms the tensor-core units use (16-byte
 // multiple, so that it can be bulk-copied).
+//
+// INT4 units compute S = K_codes x Q^T with the tokens as MMA rows (A = the K
+// codes of 16 tokens, entered as fp16 subnormals whose bit pattern is the
+// code) and the query as B, one 32-channel block per pair of k-steps.  B's
+// eight columns are (head j, parity p) = (n >> 1, n & 1): block b contributes
+// to the columns of parity b & 1 only, so that one accumulator holds two
+// blocks and every lane ends with the four blocks of one head.  Lane
+// (r', q') (lane = 4 r' + q') of block b holds, for head j = r' >> 1 when
+// b & 1 == r' & 1 (else zeros), the channels c0 = 32 b + 8 q':
+//   lo k-step: (16 q~[c0], 16 q~[c0 + 4]), (16 q~[c0 + 2], 16 q~[c0 + 6])
+//   hi k-step: (q~[c0 + 1], q~[c0 + 5]),   (q~[c0 + 3], q~[c0 + 7])
+// matching the widened code words (low nibbles c 2^-24, high nibbles
+// 16 c 2^-24), so every product is q~ c 2^-20.  q~ = q 2^e_j is the head's
+// query scaled by a power of two that puts max |q~| in [2^10, 2^11): exact,
+// inside fp16's normal range for all but negligible elements, and 16 q~ below
+// fp16's largest value.  The score of token t for head j (log2 domain) is then
+//   s = ks[j] * sum_b Delta_(t, group(b)) S_(t, j, b) + sum_g m_(t, g) qs[j][g]
+// with ks[j] = scale_log2 2^20 2^-e_j and qs[j][g] = scale_log2 sum_(d in g) q_d
+// (eq. 5.1 per group).
 struct __align__(16) QPrep {
-  uint32_t qfrag4[8][32][4];  // INT4 path: block-diagonal query fragments per k-step and lane
+  uint4 qb[4][32];            // INT4 path: B fragments [block][lane]: lo b0, lo b1, hi b0, hi b1
   uint2 qfrag8[8][16];        // INT8 path: query fragments (a0, a2) of lanes 0..15
-  float qsum[SD / 32][SG];    // per 32-channel block sums of the query
-  float kc[4][SG];            // per (group, head): the constant part of the INT4 QK sums
+  float qs[SG][4];            // [head][group]: scale_log2 x the group's query sum (fp32)
+  float ks[SG];               // [head]: scale_log2 x 2^20 x 2^-e_head
 };
 static_assert(sizeof(QPrep) % 16 == 0, "QPrep is copied in 16-byte units");
 
 // Everything the units of one pair need from its query (qr: G rows of D
-// bf16), built by 128 threads (t = thread index): per-32-channel-block sums,
-// both fragment sets, and per (group, head) the constant 1024-part of the
-// INT4 QK sums.
+// bf16), built by 128 threads (t = thread index; warp j builds head j's
+// entries: its exponent, group sums and B fragments, then a share of the
+// INT8 fragments).
 template <int NG>
-__device__ inline void build_qprep(const uint16_t* qr, QPrep& qp, int t) {
+__device__ inline void build_qprep(const uint16_t* qr, QPrep& qp, int t, float scale_log2) {
   constexpr int GS = SD / NG;
-  {
-    // warp j: head j, lane: channels 4 * lane .. + 3
-    const int jj = t >> 5, ln = t & 31;
-    const uint2 raw = reinterpret_cast<const uint2*>(qr)[t];
-    const uint32_t b[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-    float sq = 0.f, sa = 0.f;
+  const int j = t >> 5, ln = t & 31;
+  // lane ln of warp j: channels 4 ln .. 4 ln + 3 of head j
+  const uint2 raw = reinterpret_cast<const uint2*>(qr + j * SD)[ln];
+  const uint32_t b4[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+  float mx = 0.f, sq = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      sq += bf16_bits_to_f32(b[i]);
-      sa += __half2float(__ushort_as_half((unsigned short)q16(b[i], i & 1)));
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-#pragma unroll
-    for (int o = 1; o < GS / 4; o <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, o);
-    if ((ln & 7) == 0) qp.qsum[ln >> 3][jj] = sq;
-    if ((ln % (GS / 4)) == 0) qp.kc[ln / (GS / 4)][jj] = fold_k_offset<NG>() ? 1024.f * sa : 0.f;
+  for (int i = 0; i < 4; ++i) {
+    const float v = bf16_bits_to_f32(b4[i]);
+    sq += v;
+    mx = fmaxf(mx, fabsf(v));
   }
-  // INT4 fragments: A rows (group, head), block diagonal; k-index order as the
-  // widened K words produce it.  The B values are 1024 + c for even channels
-  // (low nibbles) and 1024 + 16 c for odd ones (high nibbles, k-indices 8..15
-  // of each step, A registers 2 and 3), so the odd channels' query values are
-  // stored divided by 16 (exact in fp16 for |q| >= 2^-10).
-  {
-    // thread t (< 128) fills word k of lane ln at every k-step: row (group,
-    // head) and the channel block are the same at every step
-    const int ln = (t >> 2) & 31, k = t & 3;
-    const int rr = ln >> 2, qq = ln & 3;
-    const int row = rr + 8 * (k & 1);
-    const int grp = row >> 2, jj = row & 3;
-    // the step's channels 32 qq + [0, 32) lie in group (32 qq) / GS
-    const bool in_group = grp < NG && (32 * qq) / GS == grp;
-    const bool sixteenth = fold_k_offset<NG>() && (k & 2);
-    const uint16_t* qrow = qr + jj * SD + 32 * qq + ((k & 2) ? 1 : 0);
 #pragma unroll
-    for (int s_ = 0; s_ < 8; ++s_) {
-      const int off = 8 * (s_ >> 1) + 2 * (s_ & 1);  // channels off and off + 4 of the block
-      uint32_t w = 0u;
-      if (in_group)
-        w = q16(qrow[off], sixteenth) | (q16(qrow[off + 4], sixteenth) << 16);
-      qp.qfrag4[s_][ln][k] = w;
+  for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+  for (int o = 1; o < GS / 4; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  // e_j: max |q| 2^e in [2^10, 2^11); a zero or non-finite head keeps e = 0
+  int e = 0;
+  if (mx > 0.f && mx <= 3.0e38f) {
+    const int ex = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2 mx), normal mx
+    e = min(40, max(-20, 10 - max(ex, -126)));
+  }
+  const float two_e = __int_as_float((127 + e) << 23);
+  if ((ln % (GS / 4)) == 0) qp.qs[j][ln / (GS / 4)] = scale_log2 * sq;
+  if (ln == 0) qp.ks[j] = scale_log2 * __int_as_float((127 + 20 - e) << 23);
+  {
+    // thread ln of warp j: lane (r', q') = (2 j + (ln >> 4), (ln >> 2) & 3), block ln & 3
+    const int rp = 2 * j + (ln >> 4), qp_ = (ln >> 2) & 3, blk = ln & 3;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if ((blk & 1) == (rp & 1)) {
+      const uint16_t* c0 = qr + j * SD + 32 * blk + 8 * qp_;
+      const float two_e4 = two_e * 16.f;
+      w.x = q16_scaled(c0[0], two_e4) | (q16_scaled(c0[4], two_e4) << 16);
+      w.y = q16_scaled(c0[2], two_e4) | (q16_scaled(c0[6], two_e4) << 16);
+      w.z = q16_scaled(c0[1], two_e) | (q16_scaled(c0[5], two_e) << 16);
+      w.w = q16_scaled(c0[3], two_e) | (q16_scaled(c0[7], two_e) << 16);
     }
+    qp.qb[blk][4 * rp + qp_] = w;
   }
   // INT8 fragments: A rows = heads 0..3; k-step s, lane quad qd covers
   // channels 32*qd + 4*s + {0,1} (a0) and + {2,3} (a2)
   // (lanes 16..31, rows 4..7, read lane - 16's words: they duplicate heads
   // 0..3, whose results those lanes never publish)
   for (int idx = t; idx < 8 * 16; idx += 128) {
-    const int s_ = idx >> 4, ln = idx & 15;
-    const int rr = ln >> 2, qq = ln & 3;
+    const int s_ = idx >> 4, l2 = idx & 15;
+    const int rr = l2 >> 2, qq = l2 & 3;
     const uint16_t* src = qr + rr * SD + 32 * qq + 4 * s_;
     uint2 w;
-    w.x = q16(src[0], false) | (q16(src[1], false) << 16);
-    w.y = q16(src[2], false) | (q16(src[3], false) << 16);
-    qp.qfrag8[s_][ln] = w;
+    w.x = q16(src[0]) | (q16(src[1]) << 16);
+    w.y = q16(src[2]) | (q16(src[3]) << 16);
+    qp.qfrag8[s_][l2] = w;
   }
 }
 

@@ -20,7 +20,7 @@
  *   - INT8 scale = max|x| / 127 per token-head (course page "KV cache
  *     quantization", INT8 per-token-head write path)
  *
- * Readings where the pages leave a step open (each also listed in the design doc):
+ * Readings where the pages leave a step open:
  *   R1 group size g is a parameter (the paper deploys 128; its ablation uses 32).
  *   R2 Delta and m come from the group min/max (asymmetric).  m is the FP16 value
  *      rounded DOWN from the min; Delta is the FP16 value rounded UP from
@@ -300,15 +300,22 @@ void kv4o_hadamard_f32_n(float* x, long rows, int n) {
  *
  *   paged cache = [num_pages][h_kv][chunk], chunk bytes = 16*d_h + 128*(d_h/g)
  *   (page size 16), and inside one chunk:
- *     K codes  [16 slots][d_h/2 bytes]   logical byte i of a slot row holds
+ *     K codes  [16 slots][d_h/2 bytes]   a byte holds two consecutive channels,
+ *                                        the even one in its low nibble; a slot
+ *                                        row is 4 quarters q = 0..3 of d_h/32
+ *                                        four-byte words, and word b of quarter
+ *                                        q holds channels 32b + 8q .. 32b + 8q + 7
+ *                                        in increasing byte order
+ *     V codes  [16 slots][d_h/2 bytes]   logical byte i of a slot row holds
  *                                        channel 2i in its low nibble and channel
  *                                        2i+1 in its high nibble; the row is cut
  *                                        into 16-byte pieces of 32 channels and
  *                                        piece P of slot t is stored at piece
  *                                        position P xor ((t / 2) mod (d_h / 32))
- *     V codes  [16 slots][d_h/2 bytes]   same as K
  *     K meta   [16 slots][d_h/g][2 x u16] (Delta16, m16) per group
- *     V meta   [16 slots][d_h/g][2 x u16]
+ *     V Delta  [4 quads][d_h/g][4 x u16]  Delta16 of (slot, group); quad u lists
+ *                                        slots 2u, 2u+1, 2u+8, 2u+9 in that order
+ *     V m      [4 quads][d_h/g][4 x u16]  m16, same order
  *
  *   side cache = [max_seqs][h_kv][block], NS = S + R, NSP = NS rounded up to
  *   a multiple of 8, block bytes = 2*NS*d_h + 4*NSP, and inside one block:
@@ -373,17 +380,32 @@ int kv4o_quant_append(int h_kv, int d_h, int g, int S, int R, int max_seqs, int 
         for (int d = 0; d < d_h; ++d) x[d] = kv4o_bf16_to_f32(src[d]);
         if (rotate_k && kv == 0) kv4o_hadamard_f32(x, d_h);
         uint8_t* rows = chunk + (long)kv * 16 * (d_h / 2) + (long)slot * (d_h / 2);
-        uint8_t* meta = chunk + 16L * d_h + (long)kv * 16 * ng * 4 + (long)slot * ng * 4;
         for (int j = 0; j < ng; ++j) {
           uint16_t d16, m16;
           status |= kv4o_int4_encode_group(x + j * g, g, c4 + j * g, &d16, &m16);
-          put_u16(meta + 4 * j, d16);
-          put_u16(meta + 4 * j + 2, m16);
+          if (kv == 0) {
+            uint8_t* meta = chunk + 16L * d_h + (long)slot * ng * 4 + 4 * j;
+            put_u16(meta, d16);
+            put_u16(meta + 2, m16);
+          } else {
+            /* quad of the slot, its place among the quad's 4 entries */
+            int quad = (slot % 8) / 2, at = 2 * (slot / 8) + slot % 2;
+            long entry = ((long)quad * ng + j) * 4 + at;
+            uint8_t* vmeta = chunk + 16L * d_h + 64L * ng;
+            put_u16(vmeta + 2 * entry, d16);
+            put_u16(vmeta + 32L * ng + 2 * entry, m16);
+          }
         }
         int npieces = d_h / 32;
         for (int i = 0; i < d_h / 2; ++i) {
-          int piece = i / 16, within = i % 16;
-          int dst = 16 * (piece ^ ((slot / 2) % npieces)) + within;
+          int dst;
+          if (kv == 0) {
+            int ch = 2 * i, blk = ch / 32, quarter = (ch % 32) / 8;
+            dst = 4 * (quarter * npieces + blk) + (ch % 8) / 2;
+          } else {
+            int piece = i / 16, within = i % 16;
+            dst = 16 * (piece ^ ((slot / 2) % npieces)) + within;
+          }
           rows[dst] = (uint8_t)(c4[2 * i] | (c4[2 * i + 1] << 4));
         }
         if (prot) {

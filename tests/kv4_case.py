@@ -9,7 +9,7 @@ import numpy as np
 import oracle
 from int8_kv_cache_kv4_gb300 import workloads as W
 
-# spec tolerance for bf16 attention outputs against the fp64 oracle
+# stated tolerance for bf16 attention outputs against the fp64 oracle
 MAX_ABS = 2e-3
 MEAN_ABS = 2e-4
 LSE_ABS = 1e-3   # fp32 scores and normaliser vs fp64

@@ -176,10 +176,16 @@ def test_rollout_batch256_100_steps():
     d, ng = w.d_h, w.d_h // w.group
     row, meta = d // 2, 4 * ng
 
-    def rel(slot):  # byte offsets of one slot inside a chunk: K row, V row, K meta, V meta
+    def rel(slot):
+        """Byte offsets of one slot inside a chunk: its K row, V row, K meta
+        and, per group, its V Delta and V m entries (quad (slot % 8) // 2,
+        entry 2 (slot // 8) + slot % 2 of the quad)."""
+        ent = np.array([((slot % 8) // 2 * ng + j) * 4 + 2 * (slot // 8) + slot % 2
+                        for j in range(ng)])
+        vmeta = np.concatenate([32 * row + 16 * meta + 2 * ent[:, None] + np.arange(2),
+                                32 * row + 24 * meta + 2 * ent[:, None] + np.arange(2)]).ravel()
         return np.concatenate([slot * row + np.arange(row), 16 * row + slot * row + np.arange(row),
-                               32 * row + slot * meta + np.arange(meta),
-                               32 * row + 16 * meta + slot * meta + np.arange(meta)])
+                               32 * row + slot * meta + np.arange(meta), vmeta])
 
     ns, nsp = w.sink + w.recent, oracle.side_scale_entries(w.sink, w.recent)
 

@@ -17,10 +17,19 @@ CANARY = 0xA5
 
 
 def _unpack_chunk(chunk, d_h, g):
+    """Parse one (page, kv head) chunk back into per-slot codes and (Delta, m)
+    of K and V, following the layout description of include/kv4.h."""
     ng = d_h // g
+    nb = d_h // 32
     kc = chunk[: 16 * d_h // 2].reshape(16, d_h // 2)
     vc = chunk[16 * d_h // 2: 16 * d_h].reshape(16, d_h // 2)
-    meta = chunk[16 * d_h:].view(np.uint16).reshape(2, 16, ng, 2)
+    kmeta = chunk[16 * d_h: 16 * d_h + 64 * ng].view(np.uint16).reshape(16, ng, 2)
+    vd = chunk[16 * d_h + 64 * ng: 16 * d_h + 96 * ng].view(np.uint16).reshape(4, ng, 4)
+    vm = chunk[16 * d_h + 96 * ng: 16 * d_h + 128 * ng].view(np.uint16).reshape(4, ng, 4)
+    vmeta = np.empty((16, ng, 2), dtype=np.uint16)
+    for t in range(16):       # quad t%8 // 2, entry 2 (t // 8) + t % 2 of the quad
+        vmeta[t, :, 0] = vd[(t % 8) // 2, :, 2 * (t // 8) + t % 2]
+        vmeta[t, :, 1] = vm[(t % 8) // 2, :, 2 * (t // 8) + t % 2]
 
     def nib(rows):
         out = np.empty((16, d_h), dtype=np.uint8)
@@ -28,17 +37,25 @@ def _unpack_chunk(chunk, d_h, g):
         out[:, 1::2] = rows >> 4
         return out
 
-    # rows: 16-byte piece P of slot t sits at piece position P ^ ((t >> 1) % npieces)
-    npieces = d_h // 32
-
-    def unswizzle(rows):
+    # V rows: 16-byte piece P of slot t sits at piece position P ^ ((t >> 1) % npieces)
+    def unswizzle_v(rows):
         out = np.empty_like(rows)
         for t in range(16):
-            for P in range(npieces):
-                phys = P ^ ((t >> 1) % npieces)
+            for P in range(nb):
+                phys = P ^ ((t >> 1) % nb)
                 out[t, 16 * P:16 * P + 16] = rows[t, 16 * phys:16 * phys + 16]
         return out
-    return nib(unswizzle(kc)), nib(unswizzle(vc)), meta[0], meta[1]
+
+    # K rows: word b of quarter q (at word index nb q + b) holds channels 32 b + 8 q .. + 7
+    def unpermute_k(rows):
+        out = np.empty_like(rows)
+        for q in range(4):
+            for b in range(nb):
+                w = nb * q + b
+                c = 32 * b + 8 * q
+                out[:, c // 2: c // 2 + 4] = rows[:, 4 * w: 4 * w + 4]
+        return out
+    return nib(unpermute_k(kc)), nib(unswizzle_v(vc)), kmeta, vmeta
 
 
 def _unswizzle8(rows):
