@@ -210,20 +210,6 @@ __device__ inline void bulk_g2s_s(uint32_t smem_dst, const void* gmem_src, uint3
       : "memory");
 }
 
-// ------------------------------------------ cp.async (16-byte, L2 only)
-// Copy 16 bytes global -> shared; src_bytes 0 writes zeros and reads nothing.
-__device__ inline void cp_async16(uint32_t smem_dst, const void* gmem_src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gmem_src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most N of this thread's committed groups are pending.
-template <int N>
-__device__ inline void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ------------------------------------------------------------ reductions
 __device__ inline float warp_max(float v) {
 #pragma unroll

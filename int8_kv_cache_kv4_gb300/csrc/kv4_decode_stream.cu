@@ -162,6 +162,7 @@ struct __align__(16) StreamSmem {
   int go;                           // comb is valid
   int new_q;                        // the next segment starts a new pair
   int start_b;
+  uint64_t bar[kSW][kSStages];      // stage completion (one per warp and stage)
   uint64_t qbar;                    // completion of the qraw copy
 };
 
@@ -387,6 +388,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         out_lse[(long long)b * L.h_q + idx] = -INFINITY;
   }
   if (lane == 0) {
+    for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
     if (warp == 0) mbar_init(&sm.qbar, 1);
     fence_mbar_init();
   }
@@ -409,55 +411,45 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   }
   __syncthreads();
 
-  // ------------------------------------------------------ producer (all lanes)
+  // ------------------------------------------------------ producer (lane 0)
   const int NS = L.S + L.R;
   const int NSP = side_scale_entries(L.S, L.R);
   const long long side_blk = side_block_bytes(D, L.S, L.R);
   constexpr int SB = kSPages * cb;  // stage bytes: two INT4 chunks or one 16-slot INT8 unit
   static_assert(2 * kProtUnit * SD + 4 * kProtUnit <= SB, "an INT8 unit fits a stage");
-  constexpr int kFull = cb / 512, kRem = (cb % 512) / 16;  // 16-byte chunks of a page per lane
   uint8_t* my_stages = stage_base + (size_t)warp * kSStages * SB;
-  // Producer: every lane of the warp, in step.  Each unit is one group of
-  // 16-byte cp.async copies (lane l copies chunks l, l + 32, ...: every
-  // instruction moves 512 contiguous bytes), committed in the order the warp
-  // consumes the units.  Group k fills stage k % kSStages; after consuming
-  // group k the warp commits group k + kSStages (an empty group when nothing
-  // is left), so that waiting for "at most kSStages - 1 groups pending"
-  // always waits for exactly the unit at hand.  The segment cursor lives in shared memory (written by
-  // lane 0) and moves only when a segment is used up; what each unit needs is
-  // kept in registers: the unit index in the segment and its end, the
-  // segment's type, INT4 page count, block-table row, copy source (INT4: this
-  // head's column of the pool; INT8: the pair's side block) and the next
-  // unit's pages, read one unit ahead so that the load's latency is not
-  // waited for at the issue.
+  // Producer: lane 0 of each warp.  A unit is one or two 1-D bulk copies
+  // (cp.async.bulk, executed by the copy engine) per page, or four for a
+  // protected unit, completing on the stage's mbarrier.  Its segment cursor
+  // lives in shared memory and moves only when a segment is used up; what
+  // each unit needs is kept in registers: the unit index in the segment and
+  // its end, the segment's type, INT4 page count, block-table row, copy source
+  // (INT4: this head's column of the pool; INT8: the pair's side block) and the
+  // next unit's pages, read one unit ahead so that the load's latency is not
+  // waited for at the issue.  vbits (lane 0) records which pages of each
+  // stage were copied; the consumers read it with a shuffle.
   int p_more = 0, p_j = 0, p_hi = 0, p_type = 0, p_np4 = 0, p_ns = 0;
   const int32_t* p_bt = block_table;
   const uint8_t* p_src = paged;
   int pphys = -1, pphys1 = -1;  // the unit's two pages (-2: no second page)
   uint32_t vbits = 0;           // bit 2 st + p: page p of stage st was copied
-  const uint32_t stages_s = smem_u32(my_stages);
+  const uint32_t stages_s = smem_u32(my_stages), bars_s = smem_u32(&sm.bar[warp][0]);
   // slow path: (cursor, p_j) may lie past its segment's end; move over
   // segments until it names a unit of this warp
   auto prod_next = [&]() {
-    Seg s_ = sm.prod[warp];
+    Seg& s_ = sm.prod[warp];
     const long long ub = sm.u_begin, ue = sm.u_end;
     while (true) {
       if (s_.b >= B || s_.start >= ue) {
         p_more = 0;
-        break;
+        return;
       }
       p_hi = (int)(min(ue, s_.start + s_.n) - s_.start);
-      if (p_j < p_hi) {
-        p_more = 1;
-        break;
-      }
+      if (p_j < p_hi) break;
       seg_next(s_, L, seq_lens, B, ue);
       p_j = (int)(max(ub, s_.start) - s_.start) + warp;
     }
-    __syncwarp();
-    if (lane == 0) sm.prod[warp] = s_;
-    __syncwarp();
-    if (!p_more) return;
+    p_more = 1;
     p_type = s_.type;
     p_bt = block_table + (long long)s_.b * L.max_pages + min(s_.len, L.S) / kPage;
     p_np4 = int4_pages(s_.len, L);
@@ -470,55 +462,48 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     }
   };
   auto issue = [&](int st) {
-    const uint32_t dst = stages_s + (uint32_t)(st * SB) + 16u * lane;
+    const uint32_t bar = bars_s + 8u * st;
+    const uint32_t dst = stages_s + (uint32_t)(st * SB);
     if (p_type == 1) {
-      // pages 2j and 2j + 1 of the segment (the second may not exist: -2);
-      // a page id outside the pool is zero-filled and marked not copied
+      // pages 2j and 2j + 1 of the segment (the second may not exist: -2); a
+      // page id outside the pool is not copied and its slots are masked
       const bool good0 = (unsigned)pphys < (unsigned)L.num_pages;
       const bool good1 = (unsigned)pphys1 < (unsigned)L.num_pages;
-      if (lane == 0 && (!good0 || (pphys1 != -2 && !good1))) set_status(status, KV4_STATUS_BAD_PAGE);
+      if (!good0 || (pphys1 != -2 && !good1)) set_status(status, KV4_STATUS_BAD_PAGE);
       vbits = (vbits & ~(3u << (2 * st))) | ((good0 ? 1u : 0u) << (2 * st)) |
               ((good1 ? 1u : 0u) << (2 * st + 1));
-      const int page_stride = L.h_kv * cb;  // bytes between pages of one head (< 2^31)
-      const uint8_t* s0 = good0 ? p_src + (long long)pphys * page_stride + 16 * lane : paged;
-      const uint32_t n0 = good0 ? 16u : 0u;
-#pragma unroll
-      for (int k = 0; k < kFull; ++k) cp_async16(dst + 512u * k, s0 + 512 * k, n0);
-      if (kRem && lane < kRem) cp_async16(dst + 512u * kFull, s0 + 512 * kFull, n0);
-      if (pphys1 != -2) {
-        const uint8_t* s1 = good1 ? p_src + (long long)pphys1 * page_stride + 16 * lane : paged;
-        const uint32_t n1 = good1 ? 16u : 0u;
-#pragma unroll
-        for (int k = 0; k < kFull; ++k) cp_async16(dst + cb + 512u * k, s1 + 512 * k, n1);
-        if (kRem && lane < kRem) cp_async16(dst + cb + 512u * kFull, s1 + 512 * kFull, n1);
-      }
+      const long long page_stride = (long long)L.h_kv * cb;  // bytes between pages of one head
+      mbar_arrive_expect_tx_s(bar, (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u));
+      if (good0) bulk_g2s_s(dst, p_src + pphys * page_stride, (uint32_t)cb, bar);
+      if (good1) bulk_g2s_s(dst + cb, p_src + pphys1 * page_stride, (uint32_t)cb, bar);
     } else {
-      // INT8 unit: rows slot0 .. slot0 + rows - 1 of the K8 and V8 codes, and
-      // the scales of the 8-slot runs that hold them (within the padding)
       const int slot0 = p_j * kProtUnit;
-      const int rows = min(kProtUnit, p_ns - slot0);
-      const uint8_t* kc = p_src + (long long)slot0 * D;
-      const uint8_t* vc = p_src + (long long)(NS + slot0) * D;
-#pragma unroll
-      for (int k = 0; k < kProtUnit * D / 512; ++k) {
-        const int c = lane + 32 * k;
-        if (c < rows * (D / 16)) {
-          cp_async16(dst + 512u * k, kc + 512 * k + 16 * lane, 16u);
-          cp_async16(dst + kProtUnit * D + 512u * k, vc + 512 * k + 16 * lane, 16u);
-        }
-      }
-      const int runs = (rows + 7) / 8;  // 16-byte scale chunks
-      if (lane < 4 && (lane & 1) < runs) {
-        const int which = lane >> 1, c = lane & 1;  // K (0) or V (1) scales, chunk c
-        cp_async16(stages_s + (uint32_t)(st * SB) + 2 * kProtUnit * D + which * 2 * kProtUnit + 16 * c,
-                   p_src + 2LL * NS * D + which * 2LL * NSP + 2 * slot0 + 16 * c, 16u);
-      }
+      const uint32_t rows = (uint32_t)min(kProtUnit, p_ns - slot0);
+      vbits |= 3u << (2 * st);  // (a protected unit is always copied)
+      // scales of the 8-slot runs that hold copied rows (within the NSP padding)
+      const uint32_t sbytes = 16u * ((rows + 7) / 8);
+      mbar_arrive_expect_tx_s(bar, 2u * rows * D + 2u * sbytes);
+      bulk_g2s_s(dst, p_src + (long long)slot0 * D, rows * D, bar);
+      bulk_g2s_s(dst + kProtUnit * D, p_src + (long long)(NS + slot0) * D, rows * D, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D, p_src + 2LL * NS * D + 2 * slot0, sbytes, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D + 2 * kProtUnit, p_src + 2LL * NS * D + 2LL * NSP + 2 * slot0,
+                 sbytes, bar);
     }
   };
+  if (lane == 0) {
+    sm.prod[warp] = sm.cs;
+    p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
+    prod_next();
+    for (int st = 0; st < kSStages && p_more; ++st) {
+      issue(st);
+      p_j += kSW;
+      prod_next();
+    }
+  }
   // After the warp consumed the unit in stage st: the next unit into it.
   auto refill = [&](int st) {
     __syncwarp();  // every lane is past its reads of stage st
-    if (p_more) {
+    if (lane == 0 && p_more) {
       issue(st);
       p_j += kSW;
       if (p_j < p_hi) {  // fast path: next unit of the same segment
@@ -530,21 +515,18 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         prod_next();
       }
     }
-    cp_async_commit();
   };
-  if (lane == 0) sm.prod[warp] = sm.cs;
-  __syncwarp();
-  p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
-  prod_next();
-#pragma unroll 1
-  for (int st = 0; st < kSStages; ++st) {
-    if (p_more) {
-      issue(st);
-      p_j += kSW;
-      prod_next();
-    }
-    cp_async_commit();
-  }
+  uint32_t phase = 0;  // bit st: parity of stage st's next completion
+  // Wait for the unit in stage st (bounded: a wait that expires sets
+  // KV4_STATUS_TIMEOUT and the unit is treated as not copied).  Returns which
+  // of its pages were copied (bits 0, 1; a protected unit reads 3).
+  auto stage_wait = [&](int st) -> uint32_t {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][st], (phase >> st) & 1u));
+    phase ^= 1u << st;
+    if (!ok && lane == 0) set_status(status, KV4_STATUS_TIMEOUT);
+    const uint32_t pv = __shfl_sync(0xffffffffu, vbits >> (2 * st), 0) & 3u;
+    return ok ? pv : 0u;
+  };
 
   // ------------------------------------------------------ per-lane constants
   const int r = lane >> 2, qd = lane & 3;
@@ -662,9 +644,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       for (int jj = lo + warp; jj < hi; jj += kSW) {
         const int ST = it;
         const uint32_t sb = stages_s + (uint32_t)(ST * SB);
-        cp_async_wait<kSStages - 1>();  // this lane's copies of the unit
-        __syncwarp();        // ... and every other lane's
-        const uint32_t pv = (vbits >> (2 * ST)) & 3u;  // pages copied
+        const uint32_t pv = stage_wait(ST);  // pages copied
         const bool clean = (unsigned)(jj - 1) < (unsigned)(last_j - 1) && pv == 3u;
         const int pg0 = first_page + kSPages * jj;
         // ---------------- S = K codes x Q^T and scores (eq. 5.1 per group),
@@ -870,10 +850,9 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
       for (int jj = lo + warp; jj < hi; jj += kSW, it = it + 1 == kSStages ? 0 : it + 1) {
         const int st = it;
-        cp_async_wait<kSStages - 1>();  // this lane's copies of the unit
-        __syncwarp();        // ... and every other lane's
+        const bool ok = stage_wait(st) != 0u;
         const uint32_t stg = smem_u32(my_stages) + st * SB;
-        {
+        if (ok) {
           const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
           // a sequence of at least S + R tokens fills every sink and ring slot:
           // only a unit reaching into the padding past NS needs the test
@@ -1013,7 +992,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
                      out_lse);
     }
   }
-  cp_async_wait<0>();  // (every group left is empty: the warp consumed every unit it copied)
   // the last partial's ticket
   __syncthreads();
   if (threadIdx.x == kTicketThread) {
