@@ -611,9 +611,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       uint4 qbf[4];  // this lane's B fragments of the four blocks (lo b0, lo b1, hi b0, hi b1)
 #pragma unroll
       for (int bl = 0; bl < 4; ++bl) qbf[bl] = sm.qp.qb[bl][lane];
-      float qsv[4];
-#pragma unroll
-      for (int gg = 0; gg < 4; ++gg) qsv[gg] = gg < NG ? sm.qp.qs[qd][gg] : 0.f;
+      const uint32_t qmf = sm.qp.qm[lane];  // offset-term B fragment
       const float ksc = sm.qp.ks[qd];
       const int first_page = rg.sink_end / kPage;
       const int len = cs.len;
@@ -656,6 +654,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
           const uint32_t pb = sb + pp * cb;
           const uint4 w0 = lds128(pb + kq_off), w1 = lds128(pb + kq_off + 512);
           float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
+          // offset part sum_g m_(t, g) qs_g of tokens r and r + 8 (columns of parity 0)
+          float sM[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const uint32_t m0 = qd < NG ? lds32(pb + km_off + 4 * qd) : 0u;
+            const uint32_t m1 = qd < NG ? lds32(pb + km_off + 8 * NG * 4 + 4 * qd) : 0u;
+            mma_f16(sM, __byte_perm(m0, 0u, 0x3232), __byte_perm(m1, 0u, 0x3232), 0u, 0u, qmf, 0u);
+          }
 #pragma unroll
           for (int bl = 0; bl < 4; ++bl) {
             uint32_t x0[4], x1[4];
@@ -672,25 +677,25 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
             // block sums of this token: blocks 0, 1 in set A, 2, 3 in set B
             const float s0 = sA[2 * e], s1 = sA[2 * e + 1];
             const float s2 = sB[2 * e], s3 = sB[2 * e + 1];
-            float dsum, msum = -mref;
+            float dsum;
             if (NG == 4) {
-              const float2 g0 = h2f2(km.get(0)), g1 = h2f2(km.get(1));
-              const float2 g2 = h2f2(km.get(2)), g3 = h2f2(km.get(3));
-              dsum = fmaf(g3.x, s3, fmaf(g2.x, s2, fmaf(g1.x, s1, g0.x * s0)));
-              msum = fmaf(g3.y, qsv[3], fmaf(g2.y, qsv[2], fmaf(g1.y, qsv[1], fmaf(g0.y, qsv[0], msum))));
+              dsum = fmaf(lo_f(km.get(3)), s3, fmaf(lo_f(km.get(2)), s2,
+                          fmaf(lo_f(km.get(1)), s1, lo_f(km.get(0)) * s0)));
             } else if (NG == 2) {
-              const float2 g0 = h2f2(km.get(0)), g1 = h2f2(km.get(1));
-              dsum = fmaf(g1.x, s2 + s3, g0.x * (s0 + s1));
-              msum = fmaf(g1.y, qsv[1], fmaf(g0.y, qsv[0], msum));
+              dsum = fmaf(lo_f(km.get(1)), s2 + s3, lo_f(km.get(0)) * (s0 + s1));
             } else {
-              const float2 g0 = h2f2(km.get(0));
-              dsum = g0.x * ((s0 + s1) + (s2 + s3));
-              msum = fmaf(g0.y, qsv[0], msum);
+              dsum = lo_f(km.get(0)) * ((s0 + s1) + (s2 + s3));
             }
-            sc[pp][e] = fmaf(ksc, dsum, msum);
+            sc[pp][e] = fmaf(ksc, dsum, sM[2 * e] - mref);
           }
         }
-        if (!clean) {  // first / last unit of the segment, or a page not copied: mask
+        if (!clean) {
+          // first / last unit of the segment, or a page not copied: mask the
+          // scores outside the INT4 region, and zero the V metadata of slots
+          // that hold no data of this sequence (a page not copied, or slots
+          // at or past the length: their bytes may be anything), so that
+          // their P' = p Delta and offset p m are exactly zero in the PV
+          // products below, which then need no mask
 #pragma unroll
           for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
@@ -699,6 +704,18 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
               const bool in = ((pv >> pp) & 1u) && pos >= rg.sink_end && pos < rg.rec_start;
               if (!in) sc[pp][e] = -INFINITY;
             }
+          if (lane < 2 * kPage) {
+            const int pp = lane >> 4, t = lane & 15;
+            if (!((pv >> pp) & 1u) || (pg0 + pp) * kPage + t >= len) {
+              const uint32_t ch = sb + pp * cb;  // (volatile stores: kept before the loads below)
+#pragma unroll
+              for (int gg = 0; gg < NG; ++gg) {
+                sts16(ch + v_delta_byte(t, gg, D, GS), 0u);
+                sts16(ch + v_offset_byte(t, gg, D, GS), 0u);
+              }
+            }
+          }
+          __syncwarp();
         }
         // ---------------- online softmax for head q over both pages.  Lazy
         // rescaling: the reference m_run moves only when a score exceeds it
@@ -743,7 +760,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         // ---------------- PV, one page at a time
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
-          if (!clean && !((pv >> pp) & 1u)) continue;  // not copied: all its p are 0
           const uint32_t pb = sb + pp * cb;
           // p of tokens 2 q + {0, 1} (b0) and 2 q + {8, 9} (b1), head r
           const uint32_t ph = pack_f16(pr_[pp][0], pr_[pp][1]);
@@ -767,20 +783,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
             const uint2 a = lds64(pb + vd_off);
             dl[0][0] = a.x; dl[0][1] = a.y;
           }
-          uint2 mw = lds64(pb + vm_off);  // V offsets of group mrow, same tokens
-          if (!clean && (pg0 + pp + 1) * kPage > len) {
-            // slots at or past the length were never written: zero their metadata
-            const int p0 = (pg0 + pp) * kPage + 2 * qd;
-            const uint32_t k0 = (p0 < len ? 0x0000FFFFu : 0u) | (p0 + 1 < len ? 0xFFFF0000u : 0u);
-            const uint32_t k1 = (p0 + 8 < len ? 0x0000FFFFu : 0u) | (p0 + 9 < len ? 0xFFFF0000u : 0u);
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) {
-              dl[gg][0] &= k0;
-              dl[gg][1] &= k1;
-            }
-            mw.x &= k0;
-            mw.y &= k1;
-          }
+          const uint2 mw = lds64(pb + vm_off);  // V offsets of group mrow, same tokens
           // offset term: rows = groups (their m), columns = heads, against p
           mma_f16(mtacc, mw.x, 0u, mw.y, 0u, p01, p23);
 #pragma unroll

@@ -77,6 +77,10 @@ __device__ inline uint32_t lds32(uint32_t a) {
   return v;
 }
 
+__device__ inline void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v));
+}
+
 // (a & m) | c as one three-input logic op.  Written as C++ the same
 // expression compiled to two logic ops per value on sm_103a (measured with
 // the executed-instruction counters); the widening routines below are the

@@ -138,11 +138,16 @@ __device__ inline uint32_t q16_scaled(uint32_t bf, float two_e) {
 // fp16's largest value.  The score of token t for head j (log2 domain) is then
 //   s = ks[j] * sum_b Delta_(t, group(b)) S_(t, j, b) + sum_g m_(t, g) qs[j][g]
 // with ks[j] = scale_log2 2^20 2^-e_j and qs[j][g] = scale_log2 sum_(d in g) q_d
-// (eq. 5.1 per group).
+// (eq. 5.1 per group).  The offset part sum_g m qs is one more MMA per page:
+// A = each token's offsets m_(t, g) at k = 2 g and 2 g + 1, B = qs[j][g]
+// split into an fp16 head and tail (k = 2 g, 2 g + 1) in the parity-0
+// columns, so that its products are exact and the tensor core sums them in
+// fp32 (qm: lane (r', q') holds the (head, tail) of group q' of head r' >> 1
+// when r' is even and q' < NG, else zeros).
 struct __align__(16) QPrep {
   uint4 qb[4][32];            // INT4 path: B fragments [block][lane]: lo b0, lo b1, hi b0, hi b1
   uint2 qfrag8[8][16];        // INT8 path: query fragments (a0, a2) of lanes 0..15
-  float qs[SG][4];            // [head][group]: scale_log2 x the group's query sum (fp32)
+  uint32_t qm[32];            // INT4 path: B fragment (b0) of the offset-term MMA, per lane
   float ks[SG];               // [head]: scale_log2 x 2^20 x 2^-e_head
 };
 static_assert(sizeof(QPrep) % 16 == 0, "QPrep is copied in 16-byte units");
@@ -176,7 +181,20 @@ __device__ inline void build_qprep(const uint16_t* qr, QPrep& qp, int t, float s
     e = min(40, max(-20, 10 - max(ex, -126)));
   }
   const float two_e = __int_as_float((127 + e) << 23);
-  if ((ln % (GS / 4)) == 0) qp.qs[j][ln / (GS / 4)] = scale_log2 * sq;
+  // lanes 8 j .. 8 j + 7 of the offset-term fragment: group q' of head j
+  // (lane ln < 4 reads group ln's sum from lane ln * GS / 4)
+  {
+    const float qsg = scale_log2 * __shfl_sync(0xffffffffu, sq, (ln & 3) * (GS / 4));
+    if (ln < 8) {
+      uint32_t w = 0u;
+      if (ln < 4 && ln < NG) {
+        const __half hi = __float2half_rn(qsg);
+        const __half lo = __float2half_rn(qsg - __half2float(hi));
+        w = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+      }
+      qp.qm[8 * j + ln] = w;
+    }
+  }
   if (ln == 0) qp.ks[j] = scale_log2 * __int_as_float((127 + 20 - e) << 23);
   {
     // thread ln of warp j: lane (r', q') = (2 j + (ln >> 4), (ln >> 2) & 3), block ln & 3
