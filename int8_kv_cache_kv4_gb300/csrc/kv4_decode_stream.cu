@@ -3,33 +3,37 @@
 // and eq. A1), head_dim 128 with 4 query heads per kv head.
 //
 // Work is one stream of units over all (sequence, kv head) pairs.  For each
-// pair, in order: its protected units (8 consecutive INT8 side-cache slots
-// each, the sink slots and the recent-window ring), then one unit per
-// 16-token INT4 page of the region between the sinks and the recent window.
-// A pair's protected units form one segment of the stream, its INT4 units a
-// second.  The grid is sized to fill the GPU once, and the stream is cut into
-// contiguous CTA shares of equal cost: an INT4 unit counts 4, a protected
-// unit 7 and a segment start 24 (seg_cost), the measured ratios of their
-// times, so that CTAs whose share crosses many short segments take fewer
-// units and all CTAs finish together.
+// pair, in order: its protected units (16 consecutive INT8 side-cache slots
+// each, the sink slots and the recent-window ring), then one unit per two
+// 16-token INT4 pages of the region between the sinks and the recent window.
+// A pair's units form one segment of the stream.  The grid is sized to fill
+// the GPU once, and the stream is cut into contiguous CTA shares of equal
+// cost: an INT4 unit counts 4, a protected unit 7 and a segment start 24
+// (seg_cost), the measured ratios of their times, so that CTAs whose share
+// crosses many short segments take fewer units and all CTAs finish together.
 //
 // Inside a CTA the four warps take the units of the current segment
 // round-robin; each warp streams its units through its own two-stage ring of
-// bulk copies, issued ahead across segment boundaries.  When a segment ends
-// the warps' online-softmax states are merged into one partial result (a
-// locally normalised output and its log-normaliser) for the pair's four query
-// heads.  The CTA that stores the last partial of a pair merges them (eq. A1)
-// into the output.  The CTA holding units of segment s (s = 2 * pair + region)
-// writes partial s + c: CTA ranges are contiguous, ordered and non-empty, so
-// these indices are distinct and below 2 * pairs + C.
+// bulk copies (the copy engine, one mbarrier per stage), issued ahead across
+// segment boundaries.  A warp runs its protected units of the segment, then
+// its INT4 units, carrying one online-softmax state across.  When a segment
+// ends the warps' states are merged into one partial result (a locally
+// normalised output and its log-normaliser) for the pair's four query heads.
+// A pair held by one CTA is written out directly; otherwise the CTA that
+// stores the last partial of the pair merges them (eq. A1) into the output.
+// The CTA c holding units of pair p writes partial p + c: CTA ranges are
+// contiguous, ordered and non-empty, so these indices are distinct and below
+// pairs + C.
 //
 // Per-unit math on the tensor cores (m16n8k16, fp16 operands, fp32
 // accumulation):
-//  INT4 page: as in the split kernel -- block-diagonal query rows against the
-//    widened 4-bit K codes, scores by eq. 5.1 per group, then the transposed
-//    V codes (entered as fp16 subnormals, bit pattern = code) against
-//    P' = p * Delta_v plus the offset term sum p m.
-//  INT8 unit: the query (rows = heads) against the 8 slots' K codes widened
+//  INT4 unit: the tokens as MMA rows -- the 4-bit K codes entered as fp16
+//    subnormals (bit pattern = code) against the pair's query scaled by a
+//    power of two per head, one 32-channel block per two k-steps; scores by
+//    eq. 5.1 per group with the offset term as one more MMA; then the
+//    transposed V codes (subnormals as well) against P' = p * Delta_v, plus
+//    the offset term sum p m as one MMA whose rows are the V offsets.
+//  INT8 unit: the query (rows = heads) against the 16 slots' K codes widened
 //    exactly to fp16, scores scaled by each slot's K scale; then the
 //    transposed V codes against P' = p * s_v.  Slots outside the protected
 //    set (not yet written, or outside the final recent window) are masked.
@@ -75,67 +79,34 @@ __device__ inline long long unit_at_cost(long long T, int b_lo, int b_hi, long l
                                          const int32_t* __restrict__ seq_lens) {
   for (int b = b_lo; b < b_hi; ++b) {
     const int len = clamp_len(__ldg(seq_lens + b), L);
-    const int np = prot_units(len, L), n4 = int4_units(len, L);
-    const long long pc = seg_cost(np, 0) + seg_cost(n4, 1);  // one pair
+    const int np = prot_units(len, L), n = np + int4_units(len, L);
+    const long long pc = seg_cost(np, n - np);  // one pair
     if (T < pre_c + (long long)L.h_kv * pc) {
       const long long h = (T - pre_c) / pc;
-      long long within = T - pre_c - h * pc, u = pre_u + h * (np + n4);
-      int n = np, w = kCost8;
-      if (within >= seg_cost(np, 0)) {  // in the pair's INT4 segment
-        within -= seg_cost(np, 0);
-        u += np;
-        n = n4;
-        w = kCost4;
-      }
-      // unit j > 0 of a segment starts at cost kCostSeg + j w into it
-      const long long j = within <= 0 ? 0 : max(1LL, (within - kCostSeg + w - 1) / w);
-      return u + min(j, (long long)n);  // j = n: the next segment's first unit
+      // j = n: the next segment's first unit
+      return pre_u + h * n + unit_at_within(T - pre_c - h * pc, np, n);
     }
     pre_c += (long long)L.h_kv * pc;
-    pre_u += (long long)L.h_kv * (np + n4);
+    pre_u += (long long)L.h_kv * n;
   }
   return pre_u;  // (not reached: T lies in these sequences)
 }
 
-// CTAs holding a pair's protected units (c0 .. c0 + n0 - 1) and its INT4
-// units (c1 .. c1 + n1 - 1).  gs / pcs: the pair's first unit and the stream
-// cost before it.  by_cost: the stream was cut by cost (Wc over Cw CTAs),
-// else into equal unit counts (U over Cw CTAs).
-struct PairParts {
-  int c0, n0, c1, n1;
-};
-__device__ inline PairParts pair_parts(long long gs, long long pcs, int np, int n4, bool by_cost,
-                                       long long U, long long Wc, int Cw) {
-  PairParts r{0, 0, 0, 0};
-  if (by_cost) {
-    auto at = [&](long long P) { return (int)((P * Cw) / Wc); };
-    const long long p4 = pcs + seg_cost(np, 0);
-    if (np) {
-      r.c0 = at(pcs);
-      r.n0 = at(pcs + (np > 1 ? kCostSeg + (long long)(np - 1) * kCost8 : 0)) - r.c0 + 1;
-    }
-    if (n4) {
-      r.c1 = at(p4);
-      r.n1 = at(p4 + (n4 > 1 ? kCostSeg + (long long)(n4 - 1) * kCost4 : 0)) - r.c1 + 1;
-    }
-  } else {
-    if (np) {
-      r.c0 = cta_of(gs, U, Cw);
-      r.n0 = cta_of(gs + np - 1, U, Cw) - r.c0 + 1;
-    }
-    if (n4) {
-      r.c1 = cta_of(gs + np, U, Cw);
-      r.n1 = cta_of(gs + np + n4 - 1, U, Cw) - r.c1 + 1;
-    }
-  }
-  return r;
+// CTAs c0 .. c0 + n0 - 1 holding the units of a pair (np protected, n in
+// all) whose first unit lies at stream cost pcs, when the stream of cost Wc
+// is cut over Cw CTAs: CTA c holds the units whose cost lies in
+// [ceil(c Wc / Cw), ceil((c + 1) Wc / Cw)), so a unit at cost x is in CTA
+// floor(x Cw / Wc).
+__device__ inline void pair_ctas(long long pcs, int np, int n, long long Wc, int Cw, int& c0,
+                                 int& n0) {
+  c0 = (int)((pcs * Cw) / Wc);
+  n0 = (int)(((pcs + unit_cost_at(n - 1, np)) * Cw) / Wc) - c0 + 1;
 }
 
 // A pair whose partial results are to be merged, with where they are.
 struct Pend {
   long long row0;      // first output row (sequence * h_q + kv head * G)
-  long long s0;        // partial index base of the protected segment (= 2 * pair)
-  int pair, type, c0, n0, c1, n1, valid;
+  int pair, c0, n0, valid;
 };
 
 struct __align__(16) StreamSmem {
@@ -153,23 +124,20 @@ struct __align__(16) StreamSmem {
   long long start_pre_c;            // stream cost before sequence start_b
   int cw;                           // CTAs the stream is cut over
   long long u_begin, u_end;         // this CTA's share of the stream
-  Seg cs;                           // first segment of this CTA
-  Seg prod[kSW];                 // producer cursors (segment of each warp's next unit)
-  Seg nx;                           // segment after cs (thread 0, at segment start)
-  Pend pcur;                        // partial bookkeeping of segment cs (thread 0)
-  Pend pend;                        // partial whose ticket is in flight (thread 0)
+  Seg cs;                           // current segment of this CTA
+  Seg prod[kSW];                    // producer cursors (segment of each warp's next unit)
+  Seg nx;                           // segment after cs (ticket thread, at segment start)
+  Pend pcur;                        // partial bookkeeping of segment cs (ticket thread)
+  Pend pend;                        // partial whose ticket is in flight (ticket thread)
   Pend comb;                        // pair to merge at this boundary
   int go;                           // comb is valid
-  int new_q;                        // the next segment starts a new pair
+  int new_q;                        // a next segment follows (its query is being copied)
   int start_b;
   uint64_t bar[kSW][kSStages];      // stage completion (one per warp and stage)
   uint64_t qbar;                    // completion of the qraw copy
 };
 
-// Query of pair `row0` (G consecutive bf16 rows of D) -> fp16 copy, per-block
-// sums and both fragment sets.  Every warp must be past its last use of the
-// previous query (the caller's barrier).
-// Thread 0: start the bulk copy of pair `row0`'s query (G rows of D bf16,
+// One thread: start the bulk copy of pair `row0`'s query (G rows of D bf16,
 // 1 KB, 16-byte aligned) into sm.qraw; it completes on sm.qbar.
 __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __restrict__ q,
                                           long long row0) {
@@ -184,12 +152,16 @@ __device__ __noinline__ void stream_query_setup(StreamSmem& sm, float scale_log2
   if (threadIdx.x < 128) build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x, scale_log2);
 }
 
-// Merge the warps' states of one segment and store its partial result P
-// (after a barrier that follows every warp's publish).  Warp j < G merges
-// query head j: the warps' weights 2^(m_w - M) / L are formed once, then each
-// lane combines four channels.
+// Merge the warps' states of one segment (after a barrier that follows every
+// warp's publish).  Warp j < G merges query head j: the warps' weights
+// 2^(m_w - M) / L are formed once, then each lane combines four channels.
+// The result is stored as partial P, or, for a pair no other CTA holds
+// (direct), as the pair's output rows row0 .. row0 + G - 1 and their
+// log-normalisers.
 __device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ part_o,
-                                          float* __restrict__ part_lse, long long P) {
+                                          float* __restrict__ part_lse, long long P, bool direct,
+                                          long long row0, uint16_t* __restrict__ out,
+                                          float* __restrict__ out_lse) {
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (j >= SG) return;
   const float mw = lane < kSW ? sm.mrg_m[lane][j] : -INFINITY;
@@ -216,29 +188,38 @@ __device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ pa
     o.z = fmaf(fw, a.z + mt, o.z);
     o.w = fmaf(fw, a.w + mt, o.w);
   }
-  reinterpret_cast<float4*>(part_o + (P * SG + j) * SD)[lane] = o;
-  if (lane == 0) part_lse[P * SG + j] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+  const float lse2 = empty ? -INFINITY : M + log2f(Lt);  // log2 domain
+  if (direct) {
+    const long long row = row0 + j;
+    uint16_t* po = out + row * SD + 4 * lane;  // the output need only be 2-byte aligned
+    po[0] = f32_to_bf16_bits(o.x);
+    po[1] = f32_to_bf16_bits(o.y);
+    po[2] = f32_to_bf16_bits(o.z);
+    po[3] = f32_to_bf16_bits(o.w);
+    if (out_lse && lane == 0) out_lse[row] = lse2 * kLn2;
+  } else {
+    reinterpret_cast<float4*>(part_o + (P * SG + j) * SD)[lane] = o;
+    if (lane == 0) part_lse[P * SG + j] = lse2 * kLn2;
+  }
 }
 
-// Eq. A1 over the n0 + n1 partials of one pair (partials s0 + c0 + k, then
-// s1 + c1 + k); warp j merges query head j.
+// Eq. A1 over the n partials P0 .. P0 + n - 1 of one pair; warp j merges
+// query head j.
 __device__ inline void stream_combine(const float* __restrict__ part_o,
-                                      const float* __restrict__ part_lse, long long s0, int c0,
-                                      int n0, long long s1, int c1, int n1, long long row0,
-                                      uint16_t* __restrict__ out, float* __restrict__ out_lse) {
+                                      const float* __restrict__ part_lse, long long P0, int n,
+                                      long long row0, uint16_t* __restrict__ out,
+                                      float* __restrict__ out_lse) {
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;  // warp j < G: query head j
   if (j >= SG) return;
-  const int n = n0 + n1;
-  auto pidx = [&](int k) { return k < n0 ? s0 + c0 + k : s1 + c1 + (k - n0); };
   float M = -INFINITY;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(part_lse + pidx(k) * SG + j));
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(part_lse + (P0 + k) * SG + j));
   M = warp_max(M);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float Zl = 0.f;
   if (M != -INFINITY) {
     for (int k0 = 0; k0 < n; k0 += 32) {
       const int k = k0 + lane;
-      const float z = k < n ? __ldcg(part_lse + pidx(k) * SG + j) : -INFINITY;
+      const float z = k < n ? __ldcg(part_lse + (P0 + k) * SG + j) : -INFINITY;
       const float wl = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
       Zl += wl;
       const int nr = min(32, n - k0);
@@ -249,7 +230,8 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
         for (int u = 0; u < 4; ++u) {
           wv[u] = __shfl_sync(0xffffffffu, wl, (rr + u) & 31);
           const bool use = rr + u < nr && wv[u] != 0.f;
-          o[u] = use ? __ldcg(reinterpret_cast<const float4*>(part_o + (pidx(k0 + rr + u) * SG + j) * SD) + lane)
+          o[u] = use ? __ldcg(reinterpret_cast<const float4*>(
+                               part_o + ((P0 + k0 + rr + u) * SG + j) * SD) + lane)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
           if (!use) wv[u] = 0.f;
         }
@@ -306,7 +288,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     bad_len |= len != raw;
     const int np = prot_units(len, L), n4 = int4_units(len, L);
     mine += (long long)L.h_kv * (np + n4);
-    mine_c += (long long)L.h_kv * (seg_cost(np, 0) + seg_cost(n4, 1));
+    mine_c += (long long)L.h_kv * seg_cost(np, n4);
   }
   if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
   sm.scan[threadIdx.x] = mine;
@@ -374,7 +356,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
           break;
         }
         pre += ub;
-        pre_c += (long long)L.h_kv * (seg_cost(np, 0) + seg_cost(n4, 1));
+        pre_c += (long long)L.h_kv * seg_cost(np, n4);
       }
     }
   }
@@ -396,14 +378,10 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   if (sm.start_b >= B) return;  // no units for this CTA
   if (threadIdx.x == 0) {
     Seg cs;
-    cs.b = sm.start_b;
-    cs.h = 0;
-    cs.type = 0;
-    cs.len = clamp_len(__ldg(seq_lens + cs.b), L);
+    seg_set(cs, sm.start_b, 0, clamp_len(__ldg(seq_lens + sm.start_b), L), L);
     cs.start = sm.start_pre;
     cs.cs = sm.start_pre_c;
     sm.cw = Cw;
-    cs.n = prot_units(cs.len, L);
     while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
     sm.cs = cs;
     sm.u_begin = u_begin;
@@ -418,22 +396,28 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   constexpr int SB = kSPages * cb;  // stage bytes: two INT4 chunks or one 16-slot INT8 unit
   static_assert(2 * kProtUnit * SD + 4 * kProtUnit <= SB, "an INT8 unit fits a stage");
   uint8_t* my_stages = stage_base + (size_t)warp * kSStages * SB;
-  // Producer: lane 0 of each warp.  A unit is one or two 1-D bulk copies
-  // (cp.async.bulk, executed by the copy engine) per page, or four for a
+  // Producer: lane 0 of each warp.  A unit is one 1-D bulk copy
+  // (cp.async.bulk, executed by the copy engine) per INT4 page, or four for a
   // protected unit, completing on the stage's mbarrier.  Its segment cursor
   // lives in shared memory and moves only when a segment is used up; what
   // each unit needs is kept in registers: the unit index in the segment and
-  // its end, the segment's type, INT4 page count, block-table row, copy source
-  // (INT4: this head's column of the pool; INT8: the pair's side block) and the
-  // next unit's pages, read one unit ahead so that the load's latency is not
-  // waited for at the issue.  vbits (lane 0) records which pages of each
-  // stage were copied; the consumers read it with a shuffle.
-  int p_more = 0, p_j = 0, p_hi = 0, p_type = 0, p_np4 = 0, p_ns = 0;
+  // its end, the segment's protected unit count, INT4 page count and
+  // block-table row, the pair's column of the page pool and its side block,
+  // and the next INT4 unit's pages, read one unit ahead so that the load's
+  // latency is not waited for at the issue.  vbits (lane 0) records which
+  // pages of each stage were copied; the consumers read it with a shuffle.
+  int p_more = 0, p_j = 0, p_hi = 0, p_np = 0, p_np4 = 0, p_ns = 0, p_hcb = 0;
   const int32_t* p_bt = block_table;
-  const uint8_t* p_src = paged;
-  int pphys = -1, pphys1 = -1;  // the unit's two pages (-2: no second page)
+  const uint8_t* p_src8 = side;
+  int pphys = -1, pphys1 = -1;  // the INT4 unit's two pages (-2: no second page)
   uint32_t vbits = 0;           // bit 2 st + p: page p of stage st was copied
   const uint32_t stages_s = smem_u32(my_stages), bars_s = smem_u32(&sm.bar[warp][0]);
+  // pages of INT4 unit p_j - p_np
+  auto prod_pages = [&]() {
+    const int j2 = kSPages * (p_j - p_np);
+    pphys = __ldg(p_bt + j2);
+    pphys1 = j2 + 1 < p_np4 ? __ldg(p_bt + j2 + 1) : -2;
+  };
   // slow path: (cursor, p_j) may lie past its segment's end; move over
   // segments until it names a unit of this warp
   auto prod_next = [&]() {
@@ -450,32 +434,30 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       p_j = (int)(max(ub, s_.start) - s_.start) + warp;
     }
     p_more = 1;
-    p_type = s_.type;
+    p_np = s_.np;
     p_bt = block_table + (long long)s_.b * L.max_pages + min(s_.len, L.S) / kPage;
     p_np4 = int4_pages(s_.len, L);
     p_ns = s_.len <= L.S ? s_.len : NS;
-    p_src = s_.type == 1 ? paged + (long long)s_.h * cb
-                         : side + ((long long)s_.b * L.h_kv + s_.h) * side_blk;
-    if (s_.type == 1) {
-      pphys = __ldg(p_bt + kSPages * p_j);
-      pphys1 = kSPages * p_j + 1 < p_np4 ? __ldg(p_bt + kSPages * p_j + 1) : -2;
-    }
+    p_hcb = s_.h * cb;
+    p_src8 = side + ((long long)s_.b * L.h_kv + s_.h) * side_blk;
+    if (p_j >= p_np) prod_pages();
   };
   auto issue = [&](int st) {
     const uint32_t bar = bars_s + 8u * st;
     const uint32_t dst = stages_s + (uint32_t)(st * SB);
-    if (p_type == 1) {
-      // pages 2j and 2j + 1 of the segment (the second may not exist: -2); a
-      // page id outside the pool is not copied and its slots are masked
+    if (p_j >= p_np) {
+      // INT4 pages 2 j and 2 j + 1 of the region (the second may not exist:
+      // -2); a page id outside the pool is not copied and its slots are masked
       const bool good0 = (unsigned)pphys < (unsigned)L.num_pages;
       const bool good1 = (unsigned)pphys1 < (unsigned)L.num_pages;
       if (!good0 || (pphys1 != -2 && !good1)) set_status(status, KV4_STATUS_BAD_PAGE);
       vbits = (vbits & ~(3u << (2 * st))) | ((good0 ? 1u : 0u) << (2 * st)) |
               ((good1 ? 1u : 0u) << (2 * st + 1));
       const long long page_stride = (long long)L.h_kv * cb;  // bytes between pages of one head
+      const uint8_t* src = paged + p_hcb;
       mbar_arrive_expect_tx_s(bar, (good0 ? (uint32_t)cb : 0u) + (good1 ? (uint32_t)cb : 0u));
-      if (good0) bulk_g2s_s(dst, p_src + pphys * page_stride, (uint32_t)cb, bar);
-      if (good1) bulk_g2s_s(dst + cb, p_src + pphys1 * page_stride, (uint32_t)cb, bar);
+      if (good0) bulk_g2s_s(dst, src + pphys * page_stride, (uint32_t)cb, bar);
+      if (good1) bulk_g2s_s(dst + cb, src + pphys1 * page_stride, (uint32_t)cb, bar);
     } else {
       const int slot0 = p_j * kProtUnit;
       const uint32_t rows = (uint32_t)min(kProtUnit, p_ns - slot0);
@@ -483,11 +465,11 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // scales of the 8-slot runs that hold copied rows (within the NSP padding)
       const uint32_t sbytes = 16u * ((rows + 7) / 8);
       mbar_arrive_expect_tx_s(bar, 2u * rows * D + 2u * sbytes);
-      bulk_g2s_s(dst, p_src + (long long)slot0 * D, rows * D, bar);
-      bulk_g2s_s(dst + kProtUnit * D, p_src + (long long)(NS + slot0) * D, rows * D, bar);
-      bulk_g2s_s(dst + 2 * kProtUnit * D, p_src + 2LL * NS * D + 2 * slot0, sbytes, bar);
-      bulk_g2s_s(dst + 2 * kProtUnit * D + 2 * kProtUnit, p_src + 2LL * NS * D + 2LL * NSP + 2 * slot0,
-                 sbytes, bar);
+      bulk_g2s_s(dst, p_src8 + (long long)slot0 * D, rows * D, bar);
+      bulk_g2s_s(dst + kProtUnit * D, p_src8 + (long long)(NS + slot0) * D, rows * D, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D, p_src8 + 2LL * NS * D + 2 * slot0, sbytes, bar);
+      bulk_g2s_s(dst + 2 * kProtUnit * D + 2 * kProtUnit,
+                 p_src8 + 2LL * NS * D + 2LL * NSP + 2 * slot0, sbytes, bar);
     }
   };
   if (lane == 0) {
@@ -497,7 +479,11 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     for (int st = 0; st < kSStages && p_more; ++st) {
       issue(st);
       p_j += kSW;
-      prod_next();
+      if (p_j < p_hi) {
+        if (p_j >= p_np) prod_pages();
+      } else {
+        prod_next();
+      }
     }
   }
   // After the warp consumed the unit in stage st: the next unit into it.
@@ -507,10 +493,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       issue(st);
       p_j += kSW;
       if (p_j < p_hi) {  // fast path: next unit of the same segment
-        if (p_type == 1) {
-          pphys = __ldg(p_bt + kSPages * p_j);
-          pphys1 = kSPages * p_j + 1 < p_np4 ? __ldg(p_bt + kSPages * p_j + 1) : -2;
-        }
+        if (p_j >= p_np) prod_pages();
       } else {
         prod_next();
       }
@@ -559,40 +542,150 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     const Seg cs = sm.cs;
     if (cs.b >= B || cs.start >= sm.u_end) break;
     if (threadIdx.x == kTicketThread) {
-      // the next segment (its pair's query is read ahead when it changes:
-      // the previous copy was consumed before the last barrier), and this
-      // segment's partial bookkeeping -- none of it is waited for by a barrier
-      {
-        Seg nx = cs;
-        seg_next(nx, L, seq_lens, B, sm.u_end);
-        const bool new_q = nx.b < B && nx.start < sm.u_end && (nx.b != cs.b || nx.h != cs.h);
-        sm.new_q = new_q;
-        if (new_q) stream_query_fetch(sm, q, (long long)nx.b * L.h_q + (long long)nx.h * SG);
-        // bookkeeping for the boundary, done here so that no barrier waits on it
-        sm.nx = nx;
-        const int pair = cs.b * L.h_kv + cs.h;
-        const int np = prot_units(cs.len, L), n4 = int4_units(cs.len, L);
-        const long long gs = cs.type == 0 ? cs.start : cs.start - np;  // pair's first unit
-        const long long pcs = cs.type == 0 ? cs.cs : cs.cs - seg_cost(np, 0);  // cost before it
-        const PairParts pp = pair_parts(gs, pcs, np, n4, true, sm.total, sm.totalc, sm.cw);
-        Pend pd;
-        pd.row0 = (long long)cs.b * L.h_q + (long long)cs.h * SG;
-        pd.s0 = 2LL * pair;
-        pd.pair = pair;
-        pd.type = cs.type;
-        pd.c0 = pp.c0;
-        pd.n0 = pp.n0;
-        pd.c1 = pp.c1;
-        pd.n1 = pp.n1;
-        pd.valid = 1;
-        sm.pcur = pd;
-      }
+      // the next segment (its pair's query is read ahead: the previous copy
+      // was consumed before the last barrier), and this segment's partial
+      // bookkeeping -- none of it is waited for by a barrier
+      Seg nx = cs;
+      seg_next(nx, L, seq_lens, B, sm.u_end);
+      const bool new_q = nx.b < B && nx.start < sm.u_end;
+      sm.new_q = new_q;
+      if (new_q) stream_query_fetch(sm, q, (long long)nx.b * L.h_q + (long long)nx.h * SG);
+      sm.nx = nx;
+      Pend pd;
+      pd.row0 = (long long)cs.b * L.h_q + (long long)cs.h * SG;
+      pd.pair = cs.b * L.h_kv + cs.h;
+      pair_ctas(cs.cs, cs.np, cs.n, sm.totalc, sm.cw, pd.c0, pd.n0);
+      pd.valid = 1;
+      sm.pcur = pd;
     }
     const int lo = (int)(max(sm.u_begin, cs.start) - cs.start);
     const int hi = (int)(min(sm.u_end, cs.start + cs.n) - cs.start);
     const Regions rg = regions(cs.len, L.S, L.R);
-
-    if (cs.type == 1) {
+    const int np = cs.np;
+    // this warp's units of the segment: jj = lo + warp, lo + warp + kSW, ...;
+    // the protected ones (jj < np) first
+    int jj = lo + warp;
+    const int e8 = min(hi, np);
+    const bool have8 = jj < e8;
+    if (have8) {
+      // ================================= INT8 protected units (App. A.3)
+      // Per unit of 16 side slots: QK^T with the query rows (heads) against
+      // the slots' codes widened exactly to fp16 (two 8-slot tiles), scores
+      // scaled by each slot's K scale; then PV with the transposed codes
+      // against P' = p * s_v.  Slots outside the protected set are masked.
+      const int n_rec = cs.len > L.S ? cs.len - rg.rec_start : 0;
+      const int ws_mod = L.R > 0 ? rg.rec_start % L.R : 0;
+      float m8 = -INFINITY, l8 = 0.f;
+      float acc8[8][4];
+#pragma unroll
+      for (int P = 0; P < 8; ++P)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
+      const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
+      for (; jj < e8; jj += kSW, it = it + 1 == kSStages ? 0 : it + 1) {
+        const int st = it;
+        const bool ok = stage_wait(st) != 0u;
+        const uint32_t stg = smem_u32(my_stages) + st * SB;
+        if (ok) {
+          const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
+          // a sequence of at least S + R tokens fills every sink and ring slot:
+          // only a unit reaching into the padding past NS needs the test
+          const bool all_in = cs.len >= NS && (jj + 1) * kProtUnit <= NS;
+          bool okv[4] = {true, true, true, true};
+          if (!all_in) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) okv[e] = slot_valid(sl0 + TK8[e], cs.len, L, ws_mod, n_rec);
+          }
+          // ---- QK: B = K codes of slot r (tile 0) and slot r + 8 (tile 1),
+          // channels 32*qd + [0, 32); pieces are swizzled by slot (r + 8 & 7 = r)
+          const uint4 kA0 = lds128(stg + r * D + 16 * ((2 * qd) ^ r));
+          const uint4 kB0 = lds128(stg + r * D + 16 * ((2 * qd + 1) ^ r));
+          const uint4 kA1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd) ^ r));
+          const uint4 kB1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd + 1) ^ r));
+          float dq0[4] = {0.f, 0.f, 0.f, 0.f}, dq1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s_ = 0; s_ < 8; ++s_) {
+            const uint32_t x0 = (s_ < 4 ? u4word(kA0, s_) : u4word(kB0, s_ - 4)) ^ 0x80808080u;
+            const uint32_t x1 = (s_ < 4 ? u4word(kA1, s_) : u4word(kB1, s_ - 4)) ^ 0x80808080u;
+            const uint2 qa = q8[16 * s_];
+            mma_f16(dq0, qa.x, 0u, qa.y, 0u, i8pair(x0, 0x4140u), i8pair(x0, 0x4342u));
+            mma_f16(dq1, qa.x, 0u, qa.y, 0u, i8pair(x1, 0x4140u), i8pair(x1, 0x4342u));
+          }
+          // scores of head r & 3 for the four slots
+          const float2 ksA = h2f2(lds32(stg + 2 * kProtUnit * D + 4 * qd));
+          const float2 ksB = h2f2(lds32(stg + 2 * kProtUnit * D + 16 + 4 * qd));
+          float sv[4] = {dq0[0] * ksA.x, dq0[1] * ksA.y, dq1[0] * ksB.x, dq1[1] * ksB.y};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sv[e] = okv[e] ? sv[e] * scale_log2 : -INFINITY;
+          float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+          if (__any_sync(0xffffffffu, tmax > m8 + kLazyLog2)) {  // lazy rescaling, as above
+            const float mnew = fmaxf(m8, tmax);
+            const float alpha = mnew == -INFINITY ? 1.f : ex2(m8 - mnew);
+            const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
+            const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
+#pragma unroll
+            for (int P = 0; P < 8; ++P) {
+              acc8[P][0] *= aA;
+              acc8[P][1] *= aB;
+              acc8[P][2] *= aA;
+              acc8[P][3] *= aB;
+            }
+            l8 *= alpha;
+            m8 = mnew;
+          }
+          const float mref = m8 == -INFINITY ? 0.f : m8;
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pv[e] = ex2(sv[e] - mref);
+          l8 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          // ---- PV: A = V codes transposed (rows = channels, k = 16 slots), B = p * s_v
+          uint32_t vsA = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 4 * qd);
+          uint32_t vsB = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 16 + 4 * qd);
+          vsA &= (okv[0] ? 0x0000FFFFu : 0u) | (okv[1] ? 0xFFFF0000u : 0u);
+          vsB &= (okv[2] ? 0x0000FFFFu : 0u) | (okv[3] ? 0xFFFF0000u : 0u);
+          const uint32_t pb0 = hmul2(pack_f16(pv[0], pv[1]) & p_keep, vsA);
+          const uint32_t pb1 = hmul2(pack_f16(pv[2], pv[3]) & p_keep, vsB);
+          const uint32_t vbase = stg + kProtUnit * D;
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {  // pieces 2 c2 and 2 c2 + 1
+            uint32_t vr[4];  // (slots 0-7, piece), (slots 8-15, piece), same for piece + 1
+            ldsm_x4_trans(vr, vbase + l8_row * D + 16 * ((2 * c2 + l8_pp) ^ l8_t));
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t xlo = vr[2 * h2] ^ 0x80808080u, xhi = vr[2 * h2 + 1] ^ 0x80808080u;
+              // rows r / r+8 = channels 16P + 2r / 16P + 2r + 1; k = slots 2qd,
+              // 2qd+1 (a0, a1) and 2qd+8, 2qd+9 (a2, a3)
+              mma_f16(acc8[2 * c2 + h2], i8pair(xlo, 0x4240u), i8pair(xlo, 0x4341u),
+                      i8pair(xhi, 0x4240u), i8pair(xhi, 0x4341u), pb0, pb1);
+            }
+          }
+        }
+        refill(st);
+      }
+      // publish this warp's state (it is read back below if INT4 units follow)
+      float lsum = (r < 4) ? l8 : 0.f;
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+      if (qd == 0 && r < 4) {
+        sm.mrg_m[warp][r] = m8;
+        sm.mrg_l[warp][r] = lsum;
+      }
+      if (lane < SG * (D / 32)) sm.mrg_mt[warp][lane / (D / 32)][lane % (D / 32)] = 0.f;
+      if (qd < 2) {
+        const int hA = 2 * qd, hB = 2 * qd + 1;
+#pragma unroll
+        for (int P = 0; P < 8; ++P) {
+          const int dd = 16 * P + 2 * r;
+          sm.mrg_o[warp][hA][dd] = acc8[P][0];
+          sm.mrg_o[warp][hB][dd] = acc8[P][1];
+          sm.mrg_o[warp][hA][dd + 1] = acc8[P][2];
+          sm.mrg_o[warp][hB][dd + 1] = acc8[P][3];
+        }
+      }
+    }
+    if (jj < hi || !have8) {
       // ============================================= INT4 pages (eq. 5.1)
       // Per unit of two pages.  QK^T with the tokens as MMA rows: A = the K
       // codes of the page's 16 tokens entered as fp16 subnormals (bit
@@ -606,8 +699,8 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // page PV against the transposed V codes (subnormals as well) with
       // P' = p * Delta_v, and the offset term sum_t p_t m_t of every group as
       // one more MMA whose A rows are the page's V offsets.  Units inside the
-      // region with both pages copied (all but a segment's first and last)
-      // skip every mask.
+      // region with both pages copied (all but its first and last) skip every
+      // mask.  A warp without units here publishes an empty state.
       uint4 qbf[4];  // this lane's B fragments of the four blocks (lo b0, lo b1, hi b0, hi b1)
 #pragma unroll
       for (int bl = 0; bl < 4; ++bl) qbf[bl] = sm.qp.qb[bl][lane];
@@ -615,7 +708,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       const float ksc = sm.qp.ks[qd];
       const int first_page = rg.sink_end / kPage;
       const int len = cs.len;
-      const int last_j = cs.n - 1;
+      const int n4 = cs.n - np;
       float m_run = -INFINITY, l_run = 0.f, m_thr = -INFINITY;  // m_thr = m_run + kLazyLog2
       float mtacc[4] = {0.f, 0.f, 0.f, 0.f};  // rows = groups (V offsets), columns = heads
       float acc[4][2][4];
@@ -625,6 +718,29 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[G_][hh][i] = 0.f;
+      if (have8) {
+        // carry the state of this warp's protected units over, from the
+        // publish above: the reference and sum of head q (the sum in the
+        // row-0 lanes, which the publish below adds up), and the outputs in
+        // this layout (even channels carry 2^-24, odd ones 2^-20)
+        __syncwarp();
+        m_run = sm.mrg_m[warp][qd];
+        m_thr = m_run + kLazyLog2;
+        if (r == 0) l_run = sm.mrg_l[warp][qd];
+        if (qd < 2) {
+#pragma unroll
+          for (int P = 0; P < 4; ++P)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int dd = 32 * P + 4 * r + 2 * hh;
+              acc[P][hh][0] = sm.mrg_o[warp][2 * qd][dd] * 0x1p-24f;
+              acc[P][hh][1] = sm.mrg_o[warp][2 * qd + 1][dd] * 0x1p-24f;
+              acc[P][hh][2] = sm.mrg_o[warp][2 * qd][dd + 1] * 0x1p-20f;
+              acc[P][hh][3] = sm.mrg_o[warp][2 * qd + 1][dd + 1] * 0x1p-20f;
+            }
+        }
+        __syncwarp();  // every lane has read before the publish below rewrites
+      }
       const int mrow = r < NG ? r : 0;  // offset-term MMA: this lane's A row group
       // lane offsets inside a page chunk: K codes (row r, quarter q: one word
       // per block), K meta of row r, this lane's quad of V Deltas (all
@@ -639,12 +755,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // holding tokens 2 q' and 2 q' + 1 for head r' (any value for r' > 3)
       const int src_a = (8 * qd + r) & 31, src_b = (8 * qd + 4 + r) & 31;
 
-      for (int jj = lo + warp; jj < hi; jj += kSW) {
+      for (; jj < hi; jj += kSW) {
+        const int j4 = jj - np;  // INT4 unit of the region
         const int ST = it;
         const uint32_t sb = stages_s + (uint32_t)(ST * SB);
         const uint32_t pv = stage_wait(ST);  // pages copied
-        const bool clean = (unsigned)(jj - 1) < (unsigned)(last_j - 1) && pv == 3u;
-        const int pg0 = first_page + kSPages * jj;
+        const bool clean = (unsigned)(j4 - 1) < (unsigned)(n4 - 2) && pv == 3u;
+        const int pg0 = first_page + kSPages * j4;
         // ---------------- S = K codes x Q^T and scores (eq. 5.1 per group),
         // log2 domain, relative to the running reference
         const float mref = m_run == -INFINITY ? 0.f : m_run;
@@ -836,137 +953,23 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
             sm.mrg_o[warp][hB][dd + 1] = acc[P][hh][3] * 0x1p20f;
           }
       }
-    } else {
-      // ================================= INT8 protected units (App. A.3)
-      // Per unit of 16 side slots: QK^T with the query rows (heads) against
-      // the slots' codes widened exactly to fp16 (two 8-slot tiles), scores
-      // scaled by each slot's K scale; then PV with the transposed codes
-      // against P' = p * s_v.  Slots outside the protected set are masked.
-      const int n_rec = cs.len > L.S ? cs.len - rg.rec_start : 0;
-      const int ws_mod = L.R > 0 ? rg.rec_start % L.R : 0;
-      float m8 = -INFINITY, l8 = 0.f;
-      float acc8[8][4];
-#pragma unroll
-      for (int P = 0; P < 8; ++P)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc8[P][i] = 0.f;
-      const uint2* q8 = &sm.qp.qfrag8[0][lane & 15];  // + 16 * s
-      for (int jj = lo + warp; jj < hi; jj += kSW, it = it + 1 == kSStages ? 0 : it + 1) {
-        const int st = it;
-        const bool ok = stage_wait(st) != 0u;
-        const uint32_t stg = smem_u32(my_stages) + st * SB;
-        if (ok) {
-          const int sl0 = jj * kProtUnit + 2 * qd;  // this lane's slots sl0 + {0, 1, 8, 9}
-          // a sequence of at least S + R tokens fills every sink and ring slot:
-          // only a unit reaching into the padding past NS needs the test
-          const bool all_in = cs.len >= NS && (jj + 1) * kProtUnit <= NS;
-          bool okv[4] = {true, true, true, true};
-          if (!all_in) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) okv[e] = slot_valid(sl0 + TK8[e], cs.len, L, ws_mod, n_rec);
-          }
-          // ---- QK: B = K codes of slot r (tile 0) and slot r + 8 (tile 1),
-          // channels 32*qd + [0, 32); pieces are swizzled by slot (r + 8 & 7 = r)
-          const uint4 kA0 = lds128(stg + r * D + 16 * ((2 * qd) ^ r));
-          const uint4 kB0 = lds128(stg + r * D + 16 * ((2 * qd + 1) ^ r));
-          const uint4 kA1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd) ^ r));
-          const uint4 kB1 = lds128(stg + (r + 8) * D + 16 * ((2 * qd + 1) ^ r));
-          float dq0[4] = {0.f, 0.f, 0.f, 0.f}, dq1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int s_ = 0; s_ < 8; ++s_) {
-            const uint32_t x0 = (s_ < 4 ? u4word(kA0, s_) : u4word(kB0, s_ - 4)) ^ 0x80808080u;
-            const uint32_t x1 = (s_ < 4 ? u4word(kA1, s_) : u4word(kB1, s_ - 4)) ^ 0x80808080u;
-            const uint2 qa = q8[16 * s_];
-            mma_f16(dq0, qa.x, 0u, qa.y, 0u, i8pair(x0, 0x4140u), i8pair(x0, 0x4342u));
-            mma_f16(dq1, qa.x, 0u, qa.y, 0u, i8pair(x1, 0x4140u), i8pair(x1, 0x4342u));
-          }
-          // scores of head r & 3 for the four slots
-          const float2 ksA = h2f2(lds32(stg + 2 * kProtUnit * D + 4 * qd));
-          const float2 ksB = h2f2(lds32(stg + 2 * kProtUnit * D + 16 + 4 * qd));
-          float sv[4] = {dq0[0] * ksA.x, dq0[1] * ksA.y, dq1[0] * ksB.x, dq1[1] * ksB.y};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sv[e] = okv[e] ? sv[e] * scale_log2 : -INFINITY;
-          float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-          if (__any_sync(0xffffffffu, tmax > m8 + kLazyLog2)) {  // lazy rescaling, as above
-            const float mnew = fmaxf(m8, tmax);
-            const float alpha = mnew == -INFINITY ? 1.f : ex2(m8 - mnew);
-            const float aA = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd) & 3));
-            const float aB = __shfl_sync(0xffffffffu, alpha, 4 * ((2 * qd + 1) & 3));
-#pragma unroll
-            for (int P = 0; P < 8; ++P) {
-              acc8[P][0] *= aA;
-              acc8[P][1] *= aB;
-              acc8[P][2] *= aA;
-              acc8[P][3] *= aB;
-            }
-            l8 *= alpha;
-            m8 = mnew;
-          }
-          const float mref = m8 == -INFINITY ? 0.f : m8;
-          float pv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pv[e] = ex2(sv[e] - mref);
-          l8 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-          // ---- PV: A = V codes transposed (rows = channels, k = 16 slots), B = p * s_v
-          uint32_t vsA = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 4 * qd);
-          uint32_t vsB = lds32(stg + 2 * kProtUnit * D + 2 * kProtUnit + 16 + 4 * qd);
-          vsA &= (okv[0] ? 0x0000FFFFu : 0u) | (okv[1] ? 0xFFFF0000u : 0u);
-          vsB &= (okv[2] ? 0x0000FFFFu : 0u) | (okv[3] ? 0xFFFF0000u : 0u);
-          const uint32_t pb0 = hmul2(pack_f16(pv[0], pv[1]) & p_keep, vsA);
-          const uint32_t pb1 = hmul2(pack_f16(pv[2], pv[3]) & p_keep, vsB);
-          const uint32_t vbase = stg + kProtUnit * D;
-#pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) {  // pieces 2 c2 and 2 c2 + 1
-            uint32_t vr[4];  // (slots 0-7, piece), (slots 8-15, piece), same for piece + 1
-            ldsm_x4_trans(vr, vbase + l8_row * D + 16 * ((2 * c2 + l8_pp) ^ l8_t));
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t xlo = vr[2 * h2] ^ 0x80808080u, xhi = vr[2 * h2 + 1] ^ 0x80808080u;
-              // rows r / r+8 = channels 16P + 2r / 16P + 2r + 1; k = slots 2qd,
-              // 2qd+1 (a0, a1) and 2qd+8, 2qd+9 (a2, a3)
-              mma_f16(acc8[2 * c2 + h2], i8pair(xlo, 0x4240u), i8pair(xlo, 0x4341u),
-                      i8pair(xhi, 0x4240u), i8pair(xhi, 0x4341u), pb0, pb1);
-            }
-          }
-        }
-        refill(st);
-      }
-      // publish this warp's state
-      float lsum = (r < 4) ? l8 : 0.f;
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-      if (qd == 0 && r < 4) {
-        sm.mrg_m[warp][r] = m8;
-        sm.mrg_l[warp][r] = lsum;
-      }
-      if (lane < SG * (D / 32)) sm.mrg_mt[warp][lane / (D / 32)][lane % (D / 32)] = 0.f;
-      if (qd < 2) {
-        const int hA = 2 * qd, hB = 2 * qd + 1;
-#pragma unroll
-        for (int P = 0; P < 8; ++P) {
-          const int dd = 16 * P + 2 * r;
-          sm.mrg_o[warp][hA][dd] = acc8[P][0];
-          sm.mrg_o[warp][hB][dd] = acc8[P][1];
-          sm.mrg_o[warp][hA][dd + 1] = acc8[P][2];
-          sm.mrg_o[warp][hB][dd + 1] = acc8[P][3];
-        }
-      }
     }
 
     // ----------------------------------------- segment end: partial + merge
-    // B1: every warp has published; merge into partial 2 * pair + region + c
-    // (sm.pcur, sm.new_q: written at this segment's start; the ticket thread
-    // rewrites sm.cs before the next barrier)
+    // B1: every warp has published; merge into partial pair + c, or into the
+    // output when no other CTA holds the pair (sm.pcur, sm.new_q: written at
+    // this segment's start; the ticket thread rewrites sm.cs before the next
+    // barrier)
     __syncthreads();
-    stream_merge_store(sm, part_o, part_lse, sm.pcur.s0 + sm.pcur.type + c);
+    const bool direct = sm.pcur.n0 == 1;
+    stream_merge_store(sm, part_o, part_lse, (long long)sm.pcur.pair + c, direct, sm.pcur.row0,
+                       out, out_lse);
     if (threadIdx.x == kTicketThread) {
       // the previous partial's ticket (taken one segment ago) decides whether
       // this CTA merges that pair now
       int go = 0;
       if (sm.pend.valid) {
-        go = pend_t == sm.pend.n0 + sm.pend.n1 - 1;
+        go = pend_t == sm.pend.n0 - 1;
         if (go) {
           __threadfence();  // acquire: the other CTAs' partials are visible
           sm.comb = sm.pend;
@@ -982,17 +985,21 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       stream_query_setup<NG>(sm, scale_log2);
     }
     __syncthreads();  // B2: partial stored; next pair's query set up; comb, cs written
-    if (threadIdx.x == kTicketThread && !defer) {
+    if (threadIdx.x == kTicketThread) {
       // take this partial's ticket with release semantics (the barrier above
       // makes the CTA's partial stores part of what is released); the
-      // result is read at the next boundary
-      pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], 1);
-      sm.pend = sm.pcur;
+      // result is read at the next boundary.  A pair written directly, or
+      // merged by the separate kernel (defer), takes none.
+      if (!defer && !direct) {
+        pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], 1);
+        sm.pend = sm.pcur;
+      } else {
+        sm.pend.valid = 0;
+      }
     }
     if (sm.go) {
       const Pend& cm = sm.comb;
-      stream_combine(part_o, part_lse, cm.s0, cm.c0, cm.n0, cm.s0 + 1, cm.c1, cm.n1, cm.row0, out,
-                     out_lse);
+      stream_combine(part_o, part_lse, (long long)cm.pair + cm.c0, cm.n0, cm.row0, out, out_lse);
     }
   }
   // the last partial's ticket
@@ -1000,7 +1007,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   if (threadIdx.x == kTicketThread) {
     int go = 0;
     if (sm.pend.valid) {
-      go = pend_t == sm.pend.n0 + sm.pend.n1 - 1;
+      go = pend_t == sm.pend.n0 - 1;
       if (go) {
         __threadfence();
         sm.comb = sm.pend;
@@ -1011,23 +1018,22 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   __syncthreads();
   if (sm.go) {
     const Pend& cm = sm.comb;
-    stream_combine(part_o, part_lse, cm.s0, cm.c0, cm.n0, cm.s0 + 1, cm.c1, cm.n1, cm.row0, out,
-                   out_lse);
+    stream_combine(part_o, part_lse, (long long)cm.pair + cm.c0, cm.n0, cm.row0, out, out_lse);
   }
 }
 
 // Eq. A1 for pairs whose partials are spread over many CTAs (few, long
 // sequences): run after decode_stream_kernel, one CTA per (pair, query head),
 // eight warps splitting the pair's partials.  The partial positions follow
-// from the stream's share arithmetic (U recorded by the decode kernel).
+// from the stream's share arithmetic, recounted from the lengths.
 constexpr int kMergeThreads = 256;
-// partials of one pair: each of its two regions spans at most every CTA of the grid
-constexpr int kMergeMaxParts = 2 * kMaxStreamCtas + 2;
+// partials of one pair: it spans at most every CTA of the grid
+constexpr int kMergeMaxParts = kMaxStreamCtas;
 __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
     Layout L, const int32_t* __restrict__ seq_lens, int B, const float* __restrict__ part_o,
-    const float* __restrict__ part_lse, int C, int by_cost,
-    uint16_t* __restrict__ out, float* __restrict__ out_lse) {
-  __shared__ long long red64[4][kMergeThreads / 32];
+    const float* __restrict__ part_lse, int C, uint16_t* __restrict__ out,
+    float* __restrict__ out_lse) {
+  __shared__ long long red64[2][kMergeThreads / 32];
   __shared__ float redf[kMergeThreads / 32];
   __shared__ float4 acc_s[kMergeThreads / 32][32];
   const int pair = blockIdx.x / SG, j = blockIdx.x % SG;
@@ -1035,45 +1041,35 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int len = clamp_len(__ldg(seq_lens + b), L);
   if (len == 0) return;  // the decode kernel wrote its zero output
-  // stream index and stream cost of the pair's first unit (the units and cost
-  // of all earlier sequences, then of the sequence's earlier kv heads), and the
-  // stream's length U and cost Wc, by the decode kernel's own count
-  long long v[4] = {0, 0, 0, 0};  // units and cost before sequence b; units and cost of all
+  // stream cost of the pair's first unit (the cost of all earlier sequences,
+  // then of the sequence's earlier kv heads), and the stream's cost Wc, by the
+  // decode kernel's own count
+  long long v[2] = {0, 0};  // cost before sequence b; cost of all
   for (int bb = threadIdx.x; bb < B; bb += kMergeThreads) {
     const int lb = clamp_len(__ldg(seq_lens + bb), L);
-    const int np_ = prot_units(lb, L), n4_ = int4_units(lb, L);
-    const long long u_ = (long long)L.h_kv * (np_ + n4_);
-    const long long c_ = (long long)L.h_kv * (seg_cost(np_, 0) + seg_cost(n4_, 1));
-    if (bb < b) {
-      v[0] += u_;
-      v[1] += c_;
-    }
-    v[2] += u_;
-    v[3] += c_;
+    const long long c_ = (long long)L.h_kv * seg_cost(prot_units(lb, L), int4_units(lb, L));
+    if (bb < b) v[0] += c_;
+    v[1] += c_;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
     if (lane == 0) red64[i][warp] = v[i];
   }
   __syncthreads();
-  long long pre = 0, pre_c = 0, U = 0, Wc = 0;
+  long long pre_c = 0, Wc = 0;
   for (int w = 0; w < kMergeThreads / 32; ++w) {
-    pre += red64[0][w];
-    pre_c += red64[1][w];
-    U += red64[2][w];
-    Wc += red64[3][w];
+    pre_c += red64[0][w];
+    Wc += red64[1][w];
   }
-  if (!by_cost) Wc = 0;
-  const int np = prot_units(len, L), n4 = int4_units(len, L);
-  const long long gs = pre + (long long)h * (np + n4);
-  const long long pcs = pre_c + (long long)h * (seg_cost(np, 0) + seg_cost(n4, 1));
-  const int Cw = by_cost ? stream_ctas(Wc, C) : (int)min((long long)C, U);
-  const PairParts pp = pair_parts(gs, pcs, np, n4, by_cost != 0, U, Wc, Cw);
-  const int c0 = pp.c0, n0 = pp.n0, c1 = pp.c1, n1 = pp.n1;
-  const int n = n0 + n1;
-  auto pidx = [&](int k) { return k < n0 ? 2LL * pair + c0 + k : 2LL * pair + 1 + c1 + (k - n0); };
+  const int np = prot_units(len, L), nu = np + int4_units(len, L);
+  const long long pcs = pre_c + (long long)h * seg_cost(np, nu - np);
+  int c0 = 0, n = 0;
+  pair_ctas(pcs, np, nu, Wc, stream_ctas(Wc, C), c0, n);
+  if (n == 1) return;  // a pair held by one CTA: the decode kernel wrote it
+  const long long P0 = (long long)pair + c0;
+  auto pidx = [&](int k) { return P0 + k; };
   // Everything above reads only the inputs; what follows reads what the decode
   // kernel wrote (launched as its programmatic dependent, this is where the
   // merge waits for it to complete; otherwise the wait returns at once).
@@ -1156,15 +1152,15 @@ bool stream_supported(const Layout& L) { return L.d_h == SD && L.h_q == SG * L.h
 
 // Partial results the stream kernel may write for num_seqs sequences.
 long long stream_partials(const Layout& L, int num_seqs) {
-  return 2LL * num_seqs * L.h_kv + kMaxStreamCtas;
+  return (long long)num_seqs * L.h_kv + kMaxStreamCtas;
 }
 
-// Eq. A1 for every pair from the partials a work-balanced decode kernel left
-// on a grid of C CTAs, its stream cut into equal unit counts or (by_cost)
-// equal costs; the merge recounts the stream from the lengths.
+// Eq. A1 for every pair held by more than one CTA, from the partials the
+// work-balanced decode kernel left on a grid of C CTAs; the merge recounts
+// the stream from the lengths.
 cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int num_seqs,
-                                const float* part_o, const float* part_lse, int C, int by_cost,
-                                bool overlap, uint16_t* out, float* out_lse, cudaStream_t st) {
+                                const float* part_o, const float* part_lse, int C, bool overlap,
+                                uint16_t* out, float* out_lse, cudaStream_t st) {
   // overlap: the previous kernel on the stream lets its dependents start early
   // (griddepcontrol.launch_dependents); this kernel then starts on the SMs its
   // CTAs free and waits for its completion only before reading its results
@@ -1179,7 +1175,7 @@ cudaError_t launch_stream_merge(const Layout& L, const int32_t* seq_lens, int nu
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, stream_merge_kernel, L, seq_lens, num_seqs, part_o, part_lse, C,
-                            by_cost, out, out_lse);
+                            out, out_lse);
 }
 
 template <int NG>
@@ -1223,8 +1219,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
       sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (defer)
-    e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, grid, 1, true, out, out_lse,
-                            st);
+    e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, grid, true, out, out_lse, st);
   return e;
 }
 

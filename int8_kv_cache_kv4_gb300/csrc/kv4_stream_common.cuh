@@ -1,7 +1,7 @@
-// kv4_stream_common.cuh -- the unit stream shared by the work-balanced decode
-// kernels (KV4-RL Sec. 5.3, App. A.3): per (sequence, kv head) pair, its
-// protected INT8 units, then its INT4 units; segment walking, the protected
-// slot test and the query conversion both kernels use.
+// kv4_stream_common.cuh -- the unit stream of the work-balanced decode kernel
+// (KV4-RL Sec. 5.3, App. A.3): per (sequence, kv head) pair, its protected
+// INT8 units, then its INT4 units; the cost model that cuts the stream over
+// CTAs, segment walking, the protected slot test and the query conversion.
 #pragma once
 #include "kv4_common.cuh"
 
@@ -17,11 +17,12 @@ constexpr int kProtUnit = 16;       // side-cache slots per protected unit
 // and the accumulators are rescaled on a few pages only.  The split's
 // log-normaliser m + log2(l) is exact for any reference.
 constexpr float kLazyLog2 = 8.f;
-// One segment of the stream: region `type` (0 protected, 1 INT4) of pair (b, h).
+// One segment of the stream: the units of pair (b, h), its protected units
+// first (np of them), then its INT4 units (n - np).
 struct Seg {
   long long start;  // stream index of its first unit
   long long cs;     // cost of the stream before it (see seg_cost)
-  int b, h, type, len, n;
+  int b, h, len, np, n;
 };
 
 // Cost model of the stream for splitting it over CTAs: an INT4 unit counts 4,
@@ -29,8 +30,27 @@ struct Seg {
 // barriers, merge and query setup at a segment boundary).  Ratios measured on
 // GB300 (per-CTA timelines of the work-balanced kernel).
 constexpr int kCost4 = 4, kCost8 = 7, kCostSeg = 24;
-__host__ __device__ inline long long seg_cost(int n, int type) {
-  return n ? kCostSeg + (long long)n * (type == 0 ? kCost8 : kCost4) : 0;
+// cost of a pair with np protected and n4 INT4 units
+__host__ __device__ inline long long seg_cost(int np, int n4) {
+  return np + n4 ? kCostSeg + (long long)np * kCost8 + (long long)n4 * kCost4 : 0;
+}
+// stream cost of unit j of a segment from the segment's start: unit 0 is at
+// 0 (the segment start is counted with its first unit), unit j > 0 at
+// kCostSeg + the cost of units 0 .. j - 1
+__device__ inline long long unit_cost_at(int j, int np) {
+  if (j <= 0) return 0;
+  return kCostSeg + (j <= np ? (long long)j * kCost8
+                             : (long long)np * kCost8 + (long long)(j - np) * kCost4);
+}
+// the first unit j of a segment (np protected, n units) with
+// unit_cost_at(j) >= x; n when there is none
+__device__ inline int unit_at_within(long long x, int np, int n) {
+  if (x <= 0) return 0;
+  const long long y = x - kCostSeg;
+  long long j;
+  if (y <= (long long)np * kCost8) j = (y + kCost8 - 1) / kCost8;
+  else j = np + (y - (long long)np * kCost8 + kCost4 - 1) / kCost4;
+  return (int)min((long long)n, max(1LL, j));
 }
 
 __device__ inline int clamp_len(int len, const Layout& L) {
@@ -52,6 +72,14 @@ __device__ inline int int4_pages(int len, const Layout& L) {
 __device__ inline int int4_units(int len, const Layout& L) {
   return (int4_pages(len, L) + kSPages - 1) / kSPages;
 }
+// the segment fields of sequence b's kv head h (start and cs are the caller's)
+__device__ inline void seg_set(Seg& s, int b, int h, int len, const Layout& L) {
+  s.b = b;
+  s.h = h;
+  s.len = len;
+  s.np = prot_units(len, L);
+  s.n = s.np + int4_units(len, L);
+}
 
 // Next non-empty segment (b == B when the stream is exhausted).  Sequences of
 // length 0 are skipped whole, one length load each.  A caller that needs no
@@ -61,27 +89,21 @@ __device__ inline int int4_units(int len, const Layout& L) {
 __device__ inline void seg_next(Seg& s, const Layout& L, const int32_t* seq_lens, int B,
                                 long long stop = 0x7fffffffffffffffLL) {
   s.start += s.n;
-  s.cs += seg_cost(s.n, s.type);
+  s.cs += seg_cost(s.np, s.n - s.np);
   if (s.start >= stop) {
     s.b = B;
     return;
   }
-  do {  // empty segments add nothing to start or cs
-    if (s.type == 0) {
-      s.type = 1;
-      s.n = int4_units(s.len, L);
-    } else {
-      s.type = 0;
-      if (++s.h == L.h_kv) {
-        s.h = 0;
-        do {
-          ++s.b;
-          s.len = s.b < B ? clamp_len(__ldg(seq_lens + s.b), L) : 0;
-        } while (s.len == 0 && s.b < B);
-      }
-      s.n = prot_units(s.len, L);
-    }
-  } while (s.n == 0 && s.b < B);
+  // the next kv head of the same sequence has the same units; past the last
+  // one, the next sequence that is not empty
+  if (++s.h == L.h_kv) {
+    int b = s.b, len = 0;
+    do {
+      ++b;
+      len = b < B ? clamp_len(__ldg(seq_lens + b), L) : 0;
+    } while (len == 0 && b < B);
+    seg_set(s, b, 0, len, L);
+  }
 }
 
 // Atomic add with release semantics at GPU scope; returns the old value.
@@ -89,13 +111,6 @@ __device__ inline int atom_add_release_gpu(int32_t* p, int v) {
   int old;
   asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
-}
-
-// CTA holding stream unit u when U >= C units are split over C CTAs as
-// [c*U/C, (c+1)*U/C) (every CTA then holds at least one unit); the
-// stream kernel (decode_stream_kernel) cuts by cost instead.
-__device__ inline int cta_of(long long u, long long U, int C) {
-  return (int)(((u + 1) * C - 1) / U);
 }
 
 // Is side slot sl part of the protected set of a sequence of length len?
