@@ -19,8 +19,9 @@
 // its INT4 units, carrying one online-softmax state across.  When a segment
 // ends the warps' states are merged into one partial result (a locally
 // normalised output and its log-normaliser) for the pair's four query heads.
-// A pair held by one CTA is written out directly; otherwise the CTA that
-// stores the last partial of the pair merges them (eq. A1) into the output.
+// A pair held by one CTA is written out directly; otherwise each CTA adds its
+// unit count to the pair's ticket after storing its partial, and the one that
+// completes the count merges the partials (eq. A1) into the output.
 // The CTA c holding units of pair p writes partial p + c: CTA ranges are
 // contiguous, ordered and non-empty, so these indices are distinct and below
 // pairs + C.
@@ -65,10 +66,65 @@ constexpr int kStreamMinBlocks = KV4_STREAM_CTAS_PER_SM;
 // never gives more units than the others.
 constexpr int kTicketThread = (kSW - 1) * 32;
 
-// CTAs the stream of total cost Wc is cut over: at most C, and few enough that
-// every share is at least one unit's cost wide (no CTA is left without units).
-__device__ inline int stream_ctas(long long Wc, int C) {
-  return Wc > 0 ? (int)max(1LL, min((long long)C, Wc / (kCostSeg + kCost8))) : 0;
+// Share weights by launch rank.  The grid holds kStreamMinBlocks CTAs per
+// SM, placed in block order (CTA c is the (c / SMs)-th on its SM), and the
+// warp schedulers favour the older CTAs of an SM: measured on GB300, the
+// first CTA of an SM streams its share about 18% faster than the fourth.  The
+// stream is therefore cut into shares proportional to these weights, so that
+// an SM's CTAs finish together.
+#ifndef KV4_STREAM_RANK_STEP
+#define KV4_STREAM_RANK_STEP 6
+#endif
+constexpr int kRankW0 = 118, kRankStep = KV4_STREAM_RANK_STEP;  // weight of rank k: 118 - 6 k
+__host__ __device__ constexpr int rank_w(int k) { return kRankW0 - kRankStep * k; }
+static_assert(rank_w(kStreamMinBlocks - 1) > 0, "positive weights");
+// CTAs per launch rank of a grid of C CTAs (C / kStreamMinBlocks, at least 1)
+__device__ inline int rank_width(int C) { return max(1, C / kStreamMinBlocks); }
+// summed weight of CTAs 0 .. c - 1 (S CTAs per rank; the last rank takes the rest)
+__device__ inline long long share_weight(int c, int S) {
+  long long f = 0;
+#pragma unroll
+  for (int k = 0; k < kStreamMinBlocks; ++k) {
+    const int lo = k * S, hi = k == kStreamMinBlocks - 1 ? c : min(c, lo + S);
+    if (hi > lo) f += (long long)rank_w(k) * (hi - lo);
+  }
+  return f;
+}
+// The stream of cost Wc cut over Cw CTAs: CTA c holds the units whose cost
+// lies in [T(c), T(c + 1)), T(c) = ceil(Wc F(c) / F(Cw)) with F = share_weight.
+struct Cut {
+  long long Wc, Ft;  // stream cost, summed weight of all Cw CTAs
+  int Cw, S;
+  __device__ long long start(int c) const { return (Wc * share_weight(c, S) + Ft - 1) / Ft; }
+  // the CTA holding stream cost x (0 <= x < Wc): the last c with
+  // F(c) <= floor(x F(Cw) / Wc)
+  __device__ int cta_of(long long x) const {
+    const long long Y = (x * Ft) / Wc;
+    long long f = 0;
+#pragma unroll
+    for (int k = 0; k < kStreamMinBlocks; ++k) {
+      const int lo = k * S;
+      if (lo >= Cw) break;
+      const int hi = k == kStreamMinBlocks - 1 ? Cw : min(Cw, lo + S);
+      const long long fk = (long long)rank_w(k) * (hi - lo);
+      if (Y < f + fk) return min(Cw - 1, lo + (int)((Y - f) / rank_w(k)));
+      f += fk;
+    }
+    return Cw - 1;
+  }
+};
+// The cut of a stream of cost Wc over a grid of C CTAs: at most C shares, and
+// few enough that every share is at least one unit's cost wide (no CTA is left
+// without units): a share is at least Wc w_min / (w_max Cw) wide, and
+// consecutive units start at most kCostSeg + kCost8 apart.
+__device__ inline Cut stream_cut(long long Wc, int C) {
+  Cut k;
+  k.Wc = Wc;
+  constexpr long long w_min = rank_w(kStreamMinBlocks - 1), w_max = rank_w(0);
+  k.Cw = Wc > 0 ? (int)max(1LL, min((long long)C, Wc * w_min / ((kCostSeg + kCost8) * w_max))) : 0;
+  k.S = rank_width(C);
+  k.Ft = share_weight(k.Cw, k.S);
+  return k;
 }
 
 // First unit whose stream cost (the cost of all units before it, a segment's
@@ -93,20 +149,22 @@ __device__ inline long long unit_at_cost(long long T, int b_lo, int b_hi, long l
 }
 
 // CTAs c0 .. c0 + n0 - 1 holding the units of a pair (np protected, n in
-// all) whose first unit lies at stream cost pcs, when the stream of cost Wc
-// is cut over Cw CTAs: CTA c holds the units whose cost lies in
-// [ceil(c Wc / Cw), ceil((c + 1) Wc / Cw)), so a unit at cost x is in CTA
-// floor(x Cw / Wc).
-__device__ inline void pair_ctas(long long pcs, int np, int n, long long Wc, int Cw, int& c0,
-                                 int& n0) {
-  c0 = (int)((pcs * Cw) / Wc);
-  n0 = (int)(((pcs + unit_cost_at(n - 1, np)) * Cw) / Wc) - c0 + 1;
+// all) whose first unit lies at stream cost pcs.
+__device__ inline void pair_ctas(long long pcs, int np, int n, const Cut& k, int& c0, int& n0) {
+  c0 = k.cta_of(pcs);
+  n0 = k.cta_of(pcs + unit_cost_at(n - 1, np)) - c0 + 1;
 }
 
 // A pair whose partial results are to be merged, with where they are.
 struct Pend {
-  long long row0;      // first output row (sequence * h_q + kv head * G)
-  int pair, c0, n0, valid;
+  long long row0;  // first output row (sequence * h_q + kv head * G)
+  long long pcs;   // stream cost before the pair's first unit
+  int pair;        // sequence * h_kv + kv head
+  int np, n;       // the pair's protected and total unit counts
+  int mine;        // units of the pair this CTA holds
+  int direct;      // this CTA holds all of them
+  int valid;
+  int c0, n0;      // (merging CTA) the CTAs holding the pair's partials
 };
 
 struct __align__(16) StreamSmem {
@@ -120,9 +178,8 @@ struct __align__(16) StreamSmem {
   float mrg_l[kSW][SG];
   float mrg_mt[kSW][SG][SD / 32];
   long long total, totalc;          // units and cost of the stream
-  long long start_pre;              // stream index of the first unit of sequence start_b
-  long long start_pre_c;            // stream cost before sequence start_b
-  int cw;                           // CTAs the stream is cut over
+  long long cut_b, cut_e;           // start-up: first unit of this CTA's share and of the next
+  Cut cut;                          // the stream's cut over the CTAs
   long long u_begin, u_end;         // this CTA's share of the stream
   Seg cs;                           // current segment of this CTA
   Seg prod[kSW];                    // producer cursors (segment of each warp's next unit)
@@ -257,6 +314,18 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
   if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
 }
 
+// Ticket thread: did the ticket taken for partial sm.pend (old value t) bring
+// the pair's count of finished units to its total?  Then this CTA merges the
+// pair: the CTAs holding its partials are worked out here, once per pair.
+__device__ inline int pend_take(StreamSmem& sm, int t) {
+  if (!sm.pend.valid || t + sm.pend.mine != sm.pend.n) return 0;
+  __threadfence();  // acquire: the other CTAs' partials are visible
+  Pend cm = sm.pend;
+  pair_ctas(cm.pcs, cm.np, cm.n, sm.cut, cm.c0, cm.n0);
+  sm.comb = cm;
+  return 1;
+}
+
 template <int NG>
 __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     Layout L, const uint8_t* __restrict__ paged, const uint8_t* __restrict__ side,
@@ -291,12 +360,17 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     mine_c += (long long)L.h_kv * seg_cost(np, n4);
   }
   if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
+  if (lane == 0) {  // (made visible by the barriers below)
+    for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
+    if (warp == 0) mbar_init(&sm.qbar, 1);
+    fence_mbar_init();
+  }
   sm.scan[threadIdx.x] = mine;
   sm.scan[kST + threadIdx.x] = mine_c;
   if (threadIdx.x == 0) {
     sm.start_b = B;
-    sm.u_begin = -1;  // (set below by the thread that finds this CTA's first / end unit)
-    sm.u_end = -1;
+    sm.cut_b = -1;  // (set below by the threads that find this CTA's first / end unit)
+    sm.cut_e = -1;
   }
   __syncthreads();
   if (warp < 2) {  // exclusive prefixes over the per-thread counts (warp 0) and costs (warp 1)
@@ -325,22 +399,24 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   }
   __syncthreads();
   // The stream is cut by cost over Cw CTAs: CTA c takes the units from the
-  // first whose stream cost reaches c Wc / Cw up to the first whose cost
-  // reaches (c + 1) Wc / Cw.  Cw keeps every share at least one unit's cost
-  // wide, so every working CTA holds a unit (the partial counts rely on it).
+  // first whose stream cost reaches T(c) up to the first whose cost reaches
+  // T(c + 1) (Cut: shares weighted by launch rank).  Cw keeps every share at
+  // least one unit's cost wide, so every working CTA holds a unit (the
+  // partial counts rely on it).
   const long long U = sm.total, Wc = sm.totalc;
-  const int Cw = stream_ctas(Wc, C);
+  const Cut cut = stream_cut(Wc, C);
+  const int Cw = cut.Cw;
   if (c < Cw) {
-    const long long Tb = (c * Wc + Cw - 1) / Cw, Te = ((c + 1) * Wc + Cw - 1) / Cw;
+    const long long Tb = cut.start(c), Te = cut.start(c + 1);
     const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kST + threadIdx.x];
     if (Tb >= exc && Tb < exc + mine_c)
-      sm.u_begin = unit_at_cost(Tb, b_lo, b_hi, exu, exc, L, seq_lens);
+      sm.cut_b = unit_at_cost(Tb, b_lo, b_hi, exu, exc, L, seq_lens);
     if (Te < Wc && Te >= exc && Te < exc + mine_c)
-      sm.u_end = unit_at_cost(Te, b_lo, b_hi, exu, exc, L, seq_lens);
+      sm.cut_e = unit_at_cost(Te, b_lo, b_hi, exu, exc, L, seq_lens);
   }
   __syncthreads();
-  const long long u_begin = c < Cw ? sm.u_begin : U;
-  const long long u_end = c < Cw && sm.u_end >= 0 ? sm.u_end : U;
+  const long long u_begin = c < Cw ? sm.cut_b : U;
+  const long long u_end = c < Cw && sm.cut_e >= 0 ? sm.cut_e : U;
   if (u_begin < u_end) {
     const long long ex = sm.scan[threadIdx.x];
     if (u_begin >= ex && u_begin < ex + mine) {
@@ -350,9 +426,22 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         const int np = prot_units(len, L), n4 = int4_units(len, L);
         const long long ub = (long long)L.h_kv * (np + n4);
         if (u_begin < pre + ub) {
+          // this CTA's first segment, set up by the thread that found it; the
+          // first pair's query is fetched ahead of the page copies issued
+          // below (the copy engine serves one SM's copies in order: behind
+          // them it would arrive last)
+          Seg cs;
+          seg_set(cs, b, 0, len, L);
+          cs.start = pre;
+          cs.cs = pre_c;
+          while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
+          sm.cs = cs;
           sm.start_b = b;
-          sm.start_pre = pre;
-          sm.start_pre_c = pre_c;
+          sm.u_begin = u_begin;
+          sm.u_end = u_end;
+          sm.cut = cut;
+          sm.pend.valid = 0;
+          stream_query_fetch(sm, q, (long long)cs.b * L.h_q + (long long)cs.h * SG);
           break;
         }
         pre += ub;
@@ -361,33 +450,22 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     }
   }
   // sequences with nothing to attend: zero output, log-normaliser -inf
-  for (int b = c; b < B; b += C) {
-    if (clamp_len(__ldg(seq_lens + b), L) != 0) continue;
-    for (int idx = threadIdx.x; idx < L.h_q * D; idx += kST)
-      out[(long long)b * L.h_q * D + idx] = 0;
-    if (out_lse)
-      for (int idx = threadIdx.x; idx < L.h_q; idx += kST)
-        out_lse[(long long)b * L.h_q + idx] = -INFINITY;
-  }
-  if (lane == 0) {
-    for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
-    if (warp == 0) mbar_init(&sm.qbar, 1);
-    fence_mbar_init();
-  }
+  // (written at the end, off the path to the first page copies)
+  auto zero_empty = [&]() {
+    for (int b = c; b < B; b += C) {
+      if (clamp_len(__ldg(seq_lens + b), L) != 0) continue;
+      for (int idx = threadIdx.x; idx < L.h_q * D; idx += kST)
+        out[(long long)b * L.h_q * D + idx] = 0;
+      if (out_lse)
+        for (int idx = threadIdx.x; idx < L.h_q; idx += kST)
+          out_lse[(long long)b * L.h_q + idx] = -INFINITY;
+    }
+  };
   __syncthreads();
-  if (sm.start_b >= B) return;  // no units for this CTA
-  if (threadIdx.x == 0) {
-    Seg cs;
-    seg_set(cs, sm.start_b, 0, clamp_len(__ldg(seq_lens + sm.start_b), L), L);
-    cs.start = sm.start_pre;
-    cs.cs = sm.start_pre_c;
-    sm.cw = Cw;
-    while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
-    sm.cs = cs;
-    sm.u_begin = u_begin;
-    sm.u_end = u_end;
+  if (sm.start_b >= B) {  // no units for this CTA
+    zero_empty();
+    return;
   }
-  __syncthreads();
 
   // ------------------------------------------------------ producer (lane 0)
   const int NS = L.S + L.R;
@@ -525,13 +603,9 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   constexpr int TK8[4] = {0, 1, 8, 9};  // INT8 unit: this lane's slots 2 * qd + TK8[e]
 
   int it = 0;  // stage of this warp's next unit (0 .. kSStages - 1)
-  int pend_t = 0;  // thread 0: ticket value returned for the pending partial
+  int pend_t = 0;  // ticket thread: ticket value returned for the pending partial
+  bool dep_waited = false;  // ticket thread: the ticket-zeroing grid has completed
   uint32_t qphase = 0;  // completed copies into sm.qraw
-  if (threadIdx.x == kTicketThread) {
-    sm.pend.valid = 0;
-    const Seg c0s = sm.cs;
-    stream_query_fetch(sm, q, (long long)c0s.b * L.h_q + (long long)c0s.h * SG);
-  }
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
   ++qphase;
   stream_query_setup<NG>(sm, scale_log2);
@@ -553,8 +627,12 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       sm.nx = nx;
       Pend pd;
       pd.row0 = (long long)cs.b * L.h_q + (long long)cs.h * SG;
+      pd.pcs = cs.cs;
       pd.pair = cs.b * L.h_kv + cs.h;
-      pair_ctas(cs.cs, cs.np, cs.n, sm.totalc, sm.cw, pd.c0, pd.n0);
+      pd.np = cs.np;
+      pd.n = cs.n;
+      pd.mine = (int)(min(sm.u_end, cs.start + cs.n) - max(sm.u_begin, cs.start));
+      pd.direct = pd.mine == cs.n;
       pd.valid = 1;
       sm.pcur = pd;
     }
@@ -961,21 +1039,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     // this segment's start; the ticket thread rewrites sm.cs before the next
     // barrier)
     __syncthreads();
-    const bool direct = sm.pcur.n0 == 1;
+    const bool direct = sm.pcur.direct;
     stream_merge_store(sm, part_o, part_lse, (long long)sm.pcur.pair + c, direct, sm.pcur.row0,
                        out, out_lse);
     if (threadIdx.x == kTicketThread) {
       // the previous partial's ticket (taken one segment ago) decides whether
       // this CTA merges that pair now
-      int go = 0;
-      if (sm.pend.valid) {
-        go = pend_t == sm.pend.n0 - 1;
-        if (go) {
-          __threadfence();  // acquire: the other CTAs' partials are visible
-          sm.comb = sm.pend;
-        }
-      }
-      sm.go = go;
+      sm.go = pend_take(sm, pend_t);
       sm.cs = sm.nx;  // read by all after the next barrier
     }
     if (sm.new_q) {  // fragments are not read again before the next barrier
@@ -991,7 +1061,13 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // result is read at the next boundary.  A pair written directly, or
       // merged by the separate kernel (defer), takes none.
       if (!defer && !direct) {
-        pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], 1);
+        // the tickets are zeroed by the kernel launched before this one, which
+        // lets this grid start early (programmatic dependent launch)
+        if (!dep_waited) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          dep_waited = true;
+        }
+        pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], sm.pcur.mine);
         sm.pend = sm.pcur;
       } else {
         sm.pend.valid = 0;
@@ -1005,21 +1081,23 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   // the last partial's ticket
   __syncthreads();
   if (threadIdx.x == kTicketThread) {
-    int go = 0;
-    if (sm.pend.valid) {
-      go = pend_t == sm.pend.n0 - 1;
-      if (go) {
-        __threadfence();
-        sm.comb = sm.pend;
-      }
-    }
-    sm.go = go;
+    sm.go = pend_take(sm, pend_t);
   }
   __syncthreads();
   if (sm.go) {
     const Pend& cm = sm.comb;
     stream_combine(part_o, part_lse, (long long)cm.pair + cm.c0, cm.n0, cm.row0, out, out_lse);
   }
+  zero_empty();
+}
+
+// Zeroes the completion tickets of the fused merge, then lets the decode
+// kernel launched after it start (its CTAs wait for this grid only before
+// their first ticket).
+__global__ void __launch_bounds__(256) stream_tickets_zero_kernel(int32_t* __restrict__ tickets,
+                                                                 int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) tickets[i] = 0;
 }
 
 // Eq. A1 for pairs whose partials are spread over many CTAs (few, long
@@ -1066,7 +1144,7 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   const int np = prot_units(len, L), nu = np + int4_units(len, L);
   const long long pcs = pre_c + (long long)h * seg_cost(np, nu - np);
   int c0 = 0, n = 0;
-  pair_ctas(pcs, np, nu, Wc, stream_ctas(Wc, C), c0, n);
+  pair_ctas(pcs, np, nu, stream_cut(Wc, C), c0, n);
   if (n == 1) return;  // a pair held by one CTA: the decode kernel wrote it
   const long long P0 = (long long)pair + c0;
   auto pidx = [&](int k) { return P0 + k; };
@@ -1210,14 +1288,32 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   // With few pairs each one spreads over many CTAs; its merge then runs as a
   // separate, wider kernel instead of in the last CTA.
   const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
-  // the in-kernel merge counts finished CTAs per pair on tickets that start at 0
-  if (!defer && (e = cudaMemsetAsync(tickets, 0, sizeof(int32_t) * (size_t)num_seqs * L.h_kv, st)) !=
-                    cudaSuccess)
-    return e;
-  decode_stream_kernel<NG><<<grid, kST, smem, st>>>(
-      L, (const uint8_t*)paged, (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
-      sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The in-kernel merge counts finished units per pair on tickets that start
+  // at 0.  They are zeroed by a small kernel that lets the decode grid start
+  // at once (programmatic dependent launch): its start-up overlaps the
+  // zeroing, and only the ticket thread waits for it, before its first ticket.
+  const int n_tickets = num_seqs * L.h_kv;
+  if (!defer && n_tickets > 0) {
+    stream_tickets_zero_kernel<<<std::min(64, (n_tickets + 255) / 256), 256, 0, st>>>(tickets,
+                                                                                    n_tickets);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kST);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = defer ? 0 : 1;
+    e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<NG>, L, (const uint8_t*)paged,
+                           (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
+                           sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
+    if (e != cudaSuccess) return e;
+  }
   if (defer)
     e = launch_stream_merge(L, seq_lens, num_seqs, part_o, part_lse, grid, true, out, out_lse, st);
   return e;
