@@ -186,8 +186,8 @@ struct __align__(16) StreamSmem {
   Seg nx;                           // segment after cs (ticket thread, at segment start)
   Pend pcur;                        // partial bookkeeping of segment cs (ticket thread)
   Pend pend;                        // partial whose ticket is in flight (ticket thread)
-  Pend comb;                        // pair to merge at this boundary
-  int go;                           // comb is valid
+  Pend comb[2];                     // pair to merge at boundary k (slot k & 1)
+  int go[2];                        // comb[k & 1] is valid
   int new_q;                        // a next segment follows (its query is being copied)
   int start_b;
   uint64_t bar[kSW][kSStages];      // stage completion (one per warp and stage)
@@ -233,7 +233,7 @@ __device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ pa
   for (int o = 1; o < kSW; o <<= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
   Lt = __shfl_sync(0xffffffffu, Lt, 0);
   const bool empty = !(Lt > 0.f);
-  const float f = empty ? 0.f : e / Lt;  // lanes 0 .. kSW-1: weight of warp `lane`
+  const float f = empty ? 0.f : e * __frcp_rn(Lt);  // lanes 0 .. kSW-1: weight of warp `lane`
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int w = 0; w < kSW; ++w) {
@@ -314,16 +314,22 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
   if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
 }
 
-// Ticket thread: did the ticket taken for partial sm.pend (old value t) bring
-// the pair's count of finished units to its total?  Then this CTA merges the
-// pair: the CTAs holding its partials are worked out here, once per pair.
-__device__ inline int pend_take(StreamSmem& sm, int t) {
-  if (!sm.pend.valid || t + sm.pend.mine != sm.pend.n) return 0;
-  __threadfence();  // acquire: the other CTAs' partials are visible
-  Pend cm = sm.pend;
-  pair_ctas(cm.pcs, cm.np, cm.n, sm.cut, cm.c0, cm.n0);
-  sm.comb = cm;
-  return 1;
+// Ticket thread, at boundary k: did the ticket taken for partial sm.pend
+// (old value t) bring the pair's count of finished units to its total?  Then
+// this CTA merges the pair after the boundary: the CTAs holding its partials
+// are worked out here, once per pair.  Slot k & 1 is read after the boundary's
+// second barrier; it is written again two boundaries later, when every thread
+// has passed the barriers in between.
+__device__ inline void pend_take(StreamSmem& sm, int t, int k) {
+  int go = 0;
+  if (sm.pend.valid && t + sm.pend.mine == sm.pend.n) {
+    __threadfence();  // acquire: the other CTAs' partials are visible
+    Pend cm = sm.pend;
+    pair_ctas(cm.pcs, cm.np, cm.n, sm.cut, cm.c0, cm.n0);
+    sm.comb[k & 1] = cm;
+    go = 1;
+  }
+  sm.go[k & 1] = go;
 }
 
 template <int NG>
@@ -605,6 +611,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   int it = 0;  // stage of this warp's next unit (0 .. kSStages - 1)
   int pend_t = 0;  // ticket thread: ticket value returned for the pending partial
   bool dep_waited = false;  // ticket thread: the ticket-zeroing grid has completed
+  int nb = 0;               // segment boundaries passed
   uint32_t qphase = 0;  // completed copies into sm.qraw
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
   ++qphase;
@@ -1034,6 +1041,9 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     }
 
     // ----------------------------------------- segment end: partial + merge
+    // the previous partial's ticket (taken one boundary ago) decides whether
+    // this CTA merges that pair after this boundary
+    if (threadIdx.x == kTicketThread) pend_take(sm, pend_t, nb);
     // B1: every warp has published; merge into partial pair + c, or into the
     // output when no other CTA holds the pair (sm.pcur, sm.new_q: written at
     // this segment's start; the ticket thread rewrites sm.cs before the next
@@ -1042,12 +1052,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     const bool direct = sm.pcur.direct;
     stream_merge_store(sm, part_o, part_lse, (long long)sm.pcur.pair + c, direct, sm.pcur.row0,
                        out, out_lse);
-    if (threadIdx.x == kTicketThread) {
-      // the previous partial's ticket (taken one segment ago) decides whether
-      // this CTA merges that pair now
-      sm.go = pend_take(sm, pend_t);
-      sm.cs = sm.nx;  // read by all after the next barrier
-    }
+    if (threadIdx.x == kTicketThread) sm.cs = sm.nx;  // read by all after the next barrier
     if (sm.new_q) {  // fragments are not read again before the next barrier
       if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0)
         set_status(status, KV4_STATUS_TIMEOUT);
@@ -1073,19 +1078,17 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
         sm.pend.valid = 0;
       }
     }
-    if (sm.go) {
-      const Pend& cm = sm.comb;
+    if (sm.go[nb & 1]) {
+      const Pend& cm = sm.comb[nb & 1];
       stream_combine(part_o, part_lse, (long long)cm.pair + cm.c0, cm.n0, cm.row0, out, out_lse);
     }
+    ++nb;
   }
   // the last partial's ticket
+  if (threadIdx.x == kTicketThread) pend_take(sm, pend_t, nb);
   __syncthreads();
-  if (threadIdx.x == kTicketThread) {
-    sm.go = pend_take(sm, pend_t);
-  }
-  __syncthreads();
-  if (sm.go) {
-    const Pend& cm = sm.comb;
+  if (sm.go[nb & 1]) {
+    const Pend& cm = sm.comb[nb & 1];
     stream_combine(part_o, part_lse, (long long)cm.pair + cm.c0, cm.n0, cm.row0, out, out_lse);
   }
   zero_empty();
