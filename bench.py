@@ -193,24 +193,19 @@ def run_kv4(args):
         run_step(cache, s, args.max_splits)
     torch.cuda.synchronize()
     cache.clear_status()
-    # The timed steps replay CUDA graphs captured from the same C-ABI calls
-    # (one for the append, one for the decode), so that host-side argument
-    # marshalling does not starve the GPU; --no-graph times eager calls.
-    g_app = g_dec = None
+    # The timed steps replay one CUDA graph captured from the step's C-ABI
+    # calls (append, then decode), so that host-side argument marshalling does
+    # not starve the GPU and the decode's start-up can overlap the append
+    # (programmatic dependent launch); --no-graph times eager calls.
+    g_step = None
     if not args.no_graph:
-        g_app, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_app):
-            cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
-        with torch.cuda.graph(g_dec):
-            cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            run_step(cache, s, args.max_splits)
         for _ in range(args.warmup):
-            g_app.replay()
-            g_dec.replay()
+            g_step.replay()
         torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -226,27 +221,31 @@ def run_kv4(args):
     torch.cuda._sleep(int(2.1e6 * max(5.0, 0.2 * args.steps)))
     t0.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
-        if g_app is not None:
-            g_app.replay()
-            mids[i].record(stream)
-            g_dec.replay()
+        if g_step is not None:
+            g_step.replay()
         else:
-            run_step(cache, s, args.max_splits, ev=mids[i])
-        ends[i].record(stream)
+            run_step(cache, s, args.max_splits)
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
-    dec_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    app_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
     status = cache.read_status()
+
+    # The decode call and the append call alone (the roofline's kernel time):
+    # K CUDA-event samples each, every one behind an untimed GPU sleep.
+    dec_fn = lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)  # noqa: E731
+    app_fn = lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])  # noqa: E731
+    if not args.no_graph:
+        g_dec, g_app = _graph(dec_fn), _graph(app_fn)
+        dec_fn, app_fn = g_dec.replay, g_app.replay
+    dec_t = _timed(dec_fn, warm=args.warmup, samples=max(args.steps, 20))
+    app_t = _timed(app_fn, warm=args.warmup, samples=max(args.steps, 20))
 
     ms_per_step = reduce_max_ms(total_ms, world, dev) / args.steps
     value = replica_value(world, tokens, ms_per_step)
-    dec_avg = statistics.mean(dec_ms)
+    dec_avg = dec_t["mean_ms"]
     hbm_peak, peak_kind = peaks()
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
     ksrc = kernel_source_hash()
@@ -278,6 +277,13 @@ def run_kv4(args):
     # end to end through the public API with host buffers
     e2e = run_e2e(cache, s, args, stream)
 
+    # the second configuration the target is stated on: one 128k-token
+    # sequence (8 long pairs, each spread over many CTAs), its decode call
+    # timed and held against the same roofline
+    long_rec = None
+    if not args.no_long and w.name != "long_128k":
+        long_rec = decode_record(W.WORKLOADS["long_128k"], dev, args, hbm_peak, ksrc)
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -290,23 +296,27 @@ def run_kv4(args):
                    "parallelism": f"replicas x{world}", "decode_kernel": args.kernel,
                    "launch": "eager" if args.no_graph else "CUDA graph replay of the C-ABI calls",
                    "l2": "cache working set > L2 (no flush needed)"},
-        "decode_ms": dec_avg, "append_ms": statistics.mean(app_ms),
+        "decode_ms": dec_avg, "append_ms": app_t["mean_ms"],
+        "append_exposed_ms": ms_per_step - dec_avg,
         "decode_tokens_per_s": tokens / (dec_avg / 1e3),
         "decode_algorithmic_GBps": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": decode_kernel_name(args, w),
-                     "timed": "kv4_decode_attn call on the launching stream: ticket memset + decode kernel",
+                     "timed": "kv4_decode_attn call on the launching stream (CUDA-event mean): "
+                              "ticket-zeroing kernel + decode kernel",
                      "bytes_per_launch": dec_bytes, "peak_source": peak_kind,
                      "kernel_source_hash": ksrc},
         "append_algorithmic_bytes": app_bytes,
-        # per step: quant_append_kernel and the decode kernel (plus one CUDA
-        # runtime memset of the completion counters, not ours)
-        "gpu_launches": 2 * args.steps,
+        # per step: quant_append_kernel, then the decode call's two kernels
+        # (stream_tickets_zero_kernel + decode_stream_kernel, or
+        # decode_stream_kernel + stream_merge_kernel for few long pairs)
+        "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "device_status": status,
         "e2e": e2e,
         "bf16_comparator": comparator,
+        "long_128k": long_rec,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, lens, budget_s=args.cpu_budget)
@@ -314,6 +324,35 @@ def run_kv4(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def decode_record(w: W.Workload, dev, args, hbm_peak, ksrc):
+    """Decode call alone on workload w (cache built and appended here): the
+    CUDA-event mean over max(steps, 20) graph replays, its algorithmic bytes
+    and roofline fraction, and the kernel's DRAM traffic when a capture of
+    these sources exists."""
+    import torch
+    cache, s, lens, w = build_workload(w, dev, with_bf16=False)
+    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+    dec_bytes, _, _, _ = algorithmic_bytes(lens, w)
+    fn = lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)  # noqa: E731
+    if not args.no_graph:
+        fn = _graph(fn).replay
+    cache.clear_status()
+    t = _timed(fn, warm=args.warmup, samples=max(args.steps, 20))
+    ms = t["mean_ms"]
+    achieved = dec_bytes / (ms / 1e3) / 1e9
+    traffic = TRAFFIC.get((ksrc, w.name)) if args.kernel in ("auto", "stream") and args.max_splits == 0 else None
+    rec = {"workload": w.name, "batch": int(len(lens)), "total_tokens": int(lens.sum()),
+           "decode_ms": ms, "decode_ms_median": t["median_ms"],
+           "decode_tokens_per_s": int(lens.sum()) / (ms / 1e3),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": achieved / hbm_peak, "traffic": traffic,
+                        "kernel": decode_kernel_name(args, w), "bytes_per_launch": dec_bytes},
+           "device_status": cache.read_status()}
+    del cache, s
+    torch.cuda.empty_cache()
+    return rec
 
 
 def decode_kernel_name(args, w):
@@ -703,6 +742,8 @@ def main():
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--kernel", default="auto", choices=["auto", "stream", "mma", "cuda"],
                     help="decode kernel (auto = the fastest measured for the layout)")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long_128k decode record beside the step")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-KV comparator")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos, int T,
     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
     int32_t* status, float hc) {
+  // A decode launched next as a programmatic dependent may start its set-up
+  // now: it waits for this grid before it reads any page.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= (long long)T * L.h_kv) return;

@@ -557,6 +557,12 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     }
   };
   if (lane == 0) {
+    // The grid may be launched while the kernel before it still runs
+    // (programmatic dependent launch: the append kernel lets its dependents
+    // start at once).  Everything above read only the lengths, the block
+    // table and the query; the cache pages and the completion tickets are
+    // touched only after this wait, by the lanes that wait here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     sm.prod[warp] = sm.cs;
     p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
     prod_next();
@@ -610,7 +616,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
 
   int it = 0;  // stage of this warp's next unit (0 .. kSStages - 1)
   int pend_t = 0;  // ticket thread: ticket value returned for the pending partial
-  bool dep_waited = false;  // ticket thread: the ticket-zeroing grid has completed
   int nb = 0;               // segment boundaries passed
   uint32_t qphase = 0;  // completed copies into sm.qraw
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
@@ -1066,12 +1071,6 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       // result is read at the next boundary.  A pair written directly, or
       // merged by the separate kernel (defer), takes none.
       if (!defer && !direct) {
-        // the tickets are zeroed by the kernel launched before this one, which
-        // lets this grid start early (programmatic dependent launch)
-        if (!dep_waited) {
-          asm volatile("griddepcontrol.wait;" ::: "memory");
-          dep_waited = true;
-        }
         pend_t = atom_add_release_gpu(&tickets[sm.pcur.pair], sm.pcur.mine);
         sm.pend = sm.pcur;
       } else {
@@ -1094,13 +1093,15 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   zero_empty();
 }
 
-// Zeroes the completion tickets of the fused merge, then lets the decode
-// kernel launched after it start (its CTAs wait for this grid only before
-// their first ticket).
+// Zeroes the completion tickets of the fused merge.  Launched as a
+// programmatic dependent of the kernel before it, it lets the decode kernel
+// start at once, and completes only once that earlier kernel has completed
+// (its wait), so that the decode's own wait covers both.
 __global__ void __launch_bounds__(256) stream_tickets_zero_kernel(int32_t* __restrict__ tickets,
                                                                  int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) tickets[i] = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Eq. A1 for pairs whose partials are spread over many CTAs (few, long
@@ -1292,14 +1293,23 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   // separate, wider kernel instead of in the last CTA.
   const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
   // The in-kernel merge counts finished units per pair on tickets that start
-  // at 0.  They are zeroed by a small kernel that lets the decode grid start
-  // at once (programmatic dependent launch): its start-up overlaps the
-  // zeroing, and only the ticket thread waits for it, before its first ticket.
+  // at 0, zeroed by a small kernel.  Both kernels are programmatic dependents
+  // of the kernel before them: the decode grid's start-up (the cut of the
+  // stream, its first query) overlaps the zeroing and, after kv4_quant_append,
+  // the append kernel; its waits before the first page copy cover both.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   const int n_tickets = num_seqs * L.h_kv;
   if (!defer && n_tickets > 0) {
-    stream_tickets_zero_kernel<<<std::min(64, (n_tickets + 255) / 256), 256, 0, st>>>(tickets,
-                                                                                    n_tickets);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t zc = {};
+    zc.gridDim = dim3((unsigned)std::min(64, (n_tickets + 255) / 256));
+    zc.blockDim = dim3(256);
+    zc.stream = st;
+    zc.attrs = attr;
+    zc.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&zc, stream_tickets_zero_kernel, tickets, n_tickets)) != cudaSuccess)
+      return e;
   }
   {
     cudaLaunchConfig_t cfg = {};
@@ -1307,11 +1317,8 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
     cfg.blockDim = dim3(kST);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = defer ? 0 : 1;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<NG>, L, (const uint8_t*)paged,
                            (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
                            sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
