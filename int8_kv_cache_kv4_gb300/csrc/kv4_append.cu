@@ -187,59 +187,66 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
   if (w >= (long long)T * L.h_kv) return;
   const int t = (int)(w / L.h_kv);
   const int h = (int)(w % L.h_kv);
+  const int d_h = L.d_h, g = L.g, ng = d_h / g;
+  const int lanes = d_h / 4;  // active lanes (32 at d_h = 128, 16 at 64)
+  const int span = g / 4;     // lanes per INT4 group
+  const bool active = lane < lanes;
+  const int c0 = (active ? lane : 0) * 4;
+  // The new K and V rows are read and encoded first: they do not depend on
+  // the page lookup (token -> length -> block table), so the two latencies
+  // overlap.  Both encodings are formed; the INT8 one is stored only for a
+  // protected position (non-finite input is flagged by either).
+  int bad = 0;
+  uint32_t codes[2], meta[2], c8[2];
+  uint16_t s16[2];
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {  // 4 bf16, 8-byte aligned
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>((kv == 0 ? k_new : v_new) +
+                                                         ((long long)t * L.h_kv + h) * d_h + c0));
+    float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+    if (!active) x[0] = x[1] = x[2] = x[3] = 0.f;
+    if (kRotateK && kv == 0) hadamard_warp(x, d_h, hc);  // before both encoders
+    codes[kv] = encode_int4(x, span, &meta[kv], &bad);
+    c8[kv] = encode_int8(x, lanes < 32 ? lanes : 32, &s16[kv], &bad);
+  }
   const int s = tok_seq[t], p = tok_pos[t];
   int len = 0;
   const int page = token_page(L, s, p, seq_lens, block_table, status, lane == 0 && h == 0, &len);
   if (page < 0) return;
 
-  const int d_h = L.d_h, g = L.g, ng = d_h / g;
-  const int lanes = d_h / 4;  // active lanes (32 at d_h = 128, 16 at 64)
-  const int span = g / 4;     // lanes per INT4 group
   const int slot = p % kPage;
-  const bool active = lane < lanes;
-  const int c0 = (active ? lane : 0) * 4;
   const bool prot = (p < L.S) || (L.R > 0 && p >= len - L.R);
-
   uint8_t* chunk = paged + ((long long)page * L.h_kv + h) * chunk_bytes(d_h, g);
-  int bad = 0;
 #pragma unroll
   for (int kv = 0; kv < 2; ++kv) {
-    const uint16_t* src = (kv == 0 ? k_new : v_new) + ((long long)t * L.h_kv + h) * d_h + c0;
-    uint2 raw = *reinterpret_cast<const uint2*>(src);  // 4 bf16, 8-byte aligned
-    float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
-                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
-    if (!active) x[0] = x[1] = x[2] = x[3] = 0.f;
-    if (kRotateK && kv == 0) hadamard_warp(x, d_h, hc);  // before both encoders
-    uint32_t meta;
-    uint32_t codes = encode_int4(x, span, &meta, &bad);
     if (active) {
       uint8_t* row = chunk + (kv == 0 ? 0 : codes_off_v(d_h)) + slot * (d_h / 2);
       // 4 codes of channels c0..c0+3 -> two bytes (low nibble = even channel)
       const int b = kv == 0 ? k_row_byte(c0, d_h) : row_byte(2 * lane, slot, d_h);
-      *reinterpret_cast<uint16_t*>(row + b) = (uint16_t)codes;
+      *reinterpret_cast<uint16_t*>(row + b) = (uint16_t)codes[kv];
       if ((lane % span) == 0) {
         const int grp = lane / span;
         if (kv == 0) {
-          *reinterpret_cast<uint32_t*>(chunk + meta_off_k(d_h) + slot * ng * 4 + 4 * grp) = meta;
+          *reinterpret_cast<uint32_t*>(chunk + meta_off_k(d_h) + slot * ng * 4 + 4 * grp) = meta[kv];
         } else {
-          *reinterpret_cast<uint16_t*>(chunk + v_delta_byte(slot, grp, d_h, g)) = (uint16_t)meta;
+          *reinterpret_cast<uint16_t*>(chunk + v_delta_byte(slot, grp, d_h, g)) = (uint16_t)meta[kv];
           *reinterpret_cast<uint16_t*>(chunk + v_offset_byte(slot, grp, d_h, g)) =
-              (uint16_t)(meta >> 16);
+              (uint16_t)(meta[kv] >> 16);
         }
       }
     }
     if (prot) {
-      uint16_t s16;
-      uint32_t c8 = encode_int8(x, lanes < 32 ? lanes : 32, &s16, &bad);
       const int NS = L.S + L.R;
       const int ss = side_slot(p, L.S, L.R);
       uint8_t* blk = side + ((long long)s * L.h_kv + h) * side_block_bytes(d_h, L.S, L.R);
       if (active)
         *reinterpret_cast<uint32_t*>(blk + (long long)kv * NS * d_h + (long long)ss * d_h +
-                                     side_byte(c0, ss, d_h)) = c8;
+                                     side_byte(c0, ss, d_h)) = c8[kv];
       if (lane == 0)
         *reinterpret_cast<uint16_t*>(blk + 2LL * NS * d_h +
-                                     (long long)kv * side_scale_entries(L.S, L.R) * 2 + ss * 2) = s16;
+                                     (long long)kv * side_scale_entries(L.S, L.R) * 2 + ss * 2) =
+            s16[kv];
     }
   }
   if (bad && lane == 0) set_status(status, KV4_STATUS_NONFINITE);
