@@ -203,8 +203,9 @@ int kv4_quant_append(const kv4_layout* layout, void* paged, void* side, const ui
  *
  * kv4_hadamard_bf16 -- the query side: each of `rows` rows of `dim` bf16
  *   values x becomes H x rounded to bf16 (nearest even).  Use it on q before
- *   kv4_decode_attn over a cache written by kv4_quant_append_hadamard; the
- *   scores are then sm_scale * (Hq).(k^ of Hk).
+ *   kv4_decode_attn over a cache written by kv4_quant_append_hadamard (or call
+ *   kv4_decode_attn_hadamard, which rotates the query itself); the scores are
+ *   then sm_scale * (Hq).(k^ of Hk).
  *     x, y   device bf16 [rows][dim], 8-byte aligned; y == x (in place) is
  *            allowed, any other overlap is KV4_ERR_INVALID_ARG
  *     dim    64 or 128 (the supported head dimensions), else KV4_ERR_INVALID_ARG
@@ -287,6 +288,25 @@ int kv4_decode_attn(const kv4_layout* layout, const void* paged, const void* sid
                     const int32_t* block_table, float sm_scale, int32_t max_splits,
                     void* workspace, size_t workspace_bytes, uint16_t* out, float* out_lse,
                     int32_t* dev_status, void* stream);
+
+/*
+ * kv4_decode_attn_hadamard -- kv4_decode_attn over a cache written by
+ * kv4_quant_append_hadamard, with the query rotation done by the call: each
+ * query row q is replaced by H q rounded to bf16, exactly as kv4_hadamard_bf16
+ * computes it, and the result equals kv4_hadamard_bf16 followed by
+ * kv4_decode_attn on the rotated rows, bit for bit (KV4-RL App. A.3
+ * "Encoding and allocation": Q rotated with K).  Same arguments, validation
+ * and status bits as kv4_decode_attn; q is not modified.  The default kernel
+ * rotates each (sequence, kv head) pair's query rows as it loads them.  On the
+ * other kernels (max_splits > 0, or a shape the default kernel does not
+ * serve) the rotation runs first into `out` as scratch: out must then be
+ * 16-byte aligned and must not overlap q, else KV4_ERR_INVALID_ARG.
+ */
+int kv4_decode_attn_hadamard(const kv4_layout* layout, const void* paged, const void* side,
+                             const uint16_t* q, const int32_t* seq_lens, int32_t num_seqs,
+                             const int32_t* block_table, float sm_scale, int32_t max_splits,
+                             void* workspace, size_t workspace_bytes, uint16_t* out,
+                             float* out_lse, int32_t* dev_status, void* stream);
 
 /*
  * kv4_split_combine -- the regional / split merge of KV4-RL App. A.3 eq. A1

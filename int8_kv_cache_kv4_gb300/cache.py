@@ -94,12 +94,21 @@ class MixedKVCache(_LayerCache):
             kv4.kv4_bf16_append(self.layout, self.bf16, k_new, v_new, tok_seq, tok_pos, seq_lens,
                                 self.block_table, self.status, stream)
 
-    def decode(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
+    def decode(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None,
+               separate_rotation=False):
+        """Decode of q against this cache.  With the Hadamard K-rotation the
+        query is rotated by the decode call itself (kv4_decode_attn_hadamard);
+        separate_rotation=True rotates it first with kv4_hadamard_bf16 into a
+        scratch buffer and calls kv4_decode_attn (same result, one more
+        launch)."""
         ws = self.workspace(int(q.shape[0]), max_splits)
-        if self.hadamard_k:
+        rotate = self.hadamard_k
+        if rotate and separate_rotation:
             q = self.rotated_query(q, stream)
+            rotate = False
         kv4.kv4_decode_attn(self.layout, self.paged, self.side, q, seq_lens, self.block_table, ws,
-                            out, out_lse, self.sm_scale, max_splits, self.status, stream)
+                            out, out_lse, self.sm_scale, max_splits, self.status, stream,
+                            rotate_q=rotate)
 
     def decode_bf16(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
         ws = self.workspace(int(q.shape[0]), max_splits)

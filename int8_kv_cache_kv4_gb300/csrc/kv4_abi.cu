@@ -35,7 +35,7 @@ bool stream_supported(const Layout&);
 long long stream_partials(const Layout&, int);
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
-                                 int32_t*, uint16_t*, float*, int32_t*, cudaStream_t);
+                                 int32_t*, uint16_t*, float*, int32_t*, bool, cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -284,10 +284,12 @@ int kv4_hadamard_bf16(const uint16_t* x, uint16_t* y, int32_t rows, int32_t dim,
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 
-int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, const uint16_t* q,
-                    const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
-                    float sm_scale, int32_t max_splits, void* workspace, size_t workspace_bytes,
-                    uint16_t* out, float* out_lse, int32_t* dev_status, void* stream) {
+namespace {
+// kv4_decode_attn and kv4_decode_attn_hadamard (rotate_q).
+int decode_attn(const kv4_layout* l, const void* paged, const void* side, const uint16_t* q,
+                const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
+                float sm_scale, int32_t max_splits, void* workspace, size_t workspace_bytes,
+                uint16_t* out, float* out_lse, int32_t* dev_status, bool rotate_q, void* stream) {
   int rc = kv4_check_layout(l);
   if (rc != KV4_OK) return rc;
   if (num_seqs < 0 || num_seqs > l->max_seqs || max_splits < 0) return KV4_ERR_INVALID_ARG;
@@ -309,6 +311,19 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   if (which == KV4_KERNEL_STREAM && (max_splits > 0 || !stream_supported(L)))
     which = KV4_KERNEL_MMA_SYNC;
   if (!mma_supported(L)) which = KV4_KERNEL_CUDA_CORE;
+  // Rotated queries: the stream kernel rotates each pair's query as it sets
+  // it up; for the other kernels the rotation runs first, into `out` (same
+  // shape as q, written only after every read of the query rows it holds).
+  if (rotate_q && which != KV4_KERNEL_STREAM) {
+    if (!aligned16(out)) return KV4_ERR_INVALID_ARG;
+    const uintptr_t bytes = (uintptr_t)num_seqs * l->num_q_heads * l->head_dim * 2u;
+    if ((uintptr_t)q < (uintptr_t)out + bytes && (uintptr_t)out < (uintptr_t)q + bytes)
+      return KV4_ERR_INVALID_ARG;
+    if (launch_hadamard_bf16(q, out, (long long)num_seqs * l->num_q_heads, l->head_dim, st) !=
+        cudaSuccess)
+      return KV4_ERR_LAUNCH;
+    q = out;
+  }
   // Completion tickets for the fused eq. A1 merge start at zero on every call
   // (the stream kernel's launcher clears them itself when it merges in-kernel).
   if (which != KV4_KERNEL_STREAM && cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess)
@@ -316,7 +331,8 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
   cudaError_t e;
   if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, st);
+                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, rotate_q,
+                             st);
   else if (which == KV4_KERNEL_MMA_SYNC)
     e = launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                           p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
@@ -326,6 +342,25 @@ int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, co
                       p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,
                       w.tickets, out, out_lse, dev_status, st);
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int kv4_decode_attn(const kv4_layout* l, const void* paged, const void* side, const uint16_t* q,
+                    const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
+                    float sm_scale, int32_t max_splits, void* workspace, size_t workspace_bytes,
+                    uint16_t* out, float* out_lse, int32_t* dev_status, void* stream) {
+  return decode_attn(l, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, max_splits,
+                     workspace, workspace_bytes, out, out_lse, dev_status, false, stream);
+}
+
+int kv4_decode_attn_hadamard(const kv4_layout* l, const void* paged, const void* side,
+                             const uint16_t* q, const int32_t* seq_lens, int32_t num_seqs,
+                             const int32_t* block_table, float sm_scale, int32_t max_splits,
+                             void* workspace, size_t workspace_bytes, uint16_t* out,
+                             float* out_lse, int32_t* dev_status, void* stream) {
+  return decode_attn(l, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, max_splits,
+                     workspace, workspace_bytes, out, out_lse, dev_status, true, stream);
 }
 
 int kv4_split_combine(const float* part_o, const float* part_lse, int32_t rows, int32_t n_parts,

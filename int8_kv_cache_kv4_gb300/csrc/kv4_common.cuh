@@ -2,6 +2,7 @@
 // packed-layout offsets, status reporting, and thin inline-PTX wrappers for
 // the sm_100-family asynchronous copy engine (mbarrier + cp.async.bulk).
 #pragma once
+#include <cmath>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -126,6 +127,40 @@ __host__ __device__ inline int side_slot(int p, int S, int R) { return p < S ? p
 __device__ inline void set_status(int32_t* st, int bits) {
   if (st && bits) atomicOr(st, bits);
 }
+
+// ------------------------------------------------- Hadamard rotation (eq. 3.4)
+// In-place normalized Hadamard rotation of a head_dim-vector spread over the
+// warp: lane l holds channels 4l..4l+3 in x[0..3]; lanes at or past d/4 hold
+// zeros and only ever pair among themselves.  The butterfly runs stages
+// h = 1, 2, 4, ..., d/2 in that order; at each, the pair of channels (i, i+h)
+// with bit h of i clear becomes (a + b, a - b) for a = x_i, b = x_(i+h).
+// Stages 1 and 2 stay inside a lane; stage h = 4m pairs lane l with lane
+// l ^ m.  A final multiply by c (the fp32 value nearest 1/sqrt(d)) normalizes.
+// Every step is an explicitly rounded fp32 operation in this fixed order, so
+// the result is reproducible bit for bit by any implementation of the same
+// order.  All 32 lanes must call it (full-mask shuffles).
+__device__ inline void hadamard_warp(float x[4], int d, float c) {
+  const float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
+  const float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
+  x[0] = __fadd_rn(a0, a2);
+  x[2] = __fsub_rn(a0, a2);
+  x[1] = __fadd_rn(a1, a3);
+  x[3] = __fsub_rn(a1, a3);
+  const int lane = threadIdx.x & 31;
+  for (int m = 1; 4 * m < d; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], c);
+}
+
+// fp32 value nearest 1/sqrt(d), computed on the host in double precision.
+inline float hadamard_scale(int d) { return (float)(1.0 / std::sqrt((double)d)); }
 
 // ------------------------------------------------------------ conversions
 __device__ inline float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }

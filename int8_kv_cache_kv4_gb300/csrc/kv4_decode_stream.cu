@@ -204,9 +204,25 @@ __device__ inline void stream_query_fetch(StreamSmem& sm, const uint16_t* __rest
 
 // Everything the units need from the query of the next pair, built from
 // sm.qraw once its copy has completed.  No warp may still read the old values.
+// q_rot != 0: the query is first rotated by the normalized Hadamard matrix of
+// the keys (KV4-RL eq. 3.4; q_rot is the fp32 value nearest 1/sqrt(128)) and
+// rounded to bf16, the same steps in the same order as kv4_hadamard_bf16, so
+// that the result equals a decode of the separately rotated query.  Called
+// by every thread of the CTA.
 template <int NG>
-__device__ __noinline__ void stream_query_setup(StreamSmem& sm, float scale_log2) {
-  if (threadIdx.x < 128) build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x, scale_log2);
+__device__ __noinline__ void stream_query_setup(StreamSmem& sm, float scale_log2, float q_rot) {
+  static_assert(kST == 32 * SG, "one warp per query head");
+  if (q_rot != 0.f) {
+    uint2* row = reinterpret_cast<uint2*>(sm.qraw + (threadIdx.x >> 5) * SD) + (threadIdx.x & 31);
+    const uint2 raw = *row;
+    float v[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+    hadamard_warp(v, SD, q_rot);
+    *row = make_uint2((uint32_t)f32_to_bf16_bits(v[0]) | ((uint32_t)f32_to_bf16_bits(v[1]) << 16),
+                      (uint32_t)f32_to_bf16_bits(v[2]) | ((uint32_t)f32_to_bf16_bits(v[3]) << 16));
+    __syncthreads();
+  }
+  build_qprep<NG>(sm.qraw, sm.qp, threadIdx.x, scale_log2);
 }
 
 // Merge the warps' states of one segment (after a barrier that follows every
@@ -338,7 +354,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
-    float* __restrict__ out_lse, int32_t* status, int defer) {
+    float* __restrict__ out_lse, int32_t* status, int defer, float q_rot) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   uint32_t qphase = 0;  // completed copies into sm.qraw
   if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0) set_status(status, KV4_STATUS_TIMEOUT);
   ++qphase;
-  stream_query_setup<NG>(sm, scale_log2);
+  stream_query_setup<NG>(sm, scale_log2, q_rot);
   __syncthreads();
   // The current segment lives in sm.cs (advanced by the ticket thread between
   // the boundary barriers); the loop below keeps only what the units need.
@@ -1062,7 +1078,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
       if (!mbar_wait(&sm.qbar, qphase & 1) && threadIdx.x == 0)
         set_status(status, KV4_STATUS_TIMEOUT);
       ++qphase;
-      stream_query_setup<NG>(sm, scale_log2);
+      stream_query_setup<NG>(sm, scale_log2, q_rot);
     }
     __syncthreads();  // B2: partial stored; next pair's query set up; comb, cs written
     if (threadIdx.x == kTicketThread) {
@@ -1265,7 +1281,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                             const int32_t* block_table, float sm_scale, float* part_o,
                             float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                            int32_t* status, cudaStream_t st) {
+                            int32_t* status, float q_rot, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
       ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kSW * kSStages * kSPages * cb;
@@ -1321,7 +1337,8 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<NG>, L, (const uint8_t*)paged,
                            (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
-                           sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer);
+                           sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer,
+                           q_rot);
     if (e != cudaSuccess) return e;
   }
   if (defer)
@@ -1333,17 +1350,19 @@ cudaError_t launch_decode_stream(const Layout& L, const void* paged, const void*
                                  const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                                  const int32_t* block_table, float sm_scale, float* part_o,
                                  float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                                 int32_t* status, cudaStream_t st) {
+                                 int32_t* status, bool rotate_q, cudaStream_t st) {
+  // the query rotated in the kernel's query set-up (Hadamard K-rotation)
+  const float q_rot = rotate_q ? hadamard_scale(SD) : 0.f;
   switch (L.d_h / L.g) {
     case 4:
       return launch_stream_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
     case 2:
       return launch_stream_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
     case 1:
       return launch_stream_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, st);
+                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
   }
   return cudaErrorInvalidValue;
 }

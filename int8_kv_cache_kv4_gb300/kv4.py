@@ -104,6 +104,8 @@ def load(build_if_missing: bool = False):
         "kv4_fp4_to_bf16": (ctypes.c_int, [LP, I, P, P, P]),
         "kv4_decode_attn": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, Sz, P, P,
                                            P, P]),
+        "kv4_decode_attn_hadamard": (ctypes.c_int, [LP, P, P, P, P, I, P, ctypes.c_float, I, P, Sz, P, P,
+                                           P, P]),
         "kv4_split_combine": (ctypes.c_int, [P, P, I, I, I, P, P, P]),
         "kv4_bf16_append": (ctypes.c_int, [LP, P, P, P, P, P, I, P, P, P, P]),
         "kv4_bf16_decode_attn": (ctypes.c_int, [LP, P, P, P, I, P, ctypes.c_float, I, P, Sz, P,
@@ -299,19 +301,22 @@ def _check_decode_args(name, layout, paged, side, q, seq_lens, block_table, out,
 
 
 def kv4_decode_attn(layout, paged, side, q, seq_lens, block_table, workspace, out, out_lse=None,
-                    sm_scale=None, max_splits=0, status=None, stream=None):
-    """Split-KV GQA decode attention; q/out bf16 [B][h_q][d_h]."""
+                    sm_scale=None, max_splits=0, status=None, stream=None, rotate_q=False):
+    """Split-KV GQA decode attention; q/out bf16 [B][h_q][d_h].  rotate_q:
+    kv4_decode_attn_hadamard (the query rotated by the call, for a cache
+    written with the Hadamard K-rotation)."""
     import torch
-    B = _check_decode_args("kv4_decode_attn", layout, paged, side, q, seq_lens, block_table, out,
-                           out_lse, status)
+    name = "kv4_decode_attn_hadamard" if rotate_q else "kv4_decode_attn"
+    B = _check_decode_args(name, layout, paged, side, q, seq_lens, block_table, out, out_lse,
+                           status)
     _dev(workspace, torch.uint8, "workspace")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(layout.head_dim)
-    rc = load().kv4_decode_attn(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(q),
-                                _ptr(seq_lens), B, _ptr(block_table), float(sm_scale),
-                                int(max_splits), _ptr(workspace), workspace.numel(), _ptr(out),
-                                _ptr(out_lse), _ptr(status), _stream(stream))
-    _check(rc, "kv4_decode_attn")
+    rc = getattr(load(), name)(ctypes.byref(layout), _ptr(paged), _ptr(side), _ptr(q),
+                               _ptr(seq_lens), B, _ptr(block_table), float(sm_scale),
+                               int(max_splits), _ptr(workspace), workspace.numel(), _ptr(out),
+                               _ptr(out_lse), _ptr(status), _stream(stream))
+    _check(rc, name)
 
 
 def kv4_split_combine(part_o, part_lse, out, out_lse=None, stream=None):

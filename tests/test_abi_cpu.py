@@ -107,6 +107,23 @@ def test_hadamard_entry_points_validate_on_host(lib):
     assert rc == kv4.KV4_ERR_INVALID_ARG
     assert lib.kv4_quant_append_hadamard(ctypes.byref(lay), None, None, None, None, None, None,
                                          0, None, None, None, None) == kv4.KV4_OK
+    rc = lib.kv4_decode_attn_hadamard(ctypes.byref(lay), None, None, None, None, 2, None, 0.1, 0,
+                                      None, 0, None, None, None, None)
+    assert rc == kv4.KV4_ERR_INVALID_ARG
+    # off the default kernel the rotated query goes through `out` first, so an
+    # `out` overlapping q is rejected before anything is launched
+    lay2 = kv4.make_layout(max_seqs=2, num_pages=4, max_pages_per_seq=2)
+    nws = kv4.workspace_bytes(lay2, 2)
+    mem = ctypes.create_string_buffer(nws + 65536 + 16)
+    b = (ctypes.addressof(mem) + 15) // 16 * 16
+    ws = b + 65536
+    prev = kv4.kv4_set_decode_kernel(kv4.KV4_KERNEL_MMA_SYNC)
+    try:
+        rc = lib.kv4_decode_attn_hadamard(ctypes.byref(lay2), b, b, b, b, 2, b, 0.1, 0, ws, nws,
+                                          b + 64, None, None, None)
+        assert rc == kv4.KV4_ERR_INVALID_ARG
+    finally:
+        kv4.kv4_set_decode_kernel(prev)
 
 
 def test_fp4_entry_points_validate_on_host(lib):

@@ -119,3 +119,33 @@ def test_rotation_changes_only_k():
     b = p1.reshape(-1, chunk)
     assert np.array_equal(a[:, half:2 * half], b[:, half:2 * half])      # V codes
     assert not np.array_equal(a[:, :half], b[:, :half])                  # K codes
+
+
+@pytest.mark.parametrize("which,splits", [(kv4.KV4_KERNEL_STREAM, 0), (kv4.KV4_KERNEL_MMA_SYNC, 0),
+                                          (kv4.KV4_KERNEL_CUDA_CORE, 0), (kv4.KV4_KERNEL_AUTO, 3)],
+                         ids=["stream", "mma", "cuda", "auto-splits3"])
+def test_query_rotation_in_the_decode_call_equals_separate_rotation(which, splits):
+    # kv4_decode_attn_hadamard (rotation inside the call: in the stream
+    # kernel's query set-up, else into `out` first) against kv4_hadamard_bf16
+    # followed by kv4_decode_attn: bit for bit, outputs and log-normalisers
+    lens = [0, 1, 5, 64, 85, 333, 2100]
+    c = Case(lens, S=4, R=80, g=32, seed=19, h_q=32, h_kv=8, rotate_k=True)
+    prev = kv4.kv4_set_decode_kernel(which)
+    try:
+        gc = c.gpu()
+        q = torch.from_numpy(c.q.view(np.int16)).cuda().view(torch.bfloat16)
+        q0 = q.clone()
+        lens_d = torch.from_numpy(c.lens).cuda()
+        outs = []
+        for sep in (False, True):
+            out = torch.empty((c.B, c.h_q, c.d_h), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((c.B, c.h_q), dtype=torch.float32, device="cuda")
+            gc.decode(q, lens_d, out, lse, max_splits=splits, separate_rotation=sep)
+            torch.cuda.synchronize()
+            outs.append((_bits(out), lse.cpu().numpy()))
+        assert gc.read_status() == 0
+        assert np.array_equal(_bits(q), _bits(q0))          # q untouched
+        assert np.array_equal(outs[0][0], outs[1][0])
+        assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    finally:
+        kv4.kv4_set_decode_kernel(prev)
