@@ -74,6 +74,22 @@
  *     c = clamp(rne(x /rn s), -127, 127), and c = 0 when s = 0.
  *   A group or vector with a non-finite element (or whose metadata overflows
  *   fp16) is stored as all zeros and sets KV4_STATUS_NONFINITE.
+ *
+ * Operand range of the tensor-core decode kernels (the default one and the
+ * split kernel): their PV products take P' = p * Delta_v (INT4) or p * s_v
+ * (INT8) as fp16, with softmax weights p <= 2^8 relative to a lazily moved
+ * reference.  They are accurate while every stored Delta_v and s_v is zero or
+ * a normal fp16 value of at most 255.875: V group ranges (max - min) from
+ * 15 * 2^-14 = 9.2e-4 up to 3838, and max |V| of a protected token-head from
+ * 127 * 2^-14 = 7.8e-3 up to 32496 (or exactly zero).  The append encodes
+ * other V exactly as the rules above say and sets KV4_STATUS_V_RANGE; a cache
+ * holding such V decodes correctly only with the CUDA-core kernel
+ * (kv4_set_decode_kernel(KV4_KERNEL_CUDA_CORE)), which computes in fp32.
+ * (Measured: V scaled by 2^-6 .. 2^8 stays within the output tolerance on
+ * every kernel; at 2^-10 the protected scales are subnormal and the default
+ * kernel misses it.)  The INT8 units also take the query as fp16: |q| below
+ * 65504, exact for |q| >= 2^-14 (bf16 values below that lose low bits; q
+ * scaled by 2^-12 stays within the tolerance).
  */
 #ifndef KV4_H_
 #define KV4_H_
@@ -102,6 +118,7 @@ extern "C" {
 #define KV4_STATUS_BAD_LEN 16  /* decode: seq_len < 0 or beyond the block-table capacity */
 #define KV4_STATUS_TIMEOUT 32  /* a bounded wait inside a kernel expired; its outputs are invalid */
 #define KV4_STATUS_INTERNAL 64 /* a kernel's internal consistency check failed; outputs invalid */
+#define KV4_STATUS_V_RANGE 128 /* append: a V Delta or protected V scale >= 256 or subnormal */
 
 /* Shape of one attention layer's cache.  All fields are host values. */
 typedef struct kv4_layout {

@@ -147,7 +147,9 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
     int32_t* status, float hc) {
   // A decode launched next as a programmatic dependent may start its set-up
-  // now: it waits for this grid before it reads any page.
+  // now: it waits for this grid before it reads any page.  (Before its own
+  // wait below this kernel only reads its inputs, which no kernel of this
+  // library writes.)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -181,6 +183,11 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
   int len = 0;
   const int page = token_page(L, s, p, seq_lens, block_table, status, lane == 0 && h == 0, &len);
   if (page < 0) return;
+  // Launched as a programmatic dependent of the kernel before it (often the
+  // previous step's decode, which reads the side-cache ring slot this token
+  // may overwrite): nothing of the cache is written before that kernel has
+  // completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int slot = p % kPage;
   const bool prot = (p < L.S) || (L.R > 0 && p >= len - L.R);
@@ -217,6 +224,13 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     }
   }
   if (bad && lane == 0) set_status(status, KV4_STATUS_NONFINITE);
+  // V metadata outside the range of the tensor-core decode's fp16 PV operand
+  // (P' = p Delta, p <= 2^8): Delta >= 256 (fp16 bits 0x5C00 and up; Delta is
+  // never negative) or a nonzero subnormal Delta (bits below 0x0400), and the
+  // same for a stored INT8 scale
+  auto out_of_range = [](uint32_t h) { return h >= 0x5C00u || (h != 0u && h < 0x0400u); };
+  const bool v_out = (active && out_of_range(meta[1] & 0xFFFFu)) || (prot && out_of_range(s16[1]));
+  if (__any_sync(0xffffffffu, v_out) && lane == 0) set_status(status, KV4_STATUS_V_RANGE);
 }
 
 // Comparator cache: [page][h_kv][K|V][16][d_h] bf16, plain copy.
@@ -254,15 +268,24 @@ cudaError_t launch_quant_append(const Layout& L, void* paged, void* side, const 
   const long long warps = (long long)T * L.h_kv;
   const int wpb = 8;
   const long long blocks = (warps + wpb - 1) / wpb;
+  // A programmatic dependent of the kernel before it: the grid may start (and
+  // read and encode its tokens) while that kernel still runs, and waits for it
+  // before writing the cache.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(wpb * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (rotate_k)
-    quant_append_kernel<true><<<(unsigned)blocks, wpb * 32, 0, st>>>(
-        L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
-        block_table, status, hadamard_scale(L.d_h));
-  else
-    quant_append_kernel<false><<<(unsigned)blocks, wpb * 32, 0, st>>>(
-        L, (uint8_t*)paged, (uint8_t*)side, k_new, v_new, tok_seq, tok_pos, T, seq_lens,
-        block_table, status, 1.0f);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, quant_append_kernel<true>, L, (uint8_t*)paged, (uint8_t*)side,
+                              k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table, status,
+                              hadamard_scale(L.d_h));
+  return cudaLaunchKernelEx(&cfg, quant_append_kernel<false>, L, (uint8_t*)paged, (uint8_t*)side,
+                            k_new, v_new, tok_seq, tok_pos, T, seq_lens, block_table, status, 1.0f);
 }
 
 // Query side of the K rotation: each row of d bf16 values becomes H x rounded

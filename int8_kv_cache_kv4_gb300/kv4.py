@@ -30,6 +30,7 @@ KV4_STATUS_NONFINITE = 8
 KV4_STATUS_BAD_LEN = 16
 KV4_STATUS_TIMEOUT = 32
 KV4_STATUS_INTERNAL = 64
+KV4_STATUS_V_RANGE = 128
 
 KV4_KERNEL_AUTO = 0
 KV4_KERNEL_CUDA_CORE = 1

@@ -15,12 +15,23 @@ MEAN_ABS = 2e-4
 LSE_ABS = 1e-3   # fp32 scores and normaliser vs fp64
 
 
+def scale_bf16(bits, e):
+    """bf16 values (bit patterns) times 2^e: exact while the results stay in
+    bf16's normal range (checked)."""
+    if e == 0:
+        return bits
+    x = W.bf16_bits_to_f32(bits) * np.float32(2.0 ** e)
+    out = W.f32_to_bf16_bits(x)
+    assert np.array_equal(W.bf16_bits_to_f32(out), x), "scaling left bf16's exact range"
+    return out
+
+
 class Case:
     """A batch of sequences with seeded K/V/q, a seeded page permutation and
     token lists for a populate append followed by a one-token append."""
 
     def __init__(self, lens, *, h_q=32, h_kv=8, d_h=128, g=32, S=4, R=64, seed=1, extra_pages=3,
-                 rotate_k=False):
+                 rotate_k=False, k_exp=0, v_exp=0, q_exp=0):
         self.rotate_k = bool(rotate_k)
         self.lens = np.asarray(lens, dtype=np.int32)
         self.B = len(self.lens)
@@ -34,9 +45,9 @@ class Case:
         self.v = []
         for b, L in enumerate(self.lens):
             kb, vb = W.kv_numpy_block(seed, b, h_kv, int(L), d_h, outl)
-            self.k.append(kb)
-            self.v.append(vb)
-        self.q = W.q_numpy(seed, self.B, h_q, d_h)
+            self.k.append(scale_bf16(kb, k_exp))
+            self.v.append(scale_bf16(vb, v_exp))
+        self.q = scale_bf16(W.q_numpy(seed, self.B, h_q, d_h), q_exp)
         self.sm_scale = 1.0 / math.sqrt(d_h)
 
     def layout_kw(self):
