@@ -267,10 +267,12 @@ def run_kv4(args):
         bf_ms = e0.elapsed_time(e1) / args.steps
         bf_bytes = sum(w.h_kv * int(L) * 2 * w.d_h * 2 for L in lens) + len(lens) * w.h_q * w.d_h * 4
         drift = (s["out"].float() - out16.float()).abs()
-        comparator = {"kernel": "bf16-KV paged decode (same pages, same split plan)",
+        comparator = {"kernel": "bf16-KV paged decode on the tensor cores (same pages and block table)",
                       "ms": bf_ms, "tokens_per_s": tokens / (bf_ms / 1e3),
                       "algorithmic_GBps": bf_bytes / (bf_ms / 1e3) / 1e9,
+                      "frac_of_hbm": bf_bytes / (bf_ms / 1e3) / 1e9 / hbm_peak,
                       "kv4_decode_speedup": bf_ms / dec_avg,
+                      "byte_ratio_bound": bf_bytes / dec_bytes,
                       "output_drift_vs_bf16": {"max_abs": float(drift.max()),
                                                "mean_abs": float(drift.mean())}}
 

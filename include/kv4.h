@@ -341,11 +341,20 @@ int kv4_split_combine(const float* part_o, const float* part_lse, int32_t rows, 
 
 /*
  * Comparator: the same paged GQA decode over an unquantized bf16 cache
- * (layout above), with the same pages, block table and split plan.  Not part
- * of the method; used to report the speed-up of the mixed cache and the
- * drift of its outputs.
+ * (layout above), with the same pages and block table.  Not part of the
+ * method; used to report the speed-up of the mixed cache and the drift of its
+ * outputs.
  *   kv4_bf16_append writes k_new/v_new [T][h_kv][d_h] into the bf16 pages.
+ *   kv4_bf16_decode_attn: with max_splits = 0, head_dim 128, 4 query heads
+ *   per kv head and num_seqs <= 2048, a tensor-core kernel (bf16 operands,
+ *   fp32 accumulation, softmax weights entered as a bf16 head and tail) whose
+ *   warps claim chunks of 16 pages of a (sequence, kv head) pair and merge
+ *   the chunks of a pair in order (the result does not depend on which warp
+ *   took which chunk); otherwise a CUDA-core split kernel with the split plan
+ *   of kv4_decode_attn.  Its workspace is kv4_bf16_workspace_bytes(layout,
+ *   num_seqs, max_splits) bytes (KV4_ERR_WORKSPACE if smaller).
  */
+size_t kv4_bf16_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 int kv4_bf16_append(const kv4_layout* layout, void* cache, const uint16_t* k_new,
                     const uint16_t* v_new, const int32_t* tok_seq, const int32_t* tok_pos,
                     int32_t T, const int32_t* seq_lens, const int32_t* block_table,

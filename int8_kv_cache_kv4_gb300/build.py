@@ -23,7 +23,7 @@ OUT = os.path.join(HERE, "libkv4.so")
 DIAG_OUT = os.path.join(HERE, "libkv4_diag.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["kv4_abi.cu", "kv4_append.cu", "kv4_decode.cu", "kv4_decode_mma.cu",
-           "kv4_decode_stream.cu", "kv4_noalloc.cu"]
+           "kv4_decode_stream.cu", "kv4_decode_bf16.cu", "kv4_noalloc.cu"]
 DIAG_SOURCES = ["diag/kv4_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -43,11 +43,12 @@ class _LayerCache:
         bt = torch.as_tensor(np.asarray(bt, dtype=np.int32))
         self.block_table[: bt.shape[0], : bt.shape[1]].copy_(bt)
 
-    def workspace(self, num_seqs: int, max_splits: int = 0):
+    def workspace(self, num_seqs: int, max_splits: int = 0, bf16: bool = False):
         import torch
-        key = (num_seqs, max_splits)
+        key = (num_seqs, max_splits, bf16)
         if key not in self._ws:
-            n = kv4.workspace_bytes(self.layout, num_seqs, max_splits)
+            n = (kv4.bf16_workspace_bytes if bf16 else kv4.workspace_bytes)(self.layout, num_seqs,
+                                                                             max_splits)
             self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws[key]
 
@@ -111,7 +112,7 @@ class MixedKVCache(_LayerCache):
                             rotate_q=rotate)
 
     def decode_bf16(self, q, seq_lens, out, out_lse=None, max_splits=0, stream=None):
-        ws = self.workspace(int(q.shape[0]), max_splits)
+        ws = self.workspace(int(q.shape[0]), max_splits, bf16=True)
         kv4.kv4_bf16_decode_attn(self.layout, self.bf16, q, seq_lens, self.block_table, ws, out,
                                  out_lse, self.sm_scale, max_splits, self.status, stream)
 
@@ -147,7 +148,7 @@ class FP4ProbeCache(_LayerCache):
         self.reconstruct(stream)
         if self.hadamard_k:
             q = self.rotated_query(q, stream)
-        ws = self.workspace(int(q.shape[0]), max_splits)
+        ws = self.workspace(int(q.shape[0]), max_splits, bf16=True)
         kv4.kv4_bf16_decode_attn(self.layout, self.bf16, q, seq_lens, self.block_table, ws, out,
                                  out_lse, self.sm_scale, max_splits, self.status, stream)
 

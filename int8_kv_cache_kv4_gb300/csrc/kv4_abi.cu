@@ -1,3 +1,4 @@
+#include <algorithm>
 // kv4_abi.cu -- the extern "C" boundary declared in include/kv4.h: argument
 // validation, buffer sizing, the split plan, and kernel launches.  No entry
 // point allocates, frees or synchronises.
@@ -26,6 +27,11 @@ cudaError_t launch_bf16_decode(const Layout&, const void*, const uint16_t*, cons
 cudaError_t launch_combine(const float*, const float*, int, int, int, uint16_t*, float*,
                            cudaStream_t);
 bool mma_supported(const Layout&);
+bool bf16_mma_supported(const Layout&, int);
+long long bf16_mma_items(const Layout&, int);
+cudaError_t launch_bf16_decode_mma(const Layout&, const void*, const uint16_t*, const int32_t*, int,
+                                   const int32_t*, float, float*, float*, int32_t*, int32_t*,
+                                   uint16_t*, float*, int32_t*, cudaStream_t);
 static int g_decode_kernel = KV4_KERNEL_AUTO;
 cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uint16_t*,
                               const int32_t*, int, const int32_t*, float, int, int, int, int,
@@ -389,6 +395,26 @@ int kv4_bf16_append(const kv4_layout* l, void* cache, const uint16_t* k_new, con
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 
+// Workspace of the bf16 comparator: the split kernel's (as kv4_decode_attn
+// with a fixed split count), or for the tensor-core kernel its per-item
+// partials, one ticket per pair and the item counter.
+static size_t bf16_ws_mma(const kv4_layout* l, int num_seqs) {
+  const Layout L = to_layout(l);
+  const size_t items = (size_t)bf16_mma_items(L, num_seqs), G = l->num_q_heads / l->num_kv_heads;
+  return round256(items * G * l->head_dim * sizeof(float)) + round256(items * G * sizeof(float)) +
+         round256(((size_t)num_seqs * l->num_kv_heads + 1) * sizeof(int32_t));
+}
+static size_t bf16_ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p) {
+  size_t n = ws_bytes(l, num_seqs, p, -1);
+  if (bf16_mma_supported(to_layout(l), num_seqs)) n = std::max(n, bf16_ws_mma(l, num_seqs));
+  return n;
+}
+
+size_t kv4_bf16_workspace_bytes(const kv4_layout* l, int32_t num_seqs, int32_t max_splits) {
+  if (kv4_check_layout(l) != KV4_OK || num_seqs < 0 || max_splits < 0) return 0;
+  return bf16_ws_bytes(l, num_seqs, make_plan(l, num_seqs, max_splits, false));
+}
+
 int kv4_bf16_decode_attn(const kv4_layout* l, const void* cache, const uint16_t* q,
                          const int32_t* seq_lens, int32_t num_seqs, const int32_t* block_table,
                          float sm_scale, int32_t max_splits, void* workspace,
@@ -401,14 +427,32 @@ int kv4_bf16_decode_attn(const kv4_layout* l, const void* cache, const uint16_t*
   if (!cache || !q || !seq_lens || !block_table || !workspace || !out) return KV4_ERR_INVALID_ARG;
   if (!aligned16(cache) || !aligned16(q) || !aligned16(workspace)) return KV4_ERR_INVALID_ARG;
   const Plan p = make_plan(l, num_seqs, max_splits, false);
-  // the comparator runs split kernels only: size as for a fixed split count
-  if (workspace_bytes < ws_bytes(l, num_seqs, p, -1)) return KV4_ERR_WORKSPACE;
-  const Workspace w = ws_layout(l, num_seqs, p, -1, workspace);
+  if (workspace_bytes < bf16_ws_bytes(l, num_seqs, p)) return KV4_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
-  cudaError_t e = launch_bf16_decode(to_layout(l), cache, q, seq_lens, num_seqs, block_table,
-                                     sm_scale, p.n4, p.pages_per_split, w.part_o, w.part_lse,
-                                     w.tickets, out, out_lse, dev_status, st);
+  const Layout L = to_layout(l);
+  cudaError_t e;
+  if (max_splits == 0 && bf16_mma_supported(L, num_seqs)) {
+    // tensor-core kernel: partials per work item, then the tickets and the
+    // item counter, which start at zero
+    const size_t items = (size_t)bf16_mma_items(L, num_seqs), G = l->num_q_heads / l->num_kv_heads;
+    const size_t o = round256(items * G * l->head_dim * sizeof(float));
+    const size_t z = round256(items * G * sizeof(float));
+    float* part_o = (float*)workspace;
+    float* part_lse = (float*)((char*)workspace + o);
+    int32_t* tickets = (int32_t*)((char*)workspace + o + z);
+    const size_t n_tk = (size_t)num_seqs * l->num_kv_heads;
+    if (cudaMemsetAsync(tickets, 0, (n_tk + 1) * sizeof(int32_t), st) != cudaSuccess)
+      return KV4_ERR_LAUNCH;
+    e = launch_bf16_decode_mma(L, cache, q, seq_lens, num_seqs, block_table, sm_scale, part_o,
+                               part_lse, tickets, tickets + n_tk, out, out_lse, dev_status, st);
+  } else {
+    // the comparator's split kernel (CUDA cores): sized as for a fixed split count
+    const Workspace w = ws_layout(l, num_seqs, p, -1, workspace);
+    if (cudaMemsetAsync(w.tickets, 0, w.ticket_bytes, st) != cudaSuccess) return KV4_ERR_LAUNCH;
+    e = launch_bf16_decode(L, cache, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
+                           p.pages_per_split, w.part_o, w.part_lse, w.tickets, out, out_lse,
+                           dev_status, st);
+  }
   return e == cudaSuccess ? KV4_OK : KV4_ERR_LAUNCH;
 }
 

@@ -97,6 +97,7 @@ def load(build_if_missing: bool = False):
         "kv4_bf16_cache_bytes": (Sz, [LP]),
         "kv4_num_splits": (I, [LP, I, I]),
         "kv4_workspace_bytes": (Sz, [LP, I, I]),
+        "kv4_bf16_workspace_bytes": (Sz, [LP, I, I]),
         "kv4_quant_append": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_quant_append_hadamard": (ctypes.c_int, [LP, P, P, P, P, P, P, I, P, P, P, P]),
         "kv4_hadamard_bf16": (ctypes.c_int, [P, P, I, I, P]),
@@ -179,6 +180,10 @@ def num_splits(layout: kv4_layout, num_seqs: int, max_splits: int = 0) -> int:
 
 def workspace_bytes(layout: kv4_layout, num_seqs: int, max_splits: int = 0) -> int:
     return int(load().kv4_workspace_bytes(ctypes.byref(layout), num_seqs, max_splits))
+
+
+def bf16_workspace_bytes(layout: kv4_layout, num_seqs: int, max_splits: int = 0) -> int:
+    return int(load().kv4_bf16_workspace_bytes(ctypes.byref(layout), num_seqs, max_splits))
 
 
 def kv4_quant_append(layout, paged, side, k_new, v_new, tok_seq, tok_pos, seq_lens, block_table,

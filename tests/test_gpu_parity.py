@@ -101,6 +101,23 @@ def test_bf16_comparator_matches_unquantized_attention():
     compare_outputs(out, lse, ref, rlse, range(c.B), c.lens)
 
 
+@pytest.mark.parametrize("max_splits", [0, 3])
+def test_bf16_comparator_tensor_core_kernel(max_splits):
+    # head_dim 128, 4 query heads per kv head: with max_splits = 0 the
+    # tensor-core kernel (16-page work items claimed by warps; lengths with
+    # partial pages, several items per pair, an empty and a one-token
+    # sequence), else the split kernel; both against exact attention, and the
+    # tensor-core result repeated bit for bit
+    c = Case([0, 1, 15, 16, 17, 255, 256, 257, 1100, 5000], S=4, R=64, g=32, seed=12)
+    gc = c.gpu(with_bf16=True)
+    out, lse = c.gpu_decode(gc, max_splits=max_splits, bf16=True)
+    ref, rlse = c.oracle_bf16()
+    compare_outputs(out, lse, ref, rlse, range(c.B), c.lens)
+    out2, lse2 = c.gpu_decode(gc, max_splits=max_splits, bf16=True)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    assert gc.read_status() == 0
+
+
 def test_split_combine_against_oracle():
     rng = np.random.default_rng(9)
     rows, n, d = 37, 11, 128
