@@ -38,13 +38,14 @@ UNIT = "tokens/s"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the default decode kernel on the default workload, from the ncu capture
-# summarised in profiles/decode_stream_kernel_qwen3_8b_b64.md.  Keyed by a
+# summarised in profiles/decode_stream_kernel_qwen3_8b_b64.md and
+# profiles/launch_list_long_128k.md.  Keyed by a
 # hash of the sources that kernel is compiled from: once they change, the
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("37b5efaf3b5e8203", "qwen3_8b_b64"): 388365568 + 4518144,
-           ("37b5efaf3b5e8203", "long_128k"): 168151808 + 3310592}
+TRAFFIC = {("c5b559fbd04c5e8a", "qwen3_8b_b64"): 387998720 + 2321152,
+           ("c5b559fbd04c5e8a", "long_128k"): 168157952 + 1327360}
 
 
 # ------------------------------------------------------------------ helpers
@@ -715,22 +716,46 @@ def run_report(args):
                     extra={"query_rotation": tq,
                            "query_rotation_GBps": qb / (tq["median_ms"] / 1e3) / 1e9})
         del cache
-    if "5" in sel:  # one layer of the 36-layer step per sweep point (x36 for the step)
+    if "5" in sel:  # the 36-layer step: every layer appended and decoded, one graph per step
         w = W.WORKLOADS["qwen3_8b_36l"]
         base = {}
         for g in (32, 64, 128):
             for R in (0, 64, 128, 512):
-                cache, s, lens, wr = build_workload(w, dev, group=g, recent=R)
-                ln = decode_line(f"config 5 layer (g={g}, R={R})", wr, cache, s, lens)
+                layers = []
+                for layer in range(w.layers):  # independent seeds 500 + layer
+                    cache, s, lens, wl = build_workload(w, dev, group=g, recent=R,
+                                                        seed=w.seed + layer)
+                    layers.append((cache, s))
+                dec_b, app_b, _, _ = algorithmic_bytes(lens, wl)
+
+                def step():
+                    for cache, s in layers:
+                        cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+                        cache.decode(s["q"], s["lens"], s["out"], s["lse"])
+
+                def decodes():
+                    for cache, s in layers:
+                        cache.decode(s["q"], s["lens"], s["out"], s["lse"])
+
+                t_step = _timed(_graph(step).replay, warm=3, samples=10)
+                t_dec = _timed(_graph(decodes).replay, warm=3, samples=10)
+                st = [c.read_status() for c, _ in layers]
+                tok = int(lens.sum())
                 if R == 0:
-                    base[g] = ln["decode"]["median_ms"]
-                print(json.dumps({"report": "config 5 point", "group": g, "recent": R,
-                                  "layer_decode_ms": ln["decode"]["median_ms"],
-                                  "layer_append_ms": ln["append"]["median_ms"],
-                                  "step_36_layers_ms (x36, one layer timed)":
-                                      36 * (ln["decode"]["median_ms"] + ln["append"]["median_ms"]),
-                                  "cost_vs_R0": ln["decode"]["median_ms"] / base[g]}), flush=True)
-                del cache
+                    base[g] = t_step["median_ms"]
+                print(json.dumps({
+                    "report": "config 5: 36-layer step", "workload": w.name, "group": g,
+                    "recent": R, "layers": w.layers, "batch": int(len(lens)),
+                    "tokens_per_layer": tok,
+                    "step_ms": t_step, "decode_only_ms": t_dec,
+                    "decode_ms_per_layer": t_dec["median_ms"] / w.layers,
+                    "decode_bytes_per_layer": dec_b,
+                    "decode_GBps": dec_b * w.layers / (t_dec["median_ms"] / 1e3) / 1e9,
+                    "decode_frac_of_hbm": dec_b * w.layers / (t_dec["median_ms"] / 1e3) / 1e9 / hbm,
+                    "tokens_per_s_per_layer": tok * w.layers / (t_step["median_ms"] / 1e3),
+                    "step_cost_vs_R0": t_step["median_ms"] / base[g],
+                    "status": max(st)}), flush=True)
+                del layers, cache, s
                 torch.cuda.empty_cache()
 
 

@@ -218,6 +218,26 @@ def test_rollout_batch256_100_steps():
     assert mean <= 2e-4
 
 
+def test_36_layer_workload_two_layers():
+    # two independently seeded layers (seeds 500 and 501) of the 128 x 8192
+    # step at its configured point (R = 128, group 32): every sampled
+    # sequence's cache bytes and decode outputs, per layer
+    w0 = W.WORKLOADS["qwen3_8b_36l"]
+    dev = torch.device("cuda")
+    for layer in (0, 1):
+        cache, s, lens, w = build_workload(w0, dev, seed=w0.seed + layer)
+        out, lse = _run_step(cache, s)
+        seqs = W.sample_rows(w.seed, len(lens), 8)
+        qs = s["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+        srcs = {b: source_kv(w, b, int(lens[b]), dev) for b in seqs}
+        for b in seqs:
+            _check_seq_bytes(cache, w, b, *srcs[b], int(lens[b]))
+        _, mean = _check_decode(out, lse, w, seqs, srcs, qs, lens)
+        assert mean <= 2e-4
+        del cache
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("recent,group", [(0, 32), (128, 64), (512, 128), (64, 32)])
 def test_36_layer_workload_one_layer(recent, group):
     # one layer (seed 500) of the 128 x 8192 step at points of the R x group sweep
