@@ -348,7 +348,7 @@ int kv4_split_combine(const float* part_o, const float* part_lse, int32_t rows, 
  *   kv4_bf16_decode_attn: with max_splits = 0, head_dim 128, 4 query heads
  *   per kv head and num_seqs <= 2048, a tensor-core kernel (bf16 operands,
  *   fp32 accumulation, softmax weights entered as a bf16 head and tail) whose
- *   warps claim chunks of 16 pages of a (sequence, kv head) pair and merge
+ *   warps claim chunks of 64 pages of a (sequence, kv head) pair and merge
  *   the chunks of a pair in order (the result does not depend on which warp
  *   took which chunk); otherwise a CUDA-core split kernel with the split plan
  *   of kv4_decode_attn.  Its workspace is kv4_bf16_workspace_bytes(layout,

@@ -104,11 +104,11 @@ def test_bf16_comparator_matches_unquantized_attention():
 @pytest.mark.parametrize("max_splits", [0, 3])
 def test_bf16_comparator_tensor_core_kernel(max_splits):
     # head_dim 128, 4 query heads per kv head: with max_splits = 0 the
-    # tensor-core kernel (16-page work items claimed by warps; lengths with
+    # tensor-core kernel (64-page work items claimed by warps; lengths with
     # partial pages, several items per pair, an empty and a one-token
     # sequence), else the split kernel; both against exact attention, and the
     # tensor-core result repeated bit for bit
-    c = Case([0, 1, 15, 16, 17, 255, 256, 257, 1100, 5000], S=4, R=64, g=32, seed=12)
+    c = Case([0, 1, 15, 16, 17, 511, 512, 513, 1100, 5000], S=4, R=64, g=32, seed=12)
     gc = c.gpu(with_bf16=True)
     out, lse = c.gpu_decode(gc, max_splits=max_splits, bf16=True)
     ref, rlse = c.oracle_bf16()
