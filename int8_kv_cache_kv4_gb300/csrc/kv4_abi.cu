@@ -39,9 +39,11 @@ cudaError_t launch_decode_mma(const Layout&, const void*, const void*, const uin
                               cudaStream_t);
 bool stream_supported(const Layout&);
 long long stream_partials(const Layout&, int);
+size_t stream_plan_bytes();
 cudaError_t launch_decode_stream(const Layout&, const void*, const void*, const uint16_t*,
                                  const int32_t*, int, const int32_t*, float, float*, float*,
-                                 int32_t*, uint16_t*, float*, int32_t*, bool, cudaStream_t);
+                                 int32_t*, void*, uint16_t*, float*, int32_t*, bool,
+                                 cudaStream_t);
 
 // Split planning.  The host does not know the per-sequence lengths (they live
 // on the device), so the plan is sized from the block-table capacity: about
@@ -96,11 +98,13 @@ static Layout to_layout(const kv4_layout* l) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace: fp32 partial outputs [rows][n_split][d], their log-normalisers
-// [rows][n_split] and one int32 completion ticket per (sequence, kv head).
+// [rows][n_split], one int32 completion ticket per (sequence, kv head) and,
+// where the work-balanced kernel may run, its plan (the per-CTA start table).
 struct Workspace {
   float* part_o;
   float* part_lse;
   int32_t* tickets;
+  void* plan;
   size_t ticket_bytes;
   size_t bytes;
 };
@@ -123,12 +127,15 @@ static Workspace ws_layout(const kv4_layout* l, int num_seqs, const Plan& p, int
   const size_t prow = partial_rows(l, num_seqs, p, max_splits);
   const size_t o = round256(prow * l->head_dim * sizeof(float));
   const size_t z = round256(prow * sizeof(float));
+  const bool stream = max_splits == 0 && stream_supported(to_layout(l)) && num_seqs > 0;
   Workspace w;
   w.ticket_bytes = (size_t)num_seqs * l->num_kv_heads * sizeof(int32_t);
-  w.bytes = o + z + round256(w.ticket_bytes);
+  const size_t tk = round256(w.ticket_bytes);
+  w.bytes = o + z + tk + (stream ? round256(stream_plan_bytes()) : 0);
   w.part_o = (float*)base;
   w.part_lse = (float*)((char*)base + o);
   w.tickets = (int32_t*)((char*)base + o + z);
+  w.plan = stream ? (void*)((char*)base + o + z + tk) : nullptr;
   return w;
 }
 static size_t ws_bytes(const kv4_layout* l, int num_seqs, const Plan& p, int max_splits) {
@@ -337,8 +344,8 @@ int decode_attn(const kv4_layout* l, const void* paged, const void* side, const 
   cudaError_t e;
   if (which == KV4_KERNEL_STREAM)
     e = launch_decode_stream(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                             w.part_o, w.part_lse, w.tickets, out, out_lse, dev_status, rotate_q,
-                             st);
+                             w.part_o, w.part_lse, w.tickets, w.plan, out, out_lse, dev_status,
+                             rotate_q, st);
   else if (which == KV4_KERNEL_MMA_SYNC)
     e = launch_decode_mma(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale, p.n4,
                           p.pages_per_split, p.n8, p.prot_per_split, w.part_o, w.part_lse,

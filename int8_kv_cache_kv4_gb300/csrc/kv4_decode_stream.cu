@@ -167,18 +167,28 @@ struct Pend {
   int c0, n0;      // (merging CTA) the CTAs holding the pair's partials
 };
 
+// Where one CTA of the decode grid starts: the first unit of its share and
+// the segment holding it.
+struct __align__(16) StreamStart {
+  long long u_begin;
+  Seg cs;
+};
+// The stream's cut over the decode grid, written by stream_prep_kernel and
+// read once by every CTA of decode_stream_kernel at its start: CTA c's share
+// ends where CTA c + 1's begins (start[C].u_begin = the stream's length).
+struct __align__(16) StreamPlan {
+  Cut cut;
+  long long total;  // units in the stream
+  StreamStart start[kMaxStreamCtas + 1];
+};
+
 struct __align__(16) StreamSmem {
   QPrep qp;                         // the current pair's query fragments and sums
-  union {
-    float mrg_o[kSW][SG][SD];    // per-warp unnormalised outputs at a segment end
-    long long scan[2 * kST];   // start-up: per-thread unit counts and costs, then prefixes
-  };
+  float mrg_o[kSW][SG][SD];         // per-warp unnormalised outputs at a segment end
   uint16_t qraw[SG * SD];           // next pair's query (bf16), bulk-copied ahead
   float mrg_m[kSW][SG];
   float mrg_l[kSW][SG];
   float mrg_mt[kSW][SG][SD / 32];
-  long long total, totalc;          // units and cost of the stream
-  long long cut_b, cut_e;           // start-up: first unit of this CTA's share and of the next
   Cut cut;                          // the stream's cut over the CTAs
   long long u_begin, u_end;         // this CTA's share of the stream
   Seg cs;                           // current segment of this CTA
@@ -189,7 +199,6 @@ struct __align__(16) StreamSmem {
   Pend comb[2];                     // pair to merge at boundary k (slot k & 1)
   int go[2];                        // comb[k & 1] is valid
   int new_q;                        // a next segment follows (its query is being copied)
-  int start_b;
   uint64_t bar[kSW][kSStages];      // stage completion (one per warp and stage)
   uint64_t qbar;                    // completion of the qraw copy
 };
@@ -354,7 +363,8 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_lens, int B,
     const int32_t* __restrict__ block_table, float scale_log2, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* __restrict__ tickets, uint16_t* __restrict__ out,
-    float* __restrict__ out_lse, int32_t* status, int defer, float q_rot) {
+    float* __restrict__ out_lse, int32_t* status, int defer, float q_rot,
+    const StreamPlan* __restrict__ plan) {
   constexpr int D = SD;
   constexpr int GS = D / NG;  // channels per INT4 group
   constexpr int cb = 16 * D + 128 * NG;
@@ -363,114 +373,38 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   uint8_t* stage_base = smem_raw + ((sizeof(StreamSmem) + 127) / 128) * 128;
   const int C = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // a deferred merge (stream_merge_kernel, launched as this grid's programmatic
-  // dependent) may take the SMs this grid's CTAs free; it waits for the whole
-  // grid before reading any result
-  if (defer) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ------------------------------------------ stream size and this CTA's start
-  const int per = (B + kST - 1) / kST;
-  const int b_lo = min(B, (int)threadIdx.x * per), b_hi = min(B, b_lo + per);
-  long long mine = 0, mine_c = 0;  // units and cost of this thread's sequences
-  bool bad_len = false;
-  for (int b = b_lo; b < b_hi; ++b) {
-    const int raw = __ldg(seq_lens + b);
-    const int len = clamp_len(raw, L);
-    bad_len |= len != raw;
-    const int np = prot_units(len, L), n4 = int4_units(len, L);
-    mine += (long long)L.h_kv * (np + n4);
-    mine_c += (long long)L.h_kv * seg_cost(np, n4);
-  }
-  if (c == 0 && bad_len) set_status(status, KV4_STATUS_BAD_LEN);
-  if (lane == 0) {  // (made visible by the barriers below)
+  // ------------------------------------------------ this CTA's share (plan)
+  if (lane == 0) {  // (made visible by the barrier below)
     for (int st = 0; st < kSStages; ++st) mbar_init(&sm.bar[warp][st], 1);
     if (warp == 0) mbar_init(&sm.qbar, 1);
     fence_mbar_init();
   }
-  sm.scan[threadIdx.x] = mine;
-  sm.scan[kST + threadIdx.x] = mine_c;
+  // The plan is written by stream_prep_kernel, launched just before this grid
+  // (a programmatic dependent of it, this grid may start as it exits); the
+  // wait also covers every kernel before it on the stream (the prep kernel
+  // waited for them), so that the cache pages and tickets are ready.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
-    sm.start_b = B;
-    sm.cut_b = -1;  // (set below by the threads that find this CTA's first / end unit)
-    sm.cut_e = -1;
+    const StreamStart s = plan->start[c];
+    const long long u_end = plan->start[c + 1].u_begin;
+    sm.cut = plan->cut;
+    sm.u_begin = s.u_begin;
+    sm.u_end = u_end;
+    sm.cs = s.cs;
+    sm.pend.valid = 0;
+    // the first pair's query, fetched ahead of the page copies issued below
+    // (the copy engine serves one SM's copies in order: behind them it would
+    // arrive last)
+    if (s.u_begin < u_end)
+      stream_query_fetch(sm, q, (long long)s.cs.b * L.h_q + (long long)s.cs.h * SG);
   }
   __syncthreads();
-  if (warp < 2) {  // exclusive prefixes over the per-thread counts (warp 0) and costs (warp 1)
-    constexpr int E = kST / 32;
-    long long* sc = sm.scan + warp * kST;
-    long long v[E], run = 0;
-#pragma unroll
-    for (int k = 0; k < E; ++k) {
-      v[k] = run;
-      run += sc[E * lane + k];
-    }
-    long long incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const long long excl = incl - run;
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < E; ++k) sc[E * lane + k] = excl + v[k];
-    if (lane == 31) {
-      if (warp == 0) sm.total = incl;
-      else sm.totalc = incl;
-    }
-  }
-  __syncthreads();
-  // The stream is cut by cost over Cw CTAs: CTA c takes the units from the
-  // first whose stream cost reaches T(c) up to the first whose cost reaches
-  // T(c + 1) (Cut: shares weighted by launch rank).  Cw keeps every share at
-  // least one unit's cost wide, so every working CTA holds a unit (the
-  // partial counts rely on it).
-  const long long U = sm.total, Wc = sm.totalc;
-  const Cut cut = stream_cut(Wc, C);
-  const int Cw = cut.Cw;
-  if (c < Cw) {
-    const long long Tb = cut.start(c), Te = cut.start(c + 1);
-    const long long exu = sm.scan[threadIdx.x], exc = sm.scan[kST + threadIdx.x];
-    if (Tb >= exc && Tb < exc + mine_c)
-      sm.cut_b = unit_at_cost(Tb, b_lo, b_hi, exu, exc, L, seq_lens);
-    if (Te < Wc && Te >= exc && Te < exc + mine_c)
-      sm.cut_e = unit_at_cost(Te, b_lo, b_hi, exu, exc, L, seq_lens);
-  }
-  __syncthreads();
-  const long long u_begin = c < Cw ? sm.cut_b : U;
-  const long long u_end = c < Cw && sm.cut_e >= 0 ? sm.cut_e : U;
-  if (u_begin < u_end) {
-    const long long ex = sm.scan[threadIdx.x];
-    if (u_begin >= ex && u_begin < ex + mine) {
-      long long pre = ex, pre_c = sm.scan[kST + threadIdx.x];
-      for (int b = b_lo; b < b_hi; ++b) {
-        const int len = clamp_len(__ldg(seq_lens + b), L);
-        const int np = prot_units(len, L), n4 = int4_units(len, L);
-        const long long ub = (long long)L.h_kv * (np + n4);
-        if (u_begin < pre + ub) {
-          // this CTA's first segment, set up by the thread that found it; the
-          // first pair's query is fetched ahead of the page copies issued
-          // below (the copy engine serves one SM's copies in order: behind
-          // them it would arrive last)
-          Seg cs;
-          seg_set(cs, b, 0, len, L);
-          cs.start = pre;
-          cs.cs = pre_c;
-          while (cs.start + cs.n <= u_begin) seg_next(cs, L, seq_lens, B);
-          sm.cs = cs;
-          sm.start_b = b;
-          sm.u_begin = u_begin;
-          sm.u_end = u_end;
-          sm.cut = cut;
-          sm.pend.valid = 0;
-          stream_query_fetch(sm, q, (long long)cs.b * L.h_q + (long long)cs.h * SG);
-          break;
-        }
-        pre += ub;
-        pre_c += (long long)L.h_kv * seg_cost(np, n4);
-      }
-    }
-  }
+  // Every CTA has read its plan entry: the next kernels on the stream may
+  // launch (the next call's prep kernel rewrites the plan; an append waits for
+  // this grid before it writes the cache).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long u_begin = sm.u_begin;
   // sequences with nothing to attend: zero output, log-normaliser -inf
   // (written at the end, off the path to the first page copies)
   auto zero_empty = [&]() {
@@ -483,8 +417,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
           out_lse[(long long)b * L.h_q + idx] = -INFINITY;
     }
   };
-  __syncthreads();
-  if (sm.start_b >= B) {  // no units for this CTA
+  if (u_begin >= sm.u_end) {  // no units for this CTA
     zero_empty();
     return;
   }
@@ -572,13 +505,7 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
                  p_src8 + 2LL * NS * D + 2LL * NSP + 2 * slot0, sbytes, bar);
     }
   };
-  if (lane == 0) {
-    // The grid may be launched while the kernel before it still runs
-    // (programmatic dependent launch: the append kernel lets its dependents
-    // start at once).  Everything above read only the lengths, the block
-    // table and the query; the cache pages and the completion tickets are
-    // touched only after this wait, by the lanes that wait here.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (lane == 0) {  // the warp's first units into its stages
     sm.prod[warp] = sm.cs;
     p_j = (int)(max(u_begin, sm.cs.start) - sm.cs.start) + warp;
     prod_next();
@@ -1109,15 +1036,143 @@ __global__ void __launch_bounds__(kST, kStreamMinBlocks) decode_stream_kernel(
   zero_empty();
 }
 
-// Zeroes the completion tickets of the fused merge.  Launched as a
-// programmatic dependent of the kernel before it, it lets the decode kernel
-// start at once, and completes only once that earlier kernel has completed
-// (its wait), so that the decode's own wait covers both.
-__global__ void __launch_bounds__(256) stream_tickets_zero_kernel(int32_t* __restrict__ tickets,
-                                                                 int n) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) tickets[i] = 0;
+// The stream's cut over the decode grid of C CTAs: per CTA the first unit of
+// its share and the segment holding it, then, once the kernels before it on
+// the stream have completed, the completion tickets of the fused merge set to
+// zero.  Launched as a programmatic dependent of the kernel before it (the
+// previous decode call lets its dependents launch once its CTAs have read
+// their plan entries), the cut is worked out while that kernel finishes; the
+// decode grid, launched as this kernel's dependent, starts as it exits.
+// Each CTA counts the whole stream (the lengths) and its thread k works out
+// share boundary k of the CTAs it serves (boundaries 0 .. C).
+constexpr int kPrepThreads = 128;
+// the last thread t whose prefix ex[t] is at most x (ex nondecreasing, ex[0] = 0)
+__device__ inline int prep_owner(const long long* ex, long long x) {
+  int lo = 0, hi = kPrepThreads - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ex[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+__global__ void __launch_bounds__(kPrepThreads) stream_prep_kernel(
+    Layout L, const int32_t* __restrict__ seq_lens, int B, int C, StreamPlan* __restrict__ plan,
+    const int32_t* __restrict__ block_table, const uint16_t* __restrict__ q,
+    int32_t* __restrict__ tickets, int n_tickets, int32_t* status) {
+  __shared__ long long ex_u[kPrepThreads], ex_c[kPrepThreads];
+  __shared__ long long wsum[2][kPrepThreads / 32];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // units and cost of this thread's sequences
+  const int per = (B + kPrepThreads - 1) / kPrepThreads;
+  auto b_lo = [&](int tt) { return min(B, tt * per); };
+  auto b_hi = [&](int tt) { return min(B, tt * per + per); };
+  long long mine = 0, mine_c = 0;
+  bool bad_len = false;
+  for (int b = b_lo(t); b < b_hi(t); ++b) {
+    const int raw = __ldg(seq_lens + b);
+    const int len = clamp_len(raw, L);
+    bad_len |= len != raw;
+    const int np = prot_units(len, L), n4 = int4_units(len, L);
+    mine += (long long)L.h_kv * (np + n4);
+    mine_c += (long long)L.h_kv * seg_cost(np, n4);
+  }
+  if (bad_len && blockIdx.x == 0) set_status(status, KV4_STATUS_BAD_LEN);
+  // exclusive prefixes over the threads: within each warp, then over warps
+  long long iu = mine, ic = mine_c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long yu = __shfl_up_sync(0xffffffffu, iu, o);
+    const long long yc = __shfl_up_sync(0xffffffffu, ic, o);
+    if (lane >= o) {
+      iu += yu;
+      ic += yc;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = iu;
+    wsum[1][warp] = ic;
+  }
+  __syncthreads();
+  long long bu = 0, bc = 0, U = 0, Wc = 0;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) {
+    if (w < warp) {
+      bu += wsum[0][w];
+      bc += wsum[1][w];
+    }
+    U += wsum[0][w];
+    Wc += wsum[1][w];
+  }
+  ex_u[t] = bu + iu - mine;
+  ex_c[t] = bc + ic - mine_c;
+  __syncthreads();
+  // The stream is cut by cost over Cw CTAs: CTA c takes the units from the
+  // first whose stream cost reaches T(c) up to the first whose cost reaches
+  // T(c + 1) (Cut: shares weighted by launch rank).  Cw keeps every share at
+  // least one unit's cost wide, so every working CTA holds a unit (the
+  // partial counts rely on it).  Boundaries from Cw on are the stream's end.
+  const Cut cut = stream_cut(Wc, C);
+  if (blockIdx.x == 0 && t == 0) {
+    plan->cut = cut;
+    plan->total = U;
+  }
+  const int k = blockIdx.x * kPrepThreads + t;
+  if (k <= C) {
+    StreamStart s;
+    s.u_begin = U;
+    s.cs.start = U;
+    s.cs.cs = Wc;
+    s.cs.b = B;
+    s.cs.h = 0;
+    s.cs.len = 0;
+    s.cs.np = 0;
+    s.cs.n = 0;
+    if (k < cut.Cw) {
+      const long long Tb = cut.start(k);
+      const int tb = prep_owner(ex_c, Tb);
+      s.u_begin = unit_at_cost(Tb, b_lo(tb), b_hi(tb), ex_u[tb], ex_c[tb], L, seq_lens);
+    }
+    if (k < C && s.u_begin < U) {
+      // the segment holding unit u_begin: in the sequences of the thread
+      // whose unit range holds it
+      const int tu = prep_owner(ex_u, s.u_begin);
+      long long pre = ex_u[tu], pre_c = ex_c[tu];
+      for (int b = b_lo(tu); b < b_hi(tu); ++b) {
+        const int len = clamp_len(__ldg(seq_lens + b), L);
+        const int np = prot_units(len, L), n4 = int4_units(len, L);
+        const long long ub = (long long)L.h_kv * (np + n4);
+        if (s.u_begin < pre + ub) {
+          Seg cs;
+          seg_set(cs, b, 0, len, L);
+          cs.start = pre;
+          cs.cs = pre_c;
+          while (cs.start + cs.n <= s.u_begin) seg_next(cs, L, seq_lens, B);
+          s.cs = cs;
+          // into L2 ahead of the decode grid: the pair's query rows and the
+          // block-table entries of its first INT4 units
+          const char* qr = reinterpret_cast<const char*>(
+              q + ((long long)cs.b * L.h_q + (long long)cs.h * SG) * SD);
+#pragma unroll
+          for (int o = 0; o < SG * SD * 2; o += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + o));
+          const int j0 = (int)(s.u_begin - cs.start);
+          const int p0 = kSPages * max(0, j0 - cs.np);
+          if (cs.n > cs.np)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(block_table + (long long)cs.b * L.max_pages +
+                                                           min(len, L.S) / kPage + p0));
+          break;
+        }
+        pre += ub;
+        pre_c += (long long)L.h_kv * seg_cost(np, n4);
+      }
+    }
+    plan->start[k] = s;
+  }
+  // The tickets may still be in use by the kernels before this one (a decode
+  // call on the same workspace): zero them once those have completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = k; i < n_tickets; i += gridDim.x * kPrepThreads) tickets[i] = 0;
 }
 
 // Eq. A1 for pairs whose partials are spread over many CTAs (few, long
@@ -1134,6 +1189,9 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   __shared__ long long red64[2][kMergeThreads / 32];
   __shared__ float redf[kMergeThreads / 32];
   __shared__ float4 acc_s[kMergeThreads / 32][32];
+  // the next call's prep kernel may start (it writes the plan, and the
+  // tickets only after waiting for this grid; nothing here reads either)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int pair = blockIdx.x / SG, j = blockIdx.x % SG;
   const int b = pair / L.h_kv, h = pair % L.h_kv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1253,6 +1311,9 @@ long long stream_partials(const Layout& L, int num_seqs) {
   return (long long)num_seqs * L.h_kv + kMaxStreamCtas;
 }
 
+// Bytes of the stream's plan (the per-CTA start table) in the workspace.
+size_t stream_plan_bytes() { return sizeof(StreamPlan); }
+
 // Eq. A1 for every pair held by more than one CTA, from the partials the
 // work-balanced decode kernel left on a grid of C CTAs; the merge recounts
 // the stream from the lengths.
@@ -1280,8 +1341,8 @@ template <int NG>
 cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side,
                             const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                             const int32_t* block_table, float sm_scale, float* part_o,
-                            float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                            int32_t* status, float q_rot, cudaStream_t st) {
+                            float* part_lse, int32_t* tickets, void* plan, uint16_t* out,
+                            float* out_lse, int32_t* status, float q_rot, cudaStream_t st) {
   constexpr int cb = 16 * SD + 128 * NG;
   constexpr size_t smem =
       ((sizeof(StreamSmem) + 127) / 128) * 128 + (size_t)kSW * kSStages * kSPages * cb;
@@ -1308,23 +1369,23 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
   // With few pairs each one spreads over many CTAs; its merge then runs as a
   // separate, wider kernel instead of in the last CTA.
   const int defer = 8LL * num_seqs * L.h_kv < grid ? 1 : 0;
-  // The in-kernel merge counts finished units per pair on tickets that start
-  // at 0, zeroed by a small kernel.  Both kernels are programmatic dependents
-  // of the kernel before them: the decode grid's start-up (the cut of the
-  // stream, its first query) overlaps the zeroing and, after kv4_quant_append,
-  // the append kernel; its waits before the first page copy cover both.
+  // The prep kernel cuts the stream over the grid into the plan and zeroes
+  // the completion tickets of the in-kernel merge; it is a programmatic
+  // dependent of the kernel before it, and the decode grid of it.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const int n_tickets = num_seqs * L.h_kv;
-  if (!defer && n_tickets > 0) {
-    cudaLaunchConfig_t zc = {};
-    zc.gridDim = dim3((unsigned)std::min(64, (n_tickets + 255) / 256));
-    zc.blockDim = dim3(256);
-    zc.stream = st;
-    zc.attrs = attr;
-    zc.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&zc, stream_tickets_zero_kernel, tickets, n_tickets)) != cudaSuccess)
+  StreamPlan* sp = static_cast<StreamPlan*>(plan);
+  {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)(grid / kPrepThreads + 1));  // boundaries 0 .. grid
+    pc.blockDim = dim3(kPrepThreads);
+    pc.stream = st;
+    pc.attrs = attr;
+    pc.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&pc, stream_prep_kernel, L, seq_lens, num_seqs, grid, sp,
+                                block_table, q, tickets, defer ? 0 : num_seqs * L.h_kv,
+                                status)) != cudaSuccess)
       return e;
   }
   {
@@ -1338,7 +1399,7 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
     e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<NG>, L, (const uint8_t*)paged,
                            (const uint8_t*)side, q, seq_lens, num_seqs, block_table,
                            sm_scale * kLog2e, part_o, part_lse, tickets, out, out_lse, status, defer,
-                           q_rot);
+                           q_rot, (const StreamPlan*)sp);
     if (e != cudaSuccess) return e;
   }
   if (defer)
@@ -1349,20 +1410,20 @@ cudaError_t launch_stream_t(const Layout& L, const void* paged, const void* side
 cudaError_t launch_decode_stream(const Layout& L, const void* paged, const void* side,
                                  const uint16_t* q, const int32_t* seq_lens, int num_seqs,
                                  const int32_t* block_table, float sm_scale, float* part_o,
-                                 float* part_lse, int32_t* tickets, uint16_t* out, float* out_lse,
-                                 int32_t* status, bool rotate_q, cudaStream_t st) {
+                                 float* part_lse, int32_t* tickets, void* plan, uint16_t* out,
+                                 float* out_lse, int32_t* status, bool rotate_q, cudaStream_t st) {
   // the query rotated in the kernel's query set-up (Hadamard K-rotation)
   const float q_rot = rotate_q ? hadamard_scale(SD) : 0.f;
   switch (L.d_h / L.g) {
     case 4:
       return launch_stream_t<4>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
+                                part_o, part_lse, tickets, plan, out, out_lse, status, q_rot, st);
     case 2:
       return launch_stream_t<2>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
+                                part_o, part_lse, tickets, plan, out, out_lse, status, q_rot, st);
     case 1:
       return launch_stream_t<1>(L, paged, side, q, seq_lens, num_seqs, block_table, sm_scale,
-                                part_o, part_lse, tickets, out, out_lse, status, q_rot, st);
+                                part_o, part_lse, tickets, plan, out, out_lse, status, q_rot, st);
   }
   return cudaErrorInvalidValue;
 }
