@@ -35,6 +35,8 @@ from int8_kv_cache_kv4_gb300.cache import build_workload  # noqa: E402
 
 METRIC = "decode-attn resident KV tokens/s per layer and achieved HBM GB/s vs 8 TB/s"
 UNIT = "tokens/s"
+# seed offset of the second layer cache the timed steps alternate with
+SECOND_LAYER_SEED = 100
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the default decode kernel on the default workload, from the ncu capture
@@ -44,8 +46,8 @@ UNIT = "tokens/s"
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("c5b559fbd04c5e8a", "qwen3_8b_b64"): 387998720 + 2321152,
-           ("c5b559fbd04c5e8a", "long_128k"): 168157952 + 1327360}
+TRAFFIC = {("35fac1b82f076e06", "qwen3_8b_b64"): 387802112 + 1554944,
+           ("35fac1b82f076e06", "long_128k"): 168166656 + 683264}
 
 
 # ------------------------------------------------------------------ helpers
@@ -159,7 +161,8 @@ def replica_value(world: int, tokens_per_replica: int, ms_per_step: float) -> fl
 # --------------------------------------------------------------- workload
 
 def run_step(cache, s, max_splits=0, ev=None):
-    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+    # (the KV4 cache only: a bf16 comparator cache, where built, is not part of the step)
+    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"], comparator=False)
     if ev is not None:
         ev.record()
     cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=max_splits)
@@ -186,26 +189,35 @@ def run_kv4(args):
 
     w = W.WORKLOADS[args.workload]
     cache, s, lens, w = build_workload(w, dev, with_bf16=not args.no_bf16)
+    # A second layer of the same shape (its own seeded K/V, query, outlier
+    # channels and block table): the timed steps alternate between the two, as
+    # consecutive layers of a model do, so that no step finds the previous
+    # step's pages in L2.
+    cache2, s2, _, _ = build_workload(w, dev, lens=lens, seed=w.seed + SECOND_LAYER_SEED)
+    layers = [(cache, s), (cache2, s2)]
     dec_bytes, app_bytes, n4_tok, n8_tok = algorithmic_bytes(lens, w)
     tokens = int(lens.sum())
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
-        run_step(cache, s, args.max_splits)
+    def steps(n):
+        for i in range(n):
+            run_step(*layers[i % 2], args.max_splits)
+
+    steps(max(args.warmup, 2))
     torch.cuda.synchronize()
-    cache.clear_status()
-    # The timed steps replay one CUDA graph captured from the step's C-ABI
-    # calls (append, then decode), so that host-side argument marshalling does
-    # not starve the GPU and the decode's start-up can overlap the append
-    # (programmatic dependent launch); --no-graph times eager calls.
-    g_step = None
+    for c, _ in layers:
+        c.clear_status()
+    # The K timed steps are launched as one CUDA graph captured from the
+    # steps' C-ABI calls (append, then decode, per step), so that host-side
+    # argument marshalling and per-graph launch gaps stay out of the steps;
+    # inside it each call's kernels are programmatic dependents of the kernels
+    # before them.  --no-graph launches the same calls eagerly.
+    run_timed = lambda: steps(args.steps)  # noqa: E731
     if not args.no_graph:
-        g_step = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_step):
-            run_step(cache, s, args.max_splits)
-        for _ in range(args.warmup):
-            g_step.replay()
+        g_steps = _graph(run_timed)
+        g_steps.replay()  # (the first replay uploads the graph)
         torch.cuda.synchronize()
+        run_timed = g_steps.replay
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -217,36 +229,34 @@ def run_kv4(args):
     t1 = torch.cuda.Event(enable_timing=True)
     # Keep the GPU busy while the host enqueues the timed steps, so that the
     # events bracket back-to-back device work rather than host submission
-    # latency (on a loaded host a step's launch can arrive after the previous
-    # step has finished).  The sleep precedes t0 and is not timed.
+    # latency.  The sleep precedes t0 and is not timed.
     torch.cuda._sleep(int(2.1e6 * max(5.0, 0.2 * args.steps)))
     t0.record(stream)
-    for i in range(args.steps):
-        if g_step is not None:
-            g_step.replay()
-        else:
-            run_step(cache, s, args.max_splits)
+    run_timed()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
-    status = cache.read_status()
+    status = cache.read_status() | cache2.read_status()
 
-    # The decode call and the append call alone (the roofline's kernel time):
-    # K CUDA-event samples each, every one behind an untimed GPU sleep.
-    dec_fn = lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)  # noqa: E731
-    app_fn = lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])  # noqa: E731
+    # The decode call's duration (the roofline's kernel time): the mean over
+    # back-to-back calls alternating between the two layers, as in the steps;
+    # and, beside it, single calls each behind an untimed GPU sleep.
+    dec_fns = [lambda c=c, t=t: c.decode(t["q"], t["lens"], t["out"], t["lse"],  # noqa: E731
+                                         max_splits=args.max_splits) for c, t in layers]
+    n_dec = max(2 * args.steps, 40)
+    dec_avg = _chained(dec_fns, n_dec, graph=not args.no_graph)
+    app_fn = lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"], comparator=False)  # noqa: E731
+    dec_one = dec_fns[0]
     if not args.no_graph:
-        g_dec, g_app = _graph(dec_fn), _graph(app_fn)
-        dec_fn, app_fn = g_dec.replay, g_app.replay
-    dec_t = _timed(dec_fn, warm=args.warmup, samples=max(args.steps, 20))
+        dec_one, app_fn = _graph(dec_one).replay, _graph(app_fn).replay
+    dec_iso = _timed(dec_one, warm=args.warmup, samples=max(args.steps, 20))
     app_t = _timed(app_fn, warm=args.warmup, samples=max(args.steps, 20))
 
     ms_per_step = reduce_max_ms(total_ms, world, dev) / args.steps
     value = replica_value(world, tokens, ms_per_step)
-    dec_avg = dec_t["mean_ms"]
     hbm_peak, peak_kind = peaks()
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
     ksrc = kernel_source_hash()
@@ -297,24 +307,28 @@ def run_kv4(args):
                    "sink": w.sink, "recent": w.recent, "group": w.group, "page": 16,
                    "splits": kv4.num_splits(cache.layout, int(len(lens)), args.max_splits),
                    "parallelism": f"replicas x{world}", "decode_kernel": args.kernel,
-                   "launch": "eager" if args.no_graph else "CUDA graph replay of the C-ABI calls",
-                   "l2": "cache working set > L2 (no flush needed)"},
-        "decode_ms": dec_avg, "append_ms": app_t["mean_ms"],
+                   "layers": "steps alternate between two layer caches of this shape",
+                   "launch": ("eager C-ABI calls" if args.no_graph else
+                              "one CUDA graph of the K timed steps' C-ABI calls"),
+                   "l2": "cache working set > L2, each step on the other layer (no flush needed)"},
+        "decode_ms": dec_avg, "decode_ms_isolated": dec_iso["mean_ms"],
+        "append_ms": app_t["mean_ms"],
         "append_exposed_ms": ms_per_step - dec_avg,
         "decode_tokens_per_s": tokens / (dec_avg / 1e3),
         "decode_algorithmic_GBps": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": decode_kernel_name(args, w),
-                     "timed": "kv4_decode_attn call on the launching stream (CUDA-event mean): "
-                              "ticket-zeroing kernel + decode kernel",
+                     "timed": (f"kv4_decode_attn calls (prep + decode kernels): CUDA events on "
+                               f"the launching stream around {n_dec} back-to-back calls "
+                               f"alternating two layers' caches, mean per call"),
                      "bytes_per_launch": dec_bytes, "peak_source": peak_kind,
                      "kernel_source_hash": ksrc},
         "append_algorithmic_bytes": app_bytes,
-        # per step: quant_append_kernel, then the decode call's two kernels
-        # (stream_tickets_zero_kernel + decode_stream_kernel, or
-        # decode_stream_kernel + stream_merge_kernel for few long pairs)
-        "gpu_launches": 3 * args.steps,
+        # per step: quant_append_kernel, then the decode call's kernels
+        # (stream_prep_kernel + decode_stream_kernel, and stream_merge_kernel
+        # for few long pairs)
+        "gpu_launches": (3 + (1 if _defers(w, len(lens)) else 0)) * args.steps,
         "clocks": clk,
         "device_status": status,
         "e2e": e2e,
@@ -330,32 +344,46 @@ def run_kv4(args):
 
 
 def decode_record(w: W.Workload, dev, args, hbm_peak, ksrc):
-    """Decode call alone on workload w (cache built and appended here): the
-    CUDA-event mean over max(steps, 20) graph replays, its algorithmic bytes
-    and roofline fraction, and the kernel's DRAM traffic when a capture of
-    these sources exists."""
+    """Decode call alone on workload w (two layer caches built and appended
+    here): the mean per call over back-to-back calls alternating between the
+    layers, the single-call time beside it, its algorithmic bytes and roofline
+    fraction, and the kernel's DRAM traffic when a capture of these sources
+    exists."""
     import torch
     cache, s, lens, w = build_workload(w, dev, with_bf16=False)
-    cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"])
+    cache2, s2, _, _ = build_workload(w, dev, lens=lens, seed=w.seed + SECOND_LAYER_SEED)
+    layers = [(cache, s), (cache2, s2)]
+    for c, t in layers:
+        c.append(t["k"], t["v"], t["seq"], t["pos"], t["lens"])
+        c.clear_status()
     dec_bytes, _, _, _ = algorithmic_bytes(lens, w)
-    fn = lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"], max_splits=args.max_splits)  # noqa: E731
-    if not args.no_graph:
-        fn = _graph(fn).replay
-    cache.clear_status()
-    t = _timed(fn, warm=args.warmup, samples=max(args.steps, 20))
-    ms = t["mean_ms"]
+    fns = [lambda c=c, t=t: c.decode(t["q"], t["lens"], t["out"], t["lse"],  # noqa: E731
+                                     max_splits=args.max_splits) for c, t in layers]
+    n = max(2 * args.steps, 40)
+    ms = _chained(fns, n, graph=not args.no_graph)
+    one = _graph(fns[0]).replay if not args.no_graph else fns[0]
+    iso = _timed(one, warm=args.warmup, samples=max(args.steps, 20))
     achieved = dec_bytes / (ms / 1e3) / 1e9
     traffic = TRAFFIC.get((ksrc, w.name)) if args.kernel in ("auto", "stream") and args.max_splits == 0 else None
     rec = {"workload": w.name, "batch": int(len(lens)), "total_tokens": int(lens.sum()),
-           "decode_ms": ms, "decode_ms_median": t["median_ms"],
+           "decode_ms": ms, "decode_ms_isolated": iso["mean_ms"],
            "decode_tokens_per_s": int(lens.sum()) / (ms / 1e3),
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                         "frac": achieved / hbm_peak, "traffic": traffic,
-                        "kernel": decode_kernel_name(args, w), "bytes_per_launch": dec_bytes},
-           "device_status": cache.read_status()}
-    del cache, s
+                        "kernel": decode_kernel_name(args, w), "bytes_per_launch": dec_bytes,
+                        "timed": f"{n} back-to-back calls alternating two layers' caches"},
+           "device_status": cache.read_status() | cache2.read_status()}
+    del cache, s, cache2, s2, layers, fns, one
     torch.cuda.empty_cache()
     return rec
+
+
+def _defers(w: W.Workload, num_seqs: int) -> bool:
+    """Does the work-balanced decode merge its pairs in a separate kernel
+    (few pairs, each spread over many CTAs: 8 pairs per CTA of the grid)?"""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 8 * num_seqs * w.h_kv < 4 * sms  # (the grid: 4 CTAs per SM)
 
 
 def decode_kernel_name(args, w):
@@ -531,6 +559,32 @@ def _timed(fn, warm=10, samples=90, flush=None):
     return {"median_ms": statistics.median(ts), "mean_ms": statistics.mean(ts)}
 
 
+def _chained(fns, n, graph=True, reps=5):
+    """Mean time (ms) per call of n back-to-back calls cycling through fns,
+    CUDA events on the current stream around the whole chain (captured as one
+    CUDA graph unless graph is False; median over reps chains, each behind an
+    untimed GPU sleep)."""
+    import torch
+
+    def chain():
+        for i in range(n):
+            fns[i % len(fns)]()
+
+    run = _graph(chain).replay if graph else chain
+    run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2.1e6 * 3))  # ~3 ms of untimed GPU work while the host enqueues
+        e0.record()
+        run()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / n)
+    return statistics.median(ts)
+
+
 def _graph(fn):
     """fn (one or more C-ABI calls) captured as a CUDA graph after one eager
     call (which also performs the library's one-time per-device setup)."""
@@ -561,7 +615,7 @@ def run_report(args):
         dec_b, app_b, _, _ = algorithmic_bytes(lens, w)
         f = (lambda: l2_flush.zero_()) if flush else None
         gd, ga = _graph(lambda: cache.decode(s["q"], s["lens"], s["out"], s["lse"])), \
-            _graph(lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"]))
+            _graph(lambda: cache.append(s["k"], s["v"], s["seq"], s["pos"], s["lens"], comparator=False))
         td = _timed(gd.replay, flush=f)
         ta = _timed(ga.replay, flush=f)
         tok = int(lens.sum())

@@ -29,6 +29,23 @@
  *     offending token / page is skipped.  The caller zeroes it and reads it
  *     back when convenient.  May be NULL (problems are then silently skipped).
  *   - bf16 tensors are passed as const uint16_t* (IEEE bfloat16 bit patterns).
+ *   - Stream order and early launch: kv4_quant_append and, when it runs the
+ *     work-balanced kernel (max_splits = 0), kv4_decode_attn (and its
+ *     _hadamard / _noalloc forms) launch their kernels with programmatic
+ *     stream serialisation, so a call's first kernel may start while the
+ *     kernel before it on the stream finishes.  Before waiting for that kernel
+ *     they read only inputs the library never writes: the append its new K/V
+ *     rows, tok_seq, tok_pos, seq_lens and block_table; the decode seq_lens
+ *     (and, as L2 prefetches, q and block_table).  Such an input must
+ *     therefore be complete when the kernel before the call has completed: an
+ *     ordinary kernel, a copy or an event wait before the call all ensure it;
+ *     a kernel of the caller's that lets its dependents launch early must not
+ *     write them.  Everything else (the caches, the workspace, out) is
+ *     touched only after the wait.  In turn the append, and the decode once
+ *     each of its CTAs has started, let the next kernel on the stream launch
+ *     early: a caller kernel launched with programmatic stream serialisation
+ *     after them must call cudaGridDependencySynchronize() before it touches
+ *     anything the call reads or writes (ordinary launches are unaffected).
  *
  * Packed layout (bit-exact; the CPU oracle restates it independently)
  *   paged cache  = [num_pages][num_kv_heads][chunk]
@@ -167,9 +184,9 @@ size_t kv4_bf16_cache_bytes(const kv4_layout* layout);  /* comparator pages */
 
 /* Number of context splits per (sequence, kv head) that the split kernels use
  * for `num_seqs` sequences when given `max_splits` (0 = automatic), and the
- * workspace (device scratch: partial outputs, log-normalisers and completion
- * counters) kv4_decode_attn needs with that max_splits, for every kernel
- * choice. */
+ * workspace (device scratch: partial outputs, log-normalisers, completion
+ * counters and, with max_splits = 0, the work-balanced kernel's start table)
+ * kv4_decode_attn needs with that max_splits, for every kernel choice. */
 int32_t kv4_num_splits(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 size_t kv4_workspace_bytes(const kv4_layout* layout, int32_t num_seqs, int32_t max_splits);
 

@@ -87,11 +87,13 @@ class MixedKVCache(_LayerCache):
         self.bf16 = (torch.zeros(kv4.bf16_cache_bytes(self.layout), dtype=torch.uint8,
                                  device=self.device) if with_bf16 else None)
 
-    def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None):
+    def append(self, k_new, v_new, tok_seq, tok_pos, seq_lens, stream=None, comparator=True):
+        """kv4_quant_append (or its Hadamard form); with comparator=True also
+        the bf16 comparator cache, when this cache keeps one."""
         fn = kv4.kv4_quant_append_hadamard if self.hadamard_k else kv4.kv4_quant_append
         fn(self.layout, self.paged, self.side, k_new, v_new, tok_seq, tok_pos, seq_lens,
            self.block_table, self.status, stream)
-        if self.bf16 is not None:
+        if comparator and self.bf16 is not None:
             kv4.kv4_bf16_append(self.layout, self.bf16, k_new, v_new, tok_seq, tok_pos, seq_lens,
                                 self.block_table, self.status, stream)
 
