@@ -73,3 +73,44 @@ def test_few_long_sequences_among_idle_slots(where):
     lens[pos] = [2500, 3100, 1800, 2900]
     c = Case(lens, S=4, R=64, g=32, seed=24, h_q=8, h_kv=2)
     _run(c)
+
+
+@pytest.mark.parametrize("B", [12, 4], ids=["tickets", "merge-kernel"])
+def test_back_to_back_calls_on_one_workspace(B):
+    # Calls enqueued back to back on one stream and sharing one workspace: each
+    # decode call's prep kernel rewrites the plan while the decode before it
+    # finishes, and zeroes the tickets once it has; an append between calls
+    # starts during the previous decode's tail.  Every output must equal, bit
+    # for bit, that of the same call made alone.  B = 12 (96 pairs) merges in
+    # the decode kernel, B = 4 (32 pairs) in the separate merge kernel.
+    rng = np.random.default_rng(40 + B)
+    mixes = [list(rng.integers(0, 6000, B)), [20000] + [0] * (B - 1), list(rng.integers(1, 300, B))]
+    cases = [Case(m, S=4, R=128, g=32, seed=41 + i) for i, m in enumerate(mixes)]
+    gcs = [c.gpu() for c in cases]
+    alone = [c.gpu_decode(gc) for c, gc in zip(cases, gcs)]
+    # one workspace, as large as the largest of the three calls needs
+    n = max(kv4.workspace_bytes(gc.layout, B, 0) for gc in gcs)
+    shared = torch.empty(n, dtype=torch.uint8, device=gcs[0].device)
+    for gc in gcs:
+        gc._ws[(B, 0, False)] = shared
+    dev = gcs[0].device
+    order = [0, 1, 2, 1, 0, 2, 2, 0]
+    ins = [(torch.from_numpy(c.q.view(np.int16)).to(dev).view(torch.bfloat16),
+            torch.from_numpy(c.lens).to(dev)) for c in cases]
+    outs = [(torch.empty((B, cases[i].h_q, cases[i].d_h), dtype=torch.bfloat16, device=dev),
+             torch.empty((B, cases[i].h_q), dtype=torch.float32, device=dev)) for i in order]
+    k, v, s, p, la = cases[0].tokens(1)
+    to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)  # noqa: E731
+    app = (to(k, torch.int16).view(torch.bfloat16), to(v, torch.int16).view(torch.bfloat16),
+           to(s, torch.int32), to(p, torch.int32), to(la, torch.int32))
+    torch.cuda.synchronize()
+    for n, i in enumerate(order):
+        if n == 4 and len(s):
+            gcs[0].append(*app)  # rewrites case 0's step token with the same bytes
+        gcs[i].decode(ins[i][0], ins[i][1], outs[n][0], outs[n][1])
+    torch.cuda.synchronize()
+    for gc in gcs:
+        assert gc.read_status() == 0
+    for n, i in enumerate(order):
+        assert np.array_equal(outs[n][0].float().cpu().numpy(), alone[i][0].astype(np.float32)), (n, i)
+        assert np.array_equal(outs[n][1].cpu().numpy(), alone[i][1].astype(np.float32)), (n, i)
