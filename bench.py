@@ -46,8 +46,8 @@ SECOND_LAYER_SEED = 100
 # figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = ["kv4_decode_stream.cu", "kv4_stream_common.cuh", "kv4_mma.cuh", "kv4_decode_common.cuh",
                   "kv4_common.cuh"]
-TRAFFIC = {("35fac1b82f076e06", "qwen3_8b_b64"): 387802112 + 1554944,
-           ("35fac1b82f076e06", "long_128k"): 168166656 + 683264}
+TRAFFIC = {("153be8b4d64b8801", "qwen3_8b_b64"): 387799808 + 1533440,
+           ("153be8b4d64b8801", "long_128k"): 168165632 + 687616}
 
 
 # ------------------------------------------------------------------ helpers

@@ -285,6 +285,52 @@ __device__ inline void stream_merge_store(StreamSmem& sm, float* __restrict__ pa
   }
 }
 
+// Eq. A1, folded online: the partials P0 + k, k = k0, k0 + step, ... < n of
+// query head j, this lane's four channels.  Each batch of kB partials' outputs
+// and log-normalisers is requested at once (one round of L2 latency), then
+// folded into the running maximum log-normaliser m, the sum l of e^(z - m) and
+// the weighted output sum acc.  Empty partials (z = -inf) weigh nothing.
+template <int kB>
+__device__ inline void fold_partials(const float* __restrict__ part_o,
+                                     const float* __restrict__ part_lse, long long P0, int n,
+                                     int k0, int step, int j, int lane, float& m, float& l,
+                                     float4& acc) {
+  for (int kb = k0; kb < n; kb += kB * step) {
+    float z[kB];
+    float4 o[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int k = kb + u * step;
+      const bool in = k < n;
+      z[u] = in ? __ldcg(part_lse + (P0 + k) * SG + j) : -INFINITY;
+      o[u] = in ? __ldcg(reinterpret_cast<const float4*>(part_o + ((P0 + k) * SG + j) * SD) + lane)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mb = m;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) mb = fmaxf(mb, z[u]);
+    if (mb == -INFINITY) continue;
+    const float sc = m == -INFINITY ? 0.f : exp2f((m - mb) * kLog2e);
+    l *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      if (z[u] != -INFINITY) {
+        const float w = exp2f((z[u] - mb) * kLog2e);
+        l += w;
+        acc.x = fmaf(w, o[u].x, acc.x);
+        acc.y = fmaf(w, o[u].y, acc.y);
+        acc.z = fmaf(w, o[u].z, acc.z);
+        acc.w = fmaf(w, o[u].w, acc.w);
+      }
+    }
+    m = mb;
+  }
+}
+
 // Eq. A1 over the n partials P0 .. P0 + n - 1 of one pair; warp j merges
 // query head j.
 __device__ inline void stream_combine(const float* __restrict__ part_o,
@@ -293,50 +339,18 @@ __device__ inline void stream_combine(const float* __restrict__ part_o,
                                       float* __restrict__ out_lse) {
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;  // warp j < G: query head j
   if (j >= SG) return;
-  float M = -INFINITY;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(part_lse + (P0 + k) * SG + j));
-  M = warp_max(M);
+  float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Zl = 0.f;
-  if (M != -INFINITY) {
-    for (int k0 = 0; k0 < n; k0 += 32) {
-      const int k = k0 + lane;
-      const float z = k < n ? __ldcg(part_lse + (P0 + k) * SG + j) : -INFINITY;
-      const float wl = z == -INFINITY ? 0.f : exp2f((z - M) * kLog2e);
-      Zl += wl;
-      const int nr = min(32, n - k0);
-      for (int rr = 0; rr < nr; rr += 4) {  // four partials' loads in flight
-        float wv[4];
-        float4 o[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wv[u] = __shfl_sync(0xffffffffu, wl, (rr + u) & 31);
-          const bool use = rr + u < nr && wv[u] != 0.f;
-          o[u] = use ? __ldcg(reinterpret_cast<const float4*>(
-                               part_o + ((P0 + k0 + rr + u) * SG + j) * SD) + lane)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!use) wv[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          acc.x = fmaf(wv[u], o[u].x, acc.x);
-          acc.y = fmaf(wv[u], o[u].y, acc.y);
-          acc.z = fmaf(wv[u], o[u].z, acc.z);
-          acc.w = fmaf(wv[u], o[u].w, acc.w);
-        }
-      }
-    }
-  }
-  const float Z = warp_sum(Zl);
-  const bool empty = !(Z > 0.f);
-  const float inv = empty ? 0.f : 1.f / Z;
+  fold_partials<4>(part_o, part_lse, P0, n, 0, 1, j, lane, m, l, acc);
+  const bool empty = !(l > 0.f);
+  const float inv = empty ? 0.f : 1.f / l;
   const long long row = row0 + j;
   uint16_t* o = out + row * SD + 4 * lane;  // the output need only be 2-byte aligned
   o[0] = f32_to_bf16_bits(acc.x * inv);
   o[1] = f32_to_bf16_bits(acc.y * inv);
   o[2] = f32_to_bf16_bits(acc.z * inv);
   o[3] = f32_to_bf16_bits(acc.w * inv);
-  if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : M + logf(Z);
+  if (out_lse && lane == 0) out_lse[row] = empty ? -INFINITY : m + logf(l);
 }
 
 // Ticket thread, at boundary k: did the ticket taken for partial sm.pend
@@ -1180,14 +1194,12 @@ __global__ void __launch_bounds__(kPrepThreads) stream_prep_kernel(
 // eight warps splitting the pair's partials.  The partial positions follow
 // from the stream's share arithmetic, recounted from the lengths.
 constexpr int kMergeThreads = 256;
-// partials of one pair: it spans at most every CTA of the grid
-constexpr int kMergeMaxParts = kMaxStreamCtas;
 __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
     Layout L, const int32_t* __restrict__ seq_lens, int B, const float* __restrict__ part_o,
     const float* __restrict__ part_lse, int C, uint16_t* __restrict__ out,
     float* __restrict__ out_lse) {
   __shared__ long long red64[2][kMergeThreads / 32];
-  __shared__ float redf[kMergeThreads / 32];
+  __shared__ float red_m[kMergeThreads / 32], red_l[kMergeThreads / 32];
   __shared__ float4 acc_s[kMergeThreads / 32][32];
   // the next call's prep kernel may start (it writes the plan, and the
   // tickets only after waiting for this grid; nothing here reads either)
@@ -1225,70 +1237,39 @@ __global__ void __launch_bounds__(kMergeThreads) stream_merge_kernel(
   pair_ctas(pcs, np, nu, stream_cut(Wc, C), c0, n);
   if (n == 1) return;  // a pair held by one CTA: the decode kernel wrote it
   const long long P0 = (long long)pair + c0;
-  auto pidx = [&](int k) { return P0 + k; };
   // Everything above reads only the inputs; what follows reads what the decode
   // kernel wrote (launched as its programmatic dependent, this is where the
   // merge waits for it to complete; otherwise the wait returns at once).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // log-normaliser of the whole pair: M = max z_k, Z = sum 2^(z_k - M).  Each
-  // z_k is read once and its weight kept in shared memory, so that the
-  // partials' outputs are then all requested at once.
-  __shared__ float wsm[kMergeMaxParts];
-  float M = -INFINITY;
-  for (int k = threadIdx.x; k < n; k += kMergeThreads) {
-    const float z = __ldg(part_lse + pidx(k) * SG + j);
-    wsm[k] = z;
-    M = fmaxf(M, z);
-  }
-  M = warp_max(M);
-  if (lane == 0) redf[warp] = M;
-  __syncthreads();
-  M = -INFINITY;
-  for (int w = 0; w < kMergeThreads / 32; ++w) M = fmaxf(M, redf[w]);
-  __syncthreads();
-  float Zl = 0.f;
-  for (int k = threadIdx.x; k < n; k += kMergeThreads) {  // the thread's own entries
-    const float z = wsm[k];
-    const float wv = (M == -INFINITY || z == -INFINITY) ? 0.f : exp2f((z - M) * kLog2e);
-    wsm[k] = wv;
-    Zl += wv;
-  }
-  Zl = warp_sum(Zl);
-  if (lane == 0) redf[warp] = Zl;
-  __syncthreads();
-  float Z = 0.f;
-  for (int w = 0; w < kMergeThreads / 32; ++w) Z += redf[w];
-  // sum_k w_k o_k: warp w takes partials k = w, w + 8, ...; lane: channels 4 lane ..
+  // warp w folds partials k = w, w + 8, ... (ten at a time: one round of L2
+  // latency for up to 80 partials); warp 0 then folds the warps' states
+  constexpr int NW = kMergeThreads / 32;
+  float m = -INFINITY, l = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int k0 = warp; k0 < n; k0 += 8 * (kMergeThreads / 32)) {
-      float wv[8];
-      float4 o[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {  // eight partials' loads in flight
-        const int k = k0 + u * (kMergeThreads / 32);
-        wv[u] = k < n ? wsm[k] : 0.f;
-        o[u] = wv[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(part_o + (pidx(k) * SG + j) * SD) + lane)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a.x = fmaf(wv[u], o[u].x, a.x);
-        a.y = fmaf(wv[u], o[u].y, a.y);
-        a.z = fmaf(wv[u], o[u].z, a.z);
-        a.w = fmaf(wv[u], o[u].w, a.w);
-      }
-    }
+  fold_partials<10>(part_o, part_lse, P0, n, warp, NW, j, lane, m, l, a);
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
   }
   acc_s[warp][lane] = a;
   __syncthreads();
   if (warp == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w]);
+    float Z = 0.f;
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < kMergeThreads / 32; ++w) {
-      t.x += acc_s[w][lane].x;
-      t.y += acc_s[w][lane].y;
-      t.z += acc_s[w][lane].z;
-      t.w += acc_s[w][lane].w;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = red_m[w];
+      if (mw == -INFINITY) continue;
+      const float e = exp2f((mw - M) * kLog2e);
+      const float4 aw = acc_s[w][lane];
+      Z = fmaf(e, red_l[w], Z);
+      t.x = fmaf(e, aw.x, t.x);
+      t.y = fmaf(e, aw.y, t.y);
+      t.z = fmaf(e, aw.z, t.z);
+      t.w = fmaf(e, aw.w, t.w);
     }
     const bool empty = !(Z > 0.f);
     const float inv = empty ? 0.f : 1.f / Z;
