@@ -89,8 +89,8 @@ def test_back_to_back_calls_on_one_workspace(B):
     gcs = [c.gpu() for c in cases]
     alone = [c.gpu_decode(gc) for c, gc in zip(cases, gcs)]
     # one workspace, as large as the largest of the three calls needs
-    n = max(kv4.workspace_bytes(gc.layout, B, 0) for gc in gcs)
-    shared = torch.empty(n, dtype=torch.uint8, device=gcs[0].device)
+    nbytes = max(kv4.workspace_bytes(gc.layout, B, 0) for gc in gcs)
+    shared = torch.empty(nbytes, dtype=torch.uint8, device=gcs[0].device)
     for gc in gcs:
         gc._ws[(B, 0, False)] = shared
     dev = gcs[0].device
